@@ -1,0 +1,414 @@
+"""Benchmark of the GB300 MoE feed-forward layer.
+
+One step = one pass of the whole layer on one batch: router logits, routing,
+dispatch, grouped gate/up (SwiGLU) and down GEMMs, shared expert, combine,
+and the full backward (moe_backward).  Prints ONE JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 2] [--fwd-only]
+  python bench.py --impl reference ...   (the CPU oracle, timed on host cores)
+
+Timing: W untimed warm-up steps, then K steps between a barrier and a
+device synchronise; each step is bracketed by CUDA events on the launch
+stream, and a 256 MB buffer is written before each step (outside its events)
+to flush the 129 MB L2.  Multi-GPU (torchrun): independent replicas, no
+data-path collective; time = max over ranks; value = all ranks' tokens / time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s fwd & fwd+bwd; grouped-GEMM % of GB300 bf16 tensor peak"
+WORKLOAD_NAMES = {
+    1: "tiny MoE layer: T=256, d=64, 4 routed top-2 + 1 shared, SwiGLU 128",
+    2: "KochiLLM-shaped MoE layer: T=32768, d=1536, 4 routed top-2 + 1 shared, SwiGLU 3072",
+    3: "Qwen3-MoE-shaped packed layer: T=65536 (60293 real + PAD tail), d=512, 8 experts "
+       "top-2, hidden 768",
+    4: "DeepSeekMoE-style layer: T=16384, d=2048, 64 routed top-6 + 2 shared, hidden 1408, "
+       "Zipf(1.1) selection bias",
+    5: "training-step layer: T=32768, d=1024, 128 experts top-8, hidden 768",
+}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d["bf16_tflops"], d["hbm_gbs"], "measured"
+    return 1900.0, 6800.0, "fallback"
+
+
+def gemm_flops(s):
+    """Algorithmic FLOPs (2 per multiply-add) per step, real tokens only."""
+    Tr = s.T_real if s.T_real is not None else s.T
+    routed = 2 * Tr * s.k * s.d * s.H * 3     # gate, up, down
+    shared = 2 * Tr * s.d * s.Hs_total * 3
+    return routed, shared
+
+
+class Clocks:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu = gpu_index
+        self.path = None
+
+    def start(self):
+        try:
+            import tempfile
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def launches_per_step(s, fwd_only):
+    from mixture_experts_ffn_02_gb300 import binding  # noqa: F401
+    small = s.E in (4, 8, 16) and s.d * s.E * 4 + (s.d // 8) * 16 <= 96 * 1024
+    shared = s.Hs_total > 0
+    fwd = 1 + 1 + 3 + 1 + 1 + (2 if shared else 0) + 1
+    bwd = 1 + 1 + 1 + 2 + (4 if shared else 0) + (0 if small else 1) + 1 + 2
+    return fwd if fwd_only else fwd + bwd
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from mixture_experts_ffn_02_gb300 import binding, synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    s = synth.shape(args.config)
+    training = not args.fwd_only
+    inp = synth.make_inputs(s, seed=rank, with_grad=True)
+    lay = binding.Layer.create(s, training=training, device=f"cuda:{local}")
+    dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    lay.set_inputs(dev["x"], dev["Wr"], dev["W_gu"], dev["W_down"], dev["Ws_gu"],
+                   dev["Ws_down"], bias=dev["bias"], valid=dev["valid"])
+    dY = dev["dY"]
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=f"cuda:{local}")
+
+    gu_ev = []
+
+    def step(record_gu):
+        lay.router_logits()
+        lay.route()
+        lay.permute()
+        if record_gu:
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            lay.gate_up()
+            b.record(stream)
+            gu_ev.append((a, b))
+        else:
+            lay.gate_up()
+        lay.down()
+        lay.shared()
+        lay.combine()
+        if training:
+            lay.backward(dY)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step(False)
+    torch.cuda.synchronize()
+    if lay.status() != 0:
+        raise RuntimeError(f"device status {lay.status()} after warm-up")
+
+    clocks = Clocks(local)
+    ev = []
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    for _ in range(args.steps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step(True)
+        b.record(stream)
+        ev.append((a, b))
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    status = lay.status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} in the timed region")
+    ms = sum(a.elapsed_time(b) for a, b in ev)
+    gu_ms = sum(a.elapsed_time(b) for a, b in gu_ev) / len(gu_ev)
+    t = torch.tensor([ms], device=f"cuda:{local}")
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+    ms_per_step = ms_max / args.steps
+    tokens_all = s.T * args.steps * world
+    value = tokens_all / (ms_max / 1e3)
+
+    # fwd-only rate of the same layer (reported beside the fwd+bwd headline)
+    fwd_rate = None
+    if training:
+        fe = []
+        for _ in range(max(3, args.steps // 2)):
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            lay.forward()
+            b.record(stream)
+            fe.append((a, b))
+        torch.cuda.synchronize()
+        fms = statistics.median(a.elapsed_time(b) for a, b in fe)
+        fwd_rate = s.T / (fms / 1e3)
+
+    e2e = run_e2e(args, s, inp, lay, training, local)
+
+    bf16_peak, hbm_peak, peak_src = peaks()
+    routed, shared = gemm_flops(s)
+    gu_flops = routed * 2 / 3                                  # gate + up of the routed experts
+    gu_tflops = gu_flops / (gu_ms / 1e3) / 1e12
+    layer_flops = (routed + shared) * (3 if training else 1)
+    layer_tflops = layer_flops / (ms_per_step / 1e3) / 1e12
+    traffic = load_traffic(args.config)
+
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+    out = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights)",
+        "config": {"workload": WORKLOAD_NAMES[args.config] + (" fwd" if args.fwd_only
+                                                              else " fwd+bwd"),
+                   "config_id": args.config, "T": s.T, "d": s.d, "E": s.E, "k": s.k,
+                   "H": s.H, "n_shared": s.n_shared, "H_shared": s.H_shared,
+                   "parallelism": f"replicas x{world}",
+                   "l2": "256 MB buffer written before each step, outside its events"},
+        "fwd_tokens_per_s": None if fwd_rate is None else round(fwd_rate, 1),
+        "layer_tflops": round(layer_tflops, 1),
+        "layer_frac_of_bf16_peak": round(layer_tflops / bf16_peak, 4),
+        "roofline": {"kernel": "grouped gate/up GEMM + SwiGLU (tcgen05)", "bound": "tensor",
+                     "achieved": round(gu_tflops, 1), "peak": bf16_peak, "unit": "TFLOP/s",
+                     "frac": round(gu_tflops / bf16_peak, 4), "peak_source": peak_src,
+                     "algorithmic_flops_per_launch": gu_flops,
+                     "avg_launch_ms": round(gu_ms, 4), "traffic": traffic},
+        "gpu_launches": launches_per_step(s, args.fwd_only) * args.steps,
+        "e2e": e2e,
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        out["cpu_baseline"] = cpu_baseline(args, s)
+    print(json.dumps(out), flush=True)
+
+
+def load_traffic(cfg):
+    """dram bytes per launch of the gate/up kernel from the committed ncu
+    summary, if one matches this workload (else null)."""
+    p = os.path.join(ROOT, "profiles", f"gate_up_traffic_cfg{cfg}.json")
+    if os.path.exists(p):
+        try:
+            return json.load(open(p)).get("dram_bytes_per_launch")
+        except Exception:
+            return None
+    return None
+
+
+def run_e2e(args, s, inp, lay, training, local):
+    """The same layer step through moe_forward/moe_backward with host
+    buffers: x (and dY) copied in from pinned memory, y and dx (and aux)
+    copied back, all inside the timed region."""
+    import torch
+    hx = inp["x"].pin_memory()
+    hdy = inp["dY"].pin_memory()
+    hy = torch.empty_like(inp["x"]).pin_memory()
+    hdx = torch.empty_like(inp["x"]).pin_memory()
+    haux = torch.empty(4, dtype=torch.float32).pin_memory()
+    x_dev = lay.bufs["x"]
+    dy_dev = torch.empty_like(lay.bufs["x"])
+    stream = torch.cuda.current_stream()
+    n = max(3, args.steps // 2)
+    times = []
+    for i in range(n + 2):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        x_dev.copy_(hx, non_blocking=True)
+        if training:
+            dy_dev.copy_(hdy, non_blocking=True)
+        lay.forward()
+        if training:
+            lay.backward(dy_dev)
+        hy.copy_(lay.bufs["y"], non_blocking=True)
+        haux.copy_(lay.bufs["aux"], non_blocking=True)
+        if training:
+            hdx.copy_(lay.grads["dx"], non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        if i >= 2:
+            times.append(a.elapsed_time(b))
+    ms = statistics.median(times)
+    nb = s.T * s.d * 2
+    return {"value": round(s.T / (ms / 1e3), 1), "unit": "tokens/s",
+            "h2d_bytes_per_step": nb * (2 if training else 1),
+            "d2h_bytes_per_step": nb * (2 if training else 1) + 16,
+            "ms_per_step": round(ms, 4)}
+
+
+def oracle_sample(s, n_tok, training):
+    """Time the CPU oracle on the first n_tok tokens of the workload."""
+    from mixture_experts_ffn_02_gb300 import synth
+    from oracle import moe_oracle as O
+    sub = synth.scaled(s, T=n_tok, T_real=None if s.T_real is None else min(n_tok, s.T_real))
+    inp = synth.make_inputs(sub, seed=0, with_grad=True)
+    t0 = time.perf_counter()
+    fwd = O.forward(inp["x"], inp["Wr"], inp["W_gu"], inp["W_down"], inp["Ws_gu"],
+                    inp["Ws_down"], k=s.k, bias=inp["bias"], valid=inp["valid"],
+                    norm_topk=bool(s.norm_topk))
+    if training:
+        O.backward(inp["x"], inp["Wr"], inp["W_gu"], inp["W_down"], inp["Ws_gu"],
+                   inp["Ws_down"], fwd, inp["dY"], norm_topk=bool(s.norm_topk),
+                   aux_coef=s.aux_coef)
+    return time.perf_counter() - t0
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def cpu_baseline(args, s, budget_s=12.0):
+    training = not args.fwd_only
+    n = 64
+    dt = oracle_sample(s, n, training)
+    # grow the sample towards the time budget
+    while dt < budget_s / 4 and n < s.T:
+        n = min(s.T, n * 4)
+        dt = oracle_sample(s, n, training)
+    return {"value": round(n / dt, 2), "unit": "tokens/s", "cores": blas_threads(),
+            "kind": "oracle",
+            "sample": f"first {n} of {s.T} tokens, same shapes, numpy fp64 "
+                      f"{'fwd+bwd' if training else 'fwd'}; {dt:.1f} s"}
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from mixture_experts_ffn_02_gb300 import synth
+    s = synth.shape(args.config)
+    training = not args.fwd_only
+    n = 256 if s.d * s.H <= 4e6 else 64
+    for _ in range(args.warmup):
+        oracle_sample(s, n, training)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_sample(s, n, training)
+    dt = time.perf_counter() - t0
+    v = n * args.steps / dt
+    out = {"impl": "reference", "metric": METRIC, "value": round(v, 2), "unit": "tokens/s",
+           "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(dt / args.steps * 1e3, 2), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": WORKLOAD_NAMES[args.config] + (" fwd" if args.fwd_only
+                                                                  else " fwd+bwd"),
+                      "config_id": args.config,
+                      "sample": f"{n} tokens of the workload per step"},
+           "cpu_baseline": {"value": round(v, 2), "unit": "tokens/s", "cores": blas_threads(),
+                            "kind": "oracle",
+                            "sample": f"{n} tokens per step, numpy fp64"},
+           "e2e": {"value": round(v, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--fwd-only", action="store_true")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

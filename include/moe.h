@@ -1,0 +1,241 @@
+/*
+ * moe.h -- C ABI of the GB300-native sparse Mixture-of-Experts feed-forward
+ * layer (sm_103a).
+ *
+ * What the layer computes (the pages that define it):
+ *   - "KochiLLM v1.0" model card, Architecture: the MoE FFN applies a shared
+ *     expert to every token plus the top-2 of 4 routed experts; the gate
+ *     weights are renormalised over the selected experts; the loss adds
+ *     0.01 x (E x sum_i f_i p_i) for load balancing.  Configuration: SwiGLU
+ *     experts with hidden 2 x dim.
+ *   - "spark-gpt" README, feature list: bias-free fp32-softmax top-k routing,
+ *     packed SwiGLU experts, BF16 grouped GEMM, selected-probability
+ *     renormalisation (optional), and a load-balancing statistic over real
+ *     (non-PAD) tokens only.
+ *   - "KohakUwULLM" README, Key features: DeepSeekMoE with aux-loss-free load
+ *     balancing (a per-expert bias that enters the selection only).
+ *
+ * Conventions (every entry point):
+ *   - Returns MOE_OK (0) or a positive MOE_ERR_* code; nothing is thrown.
+ *     moe_strerror() names a code.
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller, row-major,
+ *     16-byte aligned (MOE_ERR_ALIGN otherwise).  The library allocates no
+ *     device or host memory; scratch lives in a caller-owned workspace of
+ *     moe_workspace_bytes() bytes (MOE_ERR_WORKSPACE if smaller).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls are asynchronous; none synchronises the host.
+ *   - Errors found on the device (expert index out of range, non-finite
+ *     logits, a bounded wait that expired) are latched in a status word in
+ *     the workspace; moe_get_status() synchronises the stream and reads it.
+ *   - bf16 tensors are IEEE bfloat16 stored as uint16; fp32 is IEEE float.
+ *   - Shape rules (MOE_ERR_SHAPE otherwise): T >= 1, d % 64 == 0,
+ *     H % 64 == 0, 1 <= k <= min(E, 32), E <= 256, n_shared >= 0,
+ *     H_shared % 64 == 0
+ *     when n_shared > 0, T*k < 2^31, and every row count below < 2^31.
+ *
+ * Symbols: T positions (real + PAD), d model dim, E routed experts, k experts
+ * per token, H routed expert hidden, Hs = n_shared * H_shared shared hidden,
+ * M = T_real * k routed (token, slot) pairs, R_cap = moe_row_capacity().
+ *
+ * Routed rows ("permuted order").  Row r of x_perm/ab/h/out_perm holds one
+ * (token, slot) pair; pairs are grouped by expert by a stable counting sort
+ * (within an expert, ascending token).  Each expert's segment starts at a
+ * multiple of MOE_ROW_ALIGN rows: expert e owns rows
+ * [row_offsets[e], row_offsets[e+1]), of which the first counts[e] hold
+ * pairs and the rest are zero pad rows (perm = -1).  offsets[] is the exact
+ * exclusive scan of counts[] (the unpadded positions).
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_ABI_VERSION 1
+#define MOE_ROW_ALIGN 128
+
+enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_NULL = 1,        /* a required pointer is NULL                  */
+  MOE_ERR_SHAPE = 2,       /* configuration violates the shape rules      */
+  MOE_ERR_ALIGN = 3,       /* a tensor pointer is not 16-byte aligned     */
+  MOE_ERR_WORKSPACE = 4,   /* workspace NULL or smaller than required     */
+  MOE_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed        */
+  MOE_ERR_DEVICE = 6,      /* current device is not sm_100-family (sm_103a build) */
+  MOE_ERR_TIMEOUT = 7,     /* device: a bounded wait inside a kernel expired */
+  MOE_ERR_INDEX = 8,       /* device: an expert index outside [0, E)      */
+  MOE_ERR_NONFINITE = 9    /* device: a router logit is NaN or infinite   */
+};
+
+/* Layer configuration (plain data, passed by pointer, read during the call). */
+typedef struct moe_config {
+  int32_t T;          /* positions per call (real tokens + PAD filler)         */
+  int32_t d;          /* model dim                                              */
+  int32_t E;          /* routed experts                                         */
+  int32_t k;          /* experts selected per token                             */
+  int32_t H;          /* hidden size of one routed expert                       */
+  int32_t n_shared;   /* shared (always-on, ungated) experts; 0 = none          */
+  int32_t H_shared;   /* hidden size of one shared expert                       */
+  int32_t norm_topk;  /* 1: gates renormalised over the selected k; 0: raw p    */
+  float aux_coef;     /* weight of aux in the objective differentiated by
+                         moe_backward (KochiLLM card, Architecture: 0.01)       */
+} moe_config;
+
+/*
+ * Forward tensors.  Which fields a call reads (in) or writes (out) is listed
+ * with each entry point; unused fields may be NULL.
+ */
+typedef struct moe_tensors {
+  /* inputs */
+  const void* x;        /* [T][d] bf16 token activations                          */
+  const float* Wr;      /* [d][E] fp32 router weight (logits = x . Wr)           */
+  const float* bias;    /* [E] fp32 selection-only bias, or NULL                 */
+  const uint8_t* valid; /* [T] 1 = real token, 0 = PAD; NULL = all real          */
+  const void* W_gu;     /* [E][2H][d] bf16: rows [0,H) gate, [H,2H) up           */
+  const void* W_down;   /* [E][d][H] bf16                                        */
+  const void* Ws_gu;    /* [2Hs][d] bf16 shared gate rows then up rows (n_shared
+                           experts concatenated: expert s owns gate rows
+                           [s*H_shared, (s+1)*H_shared) and the same up rows)    */
+  const void* Ws_down;  /* [d][Hs] bf16 shared down (columns concatenated)        */
+  /* routing */
+  float* logits;        /* [T][E] fp32                                            */
+  int32_t* topk_idx;    /* [T][k] selected experts, slot 0 = largest key; -1 PAD  */
+  float* gates;         /* [T][k] fp32 gate weights; 0 on PAD                     */
+  int32_t* counts;      /* [E] pairs routed to each expert (real tokens only)     */
+  float* f;             /* [E] f_e = counts_e / (k T_real)                        */
+  float* p;             /* [E] p_e = mean over real tokens of softmax_e           */
+  float* aux;           /* [1] aux = E * sum_e f_e p_e                            */
+  /* dispatch */
+  int32_t* offsets;     /* [E+1] exclusive scan of counts (unpadded)              */
+  int32_t* row_offsets; /* [E+1] padded segment starts (multiples of 128)        */
+  int32_t* perm;        /* [R_cap] pair index t*k+j of each row; -1 = pad row    */
+  int32_t* inv;         /* [T*k] row of pair (t,j); -1 for PAD tokens             */
+  void* x_perm;         /* [R_cap][d] bf16 x rows in permuted order (pad rows 0) */
+  /* experts */
+  void* ab;             /* [R_cap][2H] bf16 pre-activations a|b (saved for
+                           backward; NULL skips the save)                         */
+  void* h;              /* [R_cap][H] bf16 silu(a) * b                            */
+  void* out_perm;       /* [R_cap][d] bf16 expert outputs per row                 */
+  void* s_ab;           /* [T][2Hs] bf16 shared pre-activations (or NULL)         */
+  void* s_h;            /* [T][Hs] bf16 shared hidden (0 on PAD rows)             */
+  void* s_out;          /* [T][d] bf16 shared expert output (0 on PAD rows)       */
+  /* output */
+  void* y;              /* [T][d] bf16 layer output                               */
+} moe_tensors;
+
+/* Backward tensors (gradients of J = <dY, y> + aux_coef * aux). */
+typedef struct moe_grads {
+  const void* dY;       /* [T][d] bf16 upstream gradient of y                     */
+  void* dx;             /* [T][d] bf16 gradient of x (expert, shared and router
+                           paths)                                                 */
+  float* dWr;           /* [d][E] fp32                                            */
+  void* dW_gu;          /* [E][2H][d] bf16                                        */
+  void* dW_down;        /* [E][d][H] bf16                                         */
+  void* dWs_gu;         /* [2Hs][d] bf16 (NULL when n_shared == 0)                */
+  void* dWs_down;       /* [d][Hs] bf16                                           */
+  float* d_logits;      /* [T][E] fp32 gradient of the router logits, including
+                           the aux term (f held constant)                        */
+} moe_grads;
+
+/* ---------------------------------------------------------------- queries */
+
+/* ABI version (MOE_ABI_VERSION). */
+int moe_abi_version(void);
+
+/* Static message for a status code (never NULL). */
+const char* moe_strerror(int code);
+
+/* MOE_OK if *cfg satisfies the shape rules above, else MOE_ERR_SHAPE/NULL. */
+int moe_check_config(const moe_config* cfg);
+
+/* Rows a permuted buffer must hold: the largest padded row total,
+ * floor((T*k + (MOE_ROW_ALIGN-1)*E) / MOE_ROW_ALIGN) * MOE_ROW_ALIGN.        */
+int moe_row_capacity(const moe_config* cfg, int64_t* rows);
+
+/* Workspace bytes for forward (training = 0) or forward + backward
+ * (training = 1).  The same workspace must be passed to every call of one
+ * layer step; its contents between calls are private to the library. */
+int moe_workspace_bytes(const moe_config* cfg, int training, size_t* bytes);
+
+/* Synchronise `stream`, copy the device status word to *status and reset it
+ * to MOE_OK.  The only entry point that blocks the host. */
+int moe_get_status(void* workspace, void* stream, int* status);
+
+/* ---------------------------------------------------------------- forward */
+
+/* a0. logits = x . Wr in fp32 (x widened exactly from bf16).
+ * "spark-gpt" README, feature list: bias-free router, fp32 routing.
+ * in: x, Wr.  out: logits. */
+int moe_router_logits(const moe_config* cfg, const moe_tensors* t,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* a1. Top-k routing and the load-balancing statistic.
+ * "KochiLLM v1.0" card, Architecture; "spark-gpt" README, feature list.
+ * key = logits (+ bias, one fp32 add); the k largest keys are selected, equal
+ * keys lower index first; s = fp32 softmax(logits) over all E (unbiased);
+ * gates = s_sel / sum s_sel if norm_topk else s_sel; counts, f, p, aux over
+ * real tokens.  in: logits, bias, valid.
+ * out: topk_idx, gates, counts, f, p, aux.  Device errors: NONFINITE. */
+int moe_route(const moe_config* cfg, const moe_tensors* t,
+              void* workspace, size_t workspace_bytes, void* stream);
+
+/* a2. Stable counting-sort dispatch into expert-contiguous padded rows.
+ * in: x, topk_idx.  out: counts, offsets, row_offsets, perm, inv, x_perm.
+ * Device errors: INDEX (the pair is then dropped). */
+int moe_permute(const moe_config* cfg, const moe_tensors* t,
+                void* workspace, size_t workspace_bytes, void* stream);
+
+/* a3. Grouped gate/up GEMM with SwiGLU in the epilogue (tcgen05, bf16 in,
+ * fp32 accumulate): per expert e and row r of its segment,
+ * a = x_perm[r] W_gate[e]^T, b = x_perm[r] W_up[e]^T, h[r] = silu(a) * b.
+ * "KochiLLM v1.0" card (SwiGLU experts); "spark-gpt" README, Hard-won facts
+ * (grouped GEMM with the SwiGLU fused into the epilogue).
+ * in: x_perm, row_offsets, W_gu.  out: h, ab (if non-NULL). */
+int moe_expert_gate_up(const moe_config* cfg, const moe_tensors* t,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/* a4. Grouped down GEMM: out_perm[r] = h[r] W_down[e]^T.
+ * in: h, row_offsets, W_down.  out: out_perm. */
+int moe_expert_down(const moe_config* cfg, const moe_tensors* t,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
+/* a5. Shared expert on every real token ("KochiLLM v1.0" card, Architecture):
+ * s_out[t] = SwiGLU_shared(x[t]) for real t, 0 on PAD.  No-op if n_shared=0.
+ * in: x, valid, Ws_gu, Ws_down.  out: s_h, s_out, s_ab (if non-NULL). */
+int moe_shared_ffn(const moe_config* cfg, const moe_tensors* t,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/* a6. Weighted un-permute: y[t] = sum_j gates[t][j] out_perm[inv[t,j]]
+ * (+ s_out[t]), fp32 sum in slot order, one rounding to bf16; PAD rows 0.
+ * in: out_perm, inv, gates, valid, s_out (if n_shared > 0).  out: y. */
+int moe_combine(const moe_config* cfg, const moe_tensors* t,
+                void* workspace, size_t workspace_bytes, void* stream);
+
+/* a0..a6 in order on one stream. */
+int moe_forward(const moe_config* cfg, const moe_tensors* t,
+                void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------- backward */
+
+/* a7. Gradients of J = <dY, y> + aux_coef * aux with the hard counts (f)
+ * held constant; the selection bias receives no gradient.
+ * Reads every forward tensor of `t` written by moe_forward (x, Wr, valid,
+ * weights, logits, topk_idx, gates, counts, f, row_offsets, inv, x_perm, ab,
+ * h, out_perm, s_ab, s_h); ab and (if n_shared > 0) s_ab must have been saved.
+ * Writes every field of `g` (dWs_* only when n_shared > 0).
+ * Steps: combine backward (d_out = g dY, dg = <dY, out_perm>), router-logit
+ * gradient with the aux term, grouped dH GEMM with the SwiGLU backward in its
+ * epilogue, grouped dX GEMM, ragged-K grouped dW GEMMs, the shared expert's
+ * backward, the router's input gradients, and the un-permute sum of dx. */
+int moe_backward(const moe_config* cfg, const moe_tensors* t, const moe_grads* g,
+                 void* workspace, size_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -1,0 +1,226 @@
+"""Thin Python binding of the C ABI in ``include/moe.h``.
+
+Argument marshalling only: torch allocates device memory and supplies the
+stream; every step of the layer runs in the CUDA kernels of
+``_build/libmoe_gb300.so``.  There is no fallback: if the library is missing
+or fails to load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+from . import build as _build
+
+c_int32 = ctypes.c_int32
+c_float = ctypes.c_float
+c_void_p = ctypes.c_void_p
+
+MOE_ROW_ALIGN = 128
+
+STATUS = {
+    0: "MOE_OK", 1: "MOE_ERR_NULL", 2: "MOE_ERR_SHAPE", 3: "MOE_ERR_ALIGN",
+    4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_CUDA", 6: "MOE_ERR_DEVICE", 7: "MOE_ERR_TIMEOUT",
+    8: "MOE_ERR_INDEX", 9: "MOE_ERR_NONFINITE",
+}
+
+
+class MoEConfig(ctypes.Structure):
+    _fields_ = [("T", c_int32), ("d", c_int32), ("E", c_int32), ("k", c_int32),
+                ("H", c_int32), ("n_shared", c_int32), ("H_shared", c_int32),
+                ("norm_topk", c_int32), ("aux_coef", c_float)]
+
+
+TENSOR_FIELDS = ["x", "Wr", "bias", "valid", "W_gu", "W_down", "Ws_gu", "Ws_down",
+                 "logits", "topk_idx", "gates", "counts", "f", "p", "aux",
+                 "offsets", "row_offsets", "perm", "inv", "x_perm",
+                 "ab", "h", "out_perm", "s_ab", "s_h", "s_out", "y"]
+GRAD_FIELDS = ["dY", "dx", "dWr", "dW_gu", "dW_down", "dWs_gu", "dWs_down", "d_logits"]
+
+
+class MoETensors(ctypes.Structure):
+    _fields_ = [(n, c_void_p) for n in TENSOR_FIELDS]
+
+
+class MoEGrads(ctypes.Structure):
+    _fields_ = [(n, c_void_p) for n in GRAD_FIELDS]
+
+
+_STEP = [ctypes.POINTER(MoEConfig), ctypes.POINTER(MoETensors), c_void_p, ctypes.c_size_t,
+         c_void_p]
+SIGNATURES = {
+    "moe_abi_version": (ctypes.c_int, []),
+    "moe_strerror": (ctypes.c_char_p, [ctypes.c_int]),
+    "moe_check_config": (ctypes.c_int, [ctypes.POINTER(MoEConfig)]),
+    "moe_row_capacity": (ctypes.c_int, [ctypes.POINTER(MoEConfig),
+                                        ctypes.POINTER(ctypes.c_int64)]),
+    "moe_workspace_bytes": (ctypes.c_int, [ctypes.POINTER(MoEConfig), ctypes.c_int,
+                                           ctypes.POINTER(ctypes.c_size_t)]),
+    "moe_get_status": (ctypes.c_int, [c_void_p, c_void_p, ctypes.POINTER(ctypes.c_int)]),
+    "moe_router_logits": (ctypes.c_int, _STEP),
+    "moe_route": (ctypes.c_int, _STEP),
+    "moe_permute": (ctypes.c_int, _STEP),
+    "moe_expert_gate_up": (ctypes.c_int, _STEP),
+    "moe_expert_down": (ctypes.c_int, _STEP),
+    "moe_shared_ffn": (ctypes.c_int, _STEP),
+    "moe_combine": (ctypes.c_int, _STEP),
+    "moe_forward": (ctypes.c_int, _STEP),
+    "moe_backward": (ctypes.c_int, [ctypes.POINTER(MoEConfig), ctypes.POINTER(MoETensors),
+                                    ctypes.POINTER(MoEGrads), c_void_p, ctypes.c_size_t,
+                                    c_void_p]),
+}
+
+_LIB = None
+
+
+class MoEError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {STATUS.get(code, code)}")
+
+
+def load(path: str | None = None, build_if_missing: bool = False) -> ctypes.CDLL:
+    """Load the shared library (no fallback: raises if it is absent)."""
+    global _LIB
+    if _LIB is not None and path is None:
+        return _LIB
+    p = path or _build.LIB
+    if not os.path.exists(p):
+        if build_if_missing:
+            _build.build()
+        else:
+            raise RuntimeError(f"MoE CUDA library not built: {p} (run build())")
+    lib = ctypes.CDLL(p)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path is None:
+        _LIB = lib
+    return lib
+
+
+def check(code: int, where: str):
+    if code != 0:
+        raise MoEError(code, where)
+
+
+def config(shape, **over) -> MoEConfig:
+    """MoEConfig from a synth.MoEShape (or anything with the same fields)."""
+    c = MoEConfig(T=shape.T, d=shape.d, E=shape.E, k=shape.k, H=shape.H,
+                  n_shared=shape.n_shared, H_shared=shape.H_shared,
+                  norm_topk=shape.norm_topk, aux_coef=shape.aux_coef)
+    for k_, v in over.items():
+        setattr(c, k_, v)
+    return c
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream():
+    import torch
+    return c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+@dataclass
+class Layer:
+    """One MoE layer call's device buffers (torch) and the library handle."""
+    cfg: MoEConfig
+    training: bool
+    bufs: dict
+    grads: dict
+    ws: object
+    lib: ctypes.CDLL
+
+    @classmethod
+    def create(cls, shape, training: bool = False, device: str = "cuda", lib=None, **over):
+        import torch
+        lib = lib or load()
+        cfg = config(shape, **over)
+        check(lib.moe_check_config(ctypes.byref(cfg)), "moe_check_config")
+        rows = ctypes.c_int64()
+        check(lib.moe_row_capacity(ctypes.byref(cfg), ctypes.byref(rows)), "moe_row_capacity")
+        R = rows.value
+        wsb = ctypes.c_size_t()
+        check(lib.moe_workspace_bytes(ctypes.byref(cfg), int(training), ctypes.byref(wsb)),
+              "moe_workspace_bytes")
+        T, d, E, k, H = cfg.T, cfg.d, cfg.E, cfg.k, cfg.H
+        Hs = cfg.n_shared * cfg.H_shared
+        bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
+        dev = torch.device(device)
+
+        def z(*s, dt):
+            return torch.empty(*s, dtype=dt, device=dev)
+
+        b = dict(logits=z(T, E, dt=f32), topk_idx=z(T, k, dt=i32), gates=z(T, k, dt=f32),
+                 counts=z(E, dt=i32), f=z(E, dt=f32), p=z(E, dt=f32), aux=z(4, dt=f32),
+                 offsets=z(E + 1, dt=i32), row_offsets=z(E + 1, dt=i32), perm=z(R, dt=i32),
+                 inv=z(T * k, dt=i32), x_perm=z(R, d, dt=bf), h=z(R, H, dt=bf),
+                 out_perm=z(R, d, dt=bf), y=z(T, d, dt=bf),
+                 ab=z(R, 2 * H, dt=bf) if training else None,
+                 s_h=z(T, Hs, dt=bf) if Hs else None,
+                 s_out=z(T, d, dt=bf) if Hs else None,
+                 s_ab=z(T, 2 * Hs, dt=bf) if (Hs and training) else None)
+        g = {}
+        if training:
+            g = dict(dx=z(T, d, dt=bf), dWr=z(d, E, dt=f32), dW_gu=z(E, 2 * H, d, dt=bf),
+                     dW_down=z(E, d, H, dt=bf), d_logits=z(T, E, dt=f32),
+                     dWs_gu=z(2 * Hs, d, dt=bf) if Hs else None,
+                     dWs_down=z(d, Hs, dt=bf) if Hs else None)
+        ws = torch.zeros(max(wsb.value, 16), dtype=torch.uint8, device=dev)
+        return cls(cfg=cfg, training=training, bufs=b, grads=g, ws=ws, lib=lib)
+
+    @property
+    def R_cap(self) -> int:
+        return self.bufs["perm"].shape[0]
+
+    def set_inputs(self, x, Wr, W_gu, W_down, Ws_gu=None, Ws_down=None, bias=None,
+                   valid=None):
+        self.bufs.update(x=x, Wr=Wr, W_gu=W_gu, W_down=W_down, Ws_gu=Ws_gu, Ws_down=Ws_down,
+                         bias=bias, valid=valid)
+
+    def tensors(self) -> MoETensors:
+        return MoETensors(**{n: _ptr(self.bufs.get(n)) for n in TENSOR_FIELDS})
+
+    def grad_struct(self, dY) -> MoEGrads:
+        d = {n: _ptr(self.grads.get(n)) for n in GRAD_FIELDS if n != "dY"}
+        return MoEGrads(dY=_ptr(dY), **d)
+
+    def _step(self, name):
+        t = self.tensors()
+        fn = getattr(self.lib, name)
+        check(fn(ctypes.byref(self.cfg), ctypes.byref(t), c_void_p(self.ws.data_ptr()),
+                 self.ws.numel(), _stream()), name)
+
+    def router_logits(self): self._step("moe_router_logits")
+    def route(self): self._step("moe_route")
+    def permute(self): self._step("moe_permute")
+    def gate_up(self): self._step("moe_expert_gate_up")
+    def down(self): self._step("moe_expert_down")
+    def shared(self): self._step("moe_shared_ffn")
+    def combine(self): self._step("moe_combine")
+    def forward(self): self._step("moe_forward")
+
+    def backward(self, dY):
+        t = self.tensors()
+        g = self.grad_struct(dY)
+        check(self.lib.moe_backward(ctypes.byref(self.cfg), ctypes.byref(t), ctypes.byref(g),
+                                    c_void_p(self.ws.data_ptr()), self.ws.numel(), _stream()),
+              "moe_backward")
+
+    def status(self) -> int:
+        out = ctypes.c_int()
+        check(self.lib.moe_get_status(c_void_p(self.ws.data_ptr()), _stream(),
+                                      ctypes.byref(out)), "moe_get_status")
+        return out.value
+
+
+def to_device(inputs: dict, device="cuda") -> dict:
+    """Copy the synth.make_inputs() CPU tensors to the device."""
+    out = {}
+    for k_, v in inputs.items():
+        out[k_] = v.to(device) if hasattr(v, "to") and v is not None and k_ != "shape" else v
+    return out

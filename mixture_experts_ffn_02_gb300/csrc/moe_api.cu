@@ -1,0 +1,458 @@
+// C-ABI entry points of the MoE layer: argument checks, the workspace
+// layout, and the launch order of the kernels on the caller's stream.
+#include <cstring>
+#include <mutex>
+
+#include "moe_common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr int kRouteBlocksCap = 304;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t row_capacity(const moe_config& c) {
+  const int64_t a = (int64_t)c.T * c.k + (int64_t)(kRowAlign - 1) * c.E;
+  return a / kRowAlign * kRowAlign;
+}
+
+int hs_total(const moe_config& c) { return c.n_shared > 0 ? c.n_shared * c.H_shared : 0; }
+
+int route_group_lanes(int E) {
+  int G = 1;
+  while (G < E && G < 32) G <<= 1;
+  return G;
+}
+
+}  // namespace
+
+int device_info(DeviceInfo* out) {
+  static DeviceInfo cache[64];
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  DeviceInfo& di = cache[dev];
+  if (di.device != dev) {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return MOE_ERR_CUDA;
+    di.num_sms = prop.multiProcessorCount;
+    di.cc_major = prop.major;
+    di.cc_minor = prop.minor;
+    di.max_smem_optin = prop.sharedMemPerBlockOptin;
+    di.device = dev;
+  }
+  *out = di;
+  return MOE_OK;
+}
+
+int ws_layout(const moe_config* c, int training, WsLayout* w) {
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align_up(off + bytes);
+    return o;
+  };
+  const int G = route_group_lanes(c->E);
+  const int groups = 256 / G;
+  long long rb = ((long long)c->T + groups - 1) / groups;
+  if (rb > kRouteBlocksCap) rb = kRouteBlocksCap;
+  if (rb < 1) rb = 1;
+  w->route_blocks = (int)rb;
+  w->perm_blocks = (c->T + kPermChunk - 1) / kPermChunk;
+  w->R_cap = row_capacity(*c);
+  const int Hs = hs_total(*c);
+  w->status = take(sizeof(int));
+  w->route_done = take(sizeof(int));
+  w->route_cnt = take((size_t)w->route_blocks * c->E * sizeof(int));
+  w->route_psum = take((size_t)w->route_blocks * c->E * sizeof(float));
+  w->route_treal = take((size_t)w->route_blocks * sizeof(int));
+  w->perm_hist = take((size_t)w->perm_blocks * c->E * sizeof(int));
+  w->perm_base = take((size_t)w->perm_blocks * c->E * sizeof(int));
+  w->d_out = w->d_gu = w->dx_perm = w->ds_gu = w->dxs = w->dxr = w->dwr_part = 0;
+  w->dwr_splits = 1;
+  if (training) {
+    const size_t R = (size_t)w->R_cap;
+    w->d_out = take(R * c->d * 2);
+    w->d_gu = take(R * 2 * (size_t)c->H * 2);
+    w->dx_perm = take(R * c->d * 2);
+    if (Hs > 0) {
+      w->ds_gu = take((size_t)c->T * 2 * Hs * 2);
+      w->dxs = take((size_t)c->T * c->d * 2);
+    }
+    if (!router_small_path(*c)) w->dxr = take((size_t)c->T * c->d * 4);
+    int splits = c->T / 1024;
+    if (splits < 1) splits = 1;
+    if (splits > 64) splits = 64;
+    w->dwr_splits = splits;
+    w->dwr_part = take((size_t)splits * c->d * c->E * 4);
+  }
+  w->total = off;
+  return MOE_OK;
+}
+
+namespace {
+
+int check_cfg(const moe_config* c) {
+  if (!c) return MOE_ERR_NULL;
+  if (c->T < 1 || c->d < 64 || c->d % 64 || c->H < 64 || c->H % 64) return MOE_ERR_SHAPE;
+  if (c->E < 1 || c->E > 256 || c->k < 1 || c->k > c->E || c->k > kMaxK) return MOE_ERR_SHAPE;
+  if (c->n_shared < 0) return MOE_ERR_SHAPE;
+  if (c->n_shared > 0 && (c->H_shared < 64 || c->H_shared % 64)) return MOE_ERR_SHAPE;
+  if ((int64_t)c->T * c->k >= (1ll << 31)) return MOE_ERR_SHAPE;
+  if (row_capacity(*c) >= (1ll << 31)) return MOE_ERR_SHAPE;
+  if ((int64_t)c->n_shared * c->H_shared >= (1ll << 30)) return MOE_ERR_SHAPE;
+  if ((int64_t)c->E * 2 * c->H * c->d >= (1ll << 40)) return MOE_ERR_SHAPE;
+  return MOE_OK;
+}
+
+int check_device() {
+  DeviceInfo di;
+  if (device_info(&di) != MOE_OK) return MOE_ERR_CUDA;
+  if (di.cc_major != 10) return MOE_ERR_DEVICE;
+  return MOE_OK;
+}
+
+struct Call {
+  WsLayout w;
+  char* ws;
+  int* status;
+  cudaStream_t s;
+};
+
+// Common prologue: config, device and workspace checks.
+int begin(const moe_config* c, int training, void* ws, size_t ws_bytes, void* stream,
+          Call* call) {
+  int rc = check_cfg(c);
+  if (rc) return rc;
+  rc = check_device();
+  if (rc) return rc;
+  ws_layout(c, training, &call->w);
+  if (!ws || ws_bytes < call->w.total) return MOE_ERR_WORKSPACE;
+  if (!aligned16(ws)) return MOE_ERR_ALIGN;
+  call->ws = static_cast<char*>(ws);
+  call->status = reinterpret_cast<int*>(call->ws + call->w.status);
+  call->s = static_cast<cudaStream_t>(stream);
+  return MOE_OK;
+}
+
+#define MOE_NEED(p)                    \
+  do {                                 \
+    if (!(p)) return MOE_ERR_NULL;     \
+    if (!aligned16(p)) return MOE_ERR_ALIGN; \
+  } while (0)
+#define MOE_OPT(p)                     \
+  do {                                 \
+    if ((p) && !aligned16(p)) return MOE_ERR_ALIGN; \
+  } while (0)
+#define MOE_CUDA(expr)                 \
+  do {                                 \
+    if ((expr) != cudaSuccess) return MOE_ERR_CUDA; \
+  } while (0)
+
+int do_router_logits(const moe_config* c, const moe_tensors* t, Call& k) {
+  MOE_NEED(t->x); MOE_NEED(t->Wr); MOE_NEED(t->logits);
+  MOE_CUDA(launch_router_logits(*c, t->x, t->Wr, t->logits, k.s));
+  return MOE_OK;
+}
+
+int do_route(const moe_config* c, const moe_tensors* t, Call& k) {
+  MOE_NEED(t->logits); MOE_OPT(t->bias); MOE_OPT(t->valid);
+  MOE_NEED(t->topk_idx); MOE_NEED(t->gates); MOE_NEED(t->counts);
+  MOE_NEED(t->f); MOE_NEED(t->p); MOE_NEED(t->aux);
+  MOE_CUDA(launch_route(*c, t->logits, t->bias, t->valid, t->topk_idx, t->gates, t->counts,
+                        t->f, t->p, t->aux, k.ws, k.w, k.s));
+  return MOE_OK;
+}
+
+int do_permute(const moe_config* c, const moe_tensors* t, Call& k) {
+  MOE_NEED(t->x); MOE_NEED(t->topk_idx); MOE_NEED(t->counts); MOE_NEED(t->offsets);
+  MOE_NEED(t->row_offsets); MOE_NEED(t->perm); MOE_NEED(t->inv); MOE_NEED(t->x_perm);
+  MOE_CUDA(launch_permute(*c, t->x, t->topk_idx, t->counts, t->offsets, t->row_offsets,
+                          t->perm, t->inv, t->x_perm, k.ws, k.w, k.s));
+  return MOE_OK;
+}
+
+int do_gate_up(const moe_config* c, const moe_tensors* t, Call& k) {
+  MOE_NEED(t->x_perm); MOE_NEED(t->row_offsets); MOE_NEED(t->W_gu); MOE_NEED(t->h);
+  MOE_OPT(t->ab);
+  GemmCall g{};
+  g.kind = GK_GATE_UP;
+  g.row_offsets = t->row_offsets;
+  g.E = c->E;
+  g.rows = (int)k.w.R_cap;
+  g.A = t->x_perm;
+  g.lda = c->d;
+  g.B = t->W_gu;
+  g.K = c->d;
+  g.N = c->H;
+  g.H = c->H;
+  g.out0 = t->h;
+  g.ld0 = c->H;
+  g.out1 = t->ab;
+  g.ld1 = 2 * c->H;
+  g.status = k.status;
+  MOE_CUDA(launch_gemm(g, k.s));
+  return MOE_OK;
+}
+
+int do_down(const moe_config* c, const moe_tensors* t, Call& k) {
+  MOE_NEED(t->h); MOE_NEED(t->row_offsets); MOE_NEED(t->W_down); MOE_NEED(t->out_perm);
+  GemmCall g{};
+  g.kind = GK_DOWN;
+  g.row_offsets = t->row_offsets;
+  g.E = c->E;
+  g.rows = (int)k.w.R_cap;
+  g.A = t->h;
+  g.lda = c->H;
+  g.B = t->W_down;
+  g.K = c->H;
+  g.N = c->d;
+  g.out0 = t->out_perm;
+  g.ld0 = c->d;
+  g.status = k.status;
+  MOE_CUDA(launch_gemm(g, k.s));
+  return MOE_OK;
+}
+
+int do_shared(const moe_config* c, const moe_tensors* t, Call& k) {
+  const int Hs = hs_total(*c);
+  if (Hs == 0) return MOE_OK;
+  MOE_NEED(t->x); MOE_OPT(t->valid); MOE_NEED(t->Ws_gu); MOE_NEED(t->Ws_down);
+  MOE_NEED(t->s_h); MOE_NEED(t->s_out); MOE_OPT(t->s_ab);
+  GemmCall g{};
+  g.kind = GK_GATE_UP;
+  g.row_offsets = nullptr;
+  g.E = 1;
+  g.rows = c->T;
+  g.A = t->x;
+  g.lda = c->d;
+  g.B = t->Ws_gu;
+  g.K = c->d;
+  g.N = Hs;
+  g.H = Hs;
+  g.out0 = t->s_h;
+  g.ld0 = Hs;
+  g.out1 = t->s_ab;
+  g.ld1 = 2 * Hs;
+  g.valid = t->valid;
+  g.status = k.status;
+  MOE_CUDA(launch_gemm(g, k.s));
+  GemmCall d{};
+  d.kind = GK_DOWN;
+  d.row_offsets = nullptr;
+  d.E = 1;
+  d.rows = c->T;
+  d.A = t->s_h;
+  d.lda = Hs;
+  d.B = t->Ws_down;
+  d.K = Hs;
+  d.N = c->d;
+  d.out0 = t->s_out;
+  d.ld0 = c->d;
+  d.status = k.status;
+  MOE_CUDA(launch_gemm(d, k.s));
+  return MOE_OK;
+}
+
+int do_combine(const moe_config* c, const moe_tensors* t, Call& k) {
+  MOE_NEED(t->out_perm); MOE_NEED(t->inv); MOE_NEED(t->gates); MOE_OPT(t->valid);
+  MOE_NEED(t->y);
+  const void* s_out = nullptr;
+  if (hs_total(*c) > 0) {
+    MOE_NEED(t->s_out);
+    s_out = t->s_out;
+  }
+  MOE_CUDA(launch_combine(*c, t->out_perm, t->inv, t->gates, t->valid, s_out, t->y, k.s));
+  return MOE_OK;
+}
+
+int do_backward(const moe_config* c, const moe_tensors* t, const moe_grads* g, Call& k) {
+  if (!g) return MOE_ERR_NULL;
+  const int Hs = hs_total(*c);
+  MOE_NEED(g->dY); MOE_NEED(g->dx); MOE_NEED(g->dWr); MOE_NEED(g->dW_gu);
+  MOE_NEED(g->dW_down); MOE_NEED(g->d_logits);
+  MOE_NEED(t->x); MOE_NEED(t->Wr); MOE_OPT(t->valid); MOE_NEED(t->W_gu); MOE_NEED(t->W_down);
+  MOE_NEED(t->logits); MOE_NEED(t->topk_idx); MOE_NEED(t->gates); MOE_NEED(t->counts);
+  MOE_NEED(t->f); MOE_NEED(t->row_offsets); MOE_NEED(t->inv); MOE_NEED(t->x_perm);
+  MOE_NEED(t->ab); MOE_NEED(t->h); MOE_NEED(t->out_perm);
+  if (Hs > 0) {
+    MOE_NEED(t->Ws_gu); MOE_NEED(t->Ws_down); MOE_NEED(t->s_ab); MOE_NEED(t->s_h);
+    MOE_NEED(g->dWs_gu); MOE_NEED(g->dWs_down);
+  }
+  const WsLayout& w = k.w;
+  void* d_out = k.ws + w.d_out;
+  void* d_gu = k.ws + w.d_gu;
+  void* dx_perm = k.ws + w.dx_perm;
+  const int R = (int)w.R_cap;
+
+  // (i) + (vii): d_out, dg and the router-logit gradient
+  MOE_CUDA(launch_combine_bwd(*c, g->dY, t->out_perm, t->inv, t->topk_idx, t->gates, t->logits,
+                              t->f, t->counts, t->valid, t->row_offsets, d_out, g->d_logits,
+                              k.status, k.s));
+  // (ii) dH = d_out W_down[e], SwiGLU backward -> d_gu = [da | db]
+  GemmCall gh{};
+  gh.kind = GK_DH; gh.row_offsets = t->row_offsets; gh.E = c->E; gh.rows = R;
+  gh.A = d_out; gh.lda = c->d; gh.B = t->W_down; gh.K = c->d; gh.N = c->H; gh.H = c->H;
+  gh.out0 = d_gu; gh.ld0 = 2 * c->H; gh.aux_in = t->ab; gh.ld_aux = 2 * c->H;
+  gh.status = k.status;
+  MOE_CUDA(launch_gemm(gh, k.s));
+  // (iii) dx_perm = d_gu W_gu[e]
+  GemmCall gx{};
+  gx.kind = GK_DX; gx.row_offsets = t->row_offsets; gx.E = c->E; gx.rows = R;
+  gx.A = d_gu; gx.lda = 2 * c->H; gx.B = t->W_gu; gx.K = 2 * c->H; gx.N = c->d;
+  gx.out0 = dx_perm; gx.ld0 = c->d; gx.status = k.status;
+  MOE_CUDA(launch_gemm(gx, k.s));
+  // (iv) dW_down[e] = d_out_e^T h_e ; dW_gu[e] = d_gu_e^T x_perm_e
+  GemmCall wd{};
+  wd.kind = GK_DW; wd.row_offsets = t->row_offsets; wd.E = c->E; wd.rows = R;
+  wd.A = d_out; wd.lda = c->d; wd.Mdw = c->d; wd.B = t->h; wd.N = c->H;
+  wd.out0 = g->dW_down; wd.ld0 = c->H; wd.status = k.status;
+  MOE_CUDA(launch_gemm(wd, k.s));
+  GemmCall wg{};
+  wg.kind = GK_DW; wg.row_offsets = t->row_offsets; wg.E = c->E; wg.rows = R;
+  wg.A = d_gu; wg.lda = 2 * c->H; wg.Mdw = 2 * c->H; wg.B = t->x_perm; wg.N = c->d;
+  wg.out0 = g->dW_gu; wg.ld0 = c->d; wg.status = k.status;
+  MOE_CUDA(launch_gemm(wg, k.s));
+  // (v) shared expert
+  void* dxs = nullptr;
+  if (Hs > 0) {
+    void* ds_gu = k.ws + w.ds_gu;
+    dxs = k.ws + w.dxs;
+    GemmCall sh{};
+    sh.kind = GK_DH; sh.row_offsets = nullptr; sh.E = 1; sh.rows = c->T;
+    sh.A = g->dY; sh.lda = c->d; sh.B = t->Ws_down; sh.K = c->d; sh.N = Hs; sh.H = Hs;
+    sh.out0 = ds_gu; sh.ld0 = 2 * Hs; sh.aux_in = t->s_ab; sh.ld_aux = 2 * Hs;
+    sh.status = k.status;
+    MOE_CUDA(launch_gemm(sh, k.s));
+    GemmCall sx{};
+    sx.kind = GK_DX; sx.row_offsets = nullptr; sx.E = 1; sx.rows = c->T;
+    sx.A = ds_gu; sx.lda = 2 * Hs; sx.B = t->Ws_gu; sx.K = 2 * Hs; sx.N = c->d;
+    sx.out0 = dxs; sx.ld0 = c->d; sx.status = k.status;
+    MOE_CUDA(launch_gemm(sx, k.s));
+    GemmCall sw{};
+    sw.kind = GK_DW; sw.row_offsets = nullptr; sw.E = 1; sw.rows = c->T;
+    sw.A = g->dY; sw.lda = c->d; sw.Mdw = c->d; sw.B = t->s_h; sw.N = Hs;
+    sw.out0 = g->dWs_down; sw.ld0 = Hs; sw.status = k.status;
+    MOE_CUDA(launch_gemm(sw, k.s));
+    GemmCall sg{};
+    sg.kind = GK_DW; sg.row_offsets = nullptr; sg.E = 1; sg.rows = c->T;
+    sg.A = ds_gu; sg.lda = 2 * Hs; sg.Mdw = 2 * Hs; sg.B = t->x; sg.N = c->d;
+    sg.out0 = g->dWs_gu; sg.ld0 = c->d; sg.status = k.status;
+    MOE_CUDA(launch_gemm(sg, k.s));
+  }
+  // (vi) router input gradient and the un-permute sum of dx
+  float* dxr = nullptr;
+  if (!router_small_path(*c)) {
+    dxr = reinterpret_cast<float*>(k.ws + w.dxr);
+    MOE_CUDA(launch_router_dx(*c, g->d_logits, t->Wr, dxr, k.s));
+  }
+  MOE_CUDA(launch_dx_gather(*c, dx_perm, t->inv, dxs, dxr, g->d_logits, t->Wr, t->valid, g->dx,
+                            k.s));
+  MOE_CUDA(launch_router_dw(*c, t->x, g->d_logits, g->dWr,
+                            reinterpret_cast<float*>(k.ws + w.dwr_part), w.dwr_splits, k.s));
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_abi_version(void) { return MOE_ABI_VERSION; }
+
+const char* moe_strerror(int code) {
+  switch (code) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_NULL: return "a required pointer is NULL";
+    case MOE_ERR_SHAPE: return "configuration violates the shape rules";
+    case MOE_ERR_ALIGN: return "a tensor pointer is not 16-byte aligned";
+    case MOE_ERR_WORKSPACE: return "workspace missing or too small";
+    case MOE_ERR_CUDA: return "CUDA runtime call or kernel launch failed";
+    case MOE_ERR_DEVICE: return "current device is not an sm_100-family GPU";
+    case MOE_ERR_TIMEOUT: return "a bounded wait inside a kernel expired";
+    case MOE_ERR_INDEX: return "expert index out of range";
+    case MOE_ERR_NONFINITE: return "non-finite router logit";
+    default: return "unknown status code";
+  }
+}
+
+int moe_check_config(const moe_config* cfg) { return check_cfg(cfg); }
+
+int moe_row_capacity(const moe_config* cfg, int64_t* rows) {
+  int rc = check_cfg(cfg);
+  if (rc) return rc;
+  if (!rows) return MOE_ERR_NULL;
+  *rows = row_capacity(*cfg);
+  return MOE_OK;
+}
+
+int moe_workspace_bytes(const moe_config* cfg, int training, size_t* bytes) {
+  int rc = check_cfg(cfg);
+  if (rc) return rc;
+  if (!bytes) return MOE_ERR_NULL;
+  WsLayout w;
+  ws_layout(cfg, training, &w);
+  *bytes = w.total;
+  return MOE_OK;
+}
+
+int moe_get_status(void* workspace, void* stream, int* status) {
+  if (!workspace || !status) return MOE_ERR_NULL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int v = 0;
+  int* dev = static_cast<int*>(workspace);  // the status word sits at offset 0
+  if (cudaMemcpyAsync(&v, dev, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemsetAsync(dev, 0, sizeof(int), s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  *status = v;
+  return MOE_OK;
+}
+
+#define MOE_ENTRY(name, training, body)                                                      \
+  int name(const moe_config* cfg, const moe_tensors* t, void* workspace,                     \
+           size_t workspace_bytes, void* stream) {                                           \
+    Call k;                                                                                  \
+    int rc = begin(cfg, training, workspace, workspace_bytes, stream, &k);                   \
+    if (rc) return rc;                                                                       \
+    if (!t) return MOE_ERR_NULL;                                                             \
+    body                                                                                     \
+  }
+
+MOE_ENTRY(moe_router_logits, 0, { return do_router_logits(cfg, t, k); })
+MOE_ENTRY(moe_route, 0, { return do_route(cfg, t, k); })
+MOE_ENTRY(moe_permute, 0, { return do_permute(cfg, t, k); })
+MOE_ENTRY(moe_expert_gate_up, 0, { return do_gate_up(cfg, t, k); })
+MOE_ENTRY(moe_expert_down, 0, { return do_down(cfg, t, k); })
+MOE_ENTRY(moe_shared_ffn, 0, { return do_shared(cfg, t, k); })
+MOE_ENTRY(moe_combine, 0, { return do_combine(cfg, t, k); })
+MOE_ENTRY(moe_forward, 0, {
+  if ((rc = do_router_logits(cfg, t, k))) return rc;
+  if ((rc = do_route(cfg, t, k))) return rc;
+  if ((rc = do_permute(cfg, t, k))) return rc;
+  if ((rc = do_gate_up(cfg, t, k))) return rc;
+  if ((rc = do_down(cfg, t, k))) return rc;
+  if ((rc = do_shared(cfg, t, k))) return rc;
+  return do_combine(cfg, t, k);
+})
+
+int moe_backward(const moe_config* cfg, const moe_tensors* t, const moe_grads* g,
+                 void* workspace, size_t workspace_bytes, void* stream) {
+  Call k;
+  int rc = begin(cfg, 1, workspace, workspace_bytes, stream, &k);
+  if (rc) return rc;
+  if (!t) return MOE_ERR_NULL;
+  return do_backward(cfg, t, g, k);
+}
+
+}  // extern "C"

@@ -1,0 +1,891 @@
+// Bandwidth-bound kernels of the MoE layer (sm_103a): router logits for small
+// E, top-k routing with the f.p statistic, the stable counting-sort dispatch,
+// the weighted combine, and their backward passes; plus the router GEMMs on
+// the CUDA cores for large E.
+//
+// Pages: "KochiLLM v1.0" model card, Architecture (shared expert + top-2 of 4
+// routed, gates renormalised over the selected, E * sum f p balancing term);
+// "spark-gpt" README, feature list (fp32-softmax top-k routing, statistic over
+// real tokens, PAD filler positions).
+#include <float.h>
+#include <math.h>
+
+#include "moe_common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ bool row_real(const uint8_t* valid, int t) {
+  return valid == nullptr || valid[t] != 0;
+}
+
+// --------------------------------------------------------------------------
+// a0 (small E): logits[t][e] = sum_c x[t][c] * Wr[c][e], one warp per token.
+// Wr is staged in shared memory as [c][E] with 4 floats of padding after
+// every 8 rows, so the 8 rows a lane reads sit in distinct banks.
+// --------------------------------------------------------------------------
+__device__ __forceinline__ int wr_smem_index(int c, int e, int E) {
+  return c * E + (c >> 3) * 4 + e;
+}
+
+template <int E>
+__global__ void __launch_bounds__(kThreads)
+router_logits_small_kernel(const bf16* __restrict__ x, const float* __restrict__ Wr,
+                           float* __restrict__ L, int T, int d) {
+  extern __shared__ float wr_s[];
+  for (int i = threadIdx.x; i < d * E; i += blockDim.x) {
+    int c = i / E, e = i - c * E;
+    wr_s[wr_smem_index(c, e, E)] = Wr[i];
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int wpb = blockDim.x >> 5;
+  for (int t = blockIdx.x * wpb + (threadIdx.x >> 5); t < T; t += gridDim.x * wpb) {
+    float acc[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+    const bf16* xr = x + (size_t)t * d;
+    for (int c0 = lane * 8; c0 < d; c0 += 256) {
+      float xf[8];
+      unpack8(ld_nc_v4(xr + c0), xf);
+      const float* w = wr_s + wr_smem_index(c0, 0, E);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+#pragma unroll
+        for (int e4 = 0; e4 < E; e4 += 4) {
+          float4 wv = *reinterpret_cast<const float4*>(w + u * E + e4);
+          acc[e4 + 0] = fmaf(xf[u], wv.x, acc[e4 + 0]);
+          acc[e4 + 1] = fmaf(xf[u], wv.y, acc[e4 + 1]);
+          acc[e4 + 2] = fmaf(xf[u], wv.z, acc[e4 + 2]);
+          acc[e4 + 3] = fmaf(xf[u], wv.w, acc[e4 + 3]);
+        }
+      }
+    }
+    float mine = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      float v = warp_sum(acc[e]);
+      if (lane == e) mine = v;
+    }
+    if (lane < E) L[(size_t)t * E + lane] = mine;
+  }
+}
+
+// --------------------------------------------------------------------------
+// Generic fp32 GEMM on the CUDA cores: C[m][n] = sum_k A(m,k) B(k,n).
+// A(m,k) = A[m*sam + k*sak] (bf16 or fp32), B(k,n) = B[k*sbk + n*sbn] (fp32).
+// 64x64 tile, 16-deep K slices, 256 threads x (4x4) outputs.  Split-K along
+// gridDim.z writes partial tiles to C + z*M*N.
+// --------------------------------------------------------------------------
+template <typename TA>
+__device__ __forceinline__ float load_as_float(const TA* p);
+template <>
+__device__ __forceinline__ float load_as_float<float>(const float* p) { return *p; }
+template <>
+__device__ __forceinline__ float load_as_float<bf16>(const bf16* p) {
+  return __bfloat162float(*p);
+}
+
+template <typename TA>
+__global__ void __launch_bounds__(256)
+simt_gemm_kernel(const TA* __restrict__ A, long long sam, long long sak,
+                 const float* __restrict__ B, long long sbk, long long sbn,
+                 float* __restrict__ C, int M, int N, int K, int k_per_split) {
+  __shared__ float As[16][64 + 4];
+  __shared__ float Bs[16][64 + 4];
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
+  const int kbeg = blockIdx.z * k_per_split;
+  const int kend = min(K, kbeg + k_per_split);
+  float acc[4][4] = {};
+  for (int k0 = kbeg; k0 < kend; k0 += 16) {
+    for (int i = threadIdx.x; i < 16 * 64; i += 256) {
+      int kk, mm;
+      if (sak == 1) { mm = i / 16; kk = i % 16; } else { kk = i / 64; mm = i % 64; }
+      int m = m0 + mm, k = k0 + kk;
+      As[kk][mm] = (m < M && k < kend) ? load_as_float<TA>(A + m * sam + k * sak) : 0.f;
+    }
+    for (int i = threadIdx.x; i < 16 * 64; i += 256) {
+      int kk, nn;
+      if (sbn == 1) { kk = i / 64; nn = i % 64; } else { nn = i / 16; kk = i % 16; }
+      int n = n0 + nn, k = k0 + kk;
+      Bs[kk][nn] = (n < N && k < kend) ? B[k * sbk + n * sbn] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty + 16 * i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx + 16 * j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+  float* Cz = C + (size_t)blockIdx.z * M * N;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    int m = m0 + ty + 16 * i;
+    if (m >= M) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      int n = n0 + tx + 16 * j;
+      if (n < N) Cz[(size_t)m * N + n] = acc[i][j];
+    }
+  }
+}
+
+// Deterministic split-K reduction: out[i] = sum_z part[z][i] in z order.
+__global__ void sum_splits_kernel(const float* __restrict__ part, float* __restrict__ out,
+                                  int n, int splits) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+    float s = 0.f;
+    for (int z = 0; z < splits; ++z) s += part[(size_t)z * n + i];
+    out[i] = s;
+  }
+}
+
+// --------------------------------------------------------------------------
+// a1: routing.  A group of G lanes (a power of two <= 32) handles one token;
+// lane l of the group holds experts l, l+G, ..., (V per lane).
+// --------------------------------------------------------------------------
+struct Cand {
+  float key;
+  int idx;   // expert index, INT_MAX = none
+  float s;   // its softmax probability
+};
+
+// True if candidate (ka, ia) ranks before (kb, ib): larger key first, equal
+// keys lower index first; "none" ranks last.
+__device__ __forceinline__ bool ranks_before(float ka, int ia, float kb, int ib) {
+  if (ia == INT_MAX) return false;
+  if (ib == INT_MAX) return true;
+  return ka > kb || (ka == kb && ia < ib);
+}
+
+template <int V>
+__global__ void __launch_bounds__(kThreads)
+route_kernel(const float* __restrict__ L, const float* __restrict__ bias,
+             const uint8_t* __restrict__ valid, int T, int E, int k, int G, int norm_topk,
+             int32_t* __restrict__ topk, float* __restrict__ gates,
+             int* __restrict__ blk_cnt, float* __restrict__ blk_psum,
+             int* __restrict__ blk_treal, int* __restrict__ done,
+             int32_t* __restrict__ counts, float* __restrict__ f, float* __restrict__ p,
+             float* __restrict__ aux, int* __restrict__ status) {
+  extern __shared__ unsigned char smem_raw[];
+  const int groups = blockDim.x / G;
+  int* cnt_s = reinterpret_cast<int*>(smem_raw);                 // [E]
+  float* psum_s = reinterpret_cast<float*>(cnt_s + 256);         // [groups][E]
+  __shared__ int treal_s;
+  __shared__ int ticket_s;
+  __shared__ float red_s[kThreads / 32];
+
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt_s[e] = 0;
+  if (threadIdx.x == 0) treal_s = 0;
+  __syncthreads();
+
+  const int lane = threadIdx.x & 31;
+  const int lig = lane & (G - 1);           // lane in group
+  const int grp = threadIdx.x / G;          // group in block
+  float psum[V];
+#pragma unroll
+  for (int v = 0; v < V; ++v) psum[v] = 0.f;
+  int my_treal = 0;
+
+  const int tokens_per_iter = groups * gridDim.x;
+  for (int t0 = blockIdx.x * groups; t0 < T; t0 += tokens_per_iter) {
+    const int t = t0 + grp;
+    const bool in_range = t < T;
+    const bool real = in_range && row_real(valid, t);
+    float lv[V], kv[V], sv[V];
+    bool bad = false;
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+      const int e = lig + G * v;
+      if (in_range && e < E) {
+        lv[v] = L[(size_t)t * E + e];
+        kv[v] = bias ? lv[v] + bias[e] : lv[v];
+        bad |= !isfinite(lv[v]) || !isfinite(kv[v]);
+      } else {
+        lv[v] = -FLT_MAX;
+        kv[v] = -FLT_MAX;
+      }
+    }
+    if (bad && real) set_status(status, MOE_ERR_NONFINITE);
+    // softmax over the E logits (unbiased)
+    float m = -FLT_MAX;
+#pragma unroll
+    for (int v = 0; v < V; ++v) m = fmaxf(m, lv[v]);
+    for (int o = G >> 1; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float sum = 0.f;
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+      const int e = lig + G * v;
+      sv[v] = (in_range && e < E) ? expf(lv[v] - m) : 0.f;
+      sum += sv[v];
+    }
+    for (int o = G >> 1; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+#pragma unroll
+    for (int v = 0; v < V; ++v) sv[v] = sv[v] / sum;
+
+    // top-k by repeated group arg-max
+    unsigned taken = 0;
+    float sel_s[V];
+    int sel_i[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) { sel_s[v] = 0.f; sel_i[v] = -1; }
+    float ssum = 0.f;
+    for (int j = 0; j < k; ++j) {
+      float bk = 0.f, bs = 0.f;
+      int bi = INT_MAX;
+#pragma unroll
+      for (int v = 0; v < V; ++v) {
+        const int e = lig + G * v;
+        if (e < E && !((taken >> v) & 1u) && ranks_before(kv[v], e, bk, bi)) {
+          bk = kv[v]; bi = e; bs = sv[v];
+        }
+      }
+      for (int o = G >> 1; o > 0; o >>= 1) {
+        float ok = __shfl_xor_sync(0xffffffffu, bk, o);
+        int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        float os = __shfl_xor_sync(0xffffffffu, bs, o);
+        if (ranks_before(ok, oi, bk, bi)) { bk = ok; bi = oi; bs = os; }
+      }
+      // the owner of the winner marks it taken
+      if (bi != INT_MAX && (bi & (G - 1)) == lig) taken |= 1u << (bi / G);
+      ssum += bs;
+#pragma unroll
+      for (int v = 0; v < V; ++v)
+        if (j == lig + G * v) { sel_s[v] = bs; sel_i[v] = bi; }
+    }
+    if (in_range) {
+#pragma unroll
+      for (int v = 0; v < V; ++v) {
+        const int j = lig + G * v;
+        if (j < k) {
+          int32_t ix = real ? sel_i[v] : -1;
+          float g = real ? (norm_topk ? sel_s[v] / ssum : sel_s[v]) : 0.f;
+          topk[(size_t)t * k + j] = ix;
+          gates[(size_t)t * k + j] = g;
+          if (real) atomicAdd(&cnt_s[sel_i[v]], 1);
+        }
+      }
+    }
+    if (real) {
+#pragma unroll
+      for (int v = 0; v < V; ++v) psum[v] += sv[v];
+      if (lig == 0) ++my_treal;
+    }
+  }
+  // block partials, reduced in a fixed order
+#pragma unroll
+  for (int v = 0; v < V; ++v) {
+    const int e = lig + G * v;
+    if (e < E) psum_s[grp * E + e] = psum[v];
+  }
+  if (lig == 0 && my_treal) atomicAdd(&treal_s, my_treal);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    float s = 0.f;
+    for (int g2 = 0; g2 < groups; ++g2) s += psum_s[g2 * E + e];
+    blk_psum[(size_t)blockIdx.x * E + e] = s;
+    blk_cnt[(size_t)blockIdx.x * E + e] = cnt_s[e];
+  }
+  if (threadIdx.x == 0) blk_treal[blockIdx.x] = treal_s;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) ticket_s = atomicAdd(done, 1);
+  __syncthreads();
+  if (ticket_s != (int)gridDim.x - 1) return;
+
+  // last block: totals over blocks in block order
+  __threadfence();
+  int Tr = 0;
+  for (int b = 0; b < (int)gridDim.x; ++b) Tr += __ldcg(blk_treal + b);
+  float part = 0.f;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int c = 0;
+    float ps = 0.f;
+    for (int b = 0; b < (int)gridDim.x; ++b) {
+      c += __ldcg(blk_cnt + (size_t)b * E + e);
+      ps += __ldcg(blk_psum + (size_t)b * E + e);
+    }
+    float fe = Tr > 0 ? (float)c / (float)((long long)k * Tr) : 0.f;
+    float pe = Tr > 0 ? ps / (float)Tr : 0.f;
+    counts[e] = c;
+    f[e] = fe;
+    p[e] = pe;
+    part = fmaf(fe, pe, part);
+  }
+  part = warp_sum(part);
+  if (lane == 0) red_s[threadIdx.x >> 5] = part;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float s = 0.f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) s += red_s[w];
+    aux[0] = (float)E * s;
+    *done = 0;
+  }
+}
+
+// --------------------------------------------------------------------------
+// a2: stable counting-sort dispatch.
+// --------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads)
+perm_hist_kernel(const int32_t* __restrict__ topk, int T, int k, int E,
+                 int* __restrict__ hist, int* __restrict__ status) {
+  __shared__ int h[256];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) h[e] = 0;
+  __syncthreads();
+  const long long q0 = (long long)blockIdx.x * kPermChunk * k;
+  const long long q1 = min((long long)T * k, q0 + (long long)kPermChunk * k);
+  for (long long q = q0 + threadIdx.x; q < q1; q += blockDim.x) {
+    int e = topk[q];
+    if (e >= E) set_status(status, MOE_ERR_INDEX);
+    else if (e >= 0) atomicAdd(&h[e], 1);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[(size_t)blockIdx.x * E + e] = h[e];
+}
+
+__global__ void __launch_bounds__(kThreads)
+perm_scan_kernel(const int* __restrict__ hist, int nblk, int E, int32_t* __restrict__ counts,
+                 int32_t* __restrict__ offsets, int32_t* __restrict__ row_offsets,
+                 int* __restrict__ base) {
+  __shared__ int cnt_s[257];
+  __shared__ int off_s[257];
+  __shared__ int roff_s[257];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = 0;
+    for (int b = 0; b < nblk; ++b) {
+      base[(size_t)b * E + e] = run;
+      run += hist[(size_t)b * E + e];
+    }
+    cnt_s[e] = run;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int o = 0, ro = 0;
+    for (int e = 0; e < E; ++e) {
+      off_s[e] = o;
+      roff_s[e] = ro;
+      o += cnt_s[e];
+      ro += (cnt_s[e] + kRowAlign - 1) / kRowAlign * kRowAlign;
+    }
+    off_s[E] = o;
+    roff_s[E] = ro;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+    offsets[e] = off_s[e];
+    row_offsets[e] = roff_s[e];
+    if (e < E) counts[e] = cnt_s[e];
+  }
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    for (int b = 0; b < nblk; ++b) base[(size_t)b * E + e] += roff_s[e];
+}
+
+// Ranks each (t, j) pair of the block's token chunk in pair order with one
+// warp (warp match + popc per 32 pairs), then copies each token's x row once
+// into its k destination rows.  The block also zeroes the pad rows of the
+// experts e = blockIdx.x (mod gridDim.x).
+__global__ void __launch_bounds__(kThreads)
+perm_scatter_kernel(const bf16* __restrict__ x, const int32_t* __restrict__ topk, int T,
+                    int d, int k, int E, const int* __restrict__ base,
+                    const int32_t* __restrict__ counts, const int32_t* __restrict__ row_offsets,
+                    int32_t* __restrict__ perm, int32_t* __restrict__ inv,
+                    bf16* __restrict__ x_perm) {
+  __shared__ int base_s[256];
+  __shared__ int dest_s[kPermChunk * kMaxK];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int t_beg = blockIdx.x * kPermChunk;
+  const int t_end = min(T, t_beg + kPermChunk);
+  const int npairs = (t_end - t_beg) * k;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) base_s[e] = base[(size_t)blockIdx.x * E + e];
+  __syncthreads();
+  if (warp == 0) {
+    const unsigned lt = (1u << lane) - 1u;
+    for (int q0 = 0; q0 < npairs; q0 += 32) {
+      const int ql = q0 + lane;
+      int e = ql < npairs ? topk[(size_t)t_beg * k + ql] : -1;
+      const bool ok = e >= 0 && e < E;
+      const unsigned act = __ballot_sync(0xffffffffu, ok);
+      int dest = -1;
+      unsigned peers = 0;
+      if (ok) {
+        peers = __match_any_sync(act, e);
+        dest = base_s[e] + __popc(peers & lt);
+      }
+      __syncwarp();
+      if (ok && lane == 31 - __clz(peers)) base_s[e] += __popc(peers);
+      if (ql < npairs) dest_s[ql] = dest;
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  for (int ql = threadIdx.x; ql < npairs; ql += blockDim.x) {
+    const int dest = dest_s[ql];
+    const long long q = (long long)t_beg * k + ql;
+    inv[q] = dest;
+    if (dest >= 0) perm[dest] = (int32_t)q;
+  }
+  // row copies: one warp per token, each x row read once
+  const int wpb = blockDim.x >> 5;
+  for (int tl = warp; tl < t_end - t_beg; tl += wpb) {
+    const int t = t_beg + tl;
+    const bf16* src = x + (size_t)t * d;
+    int dst[kMaxK];
+    int nd = 0;
+    for (int j = 0; j < k; ++j) {
+      int r = dest_s[tl * k + j];
+      if (r >= 0) dst[nd++] = r;
+    }
+    if (nd == 0) continue;
+    for (int c0 = lane * 8; c0 < d; c0 += 256) {
+      uint4 v = ld_nc_v4(src + c0);
+      for (int j = 0; j < nd; ++j) st_v4(x_perm + (size_t)dst[j] * d + c0, v);
+    }
+  }
+  // zero pad rows
+  for (int e = blockIdx.x; e < E; e += gridDim.x) {
+    const int r0 = row_offsets[e] + counts[e];
+    const int r1 = row_offsets[e + 1];
+    for (int r = r0 + warp; r < r1; r += wpb) {
+      if (lane == 0) perm[r] = -1;
+      for (int c0 = lane * 8; c0 < d; c0 += 256)
+        st_v4(x_perm + (size_t)r * d + c0, make_uint4(0, 0, 0, 0));
+    }
+  }
+}
+
+// --------------------------------------------------------------------------
+// a6: y[t] = sum_j g[t][j] out_perm[inv[t][j]] (+ s_out[t]); one warp/token.
+// --------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads)
+combine_kernel(const bf16* __restrict__ out_perm, const int32_t* __restrict__ inv,
+               const float* __restrict__ gates, const uint8_t* __restrict__ valid,
+               const bf16* __restrict__ s_out, bf16* __restrict__ y, int T, int d, int k) {
+  const int lane = threadIdx.x & 31;
+  const int wpb = blockDim.x >> 5;
+  for (int t = blockIdx.x * wpb + (threadIdx.x >> 5); t < T; t += gridDim.x * wpb) {
+    const bool real = row_real(valid, t);
+    int my_r = -1;
+    float my_g = 0.f;
+    if (lane < k && real) {
+      my_r = inv[(size_t)t * k + lane];
+      my_g = gates[(size_t)t * k + lane];
+    }
+    bf16* yr = y + (size_t)t * d;
+    for (int c0 = lane * 8; c0 < d; c0 += 256) {
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (real) {
+        for (int j = 0; j < k; ++j) {
+          const int r = __shfl_sync(0xffffffffu, my_r, j);
+          const float g = __shfl_sync(0xffffffffu, my_g, j);
+          if (r < 0) continue;
+          float v[8];
+          unpack8(ld_nc_v4(out_perm + (size_t)r * d + c0), v);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) acc[u] = fmaf(g, v[u], acc[u]);
+        }
+        if (s_out) {
+          float v[8];
+          unpack8(ld_nc_v4(s_out + (size_t)t * d + c0), v);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) acc[u] += v[u];
+        }
+      }
+      st_v4(yr + c0, pack8(acc));
+    }
+  }
+}
+
+// --------------------------------------------------------------------------
+// a7 (i) + (vii): combine backward and the router-logit gradient.
+// d_out[inv[t,j]] = g[t,j] dY[t];  dg[t,j] = <dY[t], out_perm[inv[t,j]]>;
+// d_logits from dg through the gate map, plus the aux term
+// (aux_coef E / T_real) s_e (f_e - sum_i f_i s_i).  Also zeroes d_out pad rows.
+// --------------------------------------------------------------------------
+template <int V>
+__global__ void __launch_bounds__(kThreads)
+combine_bwd_kernel(const bf16* __restrict__ dY, const bf16* __restrict__ out_perm,
+                   const int32_t* __restrict__ inv, const int32_t* __restrict__ topk,
+                   const float* __restrict__ gates, const float* __restrict__ L,
+                   const float* __restrict__ f, const int32_t* __restrict__ counts,
+                   const uint8_t* __restrict__ valid, const int32_t* __restrict__ row_offsets,
+                   bf16* __restrict__ d_out, float* __restrict__ d_logits, int T, int d, int E,
+                   int k, int norm_topk, float aux_coef) {
+  __shared__ float f_s[256];
+  __shared__ float coef_s;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int wpb = blockDim.x >> 5;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) f_s[e] = f[e];
+  if (threadIdx.x == 0) {
+    long long m = 0;
+    for (int e = 0; e < E; ++e) m += counts[e];
+    const long long Tr = m / k;
+    coef_s = Tr > 0 ? aux_coef * (float)E / (float)Tr : 0.f;
+  }
+  __syncthreads();
+  const float coef = coef_s;
+  for (int t = blockIdx.x * wpb + warp; t < T; t += gridDim.x * wpb) {
+    const bool real = row_real(valid, t);
+    float* dl = d_logits + (size_t)t * E;
+    if (!real) {
+      for (int e = lane; e < E; e += 32) dl[e] = 0.f;
+      continue;
+    }
+    int my_r = -1, my_i = -1;
+    float my_g = 0.f;
+    if (lane < k) {
+      my_r = inv[(size_t)t * k + lane];
+      my_i = topk[(size_t)t * k + lane];
+      my_g = gates[(size_t)t * k + lane];
+    }
+    const bf16* dyr = dY + (size_t)t * d;
+    float my_dg = 0.f;
+    for (int j = 0; j < k; ++j) {
+      const int r = __shfl_sync(0xffffffffu, my_r, j);
+      const float g = __shfl_sync(0xffffffffu, my_g, j);
+      float dot = 0.f;
+      if (r >= 0) {
+        for (int c0 = lane * 8; c0 < d; c0 += 256) {
+          float dy[8], o[8], go[8];
+          unpack8(ld_nc_v4(dyr + c0), dy);
+          unpack8(ld_nc_v4(out_perm + (size_t)r * d + c0), o);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            dot = fmaf(dy[u], o[u], dot);
+            go[u] = g * dy[u];
+          }
+          st_v4(d_out + (size_t)r * d + c0, pack8(go));
+        }
+      }
+      dot = warp_sum(dot);
+      if (lane == j) my_dg = dot;
+    }
+    // sum_j g_j dg_j (slot order)
+    float gdg = 0.f;
+    for (int j = 0; j < k; ++j)
+      gdg = fmaf(__shfl_sync(0xffffffffu, my_g, j), __shfl_sync(0xffffffffu, my_dg, j), gdg);
+    // softmax of the logits (for the aux term and the no-renorm map)
+    float lv[V], sv[V];
+    float m = -FLT_MAX;
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+      const int e = lane + 32 * v;
+      lv[v] = e < E ? L[(size_t)t * E + e] : -FLT_MAX;
+      m = fmaxf(m, lv[v]);
+    }
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float sum = 0.f;
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+      const int e = lane + 32 * v;
+      sv[v] = e < E ? expf(lv[v] - m) : 0.f;
+      sum += sv[v];
+    }
+    sum = warp_sum(sum);
+    float fs = 0.f;
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+      const int e = lane + 32 * v;
+      sv[v] = sv[v] / sum;
+      if (e < E) fs = fmaf(f_s[e], sv[v], fs);
+    }
+    fs = warp_sum(fs);
+    float main[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) main[v] = 0.f;
+    for (int j = 0; j < k; ++j) {
+      const int ej = __shfl_sync(0xffffffffu, my_i, j);
+      const float dgj = __shfl_sync(0xffffffffu, my_dg, j);
+      const float gj = __shfl_sync(0xffffffffu, my_g, j);
+#pragma unroll
+      for (int v = 0; v < V; ++v)
+        if (lane + 32 * v == ej) main[v] += norm_topk ? gj * (dgj - gdg) : sv[v] * dgj;
+    }
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+      const int e = lane + 32 * v;
+      if (e >= E) continue;
+      float mv = main[v];
+      if (!norm_topk) mv -= sv[v] * gdg;
+      dl[e] = mv + coef * sv[v] * (f_s[e] - fs);
+    }
+  }
+  // zero d_out pad rows
+  for (int e = blockIdx.x; e < E; e += gridDim.x) {
+    const int r0 = row_offsets[e] + counts[e];
+    const int r1 = row_offsets[e + 1];
+    for (int r = r0 + warp; r < r1; r += wpb)
+      for (int c0 = lane * 8; c0 < d; c0 += 256)
+        st_v4(d_out + (size_t)r * d + c0, make_uint4(0, 0, 0, 0));
+  }
+}
+
+// --------------------------------------------------------------------------
+// a7 (vi): dx[t] = sum_j dx_perm[inv[t,j]] + dxs[t] + d_logits[t] Wr^T.
+// The router term comes from dxr (large E) or from Wr staged in shared
+// memory (small E).  PAD rows get 0.
+// --------------------------------------------------------------------------
+template <int ES>
+__global__ void __launch_bounds__(kThreads)
+dx_gather_kernel(const bf16* __restrict__ dx_perm, const int32_t* __restrict__ inv,
+                 const bf16* __restrict__ dxs, const float* __restrict__ dxr,
+                 const float* __restrict__ dL, const float* __restrict__ Wr,
+                 const uint8_t* __restrict__ valid, bf16* __restrict__ dx, int T, int d,
+                 int k) {
+  extern __shared__ float wr_s[];
+  if constexpr (ES > 0) {
+    for (int i = threadIdx.x; i < d * ES; i += blockDim.x) {
+      int c = i / ES, e = i - c * ES;
+      wr_s[wr_smem_index(c, e, ES)] = Wr[i];
+    }
+    __syncthreads();
+  }
+  const int lane = threadIdx.x & 31;
+  const int wpb = blockDim.x >> 5;
+  for (int t = blockIdx.x * wpb + (threadIdx.x >> 5); t < T; t += gridDim.x * wpb) {
+    const bool real = row_real(valid, t);
+    int my_r = -1;
+    if (lane < k && real) my_r = inv[(size_t)t * k + lane];
+    float dl[ES > 0 ? ES : 1];
+    if constexpr (ES > 0) {
+#pragma unroll
+      for (int e = 0; e < ES; ++e) dl[e] = real ? dL[(size_t)t * ES + e] : 0.f;
+    }
+    for (int c0 = lane * 8; c0 < d; c0 += 256) {
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (real) {
+        for (int j = 0; j < k; ++j) {
+          const int r = __shfl_sync(0xffffffffu, my_r, j);
+          if (r < 0) continue;
+          float v[8];
+          unpack8(ld_nc_v4(dx_perm + (size_t)r * d + c0), v);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) acc[u] += v[u];
+        }
+        if (dxs) {
+          float v[8];
+          unpack8(ld_nc_v4(dxs + (size_t)t * d + c0), v);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) acc[u] += v[u];
+        }
+        if constexpr (ES > 0) {
+          const float* w = wr_s + wr_smem_index(c0, 0, ES);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            float s = 0.f;
+#pragma unroll
+            for (int e4 = 0; e4 < ES; e4 += 4) {
+              float4 wv = *reinterpret_cast<const float4*>(w + u * ES + e4);
+              s = fmaf(dl[e4 + 0], wv.x, s);
+              s = fmaf(dl[e4 + 1], wv.y, s);
+              s = fmaf(dl[e4 + 2], wv.z, s);
+              s = fmaf(dl[e4 + 3], wv.w, s);
+            }
+            acc[u] += s;
+          }
+        } else if (dxr) {
+          const float4* pr = reinterpret_cast<const float4*>(dxr + (size_t)t * d + c0);
+          float4 a = pr[0], b = pr[1];
+          acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+          acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+        }
+      }
+      st_v4(dx + (size_t)t * d + c0, pack8(acc));
+    }
+  }
+}
+
+int grid_for(int items_per_block, long long items, int cap) {
+  long long g = (items + items_per_block - 1) / items_per_block;
+  if (g < 1) g = 1;
+  if (g > cap) g = cap;
+  return (int)g;
+}
+
+int small_E(int E) { return (E == 4 || E == 8 || E == 16) ? E : 0; }
+
+}  // namespace
+
+bool router_small_path(const moe_config& c) {
+  const int es = small_E(c.E);
+  return es > 0 && (size_t)c.d * es * 4 + (size_t)(c.d / 8) * 16 <= 96 * 1024;
+}
+
+static size_t wr_smem_bytes(int d, int E) { return (size_t)d * E * 4 + (size_t)(d / 8 + 1) * 16; }
+
+cudaError_t launch_router_logits(const moe_config& c, const void* x, const float* Wr, float* L,
+                                 cudaStream_t s) {
+  DeviceInfo di;
+  if (device_info(&di) != MOE_OK) return cudaErrorUnknown;
+  if (router_small_path(c)) {
+    const size_t smem = wr_smem_bytes(c.d, c.E);
+    const int grid = grid_for(kThreads / 32, c.T, di.num_sms * 4);
+    const bf16* xb = static_cast<const bf16*>(x);
+    switch (c.E) {
+      case 4:
+        cudaFuncSetAttribute(router_logits_small_kernel<4>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        router_logits_small_kernel<4><<<grid, kThreads, smem, s>>>(xb, Wr, L, c.T, c.d);
+        break;
+      case 8:
+        cudaFuncSetAttribute(router_logits_small_kernel<8>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        router_logits_small_kernel<8><<<grid, kThreads, smem, s>>>(xb, Wr, L, c.T, c.d);
+        break;
+      default:
+        cudaFuncSetAttribute(router_logits_small_kernel<16>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        router_logits_small_kernel<16><<<grid, kThreads, smem, s>>>(xb, Wr, L, c.T, c.d);
+        break;
+    }
+    return cudaGetLastError();
+  }
+  // L[T][E] = x[T][d] . Wr[d][E]
+  dim3 grid((c.E + 63) / 64, (c.T + 63) / 64, 1);
+  simt_gemm_kernel<bf16><<<grid, 256, 0, s>>>(static_cast<const bf16*>(x), c.d, 1, Wr, c.E, 1,
+                                               L, c.T, c.E, c.d, c.d);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_dx(const moe_config& c, const float* dL, const float* Wr, float* dxr,
+                             cudaStream_t s) {
+  // dxr[T][d] = dL[T][E] . Wr^T ; B(k=e, n=c) = Wr[c*E + e]
+  dim3 grid((c.d + 63) / 64, (c.T + 63) / 64, 1);
+  simt_gemm_kernel<float><<<grid, 256, 0, s>>>(dL, c.E, 1, Wr, 1, c.E, dxr, c.T, c.d, c.E, c.E);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_dw(const moe_config& c, const void* x, const float* dL, float* dWr,
+                             float* part, int splits, cudaStream_t s) {
+  // dWr[d][E] = sum_t x[t][c] dL[t][e]: A(m=c, k=t) = x[t*d + c]
+  const int kps = ((c.T + splits - 1) / splits + 15) / 16 * 16;
+  dim3 grid((c.E + 63) / 64, (c.d + 63) / 64, splits);
+  simt_gemm_kernel<bf16><<<grid, 256, 0, s>>>(static_cast<const bf16*>(x), 1, c.d, dL, c.E, 1,
+                                               part, c.d, c.E, c.T, kps);
+  const int n = c.d * c.E;
+  sum_splits_kernel<<<(n + 255) / 256, 256, 0, s>>>(part, dWr, n, splits);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route(const moe_config& c, const float* L, const float* bias,
+                         const uint8_t* valid, int32_t* topk, float* gates, int32_t* counts,
+                         float* f, float* p, float* aux, char* ws, const WsLayout& w,
+                         cudaStream_t s) {
+  int G = 1;
+  while (G < c.E && G < 32) G <<= 1;
+  const int V = (c.E + G - 1) / G;
+  const int groups = kThreads / G;
+  const size_t smem = 256 * sizeof(int) + (size_t)groups * c.E * sizeof(float);
+  int* done = reinterpret_cast<int*>(ws + w.route_done);
+  cudaError_t err = cudaMemsetAsync(done, 0, sizeof(int), s);
+  if (err != cudaSuccess) return err;
+  int* cnt = reinterpret_cast<int*>(ws + w.route_cnt);
+  float* psum = reinterpret_cast<float*>(ws + w.route_psum);
+  int* treal = reinterpret_cast<int*>(ws + w.route_treal);
+  int* status = reinterpret_cast<int*>(ws + w.status);
+  const int grid = w.route_blocks;
+#define MOE_ROUTE(VV)                                                                        \
+  cudaFuncSetAttribute(route_kernel<VV>, cudaFuncAttributeMaxDynamicSharedMemorySize,        \
+                       (int)smem);                                                           \
+  route_kernel<VV><<<grid, kThreads, smem, s>>>(L, bias, valid, c.T, c.E, c.k, G, c.norm_topk, \
+                                                topk, gates, cnt, psum, treal, done, counts, f, \
+                                                p, aux, status)
+  if (V <= 1) { MOE_ROUTE(1); }
+  else if (V <= 2) { MOE_ROUTE(2); }
+  else if (V <= 4) { MOE_ROUTE(4); }
+  else { MOE_ROUTE(8); }
+#undef MOE_ROUTE
+  return cudaGetLastError();
+}
+
+cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* topk,
+                           int32_t* counts, int32_t* offsets, int32_t* row_offsets,
+                           int32_t* perm, int32_t* inv, void* x_perm, char* ws,
+                           const WsLayout& w, cudaStream_t s) {
+  int* hist = reinterpret_cast<int*>(ws + w.perm_hist);
+  int* base = reinterpret_cast<int*>(ws + w.perm_base);
+  int* status = reinterpret_cast<int*>(ws + w.status);
+  const int nblk = w.perm_blocks;
+  perm_hist_kernel<<<nblk, kThreads, 0, s>>>(topk, c.T, c.k, c.E, hist, status);
+  perm_scan_kernel<<<1, kThreads, 0, s>>>(hist, nblk, c.E, counts, offsets, row_offsets, base);
+  perm_scatter_kernel<<<nblk, kThreads, 0, s>>>(static_cast<const bf16*>(x), topk, c.T, c.d,
+                                                c.k, c.E, base, counts, row_offsets, perm, inv,
+                                                static_cast<bf16*>(x_perm));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const moe_config& c, const void* out_perm, const int32_t* inv,
+                           const float* gates, const uint8_t* valid, const void* s_out,
+                           void* y, cudaStream_t s) {
+  DeviceInfo di;
+  if (device_info(&di) != MOE_OK) return cudaErrorUnknown;
+  const int grid = grid_for(kThreads / 32, c.T, di.num_sms * 8);
+  combine_kernel<<<grid, kThreads, 0, s>>>(static_cast<const bf16*>(out_perm), inv, gates, valid,
+                                           static_cast<const bf16*>(s_out),
+                                           static_cast<bf16*>(y), c.T, c.d, c.k);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_bwd(const moe_config& c, const void* dY, const void* out_perm,
+                               const int32_t* inv, const int32_t* topk, const float* gates,
+                               const float* L, const float* f, const int32_t* counts,
+                               const uint8_t* valid, const int32_t* row_offsets, void* d_out,
+                               float* d_logits, int* status, cudaStream_t s) {
+  (void)status;
+  DeviceInfo di;
+  if (device_info(&di) != MOE_OK) return cudaErrorUnknown;
+  const int grid = grid_for(kThreads / 32, c.T, di.num_sms * 8);
+  const int V = (c.E + 31) / 32;
+#define MOE_CBWD(VV)                                                                          \
+  combine_bwd_kernel<VV><<<grid, kThreads, 0, s>>>(                                           \
+      static_cast<const bf16*>(dY), static_cast<const bf16*>(out_perm), inv, topk, gates, L, f, \
+      counts, valid, row_offsets, static_cast<bf16*>(d_out), d_logits, c.T, c.d, c.E, c.k,     \
+      c.norm_topk, c.aux_coef)
+  if (V <= 1) { MOE_CBWD(1); }
+  else if (V <= 2) { MOE_CBWD(2); }
+  else if (V <= 4) { MOE_CBWD(4); }
+  else { MOE_CBWD(8); }
+#undef MOE_CBWD
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dx_gather(const moe_config& c, const void* dx_perm, const int32_t* inv,
+                             const void* dxs, const float* dxr, const float* d_logits,
+                             const float* Wr, const uint8_t* valid, void* dx, cudaStream_t s) {
+  DeviceInfo di;
+  if (device_info(&di) != MOE_OK) return cudaErrorUnknown;
+  const int grid = grid_for(kThreads / 32, c.T, di.num_sms * 4);
+  const bf16* dp = static_cast<const bf16*>(dx_perm);
+  const bf16* ds = static_cast<const bf16*>(dxs);
+  bf16* o = static_cast<bf16*>(dx);
+  if (router_small_path(c)) {
+    const size_t smem = wr_smem_bytes(c.d, c.E);
+#define MOE_DXG(EE)                                                                           \
+  cudaFuncSetAttribute(dx_gather_kernel<EE>, cudaFuncAttributeMaxDynamicSharedMemorySize,     \
+                       (int)smem);                                                            \
+  dx_gather_kernel<EE><<<grid, kThreads, smem, s>>>(dp, inv, ds, nullptr, d_logits, Wr, valid, \
+                                                    o, c.T, c.d, c.k)
+    if (c.E == 4) { MOE_DXG(4); }
+    else if (c.E == 8) { MOE_DXG(8); }
+    else { MOE_DXG(16); }
+#undef MOE_DXG
+  } else {
+    dx_gather_kernel<0><<<grid, kThreads, 0, s>>>(dp, inv, ds, dxr, d_logits, Wr, valid, o, c.T,
+                                                  c.d, c.k);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,542 @@
+// Persistent grouped GEMMs of the MoE experts on the 5th-generation tensor
+// cores (sm_103a): TMA (cp.async.bulk.tensor, 128-byte swizzle) feeds a
+// 4-stage shared-memory ring; one thread issues tcgen05.mma (bf16 x bf16 ->
+// fp32) into a double-buffered TMEM accumulator; four epilogue warps read the
+// accumulator back with tcgen05.ld and apply the fused epilogue.
+//
+// "spark-gpt" README, Hard-won facts: the MoE experts run as grouped GEMMs
+// with the SwiGLU fused into the epilogue (there on GB10 with Triton; here a
+// tcgen05/TMEM design for GB300).  "KochiLLM v1.0" card, Configuration: SwiGLU
+// experts.
+//
+// One kernel template covers the five products of the layer:
+//   GK_GATE_UP  rows x W_gu[e]^T  -> h = silu(a) * b   (A, B K-major)
+//   GK_DOWN     h x W_down[e]^T   -> out               (A, B K-major)
+//   GK_DH       d_out x W_down[e] -> SwiGLU backward   (A K-major, B MN-major)
+//   GK_DX       d_gu x W_gu[e]    -> dx_perm           (A K-major, B MN-major)
+//   GK_DW       A_e^T B_e over the rows of expert e    (A, B MN-major)
+// Row-grouped kinds read the expert of each 128-row block from the padded
+// segment offsets on the device, so no host synchronisation is needed.
+#include <cstdio>
+#include <mutex>
+
+#include "moe_common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int BM = 128;                  // tile rows (UMMA M)
+constexpr int BN = 256;                  // tile columns (UMMA N)
+constexpr int BK = 64;                   // K per stage = one 128-byte swizzle row
+constexpr int UK = 16;                   // K per tcgen05.mma (bf16)
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;     // 16 KB
+constexpr int B_BYTES = BN * BK * 2;     // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int TMEM_COLS = 512;           // two 128 x 256 fp32 accumulators
+constexpr int THREADS = 256;             // warp 0 TMA, 1 MMA, 2 TMEM, 4-7 epilogue
+constexpr int EPI_WARP0 = 4;
+constexpr uint64_t WAIT_NS = 2000000000ull;  // bounded waits give up after 2 s
+constexpr uint64_t DRAIN_NS = 200000000ull;
+constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 2048;
+
+struct Params {
+  const int32_t* row_offsets;  // routed: [E+1] padded offsets; dense: NULL
+  int E;
+  int rows;                    // dense row count (GK_DW: K rows)
+  int K;
+  int N;
+  int H;
+  int Mdw;
+  int n_tiles;
+  int m_tiles_dw;
+  bf16* out0;
+  int ld0;
+  bf16* out1;
+  int ld1;
+  const bf16* aux_in;
+  int ld_aux;
+  const uint8_t* valid;
+  int* status;
+};
+
+struct Shared {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+  int roff[257];
+};
+
+struct Tile {
+  int e, m0, n0, kbeg, ksteps;
+};
+
+template <int KIND>
+struct KindTraits {
+  static constexpr int a_mn = (KIND == GK_DW) ? 1 : 0;
+  static constexpr int b_mn = (KIND == GK_DH || KIND == GK_DX || KIND == GK_DW) ? 1 : 0;
+  // output columns covered by one tile
+  static constexpr int tile_cols = (KIND == GK_GATE_UP) ? BN / 2 : BN;
+};
+
+__device__ __forceinline__ int expert_of_row(const int* roff, int E, int m0) {
+  int lo = 0, hi = E - 1;  // last e with roff[e] <= m0
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (roff[mid] <= m0) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+template <int KIND>
+__device__ __forceinline__ int num_tiles(const Params& p, const Shared& sh) {
+  if (KIND == GK_DW) return p.E * p.m_tiles_dw * p.n_tiles;
+  const int mblocks = p.row_offsets ? sh.roff[p.E] / BM : (p.rows + BM - 1) / BM;
+  return mblocks * p.n_tiles;
+}
+
+template <int KIND>
+__device__ __forceinline__ Tile get_tile(const Params& p, const Shared& sh, int idx) {
+  Tile t;
+  if (KIND == GK_DW) {
+    const int per_e = p.m_tiles_dw * p.n_tiles;
+    t.e = idx / per_e;
+    const int r = idx - t.e * per_e;
+    t.m0 = (r / p.n_tiles) * BM;
+    t.n0 = (r % p.n_tiles) * BN;
+    int k0, k1;
+    if (p.row_offsets) { k0 = sh.roff[t.e]; k1 = sh.roff[t.e + 1]; }
+    else { k0 = 0; k1 = p.rows; }
+    t.kbeg = k0;
+    t.ksteps = (k1 - k0 + BK - 1) / BK;
+  } else {
+    const int mb = idx / p.n_tiles;
+    t.m0 = mb * BM;
+    t.n0 = (idx - mb * p.n_tiles) * KindTraits<KIND>::tile_cols;
+    t.e = p.row_offsets ? expert_of_row(sh.roff, p.E, t.m0) : 0;
+    t.kbeg = 0;
+    t.ksteps = (p.K + BK - 1) / BK;
+  }
+  return t;
+}
+
+__device__ __forceinline__ void fail(Shared& sh, int* status) {
+  set_status(status, MOE_ERR_TIMEOUT);
+  *(volatile int*)&sh.abort_flag = 1;
+}
+
+// ------------------------------------------------------------------ producer
+template <int KIND>
+__device__ __forceinline__ void issue_loads(const Tile& t, int kb, uint32_t sa, uint32_t sb,
+                                            uint32_t bar, const CUtensorMap* tmA,
+                                            const CUtensorMap* tmB) {
+  const int k0 = t.kbeg + kb * BK;
+  if (KIND == GK_GATE_UP) {
+    tma_load_2d(sa, tmA, bar, k0, t.m0);
+    tma_load_4d(sb, tmB, bar, k0, t.n0, 0, t.e);
+    tma_load_4d(sb + B_BYTES / 2, tmB, bar, k0, t.n0, 1, t.e);
+  } else if (KIND == GK_DOWN) {
+    tma_load_2d(sa, tmA, bar, k0, t.m0);
+    tma_load_3d(sb, tmB, bar, k0, t.n0, t.e);
+    tma_load_3d(sb + B_BYTES / 2, tmB, bar, k0, t.n0 + 128, t.e);
+  } else if (KIND == GK_DH || KIND == GK_DX) {
+    tma_load_2d(sa, tmA, bar, k0, t.m0);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) tma_load_3d(sb + i * 8192, tmB, bar, t.n0 + 64 * i, k0, t.e);
+  } else {  // GK_DW
+#pragma unroll
+    for (int i = 0; i < 2; ++i) tma_load_2d(sa + i * 8192, tmA, bar, t.m0 + 64 * i, k0);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) tma_load_2d(sb + i * 8192, tmB, bar, t.n0 + 64 * i, k0);
+  }
+}
+
+// ------------------------------------------------------------------ epilogue
+__device__ __forceinline__ float silu_f(float a) { return a / (1.f + __expf(-a)); }
+
+template <int KIND>
+__device__ __forceinline__ void epilogue_tile(const Params& p, const Tile& t, uint32_t tacc,
+                                              int row_in_tile) {
+  const int row = t.m0 + row_in_tile;
+  bool row_ok;
+  if (KIND == GK_DW) row_ok = row < p.Mdw;
+  else row_ok = p.row_offsets ? true : row < p.rows;
+  const bool zero_row = (KIND == GK_GATE_UP) && p.valid && row_ok && p.valid[row] == 0;
+  const bool no_acc = t.ksteps == 0;
+  uint32_t r0[32], r1[32];
+  if (KIND == GK_GATE_UP) {
+#pragma unroll 1
+    for (int cb = 0; cb < BN / 2 / 32; ++cb) {
+      __syncwarp();
+      tmem_ld32(tacc + cb * 32, r0);
+      tmem_ld32(tacc + BN / 2 + cb * 32, r1);
+      tmem_ld_wait();
+      const int col = t.n0 + cb * 32;
+      if (row_ok && col < p.H) {
+      uint4 hv[4], av[4], bv[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float hf[8], af[8], bf[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          float a = __uint_as_float(r0[q * 8 + u]);
+          float b = __uint_as_float(r1[q * 8 + u]);
+          if (zero_row) { a = 0.f; b = 0.f; }
+          af[u] = a; bf[u] = b;
+          hf[u] = silu_f(a) * b;
+        }
+        hv[q] = pack8(hf); av[q] = pack8(af); bv[q] = pack8(bf);
+      }
+      bf16* hp = p.out0 + (size_t)row * p.ld0 + col;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) st_v4(hp + q * 8, hv[q]);
+      if (p.out1) {
+        bf16* ap = p.out1 + (size_t)row * p.ld1 + col;
+        bf16* bp = ap + p.H;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) { st_v4(ap + q * 8, av[q]); st_v4(bp + q * 8, bv[q]); }
+      }
+      }
+    }
+  } else {
+#pragma unroll 1
+    for (int cb = 0; cb < BN / 32; ++cb) {
+      __syncwarp();
+      tmem_ld32(tacc + cb * 32, r0);
+      tmem_ld_wait();
+      const int col = t.n0 + cb * 32;
+      if (!(row_ok && col < p.N)) {
+        // nothing to store for this lane
+      } else if (KIND == GK_DH) {
+        // dH -> (da, db) with the saved pre-activations a, b
+        const bf16* ap = p.aux_in + (size_t)row * p.ld_aux + col;
+        const bf16* bp = ap + p.H;
+        bf16* dap = p.out0 + (size_t)row * p.ld0 + col;
+        bf16* dbp = dap + p.H;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float a8[8], b8[8], da[8], db[8];
+          unpack8(*reinterpret_cast<const uint4*>(ap + q * 8), a8);
+          unpack8(*reinterpret_cast<const uint4*>(bp + q * 8), b8);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const float dh = __uint_as_float(r0[q * 8 + u]);
+            const float a = a8[u], b = b8[u];
+            const float sg = 1.f / (1.f + __expf(-a));
+            const float sl = a * sg;
+            da[u] = dh * b * sg * (1.f + a * (1.f - sg));
+            db[u] = dh * sl;
+          }
+          st_v4(dap + q * 8, pack8(da));
+          st_v4(dbp + q * 8, pack8(db));
+        }
+      } else {
+        bf16* op;
+        if (KIND == GK_DW)
+          op = p.out0 + (size_t)t.e * p.Mdw * p.ld0 + (size_t)row * p.ld0 + col;
+        else
+          op = p.out0 + (size_t)row * p.ld0 + col;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float v[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) v[u] = no_acc ? 0.f : __uint_as_float(r0[q * 8 + u]);
+          st_v4(op + q * 8, pack8(v));
+        }
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ kernel
+template <int KIND>
+__global__ void __launch_bounds__(THREADS, 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                    const __grid_constant__ CUtensorMap tmB, const Params p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // stage buffers must start on a 1024-byte boundary (128-byte swizzle atoms)
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  unsigned char* gen_base = smem_raw + (base - raw);
+  Shared& sh = *reinterpret_cast<Shared*>(gen_base + (size_t)STAGES * STAGE_BYTES);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&sh.full[s]), 1);
+      mbar_init(smem_u32(&sh.empty[s]), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(smem_u32(&sh.tfull[a]), 1);
+      mbar_init(smem_u32(&sh.tempty[a]), 128);
+    }
+    mbar_init(smem_u32(&sh.drain), 1);
+    sh.abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (p.row_offsets)
+    for (int e = threadIdx.x; e <= p.E; e += blockDim.x) sh.roff[e] = p.row_offsets[e];
+  if (warp == 2) {
+    tmem_alloc(smem_u32(&sh.tmem_base), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh.tmem_base;
+  const int ntiles = num_tiles<KIND>(p, sh);
+  volatile int* abort_flag = &sh.abort_flag;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer
+    int stage = 0;
+    uint32_t phase = 0;
+    int pending_parity[STAGES];
+    for (int s = 0; s < STAGES; ++s) pending_parity[s] = -1;
+    bool ok = true;
+    for (int idx = blockIdx.x; idx < ntiles && ok; idx += gridDim.x) {
+      const Tile t = get_tile<KIND>(p, sh, idx);
+      for (int kb = 0; kb < t.ksteps; ++kb) {
+        if (!mbar_wait_bounded(smem_u32(&sh.empty[stage]), phase ^ 1u, abort_flag, WAIT_NS)) {
+          fail(sh, p.status);
+          ok = false;
+          break;
+        }
+        const uint32_t fb = smem_u32(&sh.full[stage]);
+        mbar_arrive_expect_tx(fb, STAGE_BYTES);
+        const uint32_t sa = base + stage * STAGE_BYTES;
+        issue_loads<KIND>(t, kb, sa, sa + A_BYTES, fb, &tmA, &tmB);
+        pending_parity[stage] = (int)phase;
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+    }
+    if (!ok) {
+      // let every copy already issued land before shared memory is released
+      for (int s = 0; s < STAGES; ++s)
+        if (pending_parity[s] >= 0) {
+          int dummy = 0;
+          mbar_wait_bounded(smem_u32(&sh.full[s]), (uint32_t)pending_parity[s], &dummy,
+                            DRAIN_NS);
+        }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer
+    constexpr uint32_t idesc =
+        umma_idesc_bf16(BM, BN, KindTraits<KIND>::a_mn, KindTraits<KIND>::b_mn);
+    constexpr uint32_t a_step = KindTraits<KIND>::a_mn ? 16 * 128 : UK * 2;
+    constexpr uint32_t b_step = KindTraits<KIND>::b_mn ? 16 * 128 : UK * 2;
+    constexpr uint32_t a_lbo = KindTraits<KIND>::a_mn ? 8192 : 16;
+    constexpr uint32_t b_lbo = KindTraits<KIND>::b_mn ? 8192 : 16;
+    int stage = 0;
+    uint32_t phase = 0;
+    int it = 0;
+    bool ok = true;
+    for (int idx = blockIdx.x; idx < ntiles && ok; idx += gridDim.x, ++it) {
+      const Tile t = get_tile<KIND>(p, sh, idx);
+      const int acc = it & 1;
+      const uint32_t acc_phase = (it >> 1) & 1;
+      if (!mbar_wait_bounded(smem_u32(&sh.tempty[acc]), acc_phase ^ 1u, abort_flag, WAIT_NS)) {
+        fail(sh, p.status);
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem + acc * BN;
+      for (int kb = 0; kb < t.ksteps; ++kb) {
+        if (!mbar_wait_bounded(smem_u32(&sh.full[stage]), phase, abort_flag, WAIT_NS)) {
+          fail(sh, p.status);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sa = base + stage * STAGE_BYTES;
+        const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BK / UK; ++kk) {
+          const uint64_t ad = umma_desc_sw128(sa + kk * a_step, a_lbo, 1024);
+          const uint64_t bd = umma_desc_sw128(sb + kk * b_step, b_lbo, 1024);
+          umma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+        }
+        umma_commit(smem_u32(&sh.empty[stage]));
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) break;
+      umma_commit(smem_u32(&sh.tfull[acc]));
+    }
+    // all issued MMAs complete before TMEM can be released
+    umma_commit(smem_u32(&sh.drain));
+    int dummy = 0;
+    mbar_wait_bounded(smem_u32(&sh.drain), 0, &dummy, DRAIN_NS);
+  } else if (warp >= EPI_WARP0) {
+    // ---------------- epilogue warps: TMEM lanes 32*(warp%4) .. +31
+    const int q = warp - EPI_WARP0;
+    const int row_in_tile = q * 32 + lane;
+    int it = 0;
+    for (int idx = blockIdx.x; idx < ntiles; idx += gridDim.x, ++it) {
+      const Tile t = get_tile<KIND>(p, sh, idx);
+      const int acc = it & 1;
+      const uint32_t acc_phase = (it >> 1) & 1;
+      if (!mbar_wait_bounded(smem_u32(&sh.tfull[acc]), acc_phase, abort_flag, WAIT_NS)) {
+        if (lane == 0) fail(sh, p.status);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tacc = tmem + ((uint32_t)(q * 32) << 16) + acc * BN;
+      epilogue_tile<KIND>(p, t, tacc, row_in_tile);
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sh.tempty[acc]));
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// bf16 tensor map, 128-byte swizzle, zero fill out of bounds.
+// dims/strides: innermost first; strides in bytes for dims 1..rank-1.
+bool make_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims,
+              const uint64_t* strides, const uint32_t* box) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t gd[5], gs[4];
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < rank; ++i) { gd[i] = dims[i]; bx[i] = box[i]; es[i] = 1; }
+  for (int i = 0; i < rank - 1; ++i) gs[i] = strides[i];
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(ptr),
+                  gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int KIND>
+cudaError_t launch_kind(const CUtensorMap& a, const CUtensorMap& b, const Params& p,
+                        int grid, cudaStream_t s) {
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(grouped_gemm_kernel<KIND>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)SMEM_BYTES);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  grouped_gemm_kernel<KIND><<<grid, THREADS, SMEM_BYTES, s>>>(a, b, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmCall& g, cudaStream_t s) {
+  static_assert(sizeof(Shared) + 1024 <= 2048 + 1024, "shared bookkeeping too large");
+  DeviceInfo di;
+  if (device_info(&di) != MOE_OK) return cudaErrorUnknown;
+  CUtensorMap ta, tb;
+  Params p{};
+  p.row_offsets = g.row_offsets;
+  p.E = g.E;
+  p.rows = g.rows;
+  p.K = g.K;
+  p.N = g.N;
+  p.H = g.H;
+  p.Mdw = g.Mdw;
+  p.out0 = static_cast<bf16*>(g.out0);
+  p.ld0 = g.ld0;
+  p.out1 = static_cast<bf16*>(g.out1);
+  p.ld1 = g.ld1;
+  p.aux_in = static_cast<const bf16*>(g.aux_in);
+  p.ld_aux = g.ld_aux;
+  p.valid = g.valid;
+  p.status = g.status;
+  const uint64_t rows = (uint64_t)g.rows;
+  bool ok = true;
+  switch (g.kind) {
+    case GK_GATE_UP: {
+      // A: [rows][K] ; B: W_gu [E][2][H][K] -> dims {K, H, 2, E}
+      uint64_t da[2] = {(uint64_t)g.K, rows}, sa[1] = {(uint64_t)g.lda * 2};
+      uint32_t ba[2] = {64, 128};
+      uint64_t db[4] = {(uint64_t)g.K, (uint64_t)g.H, 2, (uint64_t)g.E};
+      uint64_t sb[3] = {(uint64_t)g.K * 2, (uint64_t)g.H * g.K * 2, (uint64_t)2 * g.H * g.K * 2};
+      uint32_t bb[4] = {64, 128, 1, 1};
+      ok = make_map(&ta, g.A, 2, da, sa, ba) && make_map(&tb, g.B, 4, db, sb, bb);
+      p.n_tiles = (g.H + BN / 2 - 1) / (BN / 2);
+      break;
+    }
+    case GK_DOWN: {
+      // A: [rows][K=H] ; B: W_down [E][N=d][K=H] -> dims {K, N, E}
+      uint64_t da[2] = {(uint64_t)g.K, rows}, sa[1] = {(uint64_t)g.lda * 2};
+      uint32_t ba[2] = {64, 128};
+      uint64_t db[3] = {(uint64_t)g.K, (uint64_t)g.N, (uint64_t)g.E};
+      uint64_t sb[2] = {(uint64_t)g.K * 2, (uint64_t)g.N * g.K * 2};
+      uint32_t bb[3] = {64, 128, 1};
+      ok = make_map(&ta, g.A, 2, da, sa, ba) && make_map(&tb, g.B, 3, db, sb, bb);
+      p.n_tiles = (g.N + BN - 1) / BN;
+      break;
+    }
+    case GK_DH:
+    case GK_DX: {
+      // A: [rows][K] ; B: [E][K][N] (N contiguous) -> dims {N, K, E}
+      uint64_t da[2] = {(uint64_t)g.K, rows}, sa[1] = {(uint64_t)g.lda * 2};
+      uint32_t ba[2] = {64, 128};
+      uint64_t db[3] = {(uint64_t)g.N, (uint64_t)g.K, (uint64_t)g.E};
+      uint64_t sb[2] = {(uint64_t)g.N * 2, (uint64_t)g.K * g.N * 2};
+      uint32_t bb[3] = {64, 64, 1};
+      ok = make_map(&ta, g.A, 2, da, sa, ba) && make_map(&tb, g.B, 3, db, sb, bb);
+      p.n_tiles = (g.N + BN - 1) / BN;
+      break;
+    }
+    case GK_DW: {
+      // A: [rows][Mdw] (M contiguous) ; B: [rows][N] (N contiguous)
+      uint64_t da[2] = {(uint64_t)g.Mdw, rows}, sa[1] = {(uint64_t)g.lda * 2};
+      uint32_t ba[2] = {64, 64};
+      uint64_t db[2] = {(uint64_t)g.N, rows}, sb[1] = {(uint64_t)g.N * 2};
+      uint32_t bb[2] = {64, 64};
+      ok = make_map(&ta, g.A, 2, da, sa, ba) && make_map(&tb, g.B, 2, db, sb, bb);
+      p.n_tiles = (g.N + BN - 1) / BN;
+      p.m_tiles_dw = (g.Mdw + BM - 1) / BM;
+      break;
+    }
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  const int grid = di.num_sms;
+  switch (g.kind) {
+    case GK_GATE_UP: return launch_kind<GK_GATE_UP>(ta, tb, p, grid, s);
+    case GK_DOWN: return launch_kind<GK_DOWN>(ta, tb, p, grid, s);
+    case GK_DH: return launch_kind<GK_DH>(ta, tb, p, grid, s);
+    case GK_DX: return launch_kind<GK_DX>(ta, tb, p, grid, s);
+    case GK_DW: return launch_kind<GK_DW>(ta, tb, p, grid, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace moe

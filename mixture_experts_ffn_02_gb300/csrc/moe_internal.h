@@ -1,0 +1,118 @@
+// Host-side declarations shared by the translation units of the library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+constexpr int kRowAlign = MOE_ROW_ALIGN;  // expert segments start at multiples
+constexpr int kPermChunk = 128;           // tokens per block in the dispatch kernels
+constexpr int kMaxK = 32;                 // experts per token supported
+
+// Per-device facts, cached after the first query.
+struct DeviceInfo {
+  int device = -1;
+  int num_sms = 0;
+  int cc_major = 0;
+  int cc_minor = 0;
+  size_t max_smem_optin = 0;
+};
+int device_info(DeviceInfo* out);
+
+// ---- workspace layout (byte offsets into the caller's workspace) -----------
+struct WsLayout {
+  size_t status;        // int32 status word
+  size_t route_done;    // int32 ticket counter of the route kernel
+  size_t route_cnt;     // [route_blocks][E] int32
+  size_t route_psum;    // [route_blocks][E] fp32
+  size_t route_treal;   // [route_blocks] int32
+  size_t perm_hist;     // [perm_blocks][E] int32
+  size_t perm_base;     // [perm_blocks][E] int32
+  // backward scratch
+  size_t d_out;         // [R_cap][d] bf16
+  size_t d_gu;          // [R_cap][2H] bf16
+  size_t dx_perm;       // [R_cap][d] bf16
+  size_t ds_gu;         // [T][2Hs] bf16
+  size_t dxs;           // [T][d] bf16
+  size_t dxr;           // [T][d] fp32 (router input gradient, large E)
+  size_t dwr_part;      // [splits][d][E] fp32
+  size_t total;
+  int route_blocks;
+  int perm_blocks;
+  int dwr_splits;
+  int64_t R_cap;
+};
+int ws_layout(const moe_config* c, int training, WsLayout* out);
+
+// ---- launchers of the memory-bound / SIMT kernels (moe_dispatch.cu) --------
+cudaError_t launch_router_logits(const moe_config& c, const void* x, const float* Wr,
+                                 float* L, cudaStream_t s);
+cudaError_t launch_route(const moe_config& c, const float* L, const float* bias,
+                         const uint8_t* valid, int32_t* topk, float* gates, int32_t* counts,
+                         float* f, float* p, float* aux, char* ws, const WsLayout& w,
+                         cudaStream_t s);
+cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* topk,
+                           int32_t* counts, int32_t* offsets, int32_t* row_offsets,
+                           int32_t* perm, int32_t* inv, void* x_perm, char* ws,
+                           const WsLayout& w, cudaStream_t s);
+cudaError_t launch_combine(const moe_config& c, const void* out_perm, const int32_t* inv,
+                           const float* gates, const uint8_t* valid, const void* s_out,
+                           void* y, cudaStream_t s);
+cudaError_t launch_combine_bwd(const moe_config& c, const void* dY, const void* out_perm,
+                               const int32_t* inv, const int32_t* topk, const float* gates,
+                               const float* L, const float* f, const int32_t* counts,
+                               const uint8_t* valid, const int32_t* row_offsets,
+                               void* d_out, float* d_logits, int* status, cudaStream_t s);
+cudaError_t launch_dx_gather(const moe_config& c, const void* dx_perm, const int32_t* inv,
+                             const void* dxs, const float* dxr, const float* d_logits,
+                             const float* Wr, const uint8_t* valid, void* dx, cudaStream_t s);
+// Router GEMMs on the CUDA cores (fp32 FMA).
+cudaError_t launch_router_dx(const moe_config& c, const float* d_logits, const float* Wr,
+                             float* dxr, cudaStream_t s);
+cudaError_t launch_router_dw(const moe_config& c, const void* x, const float* d_logits,
+                             float* dWr, float* part, int splits, cudaStream_t s);
+bool router_small_path(const moe_config& c);
+
+// ---- tcgen05 grouped GEMMs (moe_gemm.cu) -----------------------------------
+// Which product a launch computes (operand majorness and epilogue).
+enum GemmKind {
+  GK_GATE_UP = 0,   // h = silu(A Wg^T) * (A Wu^T)          A K-major, B K-major
+  GK_DOWN = 1,      // out = A Wd^T                          A K-major, B K-major
+  GK_DH = 2,        // d_gu = swiglu_bwd(A Wd, ab)           A K-major, B MN-major
+  GK_DX = 3,        // dx = A Wgu                            A K-major, B MN-major
+  GK_DW = 4         // dW = A^T B over a row segment         A MN-major, B MN-major
+};
+
+struct GemmCall {
+  GemmKind kind;
+  // Row grouping: routed (row_offsets != NULL, E groups) or dense (rows).
+  const int32_t* row_offsets;  // [E+1] padded, device
+  int E;                       // groups (1 for dense)
+  int rows;                    // dense: number of rows; routed: R_cap
+  // Operand A (activations)
+  const void* A;               // [rows][lda] bf16
+  int lda;                     // elements
+  // Operand B (weights) or second activation (GK_DW)
+  const void* B;
+  // Problem dims
+  int K;                       // reduction length (not for GK_DW)
+  int N;                       // output columns (H for gate/up, d for down, ...)
+  int H;                       // gate/up split (GK_GATE_UP: rows [0,H) gate; GK_DH)
+  int Mdw;                     // GK_DW: rows of each dW matrix
+  // Outputs
+  void* out0;                  // main output
+  int ld0;
+  void* out1;                  // GK_GATE_UP: ab save (or NULL)
+  int ld1;
+  const void* aux_in;          // GK_DH: ab (a|b) saved by the forward
+  int ld_aux;
+  const uint8_t* valid;        // GK_GATE_UP dense: zero PAD rows
+  int* status;
+};
+cudaError_t launch_gemm(const GemmCall& g, cudaStream_t s);
+
+}  // namespace moe

@@ -124,10 +124,18 @@ def route(logits, k, bias=None, valid=None, norm_topk=True):
             else L + b.astype(f64)
     idx = select_topk(key, k)
     s = softmax(L.astype(f64))
+    real = np.ones(T, dtype=bool) if valid is None else (np.asarray(_np(valid)) != 0)
+    return route_stats(s, idx, real, norm_topk)
+
+
+def route_stats(s, idx, real, norm_topk=True):
+    """Gates, counts, f, p and aux for a given selection ``idx`` [T][k] of
+    the softmax ``s`` [T][E] (PAD rows: real == False)."""
+    T, E = s.shape
+    k = idx.shape[1]
+    idx = np.where(real[:, None], idx, 0)
     sel = np.take_along_axis(s, idx, axis=1)
     gates = sel / sel.sum(axis=1, keepdims=True) if norm_topk else sel.copy()
-
-    real = np.ones(T, dtype=bool) if valid is None else (np.asarray(_np(valid)) != 0)
     idx = np.where(real[:, None], idx, -1).astype(np.int64)
     gates = np.where(real[:, None], gates, 0.0)
     T_real = int(real.sum())

@@ -1,0 +1,94 @@
+"""CPU checks of the C ABI: the library builds for sm_103a, loads, exports
+every function `include/moe.h` declares, and its host-side queries (shape
+rules, row capacity, workspace size) behave as documented.  No kernel runs."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from mixture_experts_ffn_02_gb300 import binding, build, synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def clib():
+    build.build()
+    return binding.load()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:int|const char\*)\s+(moe_\w+)\s*\(", src, re.M)))
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    for n in ["moe_route", "moe_permute", "moe_expert_gate_up", "moe_expert_down",
+              "moe_shared_ffn", "moe_combine", "moe_forward", "moe_backward",
+              "moe_router_logits", "moe_workspace_bytes", "moe_get_status"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(clib):
+    for n in declared_functions():
+        assert hasattr(clib, n), n
+    assert set(declared_functions()) <= set(binding.SIGNATURES)
+
+
+def test_abi_version_and_messages(clib):
+    assert clib.moe_abi_version() == 1
+    for code in range(10):
+        assert clib.moe_strerror(code)
+    assert b"unknown" in clib.moe_strerror(99)
+
+
+def cfg(**kw):
+    base = dict(T=256, d=64, E=4, k=2, H=128, n_shared=1, H_shared=128, norm_topk=1,
+                aux_coef=0.01)
+    base.update(kw)
+    return binding.MoEConfig(**base)
+
+
+@pytest.mark.parametrize("bad", [dict(T=0), dict(d=100), dict(H=96), dict(k=0), dict(k=5),
+                                 dict(E=257, k=2), dict(E=64, k=33), dict(n_shared=-1),
+                                 dict(H_shared=100), dict(T=2 ** 30, k=8)])
+def test_shape_rules(clib, bad):
+    assert clib.moe_check_config(ctypes.byref(cfg(**bad))) == 2
+
+
+def test_valid_configs(clib):
+    for s in synth.SHAPES.values():
+        assert clib.moe_check_config(ctypes.byref(binding.config(s))) == 0
+    assert clib.moe_check_config(None) == 1
+
+
+def test_row_capacity_bounds_every_padded_layout(clib):
+    c = cfg(T=1000, E=8, k=2)
+    r = ctypes.c_int64()
+    assert clib.moe_row_capacity(ctypes.byref(c), ctypes.byref(r)) == 0
+    assert r.value == (1000 * 2 + 127 * 8) // 128 * 128
+    # worst case: every expert's count is 1 more than a multiple of 128
+    counts = [129] * 7 + [2000 - 129 * 7]
+    assert sum((n + 127) // 128 * 128 for n in counts) <= r.value
+
+
+def test_workspace_grows_with_training(clib):
+    c = binding.config(synth.shape(5))
+    a, b = ctypes.c_size_t(), ctypes.c_size_t()
+    assert clib.moe_workspace_bytes(ctypes.byref(c), 0, ctypes.byref(a)) == 0
+    assert clib.moe_workspace_bytes(ctypes.byref(c), 1, ctypes.byref(b)) == 0
+    assert 0 < a.value < b.value
+
+
+def test_entry_points_reject_bad_arguments_without_touching_the_gpu(clib):
+    c = cfg()
+    t = binding.MoETensors()
+    # NULL workspace is reported before any device work
+    for name in ["moe_forward", "moe_route", "moe_permute", "moe_combine"]:
+        rc = getattr(clib, name)(ctypes.byref(c), ctypes.byref(t), None, 0, None)
+        assert rc in (4, 5, 6), (name, rc)   # workspace, or no CUDA device here
+    bad = cfg(d=65)
+    assert clib.moe_forward(ctypes.byref(bad), ctypes.byref(t), None, 0, None) == 2
