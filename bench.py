@@ -39,6 +39,16 @@ WORKLOAD_NAMES = {
 }
 
 
+def workload_shape(args):
+    from mixture_experts_ffn_02_gb300 import synth
+    s = synth.shape(args.config)
+    if args.tokens:
+        T = args.tokens
+        T_real = None if s.T_real is None else round(s.T_real * T / s.T)
+        s = synth.scaled(s, T=T, T_real=T_real)
+    return s
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -128,7 +138,7 @@ def run_ours(args):
     torch.cuda.set_device(local)
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    s = synth.shape(args.config)
+    s = workload_shape(args)
     training = not args.fwd_only
     inp = synth.make_inputs(s, seed=rank, with_grad=True)
     lay = binding.Layer.create(s, training=training, device=f"cuda:{local}")
@@ -244,7 +254,7 @@ def run_ours(args):
         "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights)",
         "config": {"workload": WORKLOAD_NAMES[args.config] + (" fwd" if args.fwd_only
                                                               else " fwd+bwd"),
-                   "config_id": args.config, "T": s.T, "d": s.d, "E": s.E, "k": s.k,
+                   "config_id": args.config, "T": s.T, "T_real": s.T_real, "d": s.d, "E": s.E, "k": s.k,
                    "H": s.H, "n_shared": s.n_shared, "H_shared": s.H_shared,
                    "parallelism": f"replicas x{world}",
                    "l2": "256 MB buffer written before each step, outside its events"},
@@ -365,8 +375,7 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    from mixture_experts_ffn_02_gb300 import synth
-    s = synth.shape(args.config)
+    s = workload_shape(args)
     training = not args.fwd_only
     n = 256 if s.d * s.H <= 4e6 else 64
     for _ in range(args.warmup):
@@ -398,6 +407,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="smaller token count of the same layer (profiling cases)")
     ap.add_argument("--fwd-only", action="store_true")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")

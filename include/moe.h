@@ -119,10 +119,11 @@ typedef struct moe_tensors {
   void* ab;             /* [R_cap][2H] bf16 pre-activations a|b (saved for
                            backward; NULL skips the save)                         */
   void* h;              /* [R_cap][H] bf16 silu(a) * b                            */
-  void* out_perm;       /* [R_cap][d] bf16 expert outputs per row                 */
+  float* out_perm;      /* [R_cap][d] fp32 expert outputs per row (fp32 so the
+                           combine sums unrounded terms)                          */
   void* s_ab;           /* [T][2Hs] bf16 shared pre-activations (or NULL)         */
   void* s_h;            /* [T][Hs] bf16 shared hidden (0 on PAD rows)             */
-  void* s_out;          /* [T][d] bf16 shared expert output (0 on PAD rows)       */
+  float* s_out;         /* [T][d] fp32 shared expert output (0 on PAD rows)       */
   /* output */
   void* y;              /* [T][d] bf16 layer output                               */
 } moe_tensors;

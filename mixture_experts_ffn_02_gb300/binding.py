@@ -159,10 +159,10 @@ class Layer:
                  counts=z(E, dt=i32), f=z(E, dt=f32), p=z(E, dt=f32), aux=z(4, dt=f32),
                  offsets=z(E + 1, dt=i32), row_offsets=z(E + 1, dt=i32), perm=z(R, dt=i32),
                  inv=z(T * k, dt=i32), x_perm=z(R, d, dt=bf), h=z(R, H, dt=bf),
-                 out_perm=z(R, d, dt=bf), y=z(T, d, dt=bf),
+                 out_perm=z(R, d, dt=f32), y=z(T, d, dt=bf),
                  ab=z(R, 2 * H, dt=bf) if training else None,
                  s_h=z(T, Hs, dt=bf) if Hs else None,
-                 s_out=z(T, d, dt=bf) if Hs else None,
+                 s_out=z(T, d, dt=f32) if Hs else None,
                  s_ab=z(T, 2 * Hs, dt=bf) if (Hs and training) else None)
         g = {}
         if training:

@@ -81,10 +81,10 @@ int ws_layout(const moe_config* c, int training, WsLayout* w) {
     const size_t R = (size_t)w->R_cap;
     w->d_out = take(R * c->d * 2);
     w->d_gu = take(R * 2 * (size_t)c->H * 2);
-    w->dx_perm = take(R * c->d * 2);
+    w->dx_perm = take(R * c->d * 4);
     if (Hs > 0) {
       w->ds_gu = take((size_t)c->T * 2 * Hs * 2);
-      w->dxs = take((size_t)c->T * c->d * 2);
+      w->dxs = take((size_t)c->T * c->d * 4);
     }
     if (!router_small_path(*c)) w->dxr = take((size_t)c->T * c->d * 4);
     int splits = c->T / 1024;
@@ -216,6 +216,7 @@ int do_down(const moe_config* c, const moe_tensors* t, Call& k) {
   g.N = c->d;
   g.out0 = t->out_perm;
   g.ld0 = c->d;
+  g.out_f32 = 1;
   g.status = k.status;
   MOE_CUDA(launch_gemm(g, k.s));
   return MOE_OK;
@@ -256,6 +257,7 @@ int do_shared(const moe_config* c, const moe_tensors* t, Call& k) {
   d.N = c->d;
   d.out0 = t->s_out;
   d.ld0 = c->d;
+  d.out_f32 = 1;
   d.status = k.status;
   MOE_CUDA(launch_gemm(d, k.s));
   return MOE_OK;
@@ -264,7 +266,7 @@ int do_shared(const moe_config* c, const moe_tensors* t, Call& k) {
 int do_combine(const moe_config* c, const moe_tensors* t, Call& k) {
   MOE_NEED(t->out_perm); MOE_NEED(t->inv); MOE_NEED(t->gates); MOE_OPT(t->valid);
   MOE_NEED(t->y);
-  const void* s_out = nullptr;
+  const float* s_out = nullptr;
   if (hs_total(*c) > 0) {
     MOE_NEED(t->s_out);
     s_out = t->s_out;
@@ -289,7 +291,7 @@ int do_backward(const moe_config* c, const moe_tensors* t, const moe_grads* g, C
   const WsLayout& w = k.w;
   void* d_out = k.ws + w.d_out;
   void* d_gu = k.ws + w.d_gu;
-  void* dx_perm = k.ws + w.dx_perm;
+  float* dx_perm = reinterpret_cast<float*>(k.ws + w.dx_perm);
   const int R = (int)w.R_cap;
 
   // (i) + (vii): d_out, dg and the router-logit gradient
@@ -307,7 +309,7 @@ int do_backward(const moe_config* c, const moe_tensors* t, const moe_grads* g, C
   GemmCall gx{};
   gx.kind = GK_DX; gx.row_offsets = t->row_offsets; gx.E = c->E; gx.rows = R;
   gx.A = d_gu; gx.lda = 2 * c->H; gx.B = t->W_gu; gx.K = 2 * c->H; gx.N = c->d;
-  gx.out0 = dx_perm; gx.ld0 = c->d; gx.status = k.status;
+  gx.out0 = dx_perm; gx.ld0 = c->d; gx.out_f32 = 1; gx.status = k.status;
   MOE_CUDA(launch_gemm(gx, k.s));
   // (iv) dW_down[e] = d_out_e^T h_e ; dW_gu[e] = d_gu_e^T x_perm_e
   GemmCall wd{};
@@ -321,10 +323,10 @@ int do_backward(const moe_config* c, const moe_tensors* t, const moe_grads* g, C
   wg.out0 = g->dW_gu; wg.ld0 = c->d; wg.status = k.status;
   MOE_CUDA(launch_gemm(wg, k.s));
   // (v) shared expert
-  void* dxs = nullptr;
+  float* dxs = nullptr;
   if (Hs > 0) {
     void* ds_gu = k.ws + w.ds_gu;
-    dxs = k.ws + w.dxs;
+    dxs = reinterpret_cast<float*>(k.ws + w.dxs);
     GemmCall sh{};
     sh.kind = GK_DH; sh.row_offsets = nullptr; sh.E = 1; sh.rows = c->T;
     sh.A = g->dY; sh.lda = c->d; sh.B = t->Ws_down; sh.K = c->d; sh.N = Hs; sh.H = Hs;
@@ -334,7 +336,7 @@ int do_backward(const moe_config* c, const moe_tensors* t, const moe_grads* g, C
     GemmCall sx{};
     sx.kind = GK_DX; sx.row_offsets = nullptr; sx.E = 1; sx.rows = c->T;
     sx.A = ds_gu; sx.lda = 2 * Hs; sx.B = t->Ws_gu; sx.K = 2 * Hs; sx.N = c->d;
-    sx.out0 = dxs; sx.ld0 = c->d; sx.status = k.status;
+    sx.out0 = dxs; sx.ld0 = c->d; sx.out_f32 = 1; sx.status = k.status;
     MOE_CUDA(launch_gemm(sx, k.s));
     GemmCall sw{};
     sw.kind = GK_DW; sw.row_offsets = nullptr; sw.E = 1; sw.rows = c->T;

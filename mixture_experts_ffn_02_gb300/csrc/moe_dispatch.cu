@@ -23,6 +23,15 @@ __device__ __forceinline__ bool row_real(const uint8_t* valid, int t) {
   return valid == nullptr || valid[t] != 0;
 }
 
+// 8 consecutive fp32 values (32-byte aligned) through the non-coherent path.
+__device__ __forceinline__ void ld8f(const float* p, float* v) {
+  uint4 a = ld_nc_v4(p), b = ld_nc_v4(p + 4);
+  v[0] = __uint_as_float(a.x); v[1] = __uint_as_float(a.y);
+  v[2] = __uint_as_float(a.z); v[3] = __uint_as_float(a.w);
+  v[4] = __uint_as_float(b.x); v[5] = __uint_as_float(b.y);
+  v[6] = __uint_as_float(b.z); v[7] = __uint_as_float(b.w);
+}
+
 // --------------------------------------------------------------------------
 // a0 (small E): logits[t][e] = sum_c x[t][c] * Wr[c][e], one warp per token.
 // Wr is staged in shared memory as [c][E] with 4 floats of padding after
@@ -157,12 +166,6 @@ __global__ void sum_splits_kernel(const float* __restrict__ part, float* __restr
 // a1: routing.  A group of G lanes (a power of two <= 32) handles one token;
 // lane l of the group holds experts l, l+G, ..., (V per lane).
 // --------------------------------------------------------------------------
-struct Cand {
-  float key;
-  int idx;   // expert index, INT_MAX = none
-  float s;   // its softmax probability
-};
-
 // True if candidate (ka, ia) ranks before (kb, ib): larger key first, equal
 // keys lower index first; "none" ranks last.
 __device__ __forceinline__ bool ranks_before(float ka, int ia, float kb, int ib) {
@@ -470,9 +473,9 @@ perm_scatter_kernel(const bf16* __restrict__ x, const int32_t* __restrict__ topk
 // a6: y[t] = sum_j g[t][j] out_perm[inv[t][j]] (+ s_out[t]); one warp/token.
 // --------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads)
-combine_kernel(const bf16* __restrict__ out_perm, const int32_t* __restrict__ inv,
+combine_kernel(const float* __restrict__ out_perm, const int32_t* __restrict__ inv,
                const float* __restrict__ gates, const uint8_t* __restrict__ valid,
-               const bf16* __restrict__ s_out, bf16* __restrict__ y, int T, int d, int k) {
+               const float* __restrict__ s_out, bf16* __restrict__ y, int T, int d, int k) {
   const int lane = threadIdx.x & 31;
   const int wpb = blockDim.x >> 5;
   for (int t = blockIdx.x * wpb + (threadIdx.x >> 5); t < T; t += gridDim.x * wpb) {
@@ -492,13 +495,13 @@ combine_kernel(const bf16* __restrict__ out_perm, const int32_t* __restrict__ in
           const float g = __shfl_sync(0xffffffffu, my_g, j);
           if (r < 0) continue;
           float v[8];
-          unpack8(ld_nc_v4(out_perm + (size_t)r * d + c0), v);
+          ld8f(out_perm + (size_t)r * d + c0, v);
 #pragma unroll
           for (int u = 0; u < 8; ++u) acc[u] = fmaf(g, v[u], acc[u]);
         }
         if (s_out) {
           float v[8];
-          unpack8(ld_nc_v4(s_out + (size_t)t * d + c0), v);
+          ld8f(s_out + (size_t)t * d + c0, v);
 #pragma unroll
           for (int u = 0; u < 8; ++u) acc[u] += v[u];
         }
@@ -516,7 +519,7 @@ combine_kernel(const bf16* __restrict__ out_perm, const int32_t* __restrict__ in
 // --------------------------------------------------------------------------
 template <int V>
 __global__ void __launch_bounds__(kThreads)
-combine_bwd_kernel(const bf16* __restrict__ dY, const bf16* __restrict__ out_perm,
+combine_bwd_kernel(const bf16* __restrict__ dY, const float* __restrict__ out_perm,
                    const int32_t* __restrict__ inv, const int32_t* __restrict__ topk,
                    const float* __restrict__ gates, const float* __restrict__ L,
                    const float* __restrict__ f, const int32_t* __restrict__ counts,
@@ -560,7 +563,7 @@ combine_bwd_kernel(const bf16* __restrict__ dY, const bf16* __restrict__ out_per
         for (int c0 = lane * 8; c0 < d; c0 += 256) {
           float dy[8], o[8], go[8];
           unpack8(ld_nc_v4(dyr + c0), dy);
-          unpack8(ld_nc_v4(out_perm + (size_t)r * d + c0), o);
+          ld8f(out_perm + (size_t)r * d + c0, o);
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
             dot = fmaf(dy[u], o[u], dot);
@@ -639,8 +642,8 @@ combine_bwd_kernel(const bf16* __restrict__ dY, const bf16* __restrict__ out_per
 // --------------------------------------------------------------------------
 template <int ES>
 __global__ void __launch_bounds__(kThreads)
-dx_gather_kernel(const bf16* __restrict__ dx_perm, const int32_t* __restrict__ inv,
-                 const bf16* __restrict__ dxs, const float* __restrict__ dxr,
+dx_gather_kernel(const float* __restrict__ dx_perm, const int32_t* __restrict__ inv,
+                 const float* __restrict__ dxs, const float* __restrict__ dxr,
                  const float* __restrict__ dL, const float* __restrict__ Wr,
                  const uint8_t* __restrict__ valid, bf16* __restrict__ dx, int T, int d,
                  int k) {
@@ -670,13 +673,13 @@ dx_gather_kernel(const bf16* __restrict__ dx_perm, const int32_t* __restrict__ i
           const int r = __shfl_sync(0xffffffffu, my_r, j);
           if (r < 0) continue;
           float v[8];
-          unpack8(ld_nc_v4(dx_perm + (size_t)r * d + c0), v);
+          ld8f(dx_perm + (size_t)r * d + c0, v);
 #pragma unroll
           for (int u = 0; u < 8; ++u) acc[u] += v[u];
         }
         if (dxs) {
           float v[8];
-          unpack8(ld_nc_v4(dxs + (size_t)t * d + c0), v);
+          ld8f(dxs + (size_t)t * d + c0, v);
 #pragma unroll
           for (int u = 0; u < 8; ++u) acc[u] += v[u];
         }
@@ -826,19 +829,18 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* to
   return cudaGetLastError();
 }
 
-cudaError_t launch_combine(const moe_config& c, const void* out_perm, const int32_t* inv,
-                           const float* gates, const uint8_t* valid, const void* s_out,
+cudaError_t launch_combine(const moe_config& c, const float* out_perm, const int32_t* inv,
+                           const float* gates, const uint8_t* valid, const float* s_out,
                            void* y, cudaStream_t s) {
   DeviceInfo di;
   if (device_info(&di) != MOE_OK) return cudaErrorUnknown;
   const int grid = grid_for(kThreads / 32, c.T, di.num_sms * 8);
-  combine_kernel<<<grid, kThreads, 0, s>>>(static_cast<const bf16*>(out_perm), inv, gates, valid,
-                                           static_cast<const bf16*>(s_out),
+  combine_kernel<<<grid, kThreads, 0, s>>>(out_perm, inv, gates, valid, s_out,
                                            static_cast<bf16*>(y), c.T, c.d, c.k);
   return cudaGetLastError();
 }
 
-cudaError_t launch_combine_bwd(const moe_config& c, const void* dY, const void* out_perm,
+cudaError_t launch_combine_bwd(const moe_config& c, const void* dY, const float* out_perm,
                                const int32_t* inv, const int32_t* topk, const float* gates,
                                const float* L, const float* f, const int32_t* counts,
                                const uint8_t* valid, const int32_t* row_offsets, void* d_out,
@@ -850,7 +852,7 @@ cudaError_t launch_combine_bwd(const moe_config& c, const void* dY, const void* 
   const int V = (c.E + 31) / 32;
 #define MOE_CBWD(VV)                                                                          \
   combine_bwd_kernel<VV><<<grid, kThreads, 0, s>>>(                                           \
-      static_cast<const bf16*>(dY), static_cast<const bf16*>(out_perm), inv, topk, gates, L, f, \
+      static_cast<const bf16*>(dY), out_perm, inv, topk, gates, L, f,                          \
       counts, valid, row_offsets, static_cast<bf16*>(d_out), d_logits, c.T, c.d, c.E, c.k,     \
       c.norm_topk, c.aux_coef)
   if (V <= 1) { MOE_CBWD(1); }
@@ -861,14 +863,14 @@ cudaError_t launch_combine_bwd(const moe_config& c, const void* dY, const void* 
   return cudaGetLastError();
 }
 
-cudaError_t launch_dx_gather(const moe_config& c, const void* dx_perm, const int32_t* inv,
-                             const void* dxs, const float* dxr, const float* d_logits,
+cudaError_t launch_dx_gather(const moe_config& c, const float* dx_perm, const int32_t* inv,
+                             const float* dxs, const float* dxr, const float* d_logits,
                              const float* Wr, const uint8_t* valid, void* dx, cudaStream_t s) {
   DeviceInfo di;
   if (device_info(&di) != MOE_OK) return cudaErrorUnknown;
   const int grid = grid_for(kThreads / 32, c.T, di.num_sms * 4);
-  const bf16* dp = static_cast<const bf16*>(dx_perm);
-  const bf16* ds = static_cast<const bf16*>(dxs);
+  const float* dp = dx_perm;
+  const float* ds = dxs;
   bf16* o = static_cast<bf16*>(dx);
   if (router_small_path(c)) {
     const size_t smem = wr_smem_bytes(c.d, c.E);

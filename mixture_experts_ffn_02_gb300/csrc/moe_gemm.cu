@@ -52,8 +52,9 @@ struct Params {
   int Mdw;
   int n_tiles;
   int m_tiles_dw;
-  bf16* out0;
+  void* out0;        // bf16, or fp32 when out_f32 (GK_DOWN, GK_DX)
   int ld0;
+  int out_f32;
   bf16* out1;
   int ld1;
   const bf16* aux_in;
@@ -193,7 +194,7 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const Tile& t, ui
         }
         hv[q] = pack8(hf); av[q] = pack8(af); bv[q] = pack8(bf);
       }
-      bf16* hp = p.out0 + (size_t)row * p.ld0 + col;
+      bf16* hp = static_cast<bf16*>(p.out0) + (size_t)row * p.ld0 + col;
 #pragma unroll
       for (int q = 0; q < 4; ++q) st_v4(hp + q * 8, hv[q]);
       if (p.out1) {
@@ -217,7 +218,7 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const Tile& t, ui
         // dH -> (da, db) with the saved pre-activations a, b
         const bf16* ap = p.aux_in + (size_t)row * p.ld_aux + col;
         const bf16* bp = ap + p.H;
-        bf16* dap = p.out0 + (size_t)row * p.ld0 + col;
+        bf16* dap = static_cast<bf16*>(p.out0) + (size_t)row * p.ld0 + col;
         bf16* dbp = dap + p.H;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -236,12 +237,20 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const Tile& t, ui
           st_v4(dap + q * 8, pack8(da));
           st_v4(dbp + q * 8, pack8(db));
         }
+      } else if (KIND != GK_DW && p.out_f32) {
+        float* op = static_cast<float*>(p.out0) + (size_t)row * p.ld0 + col;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          uint4 v = make_uint4(r0[q * 4 + 0], r0[q * 4 + 1], r0[q * 4 + 2], r0[q * 4 + 3]);
+          st_v4(op + q * 4, v);
+        }
       } else {
         bf16* op;
         if (KIND == GK_DW)
-          op = p.out0 + (size_t)t.e * p.Mdw * p.ld0 + (size_t)row * p.ld0 + col;
+          op = static_cast<bf16*>(p.out0) + (size_t)t.e * p.Mdw * p.ld0 + (size_t)row * p.ld0 +
+               col;
         else
-          op = p.out0 + (size_t)row * p.ld0 + col;
+          op = static_cast<bf16*>(p.out0) + (size_t)row * p.ld0 + col;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           float v[8];
@@ -470,8 +479,9 @@ cudaError_t launch_gemm(const GemmCall& g, cudaStream_t s) {
   p.N = g.N;
   p.H = g.H;
   p.Mdw = g.Mdw;
-  p.out0 = static_cast<bf16*>(g.out0);
+  p.out0 = g.out0;
   p.ld0 = g.ld0;
+  p.out_f32 = g.out_f32;
   p.out1 = static_cast<bf16*>(g.out1);
   p.ld1 = g.ld1;
   p.aux_in = static_cast<const bf16*>(g.aux_in);

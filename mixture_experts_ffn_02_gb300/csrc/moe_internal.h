@@ -35,9 +35,9 @@ struct WsLayout {
   // backward scratch
   size_t d_out;         // [R_cap][d] bf16
   size_t d_gu;          // [R_cap][2H] bf16
-  size_t dx_perm;       // [R_cap][d] bf16
+  size_t dx_perm;       // [R_cap][d] fp32
   size_t ds_gu;         // [T][2Hs] bf16
-  size_t dxs;           // [T][d] bf16
+  size_t dxs;           // [T][d] fp32
   size_t dxr;           // [T][d] fp32 (router input gradient, large E)
   size_t dwr_part;      // [splits][d][E] fp32
   size_t total;
@@ -59,16 +59,16 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* to
                            int32_t* counts, int32_t* offsets, int32_t* row_offsets,
                            int32_t* perm, int32_t* inv, void* x_perm, char* ws,
                            const WsLayout& w, cudaStream_t s);
-cudaError_t launch_combine(const moe_config& c, const void* out_perm, const int32_t* inv,
-                           const float* gates, const uint8_t* valid, const void* s_out,
+cudaError_t launch_combine(const moe_config& c, const float* out_perm, const int32_t* inv,
+                           const float* gates, const uint8_t* valid, const float* s_out,
                            void* y, cudaStream_t s);
-cudaError_t launch_combine_bwd(const moe_config& c, const void* dY, const void* out_perm,
+cudaError_t launch_combine_bwd(const moe_config& c, const void* dY, const float* out_perm,
                                const int32_t* inv, const int32_t* topk, const float* gates,
                                const float* L, const float* f, const int32_t* counts,
                                const uint8_t* valid, const int32_t* row_offsets,
                                void* d_out, float* d_logits, int* status, cudaStream_t s);
-cudaError_t launch_dx_gather(const moe_config& c, const void* dx_perm, const int32_t* inv,
-                             const void* dxs, const float* dxr, const float* d_logits,
+cudaError_t launch_dx_gather(const moe_config& c, const float* dx_perm, const int32_t* inv,
+                             const float* dxs, const float* dxr, const float* d_logits,
                              const float* Wr, const uint8_t* valid, void* dx, cudaStream_t s);
 // Router GEMMs on the CUDA cores (fp32 FMA).
 cudaError_t launch_router_dx(const moe_config& c, const float* d_logits, const float* Wr,
@@ -106,6 +106,7 @@ struct GemmCall {
   // Outputs
   void* out0;                  // main output
   int ld0;
+  int out_f32;                 // GK_DOWN / GK_DX: store fp32 instead of bf16
   void* out1;                  // GK_GATE_UP: ab save (or NULL)
   int ld1;
   const void* aux_in;          // GK_DH: ab (a|b) saved by the forward

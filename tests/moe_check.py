@@ -18,28 +18,62 @@ STAT_RTOL = 1e-5
 ROW_ALIGN = 128
 
 
+BF16_U = 2.0 ** -8     # unit roundoff of bfloat16 (8 significant bits)
+
+
 def np64(t):
     if t is None:
         return None
+    if not hasattr(t, "detach"):
+        return np.asarray(t, dtype=np.float64)
     t = t.detach().cpu()
     if t.dtype == torch.bfloat16:
         t = t.float()
     return t.numpy().astype(np.float64)
 
 
-def norm_err(gpu, ref) -> float:
+def norm_err(gpu, ref, rounding=0.0) -> float:
+    """max_i (|gpu_i - ref_i| - rounding |gpu_i|)+ / RMS(ref).
+
+    ``rounding`` is the unit roundoff of the format the GPU stored the value
+    in (bf16: 2^-8): a value rounded once to that format lies within
+    rounding * |stored| of the unrounded result, so that much of the
+    difference is the output format, not the computation."""
     gpu = np.asarray(gpu, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
-    rms = float(np.sqrt(np.mean(ref * ref)))
+    diff = np.abs(gpu - ref)
+    if rounding:
+        diff = np.maximum(diff - rounding * np.abs(gpu), 0.0)
+    rms = float(np.sqrt(np.mean(ref * ref))) if ref.size else 0.0
     if rms == 0.0:
-        return float(np.abs(gpu).max()) if gpu.size else 0.0
-    return float(np.abs(gpu - ref).max()) / rms
+        return float(diff.max()) if diff.size else 0.0
+    return float(diff.max()) / rms
+
+
+class Checker:
+    """Collects every comparison of a test, then fails with the full table."""
+
+    def __init__(self):
+        self.rows = []
+
+    def close(self, name, gpu, ref, tol=NORM_TOL):
+        rounding = BF16_U if (hasattr(gpu, "dtype") and gpu.dtype == torch.bfloat16) else 0.0
+        e = norm_err(np64(gpu), ref, rounding)
+        self.rows.append((name, e, tol))
+        return e
+
+    def done(self):
+        bad = [r for r in self.rows if not (r[1] <= r[2])]
+        table = ", ".join(f"{n}={e:.2e}" for n, e, _ in self.rows)
+        print("errors:", table)
+        assert not bad, "over tolerance: " + ", ".join(f"{n} {e:.3e} > {t:.0e}"
+                                                       for n, e, t in bad) + f" | all: {table}"
 
 
 def assert_close(name, gpu, ref, tol=NORM_TOL):
-    e = norm_err(gpu, ref)
-    assert e <= tol, f"{name}: max normalised error {e:.3e} > {tol:.1e}"
-    return e
+    c = Checker()
+    c.close(name, gpu, ref, tol)
+    c.done()
 
 
 def padded_layout(topk_idx, E):

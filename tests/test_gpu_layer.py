@@ -9,7 +9,7 @@ import torch
 from mixture_experts_ffn_02_gb300 import synth
 from mixture_experts_ffn_02_gb300.binding import Layer
 from oracle import moe_oracle as O
-from moe_check import (STAT_RTOL, assert_close, logit_error_bound, np64,
+from moe_check import (STAT_RTOL, Checker, assert_close, logit_error_bound, np64,
                        reconcile_selection)
 
 pytestmark = pytest.mark.gpu
@@ -61,7 +61,7 @@ def test_forward_matches_oracle(cfg, T):
     inp, lay = run_layer(s)
     r, adopted = oracle_route_like_gpu(s, inp, lay, s.norm_topk)
     b = lay.bufs
-    assert_close("logits", np64(b["logits"]), r["logits"], tol=1e-5)
+    assert_close("logits", b["logits"], r["logits"], tol=1e-5)
     np.testing.assert_array_equal(b["topk_idx"].cpu().numpy(), r["topk_idx"])
     np.testing.assert_array_equal(b["counts"].cpu().numpy(), r["counts"])
     np.testing.assert_allclose(np64(b["f"]), r["f"], rtol=STAT_RTOL)
@@ -69,7 +69,7 @@ def test_forward_matches_oracle(cfg, T):
     assert float(b["aux"][0]) == pytest.approx(r["aux"], rel=1e-4)
     y_ref, _ = O.experts_forward(inp["x"], r["topk_idx"], r["gates"], inp["W_gu"],
                                  inp["W_down"], inp["Ws_gu"], inp["Ws_down"], inp["valid"])
-    assert_close("y", np64(b["y"]), y_ref)
+    assert_close("y", b["y"], y_ref)
 
 
 @pytest.mark.parametrize("cfg,T", SCALED)
@@ -86,14 +86,16 @@ def test_backward_matches_oracle(cfg, T, norm_topk):
                      inp["Ws_down"], fwd, inp["dY"], norm_topk=bool(norm_topk),
                      aux_coef=s.aux_coef)
     g = lay.grads
-    assert_close("d_logits", np64(g["d_logits"]), ref["d_logits"])
-    assert_close("dW_down", np64(g["dW_down"]), ref["dW_down"])
-    assert_close("dW_gu", np64(g["dW_gu"]), ref["dW_gu"])
-    assert_close("dx", np64(g["dx"]), ref["dx"])
-    assert_close("dWr", np64(g["dWr"]), ref["dWr"])
+    chk = Checker()
+    chk.close("d_logits", g["d_logits"], ref["d_logits"])
+    chk.close("dW_down", g["dW_down"], ref["dW_down"])
+    chk.close("dW_gu", g["dW_gu"], ref["dW_gu"])
+    chk.close("dx", g["dx"], ref["dx"])
+    chk.close("dWr", g["dWr"], ref["dWr"])
     if s.n_shared:
-        assert_close("dWs_down", np64(g["dWs_down"]), ref["dWs_down"])
-        assert_close("dWs_gu", np64(g["dWs_gu"]), ref["dWs_gu"])
+        chk.close("dWs_down", g["dWs_down"], ref["dWs_down"])
+        chk.close("dWs_gu", g["dWs_gu"], ref["dWs_gu"])
+    chk.done()
     if inp["valid"] is not None:
         pad = inp["valid"] == 0
         assert (g["dx"].cpu()[pad].float() == 0).all()
