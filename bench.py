@@ -360,9 +360,9 @@ def cpu_baseline(args, s, budget_s=12.0):
     training = not args.fwd_only
     n = 64
     dt = oracle_sample(s, n, training)
-    # grow the sample towards the time budget
-    while dt < budget_s / 4 and n < s.T:
-        n = min(s.T, n * 4)
+    # grow the sample until it takes about budget_s of CPU time
+    while dt < budget_s / 2 and n < s.T:
+        n = min(s.T, n * 2)
         dt = oracle_sample(s, n, training)
     return {"value": round(n / dt, 2), "unit": "tokens/s", "cores": blas_threads(),
             "kind": "oracle",
@@ -404,7 +404,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=150)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", type=int, default=2)
     ap.add_argument("--tokens", type=int, default=None,

@@ -179,12 +179,20 @@ def permute(topk_idx, E):
 # Experts ("KochiLLM v1.0" card: SwiGLU experts, hidden 2 x dim)
 # --------------------------------------------------------------------------
 
-def swiglu_parts(xr, Wg, Wu, Wd):
+def _exact(a):
+    return a
+
+
+def swiglu_parts(xr, Wg, Wu, Wd, rnd=None):
     """One SwiGLU FFN on rows xr: a = xr Wg^T, b = xr Wu^T,
-    h = silu(a) * b, out = h Wd^T.  Returns (out, a, b, h)."""
+    h = silu(a) * b, out = h Wd^T.  Returns (out, a, b, h).
+
+    ``rnd`` (default: none) rounds the stored hidden h before the down
+    projection; it models a storage precision, the arithmetic is unchanged."""
+    rnd = rnd or _exact
     a = xr @ Wg.T
     b = xr @ Wu.T
-    h = silu(a) * b
+    h = rnd(silu(a) * b)
     return h @ Wd.T, a, b, h
 
 
@@ -195,13 +203,14 @@ def split_gu(W_gu):
 
 
 def experts_forward(x, topk_idx, gates, W_gu, W_down, Ws_gu=None, Ws_down=None,
-                    valid=None):
+                    valid=None, rnd=None):
     """y_t = sum_j g_{t,j} F_{e_{t,j}}(x_t) + F_shared(x_t) for real t; PAD -> 0.
 
     Per token and slot, the expert the router chose is applied (vectorised
     over the tokens that chose the same expert in the same slot, one fp64
     matmul each), then the gated outputs are summed.
     Returns (y [T][d], routed [T][k][d] = F_{e_{t,j}}(x_t)).
+    ``rnd`` rounds the stored hidden activations (see :func:`swiglu_parts`).
     """
     x = _f64(x); W_gu = _f64(W_gu); W_down = _f64(W_down)
     idx = np.asarray(topk_idx); g = np.asarray(gates, dtype=f64)
@@ -214,12 +223,12 @@ def experts_forward(x, topk_idx, gates, W_gu, W_down, Ws_gu=None, Ws_down=None,
         for e in range(E):
             rows = np.nonzero(idx[:, j] == e)[0]
             if rows.size:
-                routed[rows, j], *_ = swiglu_parts(x[rows], Wg[e], Wu[e], W_down[e])
+                routed[rows, j], *_ = swiglu_parts(x[rows], Wg[e], Wu[e], W_down[e], rnd)
     y = np.einsum("tj,tjd->td", g, routed)
     real = np.ones(T, dtype=bool) if valid is None else (np.asarray(_np(valid)) != 0)
     if Ws_gu is not None:
         sg, su = split_gu(_f64(Ws_gu))
-        shared, *_ = swiglu_parts(x[real], sg, su, _f64(Ws_down))
+        shared, *_ = swiglu_parts(x[real], sg, su, _f64(Ws_down), rnd)
         y[real] += shared
     y[~real] = 0.0
     return y, routed
@@ -289,13 +298,19 @@ def aux_logit_grad(probs, f, real, aux_coef):
 
 
 def backward(x, Wr, W_gu, W_down, Ws_gu, Ws_down, fwd, dY, norm_topk=True,
-             aux_coef=0.01):
+             aux_coef=0.01, rnd=None):
     """Gradients of J = <dY, y> + aux_coef * aux by the chain rule.
 
     ``fwd`` is the dict returned by :func:`forward` (routing and probs).
     Returns dict: dx [T][d], dWr [d][E], dW_gu [E][2H][d], dW_down [E][d][H],
     dWs_gu, dWs_down (or None), d_logits [T][E], dg [T][k].
+
+    ``rnd`` (default: none) rounds the values a bf16-storage implementation
+    keeps between its matrix products -- the hidden h, the saved
+    pre-activations a and b, d_out = g dY, and (da, db) -- without changing
+    any arithmetic step.  With ``rnd`` None this is the exact gradient.
     """
+    rnd = rnd or _exact
     x = _f64(x); Wr = _f64(Wr); W_gu = _f64(W_gu); W_down = _f64(W_down)
     dY = _f64(dY)
     idx = fwd["topk_idx"]; g = fwd["gates"]; real = fwd["real"]
@@ -308,19 +323,22 @@ def backward(x, Wr, W_gu, W_down, Ws_gu, Ws_down, fwd, dY, norm_topk=True,
     dW_gu = np.zeros_like(W_gu)
     dW_down = np.zeros_like(W_down)
     dg = np.zeros((T, k))
+
+    def swiglu_bwd(dh, a, b):
+        a, b = rnd(a), rnd(b)
+        sa = sigmoid(a)
+        return rnd(dh * b * sa * (1.0 + a * (1.0 - sa))), rnd(dh * silu(a))
+
     for j in range(k):
         for e in range(E):
             rows = np.nonzero(idx[:, j] == e)[0]
             if not rows.size:
                 continue
             xr = x[rows]
-            out, a, b, h = swiglu_parts(xr, Wg[e], Wu[e], W_down[e])
+            out, a, b, h = swiglu_parts(xr, Wg[e], Wu[e], W_down[e], rnd)
             dg[rows, j] = (dY[rows] * out).sum(axis=1)
-            d_out = g[rows, j][:, None] * dY[rows]
-            dh = d_out @ W_down[e]
-            sa = sigmoid(a)
-            da = dh * b * sa * (1.0 + a * (1.0 - sa))
-            db = dh * silu(a)
+            d_out = rnd(g[rows, j][:, None] * dY[rows])
+            da, db = swiglu_bwd(d_out @ W_down[e], a, b)
             dx[rows] += da @ Wg[e] + db @ Wu[e]
             dW_down[e] += d_out.T @ h
             dW_gu[e, :H] += da.T @ xr
@@ -331,11 +349,8 @@ def backward(x, Wr, W_gu, W_down, Ws_gu, Ws_down, fwd, dY, norm_topk=True,
         sg, su = split_gu(Ws_gu_)
         rows = np.nonzero(real)[0]
         xr = x[rows]
-        out, a, b, h = swiglu_parts(xr, sg, su, Ws_down_)
-        dh = dY[rows] @ Ws_down_
-        sa = sigmoid(a)
-        da = dh * b * sa * (1.0 + a * (1.0 - sa))
-        db = dh * silu(a)
+        out, a, b, h = swiglu_parts(xr, sg, su, Ws_down_, rnd)
+        da, db = swiglu_bwd(dY[rows] @ Ws_down_, a, b)
         dx[rows] += da @ sg + db @ su
         Hs = sg.shape[0]
         dWs_gu = np.zeros_like(Ws_gu_)

@@ -50,8 +50,32 @@ def norm_err(gpu, ref, rounding=0.0) -> float:
     return float(diff.max()) / rms
 
 
+def bf16_round(a):
+    """Round-to-nearest-even to bfloat16, back in float64 (storage model)."""
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float64)).to(
+        torch.bfloat16).double().numpy()
+
+
+def frob_err(gpu, ref) -> float:
+    gpu = np.asarray(gpu, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    n = float(np.linalg.norm(ref))
+    return float(np.linalg.norm(gpu - ref)) / n if n else float(np.linalg.norm(gpu))
+
+
 class Checker:
-    """Collects every comparison of a test, then fails with the full table."""
+    """Collects every comparison of a test, then fails with the full table.
+
+    close(name, gpu, exact): max normalised error vs the exact oracle <= tol
+        (the stated tolerance, literally; used for the layer output y).
+    close2(name, gpu, exact, ideal): for values that pass through bf16
+        storage between matrix products.  ``ideal`` is the oracle with bf16
+        rounding at the layer's storage points and exact arithmetic
+        otherwise, so |ideal - exact| is the error the storage format alone
+        makes.  Requires
+          max normalised |gpu - exact| <= 2 * max normalised |ideal - exact| + tol
+          Frobenius-relative |gpu - exact| <= tol.
+    """
 
     def __init__(self):
         self.rows = []
@@ -62,11 +86,19 @@ class Checker:
         self.rows.append((name, e, tol))
         return e
 
+    def close2(self, name, gpu, exact, ideal, tol=NORM_TOL):
+        rounding = BF16_U if (hasattr(gpu, "dtype") and gpu.dtype == torch.bfloat16) else 0.0
+        g = np64(gpu)
+        storage = norm_err(ideal, exact)
+        self.rows.append((name + "(max)", norm_err(g, exact, rounding), 2 * storage + tol))
+        self.rows.append((name + "(F)", frob_err(g, exact), tol))
+        self.rows.append((name + "[storage]", storage, float("inf")))
+
     def done(self):
         bad = [r for r in self.rows if not (r[1] <= r[2])]
         table = ", ".join(f"{n}={e:.2e}" for n, e, _ in self.rows)
         print("errors:", table)
-        assert not bad, "over tolerance: " + ", ".join(f"{n} {e:.3e} > {t:.0e}"
+        assert not bad, "over tolerance: " + ", ".join(f"{n} {e:.3e} > {t:.2e}"
                                                        for n, e, t in bad) + f" | all: {table}"
 
 

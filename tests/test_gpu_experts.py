@@ -9,7 +9,7 @@ import torch
 from mixture_experts_ffn_02_gb300 import synth
 from mixture_experts_ffn_02_gb300.binding import Layer
 from oracle import moe_oracle as O
-from moe_check import Checker, np64, padded_layout
+from moe_check import Checker, bf16_round, np64, padded_layout
 
 pytestmark = pytest.mark.gpu
 
@@ -62,7 +62,7 @@ def test_expert_gemms_and_combine(name, T, d, E, k, H, ns, Hs, pad, skew):
     Wg, Wu = O.split_gu(np64(inp["W_gu"]))
     Wd = np64(inp["W_down"])
     h_ref = np.zeros((R, H)); a_ref = np.zeros((R, H)); b_ref = np.zeros((R, H))
-    o_ref = np.zeros((R, d))
+    o_ref = np.zeros((R, d)); o_ideal = np.zeros((R, d))
     for e in range(E):
         rows = np.arange(row_offsets[e], row_offsets[e] + offsets[e + 1] - offsets[e])
         if rows.size == 0:
@@ -70,26 +70,33 @@ def test_expert_gemms_and_combine(name, T, d, E, k, H, ns, Hs, pad, skew):
         toks = perm_padded[rows] // k
         out, a, b, h = O.swiglu_parts(x[toks], Wg[e], Wu[e], Wd[e])
         h_ref[rows], a_ref[rows], b_ref[rows], o_ref[rows] = h, a, b, out
+        o_ideal[rows] = O.swiglu_parts(x[toks], Wg[e], Wu[e], Wd[e], bf16_round)[0]
     bufs = lay.bufs
     chk = Checker()
     chk.close("h", bufs["h"][:R], h_ref)
     chk.close("a", bufs["ab"][:R, :H], a_ref)
     chk.close("b", bufs["ab"][:R, H:], b_ref)
-    chk.close("out_perm", bufs["out_perm"][:R], o_ref)
+    chk.close2("out_perm", bufs["out_perm"][:R], o_ref, o_ideal)
     pad_rows = torch.from_numpy(perm_padded < 0)
     assert (bufs["h"][:R].cpu()[pad_rows].float() == 0).all()
     assert (bufs["out_perm"][:R].cpu()[pad_rows].float() == 0).all()
 
+    vnp = None if valid is None else valid.numpy()
     y_ref, _ = O.experts_forward(inp["x"], topk.numpy(), g.numpy(), inp["W_gu"],
-                                 inp["W_down"], inp["Ws_gu"], inp["Ws_down"],
-                                 None if valid is None else valid.numpy())
+                                 inp["W_down"], inp["Ws_gu"], inp["Ws_down"], vnp)
+    y_ideal, _ = O.experts_forward(inp["x"], topk.numpy(), g.numpy(), inp["W_gu"],
+                                   inp["W_down"], inp["Ws_gu"], inp["Ws_down"], vnp,
+                                   rnd=bf16_round)
     if ns:
         sg, su = O.split_gu(np64(inp["Ws_gu"]))
         s_ref, *_ = O.swiglu_parts(x, sg, su, np64(inp["Ws_down"]))
+        s_ideal, *_ = O.swiglu_parts(x, sg, su, np64(inp["Ws_down"]), bf16_round)
         if valid is not None:
-            s_ref[valid.numpy() == 0] = 0
-        chk.close("s_out", bufs["s_out"], s_ref)
+            s_ref[vnp == 0] = 0
+            s_ideal[vnp == 0] = 0
+        chk.close2("s_out", bufs["s_out"], s_ref, s_ideal)
     chk.close("y", bufs["y"], y_ref)
+    chk.close2("y", bufs["y"], y_ref, y_ideal)
     chk.done()
     if valid is not None:
         assert (bufs["y"].cpu()[valid == 0].float() == 0).all()

@@ -1,0 +1,50 @@
+"""Why the GPU tests check gradients the way they do (CPU only).
+
+The layer stores its GEMM operands in bf16 (hidden h, saved pre-activations,
+d_out = g dY, (da, db)); tensor cores take bf16 operands.  Even an ideal
+pipeline with exact accumulation and rounding only at those storage points
+misses a max normalised error of 1e-2 on the expert weight gradients of the
+many-expert shapes, while its Frobenius-relative error stays near 2e-3.  So
+the GPU tests hold gradients to 1e-2 (max normalised) against the oracle
+with the same storage rounding, and to 1e-2 Frobenius-relative against the
+exact oracle; the layer output y is held to the literal 1e-2.
+"""
+import numpy as np
+
+from mixture_experts_ffn_02_gb300 import synth
+from oracle import moe_oracle as O
+from moe_check import bf16_round, frob_err, norm_err
+
+
+def test_ideal_bf16_storage_exceeds_literal_max_metric_on_weight_grads():
+    s = synth.scaled(synth.shape(4), T=300, T_real=None, zipf_bias=0.0)
+    inp = synth.make_inputs(s, seed=0, with_grad=True)
+    fwd = O.forward(inp["x"], inp["Wr"], inp["W_gu"], inp["W_down"], inp["Ws_gu"],
+                    inp["Ws_down"], k=s.k)
+    args = (inp["x"], inp["Wr"], inp["W_gu"], inp["W_down"], inp["Ws_gu"], inp["Ws_down"],
+            fwd, inp["dY"])
+    exact = O.backward(*args)
+    ideal = O.backward(*args, rnd=bf16_round)
+    worst = max(norm_err(ideal[n], exact[n]) for n in ("dW_gu", "dW_down"))
+    assert worst > 1e-2
+    for n in ("dW_gu", "dW_down", "dx", "d_logits", "dWr"):
+        assert frob_err(ideal[n], exact[n]) < 5e-3, n
+
+
+def test_storage_rounding_hook_is_identity_when_absent():
+    s = synth.scaled(synth.shape(1), T=40)
+    inp = synth.make_inputs(s, seed=1, with_grad=True)
+    fwd = O.forward(inp["x"], inp["Wr"], inp["W_gu"], inp["W_down"], inp["Ws_gu"],
+                    inp["Ws_down"], k=s.k)
+    args = (inp["x"], inp["Wr"], inp["W_gu"], inp["W_down"], inp["Ws_gu"], inp["Ws_down"],
+            fwd, inp["dY"])
+    a = O.backward(*args)
+    b = O.backward(*args, rnd=lambda v: v)
+    for n in a:
+        if a[n] is not None:
+            np.testing.assert_array_equal(a[n], b[n])
+    # with bf16 storage the stored hidden is exactly bf16(h)
+    xr = np.asarray(inp["x"].double())
+    Wg, Wu = O.split_gu(inp["W_gu"].double().numpy()[0])
+    _, a_, b_, h_ = O.swiglu_parts(xr, Wg, Wu, inp["W_down"].double().numpy()[0], bf16_round)
+    np.testing.assert_array_equal(h_, bf16_round(O.silu(a_) * b_))
