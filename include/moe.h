@@ -235,6 +235,40 @@ int moe_forward(const moe_config* cfg, const moe_tensors* t,
 int moe_backward(const moe_config* cfg, const moe_tensors* t, const moe_grads* g,
                  void* workspace, size_t workspace_bytes, void* stream);
 
+/* ------------------------------------------------- no-allocation routing */
+
+/* Bytes of the fixed device scratch array behind moe_route_static (per GPU). */
+#define MOE_ROUTE_STATIC_SCRATCH_BYTES (512 * 1024)
+
+/* a1 without a workspace.  The pages have no counterpart to this entry point;
+ * it exists for callers that cannot allocate device memory at all -- code
+ * running under a host framework that owns every allocation, inside a region
+ * where cudaMalloc is forbidden, or with a fixed memory plan -- and so cannot
+ * supply the workspace moe_route needs.
+ *
+ * Computes exactly what moe_route computes (same kernel, same launch shape,
+ * same bytes out).  Reads logits, bias, valid; writes topk_idx, gates,
+ * counts, f, p, aux of `t` (other fields are ignored).  `device_status` is an
+ * optional device int (NULL = not reported) where a device-side error
+ * (MOE_ERR_NONFINITE) is stored if it is still 0; the caller clears it.
+ *
+ * Scratch: a fixed array of MOE_ROUTE_STATIC_SCRATCH_BYTES in the library's
+ * device memory, held by every GPU that loads the library until the process
+ * exits.  A call needs 256 + B * (8 E + 4) bytes of it, B being the route
+ * kernel's block count (min(304, ceil(T / G)), G = tokens per block); larger
+ * configurations are rejected with MOE_ERR_WORKSPACE before any work.  Every
+ * E <= 128 fits at any T.
+ * Set-up: the first call on each device resolves the array's device address
+ * (a runtime symbol query, no allocation); make that first call before any
+ * stream capture.  The call itself allocates nothing: no cudaMalloc, no
+ * cudaFree, no allocating library routine.
+ * Sharing: all calls on a GPU use the same array, which keeps the last call's
+ * contents; the ticket counter that must start at zero is cleared at the
+ * start of each call.  Calls that overlap on the GPU (two streams at once)
+ * race on the array: serialise them. */
+int moe_route_static(const moe_config* cfg, const moe_tensors* t, int* device_status,
+                     void* stream);
+
 #ifdef __cplusplus
 }
 #endif

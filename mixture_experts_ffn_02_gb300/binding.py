@@ -69,6 +69,8 @@ SIGNATURES = {
     "moe_backward": (ctypes.c_int, [ctypes.POINTER(MoEConfig), ctypes.POINTER(MoETensors),
                                     ctypes.POINTER(MoEGrads), c_void_p, ctypes.c_size_t,
                                     c_void_p]),
+    "moe_route_static": (ctypes.c_int, [ctypes.POINTER(MoEConfig), ctypes.POINTER(MoETensors),
+                                        c_void_p, c_void_p]),
 }
 
 _LIB = None

@@ -813,6 +813,33 @@ cudaError_t launch_route(const moe_config& c, const float* L, const float* bias,
   return cudaGetLastError();
 }
 
+// The route kernel with caller-chosen scratch pointers and grid size (used by
+// the entry point whose scratch is a fixed device array instead of a
+// workspace).  Same kernel, same arithmetic.
+cudaError_t launch_route_scratch(const moe_config& c, const float* L, const float* bias,
+                                 const uint8_t* valid, int32_t* topk, float* gates,
+                                 int32_t* counts, float* f, float* p, float* aux, int* blk_cnt,
+                                 float* blk_psum, int* blk_treal, int* done, int* status,
+                                 int grid, cudaStream_t s) {
+  int G = 1;
+  while (G < c.E && G < 32) G <<= 1;
+  const int V = (c.E + G - 1) / G;
+  const int groups = kThreads / G;
+  const size_t smem = 256 * sizeof(int) + (size_t)groups * c.E * sizeof(float);
+#define MOE_ROUTE_S(VV)                                                                       \
+  cudaFuncSetAttribute(route_kernel<VV>, cudaFuncAttributeMaxDynamicSharedMemorySize,         \
+                       (int)smem);                                                            \
+  route_kernel<VV><<<grid, kThreads, smem, s>>>(L, bias, valid, c.T, c.E, c.k, G, c.norm_topk, \
+                                                topk, gates, blk_cnt, blk_psum, blk_treal, done, \
+                                                counts, f, p, aux, status)
+  if (V <= 1) { MOE_ROUTE_S(1); }
+  else if (V <= 2) { MOE_ROUTE_S(2); }
+  else if (V <= 4) { MOE_ROUTE_S(4); }
+  else { MOE_ROUTE_S(8); }
+#undef MOE_ROUTE_S
+  return cudaGetLastError();
+}
+
 cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* topk,
                            int32_t* counts, int32_t* offsets, int32_t* row_offsets,
                            int32_t* perm, int32_t* inv, void* x_perm, char* ws,

@@ -55,6 +55,11 @@ cudaError_t launch_route(const moe_config& c, const float* L, const float* bias,
                          const uint8_t* valid, int32_t* topk, float* gates, int32_t* counts,
                          float* f, float* p, float* aux, char* ws, const WsLayout& w,
                          cudaStream_t s);
+cudaError_t launch_route_scratch(const moe_config& c, const float* L, const float* bias,
+                                 const uint8_t* valid, int32_t* topk, float* gates,
+                                 int32_t* counts, float* f, float* p, float* aux, int* blk_cnt,
+                                 float* blk_psum, int* blk_treal, int* done, int* status,
+                                 int grid, cudaStream_t s);
 cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* topk,
                            int32_t* counts, int32_t* offsets, int32_t* row_offsets,
                            int32_t* perm, int32_t* inv, void* x_perm, char* ws,
