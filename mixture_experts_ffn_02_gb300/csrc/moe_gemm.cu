@@ -36,7 +36,8 @@ constexpr int A_BYTES = BM * BK * 2;     // 16 KB
 constexpr int B_BYTES = BN * BK * 2;     // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 512;           // two 128 x 256 fp32 accumulators
-constexpr int THREADS = 256;             // warp 0 TMA, 1 MMA, 2 TMEM, 4-7 epilogue
+constexpr int THREADS = 384;             // warp 0 TMA, 1 MMA, 2 TMEM, 4-11 epilogue
+constexpr int EPI_THREADS = 256;         // two warpgroups split each tile's columns
 constexpr int EPI_WARP0 = 4;
 constexpr uint64_t WAIT_NS = 2000000000ull;  // bounded waits give up after 2 s
 constexpr uint64_t DRAIN_NS = 200000000ull;
@@ -161,104 +162,134 @@ __device__ __forceinline__ void issue_loads(const Tile& t, int kb, uint32_t sa, 
 // ------------------------------------------------------------------ epilogue
 __device__ __forceinline__ float silu_f(float a) { return a / (1.f + __expf(-a)); }
 
+// Stores one 32-column chunk of a finished accumulator row (all kinds but
+// GK_GATE_UP and GK_DH).
+template <int KIND>
+__device__ __forceinline__ void store_chunk(const Params& p, const Tile& t, int row, int col,
+                                            const uint32_t* r, bool no_acc) {
+  if (KIND != GK_DW && p.out_f32) {
+    float* op = static_cast<float*>(p.out0) + (size_t)row * p.ld0 + col;
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      st_v4(op + q * 4, make_uint4(r[q * 4 + 0], r[q * 4 + 1], r[q * 4 + 2], r[q * 4 + 3]));
+  } else {
+    bf16* op = static_cast<bf16*>(p.out0) + (size_t)row * p.ld0 + col;
+    if (KIND == GK_DW) op += (size_t)t.e * p.Mdw * p.ld0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = no_acc ? 0.f : __uint_as_float(r[q * 8 + u]);
+      st_v4(op + q * 8, pack8(v));
+    }
+  }
+}
+
+// Epilogue of one tile for one thread: TMEM lane = its row, and the column
+// half `half` of the tile (two warpgroups split the columns).
 template <int KIND>
 __device__ __forceinline__ void epilogue_tile(const Params& p, const Tile& t, uint32_t tacc,
-                                              int row_in_tile) {
+                                              int row_in_tile, int half) {
   const int row = t.m0 + row_in_tile;
   bool row_ok;
   if (KIND == GK_DW) row_ok = row < p.Mdw;
   else row_ok = p.row_offsets ? true : row < p.rows;
-  const bool zero_row = (KIND == GK_GATE_UP) && p.valid && row_ok && p.valid[row] == 0;
   const bool no_acc = t.ksteps == 0;
   uint32_t r0[32], r1[32];
   if (KIND == GK_GATE_UP) {
+    const bool zero_row = p.valid && row_ok && p.valid[row] == 0;
+    constexpr int NCH = BN / 2 / 32 / 2;          // chunks per half
 #pragma unroll 1
-    for (int cb = 0; cb < BN / 2 / 32; ++cb) {
+    for (int i = 0; i < NCH; ++i) {
+      const int cb = half * NCH + i;
       __syncwarp();
       tmem_ld32(tacc + cb * 32, r0);
       tmem_ld32(tacc + BN / 2 + cb * 32, r1);
       tmem_ld_wait();
       const int col = t.n0 + cb * 32;
       if (row_ok && col < p.H) {
-      uint4 hv[4], av[4], bv[4];
+        uint4 hv[4], av[4], bv[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float hf[8], af[8], bf[8];
+        for (int q = 0; q < 4; ++q) {
+          float hf[8], af[8], bf[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          float a = __uint_as_float(r0[q * 8 + u]);
-          float b = __uint_as_float(r1[q * 8 + u]);
-          if (zero_row) { a = 0.f; b = 0.f; }
-          af[u] = a; bf[u] = b;
-          hf[u] = silu_f(a) * b;
+          for (int u = 0; u < 8; ++u) {
+            float a = __uint_as_float(r0[q * 8 + u]);
+            float b = __uint_as_float(r1[q * 8 + u]);
+            if (zero_row) { a = 0.f; b = 0.f; }
+            af[u] = a; bf[u] = b;
+            hf[u] = silu_f(a) * b;
+          }
+          hv[q] = pack8(hf); av[q] = pack8(af); bv[q] = pack8(bf);
         }
-        hv[q] = pack8(hf); av[q] = pack8(af); bv[q] = pack8(bf);
-      }
-      bf16* hp = static_cast<bf16*>(p.out0) + (size_t)row * p.ld0 + col;
+        bf16* hp = static_cast<bf16*>(p.out0) + (size_t)row * p.ld0 + col;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) st_v4(hp + q * 8, hv[q]);
-      if (p.out1) {
-        bf16* ap = p.out1 + (size_t)row * p.ld1 + col;
-        bf16* bp = ap + p.H;
+        for (int q = 0; q < 4; ++q) st_v4(hp + q * 8, hv[q]);
+        if (p.out1) {
+          bf16* ap = p.out1 + (size_t)row * p.ld1 + col;
+          bf16* bp = ap + p.H;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) { st_v4(ap + q * 8, av[q]); st_v4(bp + q * 8, bv[q]); }
-      }
+          for (int q = 0; q < 4; ++q) { st_v4(ap + q * 8, av[q]); st_v4(bp + q * 8, bv[q]); }
+        }
       }
     }
-  } else {
-#pragma unroll 1
-    for (int cb = 0; cb < BN / 32; ++cb) {
+  } else if (KIND == GK_DH) {
+    // dH -> (da, db) with the saved pre-activations a, b.  The a|b loads of
+    // the next chunk are issued before the current chunk is processed.
+    constexpr int NCH = BN / 32 / 2;
+    uint4 abuf[2][4], bbuf[2][4];
+    auto load_ab = [&](int i, uint4 (&ab4)[4], uint4 (&bb4)[4]) {
+      const int col = t.n0 + (half * NCH + i) * 32;
+      if (row_ok && col < p.N) {
+        const bf16* ap = p.aux_in + (size_t)row * p.ld_aux + col;
+        const bf16* bp = ap + p.H;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          ab4[q] = *reinterpret_cast<const uint4*>(ap + q * 8);
+          bb4[q] = *reinterpret_cast<const uint4*>(bp + q * 8);
+        }
+      }
+    };
+    load_ab(0, abuf[0], bbuf[0]);
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+      if (i + 1 < NCH) load_ab(i + 1, abuf[(i + 1) & 1], bbuf[(i + 1) & 1]);
+      const int cb = half * NCH + i;
       __syncwarp();
       tmem_ld32(tacc + cb * 32, r0);
       tmem_ld_wait();
       const int col = t.n0 + cb * 32;
-      if (!(row_ok && col < p.N)) {
-        // nothing to store for this lane
-      } else if (KIND == GK_DH) {
-        // dH -> (da, db) with the saved pre-activations a, b
-        const bf16* ap = p.aux_in + (size_t)row * p.ld_aux + col;
-        const bf16* bp = ap + p.H;
+      if (row_ok && col < p.N) {
         bf16* dap = static_cast<bf16*>(p.out0) + (size_t)row * p.ld0 + col;
         bf16* dbp = dap + p.H;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           float a8[8], b8[8], da[8], db[8];
-          unpack8(*reinterpret_cast<const uint4*>(ap + q * 8), a8);
-          unpack8(*reinterpret_cast<const uint4*>(bp + q * 8), b8);
+          unpack8(abuf[i & 1][q], a8);
+          unpack8(bbuf[i & 1][q], b8);
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
             const float dh = __uint_as_float(r0[q * 8 + u]);
             const float a = a8[u], b = b8[u];
             const float sg = 1.f / (1.f + __expf(-a));
-            const float sl = a * sg;
             da[u] = dh * b * sg * (1.f + a * (1.f - sg));
-            db[u] = dh * sl;
+            db[u] = dh * (a * sg);
           }
           st_v4(dap + q * 8, pack8(da));
           st_v4(dbp + q * 8, pack8(db));
         }
-      } else if (KIND != GK_DW && p.out_f32) {
-        float* op = static_cast<float*>(p.out0) + (size_t)row * p.ld0 + col;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          uint4 v = make_uint4(r0[q * 4 + 0], r0[q * 4 + 1], r0[q * 4 + 2], r0[q * 4 + 3]);
-          st_v4(op + q * 4, v);
-        }
-      } else {
-        bf16* op;
-        if (KIND == GK_DW)
-          op = static_cast<bf16*>(p.out0) + (size_t)t.e * p.Mdw * p.ld0 + (size_t)row * p.ld0 +
-               col;
-        else
-          op = static_cast<bf16*>(p.out0) + (size_t)row * p.ld0 + col;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          float v[8];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) v[u] = no_acc ? 0.f : __uint_as_float(r0[q * 8 + u]);
-          st_v4(op + q * 8, pack8(v));
-        }
       }
+    }
+  } else {
+    constexpr int NCH = BN / 32 / 2;
+#pragma unroll 1
+    for (int i = 0; i < NCH; ++i) {
+      const int cb = half * NCH + i;
+      __syncwarp();
+      tmem_ld32(tacc + cb * 32, r0);
+      tmem_ld_wait();
+      const int col = t.n0 + cb * 32;
+      if (row_ok && col < p.N) store_chunk<KIND>(p, t, row, col, r0, no_acc);
     }
   }
 }
@@ -284,7 +315,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&sh.tfull[a]), 1);
-      mbar_init(smem_u32(&sh.tempty[a]), 128);
+      mbar_init(smem_u32(&sh.tempty[a]), EPI_THREADS);
     }
     mbar_init(smem_u32(&sh.drain), 1);
     sh.abort_flag = 0;
@@ -387,7 +418,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     mbar_wait_bounded(smem_u32(&sh.drain), 0, &dummy, DRAIN_NS);
   } else if (warp >= EPI_WARP0) {
     // ---------------- epilogue warps: TMEM lanes 32*(warp%4) .. +31
-    const int q = warp - EPI_WARP0;
+    const int q = warp & 3;                       // TMEM lane quadrant of this warp
+    const int half = (warp - EPI_WARP0) >> 2;     // column half of the tile
     const int row_in_tile = q * 32 + lane;
     int it = 0;
     for (int idx = blockIdx.x; idx < ntiles; idx += gridDim.x, ++it) {
@@ -400,7 +432,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       }
       tc_fence_after();
       const uint32_t tacc = tmem + ((uint32_t)(q * 32) << 16) + acc * BN;
-      epilogue_tile<KIND>(p, t, tacc, row_in_tile);
+      epilogue_tile<KIND>(p, t, tacc, row_in_tile, half);
       tc_fence_before();
       mbar_arrive(smem_u32(&sh.tempty[acc]));
     }

@@ -196,6 +196,14 @@ def swiglu_parts(xr, Wg, Wu, Wd, rnd=None):
     return h @ Wd.T, a, b, h
 
 
+def swiglu_backward(dh, a, b):
+    """Chain rule through h = silu(a) * b: given dh = dJ/dh, returns
+    (da, db) = (dh * b * s(a) * (1 + a (1 - s(a))), dh * silu(a)),
+    s the logistic sigmoid."""
+    sa = sigmoid(a)
+    return dh * b * sa * (1.0 + a * (1.0 - sa)), dh * silu(a)
+
+
 def split_gu(W_gu):
     """[.., 2H, d] packed gate/up -> (gate [.., H, d], up [.., H, d])."""
     H = W_gu.shape[-2] // 2
@@ -325,9 +333,8 @@ def backward(x, Wr, W_gu, W_down, Ws_gu, Ws_down, fwd, dY, norm_topk=True,
     dg = np.zeros((T, k))
 
     def swiglu_bwd(dh, a, b):
-        a, b = rnd(a), rnd(b)
-        sa = sigmoid(a)
-        return rnd(dh * b * sa * (1.0 + a * (1.0 - sa))), rnd(dh * silu(a))
+        da, db = swiglu_backward(dh, rnd(a), rnd(b))
+        return rnd(da), rnd(db)
 
     for j in range(k):
         for e in range(E):
