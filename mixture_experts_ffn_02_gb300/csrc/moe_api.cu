@@ -90,6 +90,7 @@ int ws_layout(const moe_config* c, int training, WsLayout* w) {
     int splits = c->T / 1024;
     if (splits < 1) splits = 1;
     if (splits > 64) splits = 64;
+    if (router_small_path(*c)) splits = router_dw_small_parts(*c);
     w->dwr_splits = splits;
     w->dwr_part = take((size_t)splits * c->d * c->E * 4);
   }

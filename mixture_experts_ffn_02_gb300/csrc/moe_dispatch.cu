@@ -152,13 +152,76 @@ simt_gemm_kernel(const TA* __restrict__ A, long long sam, long long sak,
   }
 }
 
-// Deterministic split-K reduction: out[i] = sum_z part[z][i] in z order.
-__global__ void sum_splits_kernel(const float* __restrict__ part, float* __restrict__ out,
-                                  int n, int splits) {
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
-    float s = 0.f;
-    for (int z = 0; z < splits; ++z) s += part[(size_t)z * n + i];
-    out[i] = s;
+// dW_r for small E: part[z][c][e] = sum over the tokens of slice z of
+// x[t][c] * dL[t][e].  Each thread owns 8 consecutive columns (16-byte x
+// loads, coalesced across the block) and walks the block's token chunk; the
+// chunk's dL rows sit in shared memory.  When d/8 < blockDim.x the block's
+// threads also split the chunk's tokens into `slices` interleaved sets, each
+// writing its own partial.
+template <int E>
+__global__ void __launch_bounds__(kThreads)
+router_dw_small_kernel(const bf16* __restrict__ x, const float* __restrict__ dL,
+                       float* __restrict__ part, int T, int d, int tok_per_blk) {
+  extern __shared__ float dl_s[];  // [tok_per_blk][E]
+  const int t0 = blockIdx.x * tok_per_blk;
+  const int nt = min(tok_per_blk, T - t0);
+  for (int i = threadIdx.x; i < nt * E; i += blockDim.x) dl_s[i] = dL[(size_t)t0 * E + i];
+  __syncthreads();
+  const int groups = d / 8;
+  const int slices = max(1, (int)blockDim.x / groups);
+  const int s = threadIdx.x / groups;
+  for (int g = threadIdx.x % groups; g < groups && s < slices; g += (slices == 1 ? blockDim.x : groups)) {
+    float acc[8][E];
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[u][e] = 0.f;
+    for (int tl = s; tl < nt; tl += slices) {
+      float xf[8];
+      unpack8(ld_nc_v4(x + (size_t)(t0 + tl) * d + g * 8), xf);
+      const float* dl = dl_s + tl * E;
+#pragma unroll
+      for (int e4 = 0; e4 < E; e4 += 4) {
+        const float4 w = *reinterpret_cast<const float4*>(dl + e4);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          acc[u][e4 + 0] = fmaf(xf[u], w.x, acc[u][e4 + 0]);
+          acc[u][e4 + 1] = fmaf(xf[u], w.y, acc[u][e4 + 1]);
+          acc[u][e4 + 2] = fmaf(xf[u], w.z, acc[u][e4 + 2]);
+          acc[u][e4 + 3] = fmaf(xf[u], w.w, acc[u][e4 + 3]);
+        }
+      }
+    }
+    float* dst = part + ((size_t)blockIdx.x * slices + s) * d * E + (size_t)g * 8 * E;
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+#pragma unroll
+      for (int e4 = 0; e4 < E; e4 += 4)
+        *reinterpret_cast<float4*>(dst + u * E + e4) =
+            make_float4(acc[u][e4], acc[u][e4 + 1], acc[u][e4 + 2], acc[u][e4 + 3]);
+  }
+}
+
+// Deterministic split reduction out[i] = sum_z part[z][i]: a block covers 32
+// outputs with 8 lanes each; lane l sums z = l, l+8, ... and the 8 lane sums
+// are added in lane order.
+__global__ void __launch_bounds__(256)
+sum_splits_kernel(const float* __restrict__ part, float* __restrict__ out, int n, int splits) {
+  __shared__ float red[8][33];
+  const int o = blockIdx.x * 32 + (threadIdx.x & 31);
+  const int zl = threadIdx.x >> 5;
+  float acc = 0.f;
+  if (o < n) {
+#pragma unroll 4
+    for (int z = zl; z < splits; z += 8) acc += part[(size_t)z * n + o];
+  }
+  red[zl][threadIdx.x & 31] = acc;
+  __syncthreads();
+  if (zl == 0 && o < n) {
+    float v = 0.f;
+#pragma unroll
+    for (int l = 0; l < 8; ++l) v += red[l][threadIdx.x];
+    out[o] = v;
   }
 }
 
@@ -770,15 +833,44 @@ cudaError_t launch_router_dx(const moe_config& c, const float* dL, const float* 
   return cudaGetLastError();
 }
 
+int router_dw_small_parts(const moe_config& c) {
+  const int groups = c.d / 8;
+  const int slices = groups >= kThreads ? 1 : kThreads / groups;
+  return (c.T + kDwTokPerBlk - 1) / kDwTokPerBlk * slices;
+}
+
 cudaError_t launch_router_dw(const moe_config& c, const void* x, const float* dL, float* dWr,
                              float* part, int splits, cudaStream_t s) {
+  if (router_small_path(c)) {
+    const int nblk = (c.T + kDwTokPerBlk - 1) / kDwTokPerBlk;
+    const int nparts = router_dw_small_parts(c);
+    const size_t smem = (size_t)kDwTokPerBlk * c.E * sizeof(float);
+    const bf16* xb = static_cast<const bf16*>(x);
+    switch (c.E) {
+      case 4:
+        router_dw_small_kernel<4><<<nblk, kThreads, smem, s>>>(xb, dL, part, c.T, c.d,
+                                                               kDwTokPerBlk);
+        break;
+      case 8:
+        router_dw_small_kernel<8><<<nblk, kThreads, smem, s>>>(xb, dL, part, c.T, c.d,
+                                                               kDwTokPerBlk);
+        break;
+      default:
+        router_dw_small_kernel<16><<<nblk, kThreads, smem, s>>>(xb, dL, part, c.T, c.d,
+                                                                kDwTokPerBlk);
+        break;
+    }
+    const int n = c.d * c.E;
+    sum_splits_kernel<<<(n + 31) / 32, 256, 0, s>>>(part, dWr, n, nparts);
+    return cudaGetLastError();
+  }
   // dWr[d][E] = sum_t x[t][c] dL[t][e]: A(m=c, k=t) = x[t*d + c]
   const int kps = ((c.T + splits - 1) / splits + 15) / 16 * 16;
   dim3 grid((c.E + 63) / 64, (c.d + 63) / 64, splits);
   simt_gemm_kernel<bf16><<<grid, 256, 0, s>>>(static_cast<const bf16*>(x), 1, c.d, dL, c.E, 1,
                                                part, c.d, c.E, c.T, kps);
   const int n = c.d * c.E;
-  sum_splits_kernel<<<(n + 255) / 256, 256, 0, s>>>(part, dWr, n, splits);
+  sum_splits_kernel<<<(n + 31) / 32, 256, 0, s>>>(part, dWr, n, splits);
   return cudaGetLastError();
 }
 

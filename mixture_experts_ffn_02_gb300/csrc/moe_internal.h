@@ -12,6 +12,7 @@ namespace moe {
 constexpr int kRowAlign = MOE_ROW_ALIGN;  // expert segments start at multiples
 constexpr int kPermChunk = 128;           // tokens per block in the dispatch kernels
 constexpr int kMaxK = 32;                 // experts per token supported
+constexpr int kDwTokPerBlk = 256;         // tokens per block of the small-E dW_r kernel
 
 // Per-device facts, cached after the first query.
 struct DeviceInfo {
@@ -81,6 +82,7 @@ cudaError_t launch_router_dx(const moe_config& c, const float* d_logits, const f
 cudaError_t launch_router_dw(const moe_config& c, const void* x, const float* d_logits,
                              float* dWr, float* part, int splits, cudaStream_t s);
 bool router_small_path(const moe_config& c);
+int router_dw_small_parts(const moe_config& c);   // partial slices of the small-E dW_r
 
 // ---- tcgen05 grouped GEMMs (moe_gemm.cu) -----------------------------------
 // Which product a launch computes (operand majorness and epilogue).
