@@ -118,11 +118,14 @@ class Clocks:
 
 
 def launches_per_step(s, fwd_only):
-    from mixture_experts_ffn_02_gb300 import binding  # noqa: F401
+    """Kernels of this library launched per step (by router path and shared expert)."""
     small = s.E in (4, 8, 16) and s.d * s.E * 4 + (s.d // 8) * 16 <= 96 * 1024
+    tc = not small and s.E % 32 == 0
     shared = s.Hs_total > 0
-    fwd = 1 + 1 + 3 + 1 + 1 + (2 if shared else 0) + 1
-    bwd = 1 + 1 + 1 + 2 + (4 if shared else 0) + (0 if small else 1) + 1 + 2
+    router_fwd = 1
+    router_bwd = 5 if tc else (2 if small else 3)
+    fwd = router_fwd + 1 + 3 + 1 + 1 + (2 if shared else 0) + 1
+    bwd = 1 + 1 + 1 + 2 + (4 if shared else 0) + 1 + router_bwd
     return fwd if fwd_only else fwd + bwd
 
 

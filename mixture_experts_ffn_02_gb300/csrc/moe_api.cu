@@ -76,7 +76,9 @@ int ws_layout(const moe_config* c, int training, WsLayout* w) {
   w->perm_hist = take((size_t)w->perm_blocks * c->E * sizeof(int));
   w->perm_base = take((size_t)w->perm_blocks * c->E * sizeof(int));
   w->d_out = w->d_gu = w->dx_perm = w->ds_gu = w->dxs = w->dxr = w->dwr_part = 0;
+  w->wr2 = w->dl3 = w->dl2 = w->goff = 0;
   w->dwr_splits = 1;
+  const bool tc_router = router_tc_path(*c);
   if (training) {
     const size_t R = (size_t)w->R_cap;
     w->d_out = take(R * c->d * 2);
@@ -91,6 +93,15 @@ int ws_layout(const moe_config* c, int training, WsLayout* w) {
     if (splits < 1) splits = 1;
     if (splits > 64) splits = 64;
     if (router_small_path(*c)) splits = router_dw_small_parts(*c);
+    if (tc_router) {
+      int Tp, G, chunk;
+      router_tc_sizes(*c, &Tp, &G, &chunk);
+      splits = G;
+      w->wr2 = take((size_t)c->d * 3 * c->E * 2);
+      w->dl3 = take((size_t)c->T * 3 * c->E * 2);
+      w->dl2 = take((size_t)2 * Tp * c->E * 2);
+      w->goff = take((size_t)(G + 1) * sizeof(int));
+    }
     w->dwr_splits = splits;
     w->dwr_part = take((size_t)splits * c->d * c->E * 4);
   }
@@ -352,14 +363,20 @@ int do_backward(const moe_config* c, const moe_tensors* t, const moe_grads* g, C
   }
   // (vi) router input gradient and the un-permute sum of dx
   float* dxr = nullptr;
-  if (!router_small_path(*c)) {
+  float* part = reinterpret_cast<float*>(k.ws + w.dwr_part);
+  if (router_tc_path(*c)) {
+    dxr = reinterpret_cast<float*>(k.ws + w.dxr);
+    MOE_CUDA(launch_router_bwd_tc(*c, t->x, g->d_logits, t->Wr, dxr, g->dWr, k.ws + w.wr2,
+                                  k.ws + w.dl3, k.ws + w.dl2,
+                                  reinterpret_cast<int*>(k.ws + w.goff), part, k.status, k.s));
+  } else if (!router_small_path(*c)) {
     dxr = reinterpret_cast<float*>(k.ws + w.dxr);
     MOE_CUDA(launch_router_dx(*c, g->d_logits, t->Wr, dxr, k.s));
   }
   MOE_CUDA(launch_dx_gather(*c, dx_perm, t->inv, dxs, dxr, g->d_logits, t->Wr, t->valid, g->dx,
                             k.s));
-  MOE_CUDA(launch_router_dw(*c, t->x, g->d_logits, g->dWr,
-                            reinterpret_cast<float*>(k.ws + w.dwr_part), w.dwr_splits, k.s));
+  if (!router_tc_path(*c))
+    MOE_CUDA(launch_router_dw(*c, t->x, g->d_logits, g->dWr, part, w.dwr_splits, k.s));
   return MOE_OK;
 }
 

@@ -159,6 +159,31 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* m,
       : "memory");
 }
 
+// TMA stores (shared -> global) in bulk groups.  The source is the 128-byte
+// swizzled box the tensor map describes; the writing threads must issue
+// fence_proxy_async_smem() and synchronise before the store is issued.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
+               :: "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(src) : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, uint32_t src, int x, int y,
+                                             int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];"
+      :: "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(z), "r"(src) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until every committed store has finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Wait until every committed store has completed.
+__device__ __forceinline__ void bulk_wait0() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // ----------------------------------------------------------------- tcgen05
 
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading

@@ -202,6 +202,99 @@ router_dw_small_kernel(const bf16* __restrict__ x, const float* __restrict__ dL,
   }
 }
 
+// Router logits on the CUDA cores for large E: L[T][E] = x[T][d] . W_r[d][E]
+// with IEEE fp32 fused multiply-adds (routing decisions are taken on these
+// values).  Block tile 128 tokens x BE experts x 16 of d; 256 threads, each
+// owning 8 tokens x BE/16 experts; shared tiles double-buffered with the next
+// slice prefetched into registers.
+template <int BE>
+__global__ void __launch_bounds__(256)
+router_logits_sgemm_kernel(const bf16* __restrict__ x, const float* __restrict__ Wr,
+                           float* __restrict__ L, int T, int d, int E) {
+  constexpr int BT = 128, BK = 16, TE = BE / 16;
+  __shared__ __align__(16) float As[2][BK][BT + 4];
+  __shared__ __align__(16) float Bs[2][BK][BE + 4];
+  const int tid = threadIdx.x;
+  const int tx = tid & 15, ty = tid >> 4;       // experts tx*TE.., tokens ty*8..
+  const int t0 = blockIdx.y * BT, e0 = blockIdx.x * BE;
+  // A slice: thread -> token tid/2, k-half (tid%2)*8 (one 16-byte load)
+  const int at = tid >> 1, ak = (tid & 1) * 8;
+  // B slice: BK x BE floats, float4 per load
+  constexpr int BV = BK * BE / 4 / 256;         // float4 loads per thread (1 or 2)
+  float acc[8][TE];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < TE; ++j) acc[i][j] = 0.f;
+  uint4 areg;
+  float4 breg[BV];
+  auto load = [&](int k0) {
+    const int t = t0 + at;
+    areg = (t < T) ? ld_nc_v4(x + (size_t)t * d + k0 + ak) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int v = 0; v < BV; ++v) {
+      const int idx = tid + v * 256;            // float4 index in the BK x BE/4 slice
+      const int kk = idx / (BE / 4), e4 = (idx % (BE / 4)) * 4;
+      const int e = e0 + e4;
+      breg[v] = (e < E) ? *reinterpret_cast<const float4*>(Wr + (size_t)(k0 + kk) * E + e)
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  };
+  auto store = [&](int buf) {
+    float f[8];
+    unpack8(areg, f);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) As[buf][ak + u][at] = f[u];
+#pragma unroll
+    for (int v = 0; v < BV; ++v) {
+      const int idx = tid + v * 256;
+      const int kk = idx / (BE / 4), e4 = (idx % (BE / 4)) * 4;
+      *reinterpret_cast<float4*>(&Bs[buf][kk][e4]) = breg[v];
+    }
+  };
+  load(0);
+  store(0);
+  __syncthreads();
+  int buf = 0;
+  for (int k0 = 0; k0 < d; k0 += BK) {
+    const bool more = k0 + BK < d;
+    if (more) load(k0 + BK);
+#pragma unroll
+    for (int kk = 0; kk < BK; ++kk) {
+      const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 8]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 8 + 4]);
+      const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      float b[TE];
+#pragma unroll
+      for (int j = 0; j < TE; j += 4) {
+        const float4 bv = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * TE + j]);
+        b[j] = bv.x; b[j + 1] = bv.y; b[j + 2] = bv.z; b[j + 3] = bv.w;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < TE; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    if (more) {
+      store(buf ^ 1);
+      __syncthreads();
+      buf ^= 1;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int t = t0 + ty * 8 + i;
+    if (t >= T) continue;
+#pragma unroll
+    for (int j = 0; j < TE; j += 4) {
+      const int e = e0 + tx * TE + j;
+      if (e < E)
+        *reinterpret_cast<float4*>(L + (size_t)t * E + e) =
+            make_float4(acc[i][j], acc[i][j + 1], acc[i][j + 2], acc[i][j + 3]);
+    }
+  }
+}
+
 // Deterministic split reduction out[i] = sum_z part[z][i]: a block covers 32
 // outputs with 8 lanes each; lane l sums z = l, l+8, ... and the 8 lane sums
 // are added in lane order.
@@ -818,6 +911,19 @@ cudaError_t launch_router_logits(const moe_config& c, const void* x, const float
     }
     return cudaGetLastError();
   }
+  if (c.E % 32 == 0 && c.d % 16 == 0) {
+    // L[T][E] = x[T][d] . Wr[d][E], register-tiled fp32 FMA
+    if (c.E % 128 == 0) {
+      dim3 grid(c.E / 128, (c.T + 127) / 128, 1);
+      router_logits_sgemm_kernel<128><<<grid, 256, 0, s>>>(static_cast<const bf16*>(x), Wr, L,
+                                                           c.T, c.d, c.E);
+    } else {
+      dim3 grid((c.E + 63) / 64, (c.T + 127) / 128, 1);
+      router_logits_sgemm_kernel<64><<<grid, 256, 0, s>>>(static_cast<const bf16*>(x), Wr, L,
+                                                          c.T, c.d, c.E);
+    }
+    return cudaGetLastError();
+  }
   // L[T][E] = x[T][d] . Wr[d][E]
   dim3 grid((c.E + 63) / 64, (c.T + 63) / 64, 1);
   simt_gemm_kernel<bf16><<<grid, 256, 0, s>>>(static_cast<const bf16*>(x), c.d, 1, Wr, c.E, 1,
@@ -871,6 +977,11 @@ cudaError_t launch_router_dw(const moe_config& c, const void* x, const float* dL
                                                part, c.d, c.E, c.T, kps);
   const int n = c.d * c.E;
   sum_splits_kernel<<<(n + 31) / 32, 256, 0, s>>>(part, dWr, n, splits);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sum_splits(const float* part, float* out, int n, int splits, cudaStream_t s) {
+  sum_splits_kernel<<<(n + 31) / 32, 256, 0, s>>>(part, out, n, splits);
   return cudaGetLastError();
 }
 

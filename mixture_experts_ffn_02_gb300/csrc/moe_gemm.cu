@@ -53,6 +53,7 @@ struct Params {
   int Mdw;
   int n_tiles;
   int m_tiles_dw;
+  int a_mod;                   // A's K (GK_DOWN) or row (GK_DW) coordinate is taken mod a_mod
   void* out0;        // bf16, or fp32 when out_f32 (GK_DOWN, GK_DX)
   int ld0;
   int out_f32;
@@ -137,14 +138,15 @@ __device__ __forceinline__ void fail(Shared& sh, int* status) {
 template <int KIND>
 __device__ __forceinline__ void issue_loads(const Tile& t, int kb, uint32_t sa, uint32_t sb,
                                             uint32_t bar, const CUtensorMap* tmA,
-                                            const CUtensorMap* tmB) {
+                                            const CUtensorMap* tmB, int a_mod) {
   const int k0 = t.kbeg + kb * BK;
+  const int ka = a_mod ? k0 % a_mod : k0;   // A coordinate along K (repeated A)
   if (KIND == GK_GATE_UP) {
     tma_load_2d(sa, tmA, bar, k0, t.m0);
     tma_load_4d(sb, tmB, bar, k0, t.n0, 0, t.e);
     tma_load_4d(sb + B_BYTES / 2, tmB, bar, k0, t.n0, 1, t.e);
   } else if (KIND == GK_DOWN) {
-    tma_load_2d(sa, tmA, bar, k0, t.m0);
+    tma_load_2d(sa, tmA, bar, ka, t.m0);
     tma_load_3d(sb, tmB, bar, k0, t.n0, t.e);
     tma_load_3d(sb + B_BYTES / 2, tmB, bar, k0, t.n0 + 128, t.e);
   } else if (KIND == GK_DH || KIND == GK_DX) {
@@ -153,7 +155,7 @@ __device__ __forceinline__ void issue_loads(const Tile& t, int kb, uint32_t sa, 
     for (int i = 0; i < 4; ++i) tma_load_3d(sb + i * 8192, tmB, bar, t.n0 + 64 * i, k0, t.e);
   } else {  // GK_DW
 #pragma unroll
-    for (int i = 0; i < 2; ++i) tma_load_2d(sa + i * 8192, tmA, bar, t.m0 + 64 * i, k0);
+    for (int i = 0; i < 2; ++i) tma_load_2d(sa + i * 8192, tmA, bar, t.m0 + 64 * i, ka);
 #pragma unroll
     for (int i = 0; i < 4; ++i) tma_load_2d(sb + i * 8192, tmB, bar, t.n0 + 64 * i, k0);
   }
@@ -167,11 +169,13 @@ __device__ __forceinline__ float silu_f(float a) { return a / (1.f + __expf(-a))
 template <int KIND>
 __device__ __forceinline__ void store_chunk(const Params& p, const Tile& t, int row, int col,
                                             const uint32_t* r, bool no_acc) {
-  if (KIND != GK_DW && p.out_f32) {
+  if (p.out_f32) {
     float* op = static_cast<float*>(p.out0) + (size_t)row * p.ld0 + col;
+    if (KIND == GK_DW) op += (size_t)t.e * p.Mdw * p.ld0;
 #pragma unroll
     for (int q = 0; q < 8; ++q)
-      st_v4(op + q * 4, make_uint4(r[q * 4 + 0], r[q * 4 + 1], r[q * 4 + 2], r[q * 4 + 3]));
+      st_v4(op + q * 4, no_acc ? make_uint4(0, 0, 0, 0)
+                               : make_uint4(r[q * 4 + 0], r[q * 4 + 1], r[q * 4 + 2], r[q * 4 + 3]));
   } else {
     bf16* op = static_cast<bf16*>(p.out0) + (size_t)row * p.ld0 + col;
     if (KIND == GK_DW) op += (size_t)t.e * p.Mdw * p.ld0;
@@ -354,7 +358,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         const uint32_t fb = smem_u32(&sh.full[stage]);
         mbar_arrive_expect_tx(fb, STAGE_BYTES);
         const uint32_t sa = base + stage * STAGE_BYTES;
-        issue_loads<KIND>(t, kb, sa, sa + A_BYTES, fb, &tmA, &tmB);
+        issue_loads<KIND>(t, kb, sa, sa + A_BYTES, fb, &tmA, &tmB, p.a_mod);
         pending_parity[stage] = (int)phase;
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
@@ -514,6 +518,7 @@ cudaError_t launch_gemm(const GemmCall& g, cudaStream_t s) {
   p.out0 = g.out0;
   p.ld0 = g.ld0;
   p.out_f32 = g.out_f32;
+  p.a_mod = g.a_mod;
   p.out1 = static_cast<bf16*>(g.out1);
   p.ld1 = g.ld1;
   p.aux_in = static_cast<const bf16*>(g.aux_in);
@@ -535,8 +540,10 @@ cudaError_t launch_gemm(const GemmCall& g, cudaStream_t s) {
       break;
     }
     case GK_DOWN: {
-      // A: [rows][K=H] ; B: W_down [E][N=d][K=H] -> dims {K, N, E}
-      uint64_t da[2] = {(uint64_t)g.K, rows}, sa[1] = {(uint64_t)g.lda * 2};
+      // A: [rows][K=H] (or [rows][a_mod], read K/a_mod times) ; B: W_down [E][N=d][K=H]
+      // -> dims {K, N, E}
+      uint64_t da[2] = {(uint64_t)(g.a_mod ? g.a_mod : g.K), rows},
+               sa[1] = {(uint64_t)g.lda * 2};
       uint32_t ba[2] = {64, 128};
       uint64_t db[3] = {(uint64_t)g.K, (uint64_t)g.N, (uint64_t)g.E};
       uint64_t sb[2] = {(uint64_t)g.K * 2, (uint64_t)g.N * g.K * 2};
@@ -558,8 +565,9 @@ cudaError_t launch_gemm(const GemmCall& g, cudaStream_t s) {
       break;
     }
     case GK_DW: {
-      // A: [rows][Mdw] (M contiguous) ; B: [rows][N] (N contiguous)
-      uint64_t da[2] = {(uint64_t)g.Mdw, rows}, sa[1] = {(uint64_t)g.lda * 2};
+      // A: [a_rows][Mdw] (M contiguous; rows read mod a_mod) ; B: [rows][N] (N contiguous)
+      uint64_t da[2] = {(uint64_t)g.Mdw, (uint64_t)(g.a_rows ? g.a_rows : g.rows)},
+               sa[1] = {(uint64_t)g.lda * 2};
       uint32_t ba[2] = {64, 64};
       uint64_t db[2] = {(uint64_t)g.N, rows}, sb[1] = {(uint64_t)g.N * 2};
       uint32_t bb[2] = {64, 64};

@@ -41,6 +41,11 @@ struct WsLayout {
   size_t dxs;           // [T][d] fp32
   size_t dxr;           // [T][d] fp32 (router input gradient, large E)
   size_t dwr_part;      // [splits][d][E] fp32
+  // tensor-core router (router_tc_path)
+  size_t wr2;           // [d][3E] bf16
+  size_t dl3;           // [T][3E] bf16
+  size_t dl2;           // [2 Tp][E] bf16
+  size_t goff;          // [G+1] int32 split-K row groups
   size_t total;
   int route_blocks;
   int perm_blocks;
@@ -82,6 +87,14 @@ cudaError_t launch_router_dx(const moe_config& c, const float* d_logits, const f
 cudaError_t launch_router_dw(const moe_config& c, const void* x, const float* d_logits,
                              float* dWr, float* part, int splits, cudaStream_t s);
 bool router_small_path(const moe_config& c);
+// Router backward products on the tensor cores (E a multiple of 32 beyond the
+// small path): moe_router_tc.cu.
+bool router_tc_path(const moe_config& c);
+void router_tc_sizes(const moe_config& c, int* Tp, int* G, int* chunk);
+cudaError_t launch_router_bwd_tc(const moe_config& c, const void* x, const float* dL,
+                                 const float* Wr, float* dxr, float* dWr, void* wr2, void* dl3,
+                                 void* dl2, int* goff, float* part, int* status, cudaStream_t s);
+cudaError_t launch_sum_splits(const float* part, float* out, int n, int splits, cudaStream_t s);
 int router_dw_small_parts(const moe_config& c);   // partial slices of the small-E dW_r
 
 // ---- tcgen05 grouped GEMMs (moe_gemm.cu) -----------------------------------
@@ -113,7 +126,10 @@ struct GemmCall {
   // Outputs
   void* out0;                  // main output
   int ld0;
-  int out_f32;                 // GK_DOWN / GK_DX: store fp32 instead of bf16
+  int out_f32;                 // GK_DOWN / GK_DX / GK_DW: store fp32 instead of bf16
+  int a_mod;                   // GK_DOWN: A's K coordinate mod a_mod (A repeated along K);
+                               // GK_DW: A's row coordinate mod a_mod
+  int a_rows;                  // GK_DW: rows of A when they differ from B's (0 = rows)
   void* out1;                  // GK_GATE_UP: ab save (or NULL)
   int ld1;
   const void* aux_in;          // GK_DH: ab (a|b) saved by the forward

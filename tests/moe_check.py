@@ -142,7 +142,7 @@ def routing_margin(key, k):
 
 def logit_error_bound(x, Wr):
     """A bound on |fp32 logits - exact| for any summation order:
-    2 * d * eps32 * sum_c |x_c W_ce|  (plus the final rounding)."""
+    (2d + 2) * eps32 * sum_c |x_c W_ce|."""
     xa = np.abs(np.asarray(x, dtype=np.float64))
     wa = np.abs(np.asarray(Wr, dtype=np.float64))
     d = xa.shape[1]
