@@ -18,6 +18,7 @@
 // Row-grouped kinds read the expert of each 128-row block from the padded
 // segment offsets on the device, so no host synchronisation is needed.
 #include <cstdio>
+#include <cstring>
 #include <mutex>
 
 #include "moe_common.cuh"
@@ -41,7 +42,10 @@ constexpr int EPI_THREADS = 256;         // two warpgroups split each tile's col
 constexpr int EPI_WARP0 = 4;
 constexpr uint64_t WAIT_NS = 2000000000ull;  // bounded waits give up after 2 s
 constexpr uint64_t DRAIN_NS = 200000000ull;
-constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 2048;
+constexpr int SLAB_BYTES = 32 * 128;     // per epilogue warp: 32 rows x 128 bytes
+constexpr int EPI_WARPS = EPI_THREADS / 32;
+constexpr size_t SMEM_BYTES =
+    1024 + (size_t)STAGES * STAGE_BYTES + (size_t)EPI_WARPS * SLAB_BYTES + 2048;
 
 struct Params {
   const int32_t* row_offsets;  // routed: [E+1] padded offsets; dense: NULL
@@ -164,136 +168,178 @@ __device__ __forceinline__ void issue_loads(const Tile& t, int kb, uint32_t sa, 
 // ------------------------------------------------------------------ epilogue
 __device__ __forceinline__ float silu_f(float a) { return a / (1.f + __expf(-a)); }
 
-// Stores one 32-column chunk of a finished accumulator row (all kinds but
-// GK_GATE_UP and GK_DH).
-template <int KIND>
-__device__ __forceinline__ void store_chunk(const Params& p, const Tile& t, int row, int col,
-                                            const uint32_t* r, bool no_acc) {
-  if (p.out_f32) {
-    float* op = static_cast<float*>(p.out0) + (size_t)row * p.ld0 + col;
-    if (KIND == GK_DW) op += (size_t)t.e * p.Mdw * p.ld0;
-#pragma unroll
-    for (int q = 0; q < 8; ++q)
-      st_v4(op + q * 4, no_acc ? make_uint4(0, 0, 0, 0)
-                               : make_uint4(r[q * 4 + 0], r[q * 4 + 1], r[q * 4 + 2], r[q * 4 + 3]));
-  } else {
-    bf16* op = static_cast<bf16*>(p.out0) + (size_t)row * p.ld0 + col;
-    if (KIND == GK_DW) op += (size_t)t.e * p.Mdw * p.ld0;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      float v[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) v[u] = no_acc ? 0.f : __uint_as_float(r[q * 8 + u]);
-      st_v4(op + q * 8, pack8(v));
-    }
+// One epilogue warp's staging slab: 32 rows x 128 bytes in shared memory,
+// 128-byte swizzled (16-byte chunk c of row r at chunk position c ^ (r % 8)),
+// which is the layout of the output tensor maps' boxes: the warp fills it from
+// registers without bank conflicts and one TMA store writes it out as whole
+// 128-byte lines.
+struct Slab {
+  unsigned char* gen;
+  uint32_t addr;
+};
+
+__device__ __forceinline__ void slab_put(const Slab& s, int lane, int c, const uint4& v) {
+  *reinterpret_cast<uint4*>(s.gen + lane * 128 + ((c ^ (lane & 7)) << 4)) = v;
+}
+// Before the slab is refilled, the previous store must have read it.
+__device__ __forceinline__ void slab_acquire(int lane) {
+  if (lane == 0) bulk_wait_read0();
+  __syncwarp();
+}
+__device__ __forceinline__ void slab_store(const Slab& s, const CUtensorMap* m, int lane, int x,
+                                           int y, int z, bool three_d) {
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    if (three_d) tma_store_3d(m, s.addr, x, y, z);
+    else tma_store_2d(m, s.addr, x, y);
+    bulk_commit();
   }
 }
 
-// Epilogue of one tile for one thread: TMEM lane = its row, and the column
-// half `half` of the tile (two warpgroups split the columns).
+// Epilogue of one tile for one warp: TMEM lanes (rows) q*32 .. q*32+31 and
+// the column half `half` of the tile (two warpgroups split the columns).
+// Rows past the end of the output (dense tails, dW rows past M) are clipped
+// by the TMA store; a slab starting past the end is skipped.
 template <int KIND>
 __device__ __forceinline__ void epilogue_tile(const Params& p, const Tile& t, uint32_t tacc,
-                                              int row_in_tile, int half) {
-  const int row = t.m0 + row_in_tile;
-  bool row_ok;
-  if (KIND == GK_DW) row_ok = row < p.Mdw;
-  else row_ok = p.row_offsets ? true : row < p.rows;
-  const bool no_acc = t.ksteps == 0;
+                                              int q, int lane, int half, const Slab& slab,
+                                              const CUtensorMap* tmO0, const CUtensorMap* tmO1) {
+  const int row0 = t.m0 + q * 32;
+  const int row = row0 + lane;
+  int row_end;
+  if (KIND == GK_DW) row_end = p.Mdw;
+  else row_end = p.row_offsets ? 0x7fffffff : p.rows;
+  if (row0 >= row_end) return;
+  const bool row_in = row < row_end;
   uint32_t r0[32], r1[32];
   if (KIND == GK_GATE_UP) {
-    const bool zero_row = p.valid && row_ok && p.valid[row] == 0;
-    constexpr int NCH = BN / 2 / 32 / 2;          // chunks per half
+    const int col = t.n0 + half * 64;              // 64 hidden units per half
+    if (col >= p.H) return;
+    const bool zero_row = p.valid && row_in && p.valid[row] == 0;
+    slab_acquire(lane);
 #pragma unroll 1
-    for (int i = 0; i < NCH; ++i) {
-      const int cb = half * NCH + i;
+    for (int c = 0; c < 2; ++c) {                  // h = silu(a) * b
+      const int cb = half * 2 + c;
       __syncwarp();
       tmem_ld32(tacc + cb * 32, r0);
       tmem_ld32(tacc + BN / 2 + cb * 32, r1);
       tmem_ld_wait();
-      const int col = t.n0 + cb * 32;
-      if (row_ok && col < p.H) {
-        uint4 hv[4], av[4], bv[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          float hf[8], af[8], bf[8];
+      for (int qq = 0; qq < 4; ++qq) {
+        float hf[8];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            float a = __uint_as_float(r0[q * 8 + u]);
-            float b = __uint_as_float(r1[q * 8 + u]);
-            if (zero_row) { a = 0.f; b = 0.f; }
-            af[u] = a; bf[u] = b;
-            hf[u] = silu_f(a) * b;
+        for (int u = 0; u < 8; ++u) {
+          const float a = zero_row ? 0.f : __uint_as_float(r0[qq * 8 + u]);
+          const float b = zero_row ? 0.f : __uint_as_float(r1[qq * 8 + u]);
+          hf[u] = silu_f(a) * b;
+        }
+        slab_put(slab, lane, c * 4 + qq, pack8(hf));
+      }
+    }
+    slab_store(slab, tmO0, lane, col, row0, 0, false);
+    if (p.out1) {
+#pragma unroll 1
+      for (int which = 0; which < 2; ++which) {    // saved a, then b
+        slab_acquire(lane);
+#pragma unroll 1
+        for (int c = 0; c < 2; ++c) {
+          __syncwarp();
+          tmem_ld32(tacc + which * (BN / 2) + (half * 2 + c) * 32, r0);
+          tmem_ld_wait();
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq) {
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = zero_row ? 0.f : __uint_as_float(r0[qq * 8 + u]);
+            slab_put(slab, lane, c * 4 + qq, pack8(v));
           }
-          hv[q] = pack8(hf); av[q] = pack8(af); bv[q] = pack8(bf);
         }
-        bf16* hp = static_cast<bf16*>(p.out0) + (size_t)row * p.ld0 + col;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) st_v4(hp + q * 8, hv[q]);
-        if (p.out1) {
-          bf16* ap = p.out1 + (size_t)row * p.ld1 + col;
-          bf16* bp = ap + p.H;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) { st_v4(ap + q * 8, av[q]); st_v4(bp + q * 8, bv[q]); }
-        }
+        slab_store(slab, tmO1, lane, col + which * p.H, row0, 0, false);
       }
     }
   } else if (KIND == GK_DH) {
-    // dH -> (da, db) with the saved pre-activations a, b.  The a|b loads of
-    // the next chunk are issued before the current chunk is processed.
-    constexpr int NCH = BN / 32 / 2;
-    uint4 abuf[2][4], bbuf[2][4];
-    auto load_ab = [&](int i, uint4 (&ab4)[4], uint4 (&bb4)[4]) {
-      const int col = t.n0 + (half * NCH + i) * 32;
-      if (row_ok && col < p.N) {
-        const bf16* ap = p.aux_in + (size_t)row * p.ld_aux + col;
-        const bf16* bp = ap + p.H;
+    // dH -> (da, db) with the saved pre-activations a, b; two 64-column boxes
+#pragma unroll 1
+    for (int bx = 0; bx < 2; ++bx) {
+      const int col = t.n0 + half * 128 + bx * 64;
+      if (col >= p.N) break;
+      const bf16* ap = p.aux_in + (size_t)row * p.ld_aux + col;
+#pragma unroll 1
+      for (int which = 0; which < 2; ++which) {    // da, then db
+        slab_acquire(lane);
+#pragma unroll 1
+        for (int c = 0; c < 2; ++c) {
+          uint4 av[4], bv[4];                      // saved a, b of this row's 32 columns
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          ab4[q] = *reinterpret_cast<const uint4*>(ap + q * 8);
-          bb4[q] = *reinterpret_cast<const uint4*>(bp + q * 8);
-        }
-      }
-    };
-    load_ab(0, abuf[0], bbuf[0]);
-#pragma unroll
-    for (int i = 0; i < NCH; ++i) {
-      if (i + 1 < NCH) load_ab(i + 1, abuf[(i + 1) & 1], bbuf[(i + 1) & 1]);
-      const int cb = half * NCH + i;
-      __syncwarp();
-      tmem_ld32(tacc + cb * 32, r0);
-      tmem_ld_wait();
-      const int col = t.n0 + cb * 32;
-      if (row_ok && col < p.N) {
-        bf16* dap = static_cast<bf16*>(p.out0) + (size_t)row * p.ld0 + col;
-        bf16* dbp = dap + p.H;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          float a8[8], b8[8], da[8], db[8];
-          unpack8(abuf[i & 1][q], a8);
-          unpack8(bbuf[i & 1][q], b8);
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const float dh = __uint_as_float(r0[q * 8 + u]);
-            const float a = a8[u], b = b8[u];
-            const float sg = 1.f / (1.f + __expf(-a));
-            da[u] = dh * b * sg * (1.f + a * (1.f - sg));
-            db[u] = dh * (a * sg);
+          for (int i = 0; i < 4; ++i) {
+            av[i] = row_in ? *reinterpret_cast<const uint4*>(ap + c * 32 + i * 8)
+                           : make_uint4(0, 0, 0, 0);
+            bv[i] = row_in ? *reinterpret_cast<const uint4*>(ap + p.H + c * 32 + i * 8)
+                           : make_uint4(0, 0, 0, 0);
           }
-          st_v4(dap + q * 8, pack8(da));
-          st_v4(dbp + q * 8, pack8(db));
+          __syncwarp();
+          tmem_ld32(tacc + (half * 4 + bx * 2 + c) * 32, r0);
+          tmem_ld_wait();
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq) {
+            float a8[8], b8[8], o[8];
+            unpack8(av[qq], a8);
+            unpack8(bv[qq], b8);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const float dh = __uint_as_float(r0[qq * 8 + u]);
+              const float a = a8[u], b = b8[u];
+              const float sg = 1.f / (1.f + __expf(-a));
+              o[u] = which == 0 ? dh * b * sg * (1.f + a * (1.f - sg)) : dh * (a * sg);
+            }
+            slab_put(slab, lane, c * 4 + qq, pack8(o));
+          }
         }
+        slab_store(slab, tmO0, lane, col + which * p.H, row0, 0, false);
       }
     }
   } else {
-    constexpr int NCH = BN / 32 / 2;
+    // GK_DOWN, GK_DX, GK_DW: 128 columns per half
+    const bool no_acc = t.ksteps == 0;
+    const bool three_d = KIND == GK_DW;
+    if (p.out_f32) {
 #pragma unroll 1
-    for (int i = 0; i < NCH; ++i) {
-      const int cb = half * NCH + i;
-      __syncwarp();
-      tmem_ld32(tacc + cb * 32, r0);
-      tmem_ld_wait();
-      const int col = t.n0 + cb * 32;
-      if (row_ok && col < p.N) store_chunk<KIND>(p, t, row, col, r0, no_acc);
+      for (int c = 0; c < 4; ++c) {                // one 32-column fp32 box per chunk
+        const int col = t.n0 + half * 128 + c * 32;
+        if (col >= p.N) break;
+        slab_acquire(lane);
+        __syncwarp();
+        tmem_ld32(tacc + (half * 4 + c) * 32, r0);
+        tmem_ld_wait();
+#pragma unroll
+        for (int qq = 0; qq < 8; ++qq)
+          slab_put(slab, lane, qq,
+                   no_acc ? make_uint4(0, 0, 0, 0)
+                          : make_uint4(r0[qq * 4], r0[qq * 4 + 1], r0[qq * 4 + 2], r0[qq * 4 + 3]));
+        slab_store(slab, tmO0, lane, col, row0, t.e, three_d);
+      }
+    } else {
+#pragma unroll 1
+      for (int bx = 0; bx < 2; ++bx) {             // one 64-column bf16 box per two chunks
+        const int col = t.n0 + half * 128 + bx * 64;
+        if (col >= p.N) break;
+        slab_acquire(lane);
+#pragma unroll 1
+        for (int c = 0; c < 2; ++c) {
+          __syncwarp();
+          tmem_ld32(tacc + (half * 4 + bx * 2 + c) * 32, r0);
+          tmem_ld_wait();
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq) {
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = no_acc ? 0.f : __uint_as_float(r0[qq * 8 + u]);
+            slab_put(slab, lane, c * 4 + qq, pack8(v));
+          }
+        }
+        slab_store(slab, tmO0, lane, col, row0, t.e, three_d);
+      }
     }
   }
 }
@@ -302,13 +348,16 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const Tile& t, ui
 template <int KIND>
 __global__ void __launch_bounds__(THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                    const __grid_constant__ CUtensorMap tmB, const Params p) {
+                    const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmO0,
+                    const __grid_constant__ CUtensorMap tmO1, const Params p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // stage buffers must start on a 1024-byte boundary (128-byte swizzle atoms)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   unsigned char* gen_base = smem_raw + (base - raw);
-  Shared& sh = *reinterpret_cast<Shared*>(gen_base + (size_t)STAGES * STAGE_BYTES);
+  unsigned char* slabs = gen_base + (size_t)STAGES * STAGE_BYTES;   // 1024-byte aligned
+  Shared& sh = *reinterpret_cast<Shared*>(slabs + (size_t)EPI_WARPS * SLAB_BYTES);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -326,6 +375,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmO0);
+    if (p.out1) tma_prefetch_desc(&tmO1);
   }
   if (p.row_offsets)
     for (int e = threadIdx.x; e <= p.E; e += blockDim.x) sh.roff[e] = p.row_offsets[e];
@@ -424,7 +475,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     // ---------------- epilogue warps: TMEM lanes 32*(warp%4) .. +31
     const int q = warp & 3;                       // TMEM lane quadrant of this warp
     const int half = (warp - EPI_WARP0) >> 2;     // column half of the tile
-    const int row_in_tile = q * 32 + lane;
+    Slab slab;
+    slab.gen = slabs + (size_t)(warp - EPI_WARP0) * SLAB_BYTES;
+    slab.addr = smem_u32(slab.gen);
     int it = 0;
     for (int idx = blockIdx.x; idx < ntiles; idx += gridDim.x, ++it) {
       const Tile t = get_tile<KIND>(p, sh, idx);
@@ -436,10 +489,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       }
       tc_fence_after();
       const uint32_t tacc = tmem + ((uint32_t)(q * 32) << 16) + acc * BN;
-      epilogue_tile<KIND>(p, t, tacc, row_in_tile, half);
+      epilogue_tile<KIND>(p, t, tacc, q, lane, half, slab, &tmO0, &tmO1);
       tc_fence_before();
       mbar_arrive(smem_u32(&sh.tempty[acc]));
     }
+    // every store issued from this warp's slab completes before exit
+    if (lane == 0) bulk_wait0();
+    __syncwarp();
   }
   tc_fence_before();
   __syncthreads();
@@ -472,22 +528,23 @@ EncodeTiledFn encode_fn() {
 // bf16 tensor map, 128-byte swizzle, zero fill out of bounds.
 // dims/strides: innermost first; strides in bytes for dims 1..rank-1.
 bool make_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims,
-              const uint64_t* strides, const uint32_t* box) {
+              const uint64_t* strides, const uint32_t* box,
+              CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t gd[5], gs[4];
   cuuint32_t bx[5], es[5];
   for (int i = 0; i < rank; ++i) { gd[i] = dims[i]; bx[i] = box[i]; es[i] = 1; }
   for (int i = 0; i < rank - 1; ++i) gs[i] = strides[i];
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(ptr),
+  CUresult r = fn(m, dtype, (cuuint32_t)rank, const_cast<void*>(ptr),
                   gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
 template <int KIND>
-cudaError_t launch_kind(const CUtensorMap& a, const CUtensorMap& b, const Params& p,
-                        int grid, cudaStream_t s) {
+cudaError_t launch_kind(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o0,
+                        const CUtensorMap& o1, const Params& p, int grid, cudaStream_t s) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
@@ -496,14 +553,15 @@ cudaError_t launch_kind(const CUtensorMap& a, const CUtensorMap& b, const Params
                                     (int)SMEM_BYTES);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  grouped_gemm_kernel<KIND><<<grid, THREADS, SMEM_BYTES, s>>>(a, b, p);
+  grouped_gemm_kernel<KIND><<<grid, THREADS, SMEM_BYTES, s>>>(a, b, o0, o1, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_gemm(const GemmCall& g, cudaStream_t s) {
-  static_assert(sizeof(Shared) + 1024 <= 2048 + 1024, "shared bookkeeping too large");
+  static_assert(sizeof(Shared) <= 2048, "shared bookkeeping too large");
+  static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB opt-in shared memory of a block");
   DeviceInfo di;
   if (device_info(&di) != MOE_OK) return cudaErrorUnknown;
   CUtensorMap ta, tb;
@@ -578,13 +636,55 @@ cudaError_t launch_gemm(const GemmCall& g, cudaStream_t s) {
     }
   }
   if (!ok) return cudaErrorInvalidValue;
+  // Output maps: 128-byte swizzled boxes of 128 bytes x 32 rows (one epilogue
+  // warp's slab).  Rows and columns past the tensor are clipped by the store.
+  CUtensorMap to0, to1;
+  memset(&to0, 0, sizeof(to0));
+  memset(&to1, 0, sizeof(to1));
+  const int es = g.out_f32 ? 4 : 2;
+  const CUtensorMapDataType ot =
+      g.out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const uint32_t inner = 128 / es;
+  switch (g.kind) {
+    case GK_GATE_UP: {
+      uint64_t d0[2] = {(uint64_t)g.H, rows}, s0[1] = {(uint64_t)g.ld0 * 2};
+      uint32_t b0[2] = {64, 32};
+      ok = make_map(&to0, g.out0, 2, d0, s0, b0);
+      if (ok && g.out1) {
+        uint64_t d1[2] = {(uint64_t)2 * g.H, rows}, s1[1] = {(uint64_t)g.ld1 * 2};
+        ok = make_map(&to1, g.out1, 2, d1, s1, b0);
+      }
+      break;
+    }
+    case GK_DH: {
+      uint64_t d0[2] = {(uint64_t)2 * g.H, rows}, s0[1] = {(uint64_t)g.ld0 * 2};
+      uint32_t b0[2] = {64, 32};
+      ok = make_map(&to0, g.out0, 2, d0, s0, b0);
+      break;
+    }
+    case GK_DOWN:
+    case GK_DX: {
+      uint64_t d0[2] = {(uint64_t)g.N, rows}, s0[1] = {(uint64_t)g.ld0 * es};
+      uint32_t b0[2] = {inner, 32};
+      ok = make_map(&to0, g.out0, 2, d0, s0, b0, ot);
+      break;
+    }
+    case GK_DW: {
+      uint64_t d0[3] = {(uint64_t)g.N, (uint64_t)g.Mdw, (uint64_t)g.E};
+      uint64_t s0[2] = {(uint64_t)g.ld0 * es, (uint64_t)g.Mdw * g.ld0 * es};
+      uint32_t b0[3] = {inner, 32, 1};
+      ok = make_map(&to0, g.out0, 3, d0, s0, b0, ot);
+      break;
+    }
+  }
+  if (!ok) return cudaErrorInvalidValue;
   const int grid = di.num_sms;
   switch (g.kind) {
-    case GK_GATE_UP: return launch_kind<GK_GATE_UP>(ta, tb, p, grid, s);
-    case GK_DOWN: return launch_kind<GK_DOWN>(ta, tb, p, grid, s);
-    case GK_DH: return launch_kind<GK_DH>(ta, tb, p, grid, s);
-    case GK_DX: return launch_kind<GK_DX>(ta, tb, p, grid, s);
-    case GK_DW: return launch_kind<GK_DW>(ta, tb, p, grid, s);
+    case GK_GATE_UP: return launch_kind<GK_GATE_UP>(ta, tb, to0, to1, p, grid, s);
+    case GK_DOWN: return launch_kind<GK_DOWN>(ta, tb, to0, to1, p, grid, s);
+    case GK_DH: return launch_kind<GK_DH>(ta, tb, to0, to1, p, grid, s);
+    case GK_DX: return launch_kind<GK_DX>(ta, tb, to0, to1, p, grid, s);
+    case GK_DW: return launch_kind<GK_DW>(ta, tb, to0, to1, p, grid, s);
   }
   return cudaErrorInvalidValue;
 }
