@@ -279,15 +279,24 @@ def run_ours(args):
 
 
 def load_traffic(cfg):
-    """dram bytes per launch of the gate/up kernel from the committed ncu
-    summary, if one matches this workload (else null)."""
+    """DRAM bytes per launch of the gate/up kernel from the committed ncu
+    summary for this workload, or None if there is none or if the GEMM source
+    changed since the counters were taken."""
+    import hashlib
     p = os.path.join(ROOT, "profiles", f"gate_up_traffic_cfg{cfg}.json")
-    if os.path.exists(p):
-        try:
-            return json.load(open(p)).get("dram_bytes_per_launch")
-        except Exception:
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+        h = hashlib.sha256()
+        for f in ("moe_gemm.cu", "moe_common.cuh"):
+            h.update(open(os.path.join(ROOT, "mixture_experts_ffn_02_gb300", "csrc", f),
+                          "rb").read())
+        if h.hexdigest() != d.get("source_sha256"):
             return None
-    return None
+        return d.get("dram_bytes_per_launch")
+    except Exception:
+        return None
 
 
 def run_e2e(args, s, inp, lay, training, local):
