@@ -129,6 +129,18 @@ def launches_per_step(s, fwd_only):
     return fwd if fwd_only else fwd + bwd
 
 
+def aggregate_ranks(ms_local, tokens_per_step, steps, world, dist=None, device="cpu"):
+    """Whole-job throughput of independent replicas: the timed region's
+    length is the maximum over ranks; value = tokens of all ranks / that time.
+    Returns (ms_max, tokens_per_second)."""
+    import torch
+    t = torch.tensor([float(ms_local)], dtype=torch.float64, device=device)
+    if dist is not None and world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+    return ms_max, tokens_per_step * steps * world / (ms_max / 1e3)
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -203,13 +215,9 @@ def run_ours(args):
         raise RuntimeError(f"device status {status} in the timed region")
     ms = sum(a.elapsed_time(b) for a, b in ev)
     gu_ms = sum(a.elapsed_time(b) for a, b in gu_ev) / len(gu_ev)
-    t = torch.tensor([ms], device=f"cuda:{local}")
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max = float(t.item())
+    ms_max, value = aggregate_ranks(ms, s.T, args.steps, world,
+                                    dist if world > 1 else None, f"cuda:{local}")
     ms_per_step = ms_max / args.steps
-    tokens_all = s.T * args.steps * world
-    value = tokens_all / (ms_max / 1e3)
 
     # fwd-only rate of the same layer (reported beside the fwd+bwd headline)
     fwd_rate = None

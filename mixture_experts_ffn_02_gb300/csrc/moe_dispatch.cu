@@ -465,17 +465,45 @@ route_kernel(const float* __restrict__ L, const float* __restrict__ bias,
   __syncthreads();
   if (ticket_s != (int)gridDim.x - 1) return;
 
-  // last block: totals over blocks in block order
+  // last block: totals over all blocks.  The blocks are split over the
+  // threads in a fixed partition and the partial sums are combined in
+  // partition order, so the result does not depend on scheduling.
   __threadfence();
-  int Tr = 0;
-  for (int b = 0; b < (int)gridDim.x; ++b) Tr += __ldcg(blk_treal + b);
+  __shared__ int fin_t[kThreads];
+  __shared__ int fin_c[kThreads];
+  __shared__ float fin_p[kThreads];
+  const int nb = gridDim.x;
+  int tr = 0;
+  for (int b = threadIdx.x; b < nb; b += blockDim.x) tr += __ldcg(blk_treal + b);
+  fin_t[threadIdx.x] = tr;
+  const int Gp = blockDim.x / E;                 // threads per expert (E <= 256)
+  const int ge = threadIdx.x % E, gg = threadIdx.x / E;
+  if (gg < Gp) {
+    int c = 0;
+    float ps = 0.f;
+#pragma unroll 4
+    for (int b = gg; b < nb; b += Gp) {
+      c += __ldcg(blk_cnt + (size_t)b * E + ge);
+      ps += __ldcg(blk_psum + (size_t)b * E + ge);
+    }
+    fin_c[gg * E + ge] = c;
+    fin_p[gg * E + ge] = ps;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int t = 0;
+    for (int i = 0; i < (int)blockDim.x; ++i) t += fin_t[i];
+    treal_s = t;
+  }
+  __syncthreads();
+  const int Tr = treal_s;
   float part = 0.f;
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int c = 0;
     float ps = 0.f;
-    for (int b = 0; b < (int)gridDim.x; ++b) {
-      c += __ldcg(blk_cnt + (size_t)b * E + e);
-      ps += __ldcg(blk_psum + (size_t)b * E + e);
+    for (int g2 = 0; g2 < Gp; ++g2) {
+      c += fin_c[g2 * E + e];
+      ps += fin_p[g2 * E + e];
     }
     float fe = Tr > 0 ? (float)c / (float)((long long)k * Tr) : 0.f;
     float pe = Tr > 0 ? ps / (float)Tr : 0.f;
@@ -515,41 +543,59 @@ perm_hist_kernel(const int32_t* __restrict__ topk, int T, int k, int E,
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[(size_t)blockIdx.x * E + e] = h[e];
 }
 
-__global__ void __launch_bounds__(kThreads)
+// Counts, offsets, padded row offsets and, for every (block, expert), the
+// first row that block writes for that expert.  Each expert's blocks are split
+// into contiguous ranges over kScanThreads / E threads: range sums, an
+// exclusive prefix over the ranges, then each thread walks its own range.
+constexpr int kScanThreads = 1024;
+__global__ void __launch_bounds__(kScanThreads)
 perm_scan_kernel(const int* __restrict__ hist, int nblk, int E, int32_t* __restrict__ counts,
                  int32_t* __restrict__ offsets, int32_t* __restrict__ row_offsets,
                  int* __restrict__ base) {
+  __shared__ int part[kScanThreads];
   __shared__ int cnt_s[257];
   __shared__ int off_s[257];
   __shared__ int roff_s[257];
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int run = 0;
-    for (int b = 0; b < nblk; ++b) {
-      base[(size_t)b * E + e] = run;
-      run += hist[(size_t)b * E + e];
-    }
-    cnt_s[e] = run;
+  const int G = blockDim.x / E;                  // ranges per expert (E <= 256)
+  const int e = threadIdx.x % E, g = threadIdx.x / E;
+  const bool act = g < G;
+  const int b0 = act ? (int)((long long)g * nblk / G) : 0;
+  const int b1 = act ? (int)((long long)(g + 1) * nblk / G) : 0;
+  int local = 0;
+#pragma unroll 4
+  for (int b = b0; b < b1; ++b) local += hist[(size_t)b * E + e];
+  if (act) part[g * E + e] = local;
+  __syncthreads();
+  int pre = 0;
+  if (act) {
+    for (int g2 = 0; g2 < g; ++g2) pre += part[g2 * E + e];
+    if (g == G - 1) cnt_s[e] = pre + local;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
     int o = 0, ro = 0;
-    for (int e = 0; e < E; ++e) {
-      off_s[e] = o;
-      roff_s[e] = ro;
-      o += cnt_s[e];
-      ro += (cnt_s[e] + kRowAlign - 1) / kRowAlign * kRowAlign;
+    for (int x = 0; x < E; ++x) {
+      off_s[x] = o;
+      roff_s[x] = ro;
+      o += cnt_s[x];
+      ro += (cnt_s[x] + kRowAlign - 1) / kRowAlign * kRowAlign;
     }
     off_s[E] = o;
     roff_s[E] = ro;
   }
   __syncthreads();
-  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
-    offsets[e] = off_s[e];
-    row_offsets[e] = roff_s[e];
-    if (e < E) counts[e] = cnt_s[e];
+  for (int x = threadIdx.x; x <= E; x += blockDim.x) {
+    offsets[x] = off_s[x];
+    row_offsets[x] = roff_s[x];
+    if (x < E) counts[x] = cnt_s[x];
   }
-  for (int e = threadIdx.x; e < E; e += blockDim.x)
-    for (int b = 0; b < nblk; ++b) base[(size_t)b * E + e] += roff_s[e];
+  if (act) {
+    int run = roff_s[e] + pre;
+    for (int b = b0; b < b1; ++b) {
+      base[(size_t)b * E + e] = run;
+      run += hist[(size_t)b * E + e];
+    }
+  }
 }
 
 // Ranks each (t, j) pair of the block's token chunk in pair order with one
@@ -1052,7 +1098,8 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* to
   int* status = reinterpret_cast<int*>(ws + w.status);
   const int nblk = w.perm_blocks;
   perm_hist_kernel<<<nblk, kThreads, 0, s>>>(topk, c.T, c.k, c.E, hist, status);
-  perm_scan_kernel<<<1, kThreads, 0, s>>>(hist, nblk, c.E, counts, offsets, row_offsets, base);
+  perm_scan_kernel<<<1, kScanThreads, 0, s>>>(hist, nblk, c.E, counts, offsets, row_offsets,
+                                              base);
   perm_scatter_kernel<<<nblk, kThreads, 0, s>>>(static_cast<const bf16*>(x), topk, c.T, c.d,
                                                 c.k, c.E, base, counts, row_offsets, perm, inv,
                                                 static_cast<bf16*>(x_perm));
