@@ -259,44 +259,49 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const Tile& t, ui
       }
     }
   } else if (KIND == GK_DH) {
-    // dH -> (da, db) with the saved pre-activations a, b; two 64-column boxes
+    // dH -> (da, db) with the saved pre-activations a, b, one 32-column chunk
+    // at a time: da fills the slab's first half and db its second, each a
+    // 32 x 64-byte box in the 64-byte swizzle (16-byte chunk c of row r at
+    // c ^ ((r / 2) % 4)), stored to d_gu at columns col and H + col.
 #pragma unroll 1
-    for (int bx = 0; bx < 2; ++bx) {
-      const int col = t.n0 + half * 128 + bx * 64;
+    for (int c = 0; c < 4; ++c) {
+      const int col = t.n0 + half * 128 + c * 32;
       if (col >= p.N) break;
       const bf16* ap = p.aux_in + (size_t)row * p.ld_aux + col;
-#pragma unroll 1
-      for (int which = 0; which < 2; ++which) {    // da, then db
-        slab_acquire(lane);
-#pragma unroll 1
-        for (int c = 0; c < 2; ++c) {
-          uint4 av[4], bv[4];                      // saved a, b of this row's 32 columns
+      uint4 av[4], bv[4];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            av[i] = row_in ? *reinterpret_cast<const uint4*>(ap + c * 32 + i * 8)
-                           : make_uint4(0, 0, 0, 0);
-            bv[i] = row_in ? *reinterpret_cast<const uint4*>(ap + p.H + c * 32 + i * 8)
-                           : make_uint4(0, 0, 0, 0);
-          }
-          __syncwarp();
-          tmem_ld32(tacc + (half * 4 + bx * 2 + c) * 32, r0);
-          tmem_ld_wait();
+      for (int i = 0; i < 4; ++i) {
+        av[i] = row_in ? *reinterpret_cast<const uint4*>(ap + i * 8) : make_uint4(0, 0, 0, 0);
+        bv[i] = row_in ? *reinterpret_cast<const uint4*>(ap + p.H + i * 8)
+                       : make_uint4(0, 0, 0, 0);
+      }
+      __syncwarp();
+      tmem_ld32(tacc + (half * 4 + c) * 32, r0);
+      tmem_ld_wait();
+      slab_acquire(lane);
 #pragma unroll
-          for (int qq = 0; qq < 4; ++qq) {
-            float a8[8], b8[8], o[8];
-            unpack8(av[qq], a8);
-            unpack8(bv[qq], b8);
+      for (int qq = 0; qq < 4; ++qq) {
+        float a8[8], b8[8], da[8], db[8];
+        unpack8(av[qq], a8);
+        unpack8(bv[qq], b8);
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const float dh = __uint_as_float(r0[qq * 8 + u]);
-              const float a = a8[u], b = b8[u];
-              const float sg = 1.f / (1.f + __expf(-a));
-              o[u] = which == 0 ? dh * b * sg * (1.f + a * (1.f - sg)) : dh * (a * sg);
-            }
-            slab_put(slab, lane, c * 4 + qq, pack8(o));
-          }
+        for (int u = 0; u < 8; ++u) {
+          const float dh = __uint_as_float(r0[qq * 8 + u]);
+          const float a = a8[u], b = b8[u];
+          const float sg = 1.f / (1.f + __expf(-a));
+          da[u] = dh * b * sg * (1.f + a * (1.f - sg));
+          db[u] = dh * (a * sg);
         }
-        slab_store(slab, tmO0, lane, col + which * p.H, row0, 0, false);
+        const int pos = (qq ^ ((lane >> 1) & 3)) << 4;
+        *reinterpret_cast<uint4*>(slab.gen + lane * 64 + pos) = pack8(da);
+        *reinterpret_cast<uint4*>(slab.gen + 2048 + lane * 64 + pos) = pack8(db);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(tmO0, slab.addr, col, row0);
+        tma_store_2d(tmO0, slab.addr + 2048, col + p.H, row0);
+        bulk_commit();
       }
     }
   } else {
@@ -529,7 +534,8 @@ EncodeTiledFn encode_fn() {
 // dims/strides: innermost first; strides in bytes for dims 1..rank-1.
 bool make_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims,
               const uint64_t* strides, const uint32_t* box,
-              CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
+              CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+              CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t gd[5], gs[4];
@@ -537,7 +543,7 @@ bool make_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims,
   for (int i = 0; i < rank; ++i) { gd[i] = dims[i]; bx[i] = box[i]; es[i] = 1; }
   for (int i = 0; i < rank - 1; ++i) gs[i] = strides[i];
   CUresult r = fn(m, dtype, (cuuint32_t)rank, const_cast<void*>(ptr),
-                  gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -658,8 +664,9 @@ cudaError_t launch_gemm(const GemmCall& g, cudaStream_t s) {
     }
     case GK_DH: {
       uint64_t d0[2] = {(uint64_t)2 * g.H, rows}, s0[1] = {(uint64_t)g.ld0 * 2};
-      uint32_t b0[2] = {64, 32};
-      ok = make_map(&to0, g.out0, 2, d0, s0, b0);
+      uint32_t b0[2] = {32, 32};
+      ok = make_map(&to0, g.out0, 2, d0, s0, b0, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                    CU_TENSOR_MAP_SWIZZLE_64B);
       break;
     }
     case GK_DOWN:
