@@ -1,0 +1,116 @@
+"""The oracle's pins catch plausible mistakes.
+
+Each case plants one mistake in the oracle (CPU only, through monkeypatch)
+and checks that at least one pin from test_oracle_pins fails.  A pin set
+that let any of these through would not be pinning the oracle.
+"""
+import numpy as np
+import pytest
+
+from oracle import moe_oracle as O
+import test_oracle_pins as P
+
+
+def _fails(fn, *args):
+    try:
+        fn(*args)
+    except AssertionError:
+        return True
+    return False
+
+
+def test_reversed_tie_rule_is_caught(monkeypatch):
+    def select_high_index_first(key, k):
+        key = np.asarray(key)
+        E = key.shape[1]
+        order = np.argsort(-key[:, ::-1], axis=1, kind="stable")
+        return (E - 1 - order)[:, :k]
+    monkeypatch.setattr(O, "select_topk", select_high_index_first)
+    assert _fails(P.test_selection_brute_force, 4, 2)
+    assert _fails(P.test_equal_logits_tie_rule_and_balance)
+
+
+def test_f_normalised_without_k_is_caught(monkeypatch):
+    orig = O.route_stats
+
+    def route_stats(s, idx, real, norm_topk=True):
+        r = orig(s, idx, real, norm_topk)
+        r["f"] = r["f"] * idx.shape[1]
+        r["aux"] = s.shape[1] * float(np.dot(r["f"], r["p"]))
+        return r
+    monkeypatch.setattr(O, "route_stats", route_stats)
+    assert _fails(P.test_equal_logits_tie_rule_and_balance)
+
+
+def test_missing_renormalisation_is_caught(monkeypatch):
+    orig = O.route_stats
+    monkeypatch.setattr(O, "route_stats", lambda s, idx, real, norm_topk=True:
+                        orig(s, idx, real, False))
+    assert _fails(P.test_gates_renorm_and_raw)
+
+
+def test_gate_and_up_swapped_is_caught(monkeypatch):
+    def split_swapped(W_gu):
+        H = W_gu.shape[-2] // 2
+        return W_gu[..., H:, :], W_gu[..., :H, :]
+    monkeypatch.setattr(O, "split_gu", split_swapped)
+    assert _fails(P.test_dense_masked_brute_force)
+
+
+def test_softmax_without_max_shift_is_caught(monkeypatch):
+    def softmax_unshifted(L):
+        with np.errstate(over="ignore", invalid="ignore"):
+            z = np.exp(np.asarray(L, dtype=np.float64))
+            return z / z.sum(axis=-1, keepdims=True)
+    monkeypatch.setattr(O, "softmax", softmax_unshifted)
+    assert _fails(P.test_softmax_closed_form)
+
+
+def test_unstable_dispatch_order_is_caught(monkeypatch):
+    def permute_tokens_descending(topk_idx, E):
+        idx = np.asarray(topk_idx).reshape(-1)
+        q_real = np.nonzero(idx >= 0)[0][::-1]
+        perm = q_real[np.argsort(idx[q_real], kind="stable")]
+        counts = np.bincount(idx[q_real], minlength=E)
+        offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+        inv = np.full(idx.shape[0], -1, dtype=np.int64)
+        inv[perm] = np.arange(perm.shape[0])
+        return offsets, perm, inv
+    monkeypatch.setattr(O, "permute", permute_tokens_descending)
+    assert _fails(P.test_permute_invariants_and_brute_force)
+
+
+def test_aux_gradient_sign_flip_is_caught(monkeypatch):
+    orig = O.aux_logit_grad
+    monkeypatch.setattr(O, "aux_logit_grad", lambda *a: -orig(*a))
+    assert _fails(P.test_backward_matches_central_differences, True, True, False, 4)
+
+
+def test_dropped_silu_derivative_term_is_caught(monkeypatch):
+    def swiglu_backward_wrong(dh, a, b):
+        sa = O.sigmoid(a)
+        return dh * b * sa, dh * O.silu(a)        # missing (1 + a (1 - s(a)))
+    monkeypatch.setattr(O, "swiglu_backward", swiglu_backward_wrong)
+    assert _fails(P.test_backward_matches_central_differences, True, True, False, 4)
+
+
+def test_router_input_gradient_dropped_is_caught(monkeypatch):
+    orig = O.router_logit_grad
+    monkeypatch.setattr(O, "router_logit_grad", lambda *a: 0.0 * orig(*a))
+    assert _fails(P.test_backward_matches_central_differences, False, True, False, 4)
+
+
+def test_shared_expert_gated_is_caught(monkeypatch):
+    orig = O.swiglu_parts
+    calls = {"n": 0}
+
+    def swiglu_half_shared(xr, Wg, Wu, Wd, rnd=None):
+        out, a, b, h = orig(xr, Wg, Wu, Wd, rnd)
+        # the shared expert is the call with the concatenated shared weights:
+        # scale it as if it had a gate of 1/2
+        if Wg.shape[0] == getattr(swiglu_half_shared, "Hs", -1):
+            out = 0.5 * out
+        return out, a, b, h
+    swiglu_half_shared.Hs = 8                      # shared hidden of the pin's case
+    monkeypatch.setattr(O, "swiglu_parts", swiglu_half_shared)
+    assert _fails(P.test_k_equals_E_identical_experts_is_dense_ffn)
