@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 1
+#define MOE_ABI_VERSION 2
 #define MOE_ROW_ALIGN 128
 
 enum moe_status {
@@ -83,6 +83,8 @@ typedef struct moe_config {
   int32_t norm_topk;  /* 1: gates renormalised over the selected k; 0: raw p    */
   float aux_coef;     /* weight of aux in the objective differentiated by
                          moe_backward (KochiLLM card, Architecture: 0.01)       */
+  float z_coef;       /* weight of the router z-loss in that objective (0 = off)
+                         (KohakUwULLM README, Key features: z-loss)             */
 } moe_config;
 
 /*
@@ -109,6 +111,16 @@ typedef struct moe_tensors {
   float* f;             /* [E] f_e = counts_e / (k T_real)                        */
   float* p;             /* [E] p_e = mean over real tokens of softmax_e           */
   float* aux;           /* [1] aux = E * sum_e f_e p_e                            */
+  float* router_stats;  /* [8] fp32 routing metrics, or NULL to skip them:
+                           [0] z_loss = mean over real tokens of logsumexp(L_t)^2
+                           [1] router entropy, mean over real tokens of
+                               -sum_e s_te ln s_te (nats)
+                           [2] min_e counts_e   [3] max_e counts_e
+                           [4] CV of counts (population std / mean)
+                           [5] unused experts (counts_e == 0)
+                           [6] T_real          [7] 0
+                           ("spark-gpt" README: assignment min/max/CV, router
+                           entropy, unused experts)                               */
   /* dispatch */
   int32_t* offsets;     /* [E+1] exclusive scan of counts (unpadded)              */
   int32_t* row_offsets; /* [E+1] padded segment starts (multiples of 128)        */
@@ -128,7 +140,7 @@ typedef struct moe_tensors {
   void* y;              /* [T][d] bf16 layer output                               */
 } moe_tensors;
 
-/* Backward tensors (gradients of J = <dY, y> + aux_coef * aux). */
+/* Backward tensors (gradients of J = <dY, y> + aux_coef * aux + z_coef * z_loss). */
 typedef struct moe_grads {
   const void* dY;       /* [T][d] bf16 upstream gradient of y                     */
   void* dx;             /* [T][d] bf16 gradient of x (expert, shared and router
@@ -139,7 +151,7 @@ typedef struct moe_grads {
   void* dWs_gu;         /* [2Hs][d] bf16 (NULL when n_shared == 0)                */
   void* dWs_down;       /* [d][Hs] bf16                                           */
   float* d_logits;      /* [T][E] fp32 gradient of the router logits, including
-                           the aux term (f held constant)                        */
+                           the aux term (f held constant) and the z-loss term    */
 } moe_grads;
 
 /* ---------------------------------------------------------------- queries */
@@ -180,7 +192,8 @@ int moe_router_logits(const moe_config* cfg, const moe_tensors* t,
  * keys lower index first; s = fp32 softmax(logits) over all E (unbiased);
  * gates = s_sel / sum s_sel if norm_topk else s_sel; counts, f, p, aux over
  * real tokens.  in: logits, bias, valid.
- * out: topk_idx, gates, counts, f, p, aux.  Device errors: NONFINITE. */
+ * out: topk_idx, gates, counts, f, p, aux, router_stats (if non-NULL).
+ * Device errors: NONFINITE. */
 int moe_route(const moe_config* cfg, const moe_tensors* t,
               void* workspace, size_t workspace_bytes, void* stream);
 
@@ -222,8 +235,8 @@ int moe_forward(const moe_config* cfg, const moe_tensors* t,
 
 /* ---------------------------------------------------------------- backward */
 
-/* a7. Gradients of J = <dY, y> + aux_coef * aux with the hard counts (f)
- * held constant; the selection bias receives no gradient.
+/* a7. Gradients of J = <dY, y> + aux_coef * aux + z_coef * z_loss with the
+ * hard counts (f) held constant; the selection bias receives no gradient.
  * Reads every forward tensor of `t` written by moe_forward (x, Wr, valid,
  * weights, logits, topk_idx, gates, counts, f, row_offsets, inv, x_perm, ab,
  * h, out_perm, s_ab, s_h); ab and (if n_shared > 0) s_ab must have been saved.

@@ -29,11 +29,11 @@ STATUS = {
 class MoEConfig(ctypes.Structure):
     _fields_ = [("T", c_int32), ("d", c_int32), ("E", c_int32), ("k", c_int32),
                 ("H", c_int32), ("n_shared", c_int32), ("H_shared", c_int32),
-                ("norm_topk", c_int32), ("aux_coef", c_float)]
+                ("norm_topk", c_int32), ("aux_coef", c_float), ("z_coef", c_float)]
 
 
 TENSOR_FIELDS = ["x", "Wr", "bias", "valid", "W_gu", "W_down", "Ws_gu", "Ws_down",
-                 "logits", "topk_idx", "gates", "counts", "f", "p", "aux",
+                 "logits", "topk_idx", "gates", "counts", "f", "p", "aux", "router_stats",
                  "offsets", "row_offsets", "perm", "inv", "x_perm",
                  "ab", "h", "out_perm", "s_ab", "s_h", "s_out", "y"]
 GRAD_FIELDS = ["dY", "dx", "dWr", "dW_gu", "dW_down", "dWs_gu", "dWs_down", "d_logits"]
@@ -112,7 +112,8 @@ def config(shape, **over) -> MoEConfig:
     """MoEConfig from a synth.MoEShape (or anything with the same fields)."""
     c = MoEConfig(T=shape.T, d=shape.d, E=shape.E, k=shape.k, H=shape.H,
                   n_shared=shape.n_shared, H_shared=shape.H_shared,
-                  norm_topk=shape.norm_topk, aux_coef=shape.aux_coef)
+                  norm_topk=shape.norm_topk, aux_coef=shape.aux_coef,
+                  z_coef=getattr(shape, "z_coef", 0.0))
     for k_, v in over.items():
         setattr(c, k_, v)
     return c
@@ -159,6 +160,7 @@ class Layer:
 
         b = dict(logits=z(T, E, dt=f32), topk_idx=z(T, k, dt=i32), gates=z(T, k, dt=f32),
                  counts=z(E, dt=i32), f=z(E, dt=f32), p=z(E, dt=f32), aux=z(4, dt=f32),
+                 router_stats=z(8, dt=f32),
                  offsets=z(E + 1, dt=i32), row_offsets=z(E + 1, dt=i32), perm=z(R, dt=i32),
                  inv=z(T * k, dt=i32), x_perm=z(R, d, dt=bf), h=z(R, H, dt=bf),
                  out_perm=z(R, d, dt=f32), y=z(T, d, dt=bf),

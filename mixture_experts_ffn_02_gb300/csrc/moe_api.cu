@@ -73,6 +73,7 @@ int ws_layout(const moe_config* c, int training, WsLayout* w) {
   w->route_cnt = take((size_t)w->route_blocks * c->E * sizeof(int));
   w->route_psum = take((size_t)w->route_blocks * c->E * sizeof(float));
   w->route_treal = take((size_t)w->route_blocks * sizeof(int));
+  w->route_zent = take((size_t)w->route_blocks * 2 * sizeof(float));
   w->perm_hist = take((size_t)w->perm_blocks * c->E * sizeof(int));
   w->perm_base = take((size_t)w->perm_blocks * c->E * sizeof(int));
   w->d_out = w->d_gu = w->dx_perm = w->ds_gu = w->dxs = w->dxr = w->dwr_part = 0;
@@ -116,6 +117,7 @@ int check_cfg(const moe_config* c) {
   if (c->T < 1 || c->d < 64 || c->d % 64 || c->H < 64 || c->H % 64) return MOE_ERR_SHAPE;
   if (c->E < 1 || c->E > 256 || c->k < 1 || c->k > c->E || c->k > kMaxK) return MOE_ERR_SHAPE;
   if (c->n_shared < 0) return MOE_ERR_SHAPE;
+  if (!(c->aux_coef == c->aux_coef) || !(c->z_coef == c->z_coef)) return MOE_ERR_SHAPE;
   if (c->n_shared > 0 && (c->H_shared < 64 || c->H_shared % 64)) return MOE_ERR_SHAPE;
   if ((int64_t)c->T * c->k >= (1ll << 31)) return MOE_ERR_SHAPE;
   if (row_capacity(*c) >= (1ll << 31)) return MOE_ERR_SHAPE;
@@ -177,9 +179,9 @@ int do_router_logits(const moe_config* c, const moe_tensors* t, Call& k) {
 int do_route(const moe_config* c, const moe_tensors* t, Call& k) {
   MOE_NEED(t->logits); MOE_OPT(t->bias); MOE_OPT(t->valid);
   MOE_NEED(t->topk_idx); MOE_NEED(t->gates); MOE_NEED(t->counts);
-  MOE_NEED(t->f); MOE_NEED(t->p); MOE_NEED(t->aux);
+  MOE_NEED(t->f); MOE_NEED(t->p); MOE_NEED(t->aux); MOE_OPT(t->router_stats);
   MOE_CUDA(launch_route(*c, t->logits, t->bias, t->valid, t->topk_idx, t->gates, t->counts,
-                        t->f, t->p, t->aux, k.ws, k.w, k.s));
+                        t->f, t->p, t->aux, t->router_stats, k.ws, k.w, k.s));
   return MOE_OK;
 }
 

@@ -338,7 +338,8 @@ route_kernel(const float* __restrict__ L, const float* __restrict__ bias,
              int* __restrict__ blk_cnt, float* __restrict__ blk_psum,
              int* __restrict__ blk_treal, int* __restrict__ done,
              int32_t* __restrict__ counts, float* __restrict__ f, float* __restrict__ p,
-             float* __restrict__ aux, int* __restrict__ status) {
+             float* __restrict__ aux, float* __restrict__ blk_zent, float* __restrict__ stats,
+             int* __restrict__ status) {
   extern __shared__ unsigned char smem_raw[];
   const int groups = blockDim.x / G;
   int* cnt_s = reinterpret_cast<int*>(smem_raw);                 // [E]
@@ -358,6 +359,8 @@ route_kernel(const float* __restrict__ L, const float* __restrict__ bias,
 #pragma unroll
   for (int v = 0; v < V; ++v) psum[v] = 0.f;
   int my_treal = 0;
+  float z_acc = 0.f, ent_acc = 0.f;
+  __shared__ float zred_s[kThreads / 32], ered_s[kThreads / 32];
 
   const int tokens_per_iter = groups * gridDim.x;
   for (int t0 = blockIdx.x * groups; t0 < T; t0 += tokens_per_iter) {
@@ -394,6 +397,19 @@ route_kernel(const float* __restrict__ L, const float* __restrict__ bias,
     for (int o = G >> 1; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
 #pragma unroll
     for (int v = 0; v < V; ++v) sv[v] = sv[v] / sum;
+    if (stats) {
+      // z-loss term lse^2 and entropy lse - sum_e s_e L_e of this token
+      float sl = 0.f;
+#pragma unroll
+      for (int v = 0; v < V; ++v)
+        if (lig + G * v < E) sl = fmaf(sv[v], lv[v], sl);
+      for (int o = G >> 1; o > 0; o >>= 1) sl += __shfl_xor_sync(0xffffffffu, sl, o);
+      if (real && lig == 0) {
+        const float lse = m + logf(sum);
+        z_acc = fmaf(lse, lse, z_acc);
+        ent_acc += lse - sl;
+      }
+    }
 
     // top-k by repeated group arg-max
     unsigned taken = 0;
@@ -459,6 +475,18 @@ route_kernel(const float* __restrict__ L, const float* __restrict__ bias,
     blk_cnt[(size_t)blockIdx.x * E + e] = cnt_s[e];
   }
   if (threadIdx.x == 0) blk_treal[blockIdx.x] = treal_s;
+  if (stats) {
+    z_acc = warp_sum(z_acc);
+    ent_acc = warp_sum(ent_acc);
+    if (lane == 0) { zred_s[threadIdx.x >> 5] = z_acc; ered_s[threadIdx.x >> 5] = ent_acc; }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float zs = 0.f, es = 0.f;
+      for (int w = 0; w < (int)(blockDim.x >> 5); ++w) { zs += zred_s[w]; es += ered_s[w]; }
+      blk_zent[2 * blockIdx.x] = zs;
+      blk_zent[2 * blockIdx.x + 1] = es;
+    }
+  }
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) ticket_s = atomicAdd(done, 1);
@@ -519,8 +547,41 @@ route_kernel(const float* __restrict__ L, const float* __restrict__ bias,
     float s = 0.f;
     for (int w = 0; w < (int)(blockDim.x >> 5); ++w) s += red_s[w];
     aux[0] = (float)E * s;
-    *done = 0;
   }
+  if (stats) {
+    // routing metrics: z-loss, entropy (block partials summed in block
+    // order), and min / max / CV / unused of the counts
+    for (int e = threadIdx.x; e < E; e += blockDim.x) cnt_s[e] = counts[e];
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float zs = 0.f, es = 0.f;
+      for (int b = 0; b < nb; ++b) {
+        zs += __ldcg(blk_zent + 2 * b);
+        es += __ldcg(blk_zent + 2 * b + 1);
+      }
+      double mean = 0.0, sq = 0.0;
+      int cmin = INT_MAX, cmax = 0, unused = 0;
+      for (int e = 0; e < E; ++e) {
+        const int c = cnt_s[e];
+        mean += c;
+        sq += (double)c * c;
+        cmin = min(cmin, c);
+        cmax = max(cmax, c);
+        unused += c == 0;
+      }
+      mean /= E;
+      const double var = fmax(sq / E - mean * mean, 0.0);
+      stats[0] = Tr > 0 ? zs / (float)Tr : 0.f;
+      stats[1] = Tr > 0 ? es / (float)Tr : 0.f;
+      stats[2] = (float)cmin;
+      stats[3] = (float)cmax;
+      stats[4] = mean > 0 ? (float)(sqrt(var) / mean) : 0.f;
+      stats[5] = (float)unused;
+      stats[6] = (float)Tr;
+      stats[7] = 0.f;
+    }
+  }
+  if (threadIdx.x == 0) *done = 0;
 }
 
 // --------------------------------------------------------------------------
@@ -727,9 +788,9 @@ combine_bwd_kernel(const bf16* __restrict__ dY, const float* __restrict__ out_pe
                    const float* __restrict__ f, const int32_t* __restrict__ counts,
                    const uint8_t* __restrict__ valid, const int32_t* __restrict__ row_offsets,
                    bf16* __restrict__ d_out, float* __restrict__ d_logits, int T, int d, int E,
-                   int k, int norm_topk, float aux_coef) {
+                   int k, int norm_topk, float aux_coef, float z_coef) {
   __shared__ float f_s[256];
-  __shared__ float coef_s;
+  __shared__ float coef_s, zcoef_s;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int wpb = blockDim.x >> 5;
   for (int e = threadIdx.x; e < E; e += blockDim.x) f_s[e] = f[e];
@@ -738,9 +799,11 @@ combine_bwd_kernel(const bf16* __restrict__ dY, const float* __restrict__ out_pe
     for (int e = 0; e < E; ++e) m += counts[e];
     const long long Tr = m / k;
     coef_s = Tr > 0 ? aux_coef * (float)E / (float)Tr : 0.f;
+    zcoef_s = Tr > 0 ? 2.f * z_coef / (float)Tr : 0.f;
   }
   __syncthreads();
   const float coef = coef_s;
+  const float zcoef = zcoef_s;
   for (int t = blockIdx.x * wpb + warp; t < T; t += gridDim.x * wpb) {
     const bool real = row_real(valid, t);
     float* dl = d_logits + (size_t)t * E;
@@ -799,6 +862,7 @@ combine_bwd_kernel(const bf16* __restrict__ dY, const float* __restrict__ out_pe
       sum += sv[v];
     }
     sum = warp_sum(sum);
+    const float lse = m + logf(sum);
     float fs = 0.f;
 #pragma unroll
     for (int v = 0; v < V; ++v) {
@@ -824,7 +888,8 @@ combine_bwd_kernel(const bf16* __restrict__ dY, const float* __restrict__ out_pe
       if (e >= E) continue;
       float mv = main[v];
       if (!norm_topk) mv -= sv[v] * gdg;
-      dl[e] = mv + coef * sv[v] * (f_s[e] - fs);
+      // aux term with f held constant, and the z-loss term 2 z lse s / T_real
+      dl[e] = mv + coef * sv[v] * (f_s[e] - fs) + zcoef * lse * sv[v];
     }
   }
   // zero d_out pad rows
@@ -1033,8 +1098,8 @@ cudaError_t launch_sum_splits(const float* part, float* out, int n, int splits, 
 
 cudaError_t launch_route(const moe_config& c, const float* L, const float* bias,
                          const uint8_t* valid, int32_t* topk, float* gates, int32_t* counts,
-                         float* f, float* p, float* aux, char* ws, const WsLayout& w,
-                         cudaStream_t s) {
+                         float* f, float* p, float* aux, float* stats, char* ws,
+                         const WsLayout& w, cudaStream_t s) {
   int G = 1;
   while (G < c.E && G < 32) G <<= 1;
   const int V = (c.E + G - 1) / G;
@@ -1046,6 +1111,7 @@ cudaError_t launch_route(const moe_config& c, const float* L, const float* bias,
   int* cnt = reinterpret_cast<int*>(ws + w.route_cnt);
   float* psum = reinterpret_cast<float*>(ws + w.route_psum);
   int* treal = reinterpret_cast<int*>(ws + w.route_treal);
+  float* zent = reinterpret_cast<float*>(ws + w.route_zent);
   int* status = reinterpret_cast<int*>(ws + w.status);
   const int grid = w.route_blocks;
 #define MOE_ROUTE(VV)                                                                        \
@@ -1053,7 +1119,7 @@ cudaError_t launch_route(const moe_config& c, const float* L, const float* bias,
                        (int)smem);                                                           \
   route_kernel<VV><<<grid, kThreads, smem, s>>>(L, bias, valid, c.T, c.E, c.k, G, c.norm_topk, \
                                                 topk, gates, cnt, psum, treal, done, counts, f, \
-                                                p, aux, status)
+                                                p, aux, zent, stats, status)
   if (V <= 1) { MOE_ROUTE(1); }
   else if (V <= 2) { MOE_ROUTE(2); }
   else if (V <= 4) { MOE_ROUTE(4); }
@@ -1080,7 +1146,7 @@ cudaError_t launch_route_scratch(const moe_config& c, const float* L, const floa
                        (int)smem);                                                            \
   route_kernel<VV><<<grid, kThreads, smem, s>>>(L, bias, valid, c.T, c.E, c.k, G, c.norm_topk, \
                                                 topk, gates, blk_cnt, blk_psum, blk_treal, done, \
-                                                counts, f, p, aux, status)
+                                                counts, f, p, aux, nullptr, nullptr, status)
   if (V <= 1) { MOE_ROUTE_S(1); }
   else if (V <= 2) { MOE_ROUTE_S(2); }
   else if (V <= 4) { MOE_ROUTE_S(4); }
@@ -1131,7 +1197,7 @@ cudaError_t launch_combine_bwd(const moe_config& c, const void* dY, const float*
   combine_bwd_kernel<VV><<<grid, kThreads, 0, s>>>(                                           \
       static_cast<const bf16*>(dY), out_perm, inv, topk, gates, L, f,                          \
       counts, valid, row_offsets, static_cast<bf16*>(d_out), d_logits, c.T, c.d, c.E, c.k,     \
-      c.norm_topk, c.aux_coef)
+      c.norm_topk, c.aux_coef, c.z_coef)
   if (V <= 1) { MOE_CBWD(1); }
   else if (V <= 2) { MOE_CBWD(2); }
   else if (V <= 4) { MOE_CBWD(4); }

@@ -31,6 +31,7 @@ struct WsLayout {
   size_t route_cnt;     // [route_blocks][E] int32
   size_t route_psum;    // [route_blocks][E] fp32
   size_t route_treal;   // [route_blocks] int32
+  size_t route_zent;    // [route_blocks][2] fp32 (z-loss, entropy partials)
   size_t perm_hist;     // [perm_blocks][E] int32
   size_t perm_base;     // [perm_blocks][E] int32
   // backward scratch
@@ -59,8 +60,8 @@ cudaError_t launch_router_logits(const moe_config& c, const void* x, const float
                                  float* L, cudaStream_t s);
 cudaError_t launch_route(const moe_config& c, const float* L, const float* bias,
                          const uint8_t* valid, int32_t* topk, float* gates, int32_t* counts,
-                         float* f, float* p, float* aux, char* ws, const WsLayout& w,
-                         cudaStream_t s);
+                         float* f, float* p, float* aux, float* stats, char* ws,
+                         const WsLayout& w, cudaStream_t s);
 cudaError_t launch_route_scratch(const moe_config& c, const float* L, const float* bias,
                                  const uint8_t* valid, int32_t* topk, float* gates,
                                  int32_t* counts, float* f, float* p, float* aux, int* blk_cnt,

@@ -46,6 +46,7 @@ class MoEShape:
     zipf_bias: float = 0.0         # >0: selection bias -s*ln(e+1)
     training: bool = False         # the workload includes the backward
     aux_coef: float = 0.01         # KochiLLM card, Architecture: 0.01 x aux
+    z_coef: float = 0.0            # router z-loss weight (off unless a test sets it)
 
     @property
     def Hs_total(self) -> int:

@@ -125,7 +125,37 @@ def route(logits, k, bias=None, valid=None, norm_topk=True):
     idx = select_topk(key, k)
     s = softmax(L.astype(f64))
     real = np.ones(T, dtype=bool) if valid is None else (np.asarray(_np(valid)) != 0)
-    return route_stats(s, idx, real, norm_topk)
+    r = route_stats(s, idx, real, norm_topk)
+    r.update(router_metrics(L, r["counts"], real))
+    return r
+
+
+def logsumexp(L):
+    """Row log-sum-exp in fp64: max + ln sum exp(L - max)."""
+    L = np.asarray(L, dtype=f64)
+    m = L.max(axis=-1)
+    return m + np.log(np.exp(L - m[..., None]).sum(axis=-1))
+
+
+def router_metrics(L, counts, real):
+    """Routing metrics ("spark-gpt" README: assignment min/max/CV, router
+    entropy, unused experts) and the router z-loss ("KohakUwULLM" README,
+    Key features: z-loss), read as the mean over real tokens of the squared
+    log-sum-exp of the logits.  Entropy in nats of the full softmax, averaged
+    over real tokens; CV = population std / mean of the per-expert counts."""
+    L = np.asarray(L, dtype=f64)
+    counts = np.asarray(counts, dtype=f64)
+    Tr = int(np.asarray(real).sum())
+    lse = logsumexp(L)
+    s = softmax(L)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ent = -(s * np.where(s > 0, np.log(s), 0.0)).sum(axis=-1)
+    mean = counts.mean()
+    return dict(z_loss=float((lse[real] ** 2).mean()) if Tr else 0.0,
+                entropy=float(ent[real].mean()) if Tr else 0.0,
+                count_min=float(counts.min()), count_max=float(counts.max()),
+                count_cv=float(counts.std() / mean) if mean > 0 else 0.0,
+                unused=int((counts == 0).sum()), T_real=Tr)
 
 
 def route_stats(s, idx, real, norm_topk=True):
@@ -305,9 +335,22 @@ def aux_logit_grad(probs, f, real, aux_coef):
     return out
 
 
+def z_logit_grad(L, real, z_coef):
+    """d(z_coef * mean_real(lse_t^2))/dL_{t,e} = (2 z_coef / T_real) lse_t s_{t,e}."""
+    L = np.asarray(L, dtype=f64)
+    out = np.zeros_like(L)
+    Tr = int(np.asarray(real).sum())
+    if Tr == 0 or z_coef == 0:
+        return out
+    out = (2.0 * z_coef / Tr) * logsumexp(L)[:, None] * softmax(L)
+    out[~np.asarray(real)] = 0.0
+    return out
+
+
 def backward(x, Wr, W_gu, W_down, Ws_gu, Ws_down, fwd, dY, norm_topk=True,
-             aux_coef=0.01, rnd=None):
-    """Gradients of J = <dY, y> + aux_coef * aux by the chain rule.
+             aux_coef=0.01, rnd=None, z_coef=0.0):
+    """Gradients of J = <dY, y> + aux_coef * aux + z_coef * z_loss by the
+    chain rule (z_loss needs fwd["logits"] when z_coef is non-zero).
 
     ``fwd`` is the dict returned by :func:`forward` (routing and probs).
     Returns dict: dx [T][d], dWr [d][E], dW_gu [E][2H][d], dW_down [E][d][H],
@@ -366,6 +409,8 @@ def backward(x, Wr, W_gu, W_down, Ws_gu, Ws_down, fwd, dY, norm_topk=True,
         dWs_down = dY[rows].T @ h
     d_logits = router_logit_grad(dg, idx, g, fwd["probs"], norm_topk)
     d_logits += aux_logit_grad(fwd["probs"], fwd["f"], real, aux_coef)
+    if z_coef:
+        d_logits += z_logit_grad(fwd["logits"], real, z_coef)
     dx += d_logits @ Wr.T
     dWr = x.T @ d_logits
     return dict(dx=dx, dWr=dWr, dW_gu=dW_gu, dW_down=dW_down, dWs_gu=dWs_gu,
@@ -373,8 +418,9 @@ def backward(x, Wr, W_gu, W_down, Ws_gu, Ws_down, fwd, dY, norm_topk=True,
 
 
 def objective(x, Wr, W_gu, W_down, Ws_gu, Ws_down, dY, k, bias=None, valid=None,
-              norm_topk=True, aux_coef=0.01, counts_f=None):
-    """J = <dY, y> + aux_coef * aux with fp64 logits (finite-difference pins).
+              norm_topk=True, aux_coef=0.01, counts_f=None, z_coef=0.0):
+    """J = <dY, y> + aux_coef * aux + z_coef * z_loss with fp64 logits
+    (finite-difference pins).
 
     ``counts_f`` holds f fixed (the hard counts are not differentiated).
     """
@@ -384,4 +430,4 @@ def objective(x, Wr, W_gu, W_down, Ws_gu, Ws_down, dY, k, bias=None, valid=None,
                            Ws_down, valid)
     f = r["f"] if counts_f is None else counts_f
     aux = r["probs"].shape[1] * float(np.dot(f, r["p"]))
-    return float((_f64(dY) * y).sum()) + aux_coef * aux, r
+    return float((_f64(dY) * y).sum()) + aux_coef * aux + z_coef * r["z_loss"], r

@@ -39,7 +39,7 @@ def test_library_exports_every_declared_symbol(clib):
 
 
 def test_abi_version_and_messages(clib):
-    assert clib.moe_abi_version() == 1
+    assert clib.moe_abi_version() == 2
     for code in range(10):
         assert clib.moe_strerror(code)
     assert b"unknown" in clib.moe_strerror(99)
@@ -47,14 +47,15 @@ def test_abi_version_and_messages(clib):
 
 def cfg(**kw):
     base = dict(T=256, d=64, E=4, k=2, H=128, n_shared=1, H_shared=128, norm_topk=1,
-                aux_coef=0.01)
+                aux_coef=0.01, z_coef=0.0)
     base.update(kw)
     return binding.MoEConfig(**base)
 
 
 @pytest.mark.parametrize("bad", [dict(T=0), dict(d=100), dict(H=96), dict(k=0), dict(k=5),
                                  dict(E=257, k=2), dict(E=64, k=33), dict(n_shared=-1),
-                                 dict(H_shared=100), dict(T=2 ** 30, k=8)])
+                                 dict(H_shared=100), dict(T=2 ** 30, k=8),
+                                 dict(z_coef=float("nan"))])
 def test_shape_rules(clib, bad):
     assert clib.moe_check_config(ctypes.byref(cfg(**bad))) == 2
 
@@ -92,3 +93,14 @@ def test_entry_points_reject_bad_arguments_without_touching_the_gpu(clib):
         assert rc in (4, 5, 6), (name, rc)   # workspace, or no CUDA device here
     bad = cfg(d=65)
     assert clib.moe_forward(ctypes.byref(bad), ctypes.byref(t), None, 0, None) == 2
+
+
+def test_struct_layouts_match_the_header():
+    """The binding's ctypes structures have the header's field order."""
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    for struct, cls in (("moe_config", binding.MoEConfig), ("moe_tensors", binding.MoETensors),
+                        ("moe_grads", binding.MoEGrads)):
+        body = re.search(r"typedef struct " + struct + r" \{(.*?)\} " + struct, src, re.S).group(1)
+        names = re.findall(r"\b(\w+)\s*;", body)
+        assert names == [f[0] for f in cls._fields_], struct

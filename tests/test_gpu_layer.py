@@ -104,3 +104,26 @@ def test_backward_matches_oracle(cfg, T, norm_topk):
         pad = inp["valid"] == 0
         assert (g["dx"].cpu()[pad].float() == 0).all()
         assert (g["d_logits"].cpu()[pad] == 0).all()
+
+
+@pytest.mark.parametrize("cfg,T", [(1, None), (3, 3001), (5, 1300)])
+def test_router_z_loss_gradient(cfg, T):
+    """The z-loss term of d_logits on its own: with dY = 0 and aux_coef = 0
+    the logit gradient is exactly the z-loss gradient, compared with the
+    oracle's on the same logits; the forward statistic is the oracle's z_loss."""
+    Z = 0.5
+    s = synth.scaled(scaled_shape(cfg, T), z_coef=Z, aux_coef=0.0)
+    inp = synth.make_inputs(s, seed=0, with_grad=True)
+    lay = Layer.create(s, training=True)
+    dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    lay.set_inputs(dev["x"], dev["Wr"], dev["W_gu"], dev["W_down"], dev["Ws_gu"],
+                   dev["Ws_down"], bias=dev["bias"], valid=dev["valid"])
+    lay.forward()
+    lay.backward(torch.zeros_like(dev["dY"]))
+    torch.cuda.synchronize()
+    assert lay.status() == 0
+    real = np.ones(s.T, bool) if inp["valid"] is None else inp["valid"].numpy() != 0
+    L = np64(lay.bufs["logits"])
+    assert_close("d_logits[z]", lay.grads["d_logits"], O.z_logit_grad(L, real, Z), tol=1e-5)
+    m = O.router_metrics(L, lay.bufs["counts"].cpu().numpy(), real)
+    assert float(lay.bufs["router_stats"][0]) == pytest.approx(m["z_loss"], rel=1e-5)

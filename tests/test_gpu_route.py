@@ -57,6 +57,12 @@ def test_route_bit_exact(T, E, k, quantum, norm, pad, use_bias):
     np.testing.assert_allclose(np64(b["f"]), ref["f"], rtol=STAT_RTOL, atol=0)
     np.testing.assert_allclose(np64(b["p"]), ref["p"], rtol=STAT_RTOL, atol=1e-9)
     assert float(b["aux"][0]) == pytest.approx(ref["aux"], rel=STAT_RTOL)
+    st = b["router_stats"].cpu().numpy().astype(np.float64)
+    assert st[0] == pytest.approx(ref["z_loss"], rel=STAT_RTOL)
+    assert st[1] == pytest.approx(ref["entropy"], rel=STAT_RTOL, abs=1e-7)
+    assert (st[2], st[3], st[5], st[6]) == (ref["count_min"], ref["count_max"],
+                                            ref["unused"], ref["T_real"])
+    assert st[4] == pytest.approx(ref["count_cv"], rel=1e-6, abs=1e-7)
 
 
 def test_route_equal_logits_tie_rule():

@@ -83,7 +83,7 @@ def test_unstable_dispatch_order_is_caught(monkeypatch):
 def test_aux_gradient_sign_flip_is_caught(monkeypatch):
     orig = O.aux_logit_grad
     monkeypatch.setattr(O, "aux_logit_grad", lambda *a: -orig(*a))
-    assert _fails(P.test_backward_matches_central_differences, True, True, False, 4)
+    assert _fails(P.test_backward_matches_central_differences, True, True, False, 4, 0.0)
 
 
 def test_dropped_silu_derivative_term_is_caught(monkeypatch):
@@ -91,13 +91,13 @@ def test_dropped_silu_derivative_term_is_caught(monkeypatch):
         sa = O.sigmoid(a)
         return dh * b * sa, dh * O.silu(a)        # missing (1 + a (1 - s(a)))
     monkeypatch.setattr(O, "swiglu_backward", swiglu_backward_wrong)
-    assert _fails(P.test_backward_matches_central_differences, True, True, False, 4)
+    assert _fails(P.test_backward_matches_central_differences, True, True, False, 4, 0.0)
 
 
 def test_router_input_gradient_dropped_is_caught(monkeypatch):
     orig = O.router_logit_grad
     monkeypatch.setattr(O, "router_logit_grad", lambda *a: 0.0 * orig(*a))
-    assert _fails(P.test_backward_matches_central_differences, False, True, False, 4)
+    assert _fails(P.test_backward_matches_central_differences, False, True, False, 4, 0.0)
 
 
 def test_shared_expert_gated_is_caught(monkeypatch):
@@ -114,3 +114,9 @@ def test_shared_expert_gated_is_caught(monkeypatch):
     swiglu_half_shared.Hs = 8                      # shared hidden of the pin's case
     monkeypatch.setattr(O, "swiglu_parts", swiglu_half_shared)
     assert _fails(P.test_k_equals_E_identical_experts_is_dense_ffn)
+
+
+def test_z_loss_gradient_missing_factor_two_is_caught(monkeypatch):
+    orig = O.z_logit_grad
+    monkeypatch.setattr(O, "z_logit_grad", lambda L, real, z: orig(L, real, z / 2))
+    assert _fails(P.test_backward_matches_central_differences, True, True, False, 4, 0.23)

@@ -66,6 +66,29 @@ def test_equal_logits_tie_rule_and_balance():
     np.testing.assert_allclose(r2["gates"], 1.0 / E, rtol=0, atol=1e-15)
 
 
+def test_router_metrics_closed_forms():
+    """Equal logits c: logsumexp = c + ln E, so z_loss = (c + ln E)^2; the
+    entropy is ln E (its maximum); experts 0..k-1 take every token, so
+    counts = [T]*k + [0]*(E-k): min 0, max T, E-k unused, CV = sqrt(E/k - 1)."""
+    T, E, k, c = 50, 8, 3, 0.75
+    r = O.route(np.full((T, E), c, np.float32), k)
+    assert r["z_loss"] == pytest.approx((c + math.log(E)) ** 2, rel=1e-12)
+    assert r["entropy"] == pytest.approx(math.log(E), rel=1e-12)
+    assert (r["count_min"], r["count_max"], r["unused"]) == (0.0, float(T), E - k)
+    assert r["count_cv"] == pytest.approx(math.sqrt(E / k - 1), rel=1e-12)
+    # a dominant logit: entropy -> 0, logsumexp -> that logit
+    L = np.zeros((4, E)); L[:, 2] = 60.0
+    r = O.route(L, 1)
+    assert r["entropy"] < 1e-20 and r["z_loss"] == pytest.approx(3600.0, rel=1e-12)
+    # PAD rows do not count
+    valid = np.array([1, 1, 0, 0], np.uint8)
+    L2 = np.array([[0.0] * E, [math.log(2.0)] + [0.0] * (E - 1), [9.0] * E, [5.0] * E])
+    r = O.route(L2, 2, valid=valid)
+    lse = [math.log(E), math.log(E + 1.0)]
+    assert r["z_loss"] == pytest.approx((lse[0] ** 2 + lse[1] ** 2) / 2, rel=1e-12)
+    assert r["T_real"] == 2
+
+
 def test_softmax_closed_form():
     """softmax(0, ln 2, ln 3) = (1/6, 2/6, 3/6)."""
     s = O.softmax(np.array([[0.0, math.log(2.0), math.log(3.0)]]))
@@ -320,27 +343,28 @@ def _fd_case(seed, T=12, d=8, E=4, k=2, H=6, Hs=4, pad=True, bias=False):
                 dY=dY, valid=valid, bias=b)
 
 
-@pytest.mark.parametrize("norm_topk,pad,bias,Hs", [(True, True, False, 4),
-                                                   (False, True, False, 4),
-                                                   (True, False, True, 0),
-                                                   (False, False, True, 3)])
-def test_backward_matches_central_differences(norm_topk, pad, bias, Hs):
+@pytest.mark.parametrize("norm_topk,pad,bias,Hs,zc", [(True, True, False, 4, 0.0),
+                                                      (False, True, False, 4, 0.0),
+                                                      (True, False, True, 0, 0.0),
+                                                      (False, False, True, 3, 0.0),
+                                                      (True, True, False, 4, 0.23)])
+def test_backward_matches_central_differences(norm_topk, pad, bias, Hs, zc):
     """Every gradient (x, W_r, expert and shared weights, router logits) of
-    J = <dY, y> + a * aux against central differences in fp64."""
+    J = <dY, y> + a * aux + z * z_loss against central differences in fp64."""
     c = _fd_case(21, pad=pad, bias=bias, Hs=Hs)
     k, alpha = 2, 0.37
     L = O.router_logits(c["x"], c["Wr"])
     fwd = O.forward(c["x"], c["Wr"], c["W_gu"], c["W_down"], c["Ws_gu"], c["Ws_down"], k=k,
                     bias=c["bias"], valid=c["valid"], norm_topk=norm_topk, logits=L)
     grads = O.backward(c["x"], c["Wr"], c["W_gu"], c["W_down"], c["Ws_gu"], c["Ws_down"],
-                       fwd, c["dY"], norm_topk=norm_topk, aux_coef=alpha)
+                       fwd, c["dY"], norm_topk=norm_topk, aux_coef=alpha, z_coef=zc)
     f0 = fwd["f"]
 
     def J(**over):
         a = {**c, **over}
         return O.objective(a["x"], a["Wr"], a["W_gu"], a["W_down"], a["Ws_gu"], a["Ws_down"],
                            a["dY"], k, bias=a["bias"], valid=a["valid"], norm_topk=norm_topk,
-                           aux_coef=alpha, counts_f=f0)[0]
+                           aux_coef=alpha, counts_f=f0, z_coef=zc)[0]
 
     eps = 1e-6
     rng = _rng(99)
@@ -362,7 +386,8 @@ def test_backward_matches_central_differences(norm_topk, pad, bias, Hs):
         r = O.route(Lp, k, bias=c["bias"], valid=c["valid"], norm_topk=norm_topk)
         y, _ = O.experts_forward(c["x"], r["topk_idx"], r["gates"], c["W_gu"], c["W_down"],
                                  c["Ws_gu"], c["Ws_down"], c["valid"])
-        return float((c["dY"] * y).sum()) + alpha * L.shape[1] * float(np.dot(f0, r["p"]))
+        return (float((c["dY"] * y).sum()) + alpha * L.shape[1] * float(np.dot(f0, r["p"]))
+                + zc * r["z_loss"])
 
     for t in range(L.shape[0]):
         for e in range(L.shape[1]):
