@@ -309,38 +309,95 @@ def load_traffic(cfg):
 
 def run_e2e(args, s, inp, lay, training, local):
     """The same layer step through moe_forward/moe_backward with host
-    buffers: x (and dY) copied in from pinned memory, y and dx (and aux)
-    copied back, all inside the timed region."""
+    buffers, driven the way a training loop would: every step copies its
+    inputs x and dY in from pinned host memory and its results y, aux and dx
+    back out, all inside the timed region.  The copies run on a copy stream
+    ordered by events: x, y and dx are double-buffered so the next step's x
+    upload overlaps this step's compute and this step's downloads overlap the
+    next step's; dY's upload overlaps the forward."""
     import torch
     hx = inp["x"].pin_memory()
     hdy = inp["dY"].pin_memory()
     hy = torch.empty_like(inp["x"]).pin_memory()
     hdx = torch.empty_like(inp["x"]).pin_memory()
     haux = torch.empty(4, dtype=torch.float32).pin_memory()
-    x_dev = lay.bufs["x"]
+    main = torch.cuda.current_stream()
+    copy = torch.cuda.Stream()
+    xbuf = [lay.bufs["x"], torch.empty_like(lay.bufs["x"])]
+    dxbuf = [lay.grads["dx"], torch.empty_like(lay.bufs["x"])] if training else [None, None]
+    ybuf = [lay.bufs["y"], torch.empty_like(lay.bufs["y"])]
     dy_dev = torch.empty_like(lay.bufs["x"])
-    stream = torch.cuda.current_stream()
-    n = max(3, args.steps // 2)
-    times = []
-    for i in range(n + 2):
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        x_dev.copy_(hx, non_blocking=True)
+    ev = lambda: torch.cuda.Event()            # noqa: E731
+    x_ready, bwd_done, dx_out, y_out = [None, None], [None, None], [None, None], [None, None]
+
+    def upload_x(i):
+        j = i % 2
+        if bwd_done[j] is not None:
+            copy.wait_event(bwd_done[j])       # step i-2 no longer reads this x buffer
+        with torch.cuda.stream(copy):
+            xbuf[j].copy_(hx, non_blocking=True)
+        x_ready[j] = ev()
+        x_ready[j].record(copy)
+
+    def step(i):
+        j = i % 2
+        main.wait_event(x_ready[j])
+        if dx_out[j] is not None:
+            main.wait_event(dx_out[j])         # step i-2's dx download is done
+        if y_out[j] is not None:
+            main.wait_event(y_out[j])          # step i-2's y download is done
+        lay.bufs["x"] = xbuf[j]
+        lay.bufs["y"] = ybuf[j]
         if training:
-            dy_dev.copy_(hdy, non_blocking=True)
+            lay.grads["dx"] = dxbuf[j]
+            copy.wait_stream(main)             # previous backward no longer reads dY
+            with torch.cuda.stream(copy):
+                dy_dev.copy_(hdy, non_blocking=True)
+            dy_ready = ev()
+            dy_ready.record(copy)
         lay.forward()
+        y_ready = ev()
+        y_ready.record(main)
+        copy.wait_event(y_ready)
+        with torch.cuda.stream(copy):
+            hy.copy_(ybuf[j], non_blocking=True)
+            haux.copy_(lay.bufs["aux"], non_blocking=True)
+        y_out[j] = ev()
+        y_out[j].record(copy)
+        upload_x(i + 1)                        # next step's input, during this backward
         if training:
+            main.wait_event(dy_ready)
             lay.backward(dy_dev)
-        hy.copy_(lay.bufs["y"], non_blocking=True)
-        haux.copy_(lay.bufs["aux"], non_blocking=True)
-        if training:
-            hdx.copy_(lay.grads["dx"], non_blocking=True)
-        b.record(stream)
-        b.synchronize()
-        if i >= 2:
-            times.append(a.elapsed_time(b))
-    ms = statistics.median(times)
+            bwd_done[j] = ev()
+            bwd_done[j].record(main)
+            copy.wait_event(bwd_done[j])
+            with torch.cuda.stream(copy):
+                hdx.copy_(dxbuf[j], non_blocking=True)
+            dx_out[j] = ev()
+            dx_out[j].record(copy)
+
+    i = 0
+    upload_x(0)
+    for _ in range(2):
+        step(i)
+        i += 1
+    main.wait_stream(copy)
+    torch.cuda.synchronize()
+    n = max(3, args.steps // 2)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(main)
+    for _ in range(n):
+        step(i)
+        i += 1
+    main.wait_stream(copy)                     # every copy of the timed steps is done
+    b.record(main)
+    b.synchronize()
+    lay.bufs["x"] = xbuf[0]
+    lay.bufs["y"] = ybuf[0]
+    if training:
+        lay.grads["dx"] = dxbuf[0]
+    ms = a.elapsed_time(b) / n
     nb = s.T * s.d * 2
     return {"value": round(s.T / (ms / 1e3), 1), "unit": "tokens/s",
             "h2d_bytes_per_step": nb * (2 if training else 1),
