@@ -356,12 +356,12 @@ def run_e2e(args, s, inp, lay, training, local):
             dy_ready = ev()
             dy_ready.record(copy)
         lay.forward()
+        haux.copy_(lay.bufs["aux"], non_blocking=True)   # 16 bytes, ordered on main
         y_ready = ev()
         y_ready.record(main)
         copy.wait_event(y_ready)
         with torch.cuda.stream(copy):
             hy.copy_(ybuf[j], non_blocking=True)
-            haux.copy_(lay.bufs["aux"], non_blocking=True)
         y_out[j] = ev()
         y_out[j].record(copy)
         upload_x(i + 1)                        # next step's input, during this backward
