@@ -233,6 +233,29 @@ int moe_combine(const moe_config* cfg, const moe_tensors* t,
 int moe_forward(const moe_config* cfg, const moe_tensors* t,
                 void* workspace, size_t workspace_bytes, void* stream);
 
+/* ------------------------------------------------ data-parallel statistics */
+
+/* One data-parallel exchange ("spark-gpt" README: hard counts are
+ * synchronised across DDP ranks and the differentiable local proxy is
+ * scaled so DDP averaging yields the global-batch gradient).  Each rank
+ * routes its own tokens, exports its sums with moe_route_partials, the
+ * caller all-reduces (sums) them with its collective library, and
+ * moe_route_finalize turns the global sums into the global f, p and aux.
+ *
+ * moe_route_partials: in: counts, p (from moe_route on this rank's tokens).
+ * out: sums [2E+1] fp64 device = { counts_e (E), p_e * T_real (E), T_real }.
+ * T_real is sum(counts) / k. */
+int moe_route_partials(const moe_config* cfg, const moe_tensors* t, double* sums, void* stream);
+
+/* moe_route_finalize: in: sums [2E+1] fp64 device (already summed over the
+ * ranks).  out: f, p, aux of `t` for the whole data-parallel batch
+ * (f_e = counts_e / (k T), p_e = psum_e / T, aux = E sum f p).  counts keep
+ * the rank's own values.  For the backward of the global objective, scale
+ * aux_coef and z_coef by T_real(rank) / T_real(global), and by the rank
+ * count when the caller's gradient reduction averages over ranks. */
+int moe_route_finalize(const moe_config* cfg, const moe_tensors* t, const double* sums,
+                       void* stream);
+
 /* ---------------------------------------------------------------- backward */
 
 /* a7. Gradients of J = <dY, y> + aux_coef * aux + z_coef * z_loss with the

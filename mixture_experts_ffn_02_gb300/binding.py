@@ -71,6 +71,10 @@ SIGNATURES = {
                                     c_void_p]),
     "moe_route_static": (ctypes.c_int, [ctypes.POINTER(MoEConfig), ctypes.POINTER(MoETensors),
                                         c_void_p, c_void_p]),
+    "moe_route_partials": (ctypes.c_int, [ctypes.POINTER(MoEConfig), ctypes.POINTER(MoETensors),
+                                          c_void_p, c_void_p]),
+    "moe_route_finalize": (ctypes.c_int, [ctypes.POINTER(MoEConfig), ctypes.POINTER(MoETensors),
+                                          c_void_p, c_void_p]),
 }
 
 _LIB = None
@@ -214,6 +218,20 @@ class Layer:
         check(self.lib.moe_backward(ctypes.byref(self.cfg), ctypes.byref(t), ctypes.byref(g),
                                     c_void_p(self.ws.data_ptr()), self.ws.numel(), _stream()),
               "moe_backward")
+
+    def route_partials(self, sums):
+        """This rank's routing sums into ``sums`` ([2E+1] float64, device)."""
+        t = self.tensors()
+        check(self.lib.moe_route_partials(ctypes.byref(self.cfg), ctypes.byref(t),
+                                          c_void_p(sums.data_ptr()), _stream()),
+              "moe_route_partials")
+
+    def route_finalize(self, sums):
+        """Global f, p, aux from sums added over the data-parallel ranks."""
+        t = self.tensors()
+        check(self.lib.moe_route_finalize(ctypes.byref(self.cfg), ctypes.byref(t),
+                                          c_void_p(sums.data_ptr()), _stream()),
+              "moe_route_finalize")
 
     def status(self) -> int:
         out = ctypes.c_int()

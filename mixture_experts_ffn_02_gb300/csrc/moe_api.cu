@@ -468,6 +468,28 @@ MOE_ENTRY(moe_forward, 0, {
   return do_combine(cfg, t, k);
 })
 
+int moe_route_partials(const moe_config* cfg, const moe_tensors* t, double* sums, void* stream) {
+  int rc = check_cfg(cfg);
+  if (rc) return rc;
+  if ((rc = check_device())) return rc;
+  if (!t) return MOE_ERR_NULL;
+  MOE_NEED(t->counts); MOE_NEED(t->p); MOE_NEED(sums);
+  MOE_CUDA(launch_route_partials(*cfg, t->counts, t->p, sums, static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+int moe_route_finalize(const moe_config* cfg, const moe_tensors* t, const double* sums,
+                       void* stream) {
+  int rc = check_cfg(cfg);
+  if (rc) return rc;
+  if ((rc = check_device())) return rc;
+  if (!t) return MOE_ERR_NULL;
+  MOE_NEED(sums); MOE_NEED(t->f); MOE_NEED(t->p); MOE_NEED(t->aux);
+  MOE_CUDA(launch_route_finalize(*cfg, sums, t->f, t->p, t->aux,
+                                 static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
 int moe_backward(const moe_config* cfg, const moe_tensors* t, const moe_grads* g,
                  void* workspace, size_t workspace_bytes, void* stream) {
   Call k;

@@ -585,6 +585,50 @@ route_kernel(const float* __restrict__ L, const float* __restrict__ bias,
 }
 
 // --------------------------------------------------------------------------
+// Data-parallel routing statistics: a rank's sums, and f / p / aux from sums
+// that the caller has added over the ranks.  One block; E <= 256.
+// --------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads)
+route_partials_kernel(const int32_t* __restrict__ counts, const float* __restrict__ p, int E,
+                      int k, double* __restrict__ sums) {
+  __shared__ long long tot_s;
+  if (threadIdx.x == 0) {
+    long long m = 0;
+    for (int e = 0; e < E; ++e) m += counts[e];
+    tot_s = m;
+  }
+  __syncthreads();
+  const double Tr = (double)(tot_s / k);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    sums[e] = (double)counts[e];
+    sums[E + e] = (double)p[e] * Tr;
+  }
+  if (threadIdx.x == 0) sums[2 * E] = Tr;
+}
+
+__global__ void __launch_bounds__(kThreads)
+route_finalize_kernel(const double* __restrict__ sums, int E, int k, float* __restrict__ f,
+                      float* __restrict__ p, float* __restrict__ aux) {
+  __shared__ double red[kThreads];
+  const double T = sums[2 * E];
+  double part = 0.0;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const double fe = T > 0 ? sums[e] / ((double)k * T) : 0.0;
+    const double pe = T > 0 ? sums[E + e] / T : 0.0;
+    f[e] = (float)fe;
+    p[e] = (float)pe;
+    part += fe * pe;
+  }
+  red[threadIdx.x] = part;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double s = 0.0;
+    for (int i = 0; i < (int)blockDim.x; ++i) s += red[i];
+    aux[0] = (float)((double)E * s);
+  }
+}
+
+// --------------------------------------------------------------------------
 // a2: stable counting-sort dispatch.
 // --------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads)
@@ -1152,6 +1196,18 @@ cudaError_t launch_route_scratch(const moe_config& c, const float* L, const floa
   else if (V <= 4) { MOE_ROUTE_S(4); }
   else { MOE_ROUTE_S(8); }
 #undef MOE_ROUTE_S
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_partials(const moe_config& c, const int32_t* counts, const float* p,
+                                  double* sums, cudaStream_t s) {
+  route_partials_kernel<<<1, kThreads, 0, s>>>(counts, p, c.E, c.k, sums);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_finalize(const moe_config& c, const double* sums, float* f, float* p,
+                                  float* aux, cudaStream_t s) {
+  route_finalize_kernel<<<1, kThreads, 0, s>>>(sums, c.E, c.k, f, p, aux);
   return cudaGetLastError();
 }
 

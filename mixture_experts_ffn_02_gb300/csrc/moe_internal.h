@@ -67,6 +67,10 @@ cudaError_t launch_route_scratch(const moe_config& c, const float* L, const floa
                                  int32_t* counts, float* f, float* p, float* aux, int* blk_cnt,
                                  float* blk_psum, int* blk_treal, int* done, int* status,
                                  int grid, cudaStream_t s);
+cudaError_t launch_route_partials(const moe_config& c, const int32_t* counts, const float* p,
+                                  double* sums, cudaStream_t s);
+cudaError_t launch_route_finalize(const moe_config& c, const double* sums, float* f, float* p,
+                                  float* aux, cudaStream_t s);
 cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* topk,
                            int32_t* counts, int32_t* offsets, int32_t* row_offsets,
                            int32_t* perm, int32_t* inv, void* x_perm, char* ws,
