@@ -73,6 +73,13 @@ def test_full_size_layer(cfg):
     np.testing.assert_allclose(np64(b["f"]), r["f"], rtol=STAT_RTOL)
     np.testing.assert_allclose(np64(b["p"]), r["p"], rtol=1e-4, atol=1e-7)
     assert float(b["aux"][0]) == pytest.approx(r["aux"], rel=1e-4)
+    m = O.router_metrics(L, r["counts"], real)
+    st = b["router_stats"].cpu().numpy().astype(np.float64)
+    assert st[0] == pytest.approx(m["z_loss"], rel=1e-4)
+    assert st[1] == pytest.approx(m["entropy"], rel=1e-4)
+    assert (st[2], st[3], st[5], st[6]) == (m["count_min"], m["count_max"], m["unused"],
+                                            m["T_real"])
+    assert st[4] == pytest.approx(m["count_cv"], rel=1e-5, abs=1e-7)
 
     # ---- dispatch, in full
     offsets, row_offsets, row_of_pair, perm_padded = padded_layout(r["topk_idx"], s.E)
