@@ -124,9 +124,9 @@ def launches_per_step(s, fwd_only):
     small = s.E in (4, 8, 16) and s.d * s.E * 4 + (s.d // 8) * 16 <= 96 * 1024
     tc = not small and s.E % 32 == 0
     shared = s.Hs_total > 0
-    router_fwd = 1
+    router_route = 1 if small else 2          # fused router + route, or the two kernels
     router_bwd = 5 if tc else (2 if small else 3)
-    fwd = router_fwd + 1 + 3 + 1 + 1 + (2 if shared else 0) + 1
+    fwd = router_route + 3 + 1 + 1 + (2 if shared else 0) + 1
     bwd = 1 + 1 + 1 + 2 + (4 if shared else 0) + 1 + router_bwd
     return fwd if fwd_only else fwd + bwd
 
@@ -166,24 +166,26 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=f"cuda:{local}")
 
-    gu_ev = []
+    kev = {n: [] for n in ("router_route", "permute", "gate_up", "combine")}
 
-    def step(record_gu):
-        lay.router_logits()
-        lay.route()
-        lay.permute()
-        if record_gu:
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            lay.gate_up()
-            b.record(stream)
-            gu_ev.append((a, b))
-        else:
-            lay.gate_up()
+    def timed(name, fn, record):
+        if not record:
+            fn()
+            return
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        kev[name].append((a, b))
+
+    def step(record):
+        timed("router_route", lay.router_route, record)
+        timed("permute", lay.permute, record)
+        timed("gate_up", lay.gate_up, record)
         lay.down()
         lay.shared()
-        lay.combine()
+        timed("combine", lay.combine, record)
         if training:
             lay.backward(dY)
 
@@ -216,7 +218,8 @@ def run_ours(args):
     if status != 0:
         raise RuntimeError(f"device status {status} in the timed region")
     ms = sum(a.elapsed_time(b) for a, b in ev)
-    gu_ms = sum(a.elapsed_time(b) for a, b in gu_ev) / len(gu_ev)
+    k_ms = {n: sum(a.elapsed_time(b) for a, b in v) / len(v) for n, v in kev.items()}
+    gu_ms = k_ms["gate_up"]
     ms_max, value = aggregate_ranks(ms, s.T, args.steps, world,
                                     dist if world > 1 else None, f"cuda:{local}")
     ms_per_step = ms_max / args.steps
@@ -282,6 +285,7 @@ def run_ours(args):
                      "frac_of_burst_peak": round(gu_tflops / bf16_burst, 4),
                      "algorithmic_flops_per_launch": gu_flops,
                      "avg_launch_ms": round(gu_ms, 4), "traffic": traffic},
+        "hbm_kernels": hbm_kernels(s, k_ms, hbm_peak),
         "gpu_launches": launches_per_step(s, args.fwd_only) * args.steps,
         "e2e": e2e,
         "clocks": clk,
@@ -289,6 +293,35 @@ def run_ours(args):
     if not args.no_cpu_baseline and world == 1:
         out["cpu_baseline"] = cpu_baseline(args, s)
     print(json.dumps(out), flush=True)
+
+
+def hbm_bytes(s):
+    """Algorithmic bytes of the memory-bound forward calls, each byte of the
+    tensors they must read or write counted once, in the layouts the library
+    stores (out_perm and s_out are fp32; PAD rows of the segments are not
+    counted)."""
+    T, Tr, d, E, k = s.T, (s.T_real if s.T_real is not None else s.T), s.d, s.E, s.k
+    M = Tr * k
+    valid = T if s.T_real is not None else 0
+    bias = 4 * E if s.zipf_bias > 0 else 0
+    return {
+        # x and W_r in; logits, topk_idx and gates out; valid mask and bias in
+        "router_route": T * d * 2 + d * E * 4 + T * E * 4 + T * k * 8 + valid + bias,
+        # x rows in, x_perm rows out, topk_idx in, perm + inv out
+        "permute": Tr * d * 2 + M * d * 2 + T * k * 4 + M * 4 + T * k * 4,
+        # out_perm (fp32) + s_out (fp32) in, inv + gates in, y out
+        "combine": M * d * 4 + (Tr * d * 4 if s.Hs_total else 0) + T * k * 8 + T * d * 2,
+    }
+
+
+def hbm_kernels(s, k_ms, hbm_peak):
+    out = {}
+    for name, nbytes in hbm_bytes(s).items():
+        ms = k_ms[name]
+        gbs = nbytes / (ms / 1e3) / 1e9
+        out[name] = {"avg_launch_ms": round(ms, 4), "algorithmic_bytes": nbytes,
+                     "achieved_gbs": round(gbs, 1), "frac_of_hbm_peak": round(gbs / hbm_peak, 4)}
+    return out
 
 
 def load_traffic(cfg):

@@ -197,6 +197,17 @@ int moe_router_logits(const moe_config* cfg, const moe_tensors* t,
 int moe_route(const moe_config* cfg, const moe_tensors* t,
               void* workspace, size_t workspace_bytes, void* stream);
 
+/* a0 + a1 in one call: the same results as moe_router_logits followed by
+ * moe_route (logits may differ from moe_router_logits' in the last bits,
+ * since the fp32 sums are added in another order; the routing is taken on
+ * the logits this call writes).  For E of 4, 8 or 16 with Wr in 96 KiB this
+ * is one kernel that reads x once and never reads the logits back; otherwise
+ * it runs the two steps.  "spark-gpt" README, feature list (fp32-softmax
+ * top-k router).  in: x, Wr, bias, valid.  out: logits and the outputs of
+ * moe_route.  Device errors: NONFINITE. */
+int moe_router_route(const moe_config* cfg, const moe_tensors* t,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
 /* a2. Stable counting-sort dispatch into expert-contiguous padded rows.
  * in: x, topk_idx.  out: counts, offsets, row_offsets, perm, inv, x_perm.
  * Device errors: INDEX (the pair is then dropped). */
@@ -229,7 +240,7 @@ int moe_shared_ffn(const moe_config* cfg, const moe_tensors* t,
 int moe_combine(const moe_config* cfg, const moe_tensors* t,
                 void* workspace, size_t workspace_bytes, void* stream);
 
-/* a0..a6 in order on one stream. */
+/* a0..a6 in order on one stream (a0 + a1 as moe_router_route). */
 int moe_forward(const moe_config* cfg, const moe_tensors* t,
                 void* workspace, size_t workspace_bytes, void* stream);
 
@@ -291,7 +302,8 @@ int moe_backward(const moe_config* cfg, const moe_tensors* t, const moe_grads* g
  * Scratch: a fixed array of MOE_ROUTE_STATIC_SCRATCH_BYTES in the library's
  * device memory, held by every GPU that loads the library until the process
  * exits.  A call needs 256 + B * (8 E + 4) bytes of it, B being the route
- * kernel's block count (min(304, ceil(T / G)), G = tokens per block); larger
+ * kernel's block count (min(C, ceil(T / G)), G = tokens per block, C = 456
+ * for E <= 16 and 304 above); larger
  * configurations are rejected with MOE_ERR_WORKSPACE before any work.  Every
  * E <= 128 fits at any T.
  * Set-up: the first call on each device resolves the array's device address

@@ -60,6 +60,7 @@ SIGNATURES = {
     "moe_get_status": (ctypes.c_int, [c_void_p, c_void_p, ctypes.POINTER(ctypes.c_int)]),
     "moe_router_logits": (ctypes.c_int, _STEP),
     "moe_route": (ctypes.c_int, _STEP),
+    "moe_router_route": (ctypes.c_int, _STEP),
     "moe_permute": (ctypes.c_int, _STEP),
     "moe_expert_gate_up": (ctypes.c_int, _STEP),
     "moe_expert_down": (ctypes.c_int, _STEP),
@@ -205,6 +206,7 @@ class Layer:
 
     def router_logits(self): self._step("moe_router_logits")
     def route(self): self._step("moe_route")
+    def router_route(self): self._step("moe_router_route")
     def permute(self): self._step("moe_permute")
     def gate_up(self): self._step("moe_expert_gate_up")
     def down(self): self._step("moe_expert_down")

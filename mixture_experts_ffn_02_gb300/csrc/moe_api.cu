@@ -11,6 +11,10 @@ namespace moe {
 namespace {
 
 constexpr size_t kAlign = 256;
+// Route blocks: three per SM of a 152-SM GB300 for the fused small-E router
+// (as many as its registers let reside; it streams x), two per SM for the
+// route kernel alone.
+constexpr int kRouteBlocksCapSmall = 456;
 constexpr int kRouteBlocksCap = 304;
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
@@ -23,12 +27,6 @@ int64_t row_capacity(const moe_config& c) {
 }
 
 int hs_total(const moe_config& c) { return c.n_shared > 0 ? c.n_shared * c.H_shared : 0; }
-
-int route_group_lanes(int E) {
-  int G = 1;
-  while (G < E && G < 32) G <<= 1;
-  return G;
-}
 
 }  // namespace
 
@@ -62,7 +60,8 @@ int ws_layout(const moe_config* c, int training, WsLayout* w) {
   const int G = route_group_lanes(c->E);
   const int groups = 256 / G;
   long long rb = ((long long)c->T + groups - 1) / groups;
-  if (rb > kRouteBlocksCap) rb = kRouteBlocksCap;
+  const int cap = c->E <= 16 ? kRouteBlocksCapSmall : kRouteBlocksCap;
+  if (rb > cap) rb = cap;
   if (rb < 1) rb = 1;
   w->route_blocks = (int)rb;
   w->perm_blocks = (c->T + kPermChunk - 1) / kPermChunk;
@@ -182,6 +181,21 @@ int do_route(const moe_config* c, const moe_tensors* t, Call& k) {
   MOE_NEED(t->f); MOE_NEED(t->p); MOE_NEED(t->aux); MOE_OPT(t->router_stats);
   MOE_CUDA(launch_route(*c, t->logits, t->bias, t->valid, t->topk_idx, t->gates, t->counts,
                         t->f, t->p, t->aux, t->router_stats, k.ws, k.w, k.s));
+  return MOE_OK;
+}
+
+int do_router_route(const moe_config* c, const moe_tensors* t, Call& k) {
+  if (!router_small_path(*c)) {
+    int rc = do_router_logits(c, t, k);
+    return rc ? rc : do_route(c, t, k);
+  }
+  MOE_NEED(t->x); MOE_NEED(t->Wr); MOE_NEED(t->logits);
+  MOE_OPT(t->bias); MOE_OPT(t->valid);
+  MOE_NEED(t->topk_idx); MOE_NEED(t->gates); MOE_NEED(t->counts);
+  MOE_NEED(t->f); MOE_NEED(t->p); MOE_NEED(t->aux); MOE_OPT(t->router_stats);
+  MOE_CUDA(launch_router_route(*c, t->x, t->Wr, t->bias, t->valid, t->logits, t->topk_idx,
+                               t->gates, t->counts, t->f, t->p, t->aux, t->router_stats, k.ws,
+                               k.w, k.s));
   return MOE_OK;
 }
 
@@ -453,14 +467,14 @@ int moe_get_status(void* workspace, void* stream, int* status) {
 
 MOE_ENTRY(moe_router_logits, 0, { return do_router_logits(cfg, t, k); })
 MOE_ENTRY(moe_route, 0, { return do_route(cfg, t, k); })
+MOE_ENTRY(moe_router_route, 0, { return do_router_route(cfg, t, k); })
 MOE_ENTRY(moe_permute, 0, { return do_permute(cfg, t, k); })
 MOE_ENTRY(moe_expert_gate_up, 0, { return do_gate_up(cfg, t, k); })
 MOE_ENTRY(moe_expert_down, 0, { return do_down(cfg, t, k); })
 MOE_ENTRY(moe_shared_ffn, 0, { return do_shared(cfg, t, k); })
 MOE_ENTRY(moe_combine, 0, { return do_combine(cfg, t, k); })
 MOE_ENTRY(moe_forward, 0, {
-  if ((rc = do_router_logits(cfg, t, k))) return rc;
-  if ((rc = do_route(cfg, t, k))) return rc;
+  if ((rc = do_router_route(cfg, t, k))) return rc;
   if ((rc = do_permute(cfg, t, k))) return rc;
   if ((rc = do_gate_up(cfg, t, k))) return rc;
   if ((rc = do_down(cfg, t, k))) return rc;

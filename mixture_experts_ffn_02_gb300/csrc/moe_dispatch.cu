@@ -41,15 +41,24 @@ __device__ __forceinline__ int wr_smem_index(int c, int e, int E) {
   return c * E + (c >> 3) * 4 + e;
 }
 
+// Wr [d][E] fp32 -> padded shared copy, four experts of one row per 16-byte
+// load (E is a multiple of 4), several loads in flight per thread.
+__device__ __forceinline__ void stage_wr(const float* __restrict__ Wr, float* wr_s, int d, int E) {
+  const int n4 = d * E / 4;
+#pragma unroll 4
+  for (int i4 = threadIdx.x; i4 < n4; i4 += blockDim.x) {
+    const int i = i4 * 4, c = i / E, e = i - c * E;
+    *reinterpret_cast<float4*>(wr_s + wr_smem_index(c, e, E)) =
+        __ldg(reinterpret_cast<const float4*>(Wr) + i4);
+  }
+}
+
 template <int E>
 __global__ void __launch_bounds__(kThreads)
 router_logits_small_kernel(const bf16* __restrict__ x, const float* __restrict__ Wr,
                            float* __restrict__ L, int T, int d) {
   extern __shared__ float wr_s[];
-  for (int i = threadIdx.x; i < d * E; i += blockDim.x) {
-    int c = i / E, e = i - c * E;
-    wr_s[wr_smem_index(c, e, E)] = Wr[i];
-  }
+  stage_wr(Wr, wr_s, d, E);
   __syncthreads();
   const int lane = threadIdx.x & 31;
   const int wpb = blockDim.x >> 5;
@@ -330,6 +339,264 @@ __device__ __forceinline__ bool ranks_before(float ka, int ia, float kb, int ib)
   return ka > kb || (ka == kb && ia < ib);
 }
 
+// Routes the token held by a group of G lanes.  Lane lig of the group holds
+// the logits of experts lig + G*v in lv[v] (any value where lig + G*v >= E).
+// Softmax (unbiased), top-k on the biased keys with ties to the lower index,
+// gates; writes topk and gates of a real token (-1 and 0 on PAD) and adds it
+// to the block's counts and to this lane's statistics.
+template <int V>
+__device__ __forceinline__ void route_token(const float (&lv_in)[V], const float* __restrict__ bias,
+                                            int t, bool in_range, bool real, int E, int k, int G,
+                                            int lig, int norm_topk, bool want_stats,
+                                            int32_t* __restrict__ topk, float* __restrict__ gates,
+                                            int* cnt_s, float (&psum)[V], int& my_treal,
+                                            float& z_acc, float& ent_acc, int* __restrict__ status) {
+  float lv[V], kv[V], sv[V];
+  bool bad = false;
+#pragma unroll
+  for (int v = 0; v < V; ++v) {
+    const int e = lig + G * v;
+    if (in_range && e < E) {
+      lv[v] = lv_in[v];
+      kv[v] = bias ? lv[v] + bias[e] : lv[v];
+      bad |= !isfinite(lv[v]) || !isfinite(kv[v]);
+    } else {
+      lv[v] = -FLT_MAX;
+      kv[v] = -FLT_MAX;
+    }
+  }
+  if (bad && real) set_status(status, MOE_ERR_NONFINITE);
+  // softmax over the E logits (unbiased)
+  float m = -FLT_MAX;
+#pragma unroll
+  for (int v = 0; v < V; ++v) m = fmaxf(m, lv[v]);
+  for (int o = G >> 1; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float sum = 0.f;
+#pragma unroll
+  for (int v = 0; v < V; ++v) {
+    const int e = lig + G * v;
+    sv[v] = (in_range && e < E) ? expf(lv[v] - m) : 0.f;
+    sum += sv[v];
+  }
+  for (int o = G >> 1; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+#pragma unroll
+  for (int v = 0; v < V; ++v) sv[v] = sv[v] / sum;
+  if (want_stats) {
+    // z-loss term lse^2 and entropy lse - sum_e s_e L_e of this token
+    float sl = 0.f;
+#pragma unroll
+    for (int v = 0; v < V; ++v)
+      if (lig + G * v < E) sl = fmaf(sv[v], lv[v], sl);
+    for (int o = G >> 1; o > 0; o >>= 1) sl += __shfl_xor_sync(0xffffffffu, sl, o);
+    if (real && lig == 0) {
+      const float lse = m + logf(sum);
+      z_acc = fmaf(lse, lse, z_acc);
+      ent_acc += lse - sl;
+    }
+  }
+
+  // top-k by repeated group arg-max
+  unsigned taken = 0;
+  float sel_s[V];
+  int sel_i[V];
+#pragma unroll
+  for (int v = 0; v < V; ++v) { sel_s[v] = 0.f; sel_i[v] = -1; }
+  float ssum = 0.f;
+  for (int j = 0; j < k; ++j) {
+    float bk = 0.f, bs = 0.f;
+    int bi = INT_MAX;
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+      const int e = lig + G * v;
+      if (e < E && !((taken >> v) & 1u) && ranks_before(kv[v], e, bk, bi)) {
+        bk = kv[v]; bi = e; bs = sv[v];
+      }
+    }
+    for (int o = G >> 1; o > 0; o >>= 1) {
+      float ok = __shfl_xor_sync(0xffffffffu, bk, o);
+      int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      float os = __shfl_xor_sync(0xffffffffu, bs, o);
+      if (ranks_before(ok, oi, bk, bi)) { bk = ok; bi = oi; bs = os; }
+    }
+    // the owner of the winner marks it taken
+    if (bi != INT_MAX && (bi & (G - 1)) == lig) taken |= 1u << (bi / G);
+    ssum += bs;
+#pragma unroll
+    for (int v = 0; v < V; ++v)
+      if (j == lig + G * v) { sel_s[v] = bs; sel_i[v] = bi; }
+  }
+  if (in_range) {
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+      const int j = lig + G * v;
+      if (j < k) {
+        int32_t ix = real ? sel_i[v] : -1;
+        float g = real ? (norm_topk ? sel_s[v] / ssum : sel_s[v]) : 0.f;
+        topk[(size_t)t * k + j] = ix;
+        gates[(size_t)t * k + j] = g;
+        if (real) atomicAdd(&cnt_s[sel_i[v]], 1);
+      }
+    }
+  }
+  if (real) {
+#pragma unroll
+    for (int v = 0; v < V; ++v) psum[v] += sv[v];
+    if (lig == 0) ++my_treal;
+  }
+}
+
+// End of a routing block: the block's counts, probability sums, real-token
+// count and metric sums go to per-block slots; the last block to finish adds
+// the slots up (fixed partitions combined in a fixed order, so the totals do
+// not depend on scheduling) and writes counts, f, p, aux and the metrics.
+// psum_s holds [blockDim/G][E] floats; cnt_s [E] ints with the block's counts.
+template <int V>
+__device__ __forceinline__ void route_block_end(
+    const float (&psum)[V], int my_treal, float z_acc, float ent_acc, int* cnt_s, float* psum_s,
+    int G, int lig, int grp, int E, int k, int* __restrict__ blk_cnt,
+    float* __restrict__ blk_psum, int* __restrict__ blk_treal, int* __restrict__ done,
+    int32_t* __restrict__ counts, float* __restrict__ f, float* __restrict__ p,
+    float* __restrict__ aux, float* __restrict__ blk_zent, float* __restrict__ stats) {
+  __shared__ int treal_s, tot_s, ticket_s;
+  __shared__ float red_s[kThreads / 32], zred_s[kThreads / 32], ered_s[kThreads / 32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
+  const int groups = blockDim.x / G;
+  if (threadIdx.x == 0) { treal_s = 0; tot_s = 0; }
+  __syncthreads();
+#pragma unroll
+  for (int v = 0; v < V; ++v) {
+    const int e = lig + G * v;
+    if (e < E) psum_s[grp * E + e] = psum[v];
+  }
+  if (lig == 0 && my_treal) atomicAdd(&treal_s, my_treal);
+  if (stats) {
+    z_acc = warp_sum(z_acc);
+    ent_acc = warp_sum(ent_acc);
+    if (lane == 0) { zred_s[warp] = z_acc; ered_s[warp] = ent_acc; }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    float s = 0.f;
+    for (int g2 = 0; g2 < groups; ++g2) s += psum_s[g2 * E + e];
+    blk_psum[(size_t)blockIdx.x * E + e] = s;
+    blk_cnt[(size_t)blockIdx.x * E + e] = cnt_s[e];
+  }
+  if (threadIdx.x == 0) {
+    blk_treal[blockIdx.x] = treal_s;
+    if (stats) {
+      float zs = 0.f, es = 0.f;
+      for (int w = 0; w < nwarps; ++w) { zs += zred_s[w]; es += ered_s[w]; }
+      blk_zent[2 * blockIdx.x] = zs;
+      blk_zent[2 * blockIdx.x + 1] = es;
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) ticket_s = atomicAdd(done, 1);
+  __syncthreads();
+  if (ticket_s != (int)gridDim.x - 1) return;
+
+  // last block
+  __threadfence();
+  __shared__ int fin_c[kThreads];
+  __shared__ float fin_p[kThreads];
+  const int nb = gridDim.x;
+  int tr = 0;
+  float zp = 0.f, ep = 0.f;
+  for (int b = threadIdx.x; b < nb; b += blockDim.x) {
+    tr += __ldcg(blk_treal + b);
+    if (stats) {
+      zp += __ldcg(blk_zent + 2 * b);
+      ep += __ldcg(blk_zent + 2 * b + 1);
+    }
+  }
+  if (tr) atomicAdd(&tot_s, tr);                 // integers: exact in any order
+  if (stats) {
+    zp = warp_sum(zp);
+    ep = warp_sum(ep);
+  }
+  const int Gp = blockDim.x / E;                 // threads per expert (E <= 256)
+  const int ge = threadIdx.x % E, gg = threadIdx.x / E;
+  if (gg < Gp) {
+    int c = 0;
+    float ps = 0.f;
+#pragma unroll 4
+    for (int b = gg; b < nb; b += Gp) {
+      c += __ldcg(blk_cnt + (size_t)b * E + ge);
+      ps += __ldcg(blk_psum + (size_t)b * E + ge);
+    }
+    fin_c[gg * E + ge] = c;
+    fin_p[gg * E + ge] = ps;
+  }
+  __syncthreads();                               // tot_s, fin_*; zred_s/ered_s free again
+  if (stats && lane == 0) { zred_s[warp] = zp; ered_s[warp] = ep; }
+  const int Tr = tot_s;
+  float part = 0.f;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int c = 0;
+    float ps = 0.f;
+    for (int g2 = 0; g2 < Gp; ++g2) {
+      c += fin_c[g2 * E + e];
+      ps += fin_p[g2 * E + e];
+    }
+    float fe = Tr > 0 ? (float)c / (float)((long long)k * Tr) : 0.f;
+    float pe = Tr > 0 ? ps / (float)Tr : 0.f;
+    counts[e] = c;
+    cnt_s[e] = c;
+    f[e] = fe;
+    p[e] = pe;
+    part = fmaf(fe, pe, part);
+  }
+  part = warp_sum(part);
+  if (lane == 0) red_s[warp] = part;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float s = 0.f;
+    for (int w = 0; w < nwarps; ++w) s += red_s[w];
+    aux[0] = (float)E * s;
+  }
+  if (stats && warp == 0) {
+    // routing metrics: z-loss and entropy (warp partials in warp order), and
+    // min / max / CV / unused of the counts (one warp, fixed shuffle order)
+    double sum = 0.0, sq = 0.0;
+    int cmin = INT_MAX, cmax = 0, unused = 0;
+    for (int e = lane; e < E; e += 32) {
+      const int c = cnt_s[e];
+      sum += c;
+      sq += (double)c * c;
+      cmin = min(cmin, c);
+      cmax = max(cmax, c);
+      unused += c == 0;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      sq += __shfl_xor_sync(0xffffffffu, sq, o);
+      cmin = min(cmin, __shfl_xor_sync(0xffffffffu, cmin, o));
+      cmax = max(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
+      unused += __shfl_xor_sync(0xffffffffu, unused, o);
+    }
+    if (lane == 0) {
+      float zs = 0.f, es = 0.f;
+      for (int w = 0; w < nwarps; ++w) { zs += zred_s[w]; es += ered_s[w]; }
+      const double mean = sum / E;
+      const double var = fmax(sq / E - mean * mean, 0.0);
+      stats[0] = Tr > 0 ? zs / (float)Tr : 0.f;
+      stats[1] = Tr > 0 ? es / (float)Tr : 0.f;
+      stats[2] = (float)cmin;
+      stats[3] = (float)cmax;
+      stats[4] = mean > 0 ? (float)(sqrt(var) / mean) : 0.f;
+      stats[5] = (float)unused;
+      stats[6] = (float)Tr;
+      stats[7] = 0.f;
+    }
+  }
+  if (threadIdx.x == 0) *done = 0;
+}
+
+// a1 on logits in memory.  A group of G lanes (a power of two <= 32) handles
+// one token; lane l of the group holds experts l, l+G, ... (V per lane).
 template <int V>
 __global__ void __launch_bounds__(kThreads)
 route_kernel(const float* __restrict__ L, const float* __restrict__ bias,
@@ -344,12 +611,7 @@ route_kernel(const float* __restrict__ L, const float* __restrict__ bias,
   const int groups = blockDim.x / G;
   int* cnt_s = reinterpret_cast<int*>(smem_raw);                 // [E]
   float* psum_s = reinterpret_cast<float*>(cnt_s + 256);         // [groups][E]
-  __shared__ int treal_s;
-  __shared__ int ticket_s;
-  __shared__ float red_s[kThreads / 32];
-
   for (int e = threadIdx.x; e < E; e += blockDim.x) cnt_s[e] = 0;
-  if (threadIdx.x == 0) treal_s = 0;
   __syncthreads();
 
   const int lane = threadIdx.x & 31;
@@ -360,228 +622,143 @@ route_kernel(const float* __restrict__ L, const float* __restrict__ bias,
   for (int v = 0; v < V; ++v) psum[v] = 0.f;
   int my_treal = 0;
   float z_acc = 0.f, ent_acc = 0.f;
-  __shared__ float zred_s[kThreads / 32], ered_s[kThreads / 32];
 
   const int tokens_per_iter = groups * gridDim.x;
   for (int t0 = blockIdx.x * groups; t0 < T; t0 += tokens_per_iter) {
     const int t = t0 + grp;
     const bool in_range = t < T;
     const bool real = in_range && row_real(valid, t);
-    float lv[V], kv[V], sv[V];
-    bool bad = false;
+    float lv[V];
 #pragma unroll
     for (int v = 0; v < V; ++v) {
       const int e = lig + G * v;
-      if (in_range && e < E) {
-        lv[v] = L[(size_t)t * E + e];
-        kv[v] = bias ? lv[v] + bias[e] : lv[v];
-        bad |= !isfinite(lv[v]) || !isfinite(kv[v]);
+      lv[v] = (in_range && e < E) ? L[(size_t)t * E + e] : -FLT_MAX;
+    }
+    route_token<V>(lv, bias, t, in_range, real, E, k, G, lig, norm_topk, stats != nullptr, topk,
+                   gates, cnt_s, psum, my_treal, z_acc, ent_acc, status);
+  }
+  route_block_end<V>(psum, my_treal, z_acc, ent_acc, cnt_s, psum_s, G, lig, grp, E, k, blk_cnt,
+                     blk_psum, blk_treal, done, counts, f, p, aux, blk_zent, stats);
+}
+
+// a0 + a1 in one pass for small E (4, 8 or 16).  A warp computes the logits
+// of TT = 32/G tokens at once (G = route_group_lanes(E) = max(8, E) lanes per
+// token, as in the route kernel); every W_r value read from shared memory
+// serves TT tokens, and the next 256 columns of the TT rows are loaded while
+// the current ones are used.  The TT*E sums are then reduced across the warp
+// so that lane g*G + e ends with the logit of token g, expert e, and the
+// tokens are routed in place with the route kernel's code.  The logits are
+// written once (the backward reads them) and never read back.
+template <int E>
+__global__ void __launch_bounds__(kThreads, E < 16 ? 3 : 2)
+router_route_small_kernel(const bf16* __restrict__ x, const float* __restrict__ Wr,
+                          const float* __restrict__ bias, const uint8_t* __restrict__ valid,
+                          int T, int d, int k, int norm_topk, float* __restrict__ L,
+                          int32_t* __restrict__ topk, float* __restrict__ gates,
+                          int* __restrict__ blk_cnt, float* __restrict__ blk_psum,
+                          int* __restrict__ blk_treal, int* __restrict__ done,
+                          int32_t* __restrict__ counts, float* __restrict__ f,
+                          float* __restrict__ p, float* __restrict__ aux,
+                          float* __restrict__ blk_zent, float* __restrict__ stats,
+                          int* __restrict__ status) {
+  constexpr int G = E < 8 ? 8 : E;
+  constexpr int TT = 32 / G;
+  constexpr int N = TT * E;                      // 16 or 32 sums per warp
+  extern __shared__ float wr_s[];                // padded [d][E]
+  __shared__ int cnt_s[E];
+  __shared__ float psum_s[kThreads / G * E];
+  stage_wr(Wr, wr_s, d, E);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt_s[e] = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int wpb = blockDim.x >> 5;
+  const int lig = lane % G, tig = lane / G;      // expert and token of this lane
+  const int grp = threadIdx.x / G;
+  float psum[1] = {0.f};
+  int my_treal = 0;
+  float z_acc = 0.f, ent_acc = 0.f;
+  for (long long tile = (long long)blockIdx.x * wpb + (threadIdx.x >> 5);
+       tile * TT < T; tile += (long long)gridDim.x * wpb) {
+    const int t0 = (int)(tile * TT);
+    float acc[TT][E];
+#pragma unroll
+    for (int i = 0; i < TT; ++i)
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[i][e] = 0.f;
+    uint4 raw[TT];
+#pragma unroll
+    for (int i = 0; i < TT; ++i)
+      raw[i] = (t0 + i < T && lane * 8 < d) ? ld_nc_v4(x + (size_t)(t0 + i) * d + lane * 8)
+                                            : make_uint4(0, 0, 0, 0);
+    for (int c0 = lane * 8; c0 < d; c0 += 256) {
+      uint4 cur[TT];
+#pragma unroll
+      for (int i = 0; i < TT; ++i) cur[i] = raw[i];
+      const int cn = c0 + 256;
+#pragma unroll
+      for (int i = 0; i < TT; ++i)
+        raw[i] = (t0 + i < T && cn < d) ? ld_nc_v4(x + (size_t)(t0 + i) * d + cn)
+                                        : make_uint4(0, 0, 0, 0);
+      const float* w = wr_s + wr_smem_index(c0, 0, E);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        float xu[TT];
+#pragma unroll
+        for (int i = 0; i < TT; ++i) {
+          const uint32_t wd = (&cur[i].x)[u >> 1];
+          xu[i] = __uint_as_float((u & 1) ? (wd & 0xffff0000u) : (wd << 16));
+        }
+#pragma unroll
+        for (int e4 = 0; e4 < E; e4 += 4) {
+          const float4 wv = *reinterpret_cast<const float4*>(w + u * E + e4);
+#pragma unroll
+          for (int i = 0; i < TT; ++i) {
+            acc[i][e4 + 0] = fmaf(xu[i], wv.x, acc[i][e4 + 0]);
+            acc[i][e4 + 1] = fmaf(xu[i], wv.y, acc[i][e4 + 1]);
+            acc[i][e4 + 2] = fmaf(xu[i], wv.z, acc[i][e4 + 2]);
+            acc[i][e4 + 3] = fmaf(xu[i], wv.w, acc[i][e4 + 3]);
+          }
+        }
+      }
+    }
+    // reduce-scatter of the N values v[j] = acc[j / E][j % E] over the warp:
+    // at the step with offset o the lane keeps the half of its values that
+    // its bit o selects and adds the partner's copy of that half; after
+    // log2(N) steps lane l holds value l / (32 / N), summed over the lanes
+    // that differ in the bits used, and the remaining offsets add the rest.
+    float v[N];
+#pragma unroll
+    for (int j = 0; j < N; ++j) v[j] = acc[j / E][j % E];
+#pragma unroll
+    for (int o = 16, n = N; o > 0; o >>= 1) {
+      if (n > 1) {
+        const bool upper = (lane & o) != 0;
+#pragma unroll
+        for (int j = 0; j < n / 2; ++j) {
+          const float send = upper ? v[j] : v[j + n / 2];
+          const float keep = upper ? v[j + n / 2] : v[j];
+          v[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+        n >>= 1;
       } else {
-        lv[v] = -FLT_MAX;
-        kv[v] = -FLT_MAX;
+        v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
       }
     }
-    if (bad && real) set_status(status, MOE_ERR_NONFINITE);
-    // softmax over the E logits (unbiased)
-    float m = -FLT_MAX;
-#pragma unroll
-    for (int v = 0; v < V; ++v) m = fmaxf(m, lv[v]);
-    for (int o = G >> 1; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    float sum = 0.f;
-#pragma unroll
-    for (int v = 0; v < V; ++v) {
-      const int e = lig + G * v;
-      sv[v] = (in_range && e < E) ? expf(lv[v] - m) : 0.f;
-      sum += sv[v];
-    }
-    for (int o = G >> 1; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-#pragma unroll
-    for (int v = 0; v < V; ++v) sv[v] = sv[v] / sum;
-    if (stats) {
-      // z-loss term lse^2 and entropy lse - sum_e s_e L_e of this token
-      float sl = 0.f;
-#pragma unroll
-      for (int v = 0; v < V; ++v)
-        if (lig + G * v < E) sl = fmaf(sv[v], lv[v], sl);
-      for (int o = G >> 1; o > 0; o >>= 1) sl += __shfl_xor_sync(0xffffffffu, sl, o);
-      if (real && lig == 0) {
-        const float lse = m + logf(sum);
-        z_acc = fmaf(lse, lse, z_acc);
-        ent_acc += lse - sl;
-      }
-    }
-
-    // top-k by repeated group arg-max
-    unsigned taken = 0;
-    float sel_s[V];
-    int sel_i[V];
-#pragma unroll
-    for (int v = 0; v < V; ++v) { sel_s[v] = 0.f; sel_i[v] = -1; }
-    float ssum = 0.f;
-    for (int j = 0; j < k; ++j) {
-      float bk = 0.f, bs = 0.f;
-      int bi = INT_MAX;
-#pragma unroll
-      for (int v = 0; v < V; ++v) {
-        const int e = lig + G * v;
-        if (e < E && !((taken >> v) & 1u) && ranks_before(kv[v], e, bk, bi)) {
-          bk = kv[v]; bi = e; bs = sv[v];
-        }
-      }
-      for (int o = G >> 1; o > 0; o >>= 1) {
-        float ok = __shfl_xor_sync(0xffffffffu, bk, o);
-        int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        float os = __shfl_xor_sync(0xffffffffu, bs, o);
-        if (ranks_before(ok, oi, bk, bi)) { bk = ok; bi = oi; bs = os; }
-      }
-      // the owner of the winner marks it taken
-      if (bi != INT_MAX && (bi & (G - 1)) == lig) taken |= 1u << (bi / G);
-      ssum += bs;
-#pragma unroll
-      for (int v = 0; v < V; ++v)
-        if (j == lig + G * v) { sel_s[v] = bs; sel_i[v] = bi; }
-    }
-    if (in_range) {
-#pragma unroll
-      for (int v = 0; v < V; ++v) {
-        const int j = lig + G * v;
-        if (j < k) {
-          int32_t ix = real ? sel_i[v] : -1;
-          float g = real ? (norm_topk ? sel_s[v] / ssum : sel_s[v]) : 0.f;
-          topk[(size_t)t * k + j] = ix;
-          gates[(size_t)t * k + j] = g;
-          if (real) atomicAdd(&cnt_s[sel_i[v]], 1);
-        }
-      }
-    }
-    if (real) {
-#pragma unroll
-      for (int v = 0; v < V; ++v) psum[v] += sv[v];
-      if (lig == 0) ++my_treal;
-    }
+    // lane l holds value j = l / (32 / N): token j / E, expert j % E.  With
+    // N = 32 that is already token l / G, expert l % G; with N = 16 (E = 4,
+    // G = 8) expert e of token g sits in lanes 8g + 2e and 8g + 2e + 1.
+    float my = v[0];
+    if (N == 16) my = __shfl_sync(0xffffffffu, my, (lane & ~7) + 2 * (lig & 3));
+    const int t = t0 + tig;
+    const bool in_range = t < T;
+    const bool real = in_range && row_real(valid, t);
+    if (in_range && lig < E) L[(size_t)t * E + lig] = my;
+    float lv[1] = {my};
+    route_token<1>(lv, bias, t, in_range, real, E, k, G, lig, norm_topk, stats != nullptr, topk,
+                   gates, cnt_s, psum, my_treal, z_acc, ent_acc, status);
   }
-  // block partials, reduced in a fixed order
-#pragma unroll
-  for (int v = 0; v < V; ++v) {
-    const int e = lig + G * v;
-    if (e < E) psum_s[grp * E + e] = psum[v];
-  }
-  if (lig == 0 && my_treal) atomicAdd(&treal_s, my_treal);
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    float s = 0.f;
-    for (int g2 = 0; g2 < groups; ++g2) s += psum_s[g2 * E + e];
-    blk_psum[(size_t)blockIdx.x * E + e] = s;
-    blk_cnt[(size_t)blockIdx.x * E + e] = cnt_s[e];
-  }
-  if (threadIdx.x == 0) blk_treal[blockIdx.x] = treal_s;
-  if (stats) {
-    z_acc = warp_sum(z_acc);
-    ent_acc = warp_sum(ent_acc);
-    if (lane == 0) { zred_s[threadIdx.x >> 5] = z_acc; ered_s[threadIdx.x >> 5] = ent_acc; }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      float zs = 0.f, es = 0.f;
-      for (int w = 0; w < (int)(blockDim.x >> 5); ++w) { zs += zred_s[w]; es += ered_s[w]; }
-      blk_zent[2 * blockIdx.x] = zs;
-      blk_zent[2 * blockIdx.x + 1] = es;
-    }
-  }
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) ticket_s = atomicAdd(done, 1);
-  __syncthreads();
-  if (ticket_s != (int)gridDim.x - 1) return;
-
-  // last block: totals over all blocks.  The blocks are split over the
-  // threads in a fixed partition and the partial sums are combined in
-  // partition order, so the result does not depend on scheduling.
-  __threadfence();
-  __shared__ int fin_t[kThreads];
-  __shared__ int fin_c[kThreads];
-  __shared__ float fin_p[kThreads];
-  const int nb = gridDim.x;
-  int tr = 0;
-  for (int b = threadIdx.x; b < nb; b += blockDim.x) tr += __ldcg(blk_treal + b);
-  fin_t[threadIdx.x] = tr;
-  const int Gp = blockDim.x / E;                 // threads per expert (E <= 256)
-  const int ge = threadIdx.x % E, gg = threadIdx.x / E;
-  if (gg < Gp) {
-    int c = 0;
-    float ps = 0.f;
-#pragma unroll 4
-    for (int b = gg; b < nb; b += Gp) {
-      c += __ldcg(blk_cnt + (size_t)b * E + ge);
-      ps += __ldcg(blk_psum + (size_t)b * E + ge);
-    }
-    fin_c[gg * E + ge] = c;
-    fin_p[gg * E + ge] = ps;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int t = 0;
-    for (int i = 0; i < (int)blockDim.x; ++i) t += fin_t[i];
-    treal_s = t;
-  }
-  __syncthreads();
-  const int Tr = treal_s;
-  float part = 0.f;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int c = 0;
-    float ps = 0.f;
-    for (int g2 = 0; g2 < Gp; ++g2) {
-      c += fin_c[g2 * E + e];
-      ps += fin_p[g2 * E + e];
-    }
-    float fe = Tr > 0 ? (float)c / (float)((long long)k * Tr) : 0.f;
-    float pe = Tr > 0 ? ps / (float)Tr : 0.f;
-    counts[e] = c;
-    f[e] = fe;
-    p[e] = pe;
-    part = fmaf(fe, pe, part);
-  }
-  part = warp_sum(part);
-  if (lane == 0) red_s[threadIdx.x >> 5] = part;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float s = 0.f;
-    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) s += red_s[w];
-    aux[0] = (float)E * s;
-  }
-  if (stats) {
-    // routing metrics: z-loss, entropy (block partials summed in block
-    // order), and min / max / CV / unused of the counts
-    for (int e = threadIdx.x; e < E; e += blockDim.x) cnt_s[e] = counts[e];
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      float zs = 0.f, es = 0.f;
-      for (int b = 0; b < nb; ++b) {
-        zs += __ldcg(blk_zent + 2 * b);
-        es += __ldcg(blk_zent + 2 * b + 1);
-      }
-      double mean = 0.0, sq = 0.0;
-      int cmin = INT_MAX, cmax = 0, unused = 0;
-      for (int e = 0; e < E; ++e) {
-        const int c = cnt_s[e];
-        mean += c;
-        sq += (double)c * c;
-        cmin = min(cmin, c);
-        cmax = max(cmax, c);
-        unused += c == 0;
-      }
-      mean /= E;
-      const double var = fmax(sq / E - mean * mean, 0.0);
-      stats[0] = Tr > 0 ? zs / (float)Tr : 0.f;
-      stats[1] = Tr > 0 ? es / (float)Tr : 0.f;
-      stats[2] = (float)cmin;
-      stats[3] = (float)cmax;
-      stats[4] = mean > 0 ? (float)(sqrt(var) / mean) : 0.f;
-      stats[5] = (float)unused;
-      stats[6] = (float)Tr;
-      stats[7] = 0.f;
-    }
-  }
-  if (threadIdx.x == 0) *done = 0;
+  route_block_end<1>(psum, my_treal, z_acc, ent_acc, cnt_s, psum_s, G, lig, grp, E, k, blk_cnt,
+                     blk_psum, blk_treal, done, counts, f, p, aux, blk_zent, stats);
 }
 
 // --------------------------------------------------------------------------
@@ -704,28 +881,33 @@ perm_scan_kernel(const int* __restrict__ hist, int nblk, int E, int32_t* __restr
 }
 
 // Ranks each (t, j) pair of the block's token chunk in pair order with one
-// warp (warp match + popc per 32 pairs), then copies each token's x row once
-// into its k destination rows.  The block also zeroes the pad rows of the
-// experts e = blockIdx.x (mod gridDim.x).
-__global__ void __launch_bounds__(kThreads)
+// warp (warp match + popc per 32 pairs, on the chunk's expert ids staged in
+// shared memory by one coalesced load), then copies each token's x row once
+// into its k destination rows, several 16-byte vectors in flight per lane.
+// The block also zeroes the pad rows of the experts e = blockIdx.x (mod
+// gridDim.x).
+constexpr int kScatterThreads = 512;
+__global__ void __launch_bounds__(kScatterThreads, 2)
 perm_scatter_kernel(const bf16* __restrict__ x, const int32_t* __restrict__ topk, int T,
                     int d, int k, int E, const int* __restrict__ base,
                     const int32_t* __restrict__ counts, const int32_t* __restrict__ row_offsets,
                     int32_t* __restrict__ perm, int32_t* __restrict__ inv,
                     bf16* __restrict__ x_perm) {
   __shared__ int base_s[256];
-  __shared__ int dest_s[kPermChunk * kMaxK];
+  __shared__ int dest_s[kPermChunk * kMaxK];     // expert ids, then destination rows
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int t_beg = blockIdx.x * kPermChunk;
   const int t_end = min(T, t_beg + kPermChunk);
   const int npairs = (t_end - t_beg) * k;
   for (int e = threadIdx.x; e < E; e += blockDim.x) base_s[e] = base[(size_t)blockIdx.x * E + e];
+  for (int ql = threadIdx.x; ql < npairs; ql += blockDim.x)
+    dest_s[ql] = topk[(size_t)t_beg * k + ql];
   __syncthreads();
   if (warp == 0) {
     const unsigned lt = (1u << lane) - 1u;
     for (int q0 = 0; q0 < npairs; q0 += 32) {
       const int ql = q0 + lane;
-      int e = ql < npairs ? topk[(size_t)t_beg * k + ql] : -1;
+      const int e = ql < npairs ? dest_s[ql] : -1;
       const bool ok = e >= 0 && e < E;
       const unsigned act = __ballot_sync(0xffffffffu, ok);
       int dest = -1;
@@ -748,20 +930,24 @@ perm_scatter_kernel(const bf16* __restrict__ x, const int32_t* __restrict__ topk
     if (dest >= 0) perm[dest] = (int32_t)q;
   }
   // row copies: one warp per token, each x row read once
+  constexpr int U = 4;                           // 16-byte vectors in flight per lane
   const int wpb = blockDim.x >> 5;
   for (int tl = warp; tl < t_end - t_beg; tl += wpb) {
-    const int t = t_beg + tl;
-    const bf16* src = x + (size_t)t * d;
-    int dst[kMaxK];
-    int nd = 0;
-    for (int j = 0; j < k; ++j) {
-      int r = dest_s[tl * k + j];
-      if (r >= 0) dst[nd++] = r;
-    }
-    if (nd == 0) continue;
-    for (int c0 = lane * 8; c0 < d; c0 += 256) {
-      uint4 v = ld_nc_v4(src + c0);
-      for (int j = 0; j < nd; ++j) st_v4(x_perm + (size_t)dst[j] * d + c0, v);
+    const bf16* src = x + (size_t)(t_beg + tl) * d;
+    const int* dst = dest_s + tl * k;
+    for (int c0 = lane * 8; c0 < d; c0 += 256 * U) {
+      uint4 v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (c0 + u * 256 < d) v[u] = ld_nc_v4(src + c0 + u * 256);
+      for (int j = 0; j < k; ++j) {
+        const int r = dst[j];
+        if (r < 0) continue;
+        bf16* o = x_perm + (size_t)r * d + c0;
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (c0 + u * 256 < d) st_v4(o + u * 256, v[u]);
+      }
     }
   }
   // zero pad rows
@@ -1032,6 +1218,12 @@ int small_E(int E) { return (E == 4 || E == 8 || E == 16) ? E : 0; }
 
 }  // namespace
 
+int route_group_lanes(int E) {
+  int G = 8;
+  while (G < E && G < 32) G <<= 1;
+  return G;
+}
+
 bool router_small_path(const moe_config& c) {
   const int es = small_E(c.E);
   return es > 0 && (size_t)c.d * es * 4 + (size_t)(c.d / 8) * 16 <= 96 * 1024;
@@ -1144,8 +1336,7 @@ cudaError_t launch_route(const moe_config& c, const float* L, const float* bias,
                          const uint8_t* valid, int32_t* topk, float* gates, int32_t* counts,
                          float* f, float* p, float* aux, float* stats, char* ws,
                          const WsLayout& w, cudaStream_t s) {
-  int G = 1;
-  while (G < c.E && G < 32) G <<= 1;
+  const int G = route_group_lanes(c.E);
   const int V = (c.E + G - 1) / G;
   const int groups = kThreads / G;
   const size_t smem = 256 * sizeof(int) + (size_t)groups * c.E * sizeof(float);
@@ -1180,8 +1371,7 @@ cudaError_t launch_route_scratch(const moe_config& c, const float* L, const floa
                                  int32_t* counts, float* f, float* p, float* aux, int* blk_cnt,
                                  float* blk_psum, int* blk_treal, int* done, int* status,
                                  int grid, cudaStream_t s) {
-  int G = 1;
-  while (G < c.E && G < 32) G <<= 1;
+  const int G = route_group_lanes(c.E);
   const int V = (c.E + G - 1) / G;
   const int groups = kThreads / G;
   const size_t smem = 256 * sizeof(int) + (size_t)groups * c.E * sizeof(float);
@@ -1196,6 +1386,34 @@ cudaError_t launch_route_scratch(const moe_config& c, const float* L, const floa
   else if (V <= 4) { MOE_ROUTE_S(4); }
   else { MOE_ROUTE_S(8); }
 #undef MOE_ROUTE_S
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_route(const moe_config& c, const void* x, const float* Wr,
+                                const float* bias, const uint8_t* valid, float* L, int32_t* topk,
+                                float* gates, int32_t* counts, float* f, float* p, float* aux,
+                                float* stats, char* ws, const WsLayout& w, cudaStream_t s) {
+  const size_t smem = wr_smem_bytes(c.d, c.E);
+  int* done = reinterpret_cast<int*>(ws + w.route_done);
+  cudaError_t err = cudaMemsetAsync(done, 0, sizeof(int), s);
+  if (err != cudaSuccess) return err;
+  int* cnt = reinterpret_cast<int*>(ws + w.route_cnt);
+  float* psum = reinterpret_cast<float*>(ws + w.route_psum);
+  int* treal = reinterpret_cast<int*>(ws + w.route_treal);
+  float* zent = reinterpret_cast<float*>(ws + w.route_zent);
+  int* status = reinterpret_cast<int*>(ws + w.status);
+  const int grid = w.route_blocks;        // 256 / E tokens per block and pass, as for route
+  const bf16* xb = static_cast<const bf16*>(x);
+#define MOE_RR(EE)                                                                            \
+  cudaFuncSetAttribute(router_route_small_kernel<EE>,                                         \
+                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);               \
+  router_route_small_kernel<EE><<<grid, kThreads, smem, s>>>(                                 \
+      xb, Wr, bias, valid, c.T, c.d, c.k, c.norm_topk, L, topk, gates, cnt, psum, treal, done, \
+      counts, f, p, aux, zent, stats, status)
+  if (c.E == 4) { MOE_RR(4); }
+  else if (c.E == 8) { MOE_RR(8); }
+  else { MOE_RR(16); }
+#undef MOE_RR
   return cudaGetLastError();
 }
 
@@ -1222,7 +1440,7 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* to
   perm_hist_kernel<<<nblk, kThreads, 0, s>>>(topk, c.T, c.k, c.E, hist, status);
   perm_scan_kernel<<<1, kScanThreads, 0, s>>>(hist, nblk, c.E, counts, offsets, row_offsets,
                                               base);
-  perm_scatter_kernel<<<nblk, kThreads, 0, s>>>(static_cast<const bf16*>(x), topk, c.T, c.d,
+  perm_scatter_kernel<<<nblk, kScatterThreads, 0, s>>>(static_cast<const bf16*>(x), topk, c.T, c.d,
                                                 c.k, c.E, base, counts, row_offsets, perm, inv,
                                                 static_cast<bf16*>(x_perm));
   return cudaGetLastError();

@@ -58,6 +58,11 @@ int ws_layout(const moe_config* c, int training, WsLayout* out);
 // ---- launchers of the memory-bound / SIMT kernels (moe_dispatch.cu) --------
 cudaError_t launch_router_logits(const moe_config& c, const void* x, const float* Wr,
                                  float* L, cudaStream_t s);
+// a0 + a1 fused (router_small_path only).
+cudaError_t launch_router_route(const moe_config& c, const void* x, const float* Wr,
+                                const float* bias, const uint8_t* valid, float* L, int32_t* topk,
+                                float* gates, int32_t* counts, float* f, float* p, float* aux,
+                                float* stats, char* ws, const WsLayout& w, cudaStream_t s);
 cudaError_t launch_route(const moe_config& c, const float* L, const float* bias,
                          const uint8_t* valid, int32_t* topk, float* gates, int32_t* counts,
                          float* f, float* p, float* aux, float* stats, char* ws,
@@ -91,6 +96,10 @@ cudaError_t launch_router_dx(const moe_config& c, const float* d_logits, const f
                              float* dxr, cudaStream_t s);
 cudaError_t launch_router_dw(const moe_config& c, const void* x, const float* d_logits,
                              float* dWr, float* part, int splits, cudaStream_t s);
+// Lanes that route one token: the power of two >= E, at least 8 (so the
+// fused small-E router and the route kernel share one token-to-lane layout)
+// and at most 32.
+int route_group_lanes(int E);
 bool router_small_path(const moe_config& c);
 // Router backward products on the tensor cores (E a multiple of 32 beyond the
 // small path): moe_router_tc.cu.

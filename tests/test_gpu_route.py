@@ -8,7 +8,7 @@ import torch
 from mixture_experts_ffn_02_gb300 import synth
 from mixture_experts_ffn_02_gb300.binding import Layer
 from oracle import moe_oracle as O
-from moe_check import STAT_RTOL, assert_close, np64
+from moe_check import STAT_RTOL, assert_close, logit_error_bound, np64, reconcile_selection
 
 pytestmark = pytest.mark.gpu
 
@@ -99,3 +99,56 @@ def test_router_logits_close_to_exact(cfg):
     exact = O.router_logits(inp["x"], inp["Wr"])
     # fp32 accumulation over d terms
     assert_close("logits", lay.bufs["logits"], exact, tol=1e-5)
+
+
+FUSED_CASES = [
+    # d, E, k, T, pad, zipf, norm
+    (64, 4, 2, 256, 0, 0.0, 1),
+    (1536, 4, 2, 3001, 0, 0.0, 1),          # KochiLLM width, ragged tail of the 8-token tiles
+    (512, 8, 2, 2049, 170, 0.0, 1),         # packed-batch width with a PAD tail
+    (256, 16, 4, 1003, 0, 1.1, 0),          # selection bias, no renormalisation
+    (128, 8, 8, 77, 5, 0.0, 1),             # k = E
+    (64, 4, 1, 1, 0, 0.0, 1),               # single token
+    (256, 64, 6, 500, 0, 1.1, 1),           # E > 16: the two-step path
+]
+
+
+@pytest.mark.parametrize("d,E,k,T,pad,zipf,norm", FUSED_CASES)
+def test_router_route_matches_oracle(d, E, k, T, pad, zipf, norm):
+    """moe_router_route (router and routing in one kernel for E <= 16)
+    against the oracle on exact logits, with near-ties resolved by the fp32
+    error bound; and against moe_route run on the logits it wrote, which
+    must give the same selection, gates and statistics bit for bit."""
+    s = synth.MoEShape("rr", T=T, d=d, E=E, k=k, H=64, n_shared=0, H_shared=0,
+                       T_real=(T - pad) if pad else None, zipf_bias=zipf, norm_topk=norm)
+    inp = synth.make_inputs(s, seed=d + E + T)
+    lay = Layer.create(s)
+    lay.bufs.update(x=inp["x"].cuda(), Wr=inp["Wr"].cuda(),
+                    bias=None if inp["bias"] is None else inp["bias"].cuda(),
+                    valid=None if inp["valid"] is None else inp["valid"].cuda())
+    lay.router_route()
+    torch.cuda.synchronize()
+    assert lay.status() == 0
+    b = {n: v.clone() for n, v in lay.bufs.items()
+         if n in ("logits", "topk_idx", "gates", "counts", "f", "p", "aux", "router_stats")}
+
+    L_exact = O.router_logits(inp["x"], inp["Wr"])
+    assert_close("logits", b["logits"], L_exact, tol=1e-5)
+    key = L_exact + (0.0 if inp["bias"] is None else inp["bias"].numpy().astype(np.float64))
+    real = np.ones(T, bool) if inp["valid"] is None else inp["valid"].numpy() != 0
+    sel, _ = reconcile_selection(b["topk_idx"].cpu().numpy(), key,
+                                 logit_error_bound(np64(inp["x"]), np64(inp["Wr"])), k, real)
+    r = O.route_stats(O.softmax(L_exact), sel, real, bool(norm))
+    np.testing.assert_array_equal(b["topk_idx"].cpu().numpy(), r["topk_idx"])
+    np.testing.assert_array_equal(b["counts"].cpu().numpy(), r["counts"])
+    np.testing.assert_allclose(np64(b["gates"]), r["gates"], rtol=1e-4, atol=1e-7)
+    np.testing.assert_allclose(np64(b["f"]), r["f"], rtol=STAT_RTOL)
+    np.testing.assert_allclose(np64(b["p"]), r["p"], rtol=1e-4, atol=1e-7)
+    assert float(b["aux"][0]) == pytest.approx(r["aux"], rel=1e-4)
+
+    # the separate route kernel on the same fp32 logits
+    lay.route()
+    torch.cuda.synchronize()
+    assert lay.status() == 0
+    for n in ("topk_idx", "gates", "counts", "f", "p", "aux", "router_stats"):
+        assert torch.equal(lay.bufs[n], b[n]), n
