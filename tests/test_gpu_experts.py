@@ -45,8 +45,13 @@ def _setup(T, d, E, k, H, ns, Hs, pad, skew, seed=0, training=False):
     return s, inp, valid, topk, g, lay
 
 
+@pytest.mark.parametrize("pairs", [None, "0", "1"])
 @pytest.mark.parametrize("name,T,d,E,k,H,ns,Hs,pad,skew", CASES)
-def test_expert_gemms_and_combine(name, T, d, E, k, H, ns, Hs, pad, skew):
+def test_expert_gemms_and_combine(name, T, d, E, k, H, ns, Hs, pad, skew, pairs, monkeypatch):
+    """Forward GEMMs and combine with the default kernel choice, and with
+    every product forced onto single CTAs ("0") or CTA pairs ("1")."""
+    if pairs is not None:
+        monkeypatch.setenv("MOE_GEMM_CTA_PAIRS", pairs)
     s, inp, valid, topk, g, lay = _setup(T, d, E, k, H, ns, Hs, pad, skew, training=True)
     lay.permute()
     lay.gate_up()
