@@ -234,7 +234,12 @@ __device__ __forceinline__ void issue_loads(const Tile& t, int kb, uint32_t sa, 
 }
 
 // ------------------------------------------------------------------ epilogue
-__device__ __forceinline__ float silu_f(float a) { return a / (1.f + __expf(-a)); }
+// The epilogue's results are rounded to bf16 (8 significant bits), so the
+// logistic function uses CUDA's fast exponential and approximate division
+// (errors of a few fp32 ulp).  For a -> -inf the denominator overflows to
+// +inf and the quotient is 0, the limit of both functions.
+__device__ __forceinline__ float sigmoid_f(float a) { return __fdividef(1.f, 1.f + __expf(-a)); }
+__device__ __forceinline__ float silu_f(float a) { return __fdividef(a, 1.f + __expf(-a)); }
 
 // One epilogue warp's staging slab: 32 rows x 128 bytes in shared memory,
 // 128-byte swizzled (16-byte chunk c of row r at chunk position c ^ (r % 8)),
@@ -371,7 +376,7 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const Tile& t, ui
         for (int u = 0; u < 8; ++u) {
           const float dh = __uint_as_float(r0[qq * 8 + u]);
           const float a = a8[u], b = b8[u];
-          const float sg = 1.f / (1.f + __expf(-a));
+          const float sg = sigmoid_f(a);
           da[u] = dh * b * sg * (1.f + a * (1.f - sg));
           db[u] = dh * (a * sg);
         }
@@ -774,26 +779,13 @@ cudaError_t launch_kind(const CUtensorMap& a, const CUtensorMap& b, const CUtens
   return cudaGetLastError();
 }
 
-// Which kernel a product runs on.  CTA pairs halve each SM's B traffic and
-// deepen the stage ring, which pays where the epilogue is light (DOWN, DX,
-// DW: 6-10% faster on the KochiLLM and 128-expert shapes).  With a heavy
-// epilogue (DH reads the saved pre-activations; GATE_UP writes h, a and b) a
-// pair's accumulator is freed only when both CTAs' epilogues are done, and
-// the coupling costs more than the pair gains unless the main loop is long:
-// GATE_UP pairs only for K >= 1536 (5% faster at K = 1536, 10% slower at
-// K = 1024), DH stays on single CTAs.  MOE_GEMM_CTA_PAIRS=0 / =1 forces one
-// kernel for every product (for measurement).
-bool use_pairs(int kind, int K) {
+// Which kernel the products run on: CTA pairs (6-12% faster than single CTAs
+// for every product on the KochiLLM and 128-expert shapes, 20% for DH at
+// K = 1536), or the single-CTA kernel where a cluster of two cannot be
+// launched.  MOE_GEMM_CTA_PAIRS=0 forces single CTAs (for measurement).
+bool use_pairs() {
   const char* v = getenv("MOE_GEMM_CTA_PAIRS");
-  if (v && v[0] == '0') return false;
-  if (v && v[0] == '1') return true;
-  switch (kind) {
-    case GK_DOWN:
-    case GK_DX:
-    case GK_DW: return true;
-    case GK_GATE_UP: return K >= 1536;
-    default: return false;
-  }
+  return !(v && v[0] == '0');
 }
 
 }  // namespace
@@ -919,7 +911,7 @@ cudaError_t launch_gemm(const GemmCall& g, cudaStream_t s) {
   }
   if (!ok) return cudaErrorInvalidValue;
   const int sms = di.num_sms;
-  const bool pairs = use_pairs(g.kind, g.K);
+  const bool pairs = use_pairs();
   switch (g.kind) {
     case GK_GATE_UP: return launch_kind<GK_GATE_UP>(ta, tb, to0, to1, p, sms, pairs, s);
     case GK_DOWN: return launch_kind<GK_DOWN>(ta, tb, to0, to1, p, sms, pairs, s);
