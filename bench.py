@@ -126,7 +126,7 @@ def launches_per_step(s, fwd_only):
     shared = s.Hs_total > 0
     router_route = 1 if small else 2          # fused router + route, or the two kernels
     router_bwd = 5 if tc else (2 if small else 3)
-    fwd = router_route + 3 + 1 + 1 + (2 if shared else 0) + 1
+    fwd = router_route + 3 + 1 + 1 + (2 if shared else 1)     # shared: combine in its down GEMM
     bwd = 1 + 1 + 1 + 2 + (4 if shared else 0) + 1 + router_bwd
     return fwd if fwd_only else fwd + bwd
 
@@ -167,6 +167,8 @@ def run_ours(args):
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=f"cuda:{local}")
 
     kev = {n: [] for n in ("router_route", "permute", "gate_up", "combine")}
+    if s.Hs_total:
+        del kev["combine"]
 
     def timed(name, fn, record):
         if not record:
@@ -184,8 +186,10 @@ def run_ours(args):
         timed("permute", lay.permute, record)
         timed("gate_up", lay.gate_up, record)
         lay.down()
-        lay.shared()
-        timed("combine", lay.combine, record)
+        if s.Hs_total:
+            lay.shared_combine()       # the combine runs in the shared expert's down GEMM
+        else:
+            timed("combine", lay.combine, record)
         if training:
             lay.backward(dY)
 
@@ -317,6 +321,8 @@ def hbm_bytes(s):
 def hbm_kernels(s, k_ms, hbm_peak):
     out = {}
     for name, nbytes in hbm_bytes(s).items():
+        if name not in k_ms:
+            continue
         ms = k_ms[name]
         gbs = nbytes / (ms / 1e3) / 1e9
         out[name] = {"avg_launch_ms": round(ms, 4), "algorithmic_bytes": nbytes,

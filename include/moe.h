@@ -240,7 +240,20 @@ int moe_shared_ffn(const moe_config* cfg, const moe_tensors* t,
 int moe_combine(const moe_config* cfg, const moe_tensors* t,
                 void* workspace, size_t workspace_bytes, void* stream);
 
-/* a0..a6 in order on one stream (a0 + a1 as moe_router_route). */
+/* a5 + a6 in one call.  With a shared expert (n_shared > 0) the combine runs
+ * in the epilogue of the shared expert's down GEMM: for token t the fp32 sum
+ * over slots j of gates[t][j] * out_perm[inv[t][j]] (slot order, unused
+ * slots skipped) plus the shared output, one rounding to bf16 -- the same
+ * operations, in the same order, as moe_shared_ffn followed by moe_combine,
+ * so y is identical; s_out is neither written nor read.  Without a shared
+ * expert it is moe_combine.  "KochiLLM v1.0" card, Architecture (shared
+ * expert beside the routed top-k).  in: x, valid, Ws_gu, Ws_down, out_perm,
+ * inv, gates.  out: s_h, s_ab (if non-NULL), y. */
+int moe_shared_ffn_combine(const moe_config* cfg, const moe_tensors* t,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* a0..a6 in order on one stream (a0 + a1 as moe_router_route, a5 + a6 as
+ * moe_shared_ffn_combine). */
 int moe_forward(const moe_config* cfg, const moe_tensors* t,
                 void* workspace, size_t workspace_bytes, void* stream);
 
@@ -301,11 +314,9 @@ int moe_backward(const moe_config* cfg, const moe_tensors* t, const moe_grads* g
  *
  * Scratch: a fixed array of MOE_ROUTE_STATIC_SCRATCH_BYTES in the library's
  * device memory, held by every GPU that loads the library until the process
- * exits.  A call needs 256 + B * (8 E + 4) bytes of it, B being the route
- * kernel's block count (min(C, ceil(T / G)), G = tokens per block, C = 456
- * for E <= 16 and 304 above); larger
- * configurations are rejected with MOE_ERR_WORKSPACE before any work.  Every
- * E <= 128 fits at any T.
+ * exits.  A call needs 3328 + 4 B bytes of it, B <= 456 being the route
+ * kernel's block count (the same grid as moe_route), so every valid
+ * configuration fits (MOE_ERR_WORKSPACE is kept as a guard).
  * Set-up: the first call on each device resolves the array's device address
  * (a runtime symbol query, no allocation); make that first call before any
  * stream capture.  The call itself allocates nothing: no cudaMalloc, no

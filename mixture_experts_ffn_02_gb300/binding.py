@@ -66,6 +66,7 @@ SIGNATURES = {
     "moe_expert_down": (ctypes.c_int, _STEP),
     "moe_shared_ffn": (ctypes.c_int, _STEP),
     "moe_combine": (ctypes.c_int, _STEP),
+    "moe_shared_ffn_combine": (ctypes.c_int, _STEP),
     "moe_forward": (ctypes.c_int, _STEP),
     "moe_backward": (ctypes.c_int, [ctypes.POINTER(MoEConfig), ctypes.POINTER(MoETensors),
                                     ctypes.POINTER(MoEGrads), c_void_p, ctypes.c_size_t,
@@ -212,6 +213,7 @@ class Layer:
     def down(self): self._step("moe_expert_down")
     def shared(self): self._step("moe_shared_ffn")
     def combine(self): self._step("moe_combine")
+    def shared_combine(self): self._step("moe_shared_ffn_combine")
     def forward(self): self._step("moe_forward")
 
     def backward(self, dY):

@@ -11,11 +11,10 @@ namespace moe {
 namespace {
 
 constexpr size_t kAlign = 256;
-// Route blocks: three per SM of a 152-SM GB300 for the fused small-E router
-// (as many as its registers let reside; it streams x), two per SM for the
-// route kernel alone.
-constexpr int kRouteBlocksCapSmall = 456;
-constexpr int kRouteBlocksCap = 304;
+// Route blocks: three per SM of a 152-SM GB300 (for the fused small-E
+// router, as many as its registers let reside).  moe_route_static runs the
+// same grid (its scratch holds the per-block slots of 456 blocks).
+constexpr int kRouteBlocksCap = 456;
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
@@ -60,17 +59,14 @@ int ws_layout(const moe_config* c, int training, WsLayout* w) {
   const int G = route_group_lanes(c->E);
   const int groups = 256 / G;
   long long rb = ((long long)c->T + groups - 1) / groups;
-  const int cap = c->E <= 16 ? kRouteBlocksCapSmall : kRouteBlocksCap;
-  if (rb > cap) rb = cap;
+  if (rb > kRouteBlocksCap) rb = kRouteBlocksCap;
   if (rb < 1) rb = 1;
   w->route_blocks = (int)rb;
   w->perm_blocks = (c->T + kPermChunk - 1) / kPermChunk;
   w->R_cap = row_capacity(*c);
   const int Hs = hs_total(*c);
   w->status = take(sizeof(int));
-  w->route_done = take(sizeof(int));
-  w->route_cnt = take((size_t)w->route_blocks * c->E * sizeof(int));
-  w->route_psum = take((size_t)w->route_blocks * c->E * sizeof(float));
+  w->route_done = take(kRouteAccBytes);
   w->route_treal = take((size_t)w->route_blocks * sizeof(int));
   w->route_zent = take((size_t)w->route_blocks * 2 * sizeof(float));
   w->perm_hist = take((size_t)w->perm_blocks * c->E * sizeof(int));
@@ -250,11 +246,20 @@ int do_down(const moe_config* c, const moe_tensors* t, Call& k) {
   return MOE_OK;
 }
 
-int do_shared(const moe_config* c, const moe_tensors* t, Call& k) {
+int do_combine(const moe_config* c, const moe_tensors* t, Call& k);
+
+// The shared expert; with `fold_combine` its down GEMM also performs the
+// combine (out_perm, inv, gates -> y) in its epilogue instead of writing s_out.
+int shared_ffn(const moe_config* c, const moe_tensors* t, Call& k, bool fold_combine) {
   const int Hs = hs_total(*c);
   if (Hs == 0) return MOE_OK;
   MOE_NEED(t->x); MOE_OPT(t->valid); MOE_NEED(t->Ws_gu); MOE_NEED(t->Ws_down);
-  MOE_NEED(t->s_h); MOE_NEED(t->s_out); MOE_OPT(t->s_ab);
+  MOE_NEED(t->s_h); MOE_OPT(t->s_ab);
+  if (fold_combine) {
+    MOE_NEED(t->out_perm); MOE_NEED(t->inv); MOE_NEED(t->gates); MOE_NEED(t->y);
+  } else {
+    MOE_NEED(t->s_out);
+  }
   GemmCall g{};
   g.kind = GK_GATE_UP;
   g.row_offsets = nullptr;
@@ -283,12 +288,33 @@ int do_shared(const moe_config* c, const moe_tensors* t, Call& k) {
   d.B = t->Ws_down;
   d.K = Hs;
   d.N = c->d;
-  d.out0 = t->s_out;
   d.ld0 = c->d;
-  d.out_f32 = 1;
   d.status = k.status;
+  if (fold_combine) {
+    d.out0 = t->y;
+    d.out_f32 = 0;
+    d.valid = t->valid;
+    d.comb_src = t->out_perm;
+    d.comb_inv = t->inv;
+    d.comb_gates = t->gates;
+    d.comb_k = c->k;
+  } else {
+    d.out0 = t->s_out;
+    d.out_f32 = 1;
+  }
   MOE_CUDA(launch_gemm(d, k.s));
   return MOE_OK;
+}
+
+int do_shared(const moe_config* c, const moe_tensors* t, Call& k) {
+  return shared_ffn(c, t, k, false);
+}
+
+// a5 + a6: with a shared expert, the combine runs in its down GEMM's
+// epilogue; without one, the combine kernel.
+int do_shared_combine(const moe_config* c, const moe_tensors* t, Call& k) {
+  if (hs_total(*c) == 0) return do_combine(c, t, k);
+  return shared_ffn(c, t, k, true);
 }
 
 int do_combine(const moe_config* c, const moe_tensors* t, Call& k) {
@@ -473,13 +499,13 @@ MOE_ENTRY(moe_expert_gate_up, 0, { return do_gate_up(cfg, t, k); })
 MOE_ENTRY(moe_expert_down, 0, { return do_down(cfg, t, k); })
 MOE_ENTRY(moe_shared_ffn, 0, { return do_shared(cfg, t, k); })
 MOE_ENTRY(moe_combine, 0, { return do_combine(cfg, t, k); })
+MOE_ENTRY(moe_shared_ffn_combine, 0, { return do_shared_combine(cfg, t, k); })
 MOE_ENTRY(moe_forward, 0, {
   if ((rc = do_router_route(cfg, t, k))) return rc;
   if ((rc = do_permute(cfg, t, k))) return rc;
   if ((rc = do_gate_up(cfg, t, k))) return rc;
   if ((rc = do_down(cfg, t, k))) return rc;
-  if ((rc = do_shared(cfg, t, k))) return rc;
-  return do_combine(cfg, t, k);
+  return do_shared_combine(cfg, t, k);
 })
 
 int moe_route_partials(const moe_config* cfg, const moe_tensors* t, double* sums, void* stream) {

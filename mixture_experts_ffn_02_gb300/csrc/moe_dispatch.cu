@@ -344,6 +344,14 @@ __device__ __forceinline__ bool ranks_before(float ka, int ia, float kb, int ib)
 // Softmax (unbiased), top-k on the biased keys with ties to the lower index,
 // gates; writes topk and gates of a real token (-1 and 0 on PAD) and adds it
 // to the block's counts and to this lane's statistics.
+// Unsigned key that orders finite floats like the floats themselves, with
+// -0 and +0 equal (both map to the key of +0); 0 is below every float's key.
+__device__ __forceinline__ unsigned order_key(float x) {
+  unsigned u = __float_as_uint(x);
+  if (u == 0x80000000u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
 template <int V>
 __device__ __forceinline__ void route_token(const float (&lv_in)[V], const float* __restrict__ bias,
                                             int t, bool in_range, bool real, int E, int k, int G,
@@ -379,8 +387,9 @@ __device__ __forceinline__ void route_token(const float (&lv_in)[V], const float
     sum += sv[v];
   }
   for (int o = G >> 1; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  const float rsum = 1.f / sum;
 #pragma unroll
-  for (int v = 0; v < V; ++v) sv[v] = sv[v] / sum;
+  for (int v = 0; v < V; ++v) sv[v] *= rsum;
   if (want_stats) {
     // z-loss term lse^2 and entropy lse - sum_e s_e L_e of this token
     float sl = 0.f;
@@ -395,35 +404,83 @@ __device__ __forceinline__ void route_token(const float (&lv_in)[V], const float
     }
   }
 
-  // top-k by repeated group arg-max
-  unsigned taken = 0;
+  // top-k
   float sel_s[V];
   int sel_i[V];
 #pragma unroll
   for (int v = 0; v < V; ++v) { sel_s[v] = 0.f; sel_i[v] = -1; }
   float ssum = 0.f;
-  for (int j = 0; j < k; ++j) {
-    float bk = 0.f, bs = 0.f;
-    int bi = INT_MAX;
+  if (G == 32) {
+    // one token per warp: each lane sorts its candidates once (largest key
+    // first; the sort is stable and a lane's expert indices ascend with v,
+    // so equal keys keep the lower index first), then every round takes the
+    // warp max of the lanes' head keys (order-preserving key bits) and the
+    // lowest expert index holding it (warp min); the winning lane pops its
+    // head.  k <= 32, so slot j is held by lane j.
+    unsigned key[V];
+    int eid[V];
+    float sval[V];
 #pragma unroll
     for (int v = 0; v < V; ++v) {
       const int e = lig + G * v;
-      if (e < E && !((taken >> v) & 1u) && ranks_before(kv[v], e, bk, bi)) {
-        bk = kv[v]; bi = e; bs = sv[v];
+      const bool ok = e < E;
+      key[v] = ok ? order_key(kv[v]) : 0u;
+      eid[v] = ok ? e : INT_MAX;
+      sval[v] = sv[v];
+    }
+#pragma unroll
+    for (int a = 1; a < V; ++a) {
+#pragma unroll
+      for (int b = a; b > 0; --b) {
+        if (key[b] > key[b - 1]) {
+          const unsigned tk = key[b]; key[b] = key[b - 1]; key[b - 1] = tk;
+          const int te = eid[b]; eid[b] = eid[b - 1]; eid[b - 1] = te;
+          const float ts = sval[b]; sval[b] = sval[b - 1]; sval[b - 1] = ts;
+        }
       }
     }
-    for (int o = G >> 1; o > 0; o >>= 1) {
-      float ok = __shfl_xor_sync(0xffffffffu, bk, o);
-      int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      float os = __shfl_xor_sync(0xffffffffu, bs, o);
-      if (ranks_before(ok, oi, bk, bi)) { bk = ok; bi = oi; bs = os; }
-    }
-    // the owner of the winner marks it taken
-    if (bi != INT_MAX && (bi & (G - 1)) == lig) taken |= 1u << (bi / G);
-    ssum += bs;
+    for (int j = 0; j < k; ++j) {
+      const unsigned kmax = __reduce_max_sync(0xffffffffu, key[0]);
+      const int win =
+          __reduce_min_sync(0xffffffffu, (key[0] == kmax && kmax != 0u) ? eid[0] : INT_MAX);
+      const float ws = __shfl_sync(0xffffffffu, sval[0], win == INT_MAX ? 0 : (win & 31));
+      if (eid[0] == win) {
 #pragma unroll
-    for (int v = 0; v < V; ++v)
-      if (j == lig + G * v) { sel_s[v] = bs; sel_i[v] = bi; }
+        for (int v = 0; v + 1 < V; ++v) {
+          key[v] = key[v + 1]; eid[v] = eid[v + 1]; sval[v] = sval[v + 1];
+        }
+        key[V - 1] = 0u;
+        eid[V - 1] = INT_MAX;
+      }
+      ssum += ws;
+      if (j == lig) { sel_s[0] = ws; sel_i[0] = win; }
+    }
+  } else {
+    // repeated group arg-max over the G lanes of the token
+    unsigned taken = 0;
+    for (int j = 0; j < k; ++j) {
+      float bk = 0.f, bs = 0.f;
+      int bi = INT_MAX;
+#pragma unroll
+      for (int v = 0; v < V; ++v) {
+        const int e = lig + G * v;
+        if (e < E && !((taken >> v) & 1u) && ranks_before(kv[v], e, bk, bi)) {
+          bk = kv[v]; bi = e; bs = sv[v];
+        }
+      }
+      for (int o = G >> 1; o > 0; o >>= 1) {
+        float ok = __shfl_xor_sync(0xffffffffu, bk, o);
+        int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        float os = __shfl_xor_sync(0xffffffffu, bs, o);
+        if (ranks_before(ok, oi, bk, bi)) { bk = ok; bi = oi; bs = os; }
+      }
+      // the owner of the winner marks it taken
+      if (bi != INT_MAX && (bi & (G - 1)) == lig) taken |= 1u << (bi / G);
+      ssum += bs;
+#pragma unroll
+      for (int v = 0; v < V; ++v)
+        if (j == lig + G * v) { sel_s[v] = bs; sel_i[v] = bi; }
+    }
   }
   if (in_range) {
 #pragma unroll
@@ -445,18 +502,23 @@ __device__ __forceinline__ void route_token(const float (&lv_in)[V], const float
   }
 }
 
-// End of a routing block: the block's counts, probability sums, real-token
-// count and metric sums go to per-block slots; the last block to finish adds
-// the slots up (fixed partitions combined in a fixed order, so the totals do
-// not depend on scheduling) and writes counts, f, p, aux and the metrics.
-// psum_s holds [blockDim/G][E] floats; cnt_s [E] ints with the block's counts.
+// End of a routing block.  The block's expert counts and probability sums
+// (its own tokens, summed in a fixed order) join totals kept as integers:
+// counts as they are, probability sums in fixed point with 32 fractional
+// bits, both by integer atomics, which are exact, so the totals do not depend
+// on the order the blocks finish in and the last block reads only E values.
+// The block's real-token count and metric sums go to per-block slots.  The
+// last block to finish writes counts, f, p, aux and the metrics.
+// psum_s holds [blockDim/G][E] floats; cnt_s [E] ints with the block's counts;
+// acc_cnt and acc_psum must be zero when the kernel starts.
 template <int V>
 __device__ __forceinline__ void route_block_end(
     const float (&psum)[V], int my_treal, float z_acc, float ent_acc, int* cnt_s, float* psum_s,
-    int G, int lig, int grp, int E, int k, int* __restrict__ blk_cnt,
-    float* __restrict__ blk_psum, int* __restrict__ blk_treal, int* __restrict__ done,
-    int32_t* __restrict__ counts, float* __restrict__ f, float* __restrict__ p,
-    float* __restrict__ aux, float* __restrict__ blk_zent, float* __restrict__ stats) {
+    int G, int lig, int grp, int E, int k, int* __restrict__ acc_cnt,
+    unsigned long long* __restrict__ acc_psum, int* __restrict__ blk_treal,
+    int* __restrict__ done, int32_t* __restrict__ counts, float* __restrict__ f,
+    float* __restrict__ p, float* __restrict__ aux, float* __restrict__ blk_zent,
+    float* __restrict__ stats) {
   __shared__ int treal_s, tot_s, ticket_s;
   __shared__ float red_s[kThreads / 32], zred_s[kThreads / 32], ered_s[kThreads / 32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -479,8 +541,9 @@ __device__ __forceinline__ void route_block_end(
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     float s = 0.f;
     for (int g2 = 0; g2 < groups; ++g2) s += psum_s[g2 * E + e];
-    blk_psum[(size_t)blockIdx.x * E + e] = s;
-    blk_cnt[(size_t)blockIdx.x * E + e] = cnt_s[e];
+    if (cnt_s[e]) atomicAdd(acc_cnt + e, cnt_s[e]);
+    const unsigned long long fx = __double2ull_rn((double)s * 4294967296.0);
+    if (fx) atomicAdd(acc_psum + e, fx);
   }
   if (threadIdx.x == 0) {
     blk_treal[blockIdx.x] = treal_s;
@@ -499,8 +562,6 @@ __device__ __forceinline__ void route_block_end(
 
   // last block
   __threadfence();
-  __shared__ int fin_c[kThreads];
-  __shared__ float fin_p[kThreads];
   const int nb = gridDim.x;
   int tr = 0;
   float zp = 0.f, ep = 0.f;
@@ -516,32 +577,15 @@ __device__ __forceinline__ void route_block_end(
     zp = warp_sum(zp);
     ep = warp_sum(ep);
   }
-  const int Gp = blockDim.x / E;                 // threads per expert (E <= 256)
-  const int ge = threadIdx.x % E, gg = threadIdx.x / E;
-  if (gg < Gp) {
-    int c = 0;
-    float ps = 0.f;
-#pragma unroll 4
-    for (int b = gg; b < nb; b += Gp) {
-      c += __ldcg(blk_cnt + (size_t)b * E + ge);
-      ps += __ldcg(blk_psum + (size_t)b * E + ge);
-    }
-    fin_c[gg * E + ge] = c;
-    fin_p[gg * E + ge] = ps;
-  }
-  __syncthreads();                               // tot_s, fin_*; zred_s/ered_s free again
+  __syncthreads();                               // tot_s; zred_s/ered_s free again
   if (stats && lane == 0) { zred_s[warp] = zp; ered_s[warp] = ep; }
   const int Tr = tot_s;
   float part = 0.f;
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int c = 0;
-    float ps = 0.f;
-    for (int g2 = 0; g2 < Gp; ++g2) {
-      c += fin_c[g2 * E + e];
-      ps += fin_p[g2 * E + e];
-    }
+    const int c = __ldcg(acc_cnt + e);
+    const double ps = (double)__ldcg(acc_psum + e) * (1.0 / 4294967296.0);
     float fe = Tr > 0 ? (float)c / (float)((long long)k * Tr) : 0.f;
-    float pe = Tr > 0 ? ps / (float)Tr : 0.f;
+    float pe = Tr > 0 ? (float)(ps / Tr) : 0.f;
     counts[e] = c;
     cnt_s[e] = c;
     f[e] = fe;
@@ -602,7 +646,7 @@ __global__ void __launch_bounds__(kThreads)
 route_kernel(const float* __restrict__ L, const float* __restrict__ bias,
              const uint8_t* __restrict__ valid, int T, int E, int k, int G, int norm_topk,
              int32_t* __restrict__ topk, float* __restrict__ gates,
-             int* __restrict__ blk_cnt, float* __restrict__ blk_psum,
+             int* __restrict__ acc_cnt, unsigned long long* __restrict__ acc_psum,
              int* __restrict__ blk_treal, int* __restrict__ done,
              int32_t* __restrict__ counts, float* __restrict__ f, float* __restrict__ p,
              float* __restrict__ aux, float* __restrict__ blk_zent, float* __restrict__ stats,
@@ -637,8 +681,8 @@ route_kernel(const float* __restrict__ L, const float* __restrict__ bias,
     route_token<V>(lv, bias, t, in_range, real, E, k, G, lig, norm_topk, stats != nullptr, topk,
                    gates, cnt_s, psum, my_treal, z_acc, ent_acc, status);
   }
-  route_block_end<V>(psum, my_treal, z_acc, ent_acc, cnt_s, psum_s, G, lig, grp, E, k, blk_cnt,
-                     blk_psum, blk_treal, done, counts, f, p, aux, blk_zent, stats);
+  route_block_end<V>(psum, my_treal, z_acc, ent_acc, cnt_s, psum_s, G, lig, grp, E, k, acc_cnt,
+                     acc_psum, blk_treal, done, counts, f, p, aux, blk_zent, stats);
 }
 
 // a0 + a1 in one pass for small E (4, 8 or 16).  A warp computes the logits
@@ -650,12 +694,12 @@ route_kernel(const float* __restrict__ L, const float* __restrict__ bias,
 // tokens are routed in place with the route kernel's code.  The logits are
 // written once (the backward reads them) and never read back.
 template <int E>
-__global__ void __launch_bounds__(kThreads, E < 16 ? 3 : 2)
+__global__ void __launch_bounds__(kThreads, E < 8 ? 3 : 2)
 router_route_small_kernel(const bf16* __restrict__ x, const float* __restrict__ Wr,
                           const float* __restrict__ bias, const uint8_t* __restrict__ valid,
                           int T, int d, int k, int norm_topk, float* __restrict__ L,
                           int32_t* __restrict__ topk, float* __restrict__ gates,
-                          int* __restrict__ blk_cnt, float* __restrict__ blk_psum,
+                          int* __restrict__ acc_cnt, unsigned long long* __restrict__ acc_psum,
                           int* __restrict__ blk_treal, int* __restrict__ done,
                           int32_t* __restrict__ counts, float* __restrict__ f,
                           float* __restrict__ p, float* __restrict__ aux,
@@ -757,8 +801,8 @@ router_route_small_kernel(const bf16* __restrict__ x, const float* __restrict__ 
     route_token<1>(lv, bias, t, in_range, real, E, k, G, lig, norm_topk, stats != nullptr, topk,
                    gates, cnt_s, psum, my_treal, z_acc, ent_acc, status);
   }
-  route_block_end<1>(psum, my_treal, z_acc, ent_acc, cnt_s, psum_s, G, lig, grp, E, k, blk_cnt,
-                     blk_psum, blk_treal, done, counts, f, p, aux, blk_zent, stats);
+  route_block_end<1>(psum, my_treal, z_acc, ent_acc, cnt_s, psum_s, G, lig, grp, E, k, acc_cnt,
+                     acc_psum, blk_treal, done, counts, f, p, aux, blk_zent, stats);
 }
 
 // --------------------------------------------------------------------------
@@ -1340,11 +1384,12 @@ cudaError_t launch_route(const moe_config& c, const float* L, const float* bias,
   const int V = (c.E + G - 1) / G;
   const int groups = kThreads / G;
   const size_t smem = 256 * sizeof(int) + (size_t)groups * c.E * sizeof(float);
-  int* done = reinterpret_cast<int*>(ws + w.route_done);
-  cudaError_t err = cudaMemsetAsync(done, 0, sizeof(int), s);
+  char* acc = ws + w.route_done;
+  cudaError_t err = cudaMemsetAsync(acc, 0, kRouteAccBytes, s);
   if (err != cudaSuccess) return err;
-  int* cnt = reinterpret_cast<int*>(ws + w.route_cnt);
-  float* psum = reinterpret_cast<float*>(ws + w.route_psum);
+  int* done = reinterpret_cast<int*>(acc);
+  int* cnt = reinterpret_cast<int*>(acc + kRouteAccCnt);
+  unsigned long long* psum = reinterpret_cast<unsigned long long*>(acc + kRouteAccPsum);
   int* treal = reinterpret_cast<int*>(ws + w.route_treal);
   float* zent = reinterpret_cast<float*>(ws + w.route_zent);
   int* status = reinterpret_cast<int*>(ws + w.status);
@@ -1368,18 +1413,22 @@ cudaError_t launch_route(const moe_config& c, const float* L, const float* bias,
 // workspace).  Same kernel, same arithmetic.
 cudaError_t launch_route_scratch(const moe_config& c, const float* L, const float* bias,
                                  const uint8_t* valid, int32_t* topk, float* gates,
-                                 int32_t* counts, float* f, float* p, float* aux, int* blk_cnt,
-                                 float* blk_psum, int* blk_treal, int* done, int* status,
-                                 int grid, cudaStream_t s) {
+                                 int32_t* counts, float* f, float* p, float* aux, char* acc,
+                                 int* blk_treal, int* status, int grid, cudaStream_t s) {
   const int G = route_group_lanes(c.E);
   const int V = (c.E + G - 1) / G;
   const int groups = kThreads / G;
   const size_t smem = 256 * sizeof(int) + (size_t)groups * c.E * sizeof(float);
+  cudaError_t err = cudaMemsetAsync(acc, 0, kRouteAccBytes, s);
+  if (err != cudaSuccess) return err;
+  int* done = reinterpret_cast<int*>(acc);
+  int* acc_cnt = reinterpret_cast<int*>(acc + kRouteAccCnt);
+  unsigned long long* acc_psum = reinterpret_cast<unsigned long long*>(acc + kRouteAccPsum);
 #define MOE_ROUTE_S(VV)                                                                       \
   cudaFuncSetAttribute(route_kernel<VV>, cudaFuncAttributeMaxDynamicSharedMemorySize,         \
                        (int)smem);                                                            \
   route_kernel<VV><<<grid, kThreads, smem, s>>>(L, bias, valid, c.T, c.E, c.k, G, c.norm_topk, \
-                                                topk, gates, blk_cnt, blk_psum, blk_treal, done, \
+                                                topk, gates, acc_cnt, acc_psum, blk_treal, done, \
                                                 counts, f, p, aux, nullptr, nullptr, status)
   if (V <= 1) { MOE_ROUTE_S(1); }
   else if (V <= 2) { MOE_ROUTE_S(2); }
@@ -1394,11 +1443,12 @@ cudaError_t launch_router_route(const moe_config& c, const void* x, const float*
                                 float* gates, int32_t* counts, float* f, float* p, float* aux,
                                 float* stats, char* ws, const WsLayout& w, cudaStream_t s) {
   const size_t smem = wr_smem_bytes(c.d, c.E);
-  int* done = reinterpret_cast<int*>(ws + w.route_done);
-  cudaError_t err = cudaMemsetAsync(done, 0, sizeof(int), s);
+  char* acc = ws + w.route_done;
+  cudaError_t err = cudaMemsetAsync(acc, 0, kRouteAccBytes, s);
   if (err != cudaSuccess) return err;
-  int* cnt = reinterpret_cast<int*>(ws + w.route_cnt);
-  float* psum = reinterpret_cast<float*>(ws + w.route_psum);
+  int* done = reinterpret_cast<int*>(acc);
+  int* cnt = reinterpret_cast<int*>(acc + kRouteAccCnt);
+  unsigned long long* psum = reinterpret_cast<unsigned long long*>(acc + kRouteAccPsum);
   int* treal = reinterpret_cast<int*>(ws + w.route_treal);
   float* zent = reinterpret_cast<float*>(ws + w.route_zent);
   int* status = reinterpret_cast<int*>(ws + w.status);

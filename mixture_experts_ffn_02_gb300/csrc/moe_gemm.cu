@@ -87,6 +87,12 @@ struct Params {
   int ld_aux;
   const uint8_t* valid;
   int* status;
+  // GK_DOWN with the combine folded in (dense rows = tokens): y[t] =
+  // bf16(sum_j g[t][j] comb_src[comb_inv[t][j]] + acc) into out0 (bf16)
+  const float* comb_src;
+  const int32_t* comb_inv;
+  const float* comb_gates;
+  int comb_k;
 };
 
 struct Shared {
@@ -396,7 +402,52 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const Tile& t, ui
     // GK_DOWN, GK_DX, GK_DW: 128 columns per half
     const bool no_acc = t.ksteps == 0;
     const bool three_d = KIND == GK_DW;
-    if (p.out_f32) {
+    if (KIND == GK_DOWN && p.comb_src) {
+      // the combine, for token t = row: y = sum_j g_j out_perm[inv(t, j)]
+      // (fp32, slot order, unused slots skipped) + this GEMM's value, one
+      // rounding to bf16 -- the combine kernel's operations in its order;
+      // PAD tokens get 0
+      const bool real = row_in && (p.valid == nullptr || p.valid[row] != 0);
+      const int32_t* inv_t = p.comb_inv + (size_t)row * p.comb_k;
+      const float* g_t = p.comb_gates + (size_t)row * p.comb_k;
+#pragma unroll 1
+      for (int bx = 0; bx < 2; ++bx) {             // one 64-column bf16 box per two chunks
+        const int col = t.n0 + half * 128 + bx * 64;
+        if (col >= p.N) break;
+        slab_acquire(lane);
+#pragma unroll 1
+        for (int c = 0; c < 2; ++c) {
+          float acc[32];
+#pragma unroll
+          for (int u = 0; u < 32; ++u) acc[u] = 0.f;
+          if (real) {
+            for (int j = 0; j < p.comb_k; ++j) {
+              const int r = inv_t[j];
+              if (r < 0) continue;
+              const float g = g_t[j];
+              const float* src = p.comb_src + (size_t)r * p.N + col + c * 32;
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const uint4 v = ld_nc_v4(src + i * 4);
+                acc[i * 4 + 0] = fmaf(g, __uint_as_float(v.x), acc[i * 4 + 0]);
+                acc[i * 4 + 1] = fmaf(g, __uint_as_float(v.y), acc[i * 4 + 1]);
+                acc[i * 4 + 2] = fmaf(g, __uint_as_float(v.z), acc[i * 4 + 2]);
+                acc[i * 4 + 3] = fmaf(g, __uint_as_float(v.w), acc[i * 4 + 3]);
+              }
+            }
+          }
+          __syncwarp();
+          tmem_ld32(tacc + (half * 4 + bx * 2 + c) * 32, r0);
+          tmem_ld_wait();
+#pragma unroll
+          for (int u = 0; u < 32; ++u)
+            acc[u] = real ? acc[u] + __uint_as_float(r0[u]) : 0.f;
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq) slab_put(slab, lane, c * 4 + qq, pack8(&acc[qq * 8]));
+        }
+        slab_store(slab, tmO0, lane, col, row0, 0, false);
+      }
+    } else if (p.out_f32) {
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {                // one 32-column fp32 box per chunk
         const int col = t.n0 + half * 128 + c * 32;
@@ -814,6 +865,10 @@ cudaError_t launch_gemm(const GemmCall& g, cudaStream_t s) {
   p.ld_aux = g.ld_aux;
   p.valid = g.valid;
   p.status = g.status;
+  p.comb_src = g.comb_src;
+  p.comb_inv = g.comb_inv;
+  p.comb_gates = g.comb_gates;
+  p.comb_k = g.comb_k;
   const uint64_t rows = (uint64_t)g.rows;
   bool ok = true;
   switch (g.kind) {

@@ -10,6 +10,9 @@
 namespace moe {
 
 constexpr int kRowAlign = MOE_ROW_ALIGN;  // expert segments start at multiples
+constexpr size_t kRouteAccCnt = 256;
+constexpr size_t kRouteAccPsum = kRouteAccCnt + 256 * 4;
+constexpr size_t kRouteAccBytes = kRouteAccPsum + 256 * 8;   // E <= 256
 constexpr int kPermChunk = 128;           // tokens per block in the dispatch kernels
 constexpr int kMaxK = 32;                 // experts per token supported
 constexpr int kDwTokPerBlk = 256;         // tokens per block of the small-E dW_r kernel
@@ -27,9 +30,10 @@ int device_info(DeviceInfo* out);
 // ---- workspace layout (byte offsets into the caller's workspace) -----------
 struct WsLayout {
   size_t status;        // int32 status word
-  size_t route_done;    // int32 ticket counter of the route kernel
-  size_t route_cnt;     // [route_blocks][E] int32
-  size_t route_psum;    // [route_blocks][E] fp32
+  size_t route_done;    // route totals, zeroed before each routing launch
+                        // (kRouteAccBytes): ticket counter at +0, expert
+                        // counts int32 [E] at +kRouteAccCnt, probability sums
+                        // in 2^-32 fixed point uint64 [E] at +kRouteAccPsum
   size_t route_treal;   // [route_blocks] int32
   size_t route_zent;    // [route_blocks][2] fp32 (z-loss, entropy partials)
   size_t perm_hist;     // [perm_blocks][E] int32
@@ -67,11 +71,12 @@ cudaError_t launch_route(const moe_config& c, const float* L, const float* bias,
                          const uint8_t* valid, int32_t* topk, float* gates, int32_t* counts,
                          float* f, float* p, float* aux, float* stats, char* ws,
                          const WsLayout& w, cudaStream_t s);
+// `acc` is a route-totals region of kRouteAccBytes (layout as WsLayout::
+// route_done); it is zeroed here before the kernel.
 cudaError_t launch_route_scratch(const moe_config& c, const float* L, const float* bias,
                                  const uint8_t* valid, int32_t* topk, float* gates,
-                                 int32_t* counts, float* f, float* p, float* aux, int* blk_cnt,
-                                 float* blk_psum, int* blk_treal, int* done, int* status,
-                                 int grid, cudaStream_t s);
+                                 int32_t* counts, float* f, float* p, float* aux, char* acc,
+                                 int* blk_treal, int* status, int grid, cudaStream_t s);
 cudaError_t launch_route_partials(const moe_config& c, const int32_t* counts, const float* p,
                                   double* sums, cudaStream_t s);
 cudaError_t launch_route_finalize(const moe_config& c, const double* sums, float* f, float* p,
@@ -148,8 +153,14 @@ struct GemmCall {
   int ld1;
   const void* aux_in;          // GK_DH: ab (a|b) saved by the forward
   int ld_aux;
-  const uint8_t* valid;        // GK_GATE_UP dense: zero PAD rows
+  const uint8_t* valid;        // GK_GATE_UP dense: zero PAD rows; combine: PAD tokens
   int* status;
+  // GK_DOWN over dense token rows with the combine folded into the epilogue:
+  // out0 = y (bf16) = sum_j comb_gates[t][j] comb_src[comb_inv[t][j]] + result
+  const float* comb_src;       // out_perm [R][N] fp32, or NULL (no combine)
+  const int32_t* comb_inv;     // [rows][comb_k], -1 = unused slot
+  const float* comb_gates;     // [rows][comb_k]
+  int comb_k;
 };
 cudaError_t launch_gemm(const GemmCall& g, cudaStream_t s);
 

@@ -26,7 +26,6 @@ namespace moe {
 namespace {
 
 constexpr size_t kStaticScratch = MOE_ROUTE_STATIC_SCRATCH_BYTES;
-constexpr size_t kHeader = 256;  // ticket counter, padded
 
 // The scratch itself.  Host code must not pass this name to a kernel: on the
 // host it only stands in for the symbol; its device address comes from
@@ -79,22 +78,18 @@ extern "C" int moe_route_static(const moe_config* cfg, const moe_tensors* t, int
   // Same grid as moe_route, so both produce the same bytes.
   WsLayout w;
   ws_layout(cfg, 0, &w);
-  const size_t per_block = (size_t)cfg->E * (sizeof(int) + sizeof(float)) + sizeof(int);
-  const size_t need_bytes = kHeader + (size_t)w.route_blocks * per_block;
+  // route totals (zeroed by the launch), then one int per route block
+  const size_t need_bytes = kRouteAccBytes + (size_t)w.route_blocks * sizeof(int);
   if (need_bytes > kStaticScratch) return MOE_ERR_WORKSPACE;
 
   void* base = nullptr;
   if ((rc = scratch_address(&base))) return rc;
   char* sc = static_cast<char*>(base);
-  int* done = reinterpret_cast<int*>(sc);
-  int* cnt = reinterpret_cast<int*>(sc + kHeader);
-  float* psum = reinterpret_cast<float*>(cnt + (size_t)w.route_blocks * cfg->E);
-  int* treal = reinterpret_cast<int*>(psum + (size_t)w.route_blocks * cfg->E);
+  int* treal = reinterpret_cast<int*>(sc + kRouteAccBytes);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(done, 0, sizeof(int), s) != cudaSuccess) return MOE_ERR_CUDA;
   if (launch_route_scratch(*cfg, t->logits, t->bias, t->valid, t->topk_idx, t->gates,
-                           t->counts, t->f, t->p, t->aux, cnt, psum, treal, done,
-                           device_status, w.route_blocks, s) != cudaSuccess)
+                           t->counts, t->f, t->p, t->aux, sc, treal, device_status,
+                           w.route_blocks, s) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }

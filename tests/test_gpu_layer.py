@@ -145,3 +145,24 @@ def test_backward_gemm_variants(cfg, T, pairs, monkeypatch):
     against the oracle; the default picks per product between the two."""
     monkeypatch.setenv("MOE_GEMM_CTA_PAIRS", pairs)
     test_backward_matches_oracle(cfg, T, 1)
+
+
+@pytest.mark.parametrize("cfg,T,pad", [(1, None, 0), (2, 700, 0), (4, 900, 37)])
+def test_shared_combine_fold_matches_steps(cfg, T, pad):
+    """With a shared expert, moe_forward runs the combine in the shared
+    expert's down-GEMM epilogue.  Same operations in the same order as the
+    step path (moe_shared_ffn, then moe_combine), so y is identical bit for
+    bit; PAD tokens are 0."""
+    s = scaled_shape(cfg, T)
+    if pad:
+        s = synth.scaled(s, T_real=s.T - pad)
+    inp, lay = run_layer(s)
+    y_fused = lay.bufs["y"].clone()
+    lay.bufs["y"].fill_(7.0)
+    lay.shared()
+    lay.combine()
+    torch.cuda.synchronize()
+    assert lay.status() == 0
+    assert torch.equal(y_fused, lay.bufs["y"])
+    if pad:
+        assert not y_fused[s.T - pad:].float().abs().max().item()
