@@ -127,7 +127,7 @@ def launches_per_step(s, fwd_only):
     router_route = 1 if small else 2          # fused router + route, or the two kernels
     router_bwd = 5 if tc else (2 if small else 3)
     fwd = router_route + 3 + 1 + 1 + (2 if shared else 1)     # shared: combine in its down GEMM
-    bwd = 1 + 1 + 1 + 2 + (4 if shared else 0) + 1 + router_bwd
+    bwd = 1 + 1 + 1 + 2 + (4 if shared else 1) + router_bwd   # shared: dx sum in its dx GEMM
     return fwd if fwd_only else fwd + bwd
 
 

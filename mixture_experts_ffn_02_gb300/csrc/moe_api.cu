@@ -82,7 +82,6 @@ int ws_layout(const moe_config* c, int training, WsLayout* w) {
     w->dx_perm = take(R * c->d * 4);
     if (Hs > 0) {
       w->ds_gu = take((size_t)c->T * 2 * Hs * 2);
-      w->dxs = take((size_t)c->T * c->d * 4);
     }
     if (!router_small_path(*c)) w->dxr = take((size_t)c->T * c->d * 4);
     int splits = c->T / 1024;
@@ -376,34 +375,8 @@ int do_backward(const moe_config* c, const moe_tensors* t, const moe_grads* g, C
   wg.A = d_gu; wg.lda = 2 * c->H; wg.Mdw = 2 * c->H; wg.B = t->x_perm; wg.N = c->d;
   wg.out0 = g->dW_gu; wg.ld0 = c->d; wg.status = k.status;
   MOE_CUDA(launch_gemm(wg, k.s));
-  // (v) shared expert
-  float* dxs = nullptr;
-  if (Hs > 0) {
-    void* ds_gu = k.ws + w.ds_gu;
-    dxs = reinterpret_cast<float*>(k.ws + w.dxs);
-    GemmCall sh{};
-    sh.kind = GK_DH; sh.row_offsets = nullptr; sh.E = 1; sh.rows = c->T;
-    sh.A = g->dY; sh.lda = c->d; sh.B = t->Ws_down; sh.K = c->d; sh.N = Hs; sh.H = Hs;
-    sh.out0 = ds_gu; sh.ld0 = 2 * Hs; sh.aux_in = t->s_ab; sh.ld_aux = 2 * Hs;
-    sh.status = k.status;
-    MOE_CUDA(launch_gemm(sh, k.s));
-    GemmCall sx{};
-    sx.kind = GK_DX; sx.row_offsets = nullptr; sx.E = 1; sx.rows = c->T;
-    sx.A = ds_gu; sx.lda = 2 * Hs; sx.B = t->Ws_gu; sx.K = 2 * Hs; sx.N = c->d;
-    sx.out0 = dxs; sx.ld0 = c->d; sx.out_f32 = 1; sx.status = k.status;
-    MOE_CUDA(launch_gemm(sx, k.s));
-    GemmCall sw{};
-    sw.kind = GK_DW; sw.row_offsets = nullptr; sw.E = 1; sw.rows = c->T;
-    sw.A = g->dY; sw.lda = c->d; sw.Mdw = c->d; sw.B = t->s_h; sw.N = Hs;
-    sw.out0 = g->dWs_down; sw.ld0 = Hs; sw.status = k.status;
-    MOE_CUDA(launch_gemm(sw, k.s));
-    GemmCall sg{};
-    sg.kind = GK_DW; sg.row_offsets = nullptr; sg.E = 1; sg.rows = c->T;
-    sg.A = ds_gu; sg.lda = 2 * Hs; sg.Mdw = 2 * Hs; sg.B = t->x; sg.N = c->d;
-    sg.out0 = g->dWs_gu; sg.ld0 = c->d; sg.status = k.status;
-    MOE_CUDA(launch_gemm(sg, k.s));
-  }
-  // (vi) router input gradient and the un-permute sum of dx
+  // router input gradient: on the tensor cores (E a multiple of 32), the
+  // CUDA cores (other large E), or inline in the dx sum (small E)
   float* dxr = nullptr;
   float* part = reinterpret_cast<float*>(k.ws + w.dwr_part);
   if (router_tc_path(*c)) {
@@ -415,8 +388,39 @@ int do_backward(const moe_config* c, const moe_tensors* t, const moe_grads* g, C
     dxr = reinterpret_cast<float*>(k.ws + w.dxr);
     MOE_CUDA(launch_router_dx(*c, g->d_logits, t->Wr, dxr, k.s));
   }
-  MOE_CUDA(launch_dx_gather(*c, dx_perm, t->inv, dxs, dxr, g->d_logits, t->Wr, t->valid, g->dx,
-                            k.s));
+  // (v) shared expert; (vi) the un-permute sum of dx runs in the epilogue of
+  // its dx GEMM (or, without a shared expert, in the gather kernel)
+  if (Hs > 0) {
+    void* ds_gu = k.ws + w.ds_gu;
+    GemmCall sh{};
+    sh.kind = GK_DH; sh.row_offsets = nullptr; sh.E = 1; sh.rows = c->T;
+    sh.A = g->dY; sh.lda = c->d; sh.B = t->Ws_down; sh.K = c->d; sh.N = Hs; sh.H = Hs;
+    sh.out0 = ds_gu; sh.ld0 = 2 * Hs; sh.aux_in = t->s_ab; sh.ld_aux = 2 * Hs;
+    sh.status = k.status;
+    MOE_CUDA(launch_gemm(sh, k.s));
+    GemmCall sx{};
+    sx.kind = GK_DX; sx.row_offsets = nullptr; sx.E = 1; sx.rows = c->T;
+    sx.A = ds_gu; sx.lda = 2 * Hs; sx.B = t->Ws_gu; sx.K = 2 * Hs; sx.N = c->d;
+    sx.out0 = g->dx; sx.ld0 = c->d; sx.out_f32 = 0; sx.status = k.status;
+    sx.valid = t->valid;
+    sx.comb_src = dx_perm; sx.comb_inv = t->inv; sx.comb_k = c->k;
+    sx.dl = g->d_logits; sx.wr = t->Wr; sx.rE = router_small_path(*c) ? c->E : 0;
+    sx.dxr = dxr;
+    MOE_CUDA(launch_gemm(sx, k.s));
+    GemmCall sw{};
+    sw.kind = GK_DW; sw.row_offsets = nullptr; sw.E = 1; sw.rows = c->T;
+    sw.A = g->dY; sw.lda = c->d; sw.Mdw = c->d; sw.B = t->s_h; sw.N = Hs;
+    sw.out0 = g->dWs_down; sw.ld0 = Hs; sw.status = k.status;
+    MOE_CUDA(launch_gemm(sw, k.s));
+    GemmCall sg{};
+    sg.kind = GK_DW; sg.row_offsets = nullptr; sg.E = 1; sg.rows = c->T;
+    sg.A = ds_gu; sg.lda = 2 * Hs; sg.Mdw = 2 * Hs; sg.B = t->x; sg.N = c->d;
+    sg.out0 = g->dWs_gu; sg.ld0 = c->d; sg.status = k.status;
+    MOE_CUDA(launch_gemm(sg, k.s));
+  } else {
+    MOE_CUDA(launch_dx_gather(*c, dx_perm, t->inv, nullptr, dxr, g->d_logits, t->Wr, t->valid,
+                              g->dx, k.s));
+  }
   if (!router_tc_path(*c))
     MOE_CUDA(launch_router_dw(*c, t->x, g->d_logits, g->dWr, part, w.dwr_splits, k.s));
   return MOE_OK;

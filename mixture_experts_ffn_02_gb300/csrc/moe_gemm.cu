@@ -93,6 +93,13 @@ struct Params {
   const int32_t* comb_inv;
   const float* comb_gates;
   int comb_k;
+  // GK_DX with the dx gather folded in (dense rows = tokens): dx[t] =
+  // bf16(sum_j comb_src[comb_inv[t][j]] + acc + router term) into out0; the
+  // router term is sum_e dl[t][e] wr[c][e] (rE > 0) or dxr[t][c]
+  const float* dl;
+  const float* wr;
+  int rE;
+  const float* dxr;
 };
 
 struct Shared {
@@ -444,6 +451,88 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const Tile& t, ui
             acc[u] = real ? acc[u] + __uint_as_float(r0[u]) : 0.f;
 #pragma unroll
           for (int qq = 0; qq < 4; ++qq) slab_put(slab, lane, c * 4 + qq, pack8(&acc[qq * 8]));
+        }
+        slab_store(slab, tmO0, lane, col, row0, 0, false);
+      }
+    } else if (KIND == GK_DX && p.comb_src) {
+      // the dx gather, for token t = row: dx = sum_j dx_perm[inv(t, j)]
+      // (slot order, unused slots skipped) + this GEMM's value + the router
+      // term, one rounding to bf16 -- the gather kernel's operations in its
+      // order; PAD tokens get 0
+      const bool real = row_in && (p.valid == nullptr || p.valid[row] != 0);
+      const int32_t* inv_t = p.comb_inv + (size_t)row * p.comb_k;
+      const float4* dl_t = reinterpret_cast<const float4*>(p.dl + (size_t)row * p.rE);
+#pragma unroll 1
+      for (int bx = 0; bx < 2; ++bx) {             // one 64-column bf16 box per two chunks
+        const int col = t.n0 + half * 128 + bx * 64;
+        if (col >= p.N) break;
+        slab_acquire(lane);
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {              // 16 columns at a time
+          const int c0 = col + c * 16;
+          float acc[16];
+#pragma unroll
+          for (int u = 0; u < 16; ++u) acc[u] = 0.f;
+          if (real) {
+            for (int j = 0; j < p.comb_k; ++j) {
+              const int r = inv_t[j];
+              if (r < 0) continue;
+              const float* src = p.comb_src + (size_t)r * p.N + c0;
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const uint4 v = ld_nc_v4(src + i * 4);
+                acc[i * 4 + 0] += __uint_as_float(v.x);
+                acc[i * 4 + 1] += __uint_as_float(v.y);
+                acc[i * 4 + 2] += __uint_as_float(v.z);
+                acc[i * 4 + 3] += __uint_as_float(v.w);
+              }
+            }
+          }
+          uint32_t r16[16];
+          __syncwarp();
+          tmem_ld16(tacc + (half * 4 + bx * 2) * 32 + c * 16, r16);
+          tmem_ld_wait();
+          if (real) {
+#pragma unroll
+            for (int u = 0; u < 16; ++u) acc[u] += __uint_as_float(r16[u]);
+            if (p.rE > 0) {
+              // sum_e dl[t][e] W_r[c][e] per column c, e in order (experts
+              // outside, columns inside: 16 running sums, 4 coefficients live)
+              float sr[16];
+#pragma unroll
+              for (int u = 0; u < 16; ++u) sr[u] = 0.f;
+#pragma unroll 1
+              for (int e4 = 0; e4 < p.rE; e4 += 4) {
+                const float4 dv = __ldg(dl_t + e4 / 4);
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                  const float4 wv =
+                      __ldg(reinterpret_cast<const float4*>(p.wr + (size_t)(c0 + u) * p.rE + e4));
+                  sr[u] = fmaf(dv.x, wv.x, sr[u]);
+                  sr[u] = fmaf(dv.y, wv.y, sr[u]);
+                  sr[u] = fmaf(dv.z, wv.z, sr[u]);
+                  sr[u] = fmaf(dv.w, wv.w, sr[u]);
+                }
+              }
+#pragma unroll
+              for (int u = 0; u < 16; ++u) acc[u] += sr[u];
+            } else if (p.dxr) {
+              const float* pr = p.dxr + (size_t)row * p.N + c0;
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const uint4 v = ld_nc_v4(pr + i * 4);
+                acc[i * 4 + 0] += __uint_as_float(v.x);
+                acc[i * 4 + 1] += __uint_as_float(v.y);
+                acc[i * 4 + 2] += __uint_as_float(v.z);
+                acc[i * 4 + 3] += __uint_as_float(v.w);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int u = 0; u < 16; ++u) acc[u] = 0.f;
+          }
+          slab_put(slab, lane, c * 2, pack8(&acc[0]));
+          slab_put(slab, lane, c * 2 + 1, pack8(&acc[8]));
         }
         slab_store(slab, tmO0, lane, col, row0, 0, false);
       }
@@ -869,6 +958,10 @@ cudaError_t launch_gemm(const GemmCall& g, cudaStream_t s) {
   p.comb_inv = g.comb_inv;
   p.comb_gates = g.comb_gates;
   p.comb_k = g.comb_k;
+  p.dl = g.dl;
+  p.wr = g.wr;
+  p.rE = g.rE;
+  p.dxr = g.dxr;
   const uint64_t rows = (uint64_t)g.rows;
   bool ok = true;
   switch (g.kind) {

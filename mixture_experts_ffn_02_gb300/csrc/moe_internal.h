@@ -161,6 +161,13 @@ struct GemmCall {
   const int32_t* comb_inv;     // [rows][comb_k], -1 = unused slot
   const float* comb_gates;     // [rows][comb_k]
   int comb_k;
+  // GK_DX over dense token rows with the dx gather folded into the epilogue:
+  // out0 = dx (bf16) = sum_j comb_src[comb_inv[t][j]] + result + router term,
+  // the router term sum_e dl[t][e] wr[c][e] (rE in {4, 8, 16}) or dxr[t][c]
+  const float* dl;             // d_logits [rows][rE]
+  const float* wr;             // W_r [N][rE]
+  int rE;                      // 0: no inline router term
+  const float* dxr;            // [rows][N] fp32 router term, or NULL
 };
 cudaError_t launch_gemm(const GemmCall& g, cudaStream_t s);
 
