@@ -185,6 +185,7 @@ router_dw_small_kernel(const bf16* __restrict__ x, const float* __restrict__ dL,
     for (int u = 0; u < 8; ++u)
 #pragma unroll
       for (int e = 0; e < E; ++e) acc[u][e] = 0.f;
+#pragma unroll 8
     for (int tl = s; tl < nt; tl += slices) {
       float xf[8];
       unpack8(ld_nc_v4(x + (size_t)(t0 + tl) * d + g * 8), xf);
@@ -224,7 +225,10 @@ router_logits_sgemm_kernel(const bf16* __restrict__ x, const float* __restrict__
   __shared__ __align__(16) float As[2][BK][BT + 4];
   __shared__ __align__(16) float Bs[2][BK][BE + 4];
   const int tid = threadIdx.x;
-  const int tx = tid & 15, ty = tid >> 4;       // experts tx*TE.., tokens ty*8..
+  // thread (tx, ty): tokens ty*8 .. ty*8+7 and experts 64 j + 4 tx .. +3 for
+  // j < TE/4, so that each quarter-warp reads one contiguous 128-byte span of
+  // the B slice (no bank conflicts)
+  const int tx = tid & 15, ty = tid >> 4;
   const int t0 = blockIdx.y * BT, e0 = blockIdx.x * BE;
   // A slice: thread -> token tid/2, k-half (tid%2)*8 (one 16-byte load)
   const int at = tid >> 1, ak = (tid & 1) * 8;
@@ -276,7 +280,7 @@ router_logits_sgemm_kernel(const bf16* __restrict__ x, const float* __restrict__
       float b[TE];
 #pragma unroll
       for (int j = 0; j < TE; j += 4) {
-        const float4 bv = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * TE + j]);
+        const float4 bv = *reinterpret_cast<const float4*>(&Bs[buf][kk][(j / 4) * 64 + tx * 4]);
         b[j] = bv.x; b[j + 1] = bv.y; b[j + 2] = bv.z; b[j + 3] = bv.w;
       }
 #pragma unroll
@@ -296,7 +300,7 @@ router_logits_sgemm_kernel(const bf16* __restrict__ x, const float* __restrict__
     if (t >= T) continue;
 #pragma unroll
     for (int j = 0; j < TE; j += 4) {
-      const int e = e0 + tx * TE + j;
+      const int e = e0 + (j / 4) * 64 + tx * 4;
       if (e < E)
         *reinterpret_cast<float4*>(L + (size_t)t * E + e) =
             make_float4(acc[i][j], acc[i][j + 1], acc[i][j + 2], acc[i][j + 3]);
@@ -1343,18 +1347,21 @@ cudaError_t launch_router_dw(const moe_config& c, const void* x, const float* dL
     const int nparts = router_dw_small_parts(c);
     const size_t smem = (size_t)kDwTokPerBlk * c.E * sizeof(float);
     const bf16* xb = static_cast<const bf16*>(x);
+    // exactly groups x slices threads (no idle thread when d/8 < 256)
+    const int groups = c.d / 8;
+    const int threads = groups >= kThreads ? kThreads : groups * (kThreads / groups);
     switch (c.E) {
       case 4:
-        router_dw_small_kernel<4><<<nblk, kThreads, smem, s>>>(xb, dL, part, c.T, c.d,
-                                                               kDwTokPerBlk);
+        router_dw_small_kernel<4><<<nblk, threads, smem, s>>>(xb, dL, part, c.T, c.d,
+                                                              kDwTokPerBlk);
         break;
       case 8:
-        router_dw_small_kernel<8><<<nblk, kThreads, smem, s>>>(xb, dL, part, c.T, c.d,
-                                                               kDwTokPerBlk);
+        router_dw_small_kernel<8><<<nblk, threads, smem, s>>>(xb, dL, part, c.T, c.d,
+                                                              kDwTokPerBlk);
         break;
       default:
-        router_dw_small_kernel<16><<<nblk, kThreads, smem, s>>>(xb, dL, part, c.T, c.d,
-                                                                kDwTokPerBlk);
+        router_dw_small_kernel<16><<<nblk, threads, smem, s>>>(xb, dL, part, c.T, c.d,
+                                                               kDwTokPerBlk);
         break;
     }
     const int n = c.d * c.E;
