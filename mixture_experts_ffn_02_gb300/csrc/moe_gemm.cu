@@ -53,17 +53,22 @@ constexpr int MAX_STAGES = 6;
 constexpr size_t SMEM_BYTES = 232448;
 constexpr size_t SHARED_RESERVE = 3072;
 
-// Geometry per CTA-group size.  CG = 1: one CTA computes a 128 x 256 tile
-// and holds all of B.  CG = 2: a CTA pair computes a 256 x 256 tile, each CTA
-// holding its 128 rows of A and half of B (128 of the 256 columns), so a
-// stage is 32 KB and six stages fit.
-template <int CG>
+// Geometry per product and CTA-group size.  CG = 1: one CTA computes a
+// 128 x 256 tile and holds all of B.  CG = 2: a CTA pair computes a 256 x 256
+// tile, each CTA holding its 128 rows of A and half of B (128 of the 256
+// columns), so a stage is 32 KB and six stages fit.  GK_DH gives one stage up
+// for a 4 KB buffer per epilogue warp into which TMA loads the saved a and b
+// of the warp's next 32-column chunk.
+constexpr int AB_BYTES = 2 * 32 * 64;    // a and b boxes: 32 rows x 32 bf16 each
+template <int KIND, int CG>
 struct Geo {
-  static constexpr int STAGES = CG == 2 ? 6 : 4;
+  static constexpr int AB_BUF = KIND == GK_DH ? EPI_WARPS * AB_BYTES : 0;
+  static constexpr int STAGES = (CG == 2 ? 6 : 4) - (KIND == GK_DH ? 1 : 0);
   static constexpr int B_BYTES = (BN / CG) * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
-  static_assert(SHARED_RESERVE + RING_BYTES + (size_t)EPI_WARPS * SLAB_BYTES <= SMEM_BYTES,
+  static_assert(SHARED_RESERVE + RING_BYTES + (size_t)EPI_WARPS * SLAB_BYTES + AB_BUF <=
+                    SMEM_BYTES,
                 "shared memory layout exceeds 227 KB");
 };
 
@@ -108,6 +113,7 @@ struct Shared {
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
+  uint64_t abfull[EPI_WARPS];  // GK_DH: a|b chunk of each epilogue warp landed
   uint32_t tmem_base;
   int abort_flag;
   int roff[257];               // padded segment offsets (row-grouped kinds)
@@ -226,7 +232,7 @@ __device__ __forceinline__ void issue_loads(const Tile& t, int kb, uint32_t sa, 
       tma_load_4d_pair(sb, tmB, bar, k0, t.n0, rank, t.e);
     } else {
       tma_load_4d(sb, tmB, bar, k0, t.n0, 0, t.e);
-      tma_load_4d(sb + Geo<CG>::B_BYTES / 2, tmB, bar, k0, t.n0, 1, t.e);
+      tma_load_4d(sb + Geo<KIND, CG>::B_BYTES / 2, tmB, bar, k0, t.n0, 1, t.e);
     }
   } else if (KIND == GK_DOWN) {
     tma_2d<KIND, CG>(sa, tmA, bar, ka, t.m0);
@@ -283,21 +289,35 @@ __device__ __forceinline__ void slab_store(const Slab& s, const CUtensorMap* m, 
   }
 }
 
-// The saved pre-activations a and b of one 32-column chunk of one row (DH
-// epilogue), loaded ahead of their use.
-struct AbChunk {
-  uint4 a[4], b[4];
+// GK_DH: the saved pre-activations a and b of one epilogue warp's 32 rows and
+// one 32-column chunk, loaded by TMA (two 32 x 32 bf16 boxes in the 64-byte
+// swizzle, a then b) into the warp's 4 KB buffer, completing on its mbarrier.
+struct AbPipe {
+  unsigned char* gen;
+  uint32_t addr;
+  uint32_t bar;
+  uint32_t phase;
+  bool pending;
 };
-__device__ __forceinline__ void load_ab_chunk(const Params& p, const Tile& t, int row, bool row_in,
-                                              int half, int c, AbChunk& v) {
-  const int col = t.n0 + half * 128 + c * 32;
-  const bool ok = row_in && col < p.N;
-  const bf16* ap = p.aux_in + (size_t)row * p.ld_aux + col;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    v.a[i] = ok ? *reinterpret_cast<const uint4*>(ap + i * 8) : make_uint4(0, 0, 0, 0);
-    v.b[i] = ok ? *reinterpret_cast<const uint4*>(ap + p.H + i * 8) : make_uint4(0, 0, 0, 0);
+__device__ __forceinline__ int ab_col(const Tile& t, int half, int c) {
+  return t.n0 + half * 128 + c * 32;
+}
+__device__ __forceinline__ void ab_issue(AbPipe& ab, const CUtensorMap* tm, const Params& p,
+                                         const Tile& t, int row0, int half, int c, int lane) {
+  const int col = ab_col(t, half, c);
+  if (col >= p.N) return;
+  if (lane == 0) {
+    mbar_arrive_expect_tx(ab.bar, AB_BYTES);
+    tma_load_2d(ab.addr, tm, ab.bar, col, row0);
+    tma_load_2d(ab.addr + AB_BYTES / 2, tm, ab.bar, col + p.H, row0);
   }
+  ab.pending = true;
+}
+__device__ __forceinline__ bool ab_wait(AbPipe& ab, volatile int* abort_flag) {
+  const bool ok = mbar_wait_bounded(ab.bar, ab.phase, abort_flag, WAIT_NS);
+  ab.phase ^= 1u;
+  ab.pending = false;
+  return ok;
 }
 
 // Epilogue of one tile for one warp: TMEM lanes (rows) q*32 .. q*32+31 and
@@ -309,7 +329,7 @@ template <int KIND>
 __device__ __forceinline__ void epilogue_tile(const Params& p, const Tile& t, uint32_t tacc,
                                               int q, int lane, int half, const Slab& slab,
                                               const CUtensorMap* tmO0, const CUtensorMap* tmO1,
-                                              AbChunk& pre) {
+                                              AbPipe& ab, volatile int* abort_flag) {
   const int row0 = t.m0 + q * 32;
   const int row = row0 + lane;
   const int row_end = t.row_end;
@@ -363,19 +383,32 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const Tile& t, ui
     }
   } else if (KIND == GK_DH) {
     // dH -> (da, db) with the saved pre-activations a, b, one 32-column chunk
-    // at a time: da fills the slab's first half and db its second, each a
-    // 32 x 64-byte box in the 64-byte swizzle (16-byte chunk c of row r at
-    // c ^ ((r / 2) % 4)), stored to d_gu at columns col and H + col.
-    // `pre` holds chunk 0 (loaded before the accumulator was waited for);
-    // chunk c + 1 is loaded while chunk c is computed
+    // at a time: a|b of chunk c arrive by TMA (chunk 0 was issued before the
+    // accumulator was waited for; chunk c + 1 is issued once chunk c is in
+    // registers); da fills the slab's first half and db its second, each a
+    // 32 x 64-byte box in the 64-byte swizzle (16-byte chunk q of row r at
+    // q ^ ((r / 2) % 4)), stored to d_gu at columns col and H + col.
+    const int swz = (lane >> 1) & 3;
 #pragma unroll 1
     for (int c = 0; c < 4; ++c) {
-      const int col = t.n0 + half * 128 + c * 32;
+      const int col = ab_col(t, half, c);
       if (col >= p.N) break;
+      if (!ab_wait(ab, abort_flag)) {
+        if (lane == 0) {
+          set_status(p.status, MOE_ERR_TIMEOUT);
+          *abort_flag = 1;
+        }
+        return;
+      }
       uint4 av[4], bv[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) { av[i] = pre.a[i]; bv[i] = pre.b[i]; }
-      if (c + 1 < 4) load_ab_chunk(p, t, row, row_in, half, c + 1, pre);
+      for (int qq = 0; qq < 4; ++qq) {
+        const int pos = ((qq ^ swz) << 4) + lane * 64;
+        av[qq] = *reinterpret_cast<const uint4*>(ab.gen + pos);
+        bv[qq] = *reinterpret_cast<const uint4*>(ab.gen + AB_BYTES / 2 + pos);
+      }
+      __syncwarp();
+      if (c + 1 < 4) ab_issue(ab, tmO1, p, t, row0, half, c + 1, lane);
       __syncwarp();
       tmem_ld32(tacc + (half * 4 + c) * 32, r0);
       tmem_ld_wait();
@@ -393,7 +426,7 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const Tile& t, ui
           da[u] = dh * b * sg * (1.f + a * (1.f - sg));
           db[u] = dh * (a * sg);
         }
-        const int pos = (qq ^ ((lane >> 1) & 3)) << 4;
+        const int pos = (qq ^ swz) << 4;
         *reinterpret_cast<uint4*>(slab.gen + lane * 64 + pos) = pack8(da);
         *reinterpret_cast<uint4*>(slab.gen + 2048 + lane * 64 + pos) = pack8(db);
       }
@@ -589,19 +622,21 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmO0,
                     const __grid_constant__ CUtensorMap tmO1, const Params p) {
-  using G = Geo<CG>;
+  using G = Geo<KIND, CG>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + (uint32_t)sizeof(Shared) + 1023u) & ~1023u;
   // the layout must fit the allocation (it does whenever the dynamic region
   // starts 1024-byte aligned); both CTAs of a pair see the same addresses,
   // so both return here together
-  if (base - raw + (size_t)G::RING_BYTES + (size_t)EPI_WARPS * SLAB_BYTES > SMEM_BYTES) {
+  if (base - raw + (size_t)G::RING_BYTES + (size_t)EPI_WARPS * SLAB_BYTES + G::AB_BUF >
+      SMEM_BYTES) {
     if (threadIdx.x == 0) set_status(p.status, MOE_ERR_DEVICE);
     return;
   }
   Shared& sh = *reinterpret_cast<Shared*>(smem_raw);
   unsigned char* slabs = smem_raw + (base - raw) + (size_t)G::RING_BYTES;
+  unsigned char* abbuf = slabs + (size_t)EPI_WARPS * SLAB_BYTES;   // GK_DH only
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = CG == 2 ? (int)cluster_ctarank() : 0;
@@ -618,12 +653,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       mbar_init(smem_u32(&sh.tempty[a]), CG == 2 ? 2 * EPI_WARPS : EPI_THREADS);
     }
     mbar_init(smem_u32(&sh.drain), 1);
+    for (int w = 0; w < EPI_WARPS; ++w) mbar_init(smem_u32(&sh.abfull[w]), 1);
     sh.abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmO0);
-    if (p.out1) tma_prefetch_desc(&tmO1);
+    if (p.out1 || KIND == GK_DH) tma_prefetch_desc(&tmO1);
   }
   if (p.row_offsets)
     for (int e = threadIdx.x; e <= p.E; e += blockDim.x) sh.roff[e] = p.row_offsets[e];
@@ -770,14 +806,19 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     slab.gen = slabs + (size_t)(warp - EPI_WARP0) * SLAB_BYTES;
     slab.addr = smem_u32(slab.gen);
     int it = 0;
-    AbChunk pre;
+    AbPipe ab;
+    ab.gen = abbuf + (size_t)(warp - EPI_WARP0) * AB_BYTES;
+    ab.addr = smem_u32(ab.gen);
+    ab.bar = smem_u32(&sh.abfull[warp - EPI_WARP0]);
+    ab.phase = 0;
+    ab.pending = false;
     for (int idx = unit; idx < ntiles; idx += nunits, ++it) {
       Tile t = get_tile<KIND, CG>(p, sh, idx);
       t.m0 += BM * rank;
-      if (KIND == GK_DH) {
-        const int row = t.m0 + q * 32 + lane;
-        load_ab_chunk(p, t, row, row < t.row_end, half, 0, pre);
-      }
+      // a|b of the tile's first chunk, unless this warp's rows are all past
+      // the tile's end (then the epilogue skips them)
+      if (KIND == GK_DH && t.m0 + q * 32 < t.row_end)
+        ab_issue(ab, &tmO1, p, t, t.m0 + q * 32, half, 0, lane);
       const int acc = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;
       if (!mbar_wait_bounded(smem_u32(&sh.tfull[acc]), acc_phase, abort_flag, WAIT_NS)) {
@@ -786,7 +827,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       }
       tc_fence_after();
       const uint32_t tacc = tmem + ((uint32_t)(q * 32) << 16) + acc * BN;
-      epilogue_tile<KIND>(p, t, tacc, q, lane, half, slab, &tmO0, &tmO1, pre);
+      epilogue_tile<KIND>(p, t, tacc, q, lane, half, slab, &tmO0, &tmO1, ab, abort_flag);
       tc_fence_before();
       if (CG == 2) {
         __syncwarp();
@@ -795,7 +836,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         mbar_arrive(smem_u32(&sh.tempty[acc]));
       }
     }
-    // every store issued from this warp's slab completes before exit
+    // a copy still on its way into this warp's a|b buffer lands, and every
+    // store issued from its slab completes, before exit
+    if (KIND == GK_DH && ab.pending) {
+      int dummy = 0;
+      mbar_wait_bounded(ab.bar, ab.phase, &dummy, DRAIN_NS);
+    }
     if (lane == 0) bulk_wait0();
     __syncwarp();
   }
@@ -1040,6 +1086,10 @@ cudaError_t launch_gemm(const GemmCall& g, cudaStream_t s) {
       uint32_t b0[2] = {32, 32};
       ok = make_map(&to0, g.out0, 2, d0, s0, b0, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                     CU_TENSOR_MAP_SWIZZLE_64B);
+      // the second map loads the saved a|b (same box and swizzle)
+      uint64_t d1[2] = {(uint64_t)2 * g.H, rows}, s1[1] = {(uint64_t)g.ld_aux * 2};
+      ok = ok && make_map(&to1, g.aux_in, 2, d1, s1, b0, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                          CU_TENSOR_MAP_SWIZZLE_64B);
       break;
     }
     case GK_DOWN:
