@@ -178,6 +178,14 @@ int moe_workspace_bytes(const moe_config* cfg, int training, size_t* bytes);
  * to MOE_OK.  The only entry point that blocks the host. */
 int moe_get_status(void* workspace, void* stream, int* status);
 
+/* Self-test of the device failure path: one GPU thread waits, with the
+ * bounded wait every GEMM role uses, on an mbarrier that nothing arrives on;
+ * after limit_ns (1 ns .. 10 s) it gives up, stores MOE_ERR_TIMEOUT in the
+ * workspace status word (read it with moe_get_status) and the kernel returns
+ * normally -- no trap, no fault, the context stays usable.  Asynchronous on
+ * `stream`.  Errors: NULL, SHAPE (limit out of range), DEVICE. */
+int moe_selftest_wait_timeout(void* workspace, uint64_t limit_ns, void* stream);
+
 /* ---------------------------------------------------------------- forward */
 
 /* a0. logits = x . Wr in fp32 (x widened exactly from bf16).

@@ -58,6 +58,7 @@ SIGNATURES = {
     "moe_workspace_bytes": (ctypes.c_int, [ctypes.POINTER(MoEConfig), ctypes.c_int,
                                            ctypes.POINTER(ctypes.c_size_t)]),
     "moe_get_status": (ctypes.c_int, [c_void_p, c_void_p, ctypes.POINTER(ctypes.c_int)]),
+    "moe_selftest_wait_timeout": (ctypes.c_int, [c_void_p, ctypes.c_uint64, c_void_p]),
     "moe_router_logits": (ctypes.c_int, _STEP),
     "moe_route": (ctypes.c_int, _STEP),
     "moe_router_route": (ctypes.c_int, _STEP),

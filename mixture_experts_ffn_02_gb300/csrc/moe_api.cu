@@ -485,6 +485,16 @@ int moe_get_status(void* workspace, void* stream, int* status) {
   return MOE_OK;
 }
 
+int moe_selftest_wait_timeout(void* workspace, uint64_t limit_ns, void* stream) {
+  if (!workspace) return MOE_ERR_NULL;
+  if (limit_ns == 0 || limit_ns > 10000000000ull) return MOE_ERR_SHAPE;
+  int rc = check_device();
+  if (rc) return rc;
+  MOE_CUDA(launch_wait_timeout_selftest(static_cast<int*>(workspace), limit_ns,
+                                        static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
 #define MOE_ENTRY(name, training, body)                                                      \
   int name(const moe_config* cfg, const moe_tensors* t, void* workspace,                     \
            size_t workspace_bytes, void* stream) {                                           \

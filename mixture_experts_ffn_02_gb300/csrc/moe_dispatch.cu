@@ -1264,6 +1264,26 @@ int grid_for(int items_per_block, long long items, int cap) {
 
 int small_E(int E) { return (E == 4 || E == 8 || E == 16) ? E : 0; }
 
+// --------------------------------------------------------------------------
+// Self-test of the GEMM kernels' failure path on a wait that cannot complete: one thread
+// waits, with the same bounded wait, on an mbarrier that nothing arrives on;
+// after `limit_ns` it gives up and latches MOE_ERR_TIMEOUT in the status word,
+// as the GEMM roles do, and the kernel returns normally.
+__global__ void wait_timeout_selftest_kernel(int* status, unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (!mbar_wait_bounded(smem_u32(&bar), 0, &abort_flag, limit_ns))
+      set_status(status, MOE_ERR_TIMEOUT);
+  }
+}
+
 }  // namespace
 
 int route_group_lanes(int E) {
@@ -1471,6 +1491,12 @@ cudaError_t launch_router_route(const moe_config& c, const void* x, const float*
   else if (c.E == 8) { MOE_RR(8); }
   else { MOE_RR(16); }
 #undef MOE_RR
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_timeout_selftest(int* status, unsigned long long limit_ns,
+                                         cudaStream_t s) {
+  wait_timeout_selftest_kernel<<<1, 32, 0, s>>>(status, limit_ns);
   return cudaGetLastError();
 }
 

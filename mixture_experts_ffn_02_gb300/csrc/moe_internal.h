@@ -170,5 +170,7 @@ struct GemmCall {
   const float* dxr;            // [rows][N] fp32 router term, or NULL
 };
 cudaError_t launch_gemm(const GemmCall& g, cudaStream_t s);
+cudaError_t launch_wait_timeout_selftest(int* status, unsigned long long limit_ns,
+                                         cudaStream_t s);
 
 }  // namespace moe

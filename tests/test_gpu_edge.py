@@ -109,3 +109,31 @@ def test_every_token_on_one_expert():
     r = _check_against_oracle(s, inp, lay)
     assert int(r["counts"][0]) == 900
     assert not lay.grads["dW_gu"][1:].float().abs().max().item()
+
+
+def test_bounded_wait_timeout_latches_status_and_context_survives():
+    """The failure path of the GEMM kernels' bounded waits, made to run out
+    on purpose without any fault: a wait on an mbarrier that nothing arrives
+    on gives up after its limit (50 ms), latches MOE_ERR_TIMEOUT in the status
+    word and the kernel returns; the next layer call on the same context runs
+    normally and matches the oracle."""
+    import ctypes
+    import time
+    from mixture_experts_ffn_02_gb300 import binding
+    s = synth.shape(1)
+    inp, lay = _run(s)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    t0 = time.perf_counter()
+    rc = lay.lib.moe_selftest_wait_timeout(ctypes.c_void_p(lay.ws.data_ptr()), 50_000_000,
+                                           stream)
+    assert rc == 0
+    assert lay.status() == 7            # MOE_ERR_TIMEOUT, read (and cleared) by the host
+    assert time.perf_counter() - t0 >= 0.045
+    assert lay.status() == 0
+    lay.forward()
+    lay.backward(inp["dY"].cuda())
+    torch.cuda.synchronize()
+    assert lay.status() == 0
+    _check_against_oracle(s, inp, lay)
+    assert lay.lib.moe_selftest_wait_timeout(ctypes.c_void_p(lay.ws.data_ptr()), 0,
+                                             stream) == 2           # MOE_ERR_SHAPE
