@@ -135,7 +135,10 @@ typedef struct moe_tensors {
                            combine sums unrounded terms)                          */
   void* s_ab;           /* [T][2Hs] bf16 shared pre-activations (or NULL)         */
   void* s_h;            /* [T][Hs] bf16 shared hidden (0 on PAD rows)             */
-  float* s_out;         /* [T][d] fp32 shared expert output (0 on PAD rows)       */
+  float* s_out;         /* [T][d] fp32 shared expert output (0 on PAD rows):
+                           written by moe_shared_ffn and read by moe_combine;
+                           moe_forward and moe_shared_ffn_combine do not use it
+                           (may be NULL for them)                               */
   /* output */
   void* y;              /* [T][d] bf16 layer output                               */
 } moe_tensors;

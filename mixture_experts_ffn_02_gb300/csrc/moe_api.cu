@@ -71,7 +71,7 @@ int ws_layout(const moe_config* c, int training, WsLayout* w) {
   w->route_zent = take((size_t)w->route_blocks * 2 * sizeof(float));
   w->perm_hist = take((size_t)w->perm_blocks * c->E * sizeof(int));
   w->perm_base = take((size_t)w->perm_blocks * c->E * sizeof(int));
-  w->d_out = w->d_gu = w->dx_perm = w->ds_gu = w->dxs = w->dxr = w->dwr_part = 0;
+  w->d_out = w->d_gu = w->dx_perm = w->ds_gu = w->dxr = w->dwr_part = 0;
   w->wr2 = w->dl3 = w->dl2 = w->goff = 0;
   w->dwr_splits = 1;
   const bool tc_router = router_tc_path(*c);
@@ -418,8 +418,8 @@ int do_backward(const moe_config* c, const moe_tensors* t, const moe_grads* g, C
     sg.out0 = g->dWs_gu; sg.ld0 = c->d; sg.status = k.status;
     MOE_CUDA(launch_gemm(sg, k.s));
   } else {
-    MOE_CUDA(launch_dx_gather(*c, dx_perm, t->inv, nullptr, dxr, g->d_logits, t->Wr, t->valid,
-                              g->dx, k.s));
+    MOE_CUDA(launch_dx_gather(*c, dx_perm, t->inv, dxr, g->d_logits, t->Wr, t->valid, g->dx,
+                              k.s));
   }
   if (!router_tc_path(*c))
     MOE_CUDA(launch_router_dw(*c, t->x, g->d_logits, g->dWr, part, w.dwr_splits, k.s));

@@ -1181,14 +1181,15 @@ combine_bwd_kernel(const bf16* __restrict__ dY, const float* __restrict__ out_pe
 }
 
 // --------------------------------------------------------------------------
-// a7 (vi): dx[t] = sum_j dx_perm[inv[t,j]] + dxs[t] + d_logits[t] Wr^T.
-// The router term comes from dxr (large E) or from Wr staged in shared
-// memory (small E).  PAD rows get 0.
+// a7 (vi), layers without a shared expert: dx[t] = sum_j dx_perm[inv[t,j]]
+// + d_logits[t] Wr^T (with a shared expert the same sum runs in the shared
+// expert's dx GEMM epilogue).  The router term comes from dxr (large E) or
+// from Wr staged in shared memory (small E).  PAD rows get 0.
 // --------------------------------------------------------------------------
 template <int ES>
 __global__ void __launch_bounds__(kThreads)
 dx_gather_kernel(const float* __restrict__ dx_perm, const int32_t* __restrict__ inv,
-                 const float* __restrict__ dxs, const float* __restrict__ dxr,
+                 const float* __restrict__ dxr,
                  const float* __restrict__ dL, const float* __restrict__ Wr,
                  const uint8_t* __restrict__ valid, bf16* __restrict__ dx, int T, int d,
                  int k) {
@@ -1219,12 +1220,6 @@ dx_gather_kernel(const float* __restrict__ dx_perm, const int32_t* __restrict__ 
           if (r < 0) continue;
           float v[8];
           ld8f(dx_perm + (size_t)r * d + c0, v);
-#pragma unroll
-          for (int u = 0; u < 8; ++u) acc[u] += v[u];
-        }
-        if (dxs) {
-          float v[8];
-          ld8f(dxs + (size_t)t * d + c0, v);
 #pragma unroll
           for (int u = 0; u < 8; ++u) acc[u] += v[u];
         }
@@ -1564,27 +1559,26 @@ cudaError_t launch_combine_bwd(const moe_config& c, const void* dY, const float*
 }
 
 cudaError_t launch_dx_gather(const moe_config& c, const float* dx_perm, const int32_t* inv,
-                             const float* dxs, const float* dxr, const float* d_logits,
+                             const float* dxr, const float* d_logits,
                              const float* Wr, const uint8_t* valid, void* dx, cudaStream_t s) {
   DeviceInfo di;
   if (device_info(&di) != MOE_OK) return cudaErrorUnknown;
   const int grid = grid_for(kThreads / 32, c.T, di.num_sms * 4);
   const float* dp = dx_perm;
-  const float* ds = dxs;
   bf16* o = static_cast<bf16*>(dx);
   if (router_small_path(c)) {
     const size_t smem = wr_smem_bytes(c.d, c.E);
 #define MOE_DXG(EE)                                                                           \
   cudaFuncSetAttribute(dx_gather_kernel<EE>, cudaFuncAttributeMaxDynamicSharedMemorySize,     \
                        (int)smem);                                                            \
-  dx_gather_kernel<EE><<<grid, kThreads, smem, s>>>(dp, inv, ds, nullptr, d_logits, Wr, valid, \
-                                                    o, c.T, c.d, c.k)
+  dx_gather_kernel<EE><<<grid, kThreads, smem, s>>>(dp, inv, nullptr, d_logits, Wr, valid, o, \
+                                                    c.T, c.d, c.k)
     if (c.E == 4) { MOE_DXG(4); }
     else if (c.E == 8) { MOE_DXG(8); }
     else { MOE_DXG(16); }
 #undef MOE_DXG
   } else {
-    dx_gather_kernel<0><<<grid, kThreads, 0, s>>>(dp, inv, ds, dxr, d_logits, Wr, valid, o, c.T,
+    dx_gather_kernel<0><<<grid, kThreads, 0, s>>>(dp, inv, dxr, d_logits, Wr, valid, o, c.T,
                                                   c.d, c.k);
   }
   return cudaGetLastError();

@@ -43,7 +43,6 @@ struct WsLayout {
   size_t d_gu;          // [R_cap][2H] bf16
   size_t dx_perm;       // [R_cap][d] fp32
   size_t ds_gu;         // [T][2Hs] bf16
-  size_t dxs;           // [T][d] fp32
   size_t dxr;           // [T][d] fp32 (router input gradient, large E)
   size_t dwr_part;      // [splits][d][E] fp32
   // tensor-core router (router_tc_path)
@@ -94,7 +93,7 @@ cudaError_t launch_combine_bwd(const moe_config& c, const void* dY, const float*
                                const uint8_t* valid, const int32_t* row_offsets,
                                void* d_out, float* d_logits, int* status, cudaStream_t s);
 cudaError_t launch_dx_gather(const moe_config& c, const float* dx_perm, const int32_t* inv,
-                             const float* dxs, const float* dxr, const float* d_logits,
+                             const float* dxr, const float* d_logits,
                              const float* Wr, const uint8_t* valid, void* dx, cudaStream_t s);
 // Router GEMMs on the CUDA cores (fp32 FMA).
 cudaError_t launch_router_dx(const moe_config& c, const float* d_logits, const float* Wr,
