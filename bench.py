@@ -244,6 +244,31 @@ def run_ours(args):
         fms = statistics.median(a.elapsed_time(b) for a, b in fe)
         fwd_rate = s.T / (fms / 1e3)
 
+    # inference forward (nothing saved for a backward), with the rows copied
+    # into x_perm and, as a memory-saving variant, gathered by the gate/up
+    # GEMM from x (no x_perm)
+    def infer_rate(gather):
+        li = binding.Layer.create(s, training=False, gather=gather, device=f"cuda:{local}")
+        li.set_inputs(dev["x"], dev["Wr"], dev["W_gu"], dev["W_down"], dev["Ws_gu"],
+                      dev["Ws_down"], bias=dev["bias"], valid=dev["valid"])
+        for _ in range(3):
+            li.forward()
+        ev_i = []
+        for _ in range(max(3, args.steps // 4)):
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            li.forward()
+            b.record(stream)
+            ev_i.append((a, b))
+        torch.cuda.synchronize()
+        if li.status() != 0:
+            raise RuntimeError(f"device status {li.status()} in the inference forward")
+        return s.T / (statistics.median(a.elapsed_time(b) for a, b in ev_i) / 1e3)
+    fwd_infer_rate = infer_rate(False)
+    fwd_infer_gather_rate = infer_rate(True)
+
     e2e = run_e2e(args, s, inp, lay, training, local)
 
     bf16_burst, bf16_peak, hbm_peak, peak_src = peaks()
@@ -279,6 +304,8 @@ def run_ours(args):
                    "parallelism": f"replicas x{world}",
                    "l2": "256 MB buffer written before each step, outside its events"},
         "fwd_tokens_per_s": None if fwd_rate is None else round(fwd_rate, 1),
+        "fwd_inference_tokens_per_s": round(fwd_infer_rate, 1),
+        "fwd_inference_gathered_tokens_per_s": round(fwd_infer_gather_rate, 1),
         "layer_tflops": round(layer_tflops, 1),
         "layer_frac_of_bf16_peak": round(layer_tflops / bf16_peak, 4),
         "layer_frac_of_burst_peak": round(layer_tflops / bf16_burst, 4),

@@ -221,6 +221,9 @@ int moe_router_route(const moe_config* cfg, const moe_tensors* t,
 
 /* a2. Stable counting-sort dispatch into expert-contiguous padded rows.
  * in: x, topk_idx.  out: counts, offsets, row_offsets, perm, inv, x_perm.
+ * x_perm may be NULL: then no rows are copied, and moe_expert_gate_up (with
+ * x_perm NULL too) gathers the rows from x through perm instead.  The
+ * backward needs x_perm, so a training forward passes it.
  * Device errors: INDEX (the pair is then dropped). */
 int moe_permute(const moe_config* cfg, const moe_tensors* t,
                 void* workspace, size_t workspace_bytes, void* stream);
@@ -230,7 +233,12 @@ int moe_permute(const moe_config* cfg, const moe_tensors* t,
  * a = x_perm[r] W_gate[e]^T, b = x_perm[r] W_up[e]^T, h[r] = silu(a) * b.
  * "KochiLLM v1.0" card (SwiGLU experts); "spark-gpt" README, Hard-won facts
  * (grouped GEMM with the SwiGLU fused into the epilogue).
- * in: x_perm, row_offsets, W_gu.  out: h, ab (if non-NULL). */
+ * With x_perm NULL the permute is folded into the GEMM's A load: row r is
+ * token perm[r] / k of x, fetched by TMA four rows at a time (tile::gather4),
+ * pad rows read as zeros -- the same products as from x_perm, without the
+ * x_perm buffer (2 d T k bytes); a memory-saving mode, several times slower
+ * than copied rows on GB300 (the gathers, not the MMAs, set its pace).
+ * in: x_perm (or x and perm), row_offsets, W_gu.  out: h, ab (if non-NULL). */
 int moe_expert_gate_up(const moe_config* cfg, const moe_tensors* t,
                        void* workspace, size_t workspace_bytes, void* stream);
 

@@ -146,8 +146,14 @@ class Layer:
     lib: ctypes.CDLL
 
     @classmethod
-    def create(cls, shape, training: bool = False, device: str = "cuda", lib=None, **over):
+    def create(cls, shape, training: bool = False, device: str = "cuda", lib=None,
+               gather: bool = False, **over):
+        """Device buffers for one layer.  gather=True (inference only) leaves
+        x_perm out: the permute then copies no rows and the gate/up GEMM
+        gathers them from x."""
         import torch
+        if gather and training:
+            raise ValueError("the backward needs x_perm: gather=True is for inference")
         lib = lib or load()
         cfg = config(shape, **over)
         check(lib.moe_check_config(ctypes.byref(cfg)), "moe_check_config")
@@ -169,7 +175,8 @@ class Layer:
                  counts=z(E, dt=i32), f=z(E, dt=f32), p=z(E, dt=f32), aux=z(4, dt=f32),
                  router_stats=z(8, dt=f32),
                  offsets=z(E + 1, dt=i32), row_offsets=z(E + 1, dt=i32), perm=z(R, dt=i32),
-                 inv=z(T * k, dt=i32), x_perm=z(R, d, dt=bf), h=z(R, H, dt=bf),
+                 inv=z(T * k, dt=i32), x_perm=None if gather else z(R, d, dt=bf),
+                 h=z(R, H, dt=bf),
                  out_perm=z(R, d, dt=f32), y=z(T, d, dt=bf),
                  ab=z(R, 2 * H, dt=bf) if training else None,
                  s_h=z(T, Hs, dt=bf) if Hs else None,

@@ -194,23 +194,35 @@ int do_router_route(const moe_config* c, const moe_tensors* t, Call& k) {
   return MOE_OK;
 }
 
+// x_perm may be NULL: then only offsets, perm and inv are produced, and the
+// gate/up GEMM gathers its rows from x.
 int do_permute(const moe_config* c, const moe_tensors* t, Call& k) {
   MOE_NEED(t->x); MOE_NEED(t->topk_idx); MOE_NEED(t->counts); MOE_NEED(t->offsets);
-  MOE_NEED(t->row_offsets); MOE_NEED(t->perm); MOE_NEED(t->inv); MOE_NEED(t->x_perm);
+  MOE_NEED(t->row_offsets); MOE_NEED(t->perm); MOE_NEED(t->inv); MOE_OPT(t->x_perm);
   MOE_CUDA(launch_permute(*c, t->x, t->topk_idx, t->counts, t->offsets, t->row_offsets,
                           t->perm, t->inv, t->x_perm, k.ws, k.w, k.s));
   return MOE_OK;
 }
 
 int do_gate_up(const moe_config* c, const moe_tensors* t, Call& k) {
-  MOE_NEED(t->x_perm); MOE_NEED(t->row_offsets); MOE_NEED(t->W_gu); MOE_NEED(t->h);
+  MOE_OPT(t->x_perm); MOE_NEED(t->row_offsets); MOE_NEED(t->W_gu); MOE_NEED(t->h);
   MOE_OPT(t->ab);
   GemmCall g{};
   g.kind = GK_GATE_UP;
   g.row_offsets = t->row_offsets;
   g.E = c->E;
   g.rows = (int)k.w.R_cap;
-  g.A = t->x_perm;
+  if (t->x_perm) {
+    g.A = t->x_perm;
+  } else {
+    // the permute folded into the A load: rows gathered from x through perm
+    MOE_NEED(t->x); MOE_NEED(t->perm);
+    g.A = t->x;
+    g.gperm = t->perm;
+    g.gk = c->k;
+    g.gT = c->T;
+    g.grows = (int)k.w.R_cap;
+  }
   g.lda = c->d;
   g.B = t->W_gu;
   g.K = c->d;

@@ -977,10 +977,11 @@ perm_scatter_kernel(const bf16* __restrict__ x, const int32_t* __restrict__ topk
     inv[q] = dest;
     if (dest >= 0) perm[dest] = (int32_t)q;
   }
-  // row copies: one warp per token, each x row read once
+  // row copies: one warp per token, each x row read once (skipped when the
+  // gate/up GEMM gathers its rows from x itself: x_perm == NULL)
   constexpr int U = 4;                           // 16-byte vectors in flight per lane
   const int wpb = blockDim.x >> 5;
-  for (int tl = warp; tl < t_end - t_beg; tl += wpb) {
+  for (int tl = warp; x_perm != nullptr && tl < t_end - t_beg; tl += wpb) {
     const bf16* src = x + (size_t)(t_beg + tl) * d;
     const int* dst = dest_s + tl * k;
     for (int c0 = lane * 8; c0 < d; c0 += 256 * U) {
@@ -1004,8 +1005,9 @@ perm_scatter_kernel(const bf16* __restrict__ x, const int32_t* __restrict__ topk
     const int r1 = row_offsets[e + 1];
     for (int r = r0 + warp; r < r1; r += wpb) {
       if (lane == 0) perm[r] = -1;
-      for (int c0 = lane * 8; c0 < d; c0 += 256)
-        st_v4(x_perm + (size_t)r * d + c0, make_uint4(0, 0, 0, 0));
+      if (x_perm != nullptr)
+        for (int c0 = lane * 8; c0 < d; c0 += 256)
+          st_v4(x_perm + (size_t)r * d + c0, make_uint4(0, 0, 0, 0));
     }
   }
 }

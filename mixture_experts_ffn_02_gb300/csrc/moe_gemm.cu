@@ -105,6 +105,14 @@ struct Params {
   const float* wr;
   int rE;
   const float* dxr;
+  // GK_GATE_UP with the permute folded into the A load: row r of the padded
+  // permuted layout is token gperm[r] / gk of x (tmA maps x with one-row
+  // boxes); pad rows (gperm < 0, or r >= grows) read row gT, past the end,
+  // which the TMA fills with zeros
+  const int32_t* gperm;
+  int gk;
+  int gT;
+  int grows;
 };
 
 struct Shared {
@@ -217,6 +225,27 @@ __device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap* m, uint3
   if (CG == 2) tma_load_3d_pair(dst, m, bar, x, y, z);
   else tma_load_3d(dst, m, bar, x, y, z);
 }
+// Four rows of a one-row-box 2D tensor map (tile::gather4): rows y0..y3,
+// columns x .. x + box - 1, written as consecutive rows at dst.
+template <int CG>
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* m, uint32_t bar,
+                                            int x, int y0, int y1, int y2, int y3) {
+  if (CG == 2)
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile::gather4"
+        ".mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y0), "r"(y1), "r"(y2),
+           "r"(y3), "r"(bar)
+        : "memory");
+  else
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4"
+        ".mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y0), "r"(y1), "r"(y2),
+           "r"(y3), "r"(bar)
+        : "memory");
+}
+
 template <int KIND, int CG>
 __device__ __forceinline__ void issue_loads(const Tile& t, int kb, uint32_t sa, uint32_t sb,
                                             uint32_t bar, const CUtensorMap* tmA,
@@ -698,8 +727,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   const int ntiles = num_tiles<KIND, CG>(p, sh);
   volatile int* abort_flag = &sh.abort_flag;
 
-  if (warp == 0 && lane == 0) {
-    // ---------------- TMA producer (both CTAs)
+  if (warp == 0) {
+    // ---------------- TMA producer (both CTAs): lane 0 waits for free stages
+    // and issues the box loads; with the permute folded in (GK_GATE_UP,
+    // gperm set) every lane also gathers four of the stage's 128 A rows
+    const bool gather = KIND == GK_GATE_UP && p.gperm != nullptr;
     int stage = 0;
     uint32_t phase = 0;
     int pending_parity[MAX_STAGES];
@@ -708,23 +740,49 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     for (int idx = unit; idx < ntiles && ok; idx += nunits) {
       Tile t = get_tile<KIND, CG>(p, sh, idx);
       t.m0 += BM * rank;
+      int tok[4] = {0, 0, 0, 0};
+      if (gather) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = t.m0 + lane * 4 + i;
+          const int pp = r < p.grows ? p.gperm[r] : -1;
+          tok[i] = pp >= 0 ? pp / p.gk : p.gT;
+        }
+      }
       for (int kb = 0; kb < t.ksteps; ++kb) {
-        if (!mbar_wait_bounded(smem_u32(&sh.empty[stage]), phase ^ 1u, abort_flag, WAIT_NS)) {
-          fail(sh, p.status);
+        int good = 1;
+        if (lane == 0)
+          good = mbar_wait_bounded(smem_u32(&sh.empty[stage]), phase ^ 1u, abort_flag, WAIT_NS);
+        good = __shfl_sync(0xffffffffu, good, 0);
+        if (!good) {
+          if (lane == 0) fail(sh, p.status);
           ok = false;
           break;
         }
         const uint32_t fb_local = smem_u32(&sh.full[stage]);
         // the stage's bytes from both CTAs complete on rank 0's barrier
         const uint32_t fb = CG == 2 ? mapa_shared(fb_local, 0) : fb_local;
-        if (rank == 0) mbar_arrive_expect_tx(fb_local, G::STAGE_BYTES * CG);
+        if (lane == 0 && rank == 0) mbar_arrive_expect_tx(fb_local, G::STAGE_BYTES * CG);
         const uint32_t sa = base + stage * G::STAGE_BYTES;
-        issue_loads<KIND, CG>(t, kb, sa, sa + A_BYTES, fb, &tmA, &tmB, p.a_mod, rank);
+        if (gather) {
+          const int k0 = t.kbeg + kb * BK;
+          tma_gather4<CG>(sa + lane * 4 * 128, &tmA, fb, k0, tok[0], tok[1], tok[2], tok[3]);
+          if (lane == 0) {
+            if (CG == 2) {
+              tma_load_4d_pair(sa + A_BYTES, &tmB, fb, k0, t.n0, rank, t.e);
+            } else {
+              tma_load_4d(sa + A_BYTES, &tmB, fb, k0, t.n0, 0, t.e);
+              tma_load_4d(sa + A_BYTES + G::B_BYTES / 2, &tmB, fb, k0, t.n0, 1, t.e);
+            }
+          }
+        } else if (lane == 0) {
+          issue_loads<KIND, CG>(t, kb, sa, sa + A_BYTES, fb, &tmA, &tmB, p.a_mod, rank);
+        }
         pending_parity[stage] = (int)phase;
         if (++stage == G::STAGES) { stage = 0; phase ^= 1u; }
       }
     }
-    if (!ok) {
+    if (!ok && lane == 0) {
       // let every copy already issued land before shared memory is released
       if (CG == 1) {
         for (int s = 0; s < G::STAGES; ++s)
@@ -1008,13 +1066,19 @@ cudaError_t launch_gemm(const GemmCall& g, cudaStream_t s) {
   p.wr = g.wr;
   p.rE = g.rE;
   p.dxr = g.dxr;
+  p.gperm = g.gperm;
+  p.gk = g.gk;
+  p.gT = g.gT;
+  p.grows = g.grows;
   const uint64_t rows = (uint64_t)g.rows;
   bool ok = true;
   switch (g.kind) {
     case GK_GATE_UP: {
-      // A: [rows][K] ; B: W_gu [E][2][H][K] -> dims {K, H, 2, E}
-      uint64_t da[2] = {(uint64_t)g.K, rows}, sa[1] = {(uint64_t)g.lda * 2};
-      uint32_t ba[2] = {64, 128};
+      // A: [rows][K] (or, gathered, x [gT][K] with one-row boxes) ;
+      // B: W_gu [E][2][H][K] -> dims {K, H, 2, E}
+      uint64_t da[2] = {(uint64_t)g.K, g.gperm ? (uint64_t)g.gT : rows},
+               sa[1] = {(uint64_t)g.lda * 2};
+      uint32_t ba[2] = {64, g.gperm ? 1u : 128u};
       uint64_t db[4] = {(uint64_t)g.K, (uint64_t)g.H, 2, (uint64_t)g.E};
       uint64_t sb[3] = {(uint64_t)g.K * 2, (uint64_t)g.H * g.K * 2, (uint64_t)2 * g.H * g.K * 2};
       uint32_t bb[4] = {64, 128, 1, 1};

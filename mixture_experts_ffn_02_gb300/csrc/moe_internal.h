@@ -167,6 +167,12 @@ struct GemmCall {
   const float* wr;             // W_r [N][rE]
   int rE;                      // 0: no inline router term
   const float* dxr;            // [rows][N] fp32 router term, or NULL
+  // GK_GATE_UP with the permute folded into the A load: A is x [gT][K] and row
+  // r of the padded permuted layout is token gperm[r] / gk (pad rows: zeros)
+  const int32_t* gperm;        // perm [grows], -1 on pad rows; NULL = A is given
+  int gk;
+  int gT;
+  int grows;
 };
 cudaError_t launch_gemm(const GemmCall& g, cudaStream_t s);
 cudaError_t launch_wait_timeout_selftest(int* status, unsigned long long limit_ns,

@@ -166,3 +166,28 @@ def test_shared_combine_fold_matches_steps(cfg, T, pad):
     assert torch.equal(y_fused, lay.bufs["y"])
     if pad:
         assert not y_fused[s.T - pad:].float().abs().max().item()
+
+
+@pytest.mark.parametrize("cfg,T", SCALED)
+@pytest.mark.parametrize("pairs", ["1", "0"])
+def test_gathered_gate_up_matches_copied_rows(cfg, T, pairs, monkeypatch):
+    """With x_perm left out, the permute copies no rows and the gate/up GEMM
+    gathers them from x through perm (TMA tile::gather4, pad rows zero).  The
+    A tiles hold the same bf16 values as the copied rows, so h and y equal the
+    x_perm path's bit for bit -- on CTA pairs and on single CTAs."""
+    monkeypatch.setenv("MOE_GEMM_CTA_PAIRS", pairs)
+    s = scaled_shape(cfg, T)
+    inp = synth.make_inputs(s, seed=3)
+    outs = []
+    for gather in (False, True):
+        lay = Layer.create(s, gather=gather)
+        dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+        lay.set_inputs(dev["x"], dev["Wr"], dev["W_gu"], dev["W_down"], dev["Ws_gu"],
+                       dev["Ws_down"], bias=dev["bias"], valid=dev["valid"])
+        lay.forward()
+        torch.cuda.synchronize()
+        assert lay.status() == 0
+        R = int(lay.bufs["row_offsets"][-1])
+        outs.append((lay.bufs["h"][:R].clone(), lay.bufs["y"].clone()))
+    assert torch.equal(outs[0][0], outs[1][0])
+    assert torch.equal(outs[0][1], outs[1][1])
