@@ -266,8 +266,10 @@ def run_ours(args):
         if li.status() != 0:
             raise RuntimeError(f"device status {li.status()} in the inference forward")
         return s.T / (statistics.median(a.elapsed_time(b) for a, b in ev_i) / 1e3)
-    fwd_infer_rate = infer_rate(False)
-    fwd_infer_gather_rate = infer_rate(True)
+    fwd_infer_rate = fwd_infer_gather_rate = None
+    if not args.no_inference:
+        fwd_infer_rate = infer_rate(False)
+        fwd_infer_gather_rate = infer_rate(True)
 
     e2e = run_e2e(args, s, inp, lay, training, local)
 
@@ -304,8 +306,10 @@ def run_ours(args):
                    "parallelism": f"replicas x{world}",
                    "l2": "256 MB buffer written before each step, outside its events"},
         "fwd_tokens_per_s": None if fwd_rate is None else round(fwd_rate, 1),
-        "fwd_inference_tokens_per_s": round(fwd_infer_rate, 1),
-        "fwd_inference_gathered_tokens_per_s": round(fwd_infer_gather_rate, 1),
+        "fwd_inference_tokens_per_s": (None if fwd_infer_rate is None
+                                       else round(fwd_infer_rate, 1)),
+        "fwd_inference_gathered_tokens_per_s": (None if fwd_infer_gather_rate is None
+                                                else round(fwd_infer_gather_rate, 1)),
         "layer_tflops": round(layer_tflops, 1),
         "layer_frac_of_bf16_peak": round(layer_tflops / bf16_peak, 4),
         "layer_frac_of_burst_peak": round(layer_tflops / bf16_burst, 4),
@@ -560,6 +564,8 @@ def main():
     ap.add_argument("--fwd-only", action="store_true")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-inference", action="store_true",
+                    help="skip the inference-forward rates (e.g. for a launch list of the step)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
