@@ -1351,34 +1351,44 @@ cudaError_t launch_router_dx(const moe_config& c, const float* dL, const float* 
   return cudaGetLastError();
 }
 
+// Small-E dW_r: tokens per block.  128 tokens per slice, so the partial
+// count (blocks x slices, summed afterwards) stays near T / 128 whatever d is.
+int router_dw_small_chunk(const moe_config& c) {
+  const int groups = c.d / 8;
+  const int slices = groups >= kThreads ? 1 : kThreads / groups;
+  // the block's dL rows (chunk x E fp32) stay within 48 KB of shared memory
+  const int cap = (48 * 1024 / (4 * c.E)) / kDwTokPerBlk * kDwTokPerBlk;
+  const int chunk = kDwTokPerBlk * slices;
+  return chunk < cap ? chunk : cap;
+}
+
 int router_dw_small_parts(const moe_config& c) {
   const int groups = c.d / 8;
   const int slices = groups >= kThreads ? 1 : kThreads / groups;
-  return (c.T + kDwTokPerBlk - 1) / kDwTokPerBlk * slices;
+  const int chunk = router_dw_small_chunk(c);
+  return (c.T + chunk - 1) / chunk * slices;
 }
 
 cudaError_t launch_router_dw(const moe_config& c, const void* x, const float* dL, float* dWr,
                              float* part, int splits, cudaStream_t s) {
   if (router_small_path(c)) {
-    const int nblk = (c.T + kDwTokPerBlk - 1) / kDwTokPerBlk;
+    const int chunk = router_dw_small_chunk(c);
+    const int nblk = (c.T + chunk - 1) / chunk;
     const int nparts = router_dw_small_parts(c);
-    const size_t smem = (size_t)kDwTokPerBlk * c.E * sizeof(float);
+    const size_t smem = (size_t)chunk * c.E * sizeof(float);
     const bf16* xb = static_cast<const bf16*>(x);
     // exactly groups x slices threads (no idle thread when d/8 < 256)
     const int groups = c.d / 8;
     const int threads = groups >= kThreads ? kThreads : groups * (kThreads / groups);
     switch (c.E) {
       case 4:
-        router_dw_small_kernel<4><<<nblk, threads, smem, s>>>(xb, dL, part, c.T, c.d,
-                                                              kDwTokPerBlk);
+        router_dw_small_kernel<4><<<nblk, threads, smem, s>>>(xb, dL, part, c.T, c.d, chunk);
         break;
       case 8:
-        router_dw_small_kernel<8><<<nblk, threads, smem, s>>>(xb, dL, part, c.T, c.d,
-                                                              kDwTokPerBlk);
+        router_dw_small_kernel<8><<<nblk, threads, smem, s>>>(xb, dL, part, c.T, c.d, chunk);
         break;
       default:
-        router_dw_small_kernel<16><<<nblk, threads, smem, s>>>(xb, dL, part, c.T, c.d,
-                                                               kDwTokPerBlk);
+        router_dw_small_kernel<16><<<nblk, threads, smem, s>>>(xb, dL, part, c.T, c.d, chunk);
         break;
     }
     const int n = c.d * c.E;

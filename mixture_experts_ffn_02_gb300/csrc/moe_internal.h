@@ -15,7 +15,7 @@ constexpr size_t kRouteAccPsum = kRouteAccCnt + 256 * 4;
 constexpr size_t kRouteAccBytes = kRouteAccPsum + 256 * 8;   // E <= 256
 constexpr int kPermChunk = 128;           // tokens per block in the dispatch kernels
 constexpr int kMaxK = 32;                 // experts per token supported
-constexpr int kDwTokPerBlk = 128;         // tokens per block of the small-E dW_r kernel
+constexpr int kDwTokPerBlk = 128;         // tokens per slice of a small-E dW_r block
 
 // Per-device facts, cached after the first query.
 struct DeviceInfo {
