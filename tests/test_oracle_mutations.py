@@ -120,3 +120,51 @@ def test_z_loss_gradient_missing_factor_two_is_caught(monkeypatch):
     orig = O.z_logit_grad
     monkeypatch.setattr(O, "z_logit_grad", lambda L, real, z: orig(L, real, z / 2))
     assert _fails(P.test_backward_matches_central_differences, True, True, False, 4, 0.23)
+
+
+# ---------------------------------------------------------------- MX oracle
+
+import test_oracle_mx as PX
+from oracle import mx_oracle as M
+
+
+def test_mx_exponent_offset_7_is_caught(monkeypatch):
+    orig = M.mx_scale_exp
+    monkeypatch.setattr(M, "mx_scale_exp", lambda amax: np.minimum(orig(amax) + 1, 127))
+    assert _fails(PX.test_mx_scale_closed_forms)
+    assert _fails(PX.test_mx_quantize_is_nearest_on_the_block_grid)
+
+
+def test_mx_ties_to_odd_is_caught(monkeypatch):
+    tab = M.e4m3_table()
+
+    def round_odd(q):
+        q = np.asarray(q, dtype=np.float64)
+        a = np.minimum(np.abs(q), M.E4M3_MAX)
+        i = np.clip(np.searchsorted(tab, a, side="left"), 1, 126)
+        d_lo, d_hi = a - tab[i - 1], tab[i] - a
+        up = (d_hi < d_lo) | ((d_hi == d_lo) & (i % 2 == 1))
+        code = np.where(up, i, i - 1)
+        return (code | (np.signbit(q).astype(np.int64) << 7)).astype(np.uint8)
+    monkeypatch.setattr(M, "e4m3_round", round_odd)
+    assert _fails(PX.test_e4m3_round_matches_torch_float8)
+
+
+def test_mx_blocks_along_wrong_axis_is_caught(monkeypatch):
+    orig = M.mx_quantize
+
+    def cols(v):
+        v = np.asarray(v, dtype=np.float64)
+        if v.ndim < 2 or v.shape[-2] % 32:
+            return orig(v)
+        c, s = orig(np.swapaxes(v, -1, -2))
+        return np.swapaxes(c, -1, -2), s
+    monkeypatch.setattr(M, "mx_quantize", cols)
+    assert _fails(PX.test_mx_blocks_are_rows_of_32)
+
+
+def test_mx_hidden_not_quantised_is_caught(monkeypatch):
+    orig = O.experts_forward
+    monkeypatch.setattr(O, "experts_forward",
+                        lambda *a, rnd=None, **kw: orig(*a, **kw))
+    assert _fails(PX.test_mx_experts_dense_masked_formulation)
