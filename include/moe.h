@@ -314,6 +314,70 @@ int moe_route_finalize(const moe_config* cfg, const moe_tensors* t, const double
 int moe_backward(const moe_config* cfg, const moe_tensors* t, const moe_grads* g,
                  void* workspace, size_t workspace_bytes, void* stream);
 
+/* ------------------------------------------------------------ MXFP8 experts */
+
+/* The routed experts in MXFP8 ("KohakUwULLM" README, Key features: e4m3
+ * values with UE8M0 scales, one per 32 values, on the routed experts, with
+ * fully fused MXFP8 expert kernels).  Forward only (inference).
+ *
+ * Format.  A block is 32 consecutive values along the reduction axis of a
+ * product (d for x and W_gu rows, H for h and W_down rows).  Its scale byte
+ * is X + 127 with X = floor(log2 max|v|) - 8, clamped to >= -127 (all-zero
+ * blocks: -127); each value is the e4m3 code of v / 2^X, rounded to nearest
+ * even and saturated to +-448.  Codes keep the element order of the bf16
+ * tensor they replace.  Scale bytes sit in 512-byte atoms, each covering 128
+ * rows x 4 blocks (128 values along K): row r, block kb at byte
+ * (r % 32) * 16 + (r / 32) * 4 + kb.
+ *
+ * Shapes: d and H multiples of 128, else MOE_ERR_SHAPE.  All buffers are
+ * caller-owned device memory, 16-byte aligned; moe_mx_sizes gives their
+ * sizes.  Router, route, combine and the shared expert are the bf16 path's. */
+typedef struct moe_mx_tensors {
+  uint8_t* W_gu_q;    /* [E][2H][d] codes of W_gu                               */
+  uint8_t* W_gu_s;    /* [E][H/64][d/128] atoms; atom rows 0-63 = gate rows 64j..,
+                         rows 64-127 = up rows H + 64j.. (j = the second index)  */
+  uint8_t* W_down_q;  /* [E][d][H] codes of W_down                              */
+  uint8_t* W_down_s;  /* [E][d/128][H/128] atoms                                */
+  uint8_t* x_q;       /* [R_cap][d] permuted x rows (pad rows zero)              */
+  uint8_t* x_s;       /* [R_cap/128][d/128] atoms                                */
+  uint8_t* h_q;       /* [R_cap][H] hidden rows                                  */
+  uint8_t* h_s;       /* [R_cap/128][H/128] atoms                                */
+} moe_mx_tensors;
+
+#define MOE_MX_FIELDS 8
+
+/* Bytes of each field of moe_mx_tensors, in field order, into bytes[8]. */
+int moe_mx_sizes(const moe_config* cfg, size_t* bytes);
+
+/* Weights -> MXFP8: in: t->W_gu, t->W_down (bf16).  out: W_gu_q, W_gu_s,
+ * W_down_q, W_down_s.  Run once per weight update. */
+int moe_mx_quantize_weights(const moe_config* cfg, const moe_tensors* t,
+                            const moe_mx_tensors* mx, void* stream);
+
+/* a2 with the rows quantised: offsets, perm, inv exactly as moe_permute,
+ * and x_q / x_s instead of x_perm (each token's row quantised once).
+ * in: x, topk_idx.  out: counts, offsets, row_offsets, perm, inv, x_q, x_s. */
+int moe_mx_permute(const moe_config* cfg, const moe_tensors* t, const moe_mx_tensors* mx,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/* a3 on MXFP8 operands: a = x_q W_gate_q^T, b = x_q W_up_q^T (block-scaled
+ * tcgen05 MMAs, fp32 accumulate), h = silu(a) * b quantised straight to h_q
+ * / h_s in the epilogue.  in: x_q, x_s, row_offsets, W_gu_q, W_gu_s.
+ * out: h_q, h_s. */
+int moe_mx_expert_gate_up(const moe_config* cfg, const moe_tensors* t, const moe_mx_tensors* mx,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/* a4 on MXFP8 operands: out_perm = h_q W_down_q^T (fp32).
+ * in: h_q, h_s, row_offsets, W_down_q, W_down_s.  out: out_perm. */
+int moe_mx_expert_down(const moe_config* cfg, const moe_tensors* t, const moe_mx_tensors* mx,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/* The forward with MXFP8 routed experts: moe_router_route, moe_mx_permute,
+ * moe_mx_expert_gate_up, moe_mx_expert_down, moe_shared_ffn_combine.  The
+ * weights must have been quantised (moe_mx_quantize_weights). */
+int moe_mx_forward(const moe_config* cfg, const moe_tensors* t, const moe_mx_tensors* mx,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
 /* ------------------------------------------------- no-allocation routing */
 
 /* Bytes of the fixed device scratch array behind moe_route_static (per GPU). */

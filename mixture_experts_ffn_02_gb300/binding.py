@@ -47,8 +47,18 @@ class MoEGrads(ctypes.Structure):
     _fields_ = [(n, c_void_p) for n in GRAD_FIELDS]
 
 
+MOE_MX_FIELDS = 8
+MX_FIELDS = ["W_gu_q", "W_gu_s", "W_down_q", "W_down_s", "x_q", "x_s", "h_q", "h_s"]
+
+
+class MoEMxTensors(ctypes.Structure):
+    _fields_ = [(n, c_void_p) for n in MX_FIELDS]
+
+
 _STEP = [ctypes.POINTER(MoEConfig), ctypes.POINTER(MoETensors), c_void_p, ctypes.c_size_t,
          c_void_p]
+_MX_STEP = [ctypes.POINTER(MoEConfig), ctypes.POINTER(MoETensors),
+            ctypes.POINTER(MoEMxTensors), c_void_p, ctypes.c_size_t, c_void_p]
 SIGNATURES = {
     "moe_abi_version": (ctypes.c_int, []),
     "moe_strerror": (ctypes.c_char_p, [ctypes.c_int]),
@@ -74,6 +84,14 @@ SIGNATURES = {
                                     c_void_p]),
     "moe_route_static": (ctypes.c_int, [ctypes.POINTER(MoEConfig), ctypes.POINTER(MoETensors),
                                         c_void_p, c_void_p]),
+    "moe_mx_sizes": (ctypes.c_int, [ctypes.POINTER(MoEConfig), ctypes.POINTER(ctypes.c_size_t)]),
+    "moe_mx_quantize_weights": (ctypes.c_int, [ctypes.POINTER(MoEConfig),
+                                               ctypes.POINTER(MoETensors),
+                                               ctypes.POINTER(MoEMxTensors), c_void_p]),
+    "moe_mx_permute": (ctypes.c_int, _MX_STEP),
+    "moe_mx_expert_gate_up": (ctypes.c_int, _MX_STEP),
+    "moe_mx_expert_down": (ctypes.c_int, _MX_STEP),
+    "moe_mx_forward": (ctypes.c_int, _MX_STEP),
     "moe_route_partials": (ctypes.c_int, [ctypes.POINTER(MoEConfig), ctypes.POINTER(MoETensors),
                                           c_void_p, c_void_p]),
     "moe_route_finalize": (ctypes.c_int, [ctypes.POINTER(MoEConfig), ctypes.POINTER(MoETensors),
@@ -144,6 +162,7 @@ class Layer:
     grads: dict
     ws: object
     lib: ctypes.CDLL
+    mx: dict = None
 
     @classmethod
     def create(cls, shape, training: bool = False, device: str = "cuda", lib=None,
@@ -230,6 +249,39 @@ class Layer:
         check(self.lib.moe_backward(ctypes.byref(self.cfg), ctypes.byref(t), ctypes.byref(g),
                                     c_void_p(self.ws.data_ptr()), self.ws.numel(), _stream()),
               "moe_backward")
+
+    # ---- MXFP8 routed experts (inference)
+    def mx_alloc(self):
+        """Device buffers of moe_mx_tensors (sizes from moe_mx_sizes)."""
+        import torch
+        sizes = (ctypes.c_size_t * len(MX_FIELDS))()
+        check(self.lib.moe_mx_sizes(ctypes.byref(self.cfg), sizes), "moe_mx_sizes")
+        dev = self.ws.device
+        self.mx = {n: torch.empty(max(int(sz), 16), dtype=torch.uint8, device=dev)
+                   for n, sz in zip(MX_FIELDS, sizes)}
+        return self.mx
+
+    def mx_tensors(self) -> MoEMxTensors:
+        return MoEMxTensors(**{n: _ptr(self.mx.get(n)) for n in MX_FIELDS})
+
+    def _mx_step(self, name):
+        t = self.tensors()
+        m = self.mx_tensors()
+        fn = getattr(self.lib, name)
+        check(fn(ctypes.byref(self.cfg), ctypes.byref(t), ctypes.byref(m),
+                 c_void_p(self.ws.data_ptr()), self.ws.numel(), _stream()), name)
+
+    def mx_quantize_weights(self):
+        t = self.tensors()
+        m = self.mx_tensors()
+        check(self.lib.moe_mx_quantize_weights(ctypes.byref(self.cfg), ctypes.byref(t),
+                                               ctypes.byref(m), _stream()),
+              "moe_mx_quantize_weights")
+
+    def mx_permute(self): self._mx_step("moe_mx_permute")
+    def mx_gate_up(self): self._mx_step("moe_mx_expert_gate_up")
+    def mx_down(self): self._mx_step("moe_mx_expert_down")
+    def mx_forward(self): self._mx_step("moe_mx_forward")
 
     def route_partials(self, sums):
         """This rank's routing sums into ``sums`` ([2E+1] float64, device)."""

@@ -19,7 +19,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libmoe_gb300.so")
-SOURCES = ["moe_api.cu", "moe_dispatch.cu", "moe_gemm.cu", "moe_router_tc.cu", "moe_static.cu"]
+SOURCES = ["moe_api.cu", "moe_dispatch.cu", "moe_gemm.cu", "moe_mx.cu", "moe_router_tc.cu",
+           "moe_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

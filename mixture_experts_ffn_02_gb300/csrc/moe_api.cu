@@ -438,6 +438,59 @@ int do_backward(const moe_config* c, const moe_tensors* t, const moe_grads* g, C
   return MOE_OK;
 }
 
+// ---- MXFP8 routed experts
+int check_mx(const moe_config* c) {
+  if (c->d % 128 || c->H % 128) return MOE_ERR_SHAPE;
+  return MOE_OK;
+}
+
+void mx_sizes(const moe_config& c, size_t* b) {
+  const size_t E = c.E, d = c.d, H = c.H, R = (size_t)row_capacity(c);
+  b[0] = E * 2 * H * d;                                  // W_gu_q
+  b[1] = E * (H / 64) * (d / 128) * 512;                 // W_gu_s
+  b[2] = E * d * H;                                      // W_down_q
+  b[3] = E * (d / 128) * (H / 128) * 512;                // W_down_s
+  b[4] = R * d;                                          // x_q
+  b[5] = (R / 128) * (d / 128) * 512;                    // x_s
+  b[6] = R * H;                                          // h_q
+  b[7] = (R / 128) * (H / 128) * 512;                    // h_s
+}
+
+int do_mx_permute(const moe_config* c, const moe_tensors* t, const moe_mx_tensors* m, Call& k) {
+  MOE_NEED(t->x); MOE_NEED(t->topk_idx); MOE_NEED(t->counts); MOE_NEED(t->offsets);
+  MOE_NEED(t->row_offsets); MOE_NEED(t->perm); MOE_NEED(t->inv);
+  MOE_NEED(m->x_q); MOE_NEED(m->x_s);
+  MOE_CUDA(launch_permute_mx(*c, t->x, t->topk_idx, t->counts, t->offsets, t->row_offsets,
+                             t->perm, t->inv, m->x_q, m->x_s, k.ws, k.w, k.s));
+  return MOE_OK;
+}
+
+int do_mx_gemm(const moe_config* c, const moe_tensors* t, const moe_mx_tensors* m, Call& k,
+               bool gate_up) {
+  MOE_NEED(t->row_offsets);
+  MxGemmCall g{};
+  g.gate_up = gate_up ? 1 : 0;
+  g.row_offsets = t->row_offsets;
+  g.E = c->E;
+  g.rows = (int)k.w.R_cap;
+  g.d = c->d;
+  g.H = c->H;
+  g.status = k.status;
+  if (gate_up) {
+    MOE_NEED(m->x_q); MOE_NEED(m->x_s); MOE_NEED(m->W_gu_q); MOE_NEED(m->W_gu_s);
+    MOE_NEED(m->h_q); MOE_NEED(m->h_s);
+    g.A = m->x_q; g.sfa = m->x_s; g.B = m->W_gu_q; g.sfb = m->W_gu_s;
+    g.hq = m->h_q; g.hs = m->h_s;
+  } else {
+    MOE_NEED(m->h_q); MOE_NEED(m->h_s); MOE_NEED(m->W_down_q); MOE_NEED(m->W_down_s);
+    MOE_NEED(t->out_perm);
+    g.A = m->h_q; g.sfa = m->h_s; g.B = m->W_down_q; g.sfb = m->W_down_s;
+    g.out = t->out_perm;
+  }
+  MOE_CUDA(launch_mx_gemm(g, k.s));
+  return MOE_OK;
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -531,6 +584,53 @@ MOE_ENTRY(moe_forward, 0, {
   if ((rc = do_permute(cfg, t, k))) return rc;
   if ((rc = do_gate_up(cfg, t, k))) return rc;
   if ((rc = do_down(cfg, t, k))) return rc;
+  return do_shared_combine(cfg, t, k);
+})
+
+int moe_mx_sizes(const moe_config* cfg, size_t* bytes) {
+  int rc = check_cfg(cfg);
+  if (rc) return rc;
+  if ((rc = check_mx(cfg))) return rc;
+  if (!bytes) return MOE_ERR_NULL;
+  mx_sizes(*cfg, bytes);
+  return MOE_OK;
+}
+
+int moe_mx_quantize_weights(const moe_config* cfg, const moe_tensors* t,
+                            const moe_mx_tensors* mx, void* stream) {
+  int rc = check_cfg(cfg);
+  if (rc) return rc;
+  if ((rc = check_mx(cfg))) return rc;
+  if ((rc = check_device())) return rc;
+  if (!t || !mx) return MOE_ERR_NULL;
+  MOE_NEED(t->W_gu); MOE_NEED(t->W_down);
+  MOE_NEED(mx->W_gu_q); MOE_NEED(mx->W_gu_s); MOE_NEED(mx->W_down_q); MOE_NEED(mx->W_down_s);
+  MOE_CUDA(launch_mx_quant_weights(*cfg, t->W_gu, t->W_down, mx->W_gu_q, mx->W_gu_s,
+                                   mx->W_down_q, mx->W_down_s,
+                                   static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+#define MOE_MX_ENTRY(name, body)                                                             \
+  int name(const moe_config* cfg, const moe_tensors* t, const moe_mx_tensors* mx,            \
+           void* workspace, size_t workspace_bytes, void* stream) {                          \
+    Call k;                                                                                  \
+    int rc = check_cfg(cfg);                                                                 \
+    if (rc) return rc;                                                                       \
+    if ((rc = check_mx(cfg))) return rc;                                                     \
+    if ((rc = begin(cfg, 0, workspace, workspace_bytes, stream, &k))) return rc;             \
+    if (!t || !mx) return MOE_ERR_NULL;                                                      \
+    body                                                                                     \
+  }
+
+MOE_MX_ENTRY(moe_mx_permute, { return do_mx_permute(cfg, t, mx, k); })
+MOE_MX_ENTRY(moe_mx_expert_gate_up, { return do_mx_gemm(cfg, t, mx, k, true); })
+MOE_MX_ENTRY(moe_mx_expert_down, { return do_mx_gemm(cfg, t, mx, k, false); })
+MOE_MX_ENTRY(moe_mx_forward, {
+  if ((rc = do_router_route(cfg, t, k))) return rc;
+  if ((rc = do_mx_permute(cfg, t, mx, k))) return rc;
+  if ((rc = do_mx_gemm(cfg, t, mx, k, true))) return rc;
+  if ((rc = do_mx_gemm(cfg, t, mx, k, false))) return rc;
   return do_shared_combine(cfg, t, k);
 })
 

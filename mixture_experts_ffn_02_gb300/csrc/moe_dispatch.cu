@@ -11,6 +11,7 @@
 #include <math.h>
 
 #include "moe_common.cuh"
+#include "moe_mx.cuh"
 #include "moe_internal.h"
 
 namespace moe {
@@ -933,14 +934,18 @@ perm_scan_kernel(const int* __restrict__ hist, int nblk, int E, int32_t* __restr
 // shared memory by one coalesced load), then copies each token's x row once
 // into its k destination rows, several 16-byte vectors in flight per lane.
 // The block also zeroes the pad rows of the experts e = blockIdx.x (mod
-// gridDim.x).
+// gridDim.x).  MX: instead of bf16 rows it writes each token's row quantised
+// to MXFP8 (e4m3 codes [R][d] and the UE8M0 scale atoms of x_s, blocks of 32
+// along d), quantising the row once for its k destinations.
 constexpr int kScatterThreads = 512;
+template <bool MX>
 __global__ void __launch_bounds__(kScatterThreads, 2)
 perm_scatter_kernel(const bf16* __restrict__ x, const int32_t* __restrict__ topk, int T,
                     int d, int k, int E, const int* __restrict__ base,
                     const int32_t* __restrict__ counts, const int32_t* __restrict__ row_offsets,
                     int32_t* __restrict__ perm, int32_t* __restrict__ inv,
-                    bf16* __restrict__ x_perm) {
+                    bf16* __restrict__ x_perm, uint8_t* __restrict__ x_q,
+                    uint8_t* __restrict__ x_s) {
   __shared__ int base_s[256];
   __shared__ int dest_s[kPermChunk * kMaxK];     // expert ids, then destination rows
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -981,7 +986,28 @@ perm_scatter_kernel(const bf16* __restrict__ x, const int32_t* __restrict__ topk
   // gate/up GEMM gathers its rows from x itself: x_perm == NULL)
   constexpr int U = 4;                           // 16-byte vectors in flight per lane
   const int wpb = blockDim.x >> 5;
-  for (int tl = warp; x_perm != nullptr && tl < t_end - t_beg; tl += wpb) {
+  const int nb32 = d / 32, kg = d / 128;          // MX: blocks per row, atoms per row block
+  for (int tl = warp; MX && tl < t_end - t_beg; tl += wpb) {
+    const bf16* src = x + (size_t)(t_beg + tl) * d;
+    const int* dst = dest_s + tl * k;
+    for (int b = lane; b < nb32; b += 32) {
+      float v[32];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) unpack8(ld_nc_v4(src + b * 32 + u * 8), v + 8 * u);
+      uint32_t q[8];
+      const uint32_t sb = mx_quant32(v, q);
+      for (int j = 0; j < k; ++j) {
+        const int r = dst[j];
+        if (r < 0) continue;
+        uint8_t* o = x_q + (size_t)r * d + b * 32;
+        st_v4(o, make_uint4(q[0], q[1], q[2], q[3]));
+        st_v4(o + 16, make_uint4(q[4], q[5], q[6], q[7]));
+        x_s[((size_t)(r >> 7) * kg + (b >> 2)) * kMxAtom + mx_sf_byte(r & 127, b & 3)] =
+            (uint8_t)sb;
+      }
+    }
+  }
+  for (int tl = warp; !MX && x_perm != nullptr && tl < t_end - t_beg; tl += wpb) {
     const bf16* src = x + (size_t)(t_beg + tl) * d;
     const int* dst = dest_s + tl * k;
     for (int c0 = lane * 8; c0 < d; c0 += 256 * U) {
@@ -1005,9 +1031,15 @@ perm_scatter_kernel(const bf16* __restrict__ x, const int32_t* __restrict__ topk
     const int r1 = row_offsets[e + 1];
     for (int r = r0 + warp; r < r1; r += wpb) {
       if (lane == 0) perm[r] = -1;
-      if (x_perm != nullptr)
+      if (!MX && x_perm != nullptr)
         for (int c0 = lane * 8; c0 < d; c0 += 256)
           st_v4(x_perm + (size_t)r * d + c0, make_uint4(0, 0, 0, 0));
+      if (MX) {
+        for (int c0 = lane * 16; c0 < d; c0 += 512)
+          st_v4(x_q + (size_t)r * d + c0, make_uint4(0, 0, 0, 0));
+        for (int b = lane; b < nb32; b += 32)
+          x_s[((size_t)(r >> 7) * kg + (b >> 2)) * kMxAtom + mx_sf_byte(r & 127, b & 3)] = 0;
+      }
     }
   }
 }
@@ -1530,9 +1562,26 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* to
   perm_hist_kernel<<<nblk, kThreads, 0, s>>>(topk, c.T, c.k, c.E, hist, status);
   perm_scan_kernel<<<1, kScanThreads, 0, s>>>(hist, nblk, c.E, counts, offsets, row_offsets,
                                               base);
-  perm_scatter_kernel<<<nblk, kScatterThreads, 0, s>>>(static_cast<const bf16*>(x), topk, c.T, c.d,
-                                                c.k, c.E, base, counts, row_offsets, perm, inv,
-                                                static_cast<bf16*>(x_perm));
+  perm_scatter_kernel<false><<<nblk, kScatterThreads, 0, s>>>(
+      static_cast<const bf16*>(x), topk, c.T, c.d, c.k, c.E, base, counts, row_offsets, perm,
+      inv, static_cast<bf16*>(x_perm), nullptr, nullptr);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_permute_mx(const moe_config& c, const void* x, const int32_t* topk,
+                              int32_t* counts, int32_t* offsets, int32_t* row_offsets,
+                              int32_t* perm, int32_t* inv, uint8_t* x_q, uint8_t* x_s,
+                              char* ws, const WsLayout& w, cudaStream_t s) {
+  int* hist = reinterpret_cast<int*>(ws + w.perm_hist);
+  int* base = reinterpret_cast<int*>(ws + w.perm_base);
+  int* status = reinterpret_cast<int*>(ws + w.status);
+  const int nblk = w.perm_blocks;
+  perm_hist_kernel<<<nblk, kThreads, 0, s>>>(topk, c.T, c.k, c.E, hist, status);
+  perm_scan_kernel<<<1, kScanThreads, 0, s>>>(hist, nblk, c.E, counts, offsets, row_offsets,
+                                              base);
+  perm_scatter_kernel<true><<<nblk, kScatterThreads, 0, s>>>(
+      static_cast<const bf16*>(x), topk, c.T, c.d, c.k, c.E, base, counts, row_offsets, perm,
+      inv, nullptr, x_q, x_s);
   return cudaGetLastError();
 }
 

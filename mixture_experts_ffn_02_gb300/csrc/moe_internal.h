@@ -175,6 +175,33 @@ struct GemmCall {
   int grows;
 };
 cudaError_t launch_gemm(const GemmCall& g, cudaStream_t s);
+
+// ---- MXFP8 routed experts (moe_mx.cu) --------------------------------------
+// Quantising permute: offsets, perm, inv as launch_permute, and x rows as
+// e4m3 codes x_q [R_cap][d] with scale atoms x_s [R_cap/128][d/128][512].
+cudaError_t launch_permute_mx(const moe_config& c, const void* x, const int32_t* topk,
+                              int32_t* counts, int32_t* offsets, int32_t* row_offsets,
+                              int32_t* perm, int32_t* inv, uint8_t* x_q, uint8_t* x_s,
+                              char* ws, const WsLayout& w, cudaStream_t s);
+cudaError_t launch_mx_quant_weights(const moe_config& c, const void* W_gu, const void* W_down,
+                                    uint8_t* W_gu_q, uint8_t* W_gu_s, uint8_t* W_down_q,
+                                    uint8_t* W_down_s, cudaStream_t s);
+struct MxGemmCall {
+  int gate_up;                 // 1: h = silu(a) * b quantised; 0: out = h W_down^T (fp32)
+  const int32_t* row_offsets;  // [E+1] padded, device
+  int E;
+  int rows;                    // R_cap
+  int d, H;                    // multiples of 128
+  const uint8_t* A;            // x codes [rows][d] or h codes [rows][H]
+  const uint8_t* sfa;          // their scale atoms
+  const uint8_t* B;            // W_gu codes [E][2H][d] or W_down codes [E][d][H]
+  const uint8_t* sfb;          // their scale atoms
+  uint8_t* hq;                 // gate/up out: h codes [rows][H]
+  uint8_t* hs;                 // gate/up out: h scale atoms
+  float* out;                  // down out: [rows][d] fp32
+  int* status;
+};
+cudaError_t launch_mx_gemm(const MxGemmCall& g, cudaStream_t s);
 cudaError_t launch_wait_timeout_selftest(int* status, unsigned long long limit_ns,
                                          cudaStream_t s);
 

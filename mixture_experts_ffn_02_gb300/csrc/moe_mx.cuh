@@ -1,0 +1,105 @@
+// Device helpers of the MXFP8 path (sm_103a): the e4m3 / UE8M0 block
+// quantiser, the layout of scale factors in memory, and inline-PTX wrappers
+// for the block-scaled tcgen05 MMA, tcgen05.cp and the untiled bulk copy.
+//
+// "KohakUwULLM" README, Key features: MXFP8 = e4m3 values with UE8M0 scales,
+// one scale per 32 consecutive values, on the routed experts.
+#pragma once
+
+#include <cuda_fp8.h>
+
+#include "moe_common.cuh"
+
+namespace moe {
+
+// ----------------------------------------------------------------- quantiser
+// One block of 32 values: shared exponent X = floor(log2 max|v|) - 8 (8 is the
+// exponent of 448, the largest e4m3 normal), clamped below at -127 (zero and
+// fp32-subnormal maxima); the scale byte is X + 127.  Each v * 2^-X (exact: a
+// power-of-two scaling of a finite fp32 whose result stays below 512) is
+// converted to e4m3 by the hardware conversion, round to nearest even,
+// saturating at +-448.  codes[w] holds elements 4w .. 4w+3, lowest first.
+__device__ __forceinline__ uint32_t mx_quant32(const float* v, uint32_t* codes) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  int X = (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 127 - 8;
+  X = X < -127 ? -127 : X;
+  const float inv = __uint_as_float((uint32_t)(127 - X) << 23);     // 2^-X
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(v[4 * w] * inv, v[4 * w + 1] * inv),
+                                                 __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi =
+        __nv_cvt_float2_to_fp8x2(make_float2(v[4 * w + 2] * inv, v[4 * w + 3] * inv),
+                                 __NV_SATFINITE, __NV_E4M3);
+    codes[w] = (lo & 0xFFFFu) | (hi << 16);
+  }
+  return (uint32_t)(X + 127);
+}
+
+// ----------------------------------------------------------------- scale layout
+// Scale factors sit in 512-byte atoms, one per (128-row block, 128-column
+// group): 128 rows x 4 blocks of 32 along K.  Row r, block kb of the atom is
+// byte (r % 32) * 16 + (r / 32) * 4 + kb.  tcgen05.cp .32x128b.warpx4 copies
+// an atom into 4 TMEM columns, atom row r % 32 to lane r % 32 of all four lane
+// quadrants, and the block-scaled MMA reads row (or column) m's scale of the
+// K-block given by the instruction's scale-factor id from column base + m / 32,
+// byte id, in the lane of m's quadrant.
+__host__ __device__ __forceinline__ int mx_sf_byte(int r, int kb) {
+  return (r & 31) * 16 + ((r >> 5) & 3) * 4 + kb;
+}
+constexpr int kMxAtom = 512;
+
+// ----------------------------------------------------------------- tcgen05
+// Instruction descriptor of kind::mxf8f6f4 with e4m3 A and B (format 0), fp32
+// accumulate, UE8M0 scales (bit 23), both operands K-major; the A and B
+// scale-factor ids (the byte of the scale column) at bits 29-30 and 4-5.
+__host__ __device__ constexpr uint32_t umma_idesc_mx(int M, int N) {
+  return ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24);
+}
+__host__ __device__ constexpr uint32_t umma_idesc_sfid(uint32_t idesc, uint32_t id) {
+  return idesc | (id << 29) | (id << 4);
+}
+
+__device__ __forceinline__ void umma_mx(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                        uint32_t idesc, uint32_t tsfa, uint32_t tsfb,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
+      " [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+      :: "r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(tsfa), "r"(tsfb),
+         "r"(accumulate)
+      : "memory");
+}
+
+// Shared-memory descriptor without swizzle (byte offsets >> 4).
+__device__ __forceinline__ uint64_t umma_desc_plain(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  return d;
+}
+
+// One 512-byte scale atom (32 rows of 16 bytes, contiguous) from shared
+// memory into 4 TMEM columns of all 128 lanes, ordered before the MMAs the
+// same thread issues after it.
+__device__ __forceinline__ void tmem_cp_atom(uint32_t taddr, uint32_t saddr) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;"
+               :: "r"(taddr), "l"(umma_desc_plain(saddr, 128, 128)) : "memory");
+}
+
+// Untiled bulk copy global -> shared (16-byte aligned, size a multiple of 16),
+// completing on an mbarrier.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar) : "memory");
+}
+
+}  // namespace moe

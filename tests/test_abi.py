@@ -100,7 +100,29 @@ def test_struct_layouts_match_the_header():
     src = open(os.path.join(ROOT, "include", "moe.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     for struct, cls in (("moe_config", binding.MoEConfig), ("moe_tensors", binding.MoETensors),
-                        ("moe_grads", binding.MoEGrads)):
+                        ("moe_grads", binding.MoEGrads),
+                        ("moe_mx_tensors", binding.MoEMxTensors)):
         body = re.search(r"typedef struct " + struct + r" \{(.*?)\} " + struct, src, re.S).group(1)
         names = re.findall(r"\b(\w+)\s*;", body)
         assert names == [f[0] for f in cls._fields_], struct
+
+
+def test_mx_sizes_and_shape_rule(clib):
+    """MXFP8 buffers: codes keep the bf16 tensors' element counts, one scale
+    byte per 32 values in 512-byte atoms; d or H not a multiple of 128 is a
+    shape error (the tiny 64-wide layer has no MX path)."""
+    s = synth.shape(2)
+    c = binding.config(s)
+    sizes = (ctypes.c_size_t * binding.MOE_MX_FIELDS)()
+    assert clib.moe_mx_sizes(ctypes.byref(c), sizes) == 0
+    R = ctypes.c_int64()
+    assert clib.moe_row_capacity(ctypes.byref(c), ctypes.byref(R)) == 0
+    E, d, H, R = s.E, s.d, s.H, R.value
+    assert list(sizes) == [E * 2 * H * d, E * 2 * H * d // 32, E * d * H, E * d * H // 32,
+                           R * d, R * d // 32, R * H, R * H // 32]
+    tiny = binding.config(synth.shape(1))
+    assert clib.moe_mx_sizes(ctypes.byref(tiny), sizes) == 2
+    t = binding.MoETensors()
+    m = binding.MoEMxTensors()
+    assert clib.moe_mx_forward(ctypes.byref(tiny), ctypes.byref(t), ctypes.byref(m), None, 0,
+                               None) == 2
