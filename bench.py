@@ -271,6 +271,52 @@ def run_ours(args):
         fwd_infer_rate = infer_rate(False)
         fwd_infer_gather_rate = infer_rate(True)
 
+    # inference forward with MXFP8 routed experts (weights quantised once,
+    # outside the timed region, as they are between weight updates)
+    def mx_run():
+        if s.d % 128 or s.H % 128:
+            return None
+        lm = binding.Layer.create(s, training=False, device=f"cuda:{local}")
+        lm.set_inputs(dev["x"], dev["Wr"], dev["W_gu"], dev["W_down"], dev["Ws_gu"],
+                      dev["Ws_down"], bias=dev["bias"], valid=dev["valid"])
+        lm.mx_alloc()
+        qa = torch.cuda.Event(enable_timing=True)
+        qb = torch.cuda.Event(enable_timing=True)
+        qa.record(stream)
+        lm.mx_quantize_weights()
+        qb.record(stream)
+        for _ in range(3):
+            lm.mx_forward()
+        n = max(3, args.steps // 4)
+        ev_f, ev_g, ev_d = [], [], []
+        for _ in range(n):
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            lm.mx_forward()
+            b.record(stream)
+            ev_f.append((a, b))
+        for _ in range(n):         # the same steps one call at a time, GEMMs timed
+            flush.zero_()
+            lm.router_route()
+            lm.mx_permute()
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            e[0].record(stream)
+            lm.mx_gate_up()
+            e[1].record(stream)
+            lm.mx_down()
+            e[2].record(stream)
+            lm.shared_combine()
+            ev_g.append((e[0], e[1]))
+            ev_d.append((e[1], e[2]))
+        torch.cuda.synchronize()
+        if lm.status() != 0:
+            raise RuntimeError(f"device status {lm.status()} in the MX forward")
+        med = lambda v: statistics.median(a.elapsed_time(b) for a, b in v)
+        return med(ev_f), med(ev_g), med(ev_d), qa.elapsed_time(qb)
+    mx = None if args.no_inference else mx_run()
+
     e2e = run_e2e(args, s, inp, lay, training, local)
 
     bf16_burst, bf16_peak, hbm_peak, peak_src = peaks()
@@ -280,6 +326,24 @@ def run_ours(args):
     layer_flops = (routed + shared) * (3 if training else 1)
     layer_tflops = layer_flops / (ms_per_step / 1e3) / 1e12
     traffic = load_traffic(args.config)
+
+    mx_out = None
+    if mx is not None:
+        f8_peak = 2 * bf16_peak          # nominal dense fp8 / bf16 tensor ratio (4.5 / 2.25)
+        mx_f_ms, mx_g_ms, mx_d_ms, mx_q_ms = mx
+        g_tf = gu_flops / (mx_g_ms / 1e3) / 1e12
+        d_tf = routed / 3 / (mx_d_ms / 1e3) / 1e12
+        mx_out = {
+            "fwd_tokens_per_s": round(s.T / (mx_f_ms / 1e3), 1),
+            "dtype": "e4m3 x e4m3 (UE8M0 per-32 scales), fp32 accumulate",
+            "peak_tflops": round(f8_peak, 1),
+            "peak_source": f"{peak_src} sustained bf16 x 2 (nominal fp8/bf16 ratio)",
+            "gate_up": {"avg_launch_ms": round(mx_g_ms, 4), "achieved_tflops": round(g_tf, 1),
+                        "frac": round(g_tf / f8_peak, 4)},
+            "down": {"avg_launch_ms": round(mx_d_ms, 4), "achieved_tflops": round(d_tf, 1),
+                     "frac": round(d_tf / f8_peak, 4)},
+            "weight_quantise_ms": round(mx_q_ms, 4),
+        }
 
     if world > 1:
         dist.barrier()
@@ -310,6 +374,7 @@ def run_ours(args):
                                        else round(fwd_infer_rate, 1)),
         "fwd_inference_gathered_tokens_per_s": (None if fwd_infer_gather_rate is None
                                                 else round(fwd_infer_gather_rate, 1)),
+        "fwd_inference_mxfp8": mx_out,
         "layer_tflops": round(layer_tflops, 1),
         "layer_frac_of_bf16_peak": round(layer_tflops / bf16_peak, 4),
         "layer_frac_of_burst_peak": round(layer_tflops / bf16_burst, 4),

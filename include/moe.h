@@ -329,13 +329,12 @@ int moe_backward(const moe_config* cfg, const moe_tensors* t, const moe_grads* g
  * rows x 4 blocks (128 values along K): row r, block kb at byte
  * (r % 32) * 16 + (r / 32) * 4 + kb.
  *
- * Shapes: d and H multiples of 128, else MOE_ERR_SHAPE.  All buffers are
+ * Shapes: d a multiple of 256 and H of 128, else MOE_ERR_SHAPE.  All buffers are
  * caller-owned device memory, 16-byte aligned; moe_mx_sizes gives their
  * sizes.  Router, route, combine and the shared expert are the bf16 path's. */
 typedef struct moe_mx_tensors {
   uint8_t* W_gu_q;    /* [E][2H][d] codes of W_gu                               */
-  uint8_t* W_gu_s;    /* [E][H/64][d/128] atoms; atom rows 0-63 = gate rows 64j..,
-                         rows 64-127 = up rows H + 64j.. (j = the second index)  */
+  uint8_t* W_gu_s;    /* [E][2H/128][d/128] atoms (128-row blocks of W_gu[e])     */
   uint8_t* W_down_q;  /* [E][d][H] codes of W_down                              */
   uint8_t* W_down_s;  /* [E][d/128][H/128] atoms                                */
   uint8_t* x_q;       /* [R_cap][d] permuted x rows (pad rows zero)              */

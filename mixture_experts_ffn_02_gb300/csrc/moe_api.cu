@@ -440,14 +440,14 @@ int do_backward(const moe_config* c, const moe_tensors* t, const moe_grads* g, C
 
 // ---- MXFP8 routed experts
 int check_mx(const moe_config* c) {
-  if (c->d % 128 || c->H % 128) return MOE_ERR_SHAPE;
+  if (c->d % 256 || c->H % 128) return MOE_ERR_SHAPE;
   return MOE_OK;
 }
 
 void mx_sizes(const moe_config& c, size_t* b) {
   const size_t E = c.E, d = c.d, H = c.H, R = (size_t)row_capacity(c);
   b[0] = E * 2 * H * d;                                  // W_gu_q
-  b[1] = E * (H / 64) * (d / 128) * 512;                 // W_gu_s
+  b[1] = E * (2 * H / 128) * (d / 128) * 512;            // W_gu_s
   b[2] = E * d * H;                                      // W_down_q
   b[3] = E * (d / 128) * (H / 128) * 512;                // W_down_s
   b[4] = R * d;                                          // x_q

@@ -191,7 +191,7 @@ struct MxGemmCall {
   const int32_t* row_offsets;  // [E+1] padded, device
   int E;
   int rows;                    // R_cap
-  int d, H;                    // multiples of 128
+  int d, H;                    // d a multiple of 256, H of 128
   const uint8_t* A;            // x codes [rows][d] or h codes [rows][H]
   const uint8_t* sfa;          // their scale atoms
   const uint8_t* B;            // W_gu codes [E][2H][d] or W_down codes [E][d][H]

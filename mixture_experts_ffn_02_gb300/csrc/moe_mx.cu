@@ -8,15 +8,24 @@
 // Here that is:
 //   * a weight quantiser (bf16 W_gu, W_down -> e4m3 codes + scale atoms);
 //   * the quantising permute (moe_dispatch.cu, perm_scatter_kernel<true>);
-//   * a persistent grouped GEMM on tcgen05.mma kind::mxf8f6f4 with block
-//     scales: TMA brings 128 x 128-byte tiles of codes (128-byte swizzle) and
-//     a bulk copy brings each stage's two 512-byte scale atoms; the MMA thread
-//     moves the atoms into TMEM with tcgen05.cp and issues four K = 32 MMAs
-//     per stage, each picking its K-block's scale byte by the scale-factor id;
+//   * a persistent grouped GEMM on CTA pairs with tcgen05.mma.cta_group::2
+//     .kind::mxf8f6f4 and block scales.  A pair computes a 256 x 256 tile:
+//     each CTA loads (TMA, 128-byte swizzle) its 128 rows of A and half of
+//     the 256 B rows, plus three 512-byte scale atoms -- its own rows' A
+//     scales and the scales of all 256 B rows, which both CTAs need -- all
+//     completing on the even CTA's barrier.  The even CTA's MMA thread moves
+//     both CTAs' atoms into their TMEM with tcgen05.cp.cta_group::2 and issues
+//     four K = 32 MMAs per stage, each picking its K-block's scale byte by the
+//     scale-factor id;
 //   * epilogues: gate/up -> h = silu(a) * b quantised straight to MXFP8 (codes
 //     and scale atoms of h, no bf16 h); down -> out_perm fp32 for the combine.
-// One CTA per SM, 128 x 128 tiles, double-buffered 128-column accumulators;
-// the scale slots of the six stages take TMEM columns 256-303.
+// Per CTA: one 256-column accumulator (the scale slots of the six 34 KB
+// stages take TMEM columns 256-351, so a second accumulator does not fit);
+// the epilogue warps pull the accumulator into registers and release it
+// before their arithmetic, so the MMAs of the next tile wait only for that
+// drain.  The tile shape is set by load traffic: at fp8 rates the L2 -> SM
+// bytes per flop decide the pace (256 x 128 pair tiles were bound by about
+// 13 TB/s of loads), and 256 x 256 pair tiles halve them.
 #include <algorithm>
 #include <cstring>
 #include <mutex>
@@ -29,40 +38,40 @@ namespace moe {
 
 namespace {
 
-constexpr int XBM = 128;                    // tile rows
-constexpr int XBN = 128;                    // tile columns (UMMA N)
+constexpr int XBM = 128;                    // tile rows per CTA (256 per pair)
+constexpr int XBN = 256;                    // tile columns (UMMA N of the pair)
 constexpr int XBK = 128;                    // K per stage: one 128-byte row of e4m3
 constexpr int XUK = 32;                     // K per MMA (= one scale block)
-constexpr int XA_BYTES = XBM * XBK;         // 16 KB
-constexpr int XB_BYTES = XBN * XBK;         // 16 KB
-constexpr int XSTAGE = XA_BYTES + XB_BYTES;
+constexpr int XA_BYTES = XBM * XBK;         // 16 KB: this CTA's A rows
+constexpr int XB_BYTES = (XBN / 2) * XBK;   // 16 KB: this CTA's half of the B rows
+constexpr int XSF_OFF = XA_BYTES + XB_BYTES;
+constexpr int XLOAD = XSF_OFF + 3 * kMxAtom;    // + A atom, two B atoms: bytes per CTA and stage
+constexpr int XSTAGE = 34 * 1024;               // stage stride (1024-byte aligned)
 constexpr int XSTAGES = 6;
-constexpr int XSF_BYTES = 2 * kMxAtom;      // per stage: the A atom, then the B atom
-constexpr int XTHREADS = 384;               // warp 0 TMA, 1 MMA, 2 TMEM, 4-11 epilogue
+constexpr int XTHREADS = 384;               // warp 0 TMA, 1 MMA, 2 TMEM, 3 scan, 4-11 epilogue
 constexpr int XEPI0 = 4;
-constexpr int XEPI_THREADS = 256;
+constexpr int XEPI_WARPS = 8;
 constexpr int XTMEM_COLS = 512;
-constexpr int XSF_COL = 2 * XBN;            // stage s scales: columns 256 + 8 s (A), + 4 (B)
+constexpr int XSF_COL = XBN;                // stage s scales: columns 256 + 16 s (A), + 4 (B)
+constexpr int XSF_SLOT = 16;
 constexpr uint64_t XWAIT_NS = 2000000000ull;  // bounded waits give up after 2 s
 constexpr uint64_t XDRAIN_NS = 200000000ull;
-constexpr size_t XRESERVE = 2048;           // struct XShared
-constexpr size_t XSMEM = XRESERVE + 1024 + (size_t)XSTAGES * (XSTAGE + XSF_BYTES);
+constexpr size_t XRESERVE = 3072;           // struct XShared
+constexpr size_t XSMEM = XRESERVE + 1024 + (size_t)XSTAGES * XSTAGE;
+static_assert(XSTAGE % 1024 == 0 && XLOAD <= XSTAGE, "stage layout");
 static_assert(XSMEM <= 232448, "exceeds the 227 KB opt-in shared memory of a block");
-static_assert(XSF_COL + 8 * XSTAGES <= XTMEM_COLS, "scale slots exceed the TMEM allocation");
+static_assert(XSF_COL + XSF_SLOT * XSTAGES <= XTMEM_COLS, "scale slots exceed TMEM");
 
 enum MxKind { MXK_GATE_UP = 0, MXK_DOWN = 1 };
 
 struct XParams {
   const int32_t* row_offsets;  // [E+1] padded segment offsets (multiples of 128)
   int E;
-  int K;                       // reduction length (multiple of 128)
   int H;                       // hidden size (gate/up: output units; down: K)
   int d;                       // model dim
-  int n_tiles;                 // column tiles per 128-row block
+  int n_tiles;                 // column tiles per pair of 128-row blocks
   int kg;                      // K / 128: scale atoms per row block
-  int nbt;                     // weight scale blocks per expert
-  const uint8_t* sfa;          // activation scale atoms [R/128][kg][512]
-  const uint8_t* sfb;          // weight scale atoms [E][nbt][kg][512]
+  int nbt;                     // weight scale blocks (128 rows) per expert
   uint8_t* hq;                 // gate/up: h codes [R][H]
   uint8_t* hs;                 // gate/up: h scale atoms [R/128][H/128][512]
   float* out;                  // down: out_perm [R][d] fp32
@@ -72,17 +81,18 @@ struct XParams {
 struct XShared {
   uint64_t full[XSTAGES];
   uint64_t empty[XSTAGES];
-  uint64_t tfull[2];
-  uint64_t tempty[2];
+  uint64_t tfull;
+  uint64_t tempty;
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
-  int roff[257];
+  int roff[257];               // padded segment offsets
+  int ppre[257];               // 256-row pair tiles before expert e
 };
 static_assert(sizeof(XShared) <= XRESERVE, "bookkeeping too large");
 
 struct XTile {
-  int e, m0, n0;
+  int e, m0, n0, row_end;      // m0: the pair's first row
 };
 
 // Last index i in [0, n) with a[i] <= v (a non-decreasing, a[0] <= v).
@@ -95,16 +105,19 @@ __device__ __forceinline__ int x_last_le(const int* a, int n, int v) {
   return lo;
 }
 
-// Tile idx: 128-row block idx / n_tiles of the padded permuted rows, column
-// tile idx % n_tiles (64 hidden units = 64 gate + 64 up weight rows for
-// gate/up, 128 model columns for down).
+// Tile idx: pair unit idx / n_tiles (two 128-row blocks of one expert's
+// padded segment; an odd last block is paired with the block after the
+// segment, computed and not stored), column tile idx % n_tiles (128 hidden
+// units = 128 gate + 128 up weight rows for gate/up, 256 model columns for
+// down).
 template <int KIND>
 __device__ __forceinline__ XTile x_tile(const XParams& p, const XShared& sh, int idx) {
   XTile t;
   const int mu = idx / p.n_tiles;
   t.n0 = (idx - mu * p.n_tiles) * (KIND == MXK_GATE_UP ? XBN / 2 : XBN);
-  t.m0 = mu * XBM;
-  t.e = x_last_le(sh.roff, p.E, t.m0);
+  t.e = x_last_le(sh.ppre, p.E, mu);
+  t.m0 = sh.roff[t.e] + (mu - sh.ppre[t.e]) * 2 * XBM;
+  t.row_end = sh.roff[t.e + 1];
   return t;
 }
 
@@ -117,111 +130,136 @@ __device__ __forceinline__ void x_fail(XShared& sh, int* status) {
 // division; the result is quantised to e4m3 (3 mantissa bits) right after.
 __device__ __forceinline__ float x_silu(float a) { return __fdividef(a, 1.f + __expf(-a)); }
 
-
 // ------------------------------------------------------------------ kernel
+// CTAs run in clusters of two.  Both load their shares of each stage
+// (completing on the even CTA's full barrier, which that CTA arms for both);
+// the even CTA's MMA thread issues the pair MMAs, whose commits arrive on both
+// CTAs' empty and accumulator-full barriers; both CTAs' epilogue warps arrive
+// on the even CTA's accumulator-empty barrier once the accumulator is in
+// their registers.
 template <int KIND>
 __global__ void __launch_bounds__(XTHREADS, 1)
 mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                const XParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t ring = (raw + (uint32_t)XRESERVE + 1023u) & ~1023u;
-  const uint32_t sfring = ring + (uint32_t)(XSTAGES * XSTAGE);
-  if (sfring + (uint32_t)(XSTAGES * XSF_BYTES) - raw > (uint32_t)XSMEM) {
+  // both CTAs of a pair see the same layout, so both return here together
+  if (ring + (uint32_t)(XSTAGES * XSTAGE) - raw > (uint32_t)XSMEM) {
     if (threadIdx.x == 0) set_status(p.status, MOE_ERR_DEVICE);
     return;
   }
   XShared& sh = *reinterpret_cast<XShared*>(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = (int)cluster_ctarank();
+  const int unit = (int)(blockIdx.x >> 1);
+  const int nunits = (int)(gridDim.x >> 1);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < XSTAGES; ++s) {
       mbar_init(smem_u32(&sh.full[s]), 1);
       mbar_init(smem_u32(&sh.empty[s]), 1);
     }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(smem_u32(&sh.tfull[a]), 1);
-      mbar_init(smem_u32(&sh.tempty[a]), XEPI_THREADS);
-    }
+    mbar_init(smem_u32(&sh.tfull), 1);
+    mbar_init(smem_u32(&sh.tempty), 2 * XEPI_WARPS);
     mbar_init(smem_u32(&sh.drain), 1);
     sh.abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmSA);
+    tma_prefetch_desc(&tmSB);
   }
   for (int e = threadIdx.x; e <= p.E; e += blockDim.x) sh.roff[e] = p.row_offsets[e];
   if (warp == 2) {
-    tmem_alloc(smem_u32(&sh.tmem_base), XTMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc_pair(smem_u32(&sh.tmem_base), XTMEM_COLS);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncthreads();
+  if (warp == 3) {
+    // 256-row pair tiles per expert, prefix over experts
+    int carry = 0;
+    for (int e0 = 0; e0 < p.E; e0 += 32) {
+      const int e = e0 + lane;
+      int v = e < p.E ? ((sh.roff[e + 1] - sh.roff[e]) / XBM + 1) / 2 : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += y;
+      }
+      if (e < p.E) sh.ppre[e + 1] = carry + v;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+    if (lane == 0) sh.ppre[0] = 0;
+  }
+  // barriers of both CTAs initialised and ppre visible before any signal
+  cluster_sync();
   tc_fence_after();
   const uint32_t tmem = sh.tmem_base;
   volatile int* abort_flag = &sh.abort_flag;
-  const int ntiles = (sh.roff[p.E] / XBM) * p.n_tiles;
+  const int ntiles = sh.ppre[p.E] * p.n_tiles;
 
   if (warp == 0 && lane == 0) {
-    // ---------------- producer: codes by TMA, scale atoms by bulk copy
+    // ---------------- producer (both CTAs)
     int stage = 0;
     uint32_t phase = 0;
-    int pending[XSTAGES];
-    for (int s = 0; s < XSTAGES; ++s) pending[s] = -1;
     bool ok = true;
-    for (int idx = blockIdx.x; idx < ntiles && ok; idx += gridDim.x) {
+    for (int idx = unit; idx < ntiles && ok; idx += nunits) {
       const XTile t = x_tile<KIND>(p, sh, idx);
-      const int jb = KIND == MXK_GATE_UP ? t.n0 / (XBN / 2) : t.n0 / XBN;
-      const uint8_t* sfa = p.sfa + (size_t)(t.m0 / XBM) * p.kg * kMxAtom;
-      const uint8_t* sfb = p.sfb + ((size_t)t.e * p.nbt + jb) * p.kg * kMxAtom;
+      const int rowA = t.m0 + XBM * rank;
+      // the tile's two 128-row weight blocks: gate and up rows of the same
+      // hidden units (gate/up), or two consecutive blocks of model columns
+      const int jb0 = KIND == MXK_GATE_UP ? t.n0 / 128 : t.n0 / 128;
+      const int jb1 = KIND == MXK_GATE_UP ? (p.H + t.n0) / 128 : t.n0 / 128 + 1;
+      const int atom_a = (rowA / XBM) * p.kg;                 // this CTA's rows' scales
+      const int atom_b0 = (t.e * p.nbt + jb0) * p.kg;
+      const int atom_b1 = (t.e * p.nbt + jb1) * p.kg;
       for (int kb = 0; kb < p.kg; ++kb) {
         if (!mbar_wait_bounded(smem_u32(&sh.empty[stage]), phase ^ 1u, abort_flag, XWAIT_NS)) {
           x_fail(sh, p.status);
           ok = false;
           break;
         }
-        const uint32_t fb = smem_u32(&sh.full[stage]);
+        const uint32_t fb_local = smem_u32(&sh.full[stage]);
+        const uint32_t fb = mapa_shared(fb_local, 0);
+        if (rank == 0) mbar_arrive_expect_tx(fb_local, 2 * XLOAD);
         const uint32_t sa = ring + stage * XSTAGE;
         const uint32_t sb = sa + XA_BYTES;
-        const uint32_t sf = sfring + stage * XSF_BYTES;
-        mbar_arrive_expect_tx(fb, XSTAGE + XSF_BYTES);
-        tma_load_2d(sa, &tmA, fb, kb * XBK, t.m0);
-        if (KIND == MXK_GATE_UP) {
-          // 64 gate rows then the 64 up rows of the same hidden units
-          tma_load_4d(sb, &tmB, fb, kb * XBK, t.n0, 0, t.e);
-          tma_load_4d(sb + XB_BYTES / 2, &tmB, fb, kb * XBK, t.n0, 1, t.e);
-        } else {
-          tma_load_3d(sb, &tmB, fb, kb * XBK, t.n0, t.e);
-        }
-        bulk_load(sf, sfa + (size_t)kb * kMxAtom, kMxAtom, fb);
-        bulk_load(sf + kMxAtom, sfb + (size_t)kb * kMxAtom, kMxAtom, fb);
-        pending[stage] = (int)phase;
+        const uint32_t sf = sa + XSF_OFF;
+        tma_load_2d_pair(sa, &tmA, fb, kb * XBK, rowA);
+        if (KIND == MXK_GATE_UP)      // rank 0: the 128 gate rows, rank 1: the 128 up rows
+          tma_load_4d_pair(sb, &tmB, fb, kb * XBK, t.n0, rank, t.e);
+        else
+          tma_load_3d_pair(sb, &tmB, fb, kb * XBK, t.n0 + (XBN / 2) * rank, t.e);
+        tma_load_2d_pair(sf, &tmSA, fb, 0, (atom_a + kb) * 4);
+        tma_load_2d_pair(sf + kMxAtom, &tmSB, fb, 0, (atom_b0 + kb) * 4);
+        tma_load_2d_pair(sf + 2 * kMxAtom, &tmSB, fb, 0, (atom_b1 + kb) * 4);
         if (++stage == XSTAGES) { stage = 0; phase ^= 1u; }
       }
     }
     if (!ok) {
-      // let every copy already issued land before shared memory is released
-      for (int s = 0; s < XSTAGES; ++s)
-        if (pending[s] >= 0) {
-          int dummy = 0;
-          mbar_wait_bounded(smem_u32(&sh.full[s]), (uint32_t)pending[s], &dummy, XDRAIN_NS);
-        }
+      // this CTA's copies complete on the even CTA's barriers: give the ones
+      // in flight a bounded time to land before shared memory is released
+      const uint64_t t0 = global_ns();
+      while (global_ns() - t0 < XDRAIN_NS) {
+      }
     }
-  } else if (warp == 1 && lane == 0) {
-    // ---------------- MMA issuer
-    constexpr uint32_t idesc0 = umma_idesc_mx(XBM, XBN);
+  } else if (warp == 1 && lane == 0 && rank == 0) {
+    // ---------------- MMA issuer (even CTA)
+    constexpr uint32_t idesc0 = umma_idesc_mx(2 * XBM, XBN);
     int stage = 0;
     uint32_t phase = 0;
     int it = 0;
     bool ok = true;
-    for (int idx = blockIdx.x; idx < ntiles && ok; idx += gridDim.x, ++it) {
-      const int acc = it & 1;
-      const uint32_t acc_phase = (it >> 1) & 1;
-      if (!mbar_wait_bounded(smem_u32(&sh.tempty[acc]), acc_phase ^ 1u, abort_flag, XWAIT_NS)) {
+    for (int idx = unit; idx < ntiles && ok; idx += nunits, ++it) {
+      if (!mbar_wait_bounded_cluster(smem_u32(&sh.tempty), (it & 1) ^ 1u, abort_flag,
+                                     XWAIT_NS)) {
         x_fail(sh, p.status);
         break;
       }
       tc_fence_after();
-      const uint32_t d_tmem = tmem + acc * XBN;
       for (int kb = 0; kb < p.kg; ++kb) {
         if (!mbar_wait_bounded(smem_u32(&sh.full[stage]), phase, abort_flag, XWAIT_NS)) {
           x_fail(sh, p.status);
@@ -231,103 +269,108 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         tc_fence_after();
         const uint32_t sa = ring + stage * XSTAGE;
         const uint32_t sb = sa + XA_BYTES;
-        const uint32_t sf = sfring + stage * XSF_BYTES;
-        // this stage's scale slot is free: its previous MMAs completed
-        // before the producer could refill the stage
-        const uint32_t tsf = tmem + XSF_COL + stage * 8;
-        tmem_cp_atom(tsf, sf);
-        tmem_cp_atom(tsf + 4, sf + kMxAtom);
+        const uint32_t sf = sa + XSF_OFF;
+        // this stage's scale slot is free in both CTAs: its previous MMAs
+        // completed before either producer could refill the stage
+        const uint32_t tsf = tmem + XSF_COL + stage * XSF_SLOT;
+        tmem_cp_atom_pair(tsf, sf);
+        tmem_cp_atom_pair(tsf + 4, sf + kMxAtom);
+        tmem_cp_atom_pair(tsf + 8, sf + 2 * kMxAtom);
 #pragma unroll
         for (int kk = 0; kk < XBK / XUK; ++kk) {
           const uint64_t ad = umma_desc_sw128(sa + kk * XUK, 16, 1024);
           const uint64_t bd = umma_desc_sw128(sb + kk * XUK, 16, 1024);
-          umma_mx(d_tmem, ad, bd, umma_idesc_sfid(idesc0, (uint32_t)kk), tsf, tsf + 4,
-                  (kb | kk) != 0 ? 1u : 0u);
+          umma_mx_pair(tmem, ad, bd, umma_idesc_sfid(idesc0, (uint32_t)kk), tsf, tsf + 4,
+                       (kb | kk) != 0 ? 1u : 0u);
         }
-        umma_commit(smem_u32(&sh.empty[stage]));
+        umma_commit_pair(smem_u32(&sh.empty[stage]), 3);
         if (++stage == XSTAGES) { stage = 0; phase ^= 1u; }
       }
       if (!ok) break;
-      umma_commit(smem_u32(&sh.tfull[acc]));
+      umma_commit_pair(smem_u32(&sh.tfull), 3);
     }
     // all issued MMAs complete before TMEM can be released
-    umma_commit(smem_u32(&sh.drain));
+    umma_commit_pair(smem_u32(&sh.drain), 1);
     int dummy = 0;
     mbar_wait_bounded(smem_u32(&sh.drain), 0, &dummy, XDRAIN_NS);
   } else if (warp >= XEPI0) {
-    // ---------------- epilogue: TMEM lanes 32*(warp%4) .. +31, column half
+    // ---------------- epilogue (both CTAs): TMEM lanes 32*(warp%4) .. +31
     const int q = warp & 3;
     const int half = (warp - XEPI0) >> 2;
+    const uint32_t tempty_leader = mapa_shared(smem_u32(&sh.tempty), 0);
     int it = 0;
-    for (int idx = blockIdx.x; idx < ntiles; idx += gridDim.x, ++it) {
+    for (int idx = unit; idx < ntiles; idx += nunits, ++it) {
       const XTile t = x_tile<KIND>(p, sh, idx);
-      const int acc = it & 1;
-      const uint32_t acc_phase = (it >> 1) & 1;
-      if (!mbar_wait_bounded(smem_u32(&sh.tfull[acc]), acc_phase, abort_flag, XWAIT_NS)) {
+      if (!mbar_wait_bounded(smem_u32(&sh.tfull), it & 1, abort_flag, XWAIT_NS)) {
         if (lane == 0) x_fail(sh, p.status);
         break;
       }
       tc_fence_after();
-      const uint32_t tacc = tmem + ((uint32_t)(q * 32) << 16) + acc * XBN;
-      const int row = t.m0 + q * 32 + lane;
-      uint32_t r0[32], r1[32];
+      const uint32_t tacc = tmem + ((uint32_t)(q * 32) << 16);
+      const int blk = t.m0 + XBM * rank;            // this CTA's 128 rows
+      const bool store = blk < t.row_end;           // else the pair's padding half
+      const int row = blk + q * 32 + lane;
+      // this warp's 128 accumulator columns into registers; gate/up: gate
+      // columns half*64 .. +63 and the matching up columns 128 + half*64 ..
+      uint32_t r[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int col = KIND == MXK_GATE_UP ? (c >> 1) * (XBN / 2) + half * 64 + (c & 1) * 32
+                                            : half * 128 + c * 32;
+        tmem_ld32(tacc + col, r[c]);
+      }
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(tempty_leader);   // accumulator free
+      if (!store) continue;
       if (KIND == MXK_GATE_UP) {
-        // 32 hidden units per half: gate columns half*32.., up columns 64 + half*32..
-        tmem_ld32(tacc + half * 32, r0);
-        tmem_ld32(tacc + XBN / 2 + half * 32, r1);
-        tmem_ld_wait();
-        tc_fence_before();
-        mbar_arrive(smem_u32(&sh.tempty[acc]));    // accumulator free once in registers
-        float h[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          h[i] = x_silu(__uint_as_float(r0[i])) * __uint_as_float(r1[i]);
-        uint32_t cq[8];
-        const uint32_t sbyte = mx_quant32(h, cq);
-        const int col = t.n0 + half * 32;
-        uint8_t* o = p.hq + (size_t)row * p.H + col;
-        st_v4(o, make_uint4(cq[0], cq[1], cq[2], cq[3]));
-        st_v4(o + 16, make_uint4(cq[4], cq[5], cq[6], cq[7]));
-        p.hs[((size_t)(row >> 7) * (p.H / 128) + (col >> 7)) * kMxAtom +
-             mx_sf_byte(row & 127, (col >> 5) & 3)] = (uint8_t)sbyte;
+        for (int c = 0; c < 2; ++c) {
+          float h[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            h[i] = x_silu(__uint_as_float(r[c][i])) * __uint_as_float(r[2 + c][i]);
+          uint32_t cq[8];
+          const uint32_t sbyte = mx_quant32(h, cq);
+          const int col = t.n0 + half * 64 + c * 32;
+          uint8_t* o = p.hq + (size_t)row * p.H + col;
+          st_v4(o, make_uint4(cq[0], cq[1], cq[2], cq[3]));
+          st_v4(o + 16, make_uint4(cq[4], cq[5], cq[6], cq[7]));
+          p.hs[((size_t)(row >> 7) * (p.H / 128) + (col >> 7)) * kMxAtom +
+               mx_sf_byte(row & 127, (col >> 5) & 3)] = (uint8_t)sbyte;
+        }
       } else {
-        // 64 model columns per half, fp32
-        tmem_ld32(tacc + half * 64, r0);
-        tmem_ld32(tacc + half * 64 + 32, r1);
-        tmem_ld_wait();
-        tc_fence_before();
-        mbar_arrive(smem_u32(&sh.tempty[acc]));
-        float* o = p.out + (size_t)row * p.d + t.n0 + half * 64;
+        float* o = p.out + (size_t)row * p.d + t.n0 + half * 128;
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          st_v4(o + 4 * i, make_uint4(r0[4 * i], r0[4 * i + 1], r0[4 * i + 2], r0[4 * i + 3]));
+        for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          st_v4(o + 32 + 4 * i,
-                make_uint4(r1[4 * i], r1[4 * i + 1], r1[4 * i + 2], r1[4 * i + 3]));
+          for (int i = 0; i < 8; ++i)
+            st_v4(o + 32 * c + 4 * i, make_uint4(r[c][4 * i], r[c][4 * i + 1], r[c][4 * i + 2],
+                                                 r[c][4 * i + 3]));
       }
     }
   }
   __syncwarp();
   tc_fence_before();
-  __syncthreads();
+  // no CTA of a pair leaves (or frees TMEM) while its peer may still signal
+  // its barriers or the pair's MMAs may still write its TMEM
+  cluster_sync();
   if (warp == 2) {
     tc_fence_after();
-    tmem_dealloc(tmem, XTMEM_COLS);
+    tmem_dealloc_pair(tmem, XTMEM_COLS);
   }
 }
 
 // ------------------------------------------------------------------ weights
 // One thread per block of 32 along K of one weight row: codes stay in the
-// row's place ([rows][K]); the scale byte goes to the atom of the row's tile
-// row.  Gate/up (W_gu [E][2H][d]): tile block jb = n / 64 of the hidden units
-// holds gate rows 64 jb.. at tile rows 0-63 and the matching up rows at
-// 64-127.  Down (W_down [E][d][H]): tile block jb = n / 128, tile row n % 128.
+// row's place ([rows][K]); the scale byte goes to the atom of the row's
+// 128-row block of its expert's matrix (W_gu [E][2H][d]: blocks of gate rows,
+// then of up rows; W_down [E][d][H]).
 __global__ void __launch_bounds__(256)
 mx_quant_weights_kernel(const bf16* __restrict__ W, uint8_t* __restrict__ Wq,
-                        uint8_t* __restrict__ Ws, long long rows, int K, int rows_per_e,
-                        int gate_up, int H) {
-  const int nb = K / 32, kg = K / 128;
+                        uint8_t* __restrict__ Ws, long long rows, int K, int rows_per_e) {
+  const int nb = K / 32, kg = K / 128, nbt = rows_per_e / 128;
   const long long total = rows * nb;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (long long)gridDim.x * blockDim.x) {
@@ -344,23 +387,10 @@ mx_quant_weights_kernel(const bf16* __restrict__ W, uint8_t* __restrict__ Wq,
     st_v4(o + 16, make_uint4(cq[4], cq[5], cq[6], cq[7]));
     const int e = (int)(row / rows_per_e);
     const int n = (int)(row - (long long)e * rows_per_e);
-    int jb, v_row, nbt;
-    if (gate_up) {
-      const bool up = n >= H;
-      const int nn = up ? n - H : n;
-      jb = nn / 64;
-      v_row = nn % 64 + (up ? 64 : 0);
-      nbt = H / 64;
-    } else {
-      jb = n / 128;
-      v_row = n % 128;
-      nbt = rows_per_e / 128;
-    }
-    Ws[(((size_t)e * nbt + jb) * kg + (b >> 2)) * kMxAtom + mx_sf_byte(v_row, b & 3)] =
+    Ws[(((size_t)e * nbt + n / 128) * kg + (b >> 2)) * kMxAtom + mx_sf_byte(n % 128, b & 3)] =
         (uint8_t)sbyte;
   }
 }
-
 
 // ------------------------------------------------------------------ host side
 typedef CUresult (*XEncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -382,10 +412,11 @@ XEncodeFn x_encode_fn() {
   return fn;
 }
 
-// Byte tensor map (e4m3 codes), 128-byte swizzle, zero fill out of bounds.
-// dims innermost first; strides in bytes for dims 1..rank-1.
+// Byte tensor map, zero fill out of bounds; dims innermost first, strides in
+// bytes for dims 1..rank-1.  Codes use the 128-byte swizzle; scale atoms are
+// copied as plain 4 x 128-byte boxes.
 bool x_make_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims,
-                const uint64_t* strides, const uint32_t* box) {
+                const uint64_t* strides, const uint32_t* box, bool swizzle) {
   XEncodeFn fn = x_encode_fn();
   if (!fn) return false;
   cuuint64_t gd[5], gs[4];
@@ -393,23 +424,78 @@ bool x_make_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims,
   for (int i = 0; i < rank; ++i) { gd[i] = dims[i]; bx[i] = box[i]; es[i] = 1; }
   for (int i = 0; i < rank - 1; ++i) gs[i] = strides[i];
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, (cuuint32_t)rank, const_cast<void*>(ptr), gd, gs,
-            bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Scale atoms [n_atoms][512] as a [4 n_atoms][128] byte matrix, one atom per box.
+bool x_atom_map(CUtensorMap* m, const void* ptr, size_t n_atoms) {
+  uint64_t dims[2] = {128, (uint64_t)n_atoms * 4}, strides[1] = {128};
+  uint32_t box[2] = {128, 4};
+  return x_make_map(m, ptr, 2, dims, strides, box, false);
+}
+
 template <int KIND>
-cudaError_t x_launch(const CUtensorMap& a, const CUtensorMap& b, const XParams& p, int sms,
-                     cudaStream_t s) {
+cudaError_t x_set_attr() {
   static std::once_flag once;
   static cudaError_t err = cudaSuccess;
   std::call_once(once, [] {
     err = cudaFuncSetAttribute(mx_gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)XSMEM);
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(mx_gemm_kernel<KIND>,
+                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
   });
+  return err;
+}
+
+// Clusters of two that can be resident at once (0 if none).
+template <int KIND>
+int x_pair_clusters(int num_sms) {
+  static std::once_flag once;
+  static int n = 0;
+  std::call_once(once, [num_sms] {
+    if (x_set_attr<KIND>() != cudaSuccess) return;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(num_sms & ~1), 1, 1);
+    cfg.blockDim = dim3(XTHREADS, 1, 1);
+    cfg.dynamicSmemBytes = XSMEM;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int c = 0;
+    if (cudaOccupancyMaxActiveClusters(&c, mx_gemm_kernel<KIND>, &cfg) == cudaSuccess) n = c;
+    else cudaGetLastError();
+  });
+  return n;
+}
+
+template <int KIND>
+cudaError_t x_launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& sa,
+                     const CUtensorMap& sb, const XParams& p, int sms, cudaStream_t s) {
+  cudaError_t err = x_set_attr<KIND>();
   if (err != cudaSuccess) return err;
-  mx_gemm_kernel<KIND><<<sms, XTHREADS, XSMEM, s>>>(a, b, p);
-  return cudaGetLastError();
+  const int clusters = std::min(x_pair_clusters<KIND>(sms), sms / 2);
+  if (clusters <= 0) return cudaErrorLaunchOutOfResources;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
+  cfg.blockDim = dim3(XTHREADS, 1, 1);
+  cfg.dynamicSmemBytes = XSMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mx_gemm_kernel<KIND>, a, b, sa, sb, p);
 }
 
 }  // namespace
@@ -422,42 +508,43 @@ cudaError_t launch_mx_gemm(const MxGemmCall& g, cudaStream_t s) {
   p.E = g.E;
   p.H = g.H;
   p.d = g.d;
-  p.sfa = g.sfa;
-  p.sfb = g.sfb;
   p.hq = g.hq;
   p.hs = g.hs;
   p.out = g.out;
   p.status = g.status;
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tsa, tsb;
   const uint64_t rows = (uint64_t)g.rows;
+  int K;
   bool ok;
   if (g.gate_up) {
     // A: x codes [rows][d]; B: W_gu codes [E][2][H][d] -> dims {d, H, 2, E}
-    p.K = g.d;
+    K = g.d;
     p.n_tiles = g.H / (XBN / 2);
-    p.nbt = g.H / (XBN / 2);
+    p.nbt = 2 * g.H / 128;
     uint64_t da[2] = {(uint64_t)g.d, rows}, sa[1] = {(uint64_t)g.d};
     uint32_t ba[2] = {XBK, XBM};
     uint64_t db[4] = {(uint64_t)g.d, (uint64_t)g.H, 2, (uint64_t)g.E};
     uint64_t sb[3] = {(uint64_t)g.d, (uint64_t)g.H * g.d, (uint64_t)2 * g.H * g.d};
     uint32_t bb[4] = {XBK, XBN / 2, 1, 1};
-    ok = x_make_map(&ta, g.A, 2, da, sa, ba) && x_make_map(&tb, g.B, 4, db, sb, bb);
+    ok = x_make_map(&ta, g.A, 2, da, sa, ba, true) && x_make_map(&tb, g.B, 4, db, sb, bb, true);
   } else {
     // A: h codes [rows][H]; B: W_down codes [E][d][H] -> dims {H, d, E}
-    p.K = g.H;
+    K = g.H;
     p.n_tiles = g.d / XBN;
-    p.nbt = g.d / XBN;
+    p.nbt = g.d / 128;
     uint64_t da[2] = {(uint64_t)g.H, rows}, sa[1] = {(uint64_t)g.H};
     uint32_t ba[2] = {XBK, XBM};
     uint64_t db[3] = {(uint64_t)g.H, (uint64_t)g.d, (uint64_t)g.E};
     uint64_t sb[2] = {(uint64_t)g.H, (uint64_t)g.d * g.H};
-    uint32_t bb[3] = {XBK, XBN, 1};
-    ok = x_make_map(&ta, g.A, 2, da, sa, ba) && x_make_map(&tb, g.B, 3, db, sb, bb);
+    uint32_t bb[3] = {XBK, XBN / 2, 1};
+    ok = x_make_map(&ta, g.A, 2, da, sa, ba, true) && x_make_map(&tb, g.B, 3, db, sb, bb, true);
   }
+  p.kg = K / XBK;
+  ok = ok && x_atom_map(&tsa, g.sfa, (size_t)(rows / XBM) * p.kg) &&
+       x_atom_map(&tsb, g.sfb, (size_t)g.E * p.nbt * p.kg);
   if (!ok) return cudaErrorInvalidValue;
-  p.kg = p.K / XBK;
-  return g.gate_up ? x_launch<MXK_GATE_UP>(ta, tb, p, di.num_sms, s)
-                   : x_launch<MXK_DOWN>(ta, tb, p, di.num_sms, s);
+  return g.gate_up ? x_launch<MXK_GATE_UP>(ta, tb, tsa, tsb, p, di.num_sms, s)
+                   : x_launch<MXK_DOWN>(ta, tb, tsa, tsb, p, di.num_sms, s);
 }
 
 cudaError_t launch_mx_quant_weights(const moe_config& c, const void* W_gu, const void* W_down,
@@ -467,9 +554,9 @@ cudaError_t launch_mx_quant_weights(const moe_config& c, const void* W_gu, const
   if (device_info(&di) != MOE_OK) return cudaErrorUnknown;
   const int grid = di.num_sms * 8;
   mx_quant_weights_kernel<<<grid, 256, 0, s>>>(static_cast<const bf16*>(W_gu), W_gu_q, W_gu_s,
-                                               (long long)c.E * 2 * c.H, c.d, 2 * c.H, 1, c.H);
+                                               (long long)c.E * 2 * c.H, c.d, 2 * c.H);
   mx_quant_weights_kernel<<<grid, 256, 0, s>>>(static_cast<const bf16*>(W_down), W_down_q,
-                                               W_down_s, (long long)c.E * c.d, c.H, c.d, 0, c.H);
+                                               W_down_s, (long long)c.E * c.d, c.H, c.d);
   return cudaGetLastError();
 }
 

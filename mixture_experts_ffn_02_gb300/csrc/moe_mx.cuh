@@ -75,6 +75,23 @@ __device__ __forceinline__ void umma_mx(uint32_t tmem_d, uint64_t adesc, uint64_
       : "memory");
 }
 
+// CTA-pair form: issued by one thread of the even CTA; A rows 0-127 and D
+// lanes in the even CTA, rows 128-255 in the odd one, B columns split in
+// halves; each CTA reads its rows' A scales and the scales of all N columns
+// of B from its own TMEM at the given addresses.
+__device__ __forceinline__ void umma_mx_pair(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                             uint32_t idesc, uint32_t tsfa, uint32_t tsfb,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X"
+      " [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+      :: "r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(tsfa), "r"(tsfb),
+         "r"(accumulate)
+      : "memory");
+}
+
 // Shared-memory descriptor without swizzle (byte offsets >> 4).
 __device__ __forceinline__ uint64_t umma_desc_plain(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   uint64_t d = 0;
@@ -90,6 +107,13 @@ __device__ __forceinline__ uint64_t umma_desc_plain(uint32_t saddr, uint32_t lbo
 // same thread issues after it.
 __device__ __forceinline__ void tmem_cp_atom(uint32_t taddr, uint32_t saddr) {
   asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;"
+               :: "r"(taddr), "l"(umma_desc_plain(saddr, 128, 128)) : "memory");
+}
+
+// The pair form: issued by the even CTA, each CTA's atom (same shared
+// offset) into its own TMEM (same address).
+__device__ __forceinline__ void tmem_cp_atom_pair(uint32_t taddr, uint32_t saddr) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;"
                :: "r"(taddr), "l"(umma_desc_plain(saddr, 128, 128)) : "memory");
 }
 

@@ -109,8 +109,9 @@ def test_struct_layouts_match_the_header():
 
 def test_mx_sizes_and_shape_rule(clib):
     """MXFP8 buffers: codes keep the bf16 tensors' element counts, one scale
-    byte per 32 values in 512-byte atoms; d or H not a multiple of 128 is a
-    shape error (the tiny 64-wide layer has no MX path)."""
+    byte per 32 values in 512-byte atoms; a d or H off the tile grid is a
+    shape error (d must be a multiple of 256 and H of 128; the tiny 64-wide
+    layer has no MX path)."""
     s = synth.shape(2)
     c = binding.config(s)
     sizes = (ctypes.c_size_t * binding.MOE_MX_FIELDS)()

@@ -40,14 +40,11 @@ def unpack_rows(atoms, K, rows):
 
 
 def unpack_w_gu(atoms, E, H, d):
-    """W_gu scale atoms [E][H/64][d/128][512] -> [E][2H][d/32]."""
-    a = atoms.reshape(E, H // 64, d // 128, ATOM)
+    """W_gu scale atoms [E][2H/128][d/128][512] -> [E][2H][d/32]."""
+    a = atoms.reshape(E, 2 * H // 128, d // 128, ATOM)
     n = np.arange(2 * H)
-    up = n >= H
-    nn = np.where(up, n - H, n)
-    j, v = nn // 64, nn % 64 + 64 * up
     kb = np.arange(d // 32)
-    return a[:, j[:, None], kb[None, :] // 4, sf_byte(v[:, None], kb[None, :] % 4)]
+    return a[:, n[:, None] // 128, kb[None, :] // 4, sf_byte(n[:, None] % 128, kb[None, :] % 4)]
 
 
 def unpack_w_down(atoms, E, d, H):
