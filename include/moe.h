@@ -330,8 +330,9 @@ int moe_backward(const moe_config* cfg, const moe_tensors* t, const moe_grads* g
  * (r % 32) * 16 + (r / 32) * 4 + kb.
  *
  * Shapes: d a multiple of 256 and H of 128, else MOE_ERR_SHAPE.  All buffers are
- * caller-owned device memory, 16-byte aligned; moe_mx_sizes gives their
- * sizes.  Router, route, combine and the shared expert are the bf16 path's. */
+ * caller-owned device memory, 16-byte aligned, and the four code buffers and
+ * t->out_perm 32-byte aligned (the kernels store 32 bytes per thread), else
+ * MOE_ERR_ALIGN; moe_mx_sizes gives their sizes.  Router, route, combine and the shared expert are the bf16 path's. */
 typedef struct moe_mx_tensors {
   uint8_t* W_gu_q;    /* [E][2H][d] codes of W_gu                               */
   uint8_t* W_gu_s;    /* [E][2H/128][d/128] atoms (128-row blocks of W_gu[e])     */

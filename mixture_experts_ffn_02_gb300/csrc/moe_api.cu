@@ -439,6 +439,15 @@ int do_backward(const moe_config* c, const moe_tensors* t, const moe_grads* g, C
 }
 
 // ---- MXFP8 routed experts
+// The MX kernels store 32 bytes per lane: their code buffers and out_perm
+// must be 32-byte aligned.
+bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
+#define MOE_NEED32(p)                          \
+  do {                                         \
+    if (!(p)) return MOE_ERR_NULL;             \
+    if (!aligned32(p)) return MOE_ERR_ALIGN;   \
+  } while (0)
+
 int check_mx(const moe_config* c) {
   if (c->d % 256 || c->H % 128) return MOE_ERR_SHAPE;
   return MOE_OK;
@@ -459,7 +468,7 @@ void mx_sizes(const moe_config& c, size_t* b) {
 int do_mx_permute(const moe_config* c, const moe_tensors* t, const moe_mx_tensors* m, Call& k) {
   MOE_NEED(t->x); MOE_NEED(t->topk_idx); MOE_NEED(t->counts); MOE_NEED(t->offsets);
   MOE_NEED(t->row_offsets); MOE_NEED(t->perm); MOE_NEED(t->inv);
-  MOE_NEED(m->x_q); MOE_NEED(m->x_s);
+  MOE_NEED32(m->x_q); MOE_NEED(m->x_s);
   MOE_CUDA(launch_permute_mx(*c, t->x, t->topk_idx, t->counts, t->offsets, t->row_offsets,
                              t->perm, t->inv, m->x_q, m->x_s, k.ws, k.w, k.s));
   return MOE_OK;
@@ -478,12 +487,12 @@ int do_mx_gemm(const moe_config* c, const moe_tensors* t, const moe_mx_tensors* 
   g.status = k.status;
   if (gate_up) {
     MOE_NEED(m->x_q); MOE_NEED(m->x_s); MOE_NEED(m->W_gu_q); MOE_NEED(m->W_gu_s);
-    MOE_NEED(m->h_q); MOE_NEED(m->h_s);
+    MOE_NEED32(m->h_q); MOE_NEED(m->h_s);
     g.A = m->x_q; g.sfa = m->x_s; g.B = m->W_gu_q; g.sfb = m->W_gu_s;
     g.hq = m->h_q; g.hs = m->h_s;
   } else {
     MOE_NEED(m->h_q); MOE_NEED(m->h_s); MOE_NEED(m->W_down_q); MOE_NEED(m->W_down_s);
-    MOE_NEED(t->out_perm);
+    MOE_NEED32(t->out_perm);
     g.A = m->h_q; g.sfa = m->h_s; g.B = m->W_down_q; g.sfb = m->W_down_s;
     g.out = t->out_perm;
   }
@@ -604,7 +613,8 @@ int moe_mx_quantize_weights(const moe_config* cfg, const moe_tensors* t,
   if ((rc = check_device())) return rc;
   if (!t || !mx) return MOE_ERR_NULL;
   MOE_NEED(t->W_gu); MOE_NEED(t->W_down);
-  MOE_NEED(mx->W_gu_q); MOE_NEED(mx->W_gu_s); MOE_NEED(mx->W_down_q); MOE_NEED(mx->W_down_s);
+  MOE_NEED32(mx->W_gu_q); MOE_NEED(mx->W_gu_s); MOE_NEED32(mx->W_down_q);
+  MOE_NEED(mx->W_down_s);
   MOE_CUDA(launch_mx_quant_weights(*cfg, t->W_gu, t->W_down, mx->W_gu_q, mx->W_gu_s,
                                    mx->W_down_q, mx->W_down_s,
                                    static_cast<cudaStream_t>(stream)));

@@ -999,9 +999,7 @@ perm_scatter_kernel(const bf16* __restrict__ x, const int32_t* __restrict__ topk
       for (int j = 0; j < k; ++j) {
         const int r = dst[j];
         if (r < 0) continue;
-        uint8_t* o = x_q + (size_t)r * d + b * 32;
-        st_v4(o, make_uint4(q[0], q[1], q[2], q[3]));
-        st_v4(o + 16, make_uint4(q[4], q[5], q[6], q[7]));
+        st_v8(x_q + (size_t)r * d + b * 32, q);
         x_s[((size_t)(r >> 7) * kg + (b >> 2)) * kMxAtom + mx_sf_byte(r & 127, b & 3)] =
             (uint8_t)sb;
       }

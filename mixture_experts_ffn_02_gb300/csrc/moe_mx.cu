@@ -334,9 +334,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           uint32_t cq[8];
           const uint32_t sbyte = mx_quant32(h, cq);
           const int col = t.n0 + half * 64 + c * 32;
-          uint8_t* o = p.hq + (size_t)row * p.H + col;
-          st_v4(o, make_uint4(cq[0], cq[1], cq[2], cq[3]));
-          st_v4(o + 16, make_uint4(cq[4], cq[5], cq[6], cq[7]));
+          st_v8(p.hq + (size_t)row * p.H + col, cq);
           p.hs[((size_t)(row >> 7) * (p.H / 128) + (col >> 7)) * kMxAtom +
                mx_sf_byte(row & 127, (col >> 5) & 3)] = (uint8_t)sbyte;
         }
@@ -345,9 +343,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            st_v4(o + 32 * c + 4 * i, make_uint4(r[c][4 * i], r[c][4 * i + 1], r[c][4 * i + 2],
-                                                 r[c][4 * i + 3]));
+          for (int i = 0; i < 4; ++i) st_v8(o + 32 * c + 8 * i, &r[c][8 * i]);
       }
     }
   }
@@ -382,9 +378,7 @@ mx_quant_weights_kernel(const bf16* __restrict__ W, uint8_t* __restrict__ Wq,
     for (int u = 0; u < 4; ++u) unpack8(ld_nc_v4(src + u * 8), v + 8 * u);
     uint32_t cq[8];
     const uint32_t sbyte = mx_quant32(v, cq);
-    uint8_t* o = Wq + row * K + b * 32;
-    st_v4(o, make_uint4(cq[0], cq[1], cq[2], cq[3]));
-    st_v4(o + 16, make_uint4(cq[4], cq[5], cq[6], cq[7]));
+    st_v8(Wq + row * K + b * 32, cq);
     const int e = (int)(row / rows_per_e);
     const int n = (int)(row - (long long)e * rows_per_e);
     Ws[(((size_t)e * nbt + n / 128) * kg + (b >> 2)) * kMxAtom + mx_sf_byte(n % 128, b & 3)] =

@@ -38,6 +38,14 @@ __device__ __forceinline__ uint32_t mx_quant32(const float* v, uint32_t* codes) 
   return (uint32_t)(X + 127);
 }
 
+// 32-byte global store (one full sector per lane); the address must be
+// 32-byte aligned.
+__device__ __forceinline__ void st_v8(void* p, const uint32_t* v) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+               :: "l"(p), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]),
+                  "r"(v[6]), "r"(v[7]) : "memory");
+}
+
 // ----------------------------------------------------------------- scale layout
 // Scale factors sit in 512-byte atoms, one per (128-row block, 128-column
 // group): 128 rows x 4 blocks of 32 along K.  Row r, block kb of the atom is

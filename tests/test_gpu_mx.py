@@ -227,3 +227,26 @@ def test_mx_forward_is_deterministic():
     lay.mx_forward()
     torch.cuda.synchronize()
     assert torch.equal(y0, lay.bufs["y"])
+
+
+def test_mx_rejects_code_buffers_off_32_bytes():
+    """The MX kernels store 32 bytes per thread: a code buffer or out_perm
+    that is 16- but not 32-byte aligned is refused before any launch."""
+    from mixture_experts_ffn_02_gb300 import binding
+    s = scaled_shape(5, 1300, dict(d=512, H=256))
+    _, lay = mx_layer(s)
+    keep = lay.mx["h_q"]
+    lay.mx["h_q"] = keep[16:]
+    with pytest.raises(binding.MoEError) as ei:
+        lay.mx_gate_up()
+    assert ei.value.code == 3
+    lay.mx["h_q"] = keep
+    keep = lay.bufs["out_perm"]
+    lay.bufs["out_perm"] = keep.view(-1)[4:]
+    with pytest.raises(binding.MoEError) as ei:
+        lay.mx_down()
+    assert ei.value.code == 3
+    lay.bufs["out_perm"] = keep
+    lay.mx_forward()
+    torch.cuda.synchronize()
+    assert lay.status() == 0
