@@ -8,7 +8,8 @@ What it follows:
 
 * "KohakUwULLM" README, Key features: native MXFP8 training with e4m3 values
   and UE8M0 scales, one scale per block of 32 consecutive values, applied to
-  the routed experts, with fully fused MXFP8 expert kernels.
+  the feed-forward pair and the routed experts, with fully fused MXFP8 expert
+  kernels.
 * The element and scale formats themselves (the pages name them only): e4m3
   is the 8-bit float with 1 sign bit, 4 exponent bits of bias 7 and 3
   mantissa bits, subnormals at exponent field 0, no infinities and NaN at
@@ -23,10 +24,11 @@ Readings (the pages say only "e4m3 values with UE8M0 per-32 block scales"):
   exponent of the largest e4m3 normal), clamped to [-127, 127]; an all-zero
   block takes X = -127.  Each element is v / 2^X rounded to the nearest e4m3
   value, ties to the even code, and magnitudes above 448 saturate to 448.
-* The routed experts run on MXFP8 operands: a = Q(x) Q(W_gate)^T,
-  b = Q(x) Q(W_up)^T, h = silu(a) * b, out = Q(h) Q(W_down)^T, with Q the
-  quantise-dequantise round trip above and everything else exact (fp64).
-  The shared expert, the router and the combine are unchanged (no MX).
+* The routed experts and the shared expert (the layer's dense feed-forward
+  pair) run on MXFP8 operands: a = Q(x) Q(W_gate)^T, b = Q(x) Q(W_up)^T,
+  h = silu(a) * b, out = Q(h) Q(W_down)^T, with Q the quantise-dequantise
+  round trip above and everything else exact (fp64).  The router and the
+  combine are unchanged (no MX).
 
 Pins: ``tests/test_oracle_mx.py`` (closed forms, torch's float8_e4m3fn
 conversion as a library routine, brute-force nearest rounding, round trips of
@@ -114,12 +116,13 @@ def mx_roundtrip(v):
 
 def experts_forward_mx(x, topk_idx, gates, W_gu, W_down, Ws_gu=None, Ws_down=None,
                        valid=None):
-    """The expert sum of the layer with MXFP8 routed experts.
+    """The expert sum of the layer with MXFP8 experts.
 
     Routed part: the permute/combine formulation of ``moe_oracle`` on the
     quantised operands Q(x), Q(W_gu) (blocks along d) and Q(W_down) (blocks
     along H), with the hidden h quantised along H before the down product.
-    The shared expert is the exact fp64 SwiGLU of the unquantised x.
+    The shared expert is the same SwiGLU on Q(x), Q(Ws_gu), Q(Ws_down) with
+    its hidden quantised along its width, on real tokens.
     Returns (y [T][d], routed [T][k][d])."""
     x = mo._f64(x)
     xq = mx_roundtrip(x)
@@ -129,15 +132,16 @@ def experts_forward_mx(x, topk_idx, gates, W_gu, W_down, Ws_gu=None, Ws_down=Non
     if Ws_gu is not None:
         real = np.ones(x.shape[0], dtype=bool) if valid is None else (
             np.asarray(mo._np(valid)) != 0)
-        sg, su = mo.split_gu(mo._f64(Ws_gu))
-        shared, *_ = mo.swiglu_parts(x[real], sg, su, mo._f64(Ws_down))
+        sg, su = mo.split_gu(mx_roundtrip(mo._f64(Ws_gu)))
+        shared, *_ = mo.swiglu_parts(xq[real], sg, su, mx_roundtrip(mo._f64(Ws_down)),
+                                     rnd=mx_roundtrip)
         y[real] += shared
     return y, routed
 
 
 def forward_mx(x, Wr, W_gu, W_down, Ws_gu=None, Ws_down=None, k=2, bias=None,
                valid=None, norm_topk=True, logits=None):
-    """Whole layer with MXFP8 routed experts: the router and route of
+    """Whole layer with MXFP8 experts: the router and route of
     ``moe_oracle.forward`` (fp32 logits, unchanged), then the MX expert sum."""
     if logits is None:
         logits = mo.router_logits(x, Wr).astype(np.float32)

@@ -168,3 +168,18 @@ def test_mx_hidden_not_quantised_is_caught(monkeypatch):
     monkeypatch.setattr(O, "experts_forward",
                         lambda *a, rnd=None, **kw: orig(*a, **kw))
     assert _fails(PX.test_mx_experts_dense_masked_formulation)
+
+
+def test_mx_shared_expert_left_unquantised_is_caught(monkeypatch):
+    orig = M.experts_forward_mx
+
+    def shared_exact(x, topk_idx, gates, W_gu, W_down, Ws_gu=None, Ws_down=None, valid=None):
+        y, routed = orig(x, topk_idx, gates, W_gu, W_down, valid=valid)
+        if Ws_gu is not None:
+            sg, su = O.split_gu(np.asarray(Ws_gu, dtype=np.float64))
+            shared, *_ = O.swiglu_parts(np.asarray(x, dtype=np.float64), sg, su,
+                                        np.asarray(Ws_down, dtype=np.float64))
+            y = y + shared
+        return y, routed
+    monkeypatch.setattr(M, "experts_forward_mx", shared_exact)
+    assert _fails(PX.test_mx_experts_dense_masked_formulation)

@@ -4,7 +4,7 @@ brute force, round trips and an independent dense formulation.
 
 A plausible slip (exponent offset 7 instead of 8, ties to odd, no
 saturation, blocks along the wrong axis, a dropped h quantisation, the
-shared expert quantised) fails at least one of them.
+shared expert left unquantised) fails at least one of them.
 """
 import numpy as np
 import pytest
@@ -155,7 +155,8 @@ def _tiny(seed, T=24, d=64, E=4, k=2, H=64, shared=True):
 def test_mx_experts_dense_masked_formulation():
     """Independent formulation: every expert applied to every token on the
     quantised operands, y_t = sum_e [e selected] g_{t,e} F^mx_e(x_t) + the
-    exact shared FFN, written out with explicit quantise steps."""
+    shared FFN on quantised operands, written out with explicit quantise
+    steps."""
     x, W_gu, W_down, Ws_gu, Ws_down, r = _tiny(4)
     y, _ = M.experts_forward_mx(x, r["topk_idx"], r["gates"], W_gu, W_down, Ws_gu, Ws_down)
     T, d = x.shape
@@ -176,16 +177,19 @@ def test_mx_experts_dense_masked_formulation():
         out = hq @ Wdq.T
         w = ((r["topk_idx"] == e) * r["gates"]).sum(axis=1)
         ref += w[:, None] * out
-    a = x @ Ws_gu[:H].T
-    b = x @ Ws_gu[H:].T
-    ref += (a / (1.0 + np.exp(-a)) * b) @ Ws_down.T
+    sc, ss = M.mx_quantize(Ws_gu)
+    Wsq = M.mx_dequantize(sc, ss)
+    a = xq @ Wsq[:H].T
+    b = xq @ Wsq[H:].T
+    hs = M.mx_dequantize(*M.mx_quantize(a / (1.0 + np.exp(-a)) * b))
+    ref += hs @ M.mx_dequantize(*M.mx_quantize(Ws_down)).T
     np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-12)
 
 
 def test_mx_experts_close_to_exact_and_not_equal():
-    """MX quantisation moves the routed output by a few percent of its
-    scale (3 mantissa bits: at most 1/16 relative per element), never by
-    more, and does move it; the shared expert is not quantised."""
+    """MX quantisation moves the routed and the shared outputs by a few
+    percent of their scale (3 mantissa bits: at most 1/16 relative per
+    element), never by more, and does move them."""
     x, W_gu, W_down, Ws_gu, Ws_down, r = _tiny(5)
     y_mx, routed_mx = M.experts_forward_mx(x, r["topk_idx"], r["gates"], W_gu, W_down)
     y, routed = O.experts_forward(x, r["topk_idx"], r["gates"], W_gu, W_down)
@@ -193,7 +197,9 @@ def test_mx_experts_close_to_exact_and_not_equal():
     assert 1e-3 < rel < 0.2
     ys_mx, _ = M.experts_forward_mx(x, r["topk_idx"], r["gates"], W_gu, W_down, Ws_gu, Ws_down)
     ys, _ = O.experts_forward(x, r["topk_idx"], r["gates"], W_gu, W_down, Ws_gu, Ws_down)
-    np.testing.assert_allclose(ys_mx - y_mx, ys - y, rtol=1e-12, atol=1e-12)
+    shared_mx, shared = ys_mx - y_mx, ys - y
+    rel = np.abs(shared_mx - shared).max() / np.abs(shared).max()
+    assert 1e-3 < rel < 0.2
 
 
 def test_mx_experts_exact_on_representable_operands():
