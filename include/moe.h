@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 2
+#define MOE_ABI_VERSION 3
 #define MOE_ROW_ALIGN 128
 
 enum moe_status {
@@ -316,41 +316,55 @@ int moe_backward(const moe_config* cfg, const moe_tensors* t, const moe_grads* g
 
 /* ------------------------------------------------------------ MXFP8 experts */
 
-/* The routed experts in MXFP8 ("KohakUwULLM" README, Key features: e4m3
- * values with UE8M0 scales, one per 32 values, on the routed experts, with
- * fully fused MXFP8 expert kernels).  Forward only (inference).
+/* The experts in MXFP8 ("KohakUwULLM" README, Key features: e4m3 values with
+ * UE8M0 scales, one per 32 values, on the feed-forward pair and the routed
+ * experts, with fully fused MXFP8 expert kernels).  Forward only (inference).
+ * The routed experts and the shared expert (the dense feed-forward pair) run
+ * on MXFP8 operands; router, route and combine are the bf16 path's.
  *
  * Format.  A block is 32 consecutive values along the reduction axis of a
- * product (d for x and W_gu rows, H for h and W_down rows).  Its scale byte
- * is X + 127 with X = floor(log2 max|v|) - 8, clamped to >= -127 (all-zero
- * blocks: -127); each value is the e4m3 code of v / 2^X, rounded to nearest
- * even and saturated to +-448.  Codes keep the element order of the bf16
- * tensor they replace.  Scale bytes sit in 512-byte atoms, each covering 128
- * rows x 4 blocks (128 values along K): row r, block kb at byte
- * (r % 32) * 16 + (r / 32) * 4 + kb.
+ * product (d for x and the gate/up rows, H for h and the down rows).  Its
+ * scale byte is X + 127 with X = floor(log2 max|v|) - 8, clamped to >= -127
+ * (all-zero blocks: -127); each value is the e4m3 code of v / 2^X, rounded to
+ * nearest even and saturated to +-448.  Codes keep the element order of the
+ * bf16 tensor they replace.  Scale bytes sit in 512-byte atoms, each covering
+ * 128 rows x 4 blocks (128 values along K): row r, block kb at byte
+ * (r % 32) * 16 + (r / 32) * 4 + kb; atoms are indexed [128-row block][K/128].
  *
- * Shapes: d a multiple of 256 and H of 128, else MOE_ERR_SHAPE.  All buffers are
- * caller-owned device memory, 16-byte aligned, and the four code buffers and
- * t->out_perm 32-byte aligned (the kernels store 32 bytes per thread), else
- * MOE_ERR_ALIGN; moe_mx_sizes gives their sizes.  Router, route, combine and the shared expert are the bf16 path's. */
+ * Shapes: d a multiple of 256, H and n_shared * H_shared of 128, else
+ * MOE_ERR_SHAPE.  All buffers are caller-owned device memory, 16-byte aligned,
+ * and the code buffers and t->out_perm 32-byte aligned (the kernels store 32
+ * bytes per thread), else MOE_ERR_ALIGN; moe_mx_sizes gives their sizes. */
 typedef struct moe_mx_tensors {
-  uint8_t* W_gu_q;    /* [E][2H][d] codes of W_gu                               */
-  uint8_t* W_gu_s;    /* [E][2H/128][d/128] atoms (128-row blocks of W_gu[e])     */
-  uint8_t* W_down_q;  /* [E][d][H] codes of W_down                              */
-  uint8_t* W_down_s;  /* [E][d/128][H/128] atoms                                */
+  uint8_t* W_gu_q;    /* [E][2H][d] codes of W_gu                                */
+  uint8_t* W_gu_s;    /* [E][2H/128][d/128] atoms (128-row blocks of W_gu[e])    */
+  uint8_t* W_down_q;  /* [E][d][H] codes of W_down                               */
+  uint8_t* W_down_s;  /* [E][d/128][H/128] atoms                                 */
   uint8_t* x_q;       /* [R_cap][d] permuted x rows (pad rows zero)              */
   uint8_t* x_s;       /* [R_cap/128][d/128] atoms                                */
   uint8_t* h_q;       /* [R_cap][H] hidden rows                                  */
   uint8_t* h_s;       /* [R_cap/128][H/128] atoms                                */
+  /* the shared expert (n_shared > 0; Hs = n_shared * H_shared, Tp = T rounded
+     up to a multiple of 128); unused without a shared expert                */
+  uint8_t* Ws_gu_q;   /* [2Hs][d] codes of Ws_gu                                 */
+  uint8_t* Ws_gu_s;   /* [2Hs/128][d/128] atoms                                  */
+  uint8_t* Ws_down_q; /* [d][Hs] codes of Ws_down                                */
+  uint8_t* Ws_down_s; /* [d/128][Hs/128] atoms                                   */
+  uint8_t* xt_q;      /* [Tp][d] x in token order (PAD and padding rows zero)    */
+  uint8_t* xt_s;      /* [Tp/128][d/128] atoms                                   */
+  uint8_t* hs_q;      /* [Tp][Hs] the shared expert's hidden rows                */
+  uint8_t* hs_s;      /* [Tp/128][Hs/128] atoms                                  */
 } moe_mx_tensors;
 
-#define MOE_MX_FIELDS 8
+#define MOE_MX_FIELDS 16
 
-/* Bytes of each field of moe_mx_tensors, in field order, into bytes[8]. */
+/* Bytes of each field of moe_mx_tensors, in field order, into bytes[16]
+ * (the shared expert's eight are 0 without one). */
 int moe_mx_sizes(const moe_config* cfg, size_t* bytes);
 
-/* Weights -> MXFP8: in: t->W_gu, t->W_down (bf16).  out: W_gu_q, W_gu_s,
- * W_down_q, W_down_s.  Run once per weight update. */
+/* Weights -> MXFP8: in: t->W_gu, t->W_down (and Ws_gu, Ws_down with a shared
+ * expert), bf16.  out: W_gu_q, W_gu_s, W_down_q, W_down_s (and Ws_*_q, Ws_*_s).
+ * Run once per weight update. */
 int moe_mx_quantize_weights(const moe_config* cfg, const moe_tensors* t,
                             const moe_mx_tensors* mx, void* stream);
 
@@ -372,9 +386,17 @@ int moe_mx_expert_gate_up(const moe_config* cfg, const moe_tensors* t, const moe
 int moe_mx_expert_down(const moe_config* cfg, const moe_tensors* t, const moe_mx_tensors* mx,
                        void* workspace, size_t workspace_bytes, void* stream);
 
-/* The forward with MXFP8 routed experts: moe_router_route, moe_mx_permute,
- * moe_mx_expert_gate_up, moe_mx_expert_down, moe_shared_ffn_combine.  The
- * weights must have been quantised (moe_mx_quantize_weights). */
+/* a5 on MXFP8 operands: x quantised in token order (PAD tokens as zeros),
+ * the block-scaled gate/up GEMM with the SwiGLU and h quantiser, the
+ * block-scaled down GEMM -> s_out (fp32; 0 on PAD rows).  No-op without a
+ * shared expert.  in: x, valid, Ws_gu_q/s, Ws_down_q/s.
+ * out: xt_q/s, hs_q/s, s_out. */
+int moe_mx_shared_ffn(const moe_config* cfg, const moe_tensors* t, const moe_mx_tensors* mx,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* The forward with MXFP8 experts: moe_router_route, moe_mx_permute,
+ * moe_mx_expert_gate_up, moe_mx_expert_down, moe_mx_shared_ffn, moe_combine.
+ * The weights must have been quantised (moe_mx_quantize_weights). */
 int moe_mx_forward(const moe_config* cfg, const moe_tensors* t, const moe_mx_tensors* mx,
                    void* workspace, size_t workspace_bytes, void* stream);
 

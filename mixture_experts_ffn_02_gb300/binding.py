@@ -47,8 +47,9 @@ class MoEGrads(ctypes.Structure):
     _fields_ = [(n, c_void_p) for n in GRAD_FIELDS]
 
 
-MOE_MX_FIELDS = 8
-MX_FIELDS = ["W_gu_q", "W_gu_s", "W_down_q", "W_down_s", "x_q", "x_s", "h_q", "h_s"]
+MOE_MX_FIELDS = 16
+MX_FIELDS = ["W_gu_q", "W_gu_s", "W_down_q", "W_down_s", "x_q", "x_s", "h_q", "h_s",
+             "Ws_gu_q", "Ws_gu_s", "Ws_down_q", "Ws_down_s", "xt_q", "xt_s", "hs_q", "hs_s"]
 
 
 class MoEMxTensors(ctypes.Structure):
@@ -91,6 +92,7 @@ SIGNATURES = {
     "moe_mx_permute": (ctypes.c_int, _MX_STEP),
     "moe_mx_expert_gate_up": (ctypes.c_int, _MX_STEP),
     "moe_mx_expert_down": (ctypes.c_int, _MX_STEP),
+    "moe_mx_shared_ffn": (ctypes.c_int, _MX_STEP),
     "moe_mx_forward": (ctypes.c_int, _MX_STEP),
     "moe_route_partials": (ctypes.c_int, [ctypes.POINTER(MoEConfig), ctypes.POINTER(MoETensors),
                                           c_void_p, c_void_p]),
@@ -257,7 +259,7 @@ class Layer:
         sizes = (ctypes.c_size_t * len(MX_FIELDS))()
         check(self.lib.moe_mx_sizes(ctypes.byref(self.cfg), sizes), "moe_mx_sizes")
         dev = self.ws.device
-        self.mx = {n: torch.empty(max(int(sz), 16), dtype=torch.uint8, device=dev)
+        self.mx = {n: (torch.empty(int(sz), dtype=torch.uint8, device=dev) if sz else None)
                    for n, sz in zip(MX_FIELDS, sizes)}
         return self.mx
 
@@ -281,6 +283,7 @@ class Layer:
     def mx_permute(self): self._mx_step("moe_mx_permute")
     def mx_gate_up(self): self._mx_step("moe_mx_expert_gate_up")
     def mx_down(self): self._mx_step("moe_mx_expert_down")
+    def mx_shared(self): self._mx_step("moe_mx_shared_ffn")
     def mx_forward(self): self._mx_step("moe_mx_forward")
 
     def route_partials(self, sums):

@@ -449,7 +449,7 @@ bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) ==
   } while (0)
 
 int check_mx(const moe_config* c) {
-  if (c->d % 256 || c->H % 128) return MOE_ERR_SHAPE;
+  if (c->d % 256 || c->H % 128 || hs_total(*c) % 128) return MOE_ERR_SHAPE;
   return MOE_OK;
 }
 
@@ -463,6 +463,46 @@ void mx_sizes(const moe_config& c, size_t* b) {
   b[5] = (R / 128) * (d / 128) * 512;                    // x_s
   b[6] = R * H;                                          // h_q
   b[7] = (R / 128) * (H / 128) * 512;                    // h_s
+  const size_t Hs = (size_t)hs_total(c), Tp = ((size_t)c.T + 127) / 128 * 128;
+  b[8] = 2 * Hs * d;                                     // Ws_gu_q
+  b[9] = (2 * Hs / 128) * (d / 128) * 512;               // Ws_gu_s
+  b[10] = d * Hs;                                        // Ws_down_q
+  b[11] = (d / 128) * (Hs / 128) * 512;                  // Ws_down_s
+  b[12] = Hs ? Tp * d : 0;                               // xt_q
+  b[13] = Hs ? (Tp / 128) * (d / 128) * 512 : 0;         // xt_s
+  b[14] = Tp * Hs;                                       // hs_q
+  b[15] = (Tp / 128) * (Hs / 128) * 512;                 // hs_s
+}
+
+// The shared expert on MXFP8 operands: x quantised in token order (PAD and
+// the padding to 128 rows as zeros), then the two block-scaled GEMMs over
+// the dense token rows; s_out = 0 on PAD rows because their codes are 0.
+int do_mx_shared(const moe_config* c, const moe_tensors* t, const moe_mx_tensors* m, Call& k) {
+  const int Hs = hs_total(*c);
+  if (Hs == 0) return MOE_OK;
+  MOE_NEED(t->x); MOE_OPT(t->valid); MOE_NEED32(t->s_out);
+  MOE_NEED32(m->Ws_gu_q); MOE_NEED(m->Ws_gu_s); MOE_NEED32(m->Ws_down_q); MOE_NEED(m->Ws_down_s);
+  MOE_NEED32(m->xt_q); MOE_NEED(m->xt_s); MOE_NEED32(m->hs_q); MOE_NEED(m->hs_s);
+  const int Tp = (c->T + 127) / 128 * 128;
+  MOE_CUDA(launch_mx_quant_rows(t->x, m->xt_q, m->xt_s, Tp, c->T, c->d, Tp, t->valid, k.s));
+  MxGemmCall g{};
+  g.row_offsets = nullptr;
+  g.dense_rows = c->T;
+  g.E = 1;
+  g.rows = Tp;
+  g.d = c->d;
+  g.H = Hs;
+  g.status = k.status;
+  g.gate_up = 1;
+  g.A = m->xt_q; g.sfa = m->xt_s; g.B = m->Ws_gu_q; g.sfb = m->Ws_gu_s;
+  g.hq = m->hs_q; g.hs = m->hs_s;
+  MOE_CUDA(launch_mx_gemm(g, k.s));
+  g.gate_up = 0;
+  g.A = m->hs_q; g.sfa = m->hs_s; g.B = m->Ws_down_q; g.sfb = m->Ws_down_s;
+  g.hq = nullptr; g.hs = nullptr;
+  g.out = t->s_out;
+  MOE_CUDA(launch_mx_gemm(g, k.s));
+  return MOE_OK;
 }
 
 int do_mx_permute(const moe_config* c, const moe_tensors* t, const moe_mx_tensors* m, Call& k) {
@@ -615,9 +655,21 @@ int moe_mx_quantize_weights(const moe_config* cfg, const moe_tensors* t,
   MOE_NEED(t->W_gu); MOE_NEED(t->W_down);
   MOE_NEED32(mx->W_gu_q); MOE_NEED(mx->W_gu_s); MOE_NEED32(mx->W_down_q);
   MOE_NEED(mx->W_down_s);
-  MOE_CUDA(launch_mx_quant_weights(*cfg, t->W_gu, t->W_down, mx->W_gu_q, mx->W_gu_s,
-                                   mx->W_down_q, mx->W_down_s,
-                                   static_cast<cudaStream_t>(stream)));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const long long E = cfg->E, d = cfg->d, H = cfg->H, Hs = hs_total(*cfg);
+  MOE_CUDA(launch_mx_quant_rows(t->W_gu, mx->W_gu_q, mx->W_gu_s, E * 2 * H, E * 2 * H, (int)d,
+                                (int)(2 * H), nullptr, s));
+  MOE_CUDA(launch_mx_quant_rows(t->W_down, mx->W_down_q, mx->W_down_s, E * d, E * d, (int)H,
+                                (int)d, nullptr, s));
+  if (Hs > 0) {
+    MOE_NEED(t->Ws_gu); MOE_NEED(t->Ws_down);
+    MOE_NEED32(mx->Ws_gu_q); MOE_NEED(mx->Ws_gu_s); MOE_NEED32(mx->Ws_down_q);
+    MOE_NEED(mx->Ws_down_s);
+    MOE_CUDA(launch_mx_quant_rows(t->Ws_gu, mx->Ws_gu_q, mx->Ws_gu_s, 2 * Hs, 2 * Hs, (int)d,
+                                  (int)(2 * Hs), nullptr, s));
+    MOE_CUDA(launch_mx_quant_rows(t->Ws_down, mx->Ws_down_q, mx->Ws_down_s, d, d, (int)Hs,
+                                  (int)d, nullptr, s));
+  }
   return MOE_OK;
 }
 
@@ -636,12 +688,14 @@ int moe_mx_quantize_weights(const moe_config* cfg, const moe_tensors* t,
 MOE_MX_ENTRY(moe_mx_permute, { return do_mx_permute(cfg, t, mx, k); })
 MOE_MX_ENTRY(moe_mx_expert_gate_up, { return do_mx_gemm(cfg, t, mx, k, true); })
 MOE_MX_ENTRY(moe_mx_expert_down, { return do_mx_gemm(cfg, t, mx, k, false); })
+MOE_MX_ENTRY(moe_mx_shared_ffn, { return do_mx_shared(cfg, t, mx, k); })
 MOE_MX_ENTRY(moe_mx_forward, {
   if ((rc = do_router_route(cfg, t, k))) return rc;
   if ((rc = do_mx_permute(cfg, t, mx, k))) return rc;
   if ((rc = do_mx_gemm(cfg, t, mx, k, true))) return rc;
   if ((rc = do_mx_gemm(cfg, t, mx, k, false))) return rc;
-  return do_shared_combine(cfg, t, k);
+  if ((rc = do_mx_shared(cfg, t, mx, k))) return rc;
+  return do_combine(cfg, t, k);
 })
 
 int moe_route_partials(const moe_config* cfg, const moe_tensors* t, double* sums, void* stream) {

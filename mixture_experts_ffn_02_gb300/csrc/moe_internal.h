@@ -183,14 +183,18 @@ cudaError_t launch_permute_mx(const moe_config& c, const void* x, const int32_t*
                               int32_t* counts, int32_t* offsets, int32_t* row_offsets,
                               int32_t* perm, int32_t* inv, uint8_t* x_q, uint8_t* x_s,
                               char* ws, const WsLayout& w, cudaStream_t s);
-cudaError_t launch_mx_quant_weights(const moe_config& c, const void* W_gu, const void* W_down,
-                                    uint8_t* W_gu_q, uint8_t* W_gu_s, uint8_t* W_down_q,
-                                    uint8_t* W_down_s, cudaStream_t s);
+// Rows of a bf16 [rows][K] matrix -> codes [rows][K] and scale atoms per
+// 128-row block of each group of rows_per_group rows; rows past rows_real or
+// with valid == 0 (valid may be NULL) quantise as zeros.
+cudaError_t launch_mx_quant_rows(const void* W, uint8_t* Wq, uint8_t* Ws, long long rows,
+                                 long long rows_real, int K, int rows_per_group,
+                                 const uint8_t* valid, cudaStream_t s);
 struct MxGemmCall {
   int gate_up;                 // 1: h = silu(a) * b quantised; 0: out = h W_down^T (fp32)
-  const int32_t* row_offsets;  // [E+1] padded, device
+  const int32_t* row_offsets;  // [E+1] padded, device; NULL: dense rows
+  int dense_rows;              // dense: rows (the tile grid pads them to 128)
   int E;
-  int rows;                    // R_cap
+  int rows;                    // routed: R_cap; dense: rows of A's buffer (padded)
   int d, H;                    // d a multiple of 256, H of 128
   const uint8_t* A;            // x codes [rows][d] or h codes [rows][H]
   const uint8_t* sfa;          // their scale atoms

@@ -6,7 +6,8 @@
 // intermediates in 16-bit form.
 //
 // Here that is:
-//   * a weight quantiser (bf16 W_gu, W_down -> e4m3 codes + scale atoms);
+//   * a row quantiser (bf16 weights, or x in token order for the shared
+//     expert -> e4m3 codes + scale atoms);
 //   * the quantising permute (moe_dispatch.cu, perm_scatter_kernel<true>);
 //   * a persistent grouped GEMM on CTA pairs with tcgen05.mma.cta_group::2
 //     .kind::mxf8f6f4 and block scales.  A pair computes a 256 x 256 tile:
@@ -65,7 +66,10 @@ static_assert(XSF_COL + XSF_SLOT * XSTAGES <= XTMEM_COLS, "scale slots exceed TM
 enum MxKind { MXK_GATE_UP = 0, MXK_DOWN = 1 };
 
 struct XParams {
-  const int32_t* row_offsets;  // [E+1] padded segment offsets (multiples of 128)
+  const int32_t* row_offsets;  // [E+1] padded segment offsets (multiples of 128), or NULL:
+                               // dense rows (one group of dense_rows rows, E = 1)
+  int dense_rows;
+  int row_limit;               // rows at or past it are not stored
   int E;
   int H;                       // hidden size (gate/up: output units; down: K)
   int d;                       // model dim
@@ -171,7 +175,12 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     tma_prefetch_desc(&tmSA);
     tma_prefetch_desc(&tmSB);
   }
-  for (int e = threadIdx.x; e <= p.E; e += blockDim.x) sh.roff[e] = p.row_offsets[e];
+  if (p.row_offsets) {
+    for (int e = threadIdx.x; e <= p.E; e += blockDim.x) sh.roff[e] = p.row_offsets[e];
+  } else if (threadIdx.x == 0) {
+    sh.roff[0] = 0;
+    sh.roff[1] = (p.dense_rows + XBM - 1) / XBM * XBM;
+  }
   if (warp == 2) {
     tmem_alloc_pair(smem_u32(&sh.tmem_base), XTMEM_COLS);
     tmem_relinquish_pair();
@@ -310,6 +319,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const int blk = t.m0 + XBM * rank;            // this CTA's 128 rows
       const bool store = blk < t.row_end;           // else the pair's padding half
       const int row = blk + q * 32 + lane;
+      const bool row_ok = row < p.row_limit;
       // this warp's 128 accumulator columns into registers; gate/up: gate
       // columns half*64 .. +63 and the matching up columns 128 + half*64 ..
       uint32_t r[4][32];
@@ -334,16 +344,20 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           uint32_t cq[8];
           const uint32_t sbyte = mx_quant32(h, cq);
           const int col = t.n0 + half * 64 + c * 32;
-          st_v8(p.hq + (size_t)row * p.H + col, cq);
-          p.hs[((size_t)(row >> 7) * (p.H / 128) + (col >> 7)) * kMxAtom +
-               mx_sf_byte(row & 127, (col >> 5) & 3)] = (uint8_t)sbyte;
+          if (row_ok) {
+            st_v8(p.hq + (size_t)row * p.H + col, cq);
+            p.hs[((size_t)(row >> 7) * (p.H / 128) + (col >> 7)) * kMxAtom +
+                 mx_sf_byte(row & 127, (col >> 5) & 3)] = (uint8_t)sbyte;
+          }
         }
       } else {
         float* o = p.out + (size_t)row * p.d + t.n0 + half * 128;
+        if (row_ok) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+          for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int i = 0; i < 4; ++i) st_v8(o + 32 * c + 8 * i, &r[c][8 * i]);
+            for (int i = 0; i < 4; ++i) st_v8(o + 32 * c + 8 * i, &r[c][8 * i]);
+        }
       }
     }
   }
@@ -358,29 +372,36 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   }
 }
 
-// ------------------------------------------------------------------ weights
-// One thread per block of 32 along K of one weight row: codes stay in the
-// row's place ([rows][K]); the scale byte goes to the atom of the row's
-// 128-row block of its expert's matrix (W_gu [E][2H][d]: blocks of gate rows,
-// then of up rows; W_down [E][d][H]).
+// ------------------------------------------------------------------ rows
+// One thread per block of 32 along K of one row of a [rows][K] bf16 matrix:
+// codes stay in the row's place; the scale byte goes to the atom of the row's
+// 128-row block of its group (rows_per_group rows each: an expert's W_gu or
+// W_down, or all of x).  Rows at or past rows_real, and rows with valid == 0,
+// quantise as zeros (x's padding to 128 rows and its PAD tokens).
 __global__ void __launch_bounds__(256)
-mx_quant_weights_kernel(const bf16* __restrict__ W, uint8_t* __restrict__ Wq,
-                        uint8_t* __restrict__ Ws, long long rows, int K, int rows_per_e) {
-  const int nb = K / 32, kg = K / 128, nbt = rows_per_e / 128;
+mx_quant_rows_kernel(const bf16* __restrict__ W, uint8_t* __restrict__ Wq,
+                     uint8_t* __restrict__ Ws, long long rows, long long rows_real, int K,
+                     int rows_per_group, const uint8_t* __restrict__ valid) {
+  const int nb = K / 32, kg = K / 128, nbt = rows_per_group / 128;
   const long long total = rows * nb;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (long long)gridDim.x * blockDim.x) {
     const long long row = i / nb;
     const int b = (int)(i - row * nb);
-    const bf16* src = W + row * K + b * 32;
     float v[32];
+    if (row < rows_real && !(valid && valid[row] == 0)) {
+      const bf16* src = W + row * K + b * 32;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) unpack8(ld_nc_v4(src + u * 8), v + 8 * u);
+      for (int u = 0; u < 4; ++u) unpack8(ld_nc_v4(src + u * 8), v + 8 * u);
+    } else {
+#pragma unroll
+      for (int u = 0; u < 32; ++u) v[u] = 0.f;
+    }
     uint32_t cq[8];
     const uint32_t sbyte = mx_quant32(v, cq);
     st_v8(Wq + row * K + b * 32, cq);
-    const int e = (int)(row / rows_per_e);
-    const int n = (int)(row - (long long)e * rows_per_e);
+    const int e = (int)(row / rows_per_group);
+    const int n = (int)(row - (long long)e * rows_per_group);
     Ws[(((size_t)e * nbt + n / 128) * kg + (b >> 2)) * kMxAtom + mx_sf_byte(n % 128, b & 3)] =
         (uint8_t)sbyte;
   }
@@ -499,6 +520,8 @@ cudaError_t launch_mx_gemm(const MxGemmCall& g, cudaStream_t s) {
   if (device_info(&di) != MOE_OK) return cudaErrorUnknown;
   XParams p{};
   p.row_offsets = g.row_offsets;
+  p.dense_rows = g.dense_rows;
+  p.row_limit = g.row_offsets ? g.rows : g.dense_rows;
   p.E = g.E;
   p.H = g.H;
   p.d = g.d;
@@ -541,16 +564,13 @@ cudaError_t launch_mx_gemm(const MxGemmCall& g, cudaStream_t s) {
                    : x_launch<MXK_DOWN>(ta, tb, tsa, tsb, p, di.num_sms, s);
 }
 
-cudaError_t launch_mx_quant_weights(const moe_config& c, const void* W_gu, const void* W_down,
-                                    uint8_t* W_gu_q, uint8_t* W_gu_s, uint8_t* W_down_q,
-                                    uint8_t* W_down_s, cudaStream_t s) {
+cudaError_t launch_mx_quant_rows(const void* W, uint8_t* Wq, uint8_t* Ws, long long rows,
+                                 long long rows_real, int K, int rows_per_group,
+                                 const uint8_t* valid, cudaStream_t s) {
   DeviceInfo di;
   if (device_info(&di) != MOE_OK) return cudaErrorUnknown;
-  const int grid = di.num_sms * 8;
-  mx_quant_weights_kernel<<<grid, 256, 0, s>>>(static_cast<const bf16*>(W_gu), W_gu_q, W_gu_s,
-                                               (long long)c.E * 2 * c.H, c.d, 2 * c.H);
-  mx_quant_weights_kernel<<<grid, 256, 0, s>>>(static_cast<const bf16*>(W_down), W_down_q,
-                                               W_down_s, (long long)c.E * c.d, c.H, c.d);
+  mx_quant_rows_kernel<<<di.num_sms * 8, 256, 0, s>>>(static_cast<const bf16*>(W), Wq, Ws, rows,
+                                                      rows_real, K, rows_per_group, valid);
   return cudaGetLastError();
 }
 

@@ -39,7 +39,7 @@ def test_library_exports_every_declared_symbol(clib):
 
 
 def test_abi_version_and_messages(clib):
-    assert clib.moe_abi_version() == 2
+    assert clib.moe_abi_version() == 3
     for code in range(10):
         assert clib.moe_strerror(code)
     assert b"unknown" in clib.moe_strerror(99)
@@ -119,8 +119,14 @@ def test_mx_sizes_and_shape_rule(clib):
     R = ctypes.c_int64()
     assert clib.moe_row_capacity(ctypes.byref(c), ctypes.byref(R)) == 0
     E, d, H, R = s.E, s.d, s.H, R.value
+    Hs, Tp = s.n_shared * s.H_shared, (s.T + 127) // 128 * 128
     assert list(sizes) == [E * 2 * H * d, E * 2 * H * d // 32, E * d * H, E * d * H // 32,
-                           R * d, R * d // 32, R * H, R * H // 32]
+                           R * d, R * d // 32, R * H, R * H // 32,
+                           2 * Hs * d, 2 * Hs * d // 32, d * Hs, d * Hs // 32,
+                           Tp * d, Tp * d // 32, Tp * Hs, Tp * Hs // 32]
+    c5 = binding.config(synth.shape(5))              # no shared expert: its buffers are 0
+    assert clib.moe_mx_sizes(ctypes.byref(c5), sizes) == 0
+    assert list(sizes)[8:] == [0] * 8
     tiny = binding.config(synth.shape(1))
     assert clib.moe_mx_sizes(ctypes.byref(tiny), sizes) == 2
     t = binding.MoETensors()

@@ -138,6 +138,23 @@ def test_mx_quantisation_bit_exact(cfg, T, over):
     used[rows] = True
     pad = ~used[: roff[-1]]
     assert (xq[: roff[-1]][pad] == 0).all() and (xs[: roff[-1]][pad] == 0).all()
+    if s.n_shared:
+        # the shared expert's weights, and x in token order with PAD tokens and
+        # the padding to 128 rows as zeros
+        Hs, Tp = s.n_shared * s.H_shared, (s.T + 127) // 128 * 128
+        c, sc = M.mx_quantize(np64(inp["Ws_gu"]))
+        np.testing.assert_array_equal(u8(mx["Ws_gu_q"]).reshape(2 * Hs, d), c)
+        np.testing.assert_array_equal(unpack_rows(u8(mx["Ws_gu_s"]), d, 2 * Hs), sc)
+        c, sc = M.mx_quantize(np64(inp["Ws_down"]))
+        np.testing.assert_array_equal(u8(mx["Ws_down_q"]).reshape(d, Hs), c)
+        np.testing.assert_array_equal(unpack_rows(u8(mx["Ws_down_s"]), Hs, d), sc)
+        xv = np64(inp["x"])
+        if inp["valid"] is not None:
+            xv = np.where((inp["valid"].numpy() != 0)[:, None], xv, 0.0)
+        xv = np.concatenate([xv, np.zeros((Tp - s.T, d))])
+        c, sc = M.mx_quantize(xv)
+        np.testing.assert_array_equal(u8(mx["xt_q"]).reshape(Tp, d), c)
+        np.testing.assert_array_equal(unpack_rows(u8(mx["xt_s"]), d, Tp), sc)
 
 
 @pytest.mark.parametrize("cfg,T,over", SCALED)
@@ -250,3 +267,21 @@ def test_mx_rejects_code_buffers_off_32_bytes():
     lay.mx_forward()
     torch.cuda.synchronize()
     assert lay.status() == 0
+
+
+@pytest.mark.parametrize("cfg,T,over", [(2, 700, {}), (4, 900, dict(d=512, H=384, H_shared=384))])
+def test_mx_forward_equals_its_steps(cfg, T, over):
+    """moe_mx_forward is its steps in order: moe_mx_shared_ffn (s_out) then
+    moe_combine after the routed MX calls give the same y bit for bit."""
+    s = scaled_shape(cfg, T, over)
+    _, lay = mx_layer(s)
+    y_fwd = lay.bufs["y"].clone()
+    lay.router_route()
+    lay.mx_permute()
+    lay.mx_gate_up()
+    lay.mx_down()
+    lay.mx_shared()
+    lay.combine()
+    torch.cuda.synchronize()
+    assert lay.status() == 0
+    assert torch.equal(y_fwd, lay.bufs["y"])
