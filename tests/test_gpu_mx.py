@@ -285,3 +285,34 @@ def test_mx_forward_equals_its_steps(cfg, T, over):
     torch.cuda.synchronize()
     assert lay.status() == 0
     assert torch.equal(y_fwd, lay.bufs["y"])
+
+
+@pytest.mark.parametrize("cfg,n_tok", [(3, 48), (4, 4), (5, 6)])
+def test_mx_full_size_sampled(cfg, n_tok):
+    """The packed, 64-expert and 128-expert layers at their full sizes, in
+    the configuration bench.py times: y on a sample of tokens (the last one
+    and, for the packed batch, PAD tokens included) against the MX oracle
+    evaluated on those tokens with only the experts they chose, and the
+    codes of the first and last of those experts' weights bit for bit."""
+    s = synth.shape(cfg)
+    inp, lay = mx_layer(s)
+    rng = np.random.default_rng(11 + cfg)
+    rows = np.sort(rng.choice(s.T - 1, size=n_tok - 1, replace=False))
+    rows = np.append(rows, s.T - 1)
+    r, x, valid = route_like_gpu(s, inp, lay, rows)
+    np.testing.assert_array_equal(lay.bufs["topk_idx"].cpu().numpy()[rows], r["topk_idx"])
+    topk = r["topk_idx"]
+    used = np.unique(topk[topk >= 0])
+    topk_c = np.where(topk >= 0, np.searchsorted(used, np.maximum(topk, 0)), -1)
+    W_gu = inp["W_gu"][torch.from_numpy(used)]
+    W_down = inp["W_down"][torch.from_numpy(used)]
+    y_mx, _ = M.experts_forward_mx(x, topk_c, r["gates"], W_gu, W_down, inp["Ws_gu"],
+                                   inp["Ws_down"], valid)
+    chk = Checker()
+    chk.close("y_mx[sample]", lay.bufs["y"][rows], y_mx)
+    chk.done()
+    E, d, H = s.E, s.d, s.H
+    q_gpu = u8(lay.mx["W_gu_q"], E * 2 * H * d).reshape(E, 2 * H, d)
+    for j in (0, len(used) - 1):
+        c, _ = M.mx_quantize(np64(W_gu[j]))
+        np.testing.assert_array_equal(q_gpu[used[j]], c)
