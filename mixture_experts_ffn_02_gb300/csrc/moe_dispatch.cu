@@ -855,11 +855,22 @@ route_finalize_kernel(const double* __restrict__ sums, int E, int k, float* __re
 }
 
 // --------------------------------------------------------------------------
-// a2: stable counting-sort dispatch.
+// a2: stable counting-sort dispatch.  Its three kernels run back to back with
+// programmatic dependent launch: the histogram and the scan let their
+// successor launch while they still run (griddepcontrol.launch_dependents),
+// and the scan and the scatter wait for their predecessor's completion and
+// memory (griddepcontrol.wait) before they read its results, so the launch
+// latency of the two small kernels overlaps the work.
 // --------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __global__ void __launch_bounds__(kThreads)
 perm_hist_kernel(const int32_t* __restrict__ topk, int T, int k, int E,
                  int* __restrict__ hist, int* __restrict__ status) {
+  pdl_trigger();
   __shared__ int h[256];
   for (int e = threadIdx.x; e < E; e += blockDim.x) h[e] = 0;
   __syncthreads();
@@ -883,6 +894,8 @@ __global__ void __launch_bounds__(kScanThreads)
 perm_scan_kernel(const int* __restrict__ hist, int nblk, int E, int32_t* __restrict__ counts,
                  int32_t* __restrict__ offsets, int32_t* __restrict__ row_offsets,
                  int* __restrict__ base) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int part[kScanThreads];
   __shared__ int cnt_s[257];
   __shared__ int off_s[257];
@@ -946,6 +959,7 @@ perm_scatter_kernel(const bf16* __restrict__ x, const int32_t* __restrict__ topk
                     int32_t* __restrict__ perm, int32_t* __restrict__ inv,
                     bf16* __restrict__ x_perm, uint8_t* __restrict__ x_q,
                     uint8_t* __restrict__ x_s) {
+  pdl_wait();
   __shared__ int base_s[256];
   __shared__ int dest_s[kPermChunk * kMaxK];     // expert ids, then destination rows
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -1549,6 +1563,25 @@ cudaError_t launch_route_finalize(const moe_config& c, const double* sums, float
   return cudaGetLastError();
 }
 
+// A launch that may begin while the previous kernel on the stream still runs
+// (programmatic stream serialisation); the kernel waits for that kernel's
+// completion with griddepcontrol.wait before it reads the kernel's results.
+template <typename... K, typename... A>
+cudaError_t launch_pdl(void (*kern)(K...), dim3 grid, dim3 block, cudaStream_t s, A... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* topk,
                            int32_t* counts, int32_t* offsets, int32_t* row_offsets,
                            int32_t* perm, int32_t* inv, void* x_perm, char* ws,
@@ -1558,12 +1591,12 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* to
   int* status = reinterpret_cast<int*>(ws + w.status);
   const int nblk = w.perm_blocks;
   perm_hist_kernel<<<nblk, kThreads, 0, s>>>(topk, c.T, c.k, c.E, hist, status);
-  perm_scan_kernel<<<1, kScanThreads, 0, s>>>(hist, nblk, c.E, counts, offsets, row_offsets,
-                                              base);
-  perm_scatter_kernel<false><<<nblk, kScatterThreads, 0, s>>>(
-      static_cast<const bf16*>(x), topk, c.T, c.d, c.k, c.E, base, counts, row_offsets, perm,
-      inv, static_cast<bf16*>(x_perm), nullptr, nullptr);
-  return cudaGetLastError();
+  launch_pdl(perm_scan_kernel, dim3(1), dim3(kScanThreads), s, (const int*)hist, nblk, c.E,
+             counts, offsets, row_offsets, base);
+  return launch_pdl(perm_scatter_kernel<false>, dim3(nblk), dim3(kScatterThreads), s,
+                    static_cast<const bf16*>(x), topk, c.T, c.d, c.k, c.E, (const int*)base,
+                    (const int32_t*)counts, (const int32_t*)row_offsets, perm, inv,
+                    static_cast<bf16*>(x_perm), (uint8_t*)nullptr, (uint8_t*)nullptr);
 }
 
 cudaError_t launch_permute_mx(const moe_config& c, const void* x, const int32_t* topk,
@@ -1575,12 +1608,12 @@ cudaError_t launch_permute_mx(const moe_config& c, const void* x, const int32_t*
   int* status = reinterpret_cast<int*>(ws + w.status);
   const int nblk = w.perm_blocks;
   perm_hist_kernel<<<nblk, kThreads, 0, s>>>(topk, c.T, c.k, c.E, hist, status);
-  perm_scan_kernel<<<1, kScanThreads, 0, s>>>(hist, nblk, c.E, counts, offsets, row_offsets,
-                                              base);
-  perm_scatter_kernel<true><<<nblk, kScatterThreads, 0, s>>>(
-      static_cast<const bf16*>(x), topk, c.T, c.d, c.k, c.E, base, counts, row_offsets, perm,
-      inv, nullptr, x_q, x_s);
-  return cudaGetLastError();
+  launch_pdl(perm_scan_kernel, dim3(1), dim3(kScanThreads), s, (const int*)hist, nblk, c.E,
+             counts, offsets, row_offsets, base);
+  return launch_pdl(perm_scatter_kernel<true>, dim3(nblk), dim3(kScatterThreads), s,
+                    static_cast<const bf16*>(x), topk, c.T, c.d, c.k, c.E, (const int*)base,
+                    (const int32_t*)counts, (const int32_t*)row_offsets, perm, inv,
+                    (bf16*)nullptr, x_q, x_s);
 }
 
 cudaError_t launch_combine(const moe_config& c, const float* out_perm, const int32_t* inv,
