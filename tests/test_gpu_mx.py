@@ -316,3 +316,51 @@ def test_mx_full_size_sampled(cfg, n_tok):
     for j in (0, len(used) - 1):
         c, _ = M.mx_quantize(np64(W_gu[j]))
         np.testing.assert_array_equal(q_gpu[used[j]], c)
+
+
+def _mx_run(s, bias=None, valid=None):
+    inp = synth.make_inputs(s, seed=0, with_grad=False)
+    if bias is not None:
+        inp["bias"] = bias
+    if valid is not None:
+        inp["valid"] = valid
+    lay = Layer.create(s, training=False)
+    dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    lay.set_inputs(dev["x"], dev["Wr"], dev["W_gu"], dev["W_down"], dev["Ws_gu"],
+                   dev["Ws_down"], bias=dev["bias"], valid=dev["valid"])
+    lay.mx_alloc()
+    lay.mx_quantize_weights()
+    lay.mx_forward()
+    torch.cuda.synchronize()
+    assert lay.status() == 0
+    return inp, lay
+
+
+def test_mx_all_pad_batch():
+    """T_real = 0: no routed rows (the MX GEMMs get no tiles), the shared
+    expert sees zero codes, and y is exactly zero."""
+    s = synth.MoEShape("pad", T=300, d=256, E=4, k=2, H=128, n_shared=1, H_shared=128,
+                       T_real=0)
+    _, lay = _mx_run(s, valid=torch.zeros(300, dtype=torch.uint8))
+    assert int(lay.bufs["row_offsets"][-1]) == 0
+    assert not lay.bufs["y"].float().abs().max().item()
+
+
+@pytest.mark.parametrize("name,shape,bias", [
+    ("single_token", dict(T=1, d=256, E=8, k=2, H=384, n_shared=1, H_shared=128), None),
+    ("one_expert_full", dict(T=900, d=256, E=16, k=1, H=256, n_shared=0, H_shared=0),
+     [100.0] + [0.0] * 15),
+])
+def test_mx_edge_shapes(name, shape, bias):
+    """One token (one padded 128-row block per tensor), and every token on
+    one expert (one full segment, every other expert empty)."""
+    s = synth.MoEShape(name, **shape)
+    b = None if bias is None else torch.tensor(bias, dtype=torch.float32)
+    inp, lay = _mx_run(s, bias=b)
+    r, x, valid = route_like_gpu(s, inp, lay)
+    np.testing.assert_array_equal(lay.bufs["topk_idx"].cpu().numpy(), r["topk_idx"])
+    y_mx, _ = M.experts_forward_mx(x, r["topk_idx"], r["gates"], inp["W_gu"], inp["W_down"],
+                                   inp["Ws_gu"], inp["Ws_down"], valid)
+    chk = Checker()
+    chk.close("y_mx", lay.bufs["y"], y_mx)
+    chk.done()
