@@ -1,9 +1,9 @@
-// MXFP8 routed experts on the 5th-generation tensor cores (sm_103a).
+// MXFP8 experts on the 5th-generation tensor cores (sm_103a).
 //
 // "KohakUwULLM" README, Key features and Selected measurements: MXFP8 (e4m3
-// values, UE8M0 scales per 32 values) on the routed experts, with fully fused
-// expert kernels that never materialise the (tokens * top_k, hidden)
-// intermediates in 16-bit form.
+// values, UE8M0 scales per 32 values) on the feed-forward pair and the routed
+// experts, with fully fused expert kernels that never materialise the
+// (tokens * top_k, hidden) intermediates in 16-bit form.
 //
 // Here that is:
 //   * a row quantiser (bf16 weights, or x in token order for the shared
@@ -19,7 +19,9 @@
 //     four K = 32 MMAs per stage, each picking its K-block's scale byte by the
 //     scale-factor id;
 //   * epilogues: gate/up -> h = silu(a) * b quantised straight to MXFP8 (codes
-//     and scale atoms of h, no bf16 h); down -> out_perm fp32 for the combine.
+//     and scale atoms of h, no bf16 h); down -> out_perm (routed) or s_out
+//     (the shared expert, the same kernel over dense token rows), fp32, for
+//     the combine.
 // Per CTA: one 256-column accumulator (the scale slots of the six 34 KB
 // stages take TMEM columns 256-351, so a second accumulator does not fit);
 // the epilogue warps pull the accumulator into registers and release it
@@ -53,7 +55,7 @@ constexpr int XTHREADS = 384;               // warp 0 TMA, 1 MMA, 2 TMEM, 3 scan
 constexpr int XEPI0 = 4;
 constexpr int XEPI_WARPS = 8;
 constexpr int XTMEM_COLS = 512;
-constexpr int XSF_COL = XBN;                // stage s scales: columns 256 + 16 s (A), + 4 (B)
+constexpr int XSF_COL = XBN;                // stage s scales: columns 256 + 16 s (A), + 4, + 8 (B)
 constexpr int XSF_SLOT = 16;
 constexpr uint64_t XWAIT_NS = 2000000000ull;  // bounded waits give up after 2 s
 constexpr uint64_t XDRAIN_NS = 200000000ull;

@@ -1,9 +1,11 @@
 // Device helpers of the MXFP8 path (sm_103a): the e4m3 / UE8M0 block
-// quantiser, the layout of scale factors in memory, and inline-PTX wrappers
-// for the block-scaled tcgen05 MMA, tcgen05.cp and the untiled bulk copy.
+// quantiser, 32-byte stores, the layout of scale factors in memory, and
+// inline-PTX wrappers for the block-scaled tcgen05 MMA and tcgen05.cp on CTA
+// pairs.
 //
 // "KohakUwULLM" README, Key features: MXFP8 = e4m3 values with UE8M0 scales,
-// one scale per 32 consecutive values, on the routed experts.
+// one scale per 32 consecutive values, on the feed-forward pair and the
+// routed experts.
 #pragma once
 
 #include <cuda_fp8.h>
@@ -70,19 +72,6 @@ __host__ __device__ constexpr uint32_t umma_idesc_sfid(uint32_t idesc, uint32_t 
   return idesc | (id << 29) | (id << 4);
 }
 
-__device__ __forceinline__ void umma_mx(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
-                                        uint32_t idesc, uint32_t tsfa, uint32_t tsfb,
-                                        uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %6, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
-      " [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
-      :: "r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(tsfa), "r"(tsfb),
-         "r"(accumulate)
-      : "memory");
-}
-
 // CTA-pair form: issued by one thread of the even CTA; A rows 0-127 and D
 // lanes in the even CTA, rows 128-255 in the odd one, B columns split in
 // halves; each CTA reads its rows' A scales and the scales of all N columns
@@ -110,28 +99,13 @@ __device__ __forceinline__ uint64_t umma_desc_plain(uint32_t saddr, uint32_t lbo
   return d;
 }
 
-// One 512-byte scale atom (32 rows of 16 bytes, contiguous) from shared
-// memory into 4 TMEM columns of all 128 lanes, ordered before the MMAs the
-// same thread issues after it.
-__device__ __forceinline__ void tmem_cp_atom(uint32_t taddr, uint32_t saddr) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;"
-               :: "r"(taddr), "l"(umma_desc_plain(saddr, 128, 128)) : "memory");
-}
-
-// The pair form: issued by the even CTA, each CTA's atom (same shared
-// offset) into its own TMEM (same address).
+// One 512-byte scale atom (32 rows of 16 bytes, contiguous in shared memory)
+// into 4 TMEM columns of all 128 lanes; issued by the even CTA of a pair, it
+// copies each CTA's atom (same shared offset) into its own TMEM (same
+// address), ordered before the MMAs the same thread issues after it.
 __device__ __forceinline__ void tmem_cp_atom_pair(uint32_t taddr, uint32_t saddr) {
   asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;"
                :: "r"(taddr), "l"(umma_desc_plain(saddr, 128, 128)) : "memory");
-}
-
-// Untiled bulk copy global -> shared (16-byte aligned, size a multiple of 16),
-// completing on an mbarrier.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar) : "memory");
 }
 
 }  // namespace moe
