@@ -325,11 +325,11 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       // this warp's 128 accumulator columns into registers; gate/up: gate
       // columns half*64 .. +63 and the matching up columns 128 + half*64 ..
       uint32_t r[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int col = KIND == MXK_GATE_UP ? (c >> 1) * (XBN / 2) + half * 64 + (c & 1) * 32
-                                            : half * 128 + c * 32;
-        tmem_ld32(tacc + col, r[c]);
+      if (KIND == MXK_GATE_UP) {
+        tmem_ld64(tacc + half * 64, &r[0][0]);
+        tmem_ld64(tacc + XBN / 2 + half * 64, &r[2][0]);
+      } else {
+        tmem_ld128(tacc + half * 128, &r[0][0]);
       }
       tmem_ld_wait();
       tc_fence_before();
