@@ -396,6 +396,9 @@ int moe_mx_shared_ffn(const moe_config* cfg, const moe_tensors* t, const moe_mx_
 
 /* The forward with MXFP8 experts: moe_router_route, moe_mx_permute,
  * moe_mx_expert_gate_up, moe_mx_expert_down, moe_mx_shared_ffn, moe_combine.
+ * With a shared expert its permute also writes x's token-order codes
+ * (xt_q / xt_s), so x is read and quantised once and moe_mx_shared_ffn's own
+ * quantiser pass is skipped; y is the same as from the separate calls.
  * The weights must have been quantised (moe_mx_quantize_weights). */
 int moe_mx_forward(const moe_config* cfg, const moe_tensors* t, const moe_mx_tensors* mx,
                    void* workspace, size_t workspace_bytes, void* stream);

@@ -477,14 +477,18 @@ void mx_sizes(const moe_config& c, size_t* b) {
 // The shared expert on MXFP8 operands: x quantised in token order (PAD and
 // the padding to 128 rows as zeros), then the two block-scaled GEMMs over
 // the dense token rows; s_out = 0 on PAD rows because their codes are 0.
-int do_mx_shared(const moe_config* c, const moe_tensors* t, const moe_mx_tensors* m, Call& k) {
+// quantise_x: x's token-order codes are made here (moe_mx_shared_ffn), or
+// were written by the permute (moe_mx_forward).
+int do_mx_shared(const moe_config* c, const moe_tensors* t, const moe_mx_tensors* m, Call& k,
+                 bool quantise_x) {
   const int Hs = hs_total(*c);
   if (Hs == 0) return MOE_OK;
   MOE_NEED(t->x); MOE_OPT(t->valid); MOE_NEED32(t->s_out);
   MOE_NEED32(m->Ws_gu_q); MOE_NEED(m->Ws_gu_s); MOE_NEED32(m->Ws_down_q); MOE_NEED(m->Ws_down_s);
   MOE_NEED32(m->xt_q); MOE_NEED(m->xt_s); MOE_NEED32(m->hs_q); MOE_NEED(m->hs_s);
   const int Tp = (c->T + 127) / 128 * 128;
-  MOE_CUDA(launch_mx_quant_rows(t->x, m->xt_q, m->xt_s, Tp, c->T, c->d, Tp, t->valid, k.s));
+  if (quantise_x)
+    MOE_CUDA(launch_mx_quant_rows(t->x, m->xt_q, m->xt_s, Tp, c->T, c->d, Tp, t->valid, k.s));
   MxGemmCall g{};
   g.row_offsets = nullptr;
   g.dense_rows = c->T;
@@ -505,12 +509,19 @@ int do_mx_shared(const moe_config* c, const moe_tensors* t, const moe_mx_tensors
   return MOE_OK;
 }
 
-int do_mx_permute(const moe_config* c, const moe_tensors* t, const moe_mx_tensors* m, Call& k) {
+// with_xt: also write x's codes in token order for the shared expert
+// (moe_mx_forward with a shared expert), so x is read and quantised once.
+int do_mx_permute(const moe_config* c, const moe_tensors* t, const moe_mx_tensors* m, Call& k,
+                  bool with_xt) {
   MOE_NEED(t->x); MOE_NEED(t->topk_idx); MOE_NEED(t->counts); MOE_NEED(t->offsets);
   MOE_NEED(t->row_offsets); MOE_NEED(t->perm); MOE_NEED(t->inv);
   MOE_NEED32(m->x_q); MOE_NEED(m->x_s);
+  if (with_xt) {
+    MOE_NEED32(m->xt_q); MOE_NEED(m->xt_s);
+  }
   MOE_CUDA(launch_permute_mx(*c, t->x, t->topk_idx, t->counts, t->offsets, t->row_offsets,
-                             t->perm, t->inv, m->x_q, m->x_s, k.ws, k.w, k.s));
+                             t->perm, t->inv, m->x_q, m->x_s, with_xt ? m->xt_q : nullptr,
+                             with_xt ? m->xt_s : nullptr, k.ws, k.w, k.s));
   return MOE_OK;
 }
 
@@ -685,16 +696,17 @@ int moe_mx_quantize_weights(const moe_config* cfg, const moe_tensors* t,
     body                                                                                     \
   }
 
-MOE_MX_ENTRY(moe_mx_permute, { return do_mx_permute(cfg, t, mx, k); })
+MOE_MX_ENTRY(moe_mx_permute, { return do_mx_permute(cfg, t, mx, k, false); })
 MOE_MX_ENTRY(moe_mx_expert_gate_up, { return do_mx_gemm(cfg, t, mx, k, true); })
 MOE_MX_ENTRY(moe_mx_expert_down, { return do_mx_gemm(cfg, t, mx, k, false); })
-MOE_MX_ENTRY(moe_mx_shared_ffn, { return do_mx_shared(cfg, t, mx, k); })
+MOE_MX_ENTRY(moe_mx_shared_ffn, { return do_mx_shared(cfg, t, mx, k, true); })
 MOE_MX_ENTRY(moe_mx_forward, {
   if ((rc = do_router_route(cfg, t, k))) return rc;
-  if ((rc = do_mx_permute(cfg, t, mx, k))) return rc;
+  const bool shared = hs_total(*cfg) > 0;
+  if ((rc = do_mx_permute(cfg, t, mx, k, shared))) return rc;
   if ((rc = do_mx_gemm(cfg, t, mx, k, true))) return rc;
   if ((rc = do_mx_gemm(cfg, t, mx, k, false))) return rc;
-  if ((rc = do_mx_shared(cfg, t, mx, k))) return rc;
+  if ((rc = do_mx_shared(cfg, t, mx, k, false))) return rc;
   return do_combine(cfg, t, k);
 })
 

@@ -958,7 +958,8 @@ perm_scatter_kernel(const bf16* __restrict__ x, const int32_t* __restrict__ topk
                     const int32_t* __restrict__ counts, const int32_t* __restrict__ row_offsets,
                     int32_t* __restrict__ perm, int32_t* __restrict__ inv,
                     bf16* __restrict__ x_perm, uint8_t* __restrict__ x_q,
-                    uint8_t* __restrict__ x_s) {
+                    uint8_t* __restrict__ x_s, uint8_t* __restrict__ xt_q,
+                    uint8_t* __restrict__ xt_s, int Tp) {
   pdl_wait();
   __shared__ int base_s[256];
   __shared__ int dest_s[kPermChunk * kMaxK];     // expert ids, then destination rows
@@ -1010,6 +1011,16 @@ perm_scatter_kernel(const bf16* __restrict__ x, const int32_t* __restrict__ topk
       for (int u = 0; u < 4; ++u) unpack8(ld_nc_v4(src + b * 32 + u * 8), v + 8 * u);
       uint32_t q[8];
       const uint32_t sb = mx_quant32(v, q);
+      if (xt_q != nullptr) {
+        // the same codes in token order for the shared expert; PAD tokens
+        // (no destination row) as zeros
+        const int t = t_beg + tl;
+        const bool real = dst[0] >= 0;
+        const uint32_t zero[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        st_v8(xt_q + (size_t)t * d + b * 32, real ? q : zero);
+        xt_s[((size_t)(t >> 7) * kg + (b >> 2)) * kMxAtom + mx_sf_byte(t & 127, b & 3)] =
+            real ? (uint8_t)sb : (uint8_t)0;
+      }
       for (int j = 0; j < k; ++j) {
         const int r = dst[j];
         if (r < 0) continue;
@@ -1035,6 +1046,15 @@ perm_scatter_kernel(const bf16* __restrict__ x, const int32_t* __restrict__ topk
         for (int u = 0; u < U; ++u)
           if (c0 + u * 256 < d) st_v4(o + u * 256, v[u]);
       }
+    }
+  }
+  // the token-order copy's padding rows [T, Tp) as zeros (the last block)
+  if (MX && xt_q != nullptr && blockIdx.x == gridDim.x - 1) {
+    for (int r = T + warp; r < Tp; r += wpb) {
+      for (int c0 = lane * 16; c0 < d; c0 += 512)
+        st_v4(xt_q + (size_t)r * d + c0, make_uint4(0, 0, 0, 0));
+      for (int b = lane; b < nb32; b += 32)
+        xt_s[((size_t)(r >> 7) * kg + (b >> 2)) * kMxAtom + mx_sf_byte(r & 127, b & 3)] = 0;
     }
   }
   // zero pad rows
@@ -1596,13 +1616,15 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* to
   return launch_pdl(perm_scatter_kernel<false>, dim3(nblk), dim3(kScatterThreads), s,
                     static_cast<const bf16*>(x), topk, c.T, c.d, c.k, c.E, (const int*)base,
                     (const int32_t*)counts, (const int32_t*)row_offsets, perm, inv,
-                    static_cast<bf16*>(x_perm), (uint8_t*)nullptr, (uint8_t*)nullptr);
+                    static_cast<bf16*>(x_perm), (uint8_t*)nullptr, (uint8_t*)nullptr,
+                    (uint8_t*)nullptr, (uint8_t*)nullptr, 0);
 }
 
 cudaError_t launch_permute_mx(const moe_config& c, const void* x, const int32_t* topk,
                               int32_t* counts, int32_t* offsets, int32_t* row_offsets,
                               int32_t* perm, int32_t* inv, uint8_t* x_q, uint8_t* x_s,
-                              char* ws, const WsLayout& w, cudaStream_t s) {
+                              uint8_t* xt_q, uint8_t* xt_s, char* ws, const WsLayout& w,
+                              cudaStream_t s) {
   int* hist = reinterpret_cast<int*>(ws + w.perm_hist);
   int* base = reinterpret_cast<int*>(ws + w.perm_base);
   int* status = reinterpret_cast<int*>(ws + w.status);
@@ -1613,7 +1635,7 @@ cudaError_t launch_permute_mx(const moe_config& c, const void* x, const int32_t*
   return launch_pdl(perm_scatter_kernel<true>, dim3(nblk), dim3(kScatterThreads), s,
                     static_cast<const bf16*>(x), topk, c.T, c.d, c.k, c.E, (const int*)base,
                     (const int32_t*)counts, (const int32_t*)row_offsets, perm, inv,
-                    (bf16*)nullptr, x_q, x_s);
+                    (bf16*)nullptr, x_q, x_s, xt_q, xt_s, (c.T + 127) / 128 * 128);
 }
 
 cudaError_t launch_combine(const moe_config& c, const float* out_perm, const int32_t* inv,

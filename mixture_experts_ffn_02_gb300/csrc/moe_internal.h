@@ -178,11 +178,14 @@ cudaError_t launch_gemm(const GemmCall& g, cudaStream_t s);
 
 // ---- MXFP8 routed experts (moe_mx.cu) --------------------------------------
 // Quantising permute: offsets, perm, inv as launch_permute, and x rows as
-// e4m3 codes x_q [R_cap][d] with scale atoms x_s [R_cap/128][d/128][512].
+// e4m3 codes x_q [R_cap][d] with scale atoms x_s [R_cap/128][d/128][512];
+// with xt_q non-NULL also the same codes in token order (xt_q [Tp][d], xt_s;
+// PAD tokens and rows T..Tp-1 as zeros) for the shared expert.
 cudaError_t launch_permute_mx(const moe_config& c, const void* x, const int32_t* topk,
                               int32_t* counts, int32_t* offsets, int32_t* row_offsets,
                               int32_t* perm, int32_t* inv, uint8_t* x_q, uint8_t* x_s,
-                              char* ws, const WsLayout& w, cudaStream_t s);
+                              uint8_t* xt_q, uint8_t* xt_s, char* ws, const WsLayout& w,
+                              cudaStream_t s);
 // Rows of a bf16 [rows][K] matrix -> codes [rows][K] and scale atoms per
 // 128-row block of each group of rows_per_group rows; rows past rows_real or
 // with valid == 0 (valid may be NULL) quantise as zeros.
