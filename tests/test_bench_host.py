@@ -1,0 +1,52 @@
+"""CPU checks of bench.py's host arithmetic: the algorithmic flops and bytes
+that the roofline fractions divide by, against closed forms worked out by
+hand for the five workloads (no GPU)."""
+import pytest
+
+import bench
+from mixture_experts_ffn_02_gb300 import synth
+
+
+# forward flop = 2 per multiply-add x 3 products (gate, up, down) x d x
+# (k H per real token for the routed slots + n_s H_s for the shared expert),
+# expanded by hand for each workload
+FWD_FLOP = {
+    1: 2 * 256 * 3 * 64 * (2 * 128 + 1 * 128),          # tiny: 0.0377 GFLOP
+    2: 2 * 32768 * 3 * 1536 * (2 * 3072 + 1 * 3072),    # KochiLLM: 2783.1 GFLOP
+    3: 2 * 60293 * 3 * 512 * (2 * 768),                 # packed, real tokens: 284.5 GFLOP
+    4: 2 * 16384 * 3 * 2048 * (6 * 1408 + 2 * 1408),    # 64 experts top-6: 2267.7 GFLOP
+    5: 2 * 32768 * 3 * 1024 * (8 * 768),                # 128 experts top-8: 1237.0 GFLOP
+}
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
+def test_gemm_flops_closed_form(cfg):
+    s = synth.shape(cfg)
+    routed, shared = bench.gemm_flops(s)
+    Tr = s.T_real if s.T_real is not None else s.T
+    assert routed == 2 * Tr * s.k * 3 * s.d * s.H
+    assert shared == 2 * Tr * 3 * s.d * s.n_shared * s.H_shared
+    assert routed + shared == FWD_FLOP[cfg]
+
+
+def test_hbm_bytes_closed_forms():
+    """KochiLLM shape (T = 32768, d = 1536, k = 2, no PAD): the permute reads
+    x once (100.7 MB), writes 65536 rows of x_perm (201.3 MB) and moves
+    4 bytes per topk entry in, per perm entry and per inv entry out; the
+    packed shape counts real tokens only for the row traffic."""
+    s = synth.shape(2)
+    b = bench.hbm_bytes(s)
+    T, d, k = 32768, 1536, 2
+    assert b["permute"] == T * d * 2 + T * k * d * 2 + 3 * T * k * 4 == 302776320
+    assert b["router_route"] == T * d * 2 + d * 4 * 4 + T * 4 * 4 + T * k * 8
+    p = synth.shape(3)
+    bp = bench.hbm_bytes(p)
+    Tr, M = 60293, 60293 * 2
+    assert bp["permute"] == Tr * 512 * 2 + M * 512 * 2 + 65536 * 2 * 4 + M * 4 + 65536 * 2 * 4
+    # out_perm fp32 in, no shared expert, inv + gates in, y (bf16, all positions) out
+    assert bp["combine"] == M * 512 * 4 + 65536 * 2 * 8 + 65536 * 512 * 2
+
+
+def test_aggregate_single_rank():
+    ms, v = bench.aggregate_ranks(200.0, 32768, 5, 1)
+    assert ms == 200.0 and v == pytest.approx(32768 * 5 / 0.2)
