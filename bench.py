@@ -85,7 +85,7 @@ class Clocks:
             os.close(fd)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-i", str(self.gpu), "-lms", "200"],
+                 "-i", str(self.gpu), "-lms", "50"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -170,8 +170,8 @@ def run_ours(args):
     if s.Hs_total:
         del kev["combine"]
 
-    def timed(name, fn, record):
-        if not record:
+    def timed(name, fn):
+        if name not in kev:
             fn()
             return
         a = torch.cuda.Event(enable_timing=True)
@@ -182,16 +182,8 @@ def run_ours(args):
         kev[name].append((a, b))
 
     def step(record):
-        timed("router_route", lay.router_route, record)
-        timed("permute", lay.permute, record)
-        timed("gate_up", lay.gate_up, record)
-        lay.down()
-        if s.Hs_total:
-            lay.shared_combine()       # the combine runs in the shared expert's down GEMM
-        else:
-            timed("combine", lay.combine, record)
-        if training:
-            lay.backward(dY)
+        # with a shared expert the combine runs in its down GEMM (shared_combine)
+        lay.step(dY if training else None, timed if record else None)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -319,7 +311,17 @@ def run_ours(args):
 
     e2e = run_e2e(args, s, inp, lay, training, local)
 
-    bf16_burst, bf16_peak, hbm_peak, peak_src = peaks()
+    bf16_burst, bf16_sustained, hbm_peak, peak_src = peaks()
+    # the burst figure for a kernel timed in a short region; the sustained
+    # (power-capped) one only when the timed steps ran back to back for
+    # seconds, as the sustained figure was measured
+    timed_s = ms / 1e3
+    if timed_s >= 2.0:
+        bf16_peak = bf16_sustained
+        peak_label = f"{peak_src} sustained bf16 (timed region {timed_s:.2f} s >= 2 s)"
+    else:
+        bf16_peak = bf16_burst
+        peak_label = f"{peak_src} burst bf16 (timed region {timed_s:.2f} s < 2 s)"
     routed, shared = gemm_flops(s)
     gu_flops = routed * 2 / 3                                  # gate + up of the routed experts
     gu_tflops = gu_flops / (gu_ms / 1e3) / 1e12
@@ -329,7 +331,7 @@ def run_ours(args):
 
     mx_out = None
     if mx is not None:
-        f8_peak = 2 * bf16_peak          # nominal dense fp8 / bf16 tensor ratio (4.5 / 2.25)
+        f8_peak = 2 * bf16_sustained     # nominal dense fp8 / bf16 tensor ratio (4.5 / 2.25)
         mx_f_ms, mx_g_ms, mx_d_ms, mx_q_ms = mx
         g_tf = gu_flops / (mx_g_ms / 1e3) / 1e12
         d_tf = routed / 3 / (mx_d_ms / 1e3) / 1e12
@@ -376,13 +378,14 @@ def run_ours(args):
                                                 else round(fwd_infer_gather_rate, 1)),
         "fwd_inference_mxfp8": mx_out,
         "layer_tflops": round(layer_tflops, 1),
-        "layer_frac_of_bf16_peak": round(layer_tflops / bf16_peak, 4),
         "layer_frac_of_burst_peak": round(layer_tflops / bf16_burst, 4),
+        "layer_frac_of_sustained_peak": round(layer_tflops / bf16_sustained, 4),
         "roofline": {"kernel": "grouped gate/up GEMM + SwiGLU (tcgen05)", "bound": "tensor",
                      "achieved": round(gu_tflops, 1), "peak": bf16_peak, "unit": "TFLOP/s",
                      "frac": round(gu_tflops / bf16_peak, 4),
-                     "peak_source": f"{peak_src} sustained bf16 (timed inside a long step)",
+                     "peak_source": peak_label,
                      "frac_of_burst_peak": round(gu_tflops / bf16_burst, 4),
+                     "frac_of_sustained_peak": round(gu_tflops / bf16_sustained, 4),
                      "algorithmic_flops_per_launch": gu_flops,
                      "avg_launch_ms": round(gu_ms, 4), "traffic": traffic},
         "hbm_kernels": hbm_kernels(s, k_ms, hbm_peak),
@@ -545,12 +548,21 @@ def run_e2e(args, s, inp, lay, training, local):
             "ms_per_step": round(ms, 4)}
 
 
+_SAMPLE_INPUTS = {}
+
+
 def oracle_sample(s, n_tok, training):
-    """Time the CPU oracle on the first n_tok tokens of the workload."""
+    """Time the CPU oracle on the first n_tok tokens of the workload (the
+    seeded inputs are drawn once per sample size, outside the timing)."""
     from mixture_experts_ffn_02_gb300 import synth
     from oracle import moe_oracle as O
-    sub = synth.scaled(s, T=n_tok, T_real=None if s.T_real is None else min(n_tok, s.T_real))
-    inp = synth.make_inputs(sub, seed=0, with_grad=True)
+    key = (s.name, s.T, n_tok)
+    if key not in _SAMPLE_INPUTS:
+        _SAMPLE_INPUTS.clear()
+        sub = synth.scaled(s, T=n_tok, T_real=None if s.T_real is None
+                           else min(n_tok, s.T_real))
+        _SAMPLE_INPUTS[key] = synth.make_inputs(sub, seed=0, with_grad=True)
+    inp = _SAMPLE_INPUTS[key]
     t0 = time.perf_counter()
     fwd = O.forward(inp["x"], inp["Wr"], inp["W_gu"], inp["W_down"], inp["Ws_gu"],
                     inp["Ws_down"], k=s.k, bias=inp["bias"], valid=inp["valid"],
@@ -573,18 +585,52 @@ def blas_threads():
     return os.cpu_count() or 1
 
 
-def cpu_baseline(args, s, budget_s=12.0):
-    training = not args.fwd_only
-    n = 64
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or None."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return None
+
+
+def oracle_sample_tokens(s, training, target_s=3.0):
+    """Tokens per oracle sample: doubled from 512 until one sample takes at
+    least target_s (so the oracle's fixed per-call cost -- widening the
+    weights to fp64 -- is amortised as it is on a full batch).  Returns
+    (tokens, seconds of the last sample)."""
+    n = min(512, s.T)
     dt = oracle_sample(s, n, training)
-    # grow the sample until it takes about budget_s of CPU time
-    while dt < budget_s / 2 and n < s.T:
+    while dt < target_s and n < s.T:
         n = min(s.T, n * 2)
         dt = oracle_sample(s, n, training)
-    return {"value": round(n / dt, 2), "unit": "tokens/s", "cores": blas_threads(),
-            "kind": "oracle",
+    return n, dt
+
+
+def host_desc():
+    return {"nproc": os.cpu_count(), "cpu_model": cpu_model()}
+
+
+def cpu_baseline(args, s, repeats=3):
+    """The oracle as it stands on the host cores: the same sample size as
+    the reference arm (oracle_sample_tokens), timed `repeats` times (about
+    10-20 s of CPU work in all)."""
+    training = not args.fwd_only
+    n, _ = oracle_sample_tokens(s, training)
+    t = sum(oracle_sample(s, n, training) for _ in range(repeats))
+    return {"value": round(n * repeats / t, 2), "unit": "tokens/s", "cores": blas_threads(),
+            "kind": "oracle", **host_desc(),
             "sample": f"first {n} of {s.T} tokens, same shapes, numpy fp64 "
-                      f"{'fwd+bwd' if training else 'fwd'}; {dt:.1f} s"}
+                      f"{'fwd+bwd' if training else 'fwd'}; {repeats} runs, {t:.1f} s"}
 
 
 def run_reference(args):
@@ -594,25 +640,22 @@ def run_reference(args):
         return
     s = workload_shape(args)
     training = not args.fwd_only
-    n = 256 if s.d * s.H <= 4e6 else 64
+    # the same sample size as the cpu_baseline leg, so both report one rate
+    n, _ = oracle_sample_tokens(s, training)
     for _ in range(args.warmup):
         oracle_sample(s, n, training)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        oracle_sample(s, n, training)
-    dt = time.perf_counter() - t0
+    dt = sum(oracle_sample(s, n, training) for _ in range(args.steps))
     v = n * args.steps / dt
+    sample = f"first {n} of {s.T} tokens per step, same shapes, numpy fp64"
     out = {"impl": "reference", "metric": METRIC, "value": round(v, 2), "unit": "tokens/s",
            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": round(dt / args.steps * 1e3, 2), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
            "config": {"workload": WORKLOAD_NAMES[args.config] + (" fwd" if args.fwd_only
                                                                   else " fwd+bwd"),
-                      "config_id": args.config,
-                      "sample": f"{n} tokens of the workload per step"},
+                      "config_id": args.config, "sample": sample},
            "cpu_baseline": {"value": round(v, 2), "unit": "tokens/s", "cores": blas_threads(),
-                            "kind": "oracle",
-                            "sample": f"{n} tokens per step, numpy fp64"},
+                            "kind": "oracle", **host_desc(), "sample": sample},
            "e2e": {"value": round(v, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)

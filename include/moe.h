@@ -32,6 +32,10 @@
  *     H % 64 == 0, 1 <= k <= min(E, 32), E <= 256, n_shared >= 0,
  *     H_shared % 64 == 0
  *     when n_shared > 0, T*k < 2^31, and every row count below < 2^31.
+ *     The 64-multiples come from the GEMM tiling: one K step is 64 bf16
+ *     values (one 128-byte swizzled row), and the gate/up epilogue writes
+ *     hidden units in 64-wide halves, whose a|b copies would otherwise run
+ *     into the neighbouring half of the ab row.
  *
  * Symbols: T positions (real + PAD), d model dim, E routed experts, k experts
  * per token, H routed expert hidden, Hs = n_shared * H_shared shared hidden,
@@ -55,7 +59,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 3
+#define MOE_ABI_VERSION 4
 #define MOE_ROW_ALIGN 128
 
 enum moe_status {
@@ -219,7 +223,12 @@ int moe_route(const moe_config* cfg, const moe_tensors* t,
 int moe_router_route(const moe_config* cfg, const moe_tensors* t,
                      void* workspace, size_t workspace_bytes, void* stream);
 
-/* a2. Stable counting-sort dispatch into expert-contiguous padded rows.
+/* a2. Stable counting-sort dispatch into expert-contiguous padded rows: the
+ * layout a grouped GEMM over the experts needs ("spark-gpt" README, feature
+ * list: BF16 grouped GEMM over packed SwiGLU experts; Hard-won facts: the
+ * experts run on grouped GEMMs, not a per-expert loop).  Pair (t, j) with
+ * t*k + j as the sort key goes to expert topk_idx[t][j]'s segment, tokens in
+ * ascending order within it.
  * in: x, topk_idx.  out: counts, offsets, row_offsets, perm, inv, x_perm.
  * x_perm may be NULL: then no rows are copied, and moe_expert_gate_up (with
  * x_perm NULL too) gathers the rows from x through perm instead.  The
@@ -242,7 +251,11 @@ int moe_permute(const moe_config* cfg, const moe_tensors* t,
 int moe_expert_gate_up(const moe_config* cfg, const moe_tensors* t,
                        void* workspace, size_t workspace_bytes, void* stream);
 
-/* a4. Grouped down GEMM: out_perm[r] = h[r] W_down[e]^T.
+/* a4. Grouped down GEMM: out_perm[r] = h[r] W_down[e]^T (tcgen05, bf16 in,
+ * fp32 accumulate, fp32 out).  The down projection of each SwiGLU expert
+ * ("KochiLLM v1.0" card, Configuration: SwiGLU experts, hidden 2 x dim), run
+ * as one grouped GEMM over all experts' segments ("spark-gpt" README,
+ * Hard-won facts: the MoE experts run on hand-written grouped GEMMs).
  * in: h, row_offsets, W_down.  out: out_perm. */
 int moe_expert_down(const moe_config* cfg, const moe_tensors* t,
                     void* workspace, size_t workspace_bytes, void* stream);
@@ -255,6 +268,9 @@ int moe_shared_ffn(const moe_config* cfg, const moe_tensors* t,
 
 /* a6. Weighted un-permute: y[t] = sum_j gates[t][j] out_perm[inv[t,j]]
  * (+ s_out[t]), fp32 sum in slot order, one rounding to bf16; PAD rows 0.
+ * The MoE FFN's output: the shared expert on every token plus the selected
+ * routed experts weighted by their renormalised gates ("KochiLLM v1.0" card,
+ * Architecture). 
  * in: out_perm, inv, gates, valid, s_out (if n_shared > 0).  out: y. */
 int moe_combine(const moe_config* cfg, const moe_tensors* t,
                 void* workspace, size_t workspace_bytes, void* stream);
@@ -270,6 +286,19 @@ int moe_combine(const moe_config* cfg, const moe_tensors* t,
  * inv, gates.  out: s_h, s_ab (if non-NULL), y. */
 int moe_shared_ffn_combine(const moe_config* cfg, const moe_tensors* t,
                            void* workspace, size_t workspace_bytes, void* stream);
+
+/* a3 + a4 + a5: the experts in one call -- moe_expert_gate_up,
+ * moe_expert_down, then moe_shared_ffn (no-op without a shared expert), in
+ * that order on `stream`.  The experts of the MoE FFN: SwiGLU experts
+ * ("KochiLLM v1.0" card, Configuration), routed ones on their tokens' rows
+ * and the shared one on every token (Architecture), as grouped GEMMs with the
+ * SwiGLU in the gate/up epilogue ("spark-gpt" README, Hard-won facts).
+ * in: x_perm (or x and perm, see moe_expert_gate_up), row_offsets, W_gu,
+ * W_down, and with a shared expert x, valid, Ws_gu, Ws_down.
+ * out: h, ab (if non-NULL), out_perm, and with a shared expert s_h, s_out,
+ * s_ab (if non-NULL).  moe_combine then forms y. */
+int moe_expert_ffn(const moe_config* cfg, const moe_tensors* t,
+                   void* workspace, size_t workspace_bytes, void* stream);
 
 /* a0..a6 in order on one stream (a0 + a1 as moe_router_route, a5 + a6 as
  * moe_shared_ffn_combine). */
@@ -303,6 +332,11 @@ int moe_route_finalize(const moe_config* cfg, const moe_tensors* t, const double
 
 /* a7. Gradients of J = <dY, y> + aux_coef * aux + z_coef * z_loss with the
  * hard counts (f) held constant; the selection bias receives no gradient.
+ * The training objective of the layer: the loss adds 0.01 x (E x sum_i f_i
+ * p_i) for load balancing ("KochiLLM v1.0" card, Architecture), p being the
+ * differentiable proxy and the hard counts f not differentiated ("spark-gpt"
+ * README, compute-matched MoE paragraph); the router z-loss ("KohakUwULLM"
+ * README, Key features) enters through z_coef.
  * Reads every forward tensor of `t` written by moe_forward (x, Wr, valid,
  * weights, logits, topk_idx, gates, counts, f, row_offsets, inv, x_perm, ab,
  * h, out_perm, s_ab, s_h); ab and (if n_shared > 0) s_ab must have been saved.
@@ -427,7 +461,8 @@ int moe_mx_forward(const moe_config* cfg, const moe_tensors* t, const moe_mx_ten
  * configuration fits (MOE_ERR_WORKSPACE is kept as a guard).
  * Set-up: the first call on each device resolves the array's device address
  * (a runtime symbol query, no allocation); make that first call before any
- * stream capture.  The call itself allocates nothing: no cudaMalloc, no
+ * stream capture.  If that query fails the call returns MOE_ERR_CUDA and
+ * nothing is cached: the next call on the device queries again.  The call itself allocates nothing: no cudaMalloc, no
  * cudaFree, no allocating library routine.
  * Sharing: all calls on a GPU use the same array, which keeps the last call's
  * contents; the ticket counter that must start at zero is cleared at the

@@ -79,6 +79,7 @@ SIGNATURES = {
     "moe_shared_ffn": (ctypes.c_int, _STEP),
     "moe_combine": (ctypes.c_int, _STEP),
     "moe_shared_ffn_combine": (ctypes.c_int, _STEP),
+    "moe_expert_ffn": (ctypes.c_int, _STEP),
     "moe_forward": (ctypes.c_int, _STEP),
     "moe_backward": (ctypes.c_int, [ctypes.POINTER(MoEConfig), ctypes.POINTER(MoETensors),
                                     ctypes.POINTER(MoEGrads), c_void_p, ctypes.c_size_t,
@@ -243,7 +244,29 @@ class Layer:
     def shared(self): self._step("moe_shared_ffn")
     def combine(self): self._step("moe_combine")
     def shared_combine(self): self._step("moe_shared_ffn_combine")
+    def expert_ffn(self): self._step("moe_expert_ffn")
     def forward(self): self._step("moe_forward")
+
+    def step(self, dY=None, timed=None):
+        """One pass of the layer, call by call: moe_router_route, moe_permute,
+        moe_expert_gate_up, moe_expert_down, moe_shared_ffn_combine (the
+        combine in the shared expert's down GEMM, or the combine kernel when
+        there is no shared expert), then moe_backward if dY is given.  The
+        same kernels in the same order as moe_forward + moe_backward.
+        ``timed(name, fn)``, if given, runs each call (to bracket it with
+        events); names: router_route, permute, gate_up, down, combine
+        (shared_combine with a shared expert), backward."""
+        run = timed or (lambda name, fn: fn())
+        run("router_route", self.router_route)
+        run("permute", self.permute)
+        run("gate_up", self.gate_up)
+        run("down", self.down)
+        if self.cfg.n_shared > 0:
+            run("shared_combine", self.shared_combine)
+        else:
+            run("combine", self.combine)
+        if dY is not None:
+            run("backward", lambda: self.backward(dY))
 
     def backward(self, dY):
         t = self.tensors()

@@ -639,6 +639,11 @@ MOE_ENTRY(moe_expert_down, 0, { return do_down(cfg, t, k); })
 MOE_ENTRY(moe_shared_ffn, 0, { return do_shared(cfg, t, k); })
 MOE_ENTRY(moe_combine, 0, { return do_combine(cfg, t, k); })
 MOE_ENTRY(moe_shared_ffn_combine, 0, { return do_shared_combine(cfg, t, k); })
+MOE_ENTRY(moe_expert_ffn, 0, {
+  if ((rc = do_gate_up(cfg, t, k))) return rc;
+  if ((rc = do_down(cfg, t, k))) return rc;
+  return do_shared(cfg, t, k);
+})
 MOE_ENTRY(moe_forward, 0, {
   if ((rc = do_router_route(cfg, t, k))) return rc;
   if ((rc = do_permute(cfg, t, k))) return rc;

@@ -32,24 +32,26 @@ constexpr size_t kStaticScratch = MOE_ROUTE_STATIC_SCRATCH_BYTES;
 // cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_route_scratch[kStaticScratch];
 
-struct ScratchAddr {
-  std::once_flag once;
-  cudaError_t err = cudaSuccess;
-  void* ptr = nullptr;
-};
-ScratchAddr g_addr[64];
+// Device address of the scratch per device, cached once found.  A failed
+// lookup is not cached: the next call on that device tries again.
+std::mutex g_addr_mu;
+void* g_addr[64] = {};
 
-// Device address of the scratch on the current device, resolved once per
-// device (with that device current).  No allocation happens here.
+// Device address of the scratch on the current device (with that device
+// current).  No allocation happens here.
 int scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
-  ScratchAddr& a = g_addr[dev];
-  std::call_once(a.once, [&a] {
-    a.err = cudaGetSymbolAddress(&a.ptr, g_route_scratch);
-  });
-  if (a.err != cudaSuccess || a.ptr == nullptr) return MOE_ERR_CUDA;
-  *out = a.ptr;
+  std::lock_guard<std::mutex> lock(g_addr_mu);
+  if (g_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();          // clear the error the failed query recorded
+      return MOE_ERR_CUDA;
+    }
+    g_addr[dev] = p;
+  }
+  *out = g_addr[dev];
   return MOE_OK;
 }
 

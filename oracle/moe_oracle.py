@@ -234,6 +234,24 @@ def swiglu_backward(dh, a, b):
     return dh * b * sa * (1.0 + a * (1.0 - sa)), dh * silu(a)
 
 
+def stored_d_out(g, dY, rnd=None):
+    """d_out = g dY per routed row, as kept between the combine backward and
+    the expert products: one storage rounding ``rnd`` of the product (none by
+    default)."""
+    rnd = rnd or _exact
+    return rnd(g[:, None] * dY)
+
+
+def stored_swiglu_backward(dh, a, b, rnd=None):
+    """(da, db) as kept for the dX and dW products: the chain rule of
+    :func:`swiglu_backward` taken on the stored pre-activations rnd(a) and
+    rnd(b), and each result stored once more (rnd).  dh itself is not stored:
+    it is the dH product's unrounded result."""
+    rnd = rnd or _exact
+    da, db = swiglu_backward(dh, rnd(a), rnd(b))
+    return rnd(da), rnd(db)
+
+
 def split_gu(W_gu):
     """[.., 2H, d] packed gate/up -> (gate [.., H, d], up [.., H, d])."""
     H = W_gu.shape[-2] // 2
@@ -357,9 +375,12 @@ def backward(x, Wr, W_gu, W_down, Ws_gu, Ws_down, fwd, dY, norm_topk=True,
     dWs_gu, dWs_down (or None), d_logits [T][E], dg [T][k].
 
     ``rnd`` (default: none) rounds the values a bf16-storage implementation
-    keeps between its matrix products -- the hidden h, the saved
-    pre-activations a and b, d_out = g dY, and (da, db) -- without changing
-    any arithmetic step.  With ``rnd`` None this is the exact gradient.
+    keeps between its matrix products -- the hidden h (:func:`swiglu_parts`),
+    d_out = g dY of the routed rows (:func:`stored_d_out`), the saved
+    pre-activations a and b and the results (da, db) of the SwiGLU chain rule
+    (:func:`stored_swiglu_backward`) -- without changing any arithmetic step.
+    The shared expert's d_out is dY itself (an input, not rounded again).
+    With ``rnd`` None this is the exact gradient.
     """
     rnd = rnd or _exact
     x = _f64(x); Wr = _f64(Wr); W_gu = _f64(W_gu); W_down = _f64(W_down)
@@ -375,10 +396,6 @@ def backward(x, Wr, W_gu, W_down, Ws_gu, Ws_down, fwd, dY, norm_topk=True,
     dW_down = np.zeros_like(W_down)
     dg = np.zeros((T, k))
 
-    def swiglu_bwd(dh, a, b):
-        da, db = swiglu_backward(dh, rnd(a), rnd(b))
-        return rnd(da), rnd(db)
-
     for j in range(k):
         for e in range(E):
             rows = np.nonzero(idx[:, j] == e)[0]
@@ -387,8 +404,8 @@ def backward(x, Wr, W_gu, W_down, Ws_gu, Ws_down, fwd, dY, norm_topk=True,
             xr = x[rows]
             out, a, b, h = swiglu_parts(xr, Wg[e], Wu[e], W_down[e], rnd)
             dg[rows, j] = (dY[rows] * out).sum(axis=1)
-            d_out = rnd(g[rows, j][:, None] * dY[rows])
-            da, db = swiglu_bwd(d_out @ W_down[e], a, b)
+            d_out = stored_d_out(g[rows, j], dY[rows], rnd)
+            da, db = stored_swiglu_backward(d_out @ W_down[e], a, b, rnd)
             dx[rows] += da @ Wg[e] + db @ Wu[e]
             dW_down[e] += d_out.T @ h
             dW_gu[e, :H] += da.T @ xr
@@ -400,7 +417,7 @@ def backward(x, Wr, W_gu, W_down, Ws_gu, Ws_down, fwd, dY, norm_topk=True,
         rows = np.nonzero(real)[0]
         xr = x[rows]
         out, a, b, h = swiglu_parts(xr, sg, su, Ws_down_, rnd)
-        da, db = swiglu_bwd(dY[rows] @ Ws_down_, a, b)
+        da, db = stored_swiglu_backward(dY[rows] @ Ws_down_, a, b, rnd)
         dx[rows] += da @ sg + db @ su
         Hs = sg.shape[0]
         dWs_gu = np.zeros_like(Ws_gu_)

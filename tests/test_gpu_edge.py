@@ -52,13 +52,12 @@ def _check_against_oracle(s, inp, lay):
     idl = O.backward(*bargs, norm_topk=bool(s.norm_topk), aux_coef=s.aux_coef, rnd=bf16_round)
     chk = Checker()
     if np.any(y):
-        chk.close("y", lay.bufs["y"], y)
-        chk.close2("y", lay.bufs["y"], y, yi)
+        chk.layer("y", lay.bufs["y"], y, yi)
     names = ["d_logits", "dW_down", "dW_gu", "dx", "dWr"] + (
         ["dWs_down", "dWs_gu"] if s.n_shared else [])
     for n in names:
         if np.any(ex[n]):
-            chk.close2(n, lay.grads[n], ex[n], idl[n])
+            chk.layer(n, lay.grads[n], ex[n], idl[n])
         else:
             assert not lay.grads[n].float().abs().max().item(), n
     chk.done()

@@ -81,7 +81,7 @@ def test_expert_gemms_and_combine(name, T, d, E, k, H, ns, Hs, pad, skew, pairs,
     chk.close("h", bufs["h"][:R], h_ref)
     chk.close("a", bufs["ab"][:R, :H], a_ref)
     chk.close("b", bufs["ab"][:R, H:], b_ref)
-    chk.close2("out_perm", bufs["out_perm"][:R], o_ref, o_ideal)
+    chk.layer("out_perm", bufs["out_perm"][:R], o_ref, o_ideal)
     pad_rows = torch.from_numpy(perm_padded < 0)
     assert (bufs["h"][:R].cpu()[pad_rows].float() == 0).all()
     assert (bufs["out_perm"][:R].cpu()[pad_rows].float() == 0).all()
@@ -99,9 +99,8 @@ def test_expert_gemms_and_combine(name, T, d, E, k, H, ns, Hs, pad, skew, pairs,
         if valid is not None:
             s_ref[vnp == 0] = 0
             s_ideal[vnp == 0] = 0
-        chk.close2("s_out", bufs["s_out"], s_ref, s_ideal)
-    chk.close("y", bufs["y"], y_ref)
-    chk.close2("y", bufs["y"], y_ref, y_ideal)
+        chk.layer("s_out", bufs["s_out"], s_ref, s_ideal)
+    chk.layer("y", bufs["y"], y_ref, y_ideal)
     chk.done()
     if valid is not None:
         assert (bufs["y"].cpu()[valid == 0].float() == 0).all()
@@ -118,3 +117,42 @@ def test_gate_up_repeatable():
     lay.gate_up()
     torch.cuda.synchronize()
     assert torch.equal(h1, lay.bufs["h"][:R])
+
+
+@pytest.mark.parametrize("name,T,d,E,k,H,ns,Hs,pad,skew", [CASES[1], CASES[3], CASES[4]])
+def test_expert_ffn_call(name, T, d, E, k, H, ns, Hs, pad, skew):
+    """moe_expert_ffn (gate/up, down and the shared expert in one call) then
+    moe_combine: y against the oracle, and h, out_perm, s_out bit for bit
+    the same as from the three separate calls."""
+    s, inp, valid, topk, g, lay = _setup(T, d, E, k, H, ns, Hs, pad, skew)
+    lay.permute()
+    lay.expert_ffn()
+    lay.combine()
+    torch.cuda.synchronize()
+    assert lay.status() == 0
+    R = int(lay.bufs["row_offsets"][-1])
+    one = {n: lay.bufs[n][:R].clone() for n in ("h", "out_perm")}
+    one["y"] = lay.bufs["y"].clone()
+    if ns:
+        one["s_out"] = lay.bufs["s_out"].clone()
+    vnp = None if valid is None else valid.numpy()
+    y_ref, _ = O.experts_forward(inp["x"], topk.numpy(), g.numpy(), inp["W_gu"],
+                                 inp["W_down"], inp["Ws_gu"], inp["Ws_down"], vnp)
+    y_ideal, _ = O.experts_forward(inp["x"], topk.numpy(), g.numpy(), inp["W_gu"],
+                                   inp["W_down"], inp["Ws_gu"], inp["Ws_down"], vnp,
+                                   rnd=bf16_round)
+    chk = Checker()
+    chk.layer("y", one["y"], y_ref, y_ideal)
+    chk.done()
+    for n in ("h", "out_perm", "y", "s_out"):
+        if n in one:
+            lay.bufs[n].fill_(3.0)
+    lay.gate_up()
+    lay.down()
+    lay.shared()
+    lay.combine()
+    torch.cuda.synchronize()
+    assert lay.status() == 0
+    for n, v in one.items():
+        cur = lay.bufs[n][:R] if n in ("h", "out_perm") else lay.bufs[n]
+        assert torch.equal(cur, v), n

@@ -1,7 +1,10 @@
 """GPU parity at the full workload sizes, in the launch sequence bench.py
-times, on outputs the oracle can compute one by one.
+times (Layer.step: the fused router + route, the permute, the grouped GEMMs,
+the combine folded into the shared expert's down GEMM where there is one,
+and the backward), on outputs the oracle can compute one by one.
 
-Checked in full: router logits, the routing (selection, counts, f, p, aux),
+Checked in full: router logits, the routing (selection, counts; f, p, aux
+and the metrics at 1e-5 against the oracle's route on the same fp32 logits),
 the dispatch (offsets, padded row offsets, perm, inv) and the copied rows.
 Checked on samples: the layer output y and the input gradient dx and logit
 gradient of 48 seeded tokens; 16 columns of dW_down and 16 hidden units
@@ -16,8 +19,8 @@ import torch
 from mixture_experts_ffn_02_gb300 import synth
 from mixture_experts_ffn_02_gb300.binding import Layer
 from oracle import moe_oracle as O
-from moe_check import (STAT_RTOL, Checker, bf16_round, logit_error_bound, np64, padded_layout,
-                       reconcile_selection)
+from moe_check import (Checker, assert_route_matches, bf16_round, logit_error_bound, np64,
+                       padded_layout, reconcile_selection, route_on_gpu_logits)
 
 pytestmark = pytest.mark.gpu
 
@@ -36,14 +39,7 @@ def run_bench_sequence(s):
     dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     lay.set_inputs(dev["x"], dev["Wr"], dev["W_gu"], dev["W_down"], dev["Ws_gu"],
                    dev["Ws_down"], bias=dev["bias"], valid=dev["valid"])
-    lay.router_logits()
-    lay.route()
-    lay.permute()
-    lay.gate_up()
-    lay.down()
-    lay.shared()
-    lay.combine()
-    lay.backward(dev["dY"])
+    lay.step(dev["dY"])           # bench.py's step: the same calls, in the same order
     torch.cuda.synchronize()
     assert lay.status() == 0
     return inp, lay
@@ -70,16 +66,9 @@ def test_full_size_layer(cfg):
     r = O.route_stats(probs, sel, real, bool(s.norm_topk))
     np.testing.assert_array_equal(b["topk_idx"].cpu().numpy(), r["topk_idx"])
     np.testing.assert_array_equal(b["counts"].cpu().numpy(), r["counts"])
-    np.testing.assert_allclose(np64(b["f"]), r["f"], rtol=STAT_RTOL)
-    np.testing.assert_allclose(np64(b["p"]), r["p"], rtol=1e-4, atol=1e-7)
-    assert float(b["aux"][0]) == pytest.approx(r["aux"], rel=1e-4)
-    m = O.router_metrics(L, r["counts"], real)
-    st = b["router_stats"].cpu().numpy().astype(np.float64)
-    assert st[0] == pytest.approx(m["z_loss"], rel=1e-4)
-    assert st[1] == pytest.approx(m["entropy"], rel=1e-4)
-    assert (st[2], st[3], st[5], st[6]) == (m["count_min"], m["count_max"], m["unused"],
-                                            m["T_real"])
-    assert st[4] == pytest.approx(m["count_cv"], rel=1e-5, abs=1e-7)
+    # the statistics and metrics at 1e-5: the oracle's route on the GPU's own
+    # fp32 logits (the same keys, so the same selection bit for bit)
+    assert_route_matches(b, route_on_gpu_logits(b, inp, s.k, s.norm_topk))
 
     # ---- dispatch, in full
     offsets, row_offsets, row_of_pair, perm_padded = padded_layout(r["topk_idx"], s.E)
@@ -109,16 +98,15 @@ def test_full_size_layer(cfg):
                                    inp["W_down"], inp["Ws_gu"], inp["Ws_down"],
                                    sub_real.astype(np.uint8), rnd=rnd)
         fwd["y_" + name] = y_s
-    chk.close("y[sample]", b["y"][tsd], fwd["y_exact"])
-    chk.close2("y[sample]", b["y"][tsd], fwd["y_exact"], fwd["y_ideal"])
+    chk.layer("y[sample]", b["y"][tsd], fwd["y_exact"], fwd["y_ideal"])
     # the aux term scales with 1/T_real of the whole batch, not of the sample
     coef = s.aux_coef * max(int(sub_real.sum()), 1) / int(real.sum())
     args = (xs, inp["Wr"], inp["W_gu"], inp["W_down"], inp["Ws_gu"], inp["Ws_down"], fwd,
             inp["dY"][tsc])
     ex = O.backward(*args, norm_topk=bool(s.norm_topk), aux_coef=coef)
     idl = O.backward(*args, norm_topk=bool(s.norm_topk), aux_coef=coef, rnd=bf16_round)
-    chk.close2("dx[sample]", g["dx"][tsd], ex["dx"], idl["dx"])
-    chk.close2("d_logits[sample]", g["d_logits"][tsd], ex["d_logits"], idl["d_logits"])
+    chk.layer("dx[sample]", g["dx"][tsd], ex["dx"], idl["dx"])
+    chk.layer("d_logits[sample]", g["d_logits"][tsd], ex["d_logits"], idl["d_logits"])
 
     # ---- one expert's weight gradients on sampled columns / hidden units
     counts = r["counts"]
@@ -146,7 +134,7 @@ def test_full_size_layer(cfg):
     gWg = g["dW_gu"][e][torch.from_numpy(J).cuda()]
     gWu = g["dW_gu"][e][torch.from_numpy(J + s.H).cuda()]
     for nm, gv, k_ in (("dW_down[e]", gWd, 0), ("dW_gate[e]", gWg, 1), ("dW_up[e]", gWu, 2)):
-        chk.close2(nm, gv, res["exact"][k_], res["ideal"][k_])
+        chk.layer(nm, gv, res["exact"][k_], res["ideal"][k_])
 
     if s.n_shared:
         Hs = s.Hs_total
@@ -165,7 +153,7 @@ def test_full_size_layer(cfg):
         for nm, gv, k_ in (("dWs_down", g["dWs_down"][:, jt], 0),
                            ("dWs_gate", g["dWs_gu"][jt], 1),
                            ("dWs_up", g["dWs_gu"][jt + Hs], 2)):
-            chk.close2(nm, gv, res["exact"][k_], res["ideal"][k_])
+            chk.layer(nm, gv, res["exact"][k_], res["ideal"][k_])
 
     # ---- dW_r = x^T d_logits (identity at any size)
     dWr_id = x.T @ np64(g["d_logits"])

@@ -183,3 +183,104 @@ def test_mx_shared_expert_left_unquantised_is_caught(monkeypatch):
         return y, routed
     monkeypatch.setattr(M, "experts_forward_mx", shared_exact)
     assert _fails(PX.test_mx_experts_dense_masked_formulation)
+
+
+# ---- the storage-rounding hook (tests/test_oracle_storage.py)
+
+import inspect  # noqa: E402
+
+import test_oracle_storage as S  # noqa: E402
+
+
+def _storage_pins_fail():
+    return (_fails(S.test_backward_storage_points_by_hand)
+            or _fails(S.test_forward_storage_points_by_hand))
+
+
+def _values_fail(monkeypatch):
+    """The value checks alone (a spy that records nothing) also catch it."""
+    class Quiet(S.Spy):
+        def __call__(self, v):
+            return S.q8(v)
+    monkeypatch.setattr(S, "Spy", Quiet)
+    try:
+        S.test_backward_storage_points_by_hand()
+    except AssertionError:
+        return True
+    try:
+        S.test_forward_storage_points_by_hand()
+    except AssertionError:
+        return True
+    return False
+
+
+def test_unrounded_hidden_is_caught(monkeypatch):
+    orig = O.swiglu_parts
+    monkeypatch.setattr(O, "swiglu_parts", lambda xr, Wg, Wu, Wd, rnd=None:
+                        orig(xr, Wg, Wu, Wd, None))
+    assert _storage_pins_fail()
+    assert _values_fail(monkeypatch)
+
+
+def test_rounded_expert_output_is_caught(monkeypatch):
+    orig = O.swiglu_parts
+
+    def parts(xr, Wg, Wu, Wd, rnd=None):
+        out, a, b, h = orig(xr, Wg, Wu, Wd, rnd)
+        return (rnd(out) if rnd else out), a, b, h
+    monkeypatch.setattr(O, "swiglu_parts", parts)
+    assert _storage_pins_fail()
+    assert _values_fail(monkeypatch)
+
+
+def test_unrounded_d_out_is_caught(monkeypatch):
+    monkeypatch.setattr(O, "stored_d_out", lambda g, dY, rnd=None: g[:, None] * dY)
+    assert _storage_pins_fail()
+    assert _values_fail(monkeypatch)
+
+
+def test_dh_rounded_before_the_chain_rule_is_caught(monkeypatch):
+    orig = O.stored_swiglu_backward
+    monkeypatch.setattr(O, "stored_swiglu_backward", lambda dh, a, b, rnd=None:
+                        orig(rnd(dh) if rnd else dh, a, b, rnd))
+    assert _storage_pins_fail()
+    assert _values_fail(monkeypatch)
+
+
+def test_dh_rounded_instead_of_da_db_is_caught(monkeypatch):
+    def moved(dh, a, b, rnd=None):
+        r = rnd or (lambda v: v)
+        return O.swiglu_backward(r(dh), r(a), r(b))
+    monkeypatch.setattr(O, "stored_swiglu_backward", moved)
+    assert _storage_pins_fail()
+    assert _values_fail(monkeypatch)
+
+
+def test_unrounded_saved_preactivations_are_caught(monkeypatch):
+    def exact_ab(dh, a, b, rnd=None):
+        r = rnd or (lambda v: v)
+        da, db = O.swiglu_backward(dh, a, b)
+        return r(da), r(db)
+    monkeypatch.setattr(O, "stored_swiglu_backward", exact_ab)
+    assert _storage_pins_fail()
+    assert _values_fail(monkeypatch)
+
+
+def test_unrounded_da_db_are_caught(monkeypatch):
+    def no_store(dh, a, b, rnd=None):
+        r = rnd or (lambda v: v)
+        return O.swiglu_backward(dh, r(a), r(b))
+    monkeypatch.setattr(O, "stored_swiglu_backward", no_store)
+    assert _storage_pins_fail()
+    assert _values_fail(monkeypatch)
+
+
+def test_rounded_shared_dY_is_caught(monkeypatch):
+    src = inspect.getsource(O.backward)
+    needle = "stored_swiglu_backward(dY[rows] @ Ws_down_"
+    assert needle in src
+    ns = dict(vars(O))
+    exec(src.replace(needle, "stored_swiglu_backward(rnd(dY[rows]) @ Ws_down_"), ns)
+    monkeypatch.setattr(O, "backward", ns["backward"])
+    assert _storage_pins_fail()
+    assert _values_fail(monkeypatch)
