@@ -181,6 +181,18 @@ int moe_row_capacity(const moe_config* cfg, int64_t* rows);
  * layer step; its contents between calls are private to the library. */
 int moe_workspace_bytes(const moe_config* cfg, int training, size_t* bytes);
 
+/* Byte offsets, within a training workspace (moe_workspace_bytes with
+ * training = 1), of the intermediates moe_backward stores there, for
+ * inspection by tests and debuggers after the call:
+ *   out[0] d_out   [R_cap][d]  bf16  g * dY of each routed row
+ *   out[1] d_gu    [R_cap][2H] bf16  (da | db) of each routed row
+ *   out[2] dx_perm [R_cap][d]  fp32  the dX product of each routed row
+ *   out[3] ds_gu   [T][2Hs]    bf16  the shared expert's (da | db); 0 when
+ *                                    n_shared == 0
+ * Rows follow perm (pad rows hold unspecified values).  The layout is part
+ * of this ABI version only.  Host-side query: nothing runs on the device. */
+int moe_workspace_offsets(const moe_config* cfg, size_t* out);
+
 /* Synchronise `stream`, copy the device status word to *status and reset it
  * to MOE_OK.  The only entry point that blocks the host. */
 int moe_get_status(void* workspace, void* stream, int* status);

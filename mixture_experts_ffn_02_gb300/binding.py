@@ -69,6 +69,8 @@ SIGNATURES = {
     "moe_workspace_bytes": (ctypes.c_int, [ctypes.POINTER(MoEConfig), ctypes.c_int,
                                            ctypes.POINTER(ctypes.c_size_t)]),
     "moe_get_status": (ctypes.c_int, [c_void_p, c_void_p, ctypes.POINTER(ctypes.c_int)]),
+    "moe_workspace_offsets": (ctypes.c_int, [ctypes.POINTER(MoEConfig),
+                                             ctypes.POINTER(ctypes.c_size_t)]),
     "moe_selftest_wait_timeout": (ctypes.c_int, [c_void_p, ctypes.c_uint64, c_void_p]),
     "moe_router_logits": (ctypes.c_int, _STEP),
     "moe_route": (ctypes.c_int, _STEP),
@@ -322,6 +324,30 @@ class Layer:
         check(self.lib.moe_route_finalize(ctypes.byref(self.cfg), ctypes.byref(t),
                                           c_void_p(sums.data_ptr()), _stream()),
               "moe_route_finalize")
+
+    def intermediates(self) -> dict:
+        """Views of the backward's stored intermediates in the workspace
+        (moe_workspace_offsets): d_out [R][d] bf16, d_gu [R][2H] bf16,
+        dx_perm [R][d] fp32, and ds_gu [T][2Hs] bf16 with a shared expert."""
+        import torch
+        if not self.training:
+            raise ValueError("only a training workspace holds the backward's intermediates")
+        off = (ctypes.c_size_t * 4)()
+        check(self.lib.moe_workspace_offsets(ctypes.byref(self.cfg), off),
+              "moe_workspace_offsets")
+        R, d, H = self.R_cap, self.cfg.d, self.cfg.H
+        Hs = self.cfg.n_shared * self.cfg.H_shared
+
+        def view(o, n, dt, shape):
+            nb = n * torch.empty((), dtype=dt).element_size()
+            return self.ws[o:o + nb].view(dt).view(*shape)
+        out = dict(d_out=view(off[0], R * d, torch.bfloat16, (R, d)),
+                   d_gu=view(off[1], R * 2 * H, torch.bfloat16, (R, 2 * H)),
+                   dx_perm=view(off[2], R * d, torch.float32, (R, d)))
+        if Hs:
+            out["ds_gu"] = view(off[3], self.cfg.T * 2 * Hs, torch.bfloat16,
+                                (self.cfg.T, 2 * Hs))
+        return out
 
     def status(self) -> int:
         out = ctypes.c_int()

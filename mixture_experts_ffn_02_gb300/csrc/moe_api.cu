@@ -596,6 +596,19 @@ int moe_workspace_bytes(const moe_config* cfg, int training, size_t* bytes) {
   return MOE_OK;
 }
 
+int moe_workspace_offsets(const moe_config* cfg, size_t* out) {
+  int rc = check_cfg(cfg);
+  if (rc) return rc;
+  if (!out) return MOE_ERR_NULL;
+  WsLayout w;
+  ws_layout(cfg, 1, &w);
+  out[0] = w.d_out;
+  out[1] = w.d_gu;
+  out[2] = w.dx_perm;
+  out[3] = hs_total(*cfg) > 0 ? w.ds_gu : 0;
+  return MOE_OK;
+}
+
 int moe_get_status(void* workspace, void* stream, int* status) {
   if (!workspace || !status) return MOE_ERR_NULL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

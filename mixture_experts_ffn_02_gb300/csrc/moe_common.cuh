@@ -235,6 +235,16 @@ __device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// Untiled bulk copy global -> this CTA's shared memory, completing `bytes`
+// on the mbarrier `bar`.  Both addresses must be 16-byte aligned and `bytes`
+// a multiple of 16.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar) : "memory");
+}
+
 // TMA stores (shared -> global) in bulk groups.  The source is the 128-byte
 // swizzled box the tensor map describes; the writing threads must issue
 // fence_proxy_async_smem() and synchronise before the store is issued.

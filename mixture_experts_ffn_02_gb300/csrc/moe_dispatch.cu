@@ -8,6 +8,7 @@
 // "spark-gpt" README, feature list (fp32-softmax top-k routing, statistic over
 // real tokens, PAD filler positions).
 #include <float.h>
+#include <stdlib.h>
 #include <math.h>
 
 #include "moe_common.cuh"
@@ -22,6 +23,15 @@ constexpr int kThreads = 256;
 
 __device__ __forceinline__ bool row_real(const uint8_t* valid, int t) {
   return valid == nullptr || valid[t] != 0;
+}
+
+// Programmatic dependent launch: a kernel may let its successor launch while
+// it still runs (griddepcontrol.launch_dependents); the successor waits for
+// its predecessor's completion and memory (griddepcontrol.wait) before it
+// reads the predecessor's results.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // 8 consecutive fp32 values (32-byte aligned) through the non-coherent path.
@@ -362,7 +372,8 @@ __device__ __forceinline__ void route_token(const float (&lv_in)[V], const float
                                             int t, bool in_range, bool real, int E, int k, int G,
                                             int lig, int norm_topk, bool want_stats,
                                             int32_t* __restrict__ topk, float* __restrict__ gates,
-                                            int* cnt_s, float (&psum)[V], int& my_treal,
+                                            int* cnt_s, unsigned long long (&psum)[V],
+                                            int& my_treal,
                                             float& z_acc, float& ent_acc, int* __restrict__ status) {
   float lv[V], kv[V], sv[V];
   bool bad = false;
@@ -501,31 +512,35 @@ __device__ __forceinline__ void route_token(const float (&lv_in)[V], const float
     }
   }
   if (real) {
+    // probabilities in fixed point, 32 fractional bits, per token: integer
+    // sums are exact, so p does not depend on which lane, block or kernel
+    // summed which tokens
 #pragma unroll
-    for (int v = 0; v < V; ++v) psum[v] += sv[v];
+    for (int v = 0; v < V; ++v) psum[v] += __float2ull_rn(sv[v] * 4294967296.f);
     if (lig == 0) ++my_treal;
   }
 }
 
 // End of a routing block.  The block's expert counts and probability sums
-// (its own tokens, summed in a fixed order) join totals kept as integers:
-// counts as they are, probability sums in fixed point with 32 fractional
-// bits, both by integer atomics, which are exact, so the totals do not depend
-// on the order the blocks finish in and the last block reads only E values.
+// (each token's probability in fixed point with 32 fractional bits) join
+// totals kept as integers by integer atomics, which are exact, so the totals
+// do not depend on the order the blocks finish in, nor on how tokens were
+// spread over lanes and blocks, and the last block reads only E values.
 // The block's real-token count and metric sums go to per-block slots.  The
 // last block to finish writes counts, f, p, aux and the metrics.
-// psum_s holds [blockDim/G][E] floats; cnt_s [E] ints with the block's counts;
+// psum_s holds [blockDim/G][E] fixed-point sums; cnt_s [E] ints with the block's counts;
 // acc_cnt and acc_psum must be zero when the kernel starts.
 template <int V>
 __device__ __forceinline__ void route_block_end(
-    const float (&psum)[V], int my_treal, float z_acc, float ent_acc, int* cnt_s, float* psum_s,
+    const unsigned long long (&psum)[V], int my_treal, float z_acc, float ent_acc, int* cnt_s,
+    unsigned long long* psum_s,
     int G, int lig, int grp, int E, int k, int* __restrict__ acc_cnt,
     unsigned long long* __restrict__ acc_psum, int* __restrict__ blk_treal,
     int* __restrict__ done, int32_t* __restrict__ counts, float* __restrict__ f,
     float* __restrict__ p, float* __restrict__ aux, float* __restrict__ blk_zent,
     float* __restrict__ stats) {
   __shared__ int treal_s, tot_s, ticket_s;
-  __shared__ float red_s[kThreads / 32], zred_s[kThreads / 32], ered_s[kThreads / 32];
+  __shared__ float red_s[32], zred_s[32], ered_s[32];        // up to 1024 threads
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nwarps = blockDim.x >> 5;
   const int groups = blockDim.x / G;
@@ -544,10 +559,9 @@ __device__ __forceinline__ void route_block_end(
   }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    float s = 0.f;
-    for (int g2 = 0; g2 < groups; ++g2) s += psum_s[g2 * E + e];
+    unsigned long long fx = 0ull;
+    for (int g2 = 0; g2 < groups; ++g2) fx += psum_s[g2 * E + e];
     if (cnt_s[e]) atomicAdd(acc_cnt + e, cnt_s[e]);
-    const unsigned long long fx = __double2ull_rn((double)s * 4294967296.0);
     if (fx) atomicAdd(acc_psum + e, fx);
   }
   if (threadIdx.x == 0) {
@@ -659,16 +673,16 @@ route_kernel(const float* __restrict__ L, const float* __restrict__ bias,
   extern __shared__ unsigned char smem_raw[];
   const int groups = blockDim.x / G;
   int* cnt_s = reinterpret_cast<int*>(smem_raw);                 // [E]
-  float* psum_s = reinterpret_cast<float*>(cnt_s + 256);         // [groups][E]
+  unsigned long long* psum_s = reinterpret_cast<unsigned long long*>(cnt_s + 256);  // [groups][E]
   for (int e = threadIdx.x; e < E; e += blockDim.x) cnt_s[e] = 0;
   __syncthreads();
 
   const int lane = threadIdx.x & 31;
   const int lig = lane & (G - 1);           // lane in group
   const int grp = threadIdx.x / G;          // group in block
-  float psum[V];
+  unsigned long long psum[V];
 #pragma unroll
-  for (int v = 0; v < V; ++v) psum[v] = 0.f;
+  for (int v = 0; v < V; ++v) psum[v] = 0ull;
   int my_treal = 0;
   float z_acc = 0.f, ent_acc = 0.f;
 
@@ -715,7 +729,7 @@ router_route_small_kernel(const bf16* __restrict__ x, const float* __restrict__ 
   constexpr int N = TT * E;                      // 16 or 32 sums per warp
   extern __shared__ float wr_s[];                // padded [d][E]
   __shared__ int cnt_s[E];
-  __shared__ float psum_s[kThreads / G * E];
+  __shared__ unsigned long long psum_s[kThreads / G * E];
   stage_wr(Wr, wr_s, d, E);
   for (int e = threadIdx.x; e < E; e += blockDim.x) cnt_s[e] = 0;
   __syncthreads();
@@ -723,7 +737,7 @@ router_route_small_kernel(const bf16* __restrict__ x, const float* __restrict__ 
   const int wpb = blockDim.x >> 5;
   const int lig = lane % G, tig = lane / G;      // expert and token of this lane
   const int grp = threadIdx.x / G;
-  float psum[1] = {0.f};
+  unsigned long long psum[1] = {0ull};
   int my_treal = 0;
   float z_acc = 0.f, ent_acc = 0.f;
   for (long long tile = (long long)blockIdx.x * wpb + (threadIdx.x >> 5);
@@ -810,6 +824,287 @@ router_route_small_kernel(const bf16* __restrict__ x, const float* __restrict__ 
                      acc_psum, blk_treal, done, counts, f, p, aux, blk_zent, stats);
 }
 
+// a0 + a1 streamed (small E, the default fused form): one resident block of
+// 16 warps per SM, each block on a contiguous range of the tokens.  A warp
+// works on groups of TT = 32 / G rows (or U = a multiple of TT rows when
+// whole rows fit its buffers), one column chunk of CW columns at a time
+// (CW = d when the rows are short).  Each warp owns two row buffers in
+// shared memory: while it computes on one unit (rows x chunk), lane 0 has
+// the next one in flight, loaded by untiled bulk copies (one per row, or one
+// for the whole unit when it spans whole rows) that complete on the
+// buffer's mbarrier, so loads need no registers and each SM keeps about 32
+// units in flight.  W_r is staged meanwhile, in a layout that keeps the
+// weights of two neighbouring columns side by side, so one packed fp32 FMA
+// (fma.rn.f32x2) does the two columns' products for one expert: the lane
+// sums even and odd columns separately and adds the two at the end.  After
+// a group's last chunk its logits are reduced over the warp and the tokens
+// routed with the route kernel's code.  The statistics are sums of
+// integers and of per-token values, so the route kernel run on the logits
+// this kernel wrote gives the same selection, gates, counts, f, p and aux.
+// The kernel is launched behind the small kernel that zeroes the routing
+// totals, with programmatic dependent launch: it waits for that kernel
+// (griddepcontrol.wait) only before its block-end reduction.
+constexpr int kStreamWarps = 16;
+constexpr int kStreamThreads = kStreamWarps * 32;
+constexpr int kStreamBufs = 2;                       // row buffers per warp
+constexpr uint64_t kStreamWaitNs = 2000000000ull;   // a bulk copy not done in 2 s: give up
+
+__global__ void __launch_bounds__(kThreads)
+route_zero_kernel(unsigned int* __restrict__ acc, int words) {
+  pdl_trigger();
+  for (int i = threadIdx.x; i < words; i += blockDim.x) acc[i] = 0u;
+}
+
+// W_r [d][E] in shared memory by column pairs: every 8 columns c0..c0+7 (c0 a
+// multiple of 8) take a block of 8E floats and 4 of padding (so the 8-column
+// blocks of consecutive lanes fall in distinct banks); inside it, pair q
+// (columns c0 + 2q and c0 + 2q + 1) holds for each expert e the two
+// columns' weights side by side.
+__device__ __forceinline__ int wr_pair_index(int c, int e, int E) {
+  return (c >> 3) * (8 * E + 4) + ((c & 7) >> 1) * (2 * E) + 2 * e + (c & 1);
+}
+
+// Each thread moves W_r[c][e4..e4+3] and W_r[c+1][e4..e4+3] (c even) into
+// the pair layout: 8 consecutive floats there.
+__device__ __forceinline__ void stage_wr_pairs(const float* __restrict__ Wr, float* wr_s, int d,
+                                               int E) {
+  const int nq = E / 4;
+  const int units = (d / 2) * nq;
+#pragma unroll 4
+  for (int u = threadIdx.x; u < units; u += blockDim.x) {
+    const int pc = u / nq, e4 = (u - pc * nq) * 4, c = 2 * pc;
+    const float4 r0 = __ldg(reinterpret_cast<const float4*>(Wr + (size_t)c * E + e4));
+    const float4 r1 = __ldg(reinterpret_cast<const float4*>(Wr + (size_t)(c + 1) * E + e4));
+    float* dst = wr_s + wr_pair_index(c, e4, E);
+    *reinterpret_cast<float4*>(dst) = make_float4(r0.x, r1.x, r0.y, r1.y);
+    *reinterpret_cast<float4*>(dst + 4) = make_float4(r0.z, r1.z, r0.w, r1.w);
+  }
+}
+
+__device__ __forceinline__ unsigned long long f32x2_pack(float lo, float hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float f32x2_sum(unsigned long long v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return lo + hi;
+}
+// d = a * b + c on both halves, each an IEEE fp32 fused multiply-add.
+__device__ __forceinline__ unsigned long long fma_f32x2(unsigned long long a,
+                                                       unsigned long long b,
+                                                       unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+// Warp reduce-scatter of N values, unrolled at compile time: at the step
+// with offset O the lane keeps the half of its NN values that its bit O
+// selects and adds the partner's copy of that half; once one value is left,
+// the remaining offsets add the partners' values.  Lane l ends with value
+// l / (32 / N), summed over the warp -- the same additions, in the same
+// order, as the loop in router_route_small_kernel.
+template <int O, int NN, int N>
+struct ReduceScatter {
+  static __device__ __forceinline__ void run(float (&v)[N], int lane) {
+    if constexpr (NN > 1) {
+      const bool upper = (lane & O) != 0;
+#pragma unroll
+      for (int j = 0; j < NN / 2; ++j) {
+        const float send = upper ? v[j] : v[j + NN / 2];
+        const float keep = upper ? v[j + NN / 2] : v[j];
+        v[j] = keep + __shfl_xor_sync(0xffffffffu, send, O);
+      }
+      ReduceScatter<O / 2, NN / 2, N>::run(v, lane);
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], O);
+      ReduceScatter<O / 2, 1, N>::run(v, lane);
+    }
+  }
+};
+template <int NN, int N>
+struct ReduceScatter<0, NN, N> {
+  static __device__ __forceinline__ void run(float (&)[N], int) {}
+};
+
+// One lane issues the copies of one unit -- rows [r0, r0 + rows) of x,
+// columns [c0, c0 + cw) -- into a row buffer whose rows are cw_max columns
+// apart, completing on the buffer's mbarrier: one copy when the unit spans
+// whole rows (cw = d), else one per row.  Called after the warp has finished
+// reading the buffer: the proxy fence orders those reads before the copies'
+// writes.
+__device__ __forceinline__ void stream_issue(const bf16* __restrict__ x, int d, int r0, int rows,
+                                             int c0, int cw, int cw_max, uint32_t bar,
+                                             uint32_t dst) {
+  const uint32_t row_bytes = (uint32_t)cw * 2u;
+  fence_proxy_async_smem();
+  mbar_arrive_expect_tx(bar, (uint32_t)rows * row_bytes);
+  if (cw == d) {
+    bulk_load(dst, x + (size_t)r0 * d, (uint32_t)rows * row_bytes, bar);
+  } else {
+    for (int i = 0; i < rows; ++i)
+      bulk_load(dst + (uint32_t)i * (uint32_t)cw_max * 2u, x + (size_t)(r0 + i) * d + c0,
+                row_bytes, bar);
+  }
+}
+
+// Unit n of a warp: row group j = n / nch (rows (ufirst + j * kStreamWarps)
+// * U onwards) and column chunk n % nch; false past the block's groups.
+struct StreamUnit {
+  int r0, rows, ch, c0, cw;
+};
+__device__ __forceinline__ bool stream_unit(int n, int nch, int ufirst, int u1, int U, int T,
+                                            int d, int CW, StreamUnit& s) {
+  const int j = n / nch;
+  const int u = ufirst + j * kStreamWarps;
+  if (u >= u1) return false;
+  s.ch = n - j * nch;
+  s.r0 = u * U;
+  s.rows = min(U, T - s.r0);
+  s.c0 = s.ch * CW;
+  s.cw = min(CW, d - s.c0);
+  return true;
+}
+
+template <int E>
+__global__ void __launch_bounds__(kStreamThreads, 1)
+router_route_stream_kernel(const bf16* __restrict__ x, const float* __restrict__ Wr,
+                           const float* __restrict__ bias, const uint8_t* __restrict__ valid,
+                           int T, int d, int k, int norm_topk, int U, int CW, int wr_bytes,
+                           int buf_bytes, float* __restrict__ L, int32_t* __restrict__ topk,
+                           float* __restrict__ gates, int* __restrict__ acc_cnt,
+                           unsigned long long* __restrict__ acc_psum, int* __restrict__ blk_treal,
+                           int* __restrict__ done, int32_t* __restrict__ counts,
+                           float* __restrict__ f, float* __restrict__ p, float* __restrict__ aux,
+                           float* __restrict__ blk_zent, float* __restrict__ stats,
+                           int* __restrict__ status) {
+  constexpr int G = E < 8 ? 8 : E;
+  constexpr int TT = 32 / G;
+  constexpr int N = TT * E;                      // 16 or 32 sums per warp
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  float* wr_s = reinterpret_cast<float*>(smem_raw);              // column-pair layout
+  unsigned char* rows_s = smem_raw + wr_bytes;                   // [warps][bufs][buf_bytes]
+  __shared__ __align__(8) uint64_t full[kStreamWarps * kStreamBufs];
+  __shared__ int cnt_s[E];
+  __shared__ unsigned long long psum_s[kStreamThreads / G * E];
+  __shared__ int abort_s;                        // stays 0: waits end only by time
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lig = lane % G, tig = lane / G;      // expert and token of this lane
+  const int grp = threadIdx.x / G;
+  const int nch = (d + CW - 1) / CW;             // > 1 only with U == TT
+  const int ngroups = (T + U - 1) / U;
+  const int per = (ngroups + gridDim.x - 1) / gridDim.x;
+  const int u0 = blockIdx.x * per;
+  const int u1 = min(ngroups, u0 + per);
+  const int ufirst = u0 + warp;
+  if (threadIdx.x < kStreamWarps * kStreamBufs) mbar_init(smem_u32(&full[threadIdx.x]), 1);
+  if (threadIdx.x == 0) abort_s = 0;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt_s[e] = 0;
+  fence_mbar_init();
+  __syncthreads();
+
+  const uint32_t bar0 = smem_u32(&full[warp * kStreamBufs]);
+  const uint32_t dst0 = smem_u32(rows_s + (size_t)warp * kStreamBufs * buf_bytes);
+  if (lane == 0) {
+    StreamUnit su;
+#pragma unroll
+    for (int n = 0; n < kStreamBufs; ++n)
+      if (stream_unit(n, nch, ufirst, u1, U, T, d, CW, su))
+        stream_issue(x, d, su.r0, su.rows, su.c0, su.cw, CW, bar0 + 8 * n, dst0 + n * buf_bytes);
+  }
+  stage_wr_pairs(Wr, wr_s, d, E);
+  __syncthreads();
+
+  unsigned long long psum[1] = {0ull};
+  int my_treal = 0;
+  float z_acc = 0.f, ent_acc = 0.f;
+  unsigned long long acc2[TT][E];                // (even, odd) column sums of one group
+  StreamUnit su;
+  for (int n = 0; stream_unit(n, nch, ufirst, u1, U, T, d, CW, su); ++n) {
+    const int b = n % kStreamBufs;
+    // each warp waits only for its own copies (never on another warp)
+    if (!mbar_wait_bounded(bar0 + 8 * b, (uint32_t)((n / kStreamBufs) & 1), &abort_s,
+                           kStreamWaitNs)) {
+      if (lane == 0) set_status(status, MOE_ERR_TIMEOUT);
+      // wait (bounded) for this warp's other copy in flight, so that none
+      // still targets the buffers when the block exits
+      StreamUnit sn;
+      if (stream_unit(n + 1, nch, ufirst, u1, U, T, d, CW, sn))
+        mbar_wait_bounded(bar0 + 8 * ((n + 1) % kStreamBufs),
+                          (uint32_t)(((n + 1) / kStreamBufs) & 1), &abort_s, kStreamWaitNs);
+      break;
+    }
+    const bf16* xs = reinterpret_cast<const bf16*>(
+        rows_s + ((size_t)warp * kStreamBufs + b) * buf_bytes);
+    for (int g0 = 0; g0 < su.rows; g0 += TT) {
+      if (su.ch == 0) {
+#pragma unroll
+        for (int i = 0; i < TT; ++i)
+#pragma unroll
+          for (int e = 0; e < E; ++e) acc2[i][e] = 0ull;
+      }
+      for (int cc = lane * 8; cc < su.cw; cc += 256) {
+        uint4 cur[TT];
+#pragma unroll
+        for (int i = 0; i < TT; ++i)
+          cur[i] = g0 + i < su.rows
+                       ? *reinterpret_cast<const uint4*>(xs + (size_t)(g0 + i) * CW + cc)
+                       : make_uint4(0, 0, 0, 0);
+        const float* w = wr_s + wr_pair_index(su.c0 + cc, 0, E);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {            // columns +2q, +2q+1
+          unsigned long long xp[TT];
+#pragma unroll
+          for (int i = 0; i < TT; ++i) {
+            const uint32_t wd = (&cur[i].x)[q];
+            xp[i] = f32x2_pack(__uint_as_float(wd << 16), __uint_as_float(wd & 0xffff0000u));
+          }
+#pragma unroll
+          for (int e2 = 0; e2 < E; e2 += 2) {
+            const float4 wv = *reinterpret_cast<const float4*>(w + q * 2 * E + 2 * e2);
+            const unsigned long long wa = f32x2_pack(wv.x, wv.y);
+            const unsigned long long wb = f32x2_pack(wv.z, wv.w);
+#pragma unroll
+            for (int i = 0; i < TT; ++i) {
+              acc2[i][e2] = fma_f32x2(xp[i], wa, acc2[i][e2]);
+              acc2[i][e2 + 1] = fma_f32x2(xp[i], wb, acc2[i][e2 + 1]);
+            }
+          }
+        }
+      }
+      if (su.ch == nch - 1) {
+        float v[N];
+#pragma unroll
+        for (int jj = 0; jj < N; ++jj) v[jj] = f32x2_sum(acc2[jj / E][jj % E]);
+        ReduceScatter<16, N, N>::run(v, lane);
+        // lane l holds value l / (32 / N): token (l / (32 / N)) / E; with
+        // N = 16 (E = 4, G = 8) expert e of token g sits in lanes 8g + 2e, +1
+        float my = v[0];
+        if (N == 16) my = __shfl_sync(0xffffffffu, my, (lane & ~7) + 2 * (lig & 3));
+        const int t = su.r0 + g0 + tig;
+        const bool in_range = g0 + tig < su.rows;
+        const bool real = in_range && row_real(valid, t);
+        if (in_range && lig < E) L[(size_t)t * E + lig] = my;
+        float lv[1] = {my};
+        route_token<1>(lv, bias, t, in_range, real, E, k, G, lig, norm_topk, stats != nullptr,
+                       topk, gates, cnt_s, psum, my_treal, z_acc, ent_acc, status);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) {
+      StreamUnit sn;
+      if (stream_unit(n + kStreamBufs, nch, ufirst, u1, U, T, d, CW, sn))
+        stream_issue(x, d, sn.r0, sn.rows, sn.c0, sn.cw, CW, bar0 + 8 * b, dst0 + b * buf_bytes);
+    }
+  }
+  pdl_wait();                                    // the zeroed totals
+  route_block_end<1>(psum, my_treal, z_acc, ent_acc, cnt_s, psum_s, G, lig, grp, E, k, acc_cnt,
+                     acc_psum, blk_treal, done, counts, f, p, aux, blk_zent, stats);
+}
+
 // --------------------------------------------------------------------------
 // Data-parallel routing statistics: a rank's sums, and f / p / aux from sums
 // that the caller has added over the ranks.  One block; E <= 256.
@@ -862,10 +1157,6 @@ route_finalize_kernel(const double* __restrict__ sums, int E, int k, float* __re
 // memory (griddepcontrol.wait) before they read its results, so the launch
 // latency of the two small kernels overlaps the work.
 // --------------------------------------------------------------------------
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void pdl_trigger() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
 
 __global__ void __launch_bounds__(kThreads)
 perm_hist_kernel(const int32_t* __restrict__ topk, int T, int k, int E,
@@ -1481,7 +1772,7 @@ cudaError_t launch_route(const moe_config& c, const float* L, const float* bias,
   const int G = route_group_lanes(c.E);
   const int V = (c.E + G - 1) / G;
   const int groups = kThreads / G;
-  const size_t smem = 256 * sizeof(int) + (size_t)groups * c.E * sizeof(float);
+  const size_t smem = 256 * sizeof(int) + (size_t)groups * c.E * sizeof(unsigned long long);
   char* acc = ws + w.route_done;
   cudaError_t err = cudaMemsetAsync(acc, 0, kRouteAccBytes, s);
   if (err != cudaSuccess) return err;
@@ -1516,7 +1807,7 @@ cudaError_t launch_route_scratch(const moe_config& c, const float* L, const floa
   const int G = route_group_lanes(c.E);
   const int V = (c.E + G - 1) / G;
   const int groups = kThreads / G;
-  const size_t smem = 256 * sizeof(int) + (size_t)groups * c.E * sizeof(float);
+  const size_t smem = 256 * sizeof(int) + (size_t)groups * c.E * sizeof(unsigned long long);
   cudaError_t err = cudaMemsetAsync(acc, 0, kRouteAccBytes, s);
   if (err != cudaSuccess) return err;
   int* done = reinterpret_cast<int*>(acc);
@@ -1536,10 +1827,96 @@ cudaError_t launch_route_scratch(const moe_config& c, const float* L, const floa
   return cudaGetLastError();
 }
 
+// A kernel launch with dynamic shared memory that may begin while the
+// previous kernel on the stream still runs (programmatic stream
+// serialisation); the kernel calls griddepcontrol.wait before it reads what
+// that kernel wrote.
+template <typename... K, typename... A>
+cudaError_t launch_pdl_smem(void (*kern)(K...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t s, A... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+// Units and buffers of router_route_stream_kernel: two buffers per warp,
+// each at most 1/32 of what W_r leaves of the 227 KB a block may use.  When
+// TT whole rows fit a buffer, a unit is U = TT * m whole rows (CW = d);
+// otherwise it is TT rows by a chunk of CW columns (a multiple of 256).
+// False if not even TT rows of 256 columns fit.
+bool router_stream_sizes(const moe_config& c, int* U, int* CW, int* wr_bytes, int* buf_bytes) {
+  const int G = route_group_lanes(c.E);
+  const int TT = 32 / G;
+  const int wr = (int)((wr_smem_bytes(c.d, c.E) + 127) / 128 * 128);
+  // static shared memory: mbarriers, counts, per-group sums, block-end scratch
+  const int static_smem = 1024 + (kStreamThreads / G) * c.E * 8 + 512;
+  int per_buf = (227 * 1024 - wr - static_smem) / (kStreamWarps * kStreamBufs);
+  if (per_buf > 8 * 1024) per_buf = 8 * 1024;
+  const int row_bytes = c.d * 2;
+  if (TT * row_bytes <= per_buf) {
+    *U = TT * (per_buf / (TT * row_bytes));
+    *CW = c.d;
+  } else {
+    const int cw = per_buf / (TT * 2) / 256 * 256;
+    if (cw < 256) return false;
+    *U = TT;
+    *CW = cw;
+  }
+  *wr_bytes = wr;
+  *buf_bytes = (*U * *CW * 2 + 127) / 128 * 128;
+  return true;
+}
+
 cudaError_t launch_router_route(const moe_config& c, const void* x, const float* Wr,
                                 const float* bias, const uint8_t* valid, float* L, int32_t* topk,
                                 float* gates, int32_t* counts, float* f, float* p, float* aux,
                                 float* stats, char* ws, const WsLayout& w, cudaStream_t s) {
+  int U = 0, CW = 0, wrb = 0, bufb = 0;
+  DeviceInfo di;
+  if (device_info(&di) != MOE_OK) return cudaErrorUnknown;
+  // MOE_ROUTER_STREAM=0 selects the register-loading form (comparisons)
+  const char* env = getenv("MOE_ROUTER_STREAM");
+  const bool stream_form = !(env && env[0] == '0');
+  if (stream_form && router_stream_sizes(c, &U, &CW, &wrb, &bufb)) {
+    char* acc = ws + w.route_done;
+    route_zero_kernel<<<1, kThreads, 0, s>>>(reinterpret_cast<unsigned int*>(acc),
+                                             (int)(kRouteAccBytes / 4));
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    int* done = reinterpret_cast<int*>(acc);
+    int* cnt = reinterpret_cast<int*>(acc + kRouteAccCnt);
+    unsigned long long* psum = reinterpret_cast<unsigned long long*>(acc + kRouteAccPsum);
+    int* treal = reinterpret_cast<int*>(ws + w.route_treal);
+    float* zent = reinterpret_cast<float*>(ws + w.route_zent);
+    int* status = reinterpret_cast<int*>(ws + w.status);
+    const long long ngroups = ((long long)c.T + U - 1) / U;
+    long long grid = di.num_sms;
+    if (grid > ngroups) grid = ngroups;
+    if (grid > w.route_blocks) grid = w.route_blocks;   // its per-block slots
+    if (grid < 1) grid = 1;
+    const size_t smem = (size_t)wrb + (size_t)kStreamWarps * kStreamBufs * bufb;
+    const bf16* xb = static_cast<const bf16*>(x);
+#define MOE_RRS(EE)                                                                           \
+  cudaFuncSetAttribute(router_route_stream_kernel<EE>,                                        \
+                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);               \
+  return launch_pdl_smem(router_route_stream_kernel<EE>, dim3((unsigned)grid),                \
+                         dim3(kStreamThreads), smem, s, xb, Wr, bias, valid, c.T, c.d, c.k,   \
+                         c.norm_topk, U, CW, wrb, bufb, L, topk, gates, cnt, psum, treal,     \
+                         done, counts, f, p, aux, zent, stats, status)
+    if (c.E == 4) { MOE_RRS(4); }
+    else if (c.E == 8) { MOE_RRS(8); }
+    else { MOE_RRS(16); }
+#undef MOE_RRS
+  }
   const size_t smem = wr_smem_bytes(c.d, c.E);
   char* acc = ws + w.route_done;
   cudaError_t err = cudaMemsetAsync(acc, 0, kRouteAccBytes, s);

@@ -213,16 +213,27 @@ def _exact(a):
     return a
 
 
-def swiglu_parts(xr, Wg, Wu, Wd, rnd=None):
+def _store(rnd, point, v, where):
+    """The value kept at storage point ``point`` ("h", "a", "b", "d_out",
+    "da", "db"): ``rnd(v)``, or ``rnd.store(point, v, where)`` when the hook
+    has that method (``where`` names the rows: expert e, slot j, token rows,
+    or shared=True).  No arithmetic happens here."""
+    if rnd is None:
+        return v
+    if hasattr(rnd, "store"):
+        return rnd.store(point, v, where)
+    return rnd(v)
+
+
+def swiglu_parts(xr, Wg, Wu, Wd, rnd=None, where=None):
     """One SwiGLU FFN on rows xr: a = xr Wg^T, b = xr Wu^T,
     h = silu(a) * b, out = h Wd^T.  Returns (out, a, b, h).
 
     ``rnd`` (default: none) rounds the stored hidden h before the down
     projection; it models a storage precision, the arithmetic is unchanged."""
-    rnd = rnd or _exact
     a = xr @ Wg.T
     b = xr @ Wu.T
-    h = rnd(silu(a) * b)
+    h = _store(rnd, "h", silu(a) * b, where)
     return h @ Wd.T, a, b, h
 
 
@@ -234,22 +245,20 @@ def swiglu_backward(dh, a, b):
     return dh * b * sa * (1.0 + a * (1.0 - sa)), dh * silu(a)
 
 
-def stored_d_out(g, dY, rnd=None):
+def stored_d_out(g, dY, rnd=None, where=None):
     """d_out = g dY per routed row, as kept between the combine backward and
     the expert products: one storage rounding ``rnd`` of the product (none by
     default)."""
-    rnd = rnd or _exact
-    return rnd(g[:, None] * dY)
+    return _store(rnd, "d_out", g[:, None] * dY, where)
 
 
-def stored_swiglu_backward(dh, a, b, rnd=None):
+def stored_swiglu_backward(dh, a, b, rnd=None, where=None):
     """(da, db) as kept for the dX and dW products: the chain rule of
     :func:`swiglu_backward` taken on the stored pre-activations rnd(a) and
     rnd(b), and each result stored once more (rnd).  dh itself is not stored:
     it is the dH product's unrounded result."""
-    rnd = rnd or _exact
-    da, db = swiglu_backward(dh, rnd(a), rnd(b))
-    return rnd(da), rnd(db)
+    da, db = swiglu_backward(dh, _store(rnd, "a", a, where), _store(rnd, "b", b, where))
+    return _store(rnd, "da", da, where), _store(rnd, "db", db, where)
 
 
 def split_gu(W_gu):
@@ -279,12 +288,14 @@ def experts_forward(x, topk_idx, gates, W_gu, W_down, Ws_gu=None, Ws_down=None,
         for e in range(E):
             rows = np.nonzero(idx[:, j] == e)[0]
             if rows.size:
-                routed[rows, j], *_ = swiglu_parts(x[rows], Wg[e], Wu[e], W_down[e], rnd)
+                routed[rows, j], *_ = swiglu_parts(x[rows], Wg[e], Wu[e], W_down[e], rnd,
+                                                   dict(e=e, j=j, rows=rows))
     y = np.einsum("tj,tjd->td", g, routed)
     real = np.ones(T, dtype=bool) if valid is None else (np.asarray(_np(valid)) != 0)
     if Ws_gu is not None:
         sg, su = split_gu(_f64(Ws_gu))
-        shared, *_ = swiglu_parts(x[real], sg, su, _f64(Ws_down), rnd)
+        shared, *_ = swiglu_parts(x[real], sg, su, _f64(Ws_down), rnd,
+                                  dict(shared=True, rows=np.nonzero(real)[0]))
         y[real] += shared
     y[~real] = 0.0
     return y, routed
@@ -375,14 +386,15 @@ def backward(x, Wr, W_gu, W_down, Ws_gu, Ws_down, fwd, dY, norm_topk=True,
     dWs_gu, dWs_down (or None), d_logits [T][E], dg [T][k].
 
     ``rnd`` (default: none) rounds the values a bf16-storage implementation
-    keeps between its matrix products -- the hidden h (:func:`swiglu_parts`),
+    keeps between its matrix products (see :func:`_store` for a hook that
+    also receives the storage point and rows) -- the hidden h
+    (:func:`swiglu_parts`),
     d_out = g dY of the routed rows (:func:`stored_d_out`), the saved
     pre-activations a and b and the results (da, db) of the SwiGLU chain rule
     (:func:`stored_swiglu_backward`) -- without changing any arithmetic step.
     The shared expert's d_out is dY itself (an input, not rounded again).
     With ``rnd`` None this is the exact gradient.
     """
-    rnd = rnd or _exact
     x = _f64(x); Wr = _f64(Wr); W_gu = _f64(W_gu); W_down = _f64(W_down)
     dY = _f64(dY)
     idx = fwd["topk_idx"]; g = fwd["gates"]; real = fwd["real"]
@@ -402,10 +414,11 @@ def backward(x, Wr, W_gu, W_down, Ws_gu, Ws_down, fwd, dY, norm_topk=True,
             if not rows.size:
                 continue
             xr = x[rows]
-            out, a, b, h = swiglu_parts(xr, Wg[e], Wu[e], W_down[e], rnd)
+            where = dict(e=e, j=j, rows=rows)
+            out, a, b, h = swiglu_parts(xr, Wg[e], Wu[e], W_down[e], rnd, where)
             dg[rows, j] = (dY[rows] * out).sum(axis=1)
-            d_out = stored_d_out(g[rows, j], dY[rows], rnd)
-            da, db = stored_swiglu_backward(d_out @ W_down[e], a, b, rnd)
+            d_out = stored_d_out(g[rows, j], dY[rows], rnd, where)
+            da, db = stored_swiglu_backward(d_out @ W_down[e], a, b, rnd, where)
             dx[rows] += da @ Wg[e] + db @ Wu[e]
             dW_down[e] += d_out.T @ h
             dW_gu[e, :H] += da.T @ xr
@@ -416,8 +429,9 @@ def backward(x, Wr, W_gu, W_down, Ws_gu, Ws_down, fwd, dY, norm_topk=True,
         sg, su = split_gu(Ws_gu_)
         rows = np.nonzero(real)[0]
         xr = x[rows]
-        out, a, b, h = swiglu_parts(xr, sg, su, Ws_down_, rnd)
-        da, db = stored_swiglu_backward(dY[rows] @ Ws_down_, a, b, rnd)
+        where = dict(shared=True, rows=rows)
+        out, a, b, h = swiglu_parts(xr, sg, su, Ws_down_, rnd, where)
+        da, db = stored_swiglu_backward(dY[rows] @ Ws_down_, a, b, rnd, where)
         dx[rows] += da @ sg + db @ su
         Hs = sg.shape[0]
         dWs_gu = np.zeros_like(Ws_gu_)

@@ -8,7 +8,8 @@ import torch
 from mixture_experts_ffn_02_gb300 import synth
 from mixture_experts_ffn_02_gb300.binding import Layer
 from oracle import moe_oracle as O
-from moe_check import Checker, bf16_round, logit_error_bound, np64, reconcile_selection
+from moe_check import (AdoptStored, Checker, logit_error_bound, np64, padded_layout,
+                       reconcile_selection, stored_from_layer)
 
 pytestmark = pytest.mark.gpu
 
@@ -43,14 +44,17 @@ def _check_against_oracle(s, inp, lay):
     np.testing.assert_array_equal(lay.bufs["counts"].cpu().numpy(), r["counts"])
     y = O.experts_forward(inp["x"], r["topk_idx"], r["gates"], inp["W_gu"], inp["W_down"],
                           inp["Ws_gu"], inp["Ws_down"], inp["valid"])[0]
+    rop = padded_layout(r["topk_idx"], s.E)[2]
+    adopt = AdoptStored(stored_from_layer(lay, True), rop, s.k)
     yi = O.experts_forward(inp["x"], r["topk_idx"], r["gates"], inp["W_gu"], inp["W_down"],
-                           inp["Ws_gu"], inp["Ws_down"], inp["valid"], rnd=bf16_round)[0]
+                           inp["Ws_gu"], inp["Ws_down"], inp["valid"], rnd=adopt)[0]
     fwd = dict(r, real=real)
     bargs = (inp["x"], inp["Wr"], inp["W_gu"], inp["W_down"], inp["Ws_gu"], inp["Ws_down"], fwd,
              inp["dY"])
     ex = O.backward(*bargs, norm_topk=bool(s.norm_topk), aux_coef=s.aux_coef)
-    idl = O.backward(*bargs, norm_topk=bool(s.norm_topk), aux_coef=s.aux_coef, rnd=bf16_round)
+    idl = O.backward(*bargs, norm_topk=bool(s.norm_topk), aux_coef=s.aux_coef, rnd=adopt)
     chk = Checker()
+    adopt.check(chk)
     if np.any(y):
         chk.layer("y", lay.bufs["y"], y, yi)
     names = ["d_logits", "dW_down", "dW_gu", "dx", "dWr"] + (

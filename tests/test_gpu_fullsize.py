@@ -19,17 +19,14 @@ import torch
 from mixture_experts_ffn_02_gb300 import synth
 from mixture_experts_ffn_02_gb300.binding import Layer
 from oracle import moe_oracle as O
-from moe_check import (Checker, assert_route_matches, bf16_round, logit_error_bound, np64,
-                       padded_layout, reconcile_selection, route_on_gpu_logits)
+from moe_check import (AdoptStored, Checker, assert_route_matches, logit_error_bound, np64,
+                       padded_layout, reconcile_selection, route_on_gpu_logits,
+                       stored_from_layer)
 
 pytestmark = pytest.mark.gpu
 
 N_TOK = 48
 N_COL = 16
-
-
-def _ident(a):
-    return a
 
 
 def run_bench_sequence(s):
@@ -93,7 +90,11 @@ def test_full_size_layer(cfg):
     fwd = dict(topk_idx=r["topk_idx"][ts], gates=r["gates"][ts], probs=probs[ts],
                real=sub_real, f=r["f"])
     xs = inp["x"][tsc]
-    for name, rnd in (("exact", None), ("ideal", bf16_round)):
+    # the storage-rounded oracle, continuing from the GPU's stored values
+    # where they are the other valid rounding (moe_check.AdoptStored)
+    stored = stored_from_layer(lay, True)
+    adopt = AdoptStored(stored, row_of_pair, s.k, tokens=ts)
+    for name, rnd in (("exact", None), ("ideal", adopt)):
         y_s, _ = O.experts_forward(xs, fwd["topk_idx"], fwd["gates"], inp["W_gu"],
                                    inp["W_down"], inp["Ws_gu"], inp["Ws_down"],
                                    sub_real.astype(np.uint8), rnd=rnd)
@@ -104,11 +105,14 @@ def test_full_size_layer(cfg):
     args = (xs, inp["Wr"], inp["W_gu"], inp["W_down"], inp["Ws_gu"], inp["Ws_down"], fwd,
             inp["dY"][tsc])
     ex = O.backward(*args, norm_topk=bool(s.norm_topk), aux_coef=coef)
-    idl = O.backward(*args, norm_topk=bool(s.norm_topk), aux_coef=coef, rnd=bf16_round)
+    idl = O.backward(*args, norm_topk=bool(s.norm_topk), aux_coef=coef, rnd=adopt)
     chk.layer("dx[sample]", g["dx"][tsd], ex["dx"], idl["dx"])
     chk.layer("d_logits[sample]", g["d_logits"][tsd], ex["d_logits"], idl["d_logits"])
+    adopt.check(chk)
 
-    # ---- one expert's weight gradients on sampled columns / hidden units
+    # ---- one expert's weight gradients on sampled columns / hidden units:
+    # the expert's rows in segment order, the same products as the oracle's
+    # backward (storage points through the same hook)
     counts = r["counts"]
     e = int(np.argsort(counts)[len(counts) // 2])
     seg = O.permute(r["topk_idx"], s.E)[1][offsets[e]:offsets[e + 1]]
@@ -118,42 +122,50 @@ def test_full_size_layer(cfg):
     Wd = np64(inp["W_down"][e])
     dY = np64(inp["dY"])
     J = np.sort(rng.choice(s.H, size=N_COL, replace=False))
+    adopt_e = AdoptStored(stored_from_layer(lay, True, cols=J), row_of_pair, s.k)
     res = {}
-    for name, rnd in (("exact", _ident), ("ideal", bf16_round)):
+    for name, rnd in (("exact", None), ("ideal", adopt_e)):
         xe = x[tok]
-        a = xe @ Wg[J].T
-        bb = xe @ Wu[J].T
-        h = rnd(O.silu(a) * bb)
-        d_out = rnd(gate[:, None] * dY[tok])
-        dWd = d_out.T @ h                                    # dW_down[e][:, J]
-        da, db = O.swiglu_backward(d_out @ Wd[:, J], rnd(a), rnd(bb))
-        dWg = rnd(da).T @ xe                                 # dW_gu[e][J, :]
-        dWu = rnd(db).T @ xe                                 # dW_gu[e][H+J, :]
+        dWd = np.zeros((s.d, N_COL)); dWg = np.zeros((N_COL, s.d)); dWu = np.zeros((N_COL, s.d))
+        for j in range(s.k):                       # the oracle's groups: (expert, slot)
+            m = slot == j
+            if not m.any():
+                continue
+            where = dict(e=e, j=j, rows=tok[m])
+            _, a, bb, h = O.swiglu_parts(xe[m], Wg[J], Wu[J], Wd[:, J], rnd, where)
+            d_out = O.stored_d_out(gate[m], dY[tok[m]], rnd, where)
+            da, db = O.stored_swiglu_backward(d_out @ Wd[:, J], a, bb, rnd, where)
+            dWd += d_out.T @ h                       # dW_down[e][:, J]
+            dWg += da.T @ xe[m]                      # dW_gu[e][J, :]
+            dWu += db.T @ xe[m]                      # dW_gu[e][H+J, :]
         res[name] = (dWd, dWg, dWu)
     gWd = g["dW_down"][e][:, torch.from_numpy(J).cuda()]
     gWg = g["dW_gu"][e][torch.from_numpy(J).cuda()]
     gWu = g["dW_gu"][e][torch.from_numpy(J + s.H).cuda()]
     for nm, gv, k_ in (("dW_down[e]", gWd, 0), ("dW_gate[e]", gWg, 1), ("dW_up[e]", gWu, 2)):
         chk.layer(nm, gv, res["exact"][k_], res["ideal"][k_])
+    adopt_e.check(chk)
 
     if s.n_shared:
         Hs = s.Hs_total
         Js = np.sort(rng.choice(Hs, size=N_COL, replace=False))
         sg, su = O.split_gu(np64(inp["Ws_gu"]))
         Sd = np64(inp["Ws_down"])
-        xr, dYr = x[real], dY[real]
+        rows = np.nonzero(real)[0]
+        xr, dYr = x[rows], dY[rows]
+        adopt_s = AdoptStored(stored_from_layer(lay, True, shared_cols=Js), row_of_pair, s.k)
         res = {}
-        for name, rnd in (("exact", _ident), ("ideal", bf16_round)):
-            a = xr @ sg[Js].T
-            bb = xr @ su[Js].T
-            h = rnd(O.silu(a) * bb)
-            da, db = O.swiglu_backward(dYr @ Sd[:, Js], rnd(a), rnd(bb))
-            res[name] = (dYr.T @ h, rnd(da).T @ xr, rnd(db).T @ xr)
+        for name, rnd in (("exact", None), ("ideal", adopt_s)):
+            where = dict(shared=True, rows=rows)
+            _, a, bb, h = O.swiglu_parts(xr, sg[Js], su[Js], Sd[:, Js], rnd, where)
+            da, db = O.stored_swiglu_backward(dYr @ Sd[:, Js], a, bb, rnd, where)
+            res[name] = (dYr.T @ h, da.T @ xr, db.T @ xr)
         jt = torch.from_numpy(Js).cuda()
         for nm, gv, k_ in (("dWs_down", g["dWs_down"][:, jt], 0),
                            ("dWs_gate", g["dWs_gu"][jt], 1),
                            ("dWs_up", g["dWs_gu"][jt + Hs], 2)):
             chk.layer(nm, gv, res["exact"][k_], res["ideal"][k_])
+        adopt_s.check(chk)
 
     # ---- dW_r = x^T d_logits (identity at any size)
     dWr_id = x.T @ np64(g["d_logits"])

@@ -9,8 +9,9 @@ import torch
 from mixture_experts_ffn_02_gb300 import synth
 from mixture_experts_ffn_02_gb300.binding import Layer
 from oracle import moe_oracle as O
-from moe_check import (Checker, assert_close, assert_route_matches, bf16_round,
-                       logit_error_bound, np64, reconcile_selection, route_on_gpu_logits)
+from moe_check import (AdoptStored, Checker, assert_close, assert_route_matches,
+                       logit_error_bound, np64, padded_layout, reconcile_selection,
+                       route_on_gpu_logits, stored_from_layer)
 
 pytestmark = pytest.mark.gpu
 
@@ -68,11 +69,13 @@ def test_forward_matches_oracle(cfg, T):
     assert_route_matches(b, route_on_gpu_logits(b, inp, s.k, s.norm_topk))
     y_ref, _ = O.experts_forward(inp["x"], r["topk_idx"], r["gates"], inp["W_gu"],
                                  inp["W_down"], inp["Ws_gu"], inp["Ws_down"], inp["valid"])
+    adopt = AdoptStored(stored_from_layer(lay, False), padded_layout(r["topk_idx"], s.E)[2], s.k)
     y_ideal, _ = O.experts_forward(inp["x"], r["topk_idx"], r["gates"], inp["W_gu"],
                                    inp["W_down"], inp["Ws_gu"], inp["Ws_down"], inp["valid"],
-                                   rnd=bf16_round)
+                                   rnd=adopt)
     chk = Checker()
     chk.layer("y", b["y"], y_ref, y_ideal)
+    adopt.check(chk)
     chk.done()
 
 
@@ -89,7 +92,8 @@ def test_backward_matches_oracle(cfg, T, norm_topk):
     args = (inp["x"], inp["Wr"], inp["W_gu"], inp["W_down"], inp["Ws_gu"], inp["Ws_down"],
             fwd, inp["dY"])
     ref = O.backward(*args, norm_topk=bool(norm_topk), aux_coef=s.aux_coef)
-    ideal = O.backward(*args, norm_topk=bool(norm_topk), aux_coef=s.aux_coef, rnd=bf16_round)
+    adopt = AdoptStored(stored_from_layer(lay, True), padded_layout(r["topk_idx"], s.E)[2], s.k)
+    ideal = O.backward(*args, norm_topk=bool(norm_topk), aux_coef=s.aux_coef, rnd=adopt)
     g = lay.grads
     chk = Checker()
     names = ["d_logits", "dW_down", "dW_gu", "dx", "dWr"]
@@ -97,6 +101,7 @@ def test_backward_matches_oracle(cfg, T, norm_topk):
         names += ["dWs_down", "dWs_gu"]
     for n in names:
         chk.layer(n, g[n], ref[n], ideal[n])
+    adopt.check(chk)
     chk.done()
     if inp["valid"] is not None:
         pad = inp["valid"] == 0

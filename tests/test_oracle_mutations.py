@@ -104,8 +104,8 @@ def test_shared_expert_gated_is_caught(monkeypatch):
     orig = O.swiglu_parts
     calls = {"n": 0}
 
-    def swiglu_half_shared(xr, Wg, Wu, Wd, rnd=None):
-        out, a, b, h = orig(xr, Wg, Wu, Wd, rnd)
+    def swiglu_half_shared(xr, Wg, Wu, Wd, rnd=None, where=None):
+        out, a, b, h = orig(xr, Wg, Wu, Wd, rnd, where)
         # the shared expert is the call with the concatenated shared weights:
         # scale it as if it had a gate of 1/2
         if Wg.shape[0] == getattr(swiglu_half_shared, "Hs", -1):
@@ -216,8 +216,8 @@ def _values_fail(monkeypatch):
 
 def test_unrounded_hidden_is_caught(monkeypatch):
     orig = O.swiglu_parts
-    monkeypatch.setattr(O, "swiglu_parts", lambda xr, Wg, Wu, Wd, rnd=None:
-                        orig(xr, Wg, Wu, Wd, None))
+    monkeypatch.setattr(O, "swiglu_parts", lambda xr, Wg, Wu, Wd, rnd=None, where=None:
+                        orig(xr, Wg, Wu, Wd, None, where))
     assert _storage_pins_fail()
     assert _values_fail(monkeypatch)
 
@@ -225,8 +225,8 @@ def test_unrounded_hidden_is_caught(monkeypatch):
 def test_rounded_expert_output_is_caught(monkeypatch):
     orig = O.swiglu_parts
 
-    def parts(xr, Wg, Wu, Wd, rnd=None):
-        out, a, b, h = orig(xr, Wg, Wu, Wd, rnd)
+    def parts(xr, Wg, Wu, Wd, rnd=None, where=None):
+        out, a, b, h = orig(xr, Wg, Wu, Wd, rnd, where)
         return (rnd(out) if rnd else out), a, b, h
     monkeypatch.setattr(O, "swiglu_parts", parts)
     assert _storage_pins_fail()
@@ -234,21 +234,21 @@ def test_rounded_expert_output_is_caught(monkeypatch):
 
 
 def test_unrounded_d_out_is_caught(monkeypatch):
-    monkeypatch.setattr(O, "stored_d_out", lambda g, dY, rnd=None: g[:, None] * dY)
+    monkeypatch.setattr(O, "stored_d_out", lambda g, dY, rnd=None, where=None: g[:, None] * dY)
     assert _storage_pins_fail()
     assert _values_fail(monkeypatch)
 
 
 def test_dh_rounded_before_the_chain_rule_is_caught(monkeypatch):
     orig = O.stored_swiglu_backward
-    monkeypatch.setattr(O, "stored_swiglu_backward", lambda dh, a, b, rnd=None:
-                        orig(rnd(dh) if rnd else dh, a, b, rnd))
+    monkeypatch.setattr(O, "stored_swiglu_backward", lambda dh, a, b, rnd=None, where=None:
+                        orig(rnd(dh) if rnd else dh, a, b, rnd, where))
     assert _storage_pins_fail()
     assert _values_fail(monkeypatch)
 
 
 def test_dh_rounded_instead_of_da_db_is_caught(monkeypatch):
-    def moved(dh, a, b, rnd=None):
+    def moved(dh, a, b, rnd=None, where=None):
         r = rnd or (lambda v: v)
         return O.swiglu_backward(r(dh), r(a), r(b))
     monkeypatch.setattr(O, "stored_swiglu_backward", moved)
@@ -257,7 +257,7 @@ def test_dh_rounded_instead_of_da_db_is_caught(monkeypatch):
 
 
 def test_unrounded_saved_preactivations_are_caught(monkeypatch):
-    def exact_ab(dh, a, b, rnd=None):
+    def exact_ab(dh, a, b, rnd=None, where=None):
         r = rnd or (lambda v: v)
         da, db = O.swiglu_backward(dh, a, b)
         return r(da), r(db)
@@ -267,7 +267,7 @@ def test_unrounded_saved_preactivations_are_caught(monkeypatch):
 
 
 def test_unrounded_da_db_are_caught(monkeypatch):
-    def no_store(dh, a, b, rnd=None):
+    def no_store(dh, a, b, rnd=None, where=None):
         r = rnd or (lambda v: v)
         return O.swiglu_backward(dh, r(a), r(b))
     monkeypatch.setattr(O, "stored_swiglu_backward", no_store)

@@ -47,6 +47,19 @@ class Spy:
         return q8(v)
 
 
+class NamedSpy:
+    """The same rounding through the hook's store() form, recording which
+    storage point and which rows each value belongs to."""
+
+    def __init__(self):
+        self.points = []
+
+    def store(self, point, v, where):
+        self.points.append((point, "shared" if where.get("shared") else
+                            (where["e"], where["j"]), tuple(where["rows"].tolist())))
+        return q8(v)
+
+
 X = np.array([[1.0]])
 WR = np.array([[math.log(3.0), 0.0]])
 W_GU = np.array([[[1.3], [1.7]],          # expert 0: gate 1.3, up 1.7
@@ -143,3 +156,22 @@ def test_stored_values_by_hand():
     np.testing.assert_allclose([HS_PRE, DAS_PRE, DBS_PRE], [1.8156294555, -0.6825692215,
                                                             -0.2675229985], rtol=1e-9)
     assert Y == 2.1 or abs(Y - 2.1) < 1e-14
+
+
+def test_storage_points_are_named_with_their_rows():
+    """The store() form of the hook sees each storage point once per group
+    of rows: routed expert 0, slot 0, token 0 -- h, d_out, a, b, da, db --
+    and the shared expert on token 0 -- h, a, b, da, db (no d_out: dY)."""
+    r = _forward()
+    spy = NamedSpy()
+    O.backward(X, WR, W_GU, W_DOWN, WS_GU, WS_DOWN, r, DY, norm_topk=False, aux_coef=0.0,
+               rnd=spy)
+    routed = sorted(p for p, w, rows in spy.points if w == (0, 0) and rows == (0,))
+    shared = sorted(p for p, w, rows in spy.points if w == "shared" and rows == (0,))
+    assert routed == sorted(["h", "d_out", "a", "b", "da", "db"])
+    assert shared == sorted(["h", "a", "b", "da", "db"])
+    assert len(spy.points) == 11
+    spy = NamedSpy()
+    O.experts_forward(X, r["topk_idx"], r["gates"], W_GU, W_DOWN, WS_GU, WS_DOWN, rnd=spy)
+    assert sorted(map(repr, spy.points)) == sorted(map(repr, [("h", (0, 0), (0,)),
+                                                              ("h", "shared", (0,))]))
