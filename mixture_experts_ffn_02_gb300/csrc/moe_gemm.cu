@@ -125,7 +125,7 @@ struct Shared {
   uint32_t tmem_base;
   int abort_flag;
   int roff[257];               // padded segment offsets (row-grouped kinds)
-  int ppre[257];               // CTA pairs: 256-row tiles before expert e
+  int ppre[257];               // CTA pairs: 256-row tiles before expert e (GK_DW: expert order)
 };
 static_assert(sizeof(Shared) <= SHARED_RESERVE, "bookkeeping too large");
 
@@ -172,8 +172,9 @@ __device__ __forceinline__ Tile get_tile(const Params& p, const Shared& sh, int 
   if (KIND == GK_DW) {
     const int m_units = (p.Mdw + BM * CG - 1) / (BM * CG);
     const int per_e = m_units * p.n_tiles;
-    t.e = idx / per_e;
-    const int r = idx - t.e * per_e;
+    const int pos = idx / per_e;                  // position in the heaviest-first order
+    t.e = p.row_offsets ? sh.ppre[pos] : pos;
+    const int r = idx - pos * per_e;
     t.m0 = (r / p.n_tiles) * BM * CG;
     t.n0 = (r % p.n_tiles) * BN;
     int k0, k1;
@@ -718,6 +719,22 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       carry += __shfl_sync(0xffffffffu, v, 31);
     }
     if (lane == 0) sh.ppre[0] = 0;
+  }
+  if (KIND == GK_DW && p.row_offsets) {
+    // Heaviest experts first: the dW tiles are taken in the order of their
+    // expert's segment length (the tile's K), longest first, equal lengths
+    // in index order (ppre, unused by this kind, holds that order).  Unit u
+    // takes tiles u, u + nunits, ..., so the long K loops of skewed experts
+    // are spread over the units first and the short ones fill in behind.
+    for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
+      const int le = sh.roff[e + 1] - sh.roff[e];
+      int r = 0;
+      for (int f = 0; f < p.E; ++f) {
+        const int lf = sh.roff[f + 1] - sh.roff[f];
+        r += (lf > le) || (lf == le && f < e);
+      }
+      sh.ppre[r] = e;
+    }
   }
   // barriers of both CTAs initialised (the pair signals across CTAs)
   if (CG == 2) cluster_sync();

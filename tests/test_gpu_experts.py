@@ -9,7 +9,7 @@ import torch
 from mixture_experts_ffn_02_gb300 import synth
 from mixture_experts_ffn_02_gb300.binding import Layer
 from oracle import moe_oracle as O
-from moe_check import Checker, bf16_round, np64, padded_layout
+from moe_check import AdoptStored, Checker, np64, padded_layout, stored_from_layer
 
 pytestmark = pytest.mark.gpu
 
@@ -68,14 +68,20 @@ def test_expert_gemms_and_combine(name, T, d, E, k, H, ns, Hs, pad, skew, pairs,
     Wd = np64(inp["W_down"])
     h_ref = np.zeros((R, H)); a_ref = np.zeros((R, H)); b_ref = np.zeros((R, H))
     o_ref = np.zeros((R, d)); o_ideal = np.zeros((R, d))
-    for e in range(E):
-        rows = np.arange(row_offsets[e], row_offsets[e] + offsets[e + 1] - offsets[e])
-        if rows.size == 0:
-            continue
-        toks = perm_padded[rows] // k
-        out, a, b, h = O.swiglu_parts(x[toks], Wg[e], Wu[e], Wd[e])
-        h_ref[rows], a_ref[rows], b_ref[rows], o_ref[rows] = h, a, b, out
-        o_ideal[rows] = O.swiglu_parts(x[toks], Wg[e], Wu[e], Wd[e], bf16_round)[0]
+    # the storage-rounded oracle continuing from the GPU's valid rounding
+    # choices of h (moe_check.AdoptStored), per (slot, expert) group of rows
+    adopt = AdoptStored(stored_from_layer(lay, False), row_of_pair, k)
+    tk = topk.numpy()
+    for j in range(k):
+        for e in range(E):
+            toks = np.nonzero(tk[:, j] == e)[0]
+            if toks.size == 0:
+                continue
+            rows = row_of_pair[toks * k + j]
+            out, a, b, h = O.swiglu_parts(x[toks], Wg[e], Wu[e], Wd[e])
+            h_ref[rows], a_ref[rows], b_ref[rows], o_ref[rows] = h, a, b, out
+            o_ideal[rows] = O.swiglu_parts(x[toks], Wg[e], Wu[e], Wd[e], adopt,
+                                           dict(e=e, j=j, rows=toks))[0]
     bufs = lay.bufs
     chk = Checker()
     chk.close("h", bufs["h"][:R], h_ref)
@@ -91,16 +97,17 @@ def test_expert_gemms_and_combine(name, T, d, E, k, H, ns, Hs, pad, skew, pairs,
                                  inp["W_down"], inp["Ws_gu"], inp["Ws_down"], vnp)
     y_ideal, _ = O.experts_forward(inp["x"], topk.numpy(), g.numpy(), inp["W_gu"],
                                    inp["W_down"], inp["Ws_gu"], inp["Ws_down"], vnp,
-                                   rnd=bf16_round)
+                                   rnd=adopt)
     if ns:
         sg, su = O.split_gu(np64(inp["Ws_gu"]))
-        s_ref, *_ = O.swiglu_parts(x, sg, su, np64(inp["Ws_down"]))
-        s_ideal, *_ = O.swiglu_parts(x, sg, su, np64(inp["Ws_down"]), bf16_round)
-        if valid is not None:
-            s_ref[vnp == 0] = 0
-            s_ideal[vnp == 0] = 0
+        real_rows = np.arange(T) if vnp is None else np.nonzero(vnp != 0)[0]
+        s_ref = np.zeros((T, d)); s_ideal = np.zeros((T, d))
+        s_ref[real_rows], *_ = O.swiglu_parts(x[real_rows], sg, su, np64(inp["Ws_down"]))
+        s_ideal[real_rows], *_ = O.swiglu_parts(x[real_rows], sg, su, np64(inp["Ws_down"]),
+                                                adopt, dict(shared=True, rows=real_rows))
         chk.layer("s_out", bufs["s_out"], s_ref, s_ideal)
     chk.layer("y", bufs["y"], y_ref, y_ideal)
+    adopt.check(chk)
     chk.done()
     if valid is not None:
         assert (bufs["y"].cpu()[valid == 0].float() == 0).all()
@@ -138,12 +145,16 @@ def test_expert_ffn_call(name, T, d, E, k, H, ns, Hs, pad, skew):
     vnp = None if valid is None else valid.numpy()
     y_ref, _ = O.experts_forward(inp["x"], topk.numpy(), g.numpy(), inp["W_gu"],
                                  inp["W_down"], inp["Ws_gu"], inp["Ws_down"], vnp)
+    R_ = int(lay.bufs["row_offsets"][-1])
+    adopt = AdoptStored(stored_from_layer(lay, False), padded_layout(topk.numpy(), E)[2], k)
     y_ideal, _ = O.experts_forward(inp["x"], topk.numpy(), g.numpy(), inp["W_gu"],
                                    inp["W_down"], inp["Ws_gu"], inp["Ws_down"], vnp,
-                                   rnd=bf16_round)
+                                   rnd=adopt)
     chk = Checker()
     chk.layer("y", one["y"], y_ref, y_ideal)
+    adopt.check(chk)
     chk.done()
+    assert R_ == R
     for n in ("h", "out_perm", "y", "s_out"):
         if n in one:
             lay.bufs[n].fill_(3.0)
