@@ -425,19 +425,8 @@ def backward(x, Wr, W_gu, W_down, Ws_gu, Ws_down, fwd, dY, norm_topk=True,
             dW_gu[e, H:] += db.T @ xr
     dWs_gu = dWs_down = None
     if Ws_gu is not None:
-        Ws_gu_ = _f64(Ws_gu); Ws_down_ = _f64(Ws_down)
-        sg, su = split_gu(Ws_gu_)
-        rows = np.nonzero(real)[0]
-        xr = x[rows]
-        where = dict(shared=True, rows=rows)
-        out, a, b, h = swiglu_parts(xr, sg, su, Ws_down_, rnd, where)
-        da, db = stored_swiglu_backward(dY[rows] @ Ws_down_, a, b, rnd, where)
-        dx[rows] += da @ sg + db @ su
-        Hs = sg.shape[0]
-        dWs_gu = np.zeros_like(Ws_gu_)
-        dWs_gu[:Hs] = da.T @ xr
-        dWs_gu[Hs:] = db.T @ xr
-        dWs_down = dY[rows].T @ h
+        dxs, dWs_gu, dWs_down = shared_backward(x, Ws_gu, Ws_down, dY, real, rnd)
+        dx += dxs
     d_logits = router_logit_grad(dg, idx, g, fwd["probs"], norm_topk)
     d_logits += aux_logit_grad(fwd["probs"], fwd["f"], real, aux_coef)
     if z_coef:
@@ -446,6 +435,28 @@ def backward(x, Wr, W_gu, W_down, Ws_gu, Ws_down, fwd, dY, norm_topk=True,
     dWr = x.T @ d_logits
     return dict(dx=dx, dWr=dWr, dW_gu=dW_gu, dW_down=dW_down, dWs_gu=dWs_gu,
                 dWs_down=dWs_down, d_logits=d_logits, dg=dg)
+
+
+def shared_backward(x, Ws_gu, Ws_down, dY, real, rnd=None):
+    """The shared expert's part of the backward: its SwiGLU on the real
+    tokens (weight 1), d_out = dY itself.  Returns (dx contribution [T][d],
+    dWs_gu, dWs_down); storage points through ``rnd`` as in :func:`backward`."""
+    x = _f64(x); dY = _f64(dY)
+    Ws_gu_ = _f64(Ws_gu); Ws_down_ = _f64(Ws_down)
+    sg, su = split_gu(Ws_gu_)
+    rows = np.nonzero(real)[0]
+    xr = x[rows]
+    where = dict(shared=True, rows=rows)
+    out, a, b, h = swiglu_parts(xr, sg, su, Ws_down_, rnd, where)
+    da, db = stored_swiglu_backward(dY[rows] @ Ws_down_, a, b, rnd, where)
+    dx = np.zeros_like(x)
+    dx[rows] = da @ sg + db @ su
+    Hs = sg.shape[0]
+    dWs_gu = np.zeros_like(Ws_gu_)
+    dWs_gu[:Hs] = da.T @ xr
+    dWs_gu[Hs:] = db.T @ xr
+    dWs_down = dY[rows].T @ h
+    return dx, dWs_gu, dWs_down
 
 
 def objective(x, Wr, W_gu, W_down, Ws_gu, Ws_down, dY, k, bias=None, valid=None,

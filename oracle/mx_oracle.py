@@ -1,4 +1,5 @@
-"""CPU fp64 oracle of the MXFP8 expert forward.
+"""CPU fp64 oracle of the MXFP8 experts: the forward, and the training
+step whose routed experts run in MXFP8 (:func:`backward_mx`).
 
 TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only the test suite, the smoke check
 of ``__graft_entry__`` and the CPU-baseline leg of ``bench.py`` may import or
@@ -32,8 +33,10 @@ Readings (the pages say only "e4m3 values with UE8M0 per-32 block scales"):
 
 Pins: ``tests/test_oracle_mx.py`` (closed forms, torch's float8_e4m3fn
 conversion as a library routine, brute-force nearest rounding, round trips of
-representable blocks, row independence, and the dense-masked formulation of
-the MX expert sum).
+representable blocks, row independence, the dense-masked formulation of the
+MX expert sum; for the training step the reduction to the bf16 layer's
+backward when the round trip is the identity, the axis of every quantised
+operand, and a dense-masked formulation of the MX data gradients).
 """
 from __future__ import annotations
 
@@ -115,14 +118,16 @@ def mx_roundtrip(v):
 
 
 def experts_forward_mx(x, topk_idx, gates, W_gu, W_down, Ws_gu=None, Ws_down=None,
-                       valid=None):
+                       valid=None, shared_mx=True, rnd=None):
     """The expert sum of the layer with MXFP8 experts.
 
     Routed part: the permute/combine formulation of ``moe_oracle`` on the
     quantised operands Q(x), Q(W_gu) (blocks along d) and Q(W_down) (blocks
     along H), with the hidden h quantised along H before the down product.
     The shared expert is the same SwiGLU on Q(x), Q(Ws_gu), Q(Ws_down) with
-    its hidden quantised along its width, on real tokens.
+    its hidden quantised along its width, on real tokens; with shared_mx
+    False it is the bf16 layer's (exact operands, its hidden through the
+    storage hook ``rnd``), as in the MXFP8 training step (:func:`backward_mx`).
     Returns (y [T][d], routed [T][k][d])."""
     x = mo._f64(x)
     xq = mx_roundtrip(x)
@@ -132,9 +137,15 @@ def experts_forward_mx(x, topk_idx, gates, W_gu, W_down, Ws_gu=None, Ws_down=Non
     if Ws_gu is not None:
         real = np.ones(x.shape[0], dtype=bool) if valid is None else (
             np.asarray(mo._np(valid)) != 0)
-        sg, su = mo.split_gu(mx_roundtrip(mo._f64(Ws_gu)))
-        shared, *_ = mo.swiglu_parts(xq[real], sg, su, mx_roundtrip(mo._f64(Ws_down)),
-                                     rnd=mx_roundtrip)
+        if shared_mx:
+            sg, su = mo.split_gu(mx_roundtrip(mo._f64(Ws_gu)))
+            shared, *_ = mo.swiglu_parts(xq[real], sg, su, mx_roundtrip(mo._f64(Ws_down)),
+                                         rnd=mx_roundtrip)
+        else:
+            sg, su = mo.split_gu(mo._f64(Ws_gu))
+            rows = np.nonzero(real)[0]
+            shared, *_ = mo.swiglu_parts(x[real], sg, su, mo._f64(Ws_down), rnd,
+                                         dict(shared=True, rows=rows))
         y[real] += shared
     return y, routed
 
@@ -148,5 +159,106 @@ def forward_mx(x, Wr, W_gu, W_down, Ws_gu=None, Ws_down=None, k=2, bias=None,
     r = mo.route(logits, k, bias=bias, valid=valid, norm_topk=norm_topk)
     y, routed = experts_forward_mx(x, r["topk_idx"], r["gates"], W_gu, W_down, Ws_gu,
                                    Ws_down, valid)
+    r.update(y=y, routed=routed, logits=np.asarray(logits))
+    return r
+
+
+# --------------------------------------------------------------------------
+# Training step with MXFP8 routed experts
+# --------------------------------------------------------------------------
+
+def roundtrip_k(W, quant=None):
+    """Q along axis 0 of a [K][N] matrix: the operand of ``v @ W`` quantised
+    in blocks of 32 along the product's reduction axis K."""
+    quant = quant or mx_roundtrip
+    return quant(np.asarray(W, dtype=f64).T).T
+
+
+def backward_mx(x, Wr, W_gu, W_down, Ws_gu, Ws_down, fwd, dY, norm_topk=True,
+                aux_coef=0.01, rnd=None, z_coef=0.0, quant=None):
+    """Gradients of J = <dY, y> + aux_coef * aux + z_coef * z_loss for the
+    layer whose routed experts run in MXFP8, by the chain rule.
+
+    Readings (the pages name MXFP8 training of the routed experts and the
+    formats only):
+
+    * Forward of a routed expert: a = Q(x) Q(W_gate)^T, b = Q(x) Q(W_up)^T,
+      h = silu(a) b, out = Q(h) Q(W_down)^T (as :func:`experts_forward_mx`).
+    * The data-gradient products run on MXFP8 operands quantised in blocks of
+      32 along each product's reduction axis: dH = Q(d_out) Qk(W_down) with
+      d_out = g dY (reduction over d), and dx = Q(d_gu) Qk(W_gu) with
+      d_gu = [da | db] (reduction over 2H); Qk quantises a weight along the
+      axis the product sums over (:func:`roundtrip_k`).
+    * The SwiGLU chain rule takes the saved a and b, and the weight-gradient
+      products take the saved h, d_out, d_gu and x, all at the bf16 storage
+      points of the bf16 layer (``rnd``, the hook of
+      ``moe_oracle.backward``; h here is the hidden before its MX rounding).
+    * The shared expert, the router and the routing gradient are the bf16
+      layer's (``moe_oracle.backward``).
+
+    ``quant`` (default :func:`mx_roundtrip`) is the quantise-dequantise round
+    trip; with the identity it is the bf16 layer's backward.  ``fwd`` is the
+    dict of :func:`forward_mx` (routing and probs).  Returns the dict of
+    ``moe_oracle.backward``.
+    """
+    quant = quant or mx_roundtrip
+    x = mo._f64(x); Wr = mo._f64(Wr); W_gu = mo._f64(W_gu); W_down = mo._f64(W_down)
+    dY = mo._f64(dY)
+    idx = fwd["topk_idx"]; g = fwd["gates"]; real = fwd["real"]
+    T, d = x.shape
+    E, H2, _ = W_gu.shape
+    H = H2 // 2
+    k = idx.shape[1]
+    Wg, Wu = mo.split_gu(W_gu)
+    xq = quant(x)
+    dx = np.zeros((T, d))
+    dW_gu = np.zeros_like(W_gu)
+    dW_down = np.zeros_like(W_down)
+    dg = np.zeros((T, k))
+    for j in range(k):
+        for e in range(E):
+            rows = np.nonzero(idx[:, j] == e)[0]
+            if not rows.size:
+                continue
+            where = dict(e=e, j=j, rows=rows)
+            a = xq[rows] @ quant(Wg[e]).T
+            b = xq[rows] @ quant(Wu[e]).T
+            hf = mo.silu(a) * b
+            out = quant(hf) @ quant(W_down[e]).T
+            dg[rows, j] = (dY[rows] * out).sum(axis=1)
+            h = mo._store(rnd, "h", hf, where)
+            d_out = mo.stored_d_out(g[rows, j], dY[rows], rnd, where)
+            dH = quant(d_out) @ roundtrip_k(W_down[e], quant)
+            da, db = mo.stored_swiglu_backward(dH, a, b, rnd, where)
+            d_gu = np.concatenate([da, db], axis=1)
+            dx[rows] += quant(d_gu) @ roundtrip_k(W_gu[e], quant)
+            dW_down[e] += d_out.T @ h
+            dW_gu[e, :H] += da.T @ x[rows]
+            dW_gu[e, H:] += db.T @ x[rows]
+    # the shared expert, the router and the routing gradient: the bf16 layer's
+    dWs_gu = dWs_down = None
+    if Ws_gu is not None:
+        dxs, dWs_gu, dWs_down = mo.shared_backward(x, Ws_gu, Ws_down, dY, real, rnd)
+        dx += dxs
+    d_logits = mo.router_logit_grad(dg, idx, g, fwd["probs"], norm_topk)
+    d_logits += mo.aux_logit_grad(fwd["probs"], fwd["f"], real, aux_coef)
+    if z_coef:
+        d_logits += mo.z_logit_grad(fwd["logits"], real, z_coef)
+    dx += d_logits @ Wr.T
+    dWr = x.T @ d_logits
+    return dict(dx=dx, dWr=dWr, dW_gu=dW_gu, dW_down=dW_down, dWs_gu=dWs_gu,
+                dWs_down=dWs_down, d_logits=d_logits, dg=dg)
+
+
+def forward_mx_train(x, Wr, W_gu, W_down, Ws_gu=None, Ws_down=None, k=2, bias=None,
+                     valid=None, norm_topk=True, logits=None, rnd=None):
+    """The forward of the MXFP8 training step: the routed experts in MXFP8,
+    the shared expert in bf16 (:func:`experts_forward_mx` with shared_mx
+    False), router and route unchanged."""
+    if logits is None:
+        logits = mo.router_logits(x, Wr).astype(np.float32)
+    r = mo.route(logits, k, bias=bias, valid=valid, norm_topk=norm_topk)
+    y, routed = experts_forward_mx(x, r["topk_idx"], r["gates"], W_gu, W_down, Ws_gu,
+                                   Ws_down, valid, shared_mx=False, rnd=rnd)
     r.update(y=y, routed=routed, logits=np.asarray(logits))
     return r

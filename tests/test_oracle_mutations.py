@@ -276,11 +276,42 @@ def test_unrounded_da_db_are_caught(monkeypatch):
 
 
 def test_rounded_shared_dY_is_caught(monkeypatch):
-    src = inspect.getsource(O.backward)
+    src = inspect.getsource(O.shared_backward)
     needle = "stored_swiglu_backward(dY[rows] @ Ws_down_"
     assert needle in src
     ns = dict(vars(O))
     exec(src.replace(needle, "stored_swiglu_backward(rnd(dY[rows]) @ Ws_down_"), ns)
-    monkeypatch.setattr(O, "backward", ns["backward"])
+    monkeypatch.setattr(O, "shared_backward", ns["shared_backward"])
     assert _storage_pins_fail()
     assert _values_fail(monkeypatch)
+
+
+# ---- the MXFP8 training step (tests/test_oracle_mx.py)
+
+import test_oracle_mx as MXP  # noqa: E402
+from oracle import mx_oracle as M  # noqa: E402
+
+
+def test_mx_dgrad_weights_quantised_along_the_wrong_axis_are_caught(monkeypatch):
+    monkeypatch.setattr(M, "roundtrip_k", lambda W, quant=None:
+                        (quant or M.mx_roundtrip)(np.asarray(W, dtype=np.float64)))
+    assert _fails(MXP.test_mx_backward_quantises_each_operand_along_its_reduction_axis)
+    assert _fails(MXP.test_mx_backward_dense_masked_formulation)
+
+
+def test_mx_dgrad_unquantised_d_gu_is_caught(monkeypatch):
+    src = inspect.getsource(M.backward_mx)
+    needle = "dx[rows] += quant(d_gu) @"
+    assert needle in src
+    ns = dict(vars(M))
+    exec(src.replace(needle, "dx[rows] += d_gu @"), ns)
+    monkeypatch.setattr(M, "backward_mx", ns["backward_mx"])
+    assert _fails(MXP.test_mx_backward_quantises_each_operand_along_its_reduction_axis)
+    assert _fails(MXP.test_mx_backward_dense_masked_formulation)
+
+
+def test_mx_training_shared_expert_in_mx_is_caught(monkeypatch):
+    orig = M.experts_forward_mx
+    monkeypatch.setattr(M, "experts_forward_mx", lambda *a, shared_mx=True, rnd=None, **k:
+                        orig(*a, shared_mx=True, rnd=rnd, **k))
+    assert _fails(MXP.test_mx_training_forward_has_the_bf16_shared_expert)

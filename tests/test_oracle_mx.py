@@ -219,3 +219,139 @@ def test_mx_experts_exact_on_representable_operands():
 def test_mx_rejects_ragged_blocks():
     with pytest.raises(ValueError):
         M.mx_quantize(np.ones((2, 48)))
+
+
+# ------------------------------------------------ MX training step (backward)
+
+def _bf16(a):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float64)).to(
+        torch.bfloat16).double().numpy()
+
+
+def _train_case(seed, T=20, d=64, E=4, k=2, H=96, shared=True, norm=True):
+    """A tiny layer whose sizes are all different (d, H, 2H, rows), so a
+    quantised operand's last axis tells which product it serves."""
+    rng = _rng(seed)
+    x = rng.standard_normal((T, d))
+    Wr = rng.standard_normal((d, E)) * 0.3
+    W_gu = rng.standard_normal((E, 2 * H, d)) * 0.2
+    W_down = rng.standard_normal((E, d, H)) * 0.2
+    Ws_gu = rng.standard_normal((2 * H, d)) * 0.2 if shared else None
+    Ws_down = rng.standard_normal((d, H)) * 0.2 if shared else None
+    dY = rng.standard_normal((T, d))
+    fwd = M.forward_mx_train(x, Wr, W_gu, W_down, Ws_gu, Ws_down, k=k, norm_topk=norm)
+    return x, Wr, W_gu, W_down, Ws_gu, Ws_down, dY, fwd
+
+
+@pytest.mark.parametrize("norm", [True, False])
+def test_mx_backward_is_the_bf16_backward_with_bf16_rounding(norm):
+    """With the MX round trip replaced by a bf16 round trip and inputs that
+    bf16 holds exactly, the MX training step's backward is the bf16 layer's
+    backward (pinned by finite differences and the storage pins), term for
+    term: Q(h) in the down product plays the bf16 layer's stored h, and the
+    other quantised operands are bf16 values already."""
+    x, Wr, W_gu, W_down, Ws_gu, Ws_down, dY, fwd = _train_case(7, norm=norm)
+    x, W_gu, W_down, Ws_gu, Ws_down, dY = map(_bf16, (x, W_gu, W_down, Ws_gu, Ws_down, dY))
+    fwd = M.forward_mx_train(x, Wr, W_gu, W_down, Ws_gu, Ws_down, k=2, norm_topk=norm)
+    args = (x, Wr, W_gu, W_down, Ws_gu, Ws_down, fwd, dY)
+    got = M.backward_mx(*args, norm_topk=norm, rnd=_bf16, quant=_bf16)
+    ref = O.backward(*args, norm_topk=norm, rnd=_bf16)
+    for n in ("dx", "dWr", "dW_gu", "dW_down", "dWs_gu", "dWs_down", "d_logits", "dg"):
+        np.testing.assert_allclose(got[n], ref[n], rtol=1e-12, atol=1e-12, err_msg=n)
+
+
+def test_mx_training_forward_has_the_bf16_shared_expert():
+    """The training step's forward: the routed experts' MX sum plus the bf16
+    layer's shared expert (its hidden through the storage hook)."""
+    x, Wr, W_gu, W_down, Ws_gu, Ws_down, dY, fwd = _train_case(11)
+    y_t, _ = M.experts_forward_mx(x, fwd["topk_idx"], fwd["gates"], W_gu, W_down, Ws_gu,
+                                  Ws_down, shared_mx=False, rnd=_bf16)
+    y_r, _ = M.experts_forward_mx(x, fwd["topk_idx"], fwd["gates"], W_gu, W_down)
+    sg, su = O.split_gu(Ws_gu)
+    shared, *_ = O.swiglu_parts(x, sg, su, Ws_down, _bf16)
+    np.testing.assert_allclose(y_t - y_r, shared, rtol=1e-12, atol=1e-12)
+
+
+class _AxisSpy:
+    """A quantiser that records the shape of every array it quantises (its
+    last axis is the one quantised) and then quantises it."""
+
+    def __init__(self):
+        self.shapes = []
+
+    def __call__(self, v):
+        v = np.asarray(v, dtype=np.float64)
+        self.shapes.append(v.shape)
+        return M.mx_roundtrip(v)
+
+
+def test_mx_backward_quantises_each_operand_along_its_reduction_axis():
+    """Every product of a routed expert's MX step quantises its operands in
+    blocks along the axis it sums over: the forward a, b over d (x rows and
+    W_gate, W_up rows: last axis d), out over H (h rows, W_down rows: last
+    axis H); the data gradients dH over d (d_out rows [n][d] and W_down^T
+    [H][d]) and dx over 2H (d_gu rows [n][2H] and W_gu^T [d][2H]).  With
+    d = 64, H = 96, 2H = 192 and groups of other sizes, the shapes show it."""
+    x, Wr, W_gu, W_down, Ws_gu, Ws_down, dY, fwd = _train_case(8, shared=False)
+    d, H = 64, 96
+    spy = _AxisSpy()
+    M.backward_mx(x, Wr, W_gu, W_down, None, None, fwd, dY, rnd=_bf16, quant=spy)
+    assert spy.shapes[0] == x.shape                           # Q(x), once
+    rest = spy.shapes[1:]
+    assert len(rest) % 8 == 0
+    for i in range(0, len(rest), 8):
+        g = rest[i:i + 8]
+        n = g[2][0]
+        assert g == [(H, d), (H, d), (n, H), (d, H), (n, d), (H, d), (n, 2 * H), (d, 2 * H)], g
+
+
+def test_mx_backward_dense_masked_formulation():
+    """Independent formulation of the routed data gradients: every expert on
+    every token, masked by the selection, with each quantise step written
+    out: dx_t = sum_e [e selected at slot j] Q(bf16(swiglu_bwd(Q(bf16(g dY_t))
+    Q_d(W_down_e), bf16 a, bf16 b))) Q_2H(W_gu_e), plus the shared expert and
+    the router terms of the bf16 layer."""
+    x, Wr, W_gu, W_down, Ws_gu, Ws_down, dY, fwd = _train_case(9, shared=False)
+    got = M.backward_mx(x, Wr, W_gu, W_down, None, None, fwd, dY, rnd=_bf16)
+    T, d = x.shape
+    E, H2, _ = W_gu.shape
+    H = H2 // 2
+    Q = M.mx_roundtrip
+    xq = Q(x)
+    dx = np.zeros((T, d))
+    dg = np.zeros(fwd["topk_idx"].shape)
+    for e in range(E):
+        Wg, Wu = W_gu[e][:H], W_gu[e][H:]
+        a = xq @ Q(Wg).T
+        b = xq @ Q(Wu).T
+        out = Q(a / (1 + np.exp(-a)) * b) @ Q(W_down[e]).T
+        WdT = Q(W_down[e].T)                 # rows of W_down^T: blocks along d
+        WguT = Q(W_gu[e].T)                  # rows of W_gu^T: blocks along 2H
+        for j in range(fwd["topk_idx"].shape[1]):
+            m = fwd["topk_idx"][:, j] == e
+            gte = np.where(m, fwd["gates"][:, j], 0.0)
+            dg[:, j] += np.where(m, (dY * out).sum(axis=1), 0.0)
+            d_out = _bf16(gte[:, None] * dY)
+            dH = Q(d_out) @ WdT.T
+            sa = 1 / (1 + np.exp(-_bf16(a)))
+            da = _bf16(dH * _bf16(b) * sa * (1 + _bf16(a) * (1 - sa)))
+            db = _bf16(dH * _bf16(a) * sa)
+            dx += np.where(m[:, None], Q(np.concatenate([da, db], axis=1)) @ WguT.T, 0.0)
+    dL = O.router_logit_grad(dg, fwd["topk_idx"], fwd["gates"], fwd["probs"], True)
+    dL += O.aux_logit_grad(fwd["probs"], fwd["f"], fwd["real"], 0.01)
+    dx += dL @ Wr.T
+    np.testing.assert_allclose(got["dg"], dg, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(got["dx"], dx, rtol=1e-11, atol=1e-11)
+
+
+def test_mx_backward_differs_from_bf16_by_the_quantisation():
+    """The MX data gradients move dx by a few percent of its scale against
+    the bf16 layer's, never more, and do move it; the weight gradients of
+    the bf16 wgrad products move only through their MX-forward inputs."""
+    x, Wr, W_gu, W_down, Ws_gu, Ws_down, dY, fwd = _train_case(10)
+    args = (x, Wr, W_gu, W_down, Ws_gu, Ws_down, fwd, dY)
+    mx = M.backward_mx(*args, rnd=_bf16)
+    bf = O.backward(*args, rnd=_bf16)
+    rel = np.abs(mx["dx"] - bf["dx"]).max() / np.abs(bf["dx"]).max()
+    assert 1e-3 < rel < 0.2
+    np.testing.assert_allclose(mx["dWs_gu"], bf["dWs_gu"], rtol=1e-12, atol=1e-12)
