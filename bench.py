@@ -308,6 +308,37 @@ def run_ours(args):
         med = lambda v: statistics.median(a.elapsed_time(b) for a, b in v)
         return med(ev_f), med(ev_g), med(ev_d), qa.elapsed_time(qb)
     mx = None if args.no_inference else mx_run()
+
+    # the MXFP8 training step (routed experts' forward and data-gradient
+    # products on block-scaled MMAs; weight gradients and shared expert in
+    # bf16), weights quantised once outside the timed region
+    def mx_train_run():
+        if s.d % 256 or s.H % 128:
+            return None
+        lt = binding.Layer.create(s, training=True, device=f"cuda:{local}")
+        lt.set_inputs(dev["x"], dev["Wr"], dev["W_gu"], dev["W_down"], dev["Ws_gu"],
+                      dev["Ws_down"], bias=dev["bias"], valid=dev["valid"])
+        lt.mx_alloc()
+        lt.mx_quantize_weights()
+        for _ in range(3):
+            lt.mx_step(dev["dY"])
+        ev_t = []
+        for _ in range(max(3, args.steps // 4)):
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            lt.mx_step(dev["dY"])
+            b.record(stream)
+            ev_t.append((a, b))
+        torch.cuda.synchronize()
+        if lt.status() != 0:
+            raise RuntimeError(f"device status {lt.status()} in the MX training step")
+        ms_t = statistics.median(a.elapsed_time(b) for a, b in ev_t)
+        del lt
+        torch.cuda.empty_cache()
+        return ms_t
+    mx_train_ms = None if (args.no_inference or not training) else mx_train_run()
     f8_measured = None if mx is None else fp8_gemm_peak(local)
 
     e2e = run_e2e(args, s, inp, lay, training, local)
@@ -384,6 +415,13 @@ def run_ours(args):
         "fwd_inference_gathered_tokens_per_s": (None if fwd_infer_gather_rate is None
                                                 else round(fwd_infer_gather_rate, 1)),
         "fwd_inference_mxfp8": mx_out,
+        "train_mxfp8": None if mx_train_ms is None else {
+            "fwd_bwd_tokens_per_s": round(s.T / (mx_train_ms / 1e3), 1),
+            "ms_per_step": round(mx_train_ms, 4),
+            "vs_bf16_step": round(ms_per_step / mx_train_ms, 4),
+            "what": "routed experts' forward and data-gradient GEMMs on e4m3 (UE8M0 per-32 "
+                    "scales); weight gradients, shared expert and router in bf16/fp32",
+            "timing": "median of steps, each bracketed by events after a 256 MB L2 flush"},
         "layer_tflops": round(layer_tflops, 1),
         "layer_frac_of_burst_peak": round(layer_tflops / bf16_burst, 4),
         "layer_frac_of_sustained_peak": round(layer_tflops / bf16_sustained, 4),

@@ -59,7 +59,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 4
+#define MOE_ABI_VERSION 5
 #define MOE_ROW_ALIGN 128
 
 enum moe_status {
@@ -400,17 +400,29 @@ typedef struct moe_mx_tensors {
   uint8_t* xt_s;      /* [Tp/128][d/128] atoms                                   */
   uint8_t* hs_q;      /* [Tp][Hs] the shared expert's hidden rows                */
   uint8_t* hs_s;      /* [Tp/128][Hs/128] atoms                                  */
+  /* the training step's data gradients (moe_mx_backward); unused otherwise  */
+  uint8_t* W_gu_tq;   /* [E][d][2H] codes of each W_gu[e]^T: blocks along 2H     */
+  uint8_t* W_gu_ts;   /* [E][d/128][2H/128] atoms                                */
+  uint8_t* W_down_tq; /* [E][H][d] codes of each W_down[e]^T: blocks along d     */
+  uint8_t* W_down_ts; /* [E][H/128][d/128] atoms                                 */
+  uint8_t* dout_q;    /* [R_cap][d] codes of d_out = g dY (blocks along d)       */
+  uint8_t* dout_s;    /* [R_cap/128][d/128] atoms                                */
+  uint8_t* dgu_q;     /* [R_cap][2H] codes of d_gu = da | db (blocks along 2H)   */
+  uint8_t* dgu_s;     /* [R_cap/128][2H/128] atoms                               */
+  float* ab32;        /* [R_cap][2H] fp32 the forward's a | b, for the chain rule */
 } moe_mx_tensors;
 
-#define MOE_MX_FIELDS 16
+#define MOE_MX_FIELDS 25
 
-/* Bytes of each field of moe_mx_tensors, in field order, into bytes[16]
+/* Bytes of each field of moe_mx_tensors, in field order, into bytes[25]
  * (the shared expert's eight are 0 without one). */
 int moe_mx_sizes(const moe_config* cfg, size_t* bytes);
 
 /* Weights -> MXFP8: in: t->W_gu, t->W_down (and Ws_gu, Ws_down with a shared
- * expert), bf16.  out: W_gu_q, W_gu_s, W_down_q, W_down_s (and Ws_*_q, Ws_*_s).
- * Run once per weight update. */
+ * expert), bf16.  out: W_gu_q, W_gu_s, W_down_q, W_down_s (and Ws_*_q, Ws_*_s),
+ * and, when W_gu_tq / W_down_tq are non-NULL (training), each expert's
+ * transposed weights quantised along the axis the data-gradient products
+ * sum over: W_gu_tq/ts, W_down_tq/ts.  Run once per weight update. */
 int moe_mx_quantize_weights(const moe_config* cfg, const moe_tensors* t,
                             const moe_mx_tensors* mx, void* stream);
 
@@ -448,6 +460,38 @@ int moe_mx_shared_ffn(const moe_config* cfg, const moe_tensors* t, const moe_mx_
  * The weights must have been quantised (moe_mx_quantize_weights). */
 int moe_mx_forward(const moe_config* cfg, const moe_tensors* t, const moe_mx_tensors* mx,
                    void* workspace, size_t workspace_bytes, void* stream);
+
+/* The forward of the MXFP8 training step ("KohakUwULLM" README, Key
+ * features: native MXFP8 training of the routed experts; Selected
+ * measurements: MXFP8 end-to-end training speed-ups on MoE models).  The
+ * routed experts run as in moe_mx_forward; the shared expert runs in bf16
+ * (moe_shared_ffn_combine, the combine in its down GEMM).  It also stores
+ * what moe_mx_backward needs: x_perm (bf16 rows), h (bf16, before its MX
+ * rounding), mx->ab32 (the pre-activations a | b in fp32: the chain rule's
+ * results are quantised to e4m3, which a bf16 copy of its inputs would
+ * visibly perturb) and out_perm.  t->ab is not used.
+ * in: as moe_mx_forward.  out: as moe_mx_forward plus x_perm, h, ab32, and
+ * the shared expert's s_h, s_ab (if non-NULL). */
+int moe_mx_forward_train(const moe_config* cfg, const moe_tensors* t, const moe_mx_tensors* mx,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/* The backward of the MXFP8 training step: moe_backward with the routed
+ * experts' two data-gradient products on MXFP8 operands, each quantised in
+ * blocks of 32 along the product's reduction axis: d_out = g dY is
+ * quantised along d (dout_q/s) from its fp32 value, in the kernel that forms
+ * it; dH = Q(d_out) Q(W_down[e]^T) runs on the block-scaled tcgen05 kernel
+ * with the SwiGLU chain rule (on ab32) in its epilogue, which quantises the
+ * fp32 d_gu = da | db along 2H (dgu_q/s) and stores it in bf16 for the
+ * weight gradient; and dx = Q(d_gu) Q(W_gu[e]^T).  Each MX operand is thus
+ * one rounding of its fp32 value, never of a bf16 copy.  The weight gradients, the shared expert and
+ * the router are moe_backward's (bf16 operands, fp32 accumulation).  Needs a
+ * training workspace (moe_workspace_bytes with training = 1), the forward
+ * tensors of moe_mx_forward_train, the transposed weight codes of
+ * moe_mx_quantize_weights, ab32, and dout_q/s, dgu_q/s (32-byte aligned
+ * codes).
+ * out: every field of `g`, as moe_backward. */
+int moe_mx_backward(const moe_config* cfg, const moe_tensors* t, const moe_mx_tensors* mx,
+                    const moe_grads* g, void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------- no-allocation routing */
 

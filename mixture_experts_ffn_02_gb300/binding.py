@@ -47,9 +47,12 @@ class MoEGrads(ctypes.Structure):
     _fields_ = [(n, c_void_p) for n in GRAD_FIELDS]
 
 
-MOE_MX_FIELDS = 16
+MOE_MX_FIELDS = 25
 MX_FIELDS = ["W_gu_q", "W_gu_s", "W_down_q", "W_down_s", "x_q", "x_s", "h_q", "h_s",
-             "Ws_gu_q", "Ws_gu_s", "Ws_down_q", "Ws_down_s", "xt_q", "xt_s", "hs_q", "hs_s"]
+             "Ws_gu_q", "Ws_gu_s", "Ws_down_q", "Ws_down_s", "xt_q", "xt_s", "hs_q", "hs_s",
+             "W_gu_tq", "W_gu_ts", "W_down_tq", "W_down_ts", "dout_q", "dout_s", "dgu_q",
+             "dgu_s", "ab32"]
+MX_TRAIN_FIELDS = MX_FIELDS[16:]
 
 
 class MoEMxTensors(ctypes.Structure):
@@ -97,6 +100,10 @@ SIGNATURES = {
     "moe_mx_expert_down": (ctypes.c_int, _MX_STEP),
     "moe_mx_shared_ffn": (ctypes.c_int, _MX_STEP),
     "moe_mx_forward": (ctypes.c_int, _MX_STEP),
+    "moe_mx_forward_train": (ctypes.c_int, _MX_STEP),
+    "moe_mx_backward": (ctypes.c_int, [ctypes.POINTER(MoEConfig), ctypes.POINTER(MoETensors),
+                                       ctypes.POINTER(MoEMxTensors), ctypes.POINTER(MoEGrads),
+                                       c_void_p, ctypes.c_size_t, c_void_p]),
     "moe_route_partials": (ctypes.c_int, [ctypes.POINTER(MoEConfig), ctypes.POINTER(MoETensors),
                                           c_void_p, c_void_p]),
     "moe_route_finalize": (ctypes.c_int, [ctypes.POINTER(MoEConfig), ctypes.POINTER(MoETensors),
@@ -279,12 +286,14 @@ class Layer:
 
     # ---- MXFP8 routed experts (inference)
     def mx_alloc(self):
-        """Device buffers of moe_mx_tensors (sizes from moe_mx_sizes)."""
+        """Device buffers of moe_mx_tensors (sizes from moe_mx_sizes); the
+        training step's eight only on a training layer."""
         import torch
         sizes = (ctypes.c_size_t * len(MX_FIELDS))()
         check(self.lib.moe_mx_sizes(ctypes.byref(self.cfg), sizes), "moe_mx_sizes")
         dev = self.ws.device
-        self.mx = {n: (torch.empty(int(sz), dtype=torch.uint8, device=dev) if sz else None)
+        self.mx = {n: (torch.empty(int(sz), dtype=torch.uint8, device=dev)
+                       if sz and (self.training or n not in MX_TRAIN_FIELDS) else None)
                    for n, sz in zip(MX_FIELDS, sizes)}
         return self.mx
 
@@ -310,6 +319,21 @@ class Layer:
     def mx_down(self): self._mx_step("moe_mx_expert_down")
     def mx_shared(self): self._mx_step("moe_mx_shared_ffn")
     def mx_forward(self): self._mx_step("moe_mx_forward")
+    def mx_forward_train(self): self._mx_step("moe_mx_forward_train")
+
+    def mx_step(self, dY):
+        """One MXFP8 training step: moe_mx_forward_train then moe_mx_backward
+        (the weight codes from mx_quantize_weights)."""
+        self.mx_forward_train()
+        self.mx_backward(dY)
+
+    def mx_backward(self, dY):
+        t = self.tensors()
+        m = self.mx_tensors()
+        gr = self.grad_struct(dY)
+        check(self.lib.moe_mx_backward(ctypes.byref(self.cfg), ctypes.byref(t), ctypes.byref(m),
+                                       ctypes.byref(gr), c_void_p(self.ws.data_ptr()),
+                                       self.ws.numel(), _stream()), "moe_mx_backward")
 
     def route_partials(self, sums):
         """This rank's routing sums into ``sums`` ([2E+1] float64, device)."""

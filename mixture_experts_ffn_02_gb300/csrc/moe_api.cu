@@ -340,7 +340,19 @@ int do_combine(const moe_config* c, const moe_tensors* t, Call& k) {
   return MOE_OK;
 }
 
-int do_backward(const moe_config* c, const moe_tensors* t, const moe_grads* g, Call& k) {
+bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
+#define MOE_NEED32(p)                          \
+  do {                                         \
+    if (!(p)) return MOE_ERR_NULL;             \
+    if (!aligned32(p)) return MOE_ERR_ALIGN;   \
+  } while (0)
+
+// The backward; with `m` (the MXFP8 training step) the routed experts' two
+// data-gradient products run on MXFP8 operands: d_out quantised along d,
+// dH = Q(d_out) Q(W_down^T) with the SwiGLU chain rule in its epilogue (which
+// also quantises d_gu along 2H), then dx_perm = Q(d_gu) Q(W_gu^T).
+int do_backward(const moe_config* c, const moe_tensors* t, const moe_grads* g, Call& k,
+                const moe_mx_tensors* m = nullptr) {
   if (!g) return MOE_ERR_NULL;
   const int Hs = hs_total(*c);
   MOE_NEED(g->dY); MOE_NEED(g->dx); MOE_NEED(g->dWr); MOE_NEED(g->dW_gu);
@@ -359,23 +371,46 @@ int do_backward(const moe_config* c, const moe_tensors* t, const moe_grads* g, C
   float* dx_perm = reinterpret_cast<float*>(k.ws + w.dx_perm);
   const int R = (int)w.R_cap;
 
-  // (i) + (vii): d_out, dg and the router-logit gradient
+  if (m) {
+    MOE_NEED32(m->W_gu_tq); MOE_NEED(m->W_gu_ts); MOE_NEED32(m->W_down_tq);
+    MOE_NEED(m->W_down_ts); MOE_NEED32(m->dout_q); MOE_NEED(m->dout_s);
+    MOE_NEED32(m->dgu_q); MOE_NEED(m->dgu_s); MOE_NEED(m->ab32);
+  }
+  // (i) + (vii): d_out (with the MX step, also its codes along d, quantised
+  // from the fp32 g dY), dg and the router-logit gradient
   MOE_CUDA(launch_combine_bwd(*c, g->dY, t->out_perm, t->inv, t->topk_idx, t->gates, t->logits,
-                              t->f, t->counts, t->valid, t->row_offsets, d_out, g->d_logits,
+                              t->f, t->counts, t->valid, t->row_offsets, d_out,
+                              m ? m->dout_q : nullptr, m ? m->dout_s : nullptr, g->d_logits,
                               k.status, k.s));
-  // (ii) dH = d_out W_down[e], SwiGLU backward -> d_gu = [da | db]
-  GemmCall gh{};
-  gh.kind = GK_DH; gh.row_offsets = t->row_offsets; gh.E = c->E; gh.rows = R;
-  gh.A = d_out; gh.lda = c->d; gh.B = t->W_down; gh.K = c->d; gh.N = c->H; gh.H = c->H;
-  gh.out0 = d_gu; gh.ld0 = 2 * c->H; gh.aux_in = t->ab; gh.ld_aux = 2 * c->H;
-  gh.status = k.status;
-  MOE_CUDA(launch_gemm(gh, k.s));
-  // (iii) dx_perm = d_gu W_gu[e]
-  GemmCall gx{};
-  gx.kind = GK_DX; gx.row_offsets = t->row_offsets; gx.E = c->E; gx.rows = R;
-  gx.A = d_gu; gx.lda = 2 * c->H; gx.B = t->W_gu; gx.K = 2 * c->H; gx.N = c->d;
-  gx.out0 = dx_perm; gx.ld0 = c->d; gx.out_f32 = 1; gx.status = k.status;
-  MOE_CUDA(launch_gemm(gx, k.s));
+  if (m) {
+    // (ii) dH = Q(d_out) Q(W_down^T) -> SwiGLU backward -> d_gu = [da | db]
+    // in bf16 and, from the fp32 values, its codes along 2H
+    MxGemmCall h{};
+    h.dh = 1; h.row_offsets = t->row_offsets; h.E = c->E; h.rows = R; h.d = c->d; h.H = c->H;
+    h.A = m->dout_q; h.sfa = m->dout_s; h.B = m->W_down_tq; h.sfb = m->W_down_ts;
+    h.abi = m->ab32; h.dgu = d_gu; h.dgq = m->dgu_q; h.dgs = m->dgu_s; h.status = k.status;
+    MOE_CUDA(launch_mx_gemm(h, k.s));
+    // (iii) dx_perm = Q(d_gu) Q(W_gu^T): the down kind with K = 2H, N = d
+    MxGemmCall x{};
+    x.row_offsets = t->row_offsets; x.E = c->E; x.rows = R; x.d = c->d; x.H = 2 * c->H;
+    x.A = m->dgu_q; x.sfa = m->dgu_s; x.B = m->W_gu_tq; x.sfb = m->W_gu_ts; x.out = dx_perm;
+    x.status = k.status;
+    MOE_CUDA(launch_mx_gemm(x, k.s));
+  } else {
+    // (ii) dH = d_out W_down[e], SwiGLU backward -> d_gu = [da | db]
+    GemmCall gh{};
+    gh.kind = GK_DH; gh.row_offsets = t->row_offsets; gh.E = c->E; gh.rows = R;
+    gh.A = d_out; gh.lda = c->d; gh.B = t->W_down; gh.K = c->d; gh.N = c->H; gh.H = c->H;
+    gh.out0 = d_gu; gh.ld0 = 2 * c->H; gh.aux_in = t->ab; gh.ld_aux = 2 * c->H;
+    gh.status = k.status;
+    MOE_CUDA(launch_gemm(gh, k.s));
+    // (iii) dx_perm = d_gu W_gu[e]
+    GemmCall gx{};
+    gx.kind = GK_DX; gx.row_offsets = t->row_offsets; gx.E = c->E; gx.rows = R;
+    gx.A = d_gu; gx.lda = 2 * c->H; gx.B = t->W_gu; gx.K = 2 * c->H; gx.N = c->d;
+    gx.out0 = dx_perm; gx.ld0 = c->d; gx.out_f32 = 1; gx.status = k.status;
+    MOE_CUDA(launch_gemm(gx, k.s));
+  }
   // (iv) dW_down[e] = d_out_e^T h_e ; dW_gu[e] = d_gu_e^T x_perm_e
   GemmCall wd{};
   wd.kind = GK_DW; wd.row_offsets = t->row_offsets; wd.E = c->E; wd.rows = R;
@@ -440,13 +475,7 @@ int do_backward(const moe_config* c, const moe_tensors* t, const moe_grads* g, C
 
 // ---- MXFP8 routed experts
 // The MX kernels store 32 bytes per lane: their code buffers and out_perm
-// must be 32-byte aligned.
-bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
-#define MOE_NEED32(p)                          \
-  do {                                         \
-    if (!(p)) return MOE_ERR_NULL;             \
-    if (!aligned32(p)) return MOE_ERR_ALIGN;   \
-  } while (0)
+// must be 32-byte aligned (MOE_NEED32).
 
 int check_mx(const moe_config* c) {
   if (c->d % 256 || c->H % 128 || hs_total(*c) % 128) return MOE_ERR_SHAPE;
@@ -472,6 +501,16 @@ void mx_sizes(const moe_config& c, size_t* b) {
   b[13] = Hs ? (Tp / 128) * (d / 128) * 512 : 0;         // xt_s
   b[14] = Tp * Hs;                                       // hs_q
   b[15] = (Tp / 128) * (Hs / 128) * 512;                 // hs_s
+  // the training step's data gradients
+  b[16] = E * d * 2 * H;                                 // W_gu_tq: [E][d][2H]
+  b[17] = E * (d / 128) * (2 * H / 128) * 512;           // W_gu_ts
+  b[18] = E * H * d;                                     // W_down_tq: [E][H][d]
+  b[19] = E * (H / 128) * (d / 128) * 512;               // W_down_ts
+  b[20] = R * d;                                         // dout_q
+  b[21] = (R / 128) * (d / 128) * 512;                   // dout_s
+  b[22] = R * 2 * H;                                     // dgu_q
+  b[23] = (R / 128) * (2 * H / 128) * 512;               // dgu_s
+  b[24] = R * 2 * H * 4;                                 // ab32: [R][2H] fp32
 }
 
 // The shared expert on MXFP8 operands: x quantised in token order (PAD and
@@ -512,7 +551,7 @@ int do_mx_shared(const moe_config* c, const moe_tensors* t, const moe_mx_tensors
 // with_xt: also write x's codes in token order for the shared expert
 // (moe_mx_forward with a shared expert), so x is read and quantised once.
 int do_mx_permute(const moe_config* c, const moe_tensors* t, const moe_mx_tensors* m, Call& k,
-                  bool with_xt) {
+                  bool with_xt, bool with_rows = false) {
   MOE_NEED(t->x); MOE_NEED(t->topk_idx); MOE_NEED(t->counts); MOE_NEED(t->offsets);
   MOE_NEED(t->row_offsets); MOE_NEED(t->perm); MOE_NEED(t->inv);
   MOE_NEED32(m->x_q); MOE_NEED(m->x_s);
@@ -521,12 +560,13 @@ int do_mx_permute(const moe_config* c, const moe_tensors* t, const moe_mx_tensor
   }
   MOE_CUDA(launch_permute_mx(*c, t->x, t->topk_idx, t->counts, t->offsets, t->row_offsets,
                              t->perm, t->inv, m->x_q, m->x_s, with_xt ? m->xt_q : nullptr,
-                             with_xt ? m->xt_s : nullptr, k.ws, k.w, k.s));
+                             with_xt ? m->xt_s : nullptr, with_rows ? t->x_perm : nullptr, k.ws,
+                             k.w, k.s));
   return MOE_OK;
 }
 
 int do_mx_gemm(const moe_config* c, const moe_tensors* t, const moe_mx_tensors* m, Call& k,
-               bool gate_up) {
+               bool gate_up, bool save = false) {
   MOE_NEED(t->row_offsets);
   MxGemmCall g{};
   g.gate_up = gate_up ? 1 : 0;
@@ -541,6 +581,11 @@ int do_mx_gemm(const moe_config* c, const moe_tensors* t, const moe_mx_tensors* 
     MOE_NEED32(m->h_q); MOE_NEED(m->h_s);
     g.A = m->x_q; g.sfa = m->x_s; g.B = m->W_gu_q; g.sfb = m->W_gu_s;
     g.hq = m->h_q; g.hs = m->h_s;
+    if (save) {                          // training: h in bf16, a | b in fp32
+      MOE_NEED(t->h); MOE_NEED32(m->ab32);
+      g.hb = t->h;
+      g.abo = m->ab32;
+    }
   } else {
     MOE_NEED(m->h_q); MOE_NEED(m->h_s); MOE_NEED(m->W_down_q); MOE_NEED(m->W_down_s);
     MOE_NEED32(t->out_perm);
@@ -690,6 +735,15 @@ int moe_mx_quantize_weights(const moe_config* cfg, const moe_tensors* t,
                                 (int)(2 * H), nullptr, s));
   MOE_CUDA(launch_mx_quant_rows(t->W_down, mx->W_down_q, mx->W_down_s, E * d, E * d, (int)H,
                                 (int)d, nullptr, s));
+  if (mx->W_gu_tq || mx->W_down_tq) {
+    // the training step's weights along their other axis (data gradients)
+    MOE_NEED32(mx->W_gu_tq); MOE_NEED(mx->W_gu_ts); MOE_NEED32(mx->W_down_tq);
+    MOE_NEED(mx->W_down_ts);
+    MOE_CUDA(launch_mx_quant_cols(t->W_gu, mx->W_gu_tq, mx->W_gu_ts, (int)E, (int)(2 * H),
+                                  (int)d, s));
+    MOE_CUDA(launch_mx_quant_cols(t->W_down, mx->W_down_tq, mx->W_down_ts, (int)E, (int)d,
+                                  (int)H, s));
+  }
   if (Hs > 0) {
     MOE_NEED(t->Ws_gu); MOE_NEED(t->Ws_down);
     MOE_NEED32(mx->Ws_gu_q); MOE_NEED(mx->Ws_gu_s); MOE_NEED32(mx->Ws_down_q);
@@ -727,6 +781,26 @@ MOE_MX_ENTRY(moe_mx_forward, {
   if ((rc = do_mx_shared(cfg, t, mx, k, false))) return rc;
   return do_combine(cfg, t, k);
 })
+
+MOE_MX_ENTRY(moe_mx_forward_train, {
+  MOE_NEED(t->x_perm); MOE_NEED(t->h); MOE_NEED32(t->out_perm);
+  if ((rc = do_router_route(cfg, t, k))) return rc;
+  if ((rc = do_mx_permute(cfg, t, mx, k, false, true))) return rc;
+  if ((rc = do_mx_gemm(cfg, t, mx, k, true, true))) return rc;
+  if ((rc = do_mx_gemm(cfg, t, mx, k, false))) return rc;
+  return do_shared_combine(cfg, t, k);   // the bf16 shared expert, combine in its down GEMM
+})
+
+int moe_mx_backward(const moe_config* cfg, const moe_tensors* t, const moe_mx_tensors* mx,
+                    const moe_grads* g, void* workspace, size_t workspace_bytes, void* stream) {
+  Call k;
+  int rc = check_cfg(cfg);
+  if (rc) return rc;
+  if ((rc = check_mx(cfg))) return rc;
+  if ((rc = begin(cfg, 1, workspace, workspace_bytes, stream, &k))) return rc;
+  if (!t || !mx) return MOE_ERR_NULL;
+  return do_backward(cfg, t, g, k, mx);
+}
 
 int moe_route_partials(const moe_config* cfg, const moe_tensors* t, double* sums, void* stream) {
   int rc = check_cfg(cfg);

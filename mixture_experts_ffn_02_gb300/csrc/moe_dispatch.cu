@@ -1298,8 +1298,12 @@ perm_scatter_kernel(const bf16* __restrict__ x, const int32_t* __restrict__ topk
     const int* dst = dest_s + tl * k;
     for (int b = lane; b < nb32; b += 32) {
       float v[32];
+      uint4 raw[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) unpack8(ld_nc_v4(src + b * 32 + u * 8), v + 8 * u);
+      for (int u = 0; u < 4; ++u) {
+        raw[u] = ld_nc_v4(src + b * 32 + u * 8);
+        unpack8(raw[u], v + 8 * u);
+      }
       uint32_t q[8];
       const uint32_t sb = mx_quant32(v, q);
       if (xt_q != nullptr) {
@@ -1318,6 +1322,10 @@ perm_scatter_kernel(const bf16* __restrict__ x, const int32_t* __restrict__ topk
         st_v8(x_q + (size_t)r * d + b * 32, q);
         x_s[((size_t)(r >> 7) * kg + (b >> 2)) * kMxAtom + mx_sf_byte(r & 127, b & 3)] =
             (uint8_t)sb;
+        if (x_perm != nullptr) {           // training: the bf16 rows too (weight gradients)
+#pragma unroll
+          for (int u = 0; u < 4; ++u) st_v4(x_perm + (size_t)r * d + b * 32 + u * 8, raw[u]);
+        }
       }
     }
   }
@@ -1354,7 +1362,7 @@ perm_scatter_kernel(const bf16* __restrict__ x, const int32_t* __restrict__ topk
     const int r1 = row_offsets[e + 1];
     for (int r = r0 + warp; r < r1; r += wpb) {
       if (lane == 0) perm[r] = -1;
-      if (!MX && x_perm != nullptr)
+      if (x_perm != nullptr)
         for (int c0 = lane * 8; c0 < d; c0 += 256)
           st_v4(x_perm + (size_t)r * d + c0, make_uint4(0, 0, 0, 0));
       if (MX) {
@@ -1414,6 +1422,9 @@ combine_kernel(const float* __restrict__ out_perm, const int32_t* __restrict__ i
 // d_out[inv[t,j]] = g[t,j] dY[t];  dg[t,j] = <dY[t], out_perm[inv[t,j]]>;
 // d_logits from dg through the gate map, plus the aux term
 // (aux_coef E / T_real) s_e (f_e - sum_i f_i s_i).  Also zeroes d_out pad rows.
+// With dq (the MXFP8 training step; d a multiple of 256, so every lane runs
+// the same column loop), the fp32 g dY is also quantised along d into e4m3
+// codes dq [R][d] and scale atoms ds [R/128][d/128], pad rows as zeros.
 // --------------------------------------------------------------------------
 template <int V>
 __global__ void __launch_bounds__(kThreads)
@@ -1422,7 +1433,8 @@ combine_bwd_kernel(const bf16* __restrict__ dY, const float* __restrict__ out_pe
                    const float* __restrict__ gates, const float* __restrict__ L,
                    const float* __restrict__ f, const int32_t* __restrict__ counts,
                    const uint8_t* __restrict__ valid, const int32_t* __restrict__ row_offsets,
-                   bf16* __restrict__ d_out, float* __restrict__ d_logits, int T, int d, int E,
+                   bf16* __restrict__ d_out, uint8_t* __restrict__ dq,
+                   uint8_t* __restrict__ ds, float* __restrict__ d_logits, int T, int d, int E,
                    int k, int norm_topk, float aux_coef, float z_coef) {
   __shared__ float f_s[256];
   __shared__ float coef_s, zcoef_s;
@@ -1470,6 +1482,14 @@ combine_bwd_kernel(const bf16* __restrict__ dY, const float* __restrict__ out_pe
             go[u] = g * dy[u];
           }
           st_v4(d_out + (size_t)r * d + c0, pack8(go));
+          if (dq != nullptr) {
+            uint32_t cq[2];
+            const uint32_t sb = mx_quant8x4(go, cq);
+            *reinterpret_cast<uint2*>(dq + (size_t)r * d + c0) = make_uint2(cq[0], cq[1]);
+            if ((lane & 3) == 0)
+              ds[((size_t)(r >> 7) * (d >> 7) + (c0 >> 7)) * kMxAtom +
+                 mx_sf_byte(r & 127, (c0 >> 5) & 3)] = (uint8_t)sb;
+          }
         }
       }
       dot = warp_sum(dot);
@@ -1532,8 +1552,15 @@ combine_bwd_kernel(const bf16* __restrict__ dY, const float* __restrict__ out_pe
     const int r0 = row_offsets[e] + counts[e];
     const int r1 = row_offsets[e + 1];
     for (int r = r0 + warp; r < r1; r += wpb)
-      for (int c0 = lane * 8; c0 < d; c0 += 256)
+      for (int c0 = lane * 8; c0 < d; c0 += 256) {
         st_v4(d_out + (size_t)r * d + c0, make_uint4(0, 0, 0, 0));
+        if (dq != nullptr) {
+          *reinterpret_cast<uint2*>(dq + (size_t)r * d + c0) = make_uint2(0, 0);
+          if ((lane & 3) == 0)
+            ds[((size_t)(r >> 7) * (d >> 7) + (c0 >> 7)) * kMxAtom +
+               mx_sf_byte(r & 127, (c0 >> 5) & 3)] = 0;
+        }
+      }
   }
 }
 
@@ -2000,8 +2027,8 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* to
 cudaError_t launch_permute_mx(const moe_config& c, const void* x, const int32_t* topk,
                               int32_t* counts, int32_t* offsets, int32_t* row_offsets,
                               int32_t* perm, int32_t* inv, uint8_t* x_q, uint8_t* x_s,
-                              uint8_t* xt_q, uint8_t* xt_s, char* ws, const WsLayout& w,
-                              cudaStream_t s) {
+                              uint8_t* xt_q, uint8_t* xt_s, void* x_perm, char* ws,
+                              const WsLayout& w, cudaStream_t s) {
   int* hist = reinterpret_cast<int*>(ws + w.perm_hist);
   int* base = reinterpret_cast<int*>(ws + w.perm_base);
   int* status = reinterpret_cast<int*>(ws + w.status);
@@ -2012,7 +2039,7 @@ cudaError_t launch_permute_mx(const moe_config& c, const void* x, const int32_t*
   return launch_pdl(perm_scatter_kernel<true>, dim3(nblk), dim3(kScatterThreads), s,
                     static_cast<const bf16*>(x), topk, c.T, c.d, c.k, c.E, (const int*)base,
                     (const int32_t*)counts, (const int32_t*)row_offsets, perm, inv,
-                    (bf16*)nullptr, x_q, x_s, xt_q, xt_s, (c.T + 127) / 128 * 128);
+                    static_cast<bf16*>(x_perm), x_q, x_s, xt_q, xt_s, (c.T + 127) / 128 * 128);
 }
 
 cudaError_t launch_combine(const moe_config& c, const float* out_perm, const int32_t* inv,
@@ -2030,8 +2057,10 @@ cudaError_t launch_combine_bwd(const moe_config& c, const void* dY, const float*
                                const int32_t* inv, const int32_t* topk, const float* gates,
                                const float* L, const float* f, const int32_t* counts,
                                const uint8_t* valid, const int32_t* row_offsets, void* d_out,
-                               float* d_logits, int* status, cudaStream_t s) {
+                               uint8_t* dout_q, uint8_t* dout_s, float* d_logits, int* status,
+                               cudaStream_t s) {
   (void)status;
+  if (dout_q != nullptr && (c.d % 256 != 0 || dout_s == nullptr)) return cudaErrorInvalidValue;
   DeviceInfo di;
   if (device_info(&di) != MOE_OK) return cudaErrorUnknown;
   const int grid = grid_for(kThreads / 32, c.T, di.num_sms * 8);
@@ -2039,7 +2068,8 @@ cudaError_t launch_combine_bwd(const moe_config& c, const void* dY, const float*
 #define MOE_CBWD(VV)                                                                          \
   combine_bwd_kernel<VV><<<grid, kThreads, 0, s>>>(                                           \
       static_cast<const bf16*>(dY), out_perm, inv, topk, gates, L, f,                          \
-      counts, valid, row_offsets, static_cast<bf16*>(d_out), d_logits, c.T, c.d, c.E, c.k,     \
+      counts, valid, row_offsets, static_cast<bf16*>(d_out), dout_q, dout_s, d_logits, c.T,    \
+      c.d, c.E, c.k,                                                                           \
       c.norm_topk, c.aux_coef, c.z_coef)
   if (V <= 1) { MOE_CBWD(1); }
   else if (V <= 2) { MOE_CBWD(2); }

@@ -91,7 +91,8 @@ cudaError_t launch_combine_bwd(const moe_config& c, const void* dY, const float*
                                const int32_t* inv, const int32_t* topk, const float* gates,
                                const float* L, const float* f, const int32_t* counts,
                                const uint8_t* valid, const int32_t* row_offsets,
-                               void* d_out, float* d_logits, int* status, cudaStream_t s);
+                               void* d_out, uint8_t* dout_q, uint8_t* dout_s,
+                               float* d_logits, int* status, cudaStream_t s);
 cudaError_t launch_dx_gather(const moe_config& c, const float* dx_perm, const int32_t* inv,
                              const float* dxr, const float* d_logits,
                              const float* Wr, const uint8_t* valid, void* dx, cudaStream_t s);
@@ -184,8 +185,8 @@ cudaError_t launch_gemm(const GemmCall& g, cudaStream_t s);
 cudaError_t launch_permute_mx(const moe_config& c, const void* x, const int32_t* topk,
                               int32_t* counts, int32_t* offsets, int32_t* row_offsets,
                               int32_t* perm, int32_t* inv, uint8_t* x_q, uint8_t* x_s,
-                              uint8_t* xt_q, uint8_t* xt_s, char* ws, const WsLayout& w,
-                              cudaStream_t s);
+                              uint8_t* xt_q, uint8_t* xt_s, void* x_perm, char* ws,
+                              const WsLayout& w, cudaStream_t s);
 // Rows of a bf16 [rows][K] matrix -> codes [rows][K] and scale atoms per
 // 128-row block of each group of rows_per_group rows; rows past rows_real or
 // with valid == 0 (valid may be NULL) quantise as zeros.
@@ -194,6 +195,8 @@ cudaError_t launch_mx_quant_rows(const void* W, uint8_t* Wq, uint8_t* Ws, long l
                                  const uint8_t* valid, cudaStream_t s);
 struct MxGemmCall {
   int gate_up;                 // 1: h = silu(a) * b quantised; 0: out = h W_down^T (fp32)
+  int dh;                      // 1 (gate_up 0): dH = d_out W_down with the SwiGLU chain rule:
+                               // A = d_out codes [rows][d], B = W_down^T codes [E][H][d]
   const int32_t* row_offsets;  // [E+1] padded, device; NULL: dense rows
   int dense_rows;              // dense: rows (the tile grid pads them to 128)
   int E;
@@ -205,9 +208,20 @@ struct MxGemmCall {
   const uint8_t* sfb;          // their scale atoms
   uint8_t* hq;                 // gate/up out: h codes [rows][H]
   uint8_t* hs;                 // gate/up out: h scale atoms
-  float* out;                  // down out: [rows][d] fp32
+  void* hb;                    // gate/up out (training): h [rows][H] bf16, or NULL
+  void* abo;                   // gate/up out (training): a | b [rows][2H] fp32, or NULL
+  float* out;                  // down out: [rows][d] fp32 (d is the output width)
+  const void* abi;             // dH in: saved a | b [rows][2H] fp32
+  void* dgu;                   // dH out: da | db [rows][2H] bf16
+  uint8_t* dgq;                // dH out: codes of d_gu [rows][2H]
+  uint8_t* dgs;                // dH out: their scale atoms [rows/128][2H/128]
   int* status;
 };
+// W [groups][R][C] bf16 -> codes of each group's transpose [groups][C][R],
+// blocks of 32 along R, and scale atoms [groups][C/128][R/128] (a weight
+// quantised along the axis a data-gradient product sums over).
+cudaError_t launch_mx_quant_cols(const void* W, uint8_t* Wq, uint8_t* Ws, int groups, int R, int C,
+                                 cudaStream_t s);
 cudaError_t launch_mx_gemm(const MxGemmCall& g, cudaStream_t s);
 cudaError_t launch_wait_timeout_selftest(int* status, unsigned long long limit_ns,
                                          cudaStream_t s);

@@ -65,7 +65,12 @@ static_assert(XSTAGE % 1024 == 0 && XLOAD <= XSTAGE, "stage layout");
 static_assert(XSMEM <= 232448, "exceeds the 227 KB opt-in shared memory of a block");
 static_assert(XSF_COL + XSF_SLOT * XSTAGES <= XTMEM_COLS, "scale slots exceed TMEM");
 
-enum MxKind { MXK_GATE_UP = 0, MXK_DOWN = 1 };
+// MXK_GATE_UP_SAVE: gate/up that also stores h and a | b in bf16 (training)
+enum MxKind { MXK_GATE_UP = 0, MXK_DOWN = 1, MXK_DH = 2, MXK_GATE_UP_SAVE = 3 };
+template <int KIND>
+struct XIsGateUp {
+  static constexpr bool value = KIND == MXK_GATE_UP || KIND == MXK_GATE_UP_SAVE;
+};
 
 struct XParams {
   const int32_t* row_offsets;  // [E+1] padded segment offsets (multiples of 128), or NULL:
@@ -80,7 +85,13 @@ struct XParams {
   int nbt;                     // weight scale blocks (128 rows) per expert
   uint8_t* hq;                 // gate/up: h codes [R][H]
   uint8_t* hs;                 // gate/up: h scale atoms [R/128][H/128][512]
+  bf16* hb;                    // gate/up, training: h [R][H] bf16, or NULL
+  float* abo;                  // gate/up, training: a | b [R][2H] fp32, or NULL
   float* out;                  // down: out_perm [R][d] fp32
+  const float* abi;            // dH: the saved a | b [R][2H] fp32
+  bf16* dgu;                   // dH: d_gu = da | db [R][2H] bf16
+  uint8_t* dgq;                // dH: codes of d_gu [R][2H]
+  uint8_t* dgs;                // dH: scale atoms of d_gu [R/128][2H/128][512]
   int* status;
 };
 
@@ -120,7 +131,7 @@ template <int KIND>
 __device__ __forceinline__ XTile x_tile(const XParams& p, const XShared& sh, int idx) {
   XTile t;
   const int mu = idx / p.n_tiles;
-  t.n0 = (idx - mu * p.n_tiles) * (KIND == MXK_GATE_UP ? XBN / 2 : XBN);
+  t.n0 = (idx - mu * p.n_tiles) * (XIsGateUp<KIND>::value ? XBN / 2 : XBN);
   t.e = x_last_le(sh.ppre, p.E, mu);
   t.m0 = sh.roff[t.e] + (mu - sh.ppre[t.e]) * 2 * XBM;
   t.row_end = sh.roff[t.e + 1];
@@ -135,6 +146,33 @@ __device__ __forceinline__ void x_fail(XShared& sh, int* status) {
 // The logistic function with CUDA's fast exponential and approximate
 // division; the result is quantised to e4m3 (3 mantissa bits) right after.
 __device__ __forceinline__ float x_silu(float a) { return __fdividef(a, 1.f + __expf(-a)); }
+__device__ __forceinline__ float x_sigmoid(float a) { return __fdividef(1.f, 1.f + __expf(-a)); }
+
+// 32 consecutive bf16 values: four 16-byte loads / stores.
+__device__ __forceinline__ void x_ld32(const bf16* p, float* v) {
+#pragma unroll
+  for (int u = 0; u < 4; ++u) unpack8(ld_nc_v4(p + 8 * u), v + 8 * u);
+}
+__device__ __forceinline__ void x_st32(bf16* p, const float* v) {
+#pragma unroll
+  for (int u = 0; u < 4; ++u) st_v4(p + 8 * u, pack8(v + 8 * u));
+}
+// 32 consecutive fp32 values: four 32-byte stores (p 32-byte aligned) of
+// their bits, and eight 16-byte loads.
+__device__ __forceinline__ void x_st32_f32(float* p, const uint32_t* r) {
+#pragma unroll
+  for (int u = 0; u < 4; ++u) st_v8(p + 8 * u, r + 8 * u);
+}
+__device__ __forceinline__ void x_ld32_f32(const float* p, float* v) {
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const uint4 w = ld_nc_v4(p + 4 * u);
+    v[4 * u + 0] = __uint_as_float(w.x);
+    v[4 * u + 1] = __uint_as_float(w.y);
+    v[4 * u + 2] = __uint_as_float(w.z);
+    v[4 * u + 3] = __uint_as_float(w.w);
+  }
+}
 
 // ------------------------------------------------------------------ kernel
 // CTAs run in clusters of two.  Both load their shares of each stage
@@ -222,8 +260,8 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const int rowA = t.m0 + XBM * rank;
       // the tile's two 128-row weight blocks: gate and up rows of the same
       // hidden units (gate/up), or two consecutive blocks of model columns
-      const int jb0 = KIND == MXK_GATE_UP ? t.n0 / 128 : t.n0 / 128;
-      const int jb1 = KIND == MXK_GATE_UP ? (p.H + t.n0) / 128 : t.n0 / 128 + 1;
+      const int jb0 = t.n0 / 128;
+      const int jb1 = XIsGateUp<KIND>::value ? (p.H + t.n0) / 128 : t.n0 / 128 + 1;
       const int atom_a = (rowA / XBM) * p.kg;                 // this CTA's rows' scales
       const int atom_b0 = (t.e * p.nbt + jb0) * p.kg;
       const int atom_b1 = (t.e * p.nbt + jb1) * p.kg;
@@ -240,7 +278,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const uint32_t sb = sa + XA_BYTES;
         const uint32_t sf = sa + XSF_OFF;
         tma_load_2d_pair(sa, &tmA, fb, kb * XBK, rowA);
-        if (KIND == MXK_GATE_UP)      // rank 0: the 128 gate rows, rank 1: the 128 up rows
+        if (XIsGateUp<KIND>::value)   // rank 0: the 128 gate rows, rank 1: the 128 up rows
           tma_load_4d_pair(sb, &tmB, fb, kb * XBK, t.n0, rank, t.e);
         else
           tma_load_3d_pair(sb, &tmB, fb, kb * XBK, t.n0 + (XBN / 2) * rank, t.e);
@@ -325,7 +363,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       // this warp's 128 accumulator columns into registers; gate/up: gate
       // columns half*64 .. +63 and the matching up columns 128 + half*64 ..
       uint32_t r[4][32];
-      if (KIND == MXK_GATE_UP) {
+      if (XIsGateUp<KIND>::value) {
         tmem_ld64(tacc + half * 64, &r[0][0]);
         tmem_ld64(tacc + XBN / 2 + half * 64, &r[2][0]);
       } else {
@@ -336,7 +374,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(tempty_leader);   // accumulator free
       if (!store) continue;
-      if (KIND == MXK_GATE_UP) {
+      if (XIsGateUp<KIND>::value) {
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           float h[32];
@@ -350,6 +388,54 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             st_v8(p.hq + (size_t)row * p.H + col, cq);
             p.hs[((size_t)(row >> 7) * (p.H / 128) + (col >> 7)) * kMxAtom +
                  mx_sf_byte(row & 127, (col >> 5) & 3)] = (uint8_t)sbyte;
+            if (KIND == MXK_GATE_UP_SAVE) {
+              // training: h in bf16 (the weight-gradient product's operand)
+              // and the pre-activations a | b in fp32 for the chain rule,
+              // whose results feed an e4m3 quantiser (a bf16 copy of a, b
+              // would move about 2% of those codes by a whole step)
+              x_st32(p.hb + (size_t)row * p.H + col, h);
+              x_st32_f32(p.abo + (size_t)row * 2 * p.H + col, r[c]);
+              x_st32_f32(p.abo + (size_t)row * 2 * p.H + p.H + col, r[2 + c]);
+            }
+          }
+        }
+      } else if (KIND == MXK_DH) {
+        // dH -> the SwiGLU chain rule with the saved a | b:
+        // da = dH b s(a) (1 + a (1 - s(a))), db = dH silu(a).  The fp32 da, db
+        // are quantised along 2H (blocks of 32, which never straddle da and
+        // db: H is a multiple of 128) for the dX product, and stored in bf16
+        // as d_gu = da | db for the weight-gradient product: one rounding
+        // each.  Column halves past H are the last tile's padding.
+        const int col0 = t.n0 + half * 128;
+        if (row_ok && col0 < p.H) {
+          const size_t rb = (size_t)row * 2 * p.H;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int col = col0 + 32 * c;
+            float a[32], b[32];
+            x_ld32_f32(p.abi + rb + col, a);
+            x_ld32_f32(p.abi + rb + p.H + col, b);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float dh = __uint_as_float(r[c][i]);
+              const float sg = x_sigmoid(a[i]);
+              const float da = dh * b[i] * sg * (1.f + a[i] * (1.f - sg));
+              const float db = dh * (a[i] * sg);
+              a[i] = da;
+              b[i] = db;
+            }
+            uint32_t cq[8];
+            const size_t atom_row = (size_t)(row >> 7) * (2 * p.H / 128);
+            uint32_t sbyte = mx_quant32(a, cq);
+            st_v8(p.dgq + rb + col, cq);
+            p.dgs[(atom_row + (col >> 7)) * kMxAtom + mx_sf_byte(row & 127, (col >> 5) & 3)] =
+                (uint8_t)sbyte;
+            sbyte = mx_quant32(b, cq);
+            st_v8(p.dgq + rb + p.H + col, cq);
+            p.dgs[(atom_row + ((p.H + col) >> 7)) * kMxAtom +
+                  mx_sf_byte(row & 127, ((p.H + col) >> 5) & 3)] = (uint8_t)sbyte;
+            x_st32(p.dgu + rb + col, a);
+            x_st32(p.dgu + rb + p.H + col, b);
           }
         }
       } else {
@@ -405,6 +491,35 @@ mx_quant_rows_kernel(const bf16* __restrict__ W, uint8_t* __restrict__ Wq,
     const int e = (int)(row / rows_per_group);
     const int n = (int)(row - (long long)e * rows_per_group);
     Ws[(((size_t)e * nbt + n / 128) * kg + (b >> 2)) * kMxAtom + mx_sf_byte(n % 128, b & 3)] =
+        (uint8_t)sbyte;
+  }
+}
+
+// ------------------------------------------------------------------ columns
+// One thread per (group g, column c, block rb of 32 rows) of W [G][R][C]
+// bf16: the block W[g][32 rb .. 32 rb + 31][c] (consecutive threads read
+// consecutive columns, so each row's loads are coalesced) becomes 32 codes
+// of row c of the transpose, Wq[g][c][32 rb ..], and one scale byte in the
+// atom of (row block c / 128, K group rb / 4) of group g.
+__global__ void __launch_bounds__(256)
+mx_quant_cols_kernel(const bf16* __restrict__ W, uint8_t* __restrict__ Wq,
+                     uint8_t* __restrict__ Ws, int G, int R, int C) {
+  const int nrb = R / 32, kg = R / 128, nbt = C / 128;
+  const long long total = (long long)G * nrb * C;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int c = (int)(i % C);
+    const long long gr = i / C;
+    const int rb = (int)(gr % nrb);
+    const int g = (int)(gr / nrb);
+    const bf16* src = W + ((size_t)g * R + (size_t)rb * 32) * C + c;
+    float v[32];
+#pragma unroll
+    for (int u = 0; u < 32; ++u) v[u] = __bfloat162float(src[(size_t)u * C]);
+    uint32_t cq[8];
+    const uint32_t sbyte = mx_quant32(v, cq);
+    st_v8(Wq + ((size_t)g * C + c) * R + (size_t)rb * 32, cq);
+    Ws[(((size_t)g * nbt + c / 128) * kg + (rb >> 2)) * kMxAtom + mx_sf_byte(c % 128, rb & 3)] =
         (uint8_t)sbyte;
   }
 }
@@ -529,7 +644,13 @@ cudaError_t launch_mx_gemm(const MxGemmCall& g, cudaStream_t s) {
   p.d = g.d;
   p.hq = g.hq;
   p.hs = g.hs;
+  p.hb = static_cast<bf16*>(g.hb);
+  p.abo = static_cast<float*>(g.abo);
   p.out = g.out;
+  p.abi = static_cast<const float*>(g.abi);
+  p.dgu = static_cast<bf16*>(g.dgu);
+  p.dgq = g.dgq;
+  p.dgs = g.dgs;
   p.status = g.status;
   CUtensorMap ta, tb, tsa, tsb;
   const uint64_t rows = (uint64_t)g.rows;
@@ -546,6 +667,18 @@ cudaError_t launch_mx_gemm(const MxGemmCall& g, cudaStream_t s) {
     uint64_t sb[3] = {(uint64_t)g.d, (uint64_t)g.H * g.d, (uint64_t)2 * g.H * g.d};
     uint32_t bb[4] = {XBK, XBN / 2, 1, 1};
     ok = x_make_map(&ta, g.A, 2, da, sa, ba, true) && x_make_map(&tb, g.B, 4, db, sb, bb, true);
+  } else if (g.dh) {
+    // A: d_out codes [rows][d]; B: W_down^T codes [E][H][d] -> dims {d, H, E};
+    // the output is H wide (the last tile's second half may lie past it)
+    K = g.d;
+    p.n_tiles = (g.H + XBN - 1) / XBN;
+    p.nbt = g.H / 128;
+    uint64_t da[2] = {(uint64_t)g.d, rows}, sa[1] = {(uint64_t)g.d};
+    uint32_t ba[2] = {XBK, XBM};
+    uint64_t db[3] = {(uint64_t)g.d, (uint64_t)g.H, (uint64_t)g.E};
+    uint64_t sb[2] = {(uint64_t)g.d, (uint64_t)g.H * g.d};
+    uint32_t bb[3] = {XBK, XBN / 2, 1};
+    ok = x_make_map(&ta, g.A, 2, da, sa, ba, true) && x_make_map(&tb, g.B, 3, db, sb, bb, true);
   } else {
     // A: h codes [rows][H]; B: W_down codes [E][d][H] -> dims {H, d, E}
     K = g.H;
@@ -562,8 +695,19 @@ cudaError_t launch_mx_gemm(const MxGemmCall& g, cudaStream_t s) {
   ok = ok && x_atom_map(&tsa, g.sfa, (size_t)(rows / XBM) * p.kg) &&
        x_atom_map(&tsb, g.sfb, (size_t)g.E * p.nbt * p.kg);
   if (!ok) return cudaErrorInvalidValue;
-  return g.gate_up ? x_launch<MXK_GATE_UP>(ta, tb, tsa, tsb, p, di.num_sms, s)
-                   : x_launch<MXK_DOWN>(ta, tb, tsa, tsb, p, di.num_sms, s);
+  if (g.gate_up && g.hb) return x_launch<MXK_GATE_UP_SAVE>(ta, tb, tsa, tsb, p, di.num_sms, s);
+  if (g.gate_up) return x_launch<MXK_GATE_UP>(ta, tb, tsa, tsb, p, di.num_sms, s);
+  if (g.dh) return x_launch<MXK_DH>(ta, tb, tsa, tsb, p, di.num_sms, s);
+  return x_launch<MXK_DOWN>(ta, tb, tsa, tsb, p, di.num_sms, s);
+}
+
+cudaError_t launch_mx_quant_cols(const void* W, uint8_t* Wq, uint8_t* Ws, int groups, int R, int C,
+                                 cudaStream_t s) {
+  DeviceInfo di;
+  if (device_info(&di) != MOE_OK) return cudaErrorUnknown;
+  mx_quant_cols_kernel<<<di.num_sms * 8, 256, 0, s>>>(static_cast<const bf16*>(W), Wq, Ws, groups,
+                                                      R, C);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_mx_quant_rows(const void* W, uint8_t* Wq, uint8_t* Ws, long long rows,

@@ -21,22 +21,42 @@ namespace moe {
 // power-of-two scaling of a finite fp32 whose result stays below 512) is
 // converted to e4m3 by the hardware conversion, round to nearest even,
 // saturating at +-448.  codes[w] holds elements 4w .. 4w+3, lowest first.
+__device__ __forceinline__ int mx_block_exp(float amax) {
+  const int X = (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 127 - 8;
+  return X < -127 ? -127 : X;
+}
+// Four values times inv (2^-X) as four e4m3 codes, the first lowest.
+__device__ __forceinline__ uint32_t mx_cvt4(const float* v, float inv) {
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(v[0] * inv, v[1] * inv),
+                                               __NV_SATFINITE, __NV_E4M3);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(v[2] * inv, v[3] * inv),
+                                               __NV_SATFINITE, __NV_E4M3);
+  return (lo & 0xFFFFu) | (hi << 16);
+}
 __device__ __forceinline__ uint32_t mx_quant32(const float* v, uint32_t* codes) {
   float amax = 0.f;
 #pragma unroll
   for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-  int X = (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 127 - 8;
-  X = X < -127 ? -127 : X;
+  const int X = mx_block_exp(amax);
   const float inv = __uint_as_float((uint32_t)(127 - X) << 23);     // 2^-X
 #pragma unroll
-  for (int w = 0; w < 8; ++w) {
-    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(v[4 * w] * inv, v[4 * w + 1] * inv),
-                                                 __NV_SATFINITE, __NV_E4M3);
-    const uint32_t hi =
-        __nv_cvt_float2_to_fp8x2(make_float2(v[4 * w + 2] * inv, v[4 * w + 3] * inv),
-                                 __NV_SATFINITE, __NV_E4M3);
-    codes[w] = (lo & 0xFFFFu) | (hi << 16);
-  }
+  for (int w = 0; w < 8; ++w) codes[w] = mx_cvt4(v + 4 * w, inv);
+  return (uint32_t)(X + 127);
+}
+// The same block quantiser when a block of 32 is held 8 values per lane by
+// four consecutive lanes (4q .. 4q+3, in element order): the block maximum
+// by shuffles among the four, this lane's eight codes in codes[0..1], the
+// scale byte returned to all four.  Every lane of the warp must call it.
+__device__ __forceinline__ uint32_t mx_quant8x4(const float* v, uint32_t* codes) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  const int X = mx_block_exp(amax);
+  const float inv = __uint_as_float((uint32_t)(127 - X) << 23);
+  codes[0] = mx_cvt4(v, inv);
+  codes[1] = mx_cvt4(v + 4, inv);
   return (uint32_t)(X + 127);
 }
 

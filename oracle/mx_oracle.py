@@ -133,7 +133,7 @@ def experts_forward_mx(x, topk_idx, gates, W_gu, W_down, Ws_gu=None, Ws_down=Non
     xq = mx_roundtrip(x)
     y, routed = mo.experts_forward(xq, topk_idx, gates, mx_roundtrip(mo._f64(W_gu)),
                                    mx_roundtrip(mo._f64(W_down)), valid=valid,
-                                   rnd=mx_roundtrip)
+                                   rnd=_HiddenMX(rnd))
     if Ws_gu is not None:
         real = np.ones(x.shape[0], dtype=bool) if valid is None else (
             np.asarray(mo._np(valid)) != 0)
@@ -148,6 +148,18 @@ def experts_forward_mx(x, topk_idx, gates, W_gu, W_down, Ws_gu=None, Ws_down=Non
                                          dict(shared=True, rows=rows))
         y[real] += shared
     return y, routed
+
+
+class _HiddenMX:
+    """The routed hidden's MX rounding in the form of ``moe_oracle``'s
+    storage hook: Q(h) at the quantisation point "q_h" (:func:`_quantised`,
+    so that the hook ``rnd`` may see it)."""
+
+    def __init__(self, rnd):
+        self.rnd = rnd
+
+    def store(self, point, v, where):
+        return _quantised(self.rnd, "q_h", v, mx_roundtrip, where)
 
 
 def forward_mx(x, Wr, W_gu, W_down, Ws_gu=None, Ws_down=None, k=2, bias=None,
@@ -166,6 +178,17 @@ def forward_mx(x, Wr, W_gu, W_down, Ws_gu=None, Ws_down=None, k=2, bias=None,
 # --------------------------------------------------------------------------
 # Training step with MXFP8 routed experts
 # --------------------------------------------------------------------------
+
+def _quantised(rnd, point, v, quant, where):
+    """Q(v) at a quantisation point of a routed expert ("q_h", "q_d_out" or
+    "q_d_gu", rows ``where``): ``quant(v)``, or ``rnd.quantised(point, v,
+    quant(v), where)`` when the storage hook has that method.  No arithmetic
+    happens here."""
+    q = quant(v)
+    if rnd is not None and hasattr(rnd, "quantised"):
+        return rnd.quantised(point, v, q, where)
+    return q
+
 
 def roundtrip_k(W, quant=None):
     """Q along axis 0 of a [K][N] matrix: the operand of ``v @ W`` quantised
@@ -189,10 +212,17 @@ def backward_mx(x, Wr, W_gu, W_down, Ws_gu, Ws_down, fwd, dY, norm_topk=True,
       d_out = g dY (reduction over d), and dx = Q(d_gu) Qk(W_gu) with
       d_gu = [da | db] (reduction over 2H); Qk quantises a weight along the
       axis the product sums over (:func:`roundtrip_k`).
-    * The SwiGLU chain rule takes the saved a and b, and the weight-gradient
-      products take the saved h, d_out, d_gu and x, all at the bf16 storage
-      points of the bf16 layer (``rnd``, the hook of
+    * Q(d_out) and Q(d_gu) quantise the values themselves, once: d_out = g dY
+      and the chain rule's [da | db] as computed, not their bf16 copies (a
+      bf16 rounding before the e4m3 one would move about 2% of the codes by
+      a whole e4m3 step).  For the same reason the chain rule takes a and b
+      unrounded (the step keeps them in fp32).
+    * The weight-gradient products take the saved h, d_out, d_gu and x at
+      the bf16 storage points of the bf16 layer (``rnd``, the hook of
       ``moe_oracle.backward``; h here is the hidden before its MX rounding).
+    * The quantisations of h, d_out and d_gu are points of the same hook
+      (:func:`_quantised`: "q_h", "q_d_out", "q_d_gu"), so that a test can
+      continue from another valid quantisation.
     * The shared expert, the router and the routing gradient are the bf16
       layer's (``moe_oracle.backward``).
 
@@ -215,23 +245,35 @@ def backward_mx(x, Wr, W_gu, W_down, Ws_gu, Ws_down, fwd, dY, norm_topk=True,
     dW_gu = np.zeros_like(W_gu)
     dW_down = np.zeros_like(W_down)
     dg = np.zeros((T, k))
-    for j in range(k):
-        for e in range(E):
+    for e in range(E):
+        if not (idx == e).any():
+            continue
+        # expert e's weight operands, quantised once: W_gate, W_up, W_down
+        # along their rows (the forward), W_down^T and W_gu^T along the
+        # data-gradient products' reduction axes
+        qg, qu, qd = quant(Wg[e]), quant(Wu[e]), quant(W_down[e])
+        qd_k, qgu_k = roundtrip_k(W_down[e], quant), roundtrip_k(W_gu[e], quant)
+        for j in range(k):
             rows = np.nonzero(idx[:, j] == e)[0]
             if not rows.size:
                 continue
             where = dict(e=e, j=j, rows=rows)
-            a = xq[rows] @ quant(Wg[e]).T
-            b = xq[rows] @ quant(Wu[e]).T
+            a = xq[rows] @ qg.T
+            b = xq[rows] @ qu.T
             hf = mo.silu(a) * b
-            out = quant(hf) @ quant(W_down[e]).T
+            out = _quantised(rnd, "q_h", hf, quant, where) @ qd.T
             dg[rows, j] = (dY[rows] * out).sum(axis=1)
             h = mo._store(rnd, "h", hf, where)
-            d_out = mo.stored_d_out(g[rows, j], dY[rows], rnd, where)
-            dH = quant(d_out) @ roundtrip_k(W_down[e], quant)
-            da, db = mo.stored_swiglu_backward(dH, a, b, rnd, where)
-            d_gu = np.concatenate([da, db], axis=1)
-            dx[rows] += quant(d_gu) @ roundtrip_k(W_gu[e], quant)
+            # d_out = g dY and d_gu = [da | db] enter their MX products
+            # quantised from their own values; their bf16 storage rounding
+            # feeds only the weight-gradient products
+            d_out_v = g[rows, j][:, None] * dY[rows]
+            d_out = mo._store(rnd, "d_out", d_out_v, where)
+            dH = _quantised(rnd, "q_d_out", d_out_v, quant, where) @ qd_k
+            da_v, db_v = mo.swiglu_backward(dH, a, b)
+            da, db = mo._store(rnd, "da", da_v, where), mo._store(rnd, "db", db_v, where)
+            d_gu = np.concatenate([da_v, db_v], axis=1)
+            dx[rows] += _quantised(rnd, "q_d_gu", d_gu, quant, where) @ qgu_k
             dW_down[e] += d_out.T @ h
             dW_gu[e, :H] += da.T @ x[rows]
             dW_gu[e, H:] += db.T @ x[rows]

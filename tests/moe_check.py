@@ -147,13 +147,94 @@ class AdoptStored:
     def __call__(self, v):
         return bf16_round(v)
 
+    def quantised(self, point, v, q, where):
+        """An MXFP8 quantisation point of a routed expert (q_h, q_d_out,
+        q_d_gu; the oracle's mx_oracle._quantised): the GPU's codes and block
+        scales for these rows, each checked to be the quantisation of some
+        value within the kernels' fp32 error of the oracle's unquantised v
+        (mx_valid), and continued from; q is the oracle's own Q(v).  At most
+        max_frac_q of the codes may differ from the oracle's, none may be
+        invalid.  Points without a GPU source return q."""
+        from oracle import mx_oracle as M
+        if point not in self.gpu:
+            return q
+        rows = np.asarray(where["rows"])
+        if self.tokens is not None:
+            rows = self.tokens[rows]
+        codes, sbytes = self.gpu[point][0](self.row_of_pair[rows * self.k + where["j"]])
+        valid, other = mx_valid(v, codes, sbytes)
+        st = self.stats.setdefault(point, [0, 0, 0])
+        st[0] += codes.size
+        st[1] += int(other.sum())
+        st[2] += int((~valid).sum())
+        return M.mx_dequantize(codes, sbytes)
+
     def check(self, chk):
         """Rows for a Checker: invalid choices (must be 0) and the fraction
-        of elements that took the other neighbour (<= max_frac)."""
+        of elements that took the other neighbour (<= max_frac; for the MX
+        quantisation points, <= max_frac_q of the codes)."""
         for p, (n, diff, bad) in sorted(self.stats.items()):
-            chk.rows.append((f"stored {p}: invalid", float(bad), 0.0))
-            chk.rows.append((f"stored {p}: other rounding (frac)", diff / max(n, 1),
-                             self.max_frac))
+            q = p.startswith("q_")
+            chk.rows.append((f"{'quantised' if q else 'stored'} {p}: invalid", float(bad), 0.0))
+            chk.rows.append((f"{'quantised' if q else 'stored'} {p}: other "
+                             f"{'code' if q else 'rounding'} (frac)", diff / max(n, 1),
+                             MAX_FRAC_Q if q else self.max_frac))
+
+
+# at most this fraction of a quantisation point's codes may differ from the
+# oracle's (each a valid quantisation of a value within fp32 error)
+MAX_FRAC_Q = 1e-3
+
+
+def mx_valid(v, codes, sbytes, tol_rel=2.0 ** -18, tol_abs=2.0 ** -16):
+    """Is each GPU MX code [n][K] (with its block scale bytes [n][K/32]) the
+    quantisation of a value within e = tol_rel |v| + tol_abs amax(block) of
+    the oracle's v?  The block scale must be the one of v's block maximum,
+    or one off where that maximum lies within the tolerance of a power of
+    two; each code must lie between the e4m3 roundings, under the GPU's
+    scale, of v - e and v + e (the rounding is monotone).  The tolerances
+    cover fp32 against fp64 arithmetic (products, dot products over a few
+    thousand terms) and are far below an e4m3 step (2^-4 relative).
+    Returns (valid, differs from the oracle's own code or scale), each
+    [n][K] bool."""
+    from oracle import mx_oracle as M
+    v = np.asarray(v, dtype=np.float64)
+    n, K = v.shape
+    b = v.reshape(n, K // 32, 32)
+    amax = np.abs(b).max(axis=-1)
+    c_o, s_o = M.mx_quantize(v)
+    sg = np.asarray(sbytes).astype(np.int64)
+    so = s_o.astype(np.int64)
+    t = tol_rel + tol_abs
+    crosses = M.mx_scale_exp(amax * (1 + t)) != M.mx_scale_exp(amax * (1 - t))
+    scale_ok = (sg == so) | ((np.abs(sg - so) == 1) & crosses)
+    e = tol_rel * np.abs(b) + tol_abs * amax[..., None]
+    sc = np.exp2(sg - 127.0)[..., None]
+    lo = M.e4m3_decode(M.e4m3_round((b - e) / sc))
+    hi = M.e4m3_decode(M.e4m3_round((b + e) / sc))
+    g = M.e4m3_decode(np.asarray(codes).reshape(n, K // 32, 32))
+    ok = (g >= lo) & (g <= hi) & scale_ok[..., None]
+    other = (np.asarray(codes) != c_o).reshape(n, K // 32, 32) | (sg != so)[..., None]
+    return ok.reshape(n, K), other.reshape(n, K)
+
+
+def mx_rows_from(q_buf, s_buf, R, K):
+    """Function of permuted rows -> (codes [n][K], scale bytes [n][K/32]) of
+    an MX buffer pair: codes [R][K] and scale atoms [R/128][K/128][512]
+    (row r, block kb at byte (r%32)*16 + ((r/32)%4)*4 + kb%4 of its atom)."""
+    import torch
+    cache = {}
+
+    def get(rows):
+        rows = np.asarray(rows, dtype=np.int64)
+        if "s" not in cache:
+            cache["s"] = s_buf.cpu().numpy()
+        q = q_buf[:R * K].view(R, K)[torch.as_tensor(rows, device=q_buf.device)]
+        r = rows[:, None]
+        kb = np.arange(K // 32)[None, :]
+        idx = ((r >> 7) * (K // 128) + (kb >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (kb & 3)
+        return q.cpu().numpy(), cache["s"][idx]
+    return get
 
 
 def stored_from_layer(lay, with_backward, cols=None, shared_cols=None):
@@ -186,6 +267,17 @@ def stored_from_layer(lay, with_backward, cols=None, shared_cols=None):
         out["d_out"] = (pick(it["d_out"], 0, lay.cfg.d, None), None)
         out["da"] = (pick(it["d_gu"], 0, H, cols), pick(it.get("ds_gu"), 0, Hs, shared_cols))
         out["db"] = (pick(it["d_gu"], H, H, cols), pick(it.get("ds_gu"), Hs, Hs, shared_cols))
+    mx = getattr(lay, "mx", None)
+    if mx is not None:
+        # the MXFP8 path's quantised operands (codes + block scales per row;
+        # those of h and d_gu only for whole rows of hidden units)
+        R = lay.R_cap
+        if cols is None:
+            out["q_h"] = (mx_rows_from(mx["h_q"], mx["h_s"], R, H), None)
+        if with_backward and mx.get("dout_q") is not None:
+            out["q_d_out"] = (mx_rows_from(mx["dout_q"], mx["dout_s"], R, lay.cfg.d), None)
+            if cols is None:
+                out["q_d_gu"] = (mx_rows_from(mx["dgu_q"], mx["dgu_s"], R, 2 * H), None)
     return out
 
 

@@ -46,7 +46,7 @@ def test_library_exports_every_declared_symbol(clib):
 
 
 def test_abi_version_and_messages(clib):
-    assert clib.moe_abi_version() == 4
+    assert clib.moe_abi_version() == 5
     for code in range(10):
         assert clib.moe_strerror(code)
     assert b"unknown" in clib.moe_strerror(99)
@@ -130,13 +130,21 @@ def test_mx_sizes_and_shape_rule(clib):
     assert list(sizes) == [E * 2 * H * d, E * 2 * H * d // 32, E * d * H, E * d * H // 32,
                            R * d, R * d // 32, R * H, R * H // 32,
                            2 * Hs * d, 2 * Hs * d // 32, d * Hs, d * Hs // 32,
-                           Tp * d, Tp * d // 32, Tp * Hs, Tp * Hs // 32]
+                           Tp * d, Tp * d // 32, Tp * Hs, Tp * Hs // 32,
+                           # the training step's: transposed weights, d_out, d_gu
+                           E * d * 2 * H, E * d * 2 * H // 32, E * H * d, E * H * d // 32,
+                           R * d, R * d // 32, R * 2 * H, R * 2 * H // 32, R * 2 * H * 4]
     c5 = binding.config(synth.shape(5))              # no shared expert: its buffers are 0
     assert clib.moe_mx_sizes(ctypes.byref(c5), sizes) == 0
-    assert list(sizes)[8:] == [0] * 8
+    assert list(sizes)[8:16] == [0] * 8 and min(list(sizes)[16:]) > 0
     tiny = binding.config(synth.shape(1))
     assert clib.moe_mx_sizes(ctypes.byref(tiny), sizes) == 2
     t = binding.MoETensors()
     m = binding.MoEMxTensors()
     assert clib.moe_mx_forward(ctypes.byref(tiny), ctypes.byref(t), ctypes.byref(m), None, 0,
                                None) == 2
+    assert clib.moe_mx_forward_train(ctypes.byref(tiny), ctypes.byref(t), ctypes.byref(m),
+                                     None, 0, None) == 2
+    gr = binding.MoEGrads()
+    assert clib.moe_mx_backward(ctypes.byref(tiny), ctypes.byref(t), ctypes.byref(m),
+                                ctypes.byref(gr), None, 0, None) == 2

@@ -20,7 +20,8 @@ from mixture_experts_ffn_02_gb300 import synth
 from mixture_experts_ffn_02_gb300.binding import Layer
 from oracle import moe_oracle as O
 from oracle import mx_oracle as M
-from moe_check import Checker, logit_error_bound, np64, reconcile_selection
+from moe_check import (AdoptStored, Checker, bf16_round, frob_err, logit_error_bound, np64,
+                       padded_layout, reconcile_selection, stored_from_layer)
 
 pytestmark = pytest.mark.gpu
 
@@ -52,6 +53,15 @@ def unpack_w_down(atoms, E, d, H):
     a = atoms.reshape(E, d // 128, H // 128, ATOM)
     n = np.arange(d)
     kb = np.arange(H // 32)
+    return a[:, n[:, None] // 128, kb[None, :] // 4, sf_byte(n[:, None] % 128, kb[None, :] % 4)]
+
+
+def unpack_w(atoms, E, N, K):
+    """Per-expert scale atoms [E][N/128][K/128][512] of N rows quantised
+    along K -> scale bytes [E][N][K/32]."""
+    a = atoms.reshape(E, N // 128, K // 128, ATOM)
+    n = np.arange(N)
+    kb = np.arange(K // 32)
     return a[:, n[:, None] // 128, kb[None, :] // 4, sf_byte(n[:, None] % 128, kb[None, :] % 4)]
 
 
@@ -364,3 +374,258 @@ def test_mx_edge_shapes(name, shape, bias):
     chk = Checker()
     chk.close("y_mx", lay.bufs["y"], y_mx)
     chk.done()
+
+
+# --------------------------------------------------------------------------
+# The MXFP8 training step: moe_mx_forward_train + moe_mx_backward
+# --------------------------------------------------------------------------
+
+def mx_train_layer(s, seed=0):
+    inp = synth.make_inputs(s, seed=seed, with_grad=True)
+    lay = Layer.create(s, training=True)
+    dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    lay.set_inputs(dev["x"], dev["Wr"], dev["W_gu"], dev["W_down"], dev["Ws_gu"],
+                   dev["Ws_down"], bias=dev["bias"], valid=dev["valid"])
+    lay.mx_alloc()
+    lay.mx_quantize_weights()
+    lay.mx_step(dev["dY"])
+    torch.cuda.synchronize()
+    assert lay.status() == 0
+    return inp, lay
+
+
+def train_fwd(s, inp, r):
+    fwd = dict(r)
+    fwd["real"] = np.ones(s.T, bool) if inp["valid"] is None else inp["valid"].numpy() != 0
+    return fwd
+
+
+def half_ulp_bf16_of(v):
+    a = np.abs(v)
+    return np.where(a > 0, np.exp2(np.floor(np.log2(np.where(a > 0, a, 1.0))) - 8), 0.0)
+
+
+@pytest.mark.parametrize("cfg,T,over", SCALED)
+def test_mx_train_operand_codes_bit_exact(cfg, T, over):
+    """The data-gradient products' operands: each expert's W_gu^T and
+    W_down^T quantised along 2H and d, bit for bit with the oracle's
+    quantiser; the codes of d_out = g dY (along d) bit for bit with the
+    oracle quantising the same fp32 products (the fp32 gate times the bf16
+    dY, rounded to fp32 as one multiply does), pad rows zero; and the codes
+    of d_gu (along 2H), quantised from fp32 values the GPU does not keep:
+    each block scale is that of the stored bf16 d_gu or one less, and each
+    code lies between the e4m3 roundings, under the GPU's scale, of the
+    stored value minus and plus half a bf16 ulp (the fp32 value lies there,
+    and the rounding is monotone)."""
+    s = scaled_shape(cfg, T, over)
+    inp, lay = mx_train_layer(s)
+    E, d, H, R = s.E, s.d, s.H, lay.R_cap
+    mx = lay.mx
+    c, sc = M.mx_quantize(np.swapaxes(np64(inp["W_gu"]), 1, 2))           # [E][d][2H]
+    np.testing.assert_array_equal(u8(mx["W_gu_tq"], E * d * 2 * H).reshape(E, d, 2 * H), c)
+    np.testing.assert_array_equal(unpack_w(u8(mx["W_gu_ts"], E * d * 2 * H // 32), E, d,
+                                           2 * H), sc)
+    c, sc = M.mx_quantize(np.swapaxes(np64(inp["W_down"]), 1, 2))         # [E][H][d]
+    np.testing.assert_array_equal(u8(mx["W_down_tq"], E * H * d).reshape(E, H, d), c)
+    np.testing.assert_array_equal(unpack_w(u8(mx["W_down_ts"], E * H * d // 32), E, H, d), sc)
+    inv = lay.bufs["inv"].cpu().numpy().reshape(-1)
+    pair = np.nonzero(inv >= 0)[0]
+    rows = inv[pair]
+    gates = lay.bufs["gates"].cpu().numpy().reshape(-1)[pair].astype(np.float32)
+    dY = inp["dY"].float().numpy()[pair // s.k]
+    c, sc = M.mx_quantize((gates[:, None] * dY).astype(np.float64))   # fp32 products
+    q = u8(mx["dout_q"], R * d).reshape(R, d)
+    sb = unpack_rows(u8(mx["dout_s"], R * d // 32), d, R)
+    np.testing.assert_array_equal(q[rows], c)
+    np.testing.assert_array_equal(sb[rows], sc)
+    used = np.zeros(R, bool)
+    used[rows] = True
+    n_rows = int(lay.bufs["row_offsets"][-1])
+    pad = ~used[:n_rows]
+    assert not q[:n_rows][pad].any() and not sb[:n_rows][pad].any()
+    # d_gu
+    K = 2 * H
+    v = np64(lay.intermediates()["d_gu"])[rows]
+    q = u8(mx["dgu_q"], R * K).reshape(R, K)[rows]
+    sb = unpack_rows(u8(mx["dgu_s"], R * K // 32), K, R)[rows]
+    _, s_bf = M.mx_quantize(v)
+    assert np.isin(sb.astype(int) - s_bf.astype(int), (0, -1)).all()
+    scale = np.repeat(np.exp2(sb.astype(np.float64) - 127.0), 32, axis=1)
+    hu = half_ulp_bf16_of(v)
+    lo = M.e4m3_decode(M.e4m3_round((v - hu) / scale))
+    hi = M.e4m3_decode(M.e4m3_round((v + hu) / scale))
+    got = M.e4m3_decode(q)
+    assert ((got >= lo) & (got <= hi)).all()
+    # and it is not the quantisation of the bf16 copy: that differs in a few
+    # percent of the codes (about 2%), each by one e4m3 step
+    c_bf, _ = M.mx_quantize(v)
+    frac = float((c_bf != q).mean())
+    assert 1e-3 < frac < 0.1, frac
+
+
+@pytest.mark.parametrize("cfg,T,over", SCALED)
+def test_mx_train_step_matches_oracle(cfg, T, over):
+    """y and every gradient of the MXFP8 training step against the MX
+    training oracle: max normalised |gpu - ideal| <= 1e-2, where ideal
+    continues from the GPU's stored bf16 values where they are the other
+    valid rounding, and Frobenius-relative |gpu - exact| <= 1e-2."""
+    s = scaled_shape(cfg, T, over)
+    inp, lay = mx_train_layer(s)
+    r, x, valid = route_like_gpu(s, inp, lay)
+    np.testing.assert_array_equal(lay.bufs["topk_idx"].cpu().numpy(), r["topk_idx"])
+    fwd = train_fwd(s, inp, r)
+    adopt = AdoptStored(stored_from_layer(lay, True), padded_layout(r["topk_idx"], s.E)[2], s.k)
+    fw = (x, r["topk_idx"], r["gates"], inp["W_gu"], inp["W_down"], inp["Ws_gu"],
+          inp["Ws_down"], valid)
+    y_ex, _ = M.experts_forward_mx(*fw, shared_mx=False)
+    y_id, _ = M.experts_forward_mx(*fw, shared_mx=False, rnd=adopt)
+    args = (x, inp["Wr"], inp["W_gu"], inp["W_down"], inp["Ws_gu"], inp["Ws_down"], fwd,
+            inp["dY"])
+    kw = dict(norm_topk=bool(s.norm_topk), aux_coef=s.aux_coef)
+    ex = M.backward_mx(*args, **kw)
+    idl = M.backward_mx(*args, rnd=adopt, **kw)
+    g = lay.grads
+    chk = Checker()
+    chk.layer("y", lay.bufs["y"], y_ex, y_id)
+    names = ["d_logits", "dW_down", "dW_gu", "dx", "dWr"]
+    if s.n_shared:
+        names += ["dWs_down", "dWs_gu"]
+    for n in names:
+        chk.layer(n, g[n], ex[n], idl[n])
+    adopt.check(chk)
+    chk.done()
+    if valid is not None:
+        pad = inp["valid"] == 0
+        assert (g["dx"].cpu()[pad].float() == 0).all()
+
+
+def test_mx_train_step_differs_from_bf16_layer():
+    """The tolerance tells the MX training step from the bf16 layer's: the
+    GPU's dx, dW_gu and dW_down are within 1e-2 (Frobenius-relative) of the
+    MX oracle with bf16 storage rounding and several times further from the
+    bf16 layer's oracle with the same rounding."""
+    s = synth.MoEShape("mxtrain", T=600, d=256, E=8, k=2, H=256, n_shared=0, H_shared=0,
+                       training=True)
+    inp, lay = mx_train_layer(s)
+    r, x, valid = route_like_gpu(s, inp, lay)
+    fwd = train_fwd(s, inp, r)
+    args = (x, inp["Wr"], inp["W_gu"], inp["W_down"], None, None, fwd, inp["dY"])
+    mx = M.backward_mx(*args, rnd=bf16_round)
+    bf = O.backward(*args, rnd=bf16_round)
+    for n in ("dx", "dW_gu", "dW_down"):
+        e_mx = frob_err(np64(lay.grads[n]), mx[n])
+        e_bf = frob_err(np64(lay.grads[n]), bf[n])
+        assert e_mx <= 1e-2 and e_bf > 3 * e_mx, (n, e_mx, e_bf)
+
+
+def test_mx_train_step_is_deterministic():
+    s = scaled_shape(5, 1300, dict(d=512, H=256))
+    inp, lay = mx_train_layer(s)
+    keep = {n: lay.grads[n].clone() for n in ("dx", "dW_gu", "dW_down", "d_logits")}
+    y0 = lay.bufs["y"].clone()
+    lay.mx_step(inp["dY"].cuda())
+    torch.cuda.synchronize()
+    assert torch.equal(y0, lay.bufs["y"])
+    for n, v in keep.items():
+        assert torch.equal(v, lay.grads[n]), n
+
+
+@pytest.mark.parametrize("cfg,n_tok", [(5, 3), (2, 8)])
+def test_mx_train_full_size_sampled(cfg, n_tok):
+    """The training step at its full size, in the calls bench.py times
+    (Layer.mx_step): the routing in full, and y, dx and d_logits of a few
+    seeded tokens (the last one included) against the MX training oracle
+    evaluated on those tokens with the batch's expert loads f; and eight
+    columns of dW_down and eight hidden units of dW_gu of one expert, over
+    all of that expert's rows."""
+    s = synth.shape(cfg)
+    inp, lay = mx_train_layer(s)
+    b, g = lay.bufs, lay.grads
+    x = np64(inp["x"])
+    L = O.router_logits(inp["x"], inp["Wr"])
+    bias = None if inp["bias"] is None else inp["bias"].numpy().astype(np.float64)
+    key = L + (0.0 if bias is None else bias)
+    real = np.ones(s.T, bool) if inp["valid"] is None else inp["valid"].numpy() != 0
+    sel, _ = reconcile_selection(b["topk_idx"].cpu().numpy(), key,
+                                 logit_error_bound(x, np64(inp["Wr"])), s.k, real)
+    probs = O.softmax(L)
+    r = O.route_stats(probs, sel, real, bool(s.norm_topk))
+    np.testing.assert_array_equal(b["topk_idx"].cpu().numpy(), r["topk_idx"])
+    offsets, row_offsets, row_of_pair, _ = padded_layout(r["topk_idx"], s.E)
+    np.testing.assert_array_equal(b["row_offsets"].cpu().numpy(), row_offsets)
+    np.testing.assert_array_equal(b["inv"].cpu().numpy(), row_of_pair)
+    chk = Checker()
+    # ---- sampled tokens
+    rng = np.random.default_rng(100 + cfg)
+    ts = np.append(np.sort(rng.choice(s.T - 1, size=n_tok - 1, replace=False)), s.T - 1)
+    tsc = torch.from_numpy(ts)
+    tsd = tsc.cuda()
+    fwd = dict(topk_idx=r["topk_idx"][ts], gates=r["gates"][ts], probs=probs[ts],
+               real=real[ts], f=r["f"])
+    adopt = AdoptStored(stored_from_layer(lay, True), row_of_pair, s.k, tokens=ts)
+    # the forward on the experts the sample chose (renumbered), the backward
+    # with the router's own numbering (only chosen experts are quantised)
+    topk = fwd["topk_idx"]
+    used = np.unique(topk[topk >= 0])
+    topk_c = np.where(topk >= 0, np.searchsorted(used, np.maximum(topk, 0)), -1)
+    ut = torch.from_numpy(used)
+    xs = x[ts]
+    ys = {}
+    for name, rnd in (("exact", None), ("ideal", adopt)):
+        ys[name], _ = M.experts_forward_mx(xs, topk_c, fwd["gates"], inp["W_gu"][ut],
+                                           inp["W_down"][ut], inp["Ws_gu"], inp["Ws_down"],
+                                           real[ts].astype(np.uint8), shared_mx=False, rnd=rnd)
+    chk.layer("y[sample]", b["y"][tsd], ys["exact"], ys["ideal"])
+    coef = s.aux_coef * max(int(real[ts].sum()), 1) / int(real.sum())
+    args = (xs, inp["Wr"], inp["W_gu"], inp["W_down"], inp["Ws_gu"], inp["Ws_down"], fwd,
+            inp["dY"][tsc])
+    ex = M.backward_mx(*args, norm_topk=bool(s.norm_topk), aux_coef=coef)
+    idl = M.backward_mx(*args, norm_topk=bool(s.norm_topk), aux_coef=coef, rnd=adopt)
+    chk.layer("dx[sample]", g["dx"][tsd], ex["dx"], idl["dx"])
+    chk.layer("d_logits[sample]", g["d_logits"][tsd], ex["d_logits"], idl["d_logits"])
+    adopt.check(chk)
+    # ---- one expert's weight gradients on sampled columns: the MX products
+    # restricted to hidden units J (rows of W_gate, W_up and columns of
+    # W_down are quantised on their own, and d_out's codes are whole rows, so
+    # the restriction is exact)
+    e = int(np.argsort(r["counts"])[len(r["counts"]) // 2])
+    seg = O.permute(r["topk_idx"], s.E)[1][offsets[e]:offsets[e + 1]]
+    tok, slot = seg // s.k, seg % s.k
+    gate = r["gates"][tok, slot]
+    Wg, Wu = O.split_gu(np64(inp["W_gu"][e]))
+    Wd = np64(inp["W_down"][e])
+    dY = np64(inp["dY"])
+    J = np.sort(rng.choice(s.H, size=8, replace=False))
+    xq = M.mx_roundtrip(x[tok])
+    qg, qu = M.mx_roundtrip(Wg[J]), M.mx_roundtrip(Wu[J])
+    qdk = M.roundtrip_k(Wd[:, J])
+    adopt_e = AdoptStored(stored_from_layer(lay, True, cols=J), row_of_pair, s.k)
+    res = {}
+    for name, rnd in (("exact", None), ("ideal", adopt_e)):
+        dWd = np.zeros((s.d, J.size)); dWg = np.zeros((J.size, s.d)); dWu = np.zeros((J.size, s.d))
+        for j in range(s.k):
+            m = slot == j
+            if not m.any():
+                continue
+            where = dict(e=e, j=j, rows=tok[m])
+            a = xq[m] @ qg.T
+            bb = xq[m] @ qu.T
+            h = O._store(rnd, "h", O.silu(a) * bb, where)
+            d_out_v = gate[m][:, None] * dY[tok[m]]
+            d_out = O._store(rnd, "d_out", d_out_v, where)
+            dH = M._quantised(rnd, "q_d_out", d_out_v, M.mx_roundtrip, where) @ qdk
+            da_v, db_v = O.swiglu_backward(dH, a, bb)       # a, b kept in fp32
+            da, db = O._store(rnd, "da", da_v, where), O._store(rnd, "db", db_v, where)
+            dWd += d_out.T @ h
+            dWg += da.T @ x[tok[m]]
+            dWu += db.T @ x[tok[m]]
+        res[name] = (dWd, dWg, dWu)
+    jt = torch.from_numpy(J).cuda()
+    for nm, gv, k_ in (("dW_down[e]", g["dW_down"][e][:, jt], 0),
+                       ("dW_gate[e]", g["dW_gu"][e][jt], 1),
+                       ("dW_up[e]", g["dW_gu"][e][jt + s.H], 2)):
+        chk.layer(nm, gv, res["exact"][k_], res["ideal"][k_])
+    adopt_e.check(chk)
+    chk.done()
+    del lay
+    torch.cuda.empty_cache()

@@ -301,12 +301,30 @@ def test_mx_dgrad_weights_quantised_along_the_wrong_axis_are_caught(monkeypatch)
 
 def test_mx_dgrad_unquantised_d_gu_is_caught(monkeypatch):
     src = inspect.getsource(M.backward_mx)
-    needle = "dx[rows] += quant(d_gu) @"
+    needle = 'dx[rows] += _quantised(rnd, "q_d_gu", d_gu, quant, where) @'
     assert needle in src
     ns = dict(vars(M))
     exec(src.replace(needle, "dx[rows] += d_gu @"), ns)
     monkeypatch.setattr(M, "backward_mx", ns["backward_mx"])
     assert _fails(MXP.test_mx_backward_quantises_each_operand_along_its_reduction_axis)
+    assert _fails(MXP.test_mx_backward_dense_masked_formulation)
+
+
+@pytest.mark.parametrize("needle,planted", [
+    ('dH = _quantised(rnd, "q_d_out", d_out_v,', 'dH = _quantised(rnd, "q_d_out", d_out,'),
+    ("da_v, db_v = mo.swiglu_backward(dH, a, b)",
+     'da_v, db_v = mo.swiglu_backward(dH, mo._store(rnd, "a", a, where), '
+     'mo._store(rnd, "b", b, where))'),
+    ("d_gu = np.concatenate([da_v, db_v], axis=1)", "d_gu = np.concatenate([da, db], axis=1)"),
+])
+def test_mx_dgrad_quantising_the_bf16_copy_is_caught(monkeypatch, needle, planted):
+    """Quantising the bf16-stored d_out or d_gu (a double rounding) instead
+    of the values themselves, or taking the chain rule on bf16 a and b."""
+    src = inspect.getsource(M.backward_mx)
+    assert needle in src
+    ns = dict(vars(M))
+    exec(src.replace(needle, planted), ns)
+    monkeypatch.setattr(M, "backward_mx", ns["backward_mx"])
     assert _fails(MXP.test_mx_backward_dense_masked_formulation)
 
 

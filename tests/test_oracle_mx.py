@@ -248,14 +248,23 @@ def test_mx_backward_is_the_bf16_backward_with_bf16_rounding(norm):
     """With the MX round trip replaced by a bf16 round trip and inputs that
     bf16 holds exactly, the MX training step's backward is the bf16 layer's
     backward (pinned by finite differences and the storage pins), term for
-    term: Q(h) in the down product plays the bf16 layer's stored h, and the
-    other quantised operands are bf16 values already."""
+    term, once the bf16 layer's routed experts also take the chain rule on
+    unrounded a and b (the MX step keeps them in fp32): Q(h) in the down
+    product plays the bf16 layer's stored h, Q(d_out) and Q(d_gu) its stored
+    d_out and d_gu, and the other quantised operands are bf16 values
+    already."""
     x, Wr, W_gu, W_down, Ws_gu, Ws_down, dY, fwd = _train_case(7, norm=norm)
     x, W_gu, W_down, Ws_gu, Ws_down, dY = map(_bf16, (x, W_gu, W_down, Ws_gu, Ws_down, dY))
     fwd = M.forward_mx_train(x, Wr, W_gu, W_down, Ws_gu, Ws_down, k=2, norm_topk=norm)
     args = (x, Wr, W_gu, W_down, Ws_gu, Ws_down, fwd, dY)
     got = M.backward_mx(*args, norm_topk=norm, rnd=_bf16, quant=_bf16)
-    ref = O.backward(*args, norm_topk=norm, rnd=_bf16)
+
+    class RoutedABUnrounded:
+        def store(self, point, v, where):
+            if point in ("a", "b") and not where.get("shared"):
+                return v
+            return _bf16(v)
+    ref = O.backward(*args, norm_topk=norm, rnd=RoutedABUnrounded())
     for n in ("dx", "dWr", "dW_gu", "dW_down", "dWs_gu", "dWs_down", "d_logits", "dg"):
         np.testing.assert_allclose(got[n], ref[n], rtol=1e-12, atol=1e-12, err_msg=n)
 
@@ -298,11 +307,23 @@ def test_mx_backward_quantises_each_operand_along_its_reduction_axis():
     M.backward_mx(x, Wr, W_gu, W_down, None, None, fwd, dY, rnd=_bf16, quant=spy)
     assert spy.shapes[0] == x.shape                           # Q(x), once
     rest = spy.shapes[1:]
-    assert len(rest) % 8 == 0
-    for i in range(0, len(rest), 8):
-        g = rest[i:i + 8]
-        n = g[2][0]
-        assert g == [(H, d), (H, d), (n, H), (d, H), (n, d), (H, d), (n, 2 * H), (d, 2 * H)], g
+    # per expert with rows: its weights once -- W_gate, W_up [H][d], W_down
+    # [d][H], W_down^T [H][d], W_gu^T [d][2H] -- then per group of n rows
+    # h [n][H], d_out [n][d], d_gu [n][2H]
+    weights = [(H, d), (H, d), (d, H), (H, d), (d, 2 * H)]
+    i = n_experts = n_groups = 0
+    while i < len(rest):
+        assert rest[i:i + 5] == weights, rest[i:i + 5]
+        i += 5
+        n_experts += 1
+        while i < len(rest) and rest[i:i + 5] != weights:
+            n = rest[i][0]
+            assert rest[i:i + 3] == [(n, H), (n, d), (n, 2 * H)], rest[i:i + 3]
+            i += 3
+            n_groups += 1
+    idx = fwd["topk_idx"]
+    assert n_experts == len(np.unique(idx[idx >= 0]))
+    assert n_groups == sum(len(np.unique(idx[:, j][idx[:, j] >= 0])) for j in range(idx.shape[1]))
 
 
 def test_mx_backward_dense_masked_formulation():
@@ -331,11 +352,10 @@ def test_mx_backward_dense_masked_formulation():
             m = fwd["topk_idx"][:, j] == e
             gte = np.where(m, fwd["gates"][:, j], 0.0)
             dg[:, j] += np.where(m, (dY * out).sum(axis=1), 0.0)
-            d_out = _bf16(gte[:, None] * dY)
-            dH = Q(d_out) @ WdT.T
-            sa = 1 / (1 + np.exp(-_bf16(a)))
-            da = _bf16(dH * _bf16(b) * sa * (1 + _bf16(a) * (1 - sa)))
-            db = _bf16(dH * _bf16(a) * sa)
+            dH = Q(gte[:, None] * dY) @ WdT.T       # d_out quantised from g dY itself
+            sa = 1 / (1 + np.exp(-a))
+            da = dH * b * sa * (1 + a * (1 - sa))
+            db = dH * a * sa
             dx += np.where(m[:, None], Q(np.concatenate([da, db], axis=1)) @ WguT.T, 0.0)
     dL = O.router_logit_grad(dg, fwd["topk_idx"], fwd["gates"], fwd["probs"], True)
     dL += O.aux_logit_grad(fwd["probs"], fwd["f"], fwd["real"], 0.01)
@@ -355,3 +375,59 @@ def test_mx_backward_differs_from_bf16_by_the_quantisation():
     rel = np.abs(mx["dx"] - bf["dx"]).max() / np.abs(bf["dx"]).max()
     assert 1e-3 < rel < 0.2
     np.testing.assert_allclose(mx["dWs_gu"], bf["dWs_gu"], rtol=1e-12, atol=1e-12)
+
+
+class _QuantSpy:
+    """Storage hook (bf16) with the quantisation-point method: records each
+    point with its shape and group, checks that the oracle hands it Q(v),
+    and returns Q(v) or, for the points in ``override``, override(Q(v))."""
+
+    def __init__(self, override=None):
+        self.seen = []
+        self.override = override or {}
+
+    def __call__(self, v):
+        return _bf16(v)
+
+    def quantised(self, point, v, q, where):
+        self.seen.append((point, v.shape, where["e"], where["j"]))
+        np.testing.assert_array_equal(q, M.mx_roundtrip(v))
+        return self.override.get(point, lambda a: a)(q)
+
+
+def test_mx_quantisation_points_feed_their_products():
+    """The hook sees Q(h), Q(d_out) and Q(d_gu) once per (expert, slot)
+    group, in that order and with the group's rows, and what it returns is
+    what the products use: Q(d_gu) only the routed dx, Q(d_out) the dH
+    product (so da, db and dW_gu) but not dW_down, and Q(h) only dg."""
+    x, Wr, W_gu, W_down, Ws_gu, Ws_down, dY, fwd = _train_case(8, shared=False)
+    d, H = 64, 96
+    args = (x, Wr, W_gu, W_down, None, None, fwd, dY)
+    spy = _QuantSpy()
+    base = M.backward_mx(*args, rnd=spy)
+    pts = [p for p, *_ in spy.seen]
+    assert pts == ["q_h", "q_d_out", "q_d_gu"] * (len(pts) // 3) and pts
+    for i in range(0, len(spy.seen), 3):
+        (_, sh, e, j), (_, sd, e2, j2), (_, sg, e3, j3) = spy.seen[i:i + 3]
+        n = int((fwd["topk_idx"][:, j] == e).sum())
+        assert (sh, sd, sg) == ((n, H), (n, d), (n, 2 * H)) and (e, j) == (e2, j2) == (e3, j3)
+    router_dx = base["d_logits"] @ np.asarray(Wr, dtype=np.float64).T
+    z = M.backward_mx(*args, rnd=_QuantSpy({"q_d_gu": np.zeros_like}))
+    np.testing.assert_allclose(z["dx"], router_dx, rtol=1e-12, atol=1e-12)
+    for n in ("dW_gu", "dW_down", "d_logits"):
+        np.testing.assert_array_equal(z[n], base[n])
+    z = M.backward_mx(*args, rnd=_QuantSpy({"q_d_out": np.zeros_like}))
+    assert not z["dW_gu"].any()
+    np.testing.assert_allclose(z["dx"], router_dx, rtol=1e-12, atol=1e-12)
+    np.testing.assert_array_equal(z["dW_down"], base["dW_down"])
+    z = M.backward_mx(*args, rnd=_QuantSpy({"q_h": np.zeros_like}))
+    assert not z["dg"].any()
+    for n in ("dW_gu", "dW_down"):
+        np.testing.assert_array_equal(z[n], base[n])
+    # the forward: Q(h) per group, and a zero Q(h) leaves no routed output
+    spy = _QuantSpy()
+    y0, _ = M.experts_forward_mx(x, fwd["topk_idx"], fwd["gates"], W_gu, W_down, rnd=spy)
+    assert [p for p, *_ in spy.seen] == ["q_h"] * len(spy.seen) and spy.seen
+    y1, _ = M.experts_forward_mx(x, fwd["topk_idx"], fwd["gates"], W_gu, W_down,
+                                 rnd=_QuantSpy({"q_h": np.zeros_like}))
+    assert y0.any() and not y1.any()

@@ -88,3 +88,44 @@ def test_one_ulp_flips_of_stored_h_exceed_max_metric_on_weight_grads():
     flipped = O.backward(*args, rnd=_FlipSome(1e-3))
     assert norm_err(flipped["dW_down"], ideal["dW_down"]) > 1e-2
     assert frob_err(flipped["dW_down"], ideal["dW_down"]) < 1e-3
+
+
+def test_mx_valid_accepts_exactly_the_nearby_quantisations():
+    """moe_check.mx_valid, which lets the GPU tests continue from the GPU's
+    own MX codes: the oracle's codes are valid and not "other"; the other
+    e4m3 neighbour is valid only where v lies within the fp32 tolerance of
+    the midpoint between the two; a code two steps away, or a block scale
+    one off away from a power of two, is invalid."""
+    from moe_check import mx_valid
+    from oracle import mx_oracle as M
+    rng = np.random.default_rng(3)
+    v = rng.standard_normal((4, 64))
+    c, s = M.mx_quantize(v)
+    ok, other = mx_valid(v, c, s)
+    assert ok.all() and not other.any()
+    # put element (0, 5) on the midpoint between two codes of its block grid
+    X = s[0, 0].astype(float) - 127
+    g = M.e4m3_decode(c[0, 5]) * 2.0 ** X
+    up = M.e4m3_decode(np.uint8(c[0, 5] + 1)) * 2.0 ** X
+    v2 = v.copy()
+    v2[0, 5] = (g + up) / 2 * (1 + 2.0 ** -30)       # just above the midpoint
+    c2, s2 = M.mx_quantize(v2)
+    assert s2[0, 0] == s[0, 0]
+    flip = c2.copy()
+    flip[0, 5] = c2[0, 5] - 1                         # the neighbour below: valid here
+    ok, other = mx_valid(v2, flip, s2)
+    assert ok.all() and other.sum() == 1
+    flip = c.copy()
+    flip[1, 7] = c[1, 7] + 1 if c[1, 7] & 0x7F < 0x7D else c[1, 7] - 1    # far from a midpoint
+    ok, _ = mx_valid(v, flip, s)
+    assert (~ok).sum() == 1 and not ok[1, 7]
+    two = c.copy()
+    two[2, 3] = (c[2, 3] & 0x80) | max((c[2, 3] & 0x7F) - 2, 0)
+    ok, _ = mx_valid(v, two, s)
+    assert not ok[2, 3]
+    bad_s = s.copy()
+    bad_s[3, 1] += 1
+    amax = np.abs(v[3, 32:64]).max()
+    assert abs(np.log2(amax) - np.round(np.log2(amax))) > 1e-3   # not near a power of two
+    ok, _ = mx_valid(v, c, bad_s)
+    assert not ok[3, 32:64].any() and ok[3, :32].all()
