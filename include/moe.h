@@ -409,7 +409,7 @@ typedef struct moe_mx_tensors {
   uint8_t* dout_s;    /* [R_cap/128][d/128] atoms                                */
   uint8_t* dgu_q;     /* [R_cap][2H] codes of d_gu = da | db (blocks along 2H)   */
   uint8_t* dgu_s;     /* [R_cap/128][2H/128] atoms                               */
-  float* ab32;        /* [R_cap][2H] fp32 the forward's a | b, for the chain rule */
+  void* ab16;         /* [R_cap][2H] fp16 the forward's a | b, for the chain rule */
 } moe_mx_tensors;
 
 #define MOE_MX_FIELDS 25
@@ -467,10 +467,11 @@ int moe_mx_forward(const moe_config* cfg, const moe_tensors* t, const moe_mx_ten
  * routed experts run as in moe_mx_forward; the shared expert runs in bf16
  * (moe_shared_ffn_combine, the combine in its down GEMM).  It also stores
  * what moe_mx_backward needs: x_perm (bf16 rows), h (bf16, before its MX
- * rounding), mx->ab32 (the pre-activations a | b in fp32: the chain rule's
- * results are quantised to e4m3, which a bf16 copy of its inputs would
- * visibly perturb) and out_perm.  t->ab is not used.
- * in: as moe_mx_forward.  out: as moe_mx_forward plus x_perm, h, ab32, and
+ * rounding), mx->ab16 (the pre-activations a | b in fp16, magnitudes past
+ * 65504 clamped: the chain rule's results are quantised to e4m3, whose codes
+ * a bf16 copy of its inputs (8 significant bits to fp16's 11) would move
+ * about 8 times as often) and out_perm.  t->ab is not used.
+ * in: as moe_mx_forward.  out: as moe_mx_forward plus x_perm, h, ab16, and
  * the shared expert's s_h, s_ab (if non-NULL). */
 int moe_mx_forward_train(const moe_config* cfg, const moe_tensors* t, const moe_mx_tensors* mx,
                          void* workspace, size_t workspace_bytes, void* stream);
@@ -480,14 +481,14 @@ int moe_mx_forward_train(const moe_config* cfg, const moe_tensors* t, const moe_
  * blocks of 32 along the product's reduction axis: d_out = g dY is
  * quantised along d (dout_q/s) from its fp32 value, in the kernel that forms
  * it; dH = Q(d_out) Q(W_down[e]^T) runs on the block-scaled tcgen05 kernel
- * with the SwiGLU chain rule (on ab32) in its epilogue, which quantises the
+ * with the SwiGLU chain rule (on ab16) in its epilogue, which quantises the
  * fp32 d_gu = da | db along 2H (dgu_q/s) and stores it in bf16 for the
  * weight gradient; and dx = Q(d_gu) Q(W_gu[e]^T).  Each MX operand is thus
  * one rounding of its fp32 value, never of a bf16 copy.  The weight gradients, the shared expert and
  * the router are moe_backward's (bf16 operands, fp32 accumulation).  Needs a
  * training workspace (moe_workspace_bytes with training = 1), the forward
  * tensors of moe_mx_forward_train, the transposed weight codes of
- * moe_mx_quantize_weights, ab32, and dout_q/s, dgu_q/s (32-byte aligned
+ * moe_mx_quantize_weights, ab16, and dout_q/s, dgu_q/s (32-byte aligned
  * codes).
  * out: every field of `g`, as moe_backward. */
 int moe_mx_backward(const moe_config* cfg, const moe_tensors* t, const moe_mx_tensors* mx,

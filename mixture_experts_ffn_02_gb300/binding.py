@@ -51,7 +51,7 @@ MOE_MX_FIELDS = 25
 MX_FIELDS = ["W_gu_q", "W_gu_s", "W_down_q", "W_down_s", "x_q", "x_s", "h_q", "h_s",
              "Ws_gu_q", "Ws_gu_s", "Ws_down_q", "Ws_down_s", "xt_q", "xt_s", "hs_q", "hs_s",
              "W_gu_tq", "W_gu_ts", "W_down_tq", "W_down_ts", "dout_q", "dout_s", "dgu_q",
-             "dgu_s", "ab32"]
+             "dgu_s", "ab16"]
 MX_TRAIN_FIELDS = MX_FIELDS[16:]
 
 

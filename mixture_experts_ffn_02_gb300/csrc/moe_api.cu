@@ -374,7 +374,7 @@ int do_backward(const moe_config* c, const moe_tensors* t, const moe_grads* g, C
   if (m) {
     MOE_NEED32(m->W_gu_tq); MOE_NEED(m->W_gu_ts); MOE_NEED32(m->W_down_tq);
     MOE_NEED(m->W_down_ts); MOE_NEED32(m->dout_q); MOE_NEED(m->dout_s);
-    MOE_NEED32(m->dgu_q); MOE_NEED(m->dgu_s); MOE_NEED(m->ab32);
+    MOE_NEED32(m->dgu_q); MOE_NEED(m->dgu_s); MOE_NEED(m->ab16);
   }
   // (i) + (vii): d_out (with the MX step, also its codes along d, quantised
   // from the fp32 g dY), dg and the router-logit gradient
@@ -388,7 +388,7 @@ int do_backward(const moe_config* c, const moe_tensors* t, const moe_grads* g, C
     MxGemmCall h{};
     h.dh = 1; h.row_offsets = t->row_offsets; h.E = c->E; h.rows = R; h.d = c->d; h.H = c->H;
     h.A = m->dout_q; h.sfa = m->dout_s; h.B = m->W_down_tq; h.sfb = m->W_down_ts;
-    h.abi = m->ab32; h.dgu = d_gu; h.dgq = m->dgu_q; h.dgs = m->dgu_s; h.status = k.status;
+    h.abi = m->ab16; h.dgu = d_gu; h.dgq = m->dgu_q; h.dgs = m->dgu_s; h.status = k.status;
     MOE_CUDA(launch_mx_gemm(h, k.s));
     // (iii) dx_perm = Q(d_gu) Q(W_gu^T): the down kind with K = 2H, N = d
     MxGemmCall x{};
@@ -510,7 +510,7 @@ void mx_sizes(const moe_config& c, size_t* b) {
   b[21] = (R / 128) * (d / 128) * 512;                   // dout_s
   b[22] = R * 2 * H;                                     // dgu_q
   b[23] = (R / 128) * (2 * H / 128) * 512;               // dgu_s
-  b[24] = R * 2 * H * 4;                                 // ab32: [R][2H] fp32
+  b[24] = R * 2 * H * 2;                                 // ab16: [R][2H] fp16
 }
 
 // The shared expert on MXFP8 operands: x quantised in token order (PAD and
@@ -581,10 +581,10 @@ int do_mx_gemm(const moe_config* c, const moe_tensors* t, const moe_mx_tensors* 
     MOE_NEED32(m->h_q); MOE_NEED(m->h_s);
     g.A = m->x_q; g.sfa = m->x_s; g.B = m->W_gu_q; g.sfb = m->W_gu_s;
     g.hq = m->h_q; g.hs = m->h_s;
-    if (save) {                          // training: h in bf16, a | b in fp32
-      MOE_NEED(t->h); MOE_NEED32(m->ab32);
+    if (save) {                          // training: h in bf16, a | b in fp16
+      MOE_NEED(t->h); MOE_NEED32(m->ab16);
       g.hb = t->h;
-      g.abo = m->ab32;
+      g.abo = m->ab16;
     }
   } else {
     MOE_NEED(m->h_q); MOE_NEED(m->h_s); MOE_NEED(m->W_down_q); MOE_NEED(m->W_down_s);

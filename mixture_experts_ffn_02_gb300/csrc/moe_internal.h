@@ -209,9 +209,9 @@ struct MxGemmCall {
   uint8_t* hq;                 // gate/up out: h codes [rows][H]
   uint8_t* hs;                 // gate/up out: h scale atoms
   void* hb;                    // gate/up out (training): h [rows][H] bf16, or NULL
-  void* abo;                   // gate/up out (training): a | b [rows][2H] fp32, or NULL
+  void* abo;                   // gate/up out (training): a | b [rows][2H] fp16, or NULL
   float* out;                  // down out: [rows][d] fp32 (d is the output width)
-  const void* abi;             // dH in: saved a | b [rows][2H] fp32
+  const void* abi;             // dH in: saved a | b [rows][2H] fp16
   void* dgu;                   // dH out: da | db [rows][2H] bf16
   uint8_t* dgq;                // dH out: codes of d_gu [rows][2H]
   uint8_t* dgs;                // dH out: their scale atoms [rows/128][2H/128]

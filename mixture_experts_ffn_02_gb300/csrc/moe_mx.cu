@@ -33,6 +33,8 @@
 #include <cstring>
 #include <mutex>
 
+#include <cuda_fp16.h>
+
 #include "moe_common.cuh"
 #include "moe_internal.h"
 #include "moe_mx.cuh"
@@ -60,17 +62,29 @@ constexpr int XSF_SLOT = 16;
 constexpr uint64_t XWAIT_NS = 2000000000ull;  // bounded waits give up after 2 s
 constexpr uint64_t XDRAIN_NS = 200000000ull;
 constexpr size_t XRESERVE = 3072;           // struct XShared
-constexpr size_t XSMEM = XRESERVE + 1024 + (size_t)XSTAGES * XSTAGE;
-static_assert(XSTAGE % 1024 == 0 && XLOAD <= XSTAGE, "stage layout");
-static_assert(XSMEM <= 232448, "exceeds the 227 KB opt-in shared memory of a block");
-static_assert(XSF_COL + XSF_SLOT * XSTAGES <= XTMEM_COLS, "scale slots exceed TMEM");
+// dH epilogue: each thread's two prefetch slots for its row's a | b chunks
+// (64 + 64 bytes, padded to 144 so that the rows of a warp fall on distinct
+// banks for 16-byte accesses)
+constexpr int XPRE_ROW = 144;
 
-// MXK_GATE_UP_SAVE: gate/up that also stores h and a | b in bf16 (training)
+// MXK_GATE_UP_SAVE: gate/up that also stores h in bf16 and a | b in fp16
+// (training)
 enum MxKind { MXK_GATE_UP = 0, MXK_DOWN = 1, MXK_DH = 2, MXK_GATE_UP_SAVE = 3 };
 template <int KIND>
 struct XIsGateUp {
   static constexpr bool value = KIND == MXK_GATE_UP || KIND == MXK_GATE_UP_SAVE;
 };
+// Pipeline depth and shared memory by kind: the dH kernel gives two stages
+// to the epilogue's a | b prefetch slots.
+template <int KIND>
+struct XCfg {
+  static constexpr int stages = KIND == MXK_DH ? 4 : XSTAGES;
+  static constexpr size_t pre = KIND == MXK_DH ? (size_t)XEPI_WARPS * 2 * 32 * XPRE_ROW : 0;
+  static constexpr size_t smem = XRESERVE + 1024 + (size_t)stages * XSTAGE + pre;
+  static_assert(smem <= 232448, "exceeds the 227 KB opt-in shared memory of a block");
+};
+static_assert(XSTAGE % 1024 == 0 && XLOAD <= XSTAGE, "stage layout");
+static_assert(XSF_COL + XSF_SLOT * XSTAGES <= XTMEM_COLS, "scale slots exceed TMEM");
 
 struct XParams {
   const int32_t* row_offsets;  // [E+1] padded segment offsets (multiples of 128), or NULL:
@@ -86,9 +100,9 @@ struct XParams {
   uint8_t* hq;                 // gate/up: h codes [R][H]
   uint8_t* hs;                 // gate/up: h scale atoms [R/128][H/128][512]
   bf16* hb;                    // gate/up, training: h [R][H] bf16, or NULL
-  float* abo;                  // gate/up, training: a | b [R][2H] fp32, or NULL
+  __half* abo;                 // gate/up, training: a | b [R][2H] fp16, or NULL
   float* out;                  // down: out_perm [R][d] fp32
-  const float* abi;            // dH: the saved a | b [R][2H] fp32
+  const __half* abi;           // dH: the saved a | b [R][2H] fp16
   bf16* dgu;                   // dH: d_gu = da | db [R][2H] bf16
   uint8_t* dgq;                // dH: codes of d_gu [R][2H]
   uint8_t* dgs;                // dH: scale atoms of d_gu [R/128][2H/128][512]
@@ -157,21 +171,105 @@ __device__ __forceinline__ void x_st32(bf16* p, const float* v) {
 #pragma unroll
   for (int u = 0; u < 4; ++u) st_v4(p + 8 * u, pack8(v + 8 * u));
 }
-// 32 consecutive fp32 values: four 32-byte stores (p 32-byte aligned) of
-// their bits, and eight 16-byte loads.
-__device__ __forceinline__ void x_st32_f32(float* p, const uint32_t* r) {
-#pragma unroll
-  for (int u = 0; u < 4; ++u) st_v8(p + 8 * u, r + 8 * u);
+// Two fp32 values as an fp16 pair (round to nearest even), magnitudes past
+// the largest finite fp16 (65504) clamped to it; NaN stays NaN.
+__device__ __forceinline__ uint32_t x_f16x2(float lo, float hi) {
+  lo = fabsf(lo) > 65504.f ? copysignf(65504.f, lo) : lo;
+  hi = fabsf(hi) > 65504.f ? copysignf(65504.f, hi) : hi;
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
-__device__ __forceinline__ void x_ld32_f32(const float* p, float* v) {
+// 32 fp32 values given as their bits, stored as fp16: two 32-byte stores
+// (p 32-byte aligned).
+__device__ __forceinline__ void x_st32_f16(__half* p, const uint32_t* r) {
+  uint32_t w[16];
 #pragma unroll
-  for (int u = 0; u < 8; ++u) {
-    const uint4 w = ld_nc_v4(p + 4 * u);
-    v[4 * u + 0] = __uint_as_float(w.x);
-    v[4 * u + 1] = __uint_as_float(w.y);
-    v[4 * u + 2] = __uint_as_float(w.z);
-    v[4 * u + 3] = __uint_as_float(w.w);
+  for (int u = 0; u < 16; ++u) w[u] = x_f16x2(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1]));
+  st_v8(p, w);
+  st_v8(p + 16, w + 8);
+}
+// 32-byte load through the non-coherent path (p 32-byte aligned).
+__device__ __forceinline__ void ld_nc_v8(const void* p, uint32_t* v) {
+  asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),
+                 "=r"(v[6]), "=r"(v[7])
+               : "l"(p));
+}
+__device__ __forceinline__ float x_f16_at(const uint32_t* w, int i) {
+  const __half2 h = *reinterpret_cast<const __half2*>(&w[i >> 1]);
+  return (i & 1) ? __high2float(h) : __low2float(h);
+}
+
+// The a | b chunk [col, col + 32) of one row (64 + 64 bytes of fp16) into
+// this thread's prefetch slot with asynchronous 16-byte copies (registers
+// stay free), as one commit group; an empty group when the row has none.
+__device__ __forceinline__ void x_prefetch_ab(bool work, const __half* abi, int H, int row,
+                                              int col, uint32_t slot) {
+  if (work) {
+    const __half* a = abi + (size_t)row * 2 * H + col;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(slot + 16 * u),
+                   "l"(a + 8 * u) : "memory");
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(slot + 64 + 16 * u),
+                   "l"(a + H + 8 * u) : "memory");
+    }
   }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void x_prefetch_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void ld_shared_v4(uint32_t a, uint32_t* v) {
+  asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]) : "r"(a));
+}
+
+// dH -> the SwiGLU chain rule for 32 columns [col, col + 32) of one row:
+// da = dH b s(a) (1 + a (1 - s(a))) and db = dH silu(a) from the saved fp16
+// a | b, prefetched into this thread's ``slot``.  Each fp32 result is quantised along 2H (blocks of 32, which never
+// straddle da and db: H is a multiple of 128) for the dX product, and stored
+// in bf16 as d_gu = da | db for the weight-gradient product: one rounding
+// each.  da first, then db, so that one 32-value array is live at a time.
+__device__ __forceinline__ void x_dh_chunk(const XParams& p, int row, int col,
+                                           const uint32_t* acc, uint32_t slot) {
+  const size_t rb = (size_t)row * 2 * p.H;
+  const size_t atom_row = (size_t)(row >> 7) * (2 * p.H / 128);
+  float v[32];
+  uint32_t cq[8];
+  // eight values at a time from the slot, so that little of a | b is live
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    uint32_t ah[4], bh[4];
+    ld_shared_v4(slot + 16 * u, ah);
+    ld_shared_v4(slot + 64 + 16 * u, bh);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float a = x_f16_at(ah, i), sg = x_sigmoid(a);
+      v[8 * u + i] = __uint_as_float(acc[8 * u + i]) * x_f16_at(bh, i) * sg * (1.f + a * (1.f - sg));
+    }
+  }
+  uint32_t sbyte = mx_quant32(v, cq);
+  st_v8(p.dgq + rb + col, cq);
+  p.dgs[(atom_row + (col >> 7)) * kMxAtom + mx_sf_byte(row & 127, (col >> 5) & 3)] =
+      (uint8_t)sbyte;
+  x_st32(p.dgu + rb + col, v);
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    uint32_t ah[4];
+    ld_shared_v4(slot + 16 * u, ah);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float a = x_f16_at(ah, i);
+      v[8 * u + i] = __uint_as_float(acc[8 * u + i]) * (a * x_sigmoid(a));
+    }
+  }
+  sbyte = mx_quant32(v, cq);
+  st_v8(p.dgq + rb + p.H + col, cq);
+  p.dgs[(atom_row + ((p.H + col) >> 7)) * kMxAtom +
+        mx_sf_byte(row & 127, ((p.H + col) >> 5) & 3)] = (uint8_t)sbyte;
+  x_st32(p.dgu + rb + p.H + col, v);
 }
 
 // ------------------------------------------------------------------ kernel
@@ -190,7 +288,8 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t ring = (raw + (uint32_t)XRESERVE + 1023u) & ~1023u;
   // both CTAs of a pair see the same layout, so both return here together
-  if (ring + (uint32_t)(XSTAGES * XSTAGE) - raw > (uint32_t)XSMEM) {
+  constexpr int kStages = XCfg<KIND>::stages;
+  if (ring + (uint32_t)(kStages * XSTAGE + XCfg<KIND>::pre) - raw > (uint32_t)XCfg<KIND>::smem) {
     if (threadIdx.x == 0) set_status(p.status, MOE_ERR_DEVICE);
     return;
   }
@@ -201,7 +300,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const int nunits = (int)(gridDim.x >> 1);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < XSTAGES; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&sh.full[s]), 1);
       mbar_init(smem_u32(&sh.empty[s]), 1);
     }
@@ -285,7 +384,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         tma_load_2d_pair(sf, &tmSA, fb, 0, (atom_a + kb) * 4);
         tma_load_2d_pair(sf + kMxAtom, &tmSB, fb, 0, (atom_b0 + kb) * 4);
         tma_load_2d_pair(sf + 2 * kMxAtom, &tmSB, fb, 0, (atom_b1 + kb) * 4);
-        if (++stage == XSTAGES) { stage = 0; phase ^= 1u; }
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
       }
     }
     if (!ok) {
@@ -333,7 +432,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                        (kb | kk) != 0 ? 1u : 0u);
         }
         umma_commit_pair(smem_u32(&sh.empty[stage]), 3);
-        if (++stage == XSTAGES) { stage = 0; phase ^= 1u; }
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
       }
       if (!ok) break;
       umma_commit_pair(smem_u32(&sh.tfull), 3);
@@ -347,29 +446,71 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const int q = warp & 3;
     const int half = (warp - XEPI0) >> 2;
     const uint32_t tempty_leader = mapa_shared(smem_u32(&sh.tempty), 0);
+    // dH: this thread's two a | b prefetch slots
+    const uint32_t pre = ring + (uint32_t)(kStages * XSTAGE) +
+                         (uint32_t)(((warp - XEPI0) * 2 * 32 + lane) * XPRE_ROW);
     int it = 0;
     for (int idx = unit; idx < ntiles; idx += nunits, ++it) {
       const XTile t = x_tile<KIND>(p, sh, idx);
-      if (!mbar_wait_bounded(smem_u32(&sh.tfull), it & 1, abort_flag, XWAIT_NS)) {
-        if (lane == 0) x_fail(sh, p.status);
-        break;
-      }
-      tc_fence_after();
-      const uint32_t tacc = tmem + ((uint32_t)(q * 32) << 16);
       const int blk = t.m0 + XBM * rank;            // this CTA's 128 rows
       const bool store = blk < t.row_end;           // else the pair's padding half
       const int row = blk + q * 32 + lane;
       const bool row_ok = row < p.row_limit;
+      const int col0 = t.n0 + half * 128;           // dH: this warp's first column
+      const bool work = KIND == MXK_DH && store && row_ok && col0 < p.H;
+      if (KIND == MXK_DH) {
+        // the first two chunks' a | b, fetched while the MMAs run
+        x_prefetch_ab(work, p.abi, p.H, row, col0, pre);
+        x_prefetch_ab(work, p.abi, p.H, row, col0 + 32, pre + 32 * XPRE_ROW);
+      }
+      if (!mbar_wait_bounded(smem_u32(&sh.tfull), it & 1, abort_flag, XWAIT_NS)) {
+        if (lane == 0) x_fail(sh, p.status);
+        if (KIND == MXK_DH) x_prefetch_wait<0>();
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tacc = tmem + ((uint32_t)(q * 32) << 16);
       // this warp's 128 accumulator columns into registers; gate/up: gate
       // columns half*64 .. +63 and the matching up columns 128 + half*64 ..
       uint32_t r[4][32];
       if (XIsGateUp<KIND>::value) {
         tmem_ld64(tacc + half * 64, &r[0][0]);
         tmem_ld64(tacc + XBN / 2 + half * 64, &r[2][0]);
+      } else if (KIND == MXK_DH) {
+        tmem_ld32(tacc + half * 128, &r[0][0]);     // the first 32 of the 128 columns
       } else {
         tmem_ld128(tacc + half * 128, &r[0][0]);
       }
       tmem_ld_wait();
+      if (KIND == MXK_DH) {
+        // 64 columns at a time, which keeps the chain rule in registers; the
+        // accumulator is released once the second 64 are read, about half
+        // way through this (memory-bound) epilogue, well before the next
+        // tile's MMAs could finish.  Each chunk's a | b waits in a prefetch
+        // slot, refilled with the chunk two ahead as soon as it is read.
+        // Column halves past H are the last tile's padding.
+        const uint32_t pre1 = pre + 32 * XPRE_ROW;
+        x_prefetch_wait<1>();
+        if (work) x_dh_chunk(p, row, col0, r[0], pre);
+        x_prefetch_ab(work, p.abi, p.H, row, col0 + 64, pre);
+        __syncwarp();
+        tmem_ld32(tacc + half * 128 + 32, &r[0][0]);
+        tmem_ld_wait();
+        x_prefetch_wait<1>();
+        if (work) x_dh_chunk(p, row, col0 + 32, r[0], pre1);
+        x_prefetch_ab(work, p.abi, p.H, row, col0 + 96, pre1);
+        __syncwarp();
+        tmem_ld64(tacc + half * 128 + 64, &r[0][0]);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(tempty_leader);
+        x_prefetch_wait<1>();
+        if (work) x_dh_chunk(p, row, col0 + 64, r[0], pre);
+        x_prefetch_wait<0>();
+        if (work) x_dh_chunk(p, row, col0 + 96, r[1], pre1);
+        continue;
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(tempty_leader);   // accumulator free
@@ -377,65 +518,27 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       if (XIsGateUp<KIND>::value) {
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
+          const int col = t.n0 + half * 64 + c * 32;
+          if (KIND == MXK_GATE_UP_SAVE && row_ok) {
+            // training: the pre-activations a | b in fp16 for the chain
+            // rule, whose results feed an e4m3 quantiser: 11 significant
+            // bits keep the codes it moves rare, where bf16's 8 would move
+            // about 2% of them by a whole step
+            x_st32_f16(p.abo + (size_t)row * 2 * p.H + col, r[c]);
+            x_st32_f16(p.abo + (size_t)row * 2 * p.H + p.H + col, r[2 + c]);
+          }
           float h[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i)
             h[i] = x_silu(__uint_as_float(r[c][i])) * __uint_as_float(r[2 + c][i]);
           uint32_t cq[8];
           const uint32_t sbyte = mx_quant32(h, cq);
-          const int col = t.n0 + half * 64 + c * 32;
           if (row_ok) {
             st_v8(p.hq + (size_t)row * p.H + col, cq);
             p.hs[((size_t)(row >> 7) * (p.H / 128) + (col >> 7)) * kMxAtom +
                  mx_sf_byte(row & 127, (col >> 5) & 3)] = (uint8_t)sbyte;
-            if (KIND == MXK_GATE_UP_SAVE) {
-              // training: h in bf16 (the weight-gradient product's operand)
-              // and the pre-activations a | b in fp32 for the chain rule,
-              // whose results feed an e4m3 quantiser (a bf16 copy of a, b
-              // would move about 2% of those codes by a whole step)
-              x_st32(p.hb + (size_t)row * p.H + col, h);
-              x_st32_f32(p.abo + (size_t)row * 2 * p.H + col, r[c]);
-              x_st32_f32(p.abo + (size_t)row * 2 * p.H + p.H + col, r[2 + c]);
-            }
-          }
-        }
-      } else if (KIND == MXK_DH) {
-        // dH -> the SwiGLU chain rule with the saved a | b:
-        // da = dH b s(a) (1 + a (1 - s(a))), db = dH silu(a).  The fp32 da, db
-        // are quantised along 2H (blocks of 32, which never straddle da and
-        // db: H is a multiple of 128) for the dX product, and stored in bf16
-        // as d_gu = da | db for the weight-gradient product: one rounding
-        // each.  Column halves past H are the last tile's padding.
-        const int col0 = t.n0 + half * 128;
-        if (row_ok && col0 < p.H) {
-          const size_t rb = (size_t)row * 2 * p.H;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int col = col0 + 32 * c;
-            float a[32], b[32];
-            x_ld32_f32(p.abi + rb + col, a);
-            x_ld32_f32(p.abi + rb + p.H + col, b);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float dh = __uint_as_float(r[c][i]);
-              const float sg = x_sigmoid(a[i]);
-              const float da = dh * b[i] * sg * (1.f + a[i] * (1.f - sg));
-              const float db = dh * (a[i] * sg);
-              a[i] = da;
-              b[i] = db;
-            }
-            uint32_t cq[8];
-            const size_t atom_row = (size_t)(row >> 7) * (2 * p.H / 128);
-            uint32_t sbyte = mx_quant32(a, cq);
-            st_v8(p.dgq + rb + col, cq);
-            p.dgs[(atom_row + (col >> 7)) * kMxAtom + mx_sf_byte(row & 127, (col >> 5) & 3)] =
-                (uint8_t)sbyte;
-            sbyte = mx_quant32(b, cq);
-            st_v8(p.dgq + rb + p.H + col, cq);
-            p.dgs[(atom_row + ((p.H + col) >> 7)) * kMxAtom +
-                  mx_sf_byte(row & 127, ((p.H + col) >> 5) & 3)] = (uint8_t)sbyte;
-            x_st32(p.dgu + rb + col, a);
-            x_st32(p.dgu + rb + p.H + col, b);
+            // training: h in bf16 as well (the weight-gradient product's)
+            if (KIND == MXK_GATE_UP_SAVE) x_st32(p.hb + (size_t)row * p.H + col, h);
           }
         }
       } else {
@@ -575,7 +678,7 @@ cudaError_t x_set_attr() {
   static cudaError_t err = cudaSuccess;
   std::call_once(once, [] {
     err = cudaFuncSetAttribute(mx_gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)XSMEM);
+                               (int)XCfg<KIND>::smem);
     if (err == cudaSuccess)
       err = cudaFuncSetAttribute(mx_gemm_kernel<KIND>,
                                  cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
@@ -593,7 +696,7 @@ int x_pair_clusters(int num_sms) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(num_sms & ~1), 1, 1);
     cfg.blockDim = dim3(XTHREADS, 1, 1);
-    cfg.dynamicSmemBytes = XSMEM;
+    cfg.dynamicSmemBytes = XCfg<KIND>::smem;
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = 2;
@@ -618,7 +721,7 @@ cudaError_t x_launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorM
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
   cfg.blockDim = dim3(XTHREADS, 1, 1);
-  cfg.dynamicSmemBytes = XSMEM;
+  cfg.dynamicSmemBytes = XCfg<KIND>::smem;
   cfg.stream = s;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeClusterDimension;
@@ -645,9 +748,9 @@ cudaError_t launch_mx_gemm(const MxGemmCall& g, cudaStream_t s) {
   p.hq = g.hq;
   p.hs = g.hs;
   p.hb = static_cast<bf16*>(g.hb);
-  p.abo = static_cast<float*>(g.abo);
+  p.abo = static_cast<__half*>(g.abo);
   p.out = g.out;
-  p.abi = static_cast<const float*>(g.abi);
+  p.abi = static_cast<const __half*>(g.abi);
   p.dgu = static_cast<bf16*>(g.dgu);
   p.dgq = g.dgq;
   p.dgs = g.dgs;

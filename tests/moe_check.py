@@ -89,12 +89,26 @@ def bf16_neighbours(v):
     return r, other, other_half
 
 
+def fp16_neighbours(v):
+    """As bf16_neighbours for IEEE binary16 (the MX training step's a, b):
+    the rounding of v, the neighbour on the other side of v, and the same
+    neighbour again (numpy's float16 steps across binade edges exactly)."""
+    v = np.asarray(v, dtype=np.float64)
+    r16 = np.clip(v, -65504.0, 65504.0).astype(np.float16)
+    r = r16.astype(np.float64)
+    up = np.nextafter(r16, np.float16(np.inf)).astype(np.float64)
+    dn = np.nextafter(r16, np.float16(-np.inf)).astype(np.float64)
+    other = np.where(v >= r, up, dn)
+    return r, other, other
+
+
 class AdoptStored:
     """Storage hook for the oracle (``rnd=``) that continues from the GPU's
     own stored bf16 values wherever they are a valid rounding.
 
     The layer keeps h, a, b, d_out, da and db in bf16, each the rounding of
-    an fp32 result.  Where that result lies within its accumulation error of
+    an fp32 result (the MX training step keeps a and b in fp16: points a16,
+    b16).  Where that result lies within its accumulation error of
     a rounding boundary, either bf16 neighbour is a correct outcome, as a
     near-tie in routing may go either way; one such flip in a heavy-tailed
     weight gradient moves it by a bf16 ulp of its largest product, which can
@@ -125,7 +139,7 @@ class AdoptStored:
         returns s."""
         v = np.asarray(v, dtype=np.float64)
         s = np.asarray(s, dtype=np.float64)
-        r, other, other_half = bf16_neighbours(v)
+        r, other, other_half = (fp16_neighbours if point.endswith("16") else bf16_neighbours)(v)
         rms = float(np.sqrt(np.mean(v * v))) if v.size else 0.0
         ok = (s == r) | (s == other) | (s == other_half) | (np.abs(s - v) <= 2.0 ** -12 * rms)
         st = self.stats.setdefault(point, [0, 0, 0])
@@ -272,6 +286,11 @@ def stored_from_layer(lay, with_backward, cols=None, shared_cols=None):
         # the MXFP8 path's quantised operands (codes + block scales per row;
         # those of h and d_gu only for whole rows of hidden units)
         R = lay.R_cap
+        if mx.get("ab16") is not None:
+            import torch
+            ab16 = mx["ab16"].view(torch.float16)[:R * 2 * H].view(R, 2 * H)
+            out["a16"] = (pick(ab16, 0, H, cols), None)
+            out["b16"] = (pick(ab16, H, H, cols), None)
         if cols is None:
             out["q_h"] = (mx_rows_from(mx["h_q"], mx["h_s"], R, H), None)
         if with_backward and mx.get("dout_q") is not None:

@@ -133,7 +133,7 @@ def test_mx_sizes_and_shape_rule(clib):
                            Tp * d, Tp * d // 32, Tp * Hs, Tp * Hs // 32,
                            # the training step's: transposed weights, d_out, d_gu
                            E * d * 2 * H, E * d * 2 * H // 32, E * H * d, E * H * d // 32,
-                           R * d, R * d // 32, R * 2 * H, R * 2 * H // 32, R * 2 * H * 4]
+                           R * d, R * d // 32, R * 2 * H, R * 2 * H // 32, R * 2 * H * 2]
     c5 = binding.config(synth.shape(5))              # no shared expert: its buffers are 0
     assert clib.moe_mx_sizes(ctypes.byref(c5), sizes) == 0
     assert list(sizes)[8:16] == [0] * 8 and min(list(sizes)[16:]) > 0

@@ -614,7 +614,8 @@ def test_mx_train_full_size_sampled(cfg, n_tok):
             d_out_v = gate[m][:, None] * dY[tok[m]]
             d_out = O._store(rnd, "d_out", d_out_v, where)
             dH = M._quantised(rnd, "q_d_out", d_out_v, M.mx_roundtrip, where) @ qdk
-            da_v, db_v = O.swiglu_backward(dH, a, bb)       # a, b kept in fp32
+            da_v, db_v = O.swiglu_backward(dH, M._store16(rnd, "a16", a, where),
+                                           M._store16(rnd, "b16", bb, where))
             da, db = O._store(rnd, "da", da_v, where), O._store(rnd, "db", db_v, where)
             dWd += d_out.T @ h
             dWg += da.T @ x[tok[m]]

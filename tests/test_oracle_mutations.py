@@ -312,14 +312,13 @@ def test_mx_dgrad_unquantised_d_gu_is_caught(monkeypatch):
 
 @pytest.mark.parametrize("needle,planted", [
     ('dH = _quantised(rnd, "q_d_out", d_out_v,', 'dH = _quantised(rnd, "q_d_out", d_out,'),
-    ("da_v, db_v = mo.swiglu_backward(dH, a, b)",
-     'da_v, db_v = mo.swiglu_backward(dH, mo._store(rnd, "a", a, where), '
-     'mo._store(rnd, "b", b, where))'),
+    ('_store16(rnd, "a16", a, where)', 'mo._store(rnd, "a", a, where)'),
+    ('_store16(rnd, "b16", b, where)', 'b'),
     ("d_gu = np.concatenate([da_v, db_v], axis=1)", "d_gu = np.concatenate([da, db], axis=1)"),
 ])
 def test_mx_dgrad_quantising_the_bf16_copy_is_caught(monkeypatch, needle, planted):
     """Quantising the bf16-stored d_out or d_gu (a double rounding) instead
-    of the values themselves, or taking the chain rule on bf16 a and b."""
+    of the values themselves; a in bf16 or b unrounded in the chain rule."""
     src = inspect.getsource(M.backward_mx)
     assert needle in src
     ns = dict(vars(M))

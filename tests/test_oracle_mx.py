@@ -248,8 +248,8 @@ def test_mx_backward_is_the_bf16_backward_with_bf16_rounding(norm):
     """With the MX round trip replaced by a bf16 round trip and inputs that
     bf16 holds exactly, the MX training step's backward is the bf16 layer's
     backward (pinned by finite differences and the storage pins), term for
-    term, once the bf16 layer's routed experts also take the chain rule on
-    unrounded a and b (the MX step keeps them in fp32): Q(h) in the down
+    term, once the bf16 layer's routed experts also keep a and b in fp16 (as
+    the MX step does) instead of bf16: Q(h) in the down
     product plays the bf16 layer's stored h, Q(d_out) and Q(d_gu) its stored
     d_out and d_gu, and the other quantised operands are bf16 values
     already."""
@@ -259,12 +259,12 @@ def test_mx_backward_is_the_bf16_backward_with_bf16_rounding(norm):
     args = (x, Wr, W_gu, W_down, Ws_gu, Ws_down, fwd, dY)
     got = M.backward_mx(*args, norm_topk=norm, rnd=_bf16, quant=_bf16)
 
-    class RoutedABUnrounded:
+    class RoutedABInFp16:
         def store(self, point, v, where):
             if point in ("a", "b") and not where.get("shared"):
-                return v
+                return M.fp16_round(v)
             return _bf16(v)
-    ref = O.backward(*args, norm_topk=norm, rnd=RoutedABUnrounded())
+    ref = O.backward(*args, norm_topk=norm, rnd=RoutedABInFp16())
     for n in ("dx", "dWr", "dW_gu", "dW_down", "dWs_gu", "dWs_down", "d_logits", "dg"):
         np.testing.assert_allclose(got[n], ref[n], rtol=1e-12, atol=1e-12, err_msg=n)
 
@@ -329,9 +329,11 @@ def test_mx_backward_quantises_each_operand_along_its_reduction_axis():
 def test_mx_backward_dense_masked_formulation():
     """Independent formulation of the routed data gradients: every expert on
     every token, masked by the selection, with each quantise step written
-    out: dx_t = sum_e [e selected at slot j] Q(bf16(swiglu_bwd(Q(bf16(g dY_t))
-    Q_d(W_down_e), bf16 a, bf16 b))) Q_2H(W_gu_e), plus the shared expert and
-    the router terms of the bf16 layer."""
+    out: dx_t = sum_e [e selected at slot j] Q(swiglu_bwd(Q(g dY_t)
+    Q_d(W_down_e), fp16 a, fp16 b)) Q_2H(W_gu_e), plus the shared expert and
+    the router terms of the bf16 layer.  The MX operands are quantised from
+    the unrounded d_out and d_gu (only the weight gradients take bf16
+    copies), and the chain rule takes a and b in fp16."""
     x, Wr, W_gu, W_down, Ws_gu, Ws_down, dY, fwd = _train_case(9, shared=False)
     got = M.backward_mx(x, Wr, W_gu, W_down, None, None, fwd, dY, rnd=_bf16)
     T, d = x.shape
@@ -353,9 +355,10 @@ def test_mx_backward_dense_masked_formulation():
             gte = np.where(m, fwd["gates"][:, j], 0.0)
             dg[:, j] += np.where(m, (dY * out).sum(axis=1), 0.0)
             dH = Q(gte[:, None] * dY) @ WdT.T       # d_out quantised from g dY itself
-            sa = 1 / (1 + np.exp(-a))
-            da = dH * b * sa * (1 + a * (1 - sa))
-            db = dH * a * sa
+            a16, b16 = M.fp16_round(a), M.fp16_round(b)
+            sa = 1 / (1 + np.exp(-a16))
+            da = dH * b16 * sa * (1 + a16 * (1 - sa))
+            db = dH * a16 * sa
             dx += np.where(m[:, None], Q(np.concatenate([da, db], axis=1)) @ WguT.T, 0.0)
     dL = O.router_logit_grad(dg, fwd["topk_idx"], fwd["gates"], fwd["probs"], True)
     dL += O.aux_logit_grad(fwd["probs"], fwd["f"], fwd["real"], 0.01)
@@ -431,3 +434,18 @@ def test_mx_quantisation_points_feed_their_products():
     y1, _ = M.experts_forward_mx(x, fwd["topk_idx"], fwd["gates"], W_gu, W_down,
                                  rnd=_QuantSpy({"q_h": np.zeros_like}))
     assert y0.any() and not y1.any()
+
+
+def test_fp16_round_by_hand():
+    """The binary16 rounding of the chain rule's a and b: ties to even at 1
+    (ulp 2^-10), the binade edge, subnormals (spacing 2^-24), a value of
+    ulp 1/2, and the clamp at the largest finite value."""
+    r = M.fp16_round
+    assert r(1 + 2.0 ** -11) == 1.0                       # tie -> even (1.0)
+    assert r(1 + 3 * 2.0 ** -11) == 1 + 2.0 ** -9         # tie -> even mantissa
+    assert r(1 + 2.0 ** -11 + 2.0 ** -30) == 1 + 2.0 ** -10
+    assert r(-(2 - 2.0 ** -12)) == -2.0                   # rounds up into the next binade
+    assert r(2.0 ** -24) == 2.0 ** -24 and r(2.0 ** -26) == 0.0
+    assert r(3 * 2.0 ** -26) == 2.0 ** -24                # 0.75 of the smallest subnormal
+    assert r(1000.3) == 1000.5 and r(1000.2) == 1000.0    # spacing 1/2 in [512, 1024)
+    assert r(65504.0) == 65504.0 and r(7e4) == 65504.0 and r(-1e9) == -65504.0

@@ -129,3 +129,21 @@ def test_mx_valid_accepts_exactly_the_nearby_quantisations():
     assert abs(np.log2(amax) - np.round(np.log2(amax))) > 1e-3   # not near a power of two
     ok, _ = mx_valid(v, c, bad_s)
     assert not ok[3, 32:64].any() and ok[3, :32].all()
+
+
+def test_fp16_neighbours_bracket_and_adopt():
+    """moe_check.fp16_neighbours: the rounding and the other neighbour of v
+    bracket it, one binary16 ulp apart (also across a binade edge), and an
+    AdoptStored point named *16 takes either without counting it invalid."""
+    from moe_check import AdoptStored, fp16_neighbours
+    v = np.array([1 + 2.0 ** -12, 2 - 2.0 ** -13, -3.3, 1e-6, 700.1])
+    r, other, _ = fp16_neighbours(v)
+    assert ((np.minimum(r, other) <= v) & (v <= np.maximum(r, other))).all()
+    assert r[1] == 2.0 and other[1] == 2 - 2.0 ** -10       # ulp 2^-10 below 2
+    ad = AdoptStored({}, np.zeros(1, int), 1)
+    ad.adopt("a16", v, other)
+    ad.adopt("a16", v, r)
+    n, diff, bad = ad.stats["a16"]
+    assert (n, diff, bad) == (10, 5, 0)
+    ad.adopt("a16", v, r + 4 * np.abs(other - r))
+    assert ad.stats["a16"][2] > 0
