@@ -1293,38 +1293,50 @@ perm_scatter_kernel(const bf16* __restrict__ x, const int32_t* __restrict__ topk
   constexpr int U = 4;                           // 16-byte vectors in flight per lane
   const int wpb = blockDim.x >> 5;
   const int nb32 = d / 32, kg = d / 128;          // MX: blocks per row, atoms per row block
+  // MX: 8 consecutive values per lane as in the bf16 copy (d a multiple of
+  // 256, so every lane runs the same column loop), each block of 32 shared
+  // by four lanes whose maximum comes from shuffles (mx_quant8x4)
   for (int tl = warp; MX && tl < t_end - t_beg; tl += wpb) {
     const bf16* src = x + (size_t)(t_beg + tl) * d;
     const int* dst = dest_s + tl * k;
-    for (int b = lane; b < nb32; b += 32) {
-      float v[32];
-      uint4 raw[4];
+    const int t = t_beg + tl;
+    const bool real = dst[0] >= 0;
+    for (int c00 = 0; c00 < d; c00 += 256 * U) {
+      uint4 raw[U];
+      uint32_t q[U][2], sb[U];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        raw[u] = ld_nc_v4(src + b * 32 + u * 8);
-        unpack8(raw[u], v + 8 * u);
-      }
-      uint32_t q[8];
-      const uint32_t sb = mx_quant32(v, q);
-      if (xt_q != nullptr) {
-        // the same codes in token order for the shared expert; PAD tokens
-        // (no destination row) as zeros
-        const int t = t_beg + tl;
-        const bool real = dst[0] >= 0;
-        const uint32_t zero[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        st_v8(xt_q + (size_t)t * d + b * 32, real ? q : zero);
-        xt_s[((size_t)(t >> 7) * kg + (b >> 2)) * kMxAtom + mx_sf_byte(t & 127, b & 3)] =
-            real ? (uint8_t)sb : (uint8_t)0;
-      }
-      for (int j = 0; j < k; ++j) {
-        const int r = dst[j];
-        if (r < 0) continue;
-        st_v8(x_q + (size_t)r * d + b * 32, q);
-        x_s[((size_t)(r >> 7) * kg + (b >> 2)) * kMxAtom + mx_sf_byte(r & 127, b & 3)] =
-            (uint8_t)sb;
-        if (x_perm != nullptr) {           // training: the bf16 rows too (weight gradients)
+      for (int u = 0; u < U; ++u)
+        if (c00 + u * 256 < d) raw[u] = ld_nc_v4(src + c00 + u * 256 + lane * 8);
 #pragma unroll
-          for (int u = 0; u < 4; ++u) st_v4(x_perm + (size_t)r * d + b * 32 + u * 8, raw[u]);
+      for (int u = 0; u < U; ++u) {
+        if (c00 + u * 256 >= d) break;               // uniform over the warp
+        float v[8];
+        unpack8(raw[u], v);
+        sb[u] = mx_quant8x4(v, q[u]);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int c0 = c00 + u * 256 + lane * 8;
+        if (c00 + u * 256 >= d) break;
+        const int b = c0 >> 5;
+        if (xt_q != nullptr) {
+          // the same codes in token order for the shared expert; PAD tokens
+          // (no destination row) as zeros
+          *reinterpret_cast<uint2*>(xt_q + (size_t)t * d + c0) =
+              real ? make_uint2(q[u][0], q[u][1]) : make_uint2(0, 0);
+          if ((lane & 3) == 0)
+            xt_s[((size_t)(t >> 7) * kg + (b >> 2)) * kMxAtom + mx_sf_byte(t & 127, b & 3)] =
+                real ? (uint8_t)sb[u] : (uint8_t)0;
+        }
+        for (int j = 0; j < k; ++j) {
+          const int r = dst[j];
+          if (r < 0) continue;
+          *reinterpret_cast<uint2*>(x_q + (size_t)r * d + c0) = make_uint2(q[u][0], q[u][1]);
+          if ((lane & 3) == 0)
+            x_s[((size_t)(r >> 7) * kg + (b >> 2)) * kMxAtom + mx_sf_byte(r & 127, b & 3)] =
+                (uint8_t)sb[u];
+          // training: the bf16 rows too (weight gradients)
+          if (x_perm != nullptr) st_v4(x_perm + (size_t)r * d + c0, raw[u]);
         }
       }
     }
