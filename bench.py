@@ -735,6 +735,45 @@ def run_reference(args):
     print(json.dumps(out), flush=True)
 
 
+def run_mx_train_only(args):
+    """The MXFP8 training step alone on one GPU: weights quantised once, W
+    untimed steps, then K steps each bracketed by events after an L2 flush.
+    Prints one line with the median step time and its tokens/s."""
+    import statistics
+
+    import torch
+
+    from mixture_experts_ffn_02_gb300 import binding, synth
+    s = workload_shape(args)
+    inp = synth.make_inputs(s, seed=0, with_grad=True)
+    lay = binding.Layer.create(s, training=True)
+    dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    lay.set_inputs(dev["x"], dev["Wr"], dev["W_gu"], dev["W_down"], dev["Ws_gu"],
+                   dev["Ws_down"], bias=dev["bias"], valid=dev["valid"])
+    lay.mx_alloc()
+    lay.mx_quantize_weights()
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+    for _ in range(args.warmup):
+        flush.zero_()
+        lay.mx_step(dev["dY"])
+    ev = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        lay.mx_step(dev["dY"])
+        b.record()
+        ev.append((a, b))
+    torch.cuda.synchronize()
+    if lay.status() != 0:
+        raise RuntimeError(f"device status {lay.status()} in the MX training step")
+    ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    print(json.dumps({"mx_train_step": WORKLOAD_NAMES[args.config], "T": s.T,
+                      "steps": args.steps, "ms_per_step_median": round(ms, 4),
+                      "tokens_per_s": round(s.T / (ms / 1e3), 1)}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -748,11 +787,16 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-inference", action="store_true",
                     help="skip the inference-forward rates (e.g. for a launch list of the step)")
+    ap.add_argument("--mx-train-only", action="store_true",
+                    help="time only the MXFP8 training step (for launch lists and profiles); "
+                         "prints its own line, not the benchmark's")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.mx_train_only:
+        run_mx_train_only(args)
     else:
         run_ours(args)
 
