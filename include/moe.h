@@ -72,7 +72,10 @@ enum moe_status {
   MOE_ERR_DEVICE = 6,      /* current device is not sm_100-family (sm_103a build) */
   MOE_ERR_TIMEOUT = 7,     /* device: a bounded wait inside a kernel expired */
   MOE_ERR_INDEX = 8,       /* device: an expert index outside [0, E)      */
-  MOE_ERR_NONFINITE = 9    /* device: a router logit is NaN or infinite   */
+  MOE_ERR_NONFINITE = 9,   /* device: a router logit is NaN or infinite   */
+  MOE_ERR_BOUNDS = 10      /* device, debug builds only: a row index read from
+                            * inv or row_offsets lies outside the rows that
+                            * exist (the access is skipped)                 */
 };
 
 /* Layer configuration (plain data, passed by pointer, read during the call). */
@@ -165,6 +168,11 @@ typedef struct moe_grads {
 
 /* ABI version (MOE_ABI_VERSION). */
 int moe_abi_version(void);
+
+/* 1 if this library was built with the debug bounds checks (MOE_DEBUG_BOUNDS:
+ * row indices read from inv and row_offsets are checked on the device,
+ * MOE_ERR_BOUNDS latched and the access skipped), else 0. */
+int moe_debug_bounds(void);
 
 /* Static message for a status code (never NULL). */
 const char* moe_strerror(int code);

@@ -22,7 +22,7 @@ MOE_ROW_ALIGN = 128
 STATUS = {
     0: "MOE_OK", 1: "MOE_ERR_NULL", 2: "MOE_ERR_SHAPE", 3: "MOE_ERR_ALIGN",
     4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_CUDA", 6: "MOE_ERR_DEVICE", 7: "MOE_ERR_TIMEOUT",
-    8: "MOE_ERR_INDEX", 9: "MOE_ERR_NONFINITE",
+    8: "MOE_ERR_INDEX", 9: "MOE_ERR_NONFINITE", 10: "MOE_ERR_BOUNDS",
 }
 
 
@@ -65,6 +65,7 @@ _MX_STEP = [ctypes.POINTER(MoEConfig), ctypes.POINTER(MoETensors),
             ctypes.POINTER(MoEMxTensors), c_void_p, ctypes.c_size_t, c_void_p]
 SIGNATURES = {
     "moe_abi_version": (ctypes.c_int, []),
+    "moe_debug_bounds": (ctypes.c_int, []),
     "moe_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_check_config": (ctypes.c_int, [ctypes.POINTER(MoEConfig)]),
     "moe_row_capacity": (ctypes.c_int, [ctypes.POINTER(MoEConfig),
@@ -111,6 +112,7 @@ SIGNATURES = {
 }
 
 _LIB = None
+_LIB_DEBUG = None
 
 
 class MoEError(RuntimeError):
@@ -119,12 +121,20 @@ class MoEError(RuntimeError):
         super().__init__(f"{where}: {STATUS.get(code, code)}")
 
 
-def load(path: str | None = None, build_if_missing: bool = False) -> ctypes.CDLL:
-    """Load the shared library (no fallback: raises if it is absent)."""
-    global _LIB
-    if _LIB is not None and path is None:
-        return _LIB
-    p = path or _build.LIB
+def load(path: str | None = None, build_if_missing: bool = False,
+         debug: bool | None = None) -> ctypes.CDLL:
+    """Load the shared library (no fallback: raises if it is absent).  With
+    ``debug`` (default: the environment variable MOE_DEBUG_BOUNDS=1) the
+    variant with device bounds checks, built on demand."""
+    global _LIB, _LIB_DEBUG
+    if debug is None:
+        debug = os.environ.get("MOE_DEBUG_BOUNDS") == "1"
+    cached = _LIB_DEBUG if debug else _LIB
+    if cached is not None and path is None:
+        return cached
+    p = path or (_build.LIB_DEBUG if debug else _build.LIB)
+    if debug and path is None and not os.path.exists(p):
+        _build.build(debug=True)
     if not os.path.exists(p):
         if build_if_missing:
             _build.build()
@@ -136,7 +146,10 @@ def load(path: str | None = None, build_if_missing: bool = False) -> ctypes.CDLL
         fn.restype = res
         fn.argtypes = args
     if path is None:
-        _LIB = lib
+        if debug:
+            _LIB_DEBUG = lib
+        else:
+            _LIB = lib
     return lib
 
 

@@ -4,6 +4,11 @@ Each CUDA translation unit is compiled in parallel with nvcc for
 ``-gencode arch=compute_103a,code=sm_103a`` and linked into one shared object
 that exports the C ABI of ``include/moe.h``.  No CMake, no torch extension
 machinery: plain nvcc, so the same command works on x86 and on Arm hosts.
+
+``build(debug=True)`` builds the checking variant ``_build/libmoe_gb300_debug.so``
+(objects under ``_build/debug``) with ``-DMOE_DEBUG_BOUNDS``: its kernels check
+every row index they read from ``inv`` and the segment table against the rows
+that exist, latch MOE_ERR_BOUNDS in the status word and skip the access.
 """
 from __future__ import annotations
 
@@ -19,6 +24,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libmoe_gb300.so")
+LIB_DEBUG = os.path.join(BUILD, "libmoe_gb300_debug.so")
 SOURCES = ["moe_api.cu", "moe_dispatch.cu", "moe_gemm.cu", "moe_mx.cu", "moe_router_tc.cu",
            "moe_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -45,14 +51,19 @@ def _stale(obj: str, src: str) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(verbose: bool = False, ptxas_info: bool = False, force: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, ptxas_info: bool = False, force: bool = False,
+          debug: bool = False) -> str:
+    objdir = os.path.join(BUILD, "debug") if debug else BUILD
+    lib = LIB_DEBUG if debug else LIB
+    os.makedirs(objdir, exist_ok=True)
     cc = nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_info else []
+    if debug:
+        extra.append("-DMOE_DEBUG_BOUNDS")
 
     def compile_one(src):
         path = os.path.join(CSRC, src)
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(objdir, src.replace(".cu", ".o"))
         if not force and not ptxas_info and not _stale(obj, path):
             return obj, ""
         cmd = [cc, *_flags(extra), "-c", path, "-o", obj]
@@ -68,14 +79,15 @@ def build(verbose: bool = False, ptxas_info: bool = False, force: bool = False) 
         for _, log in results:
             if log:
                 print(log, file=sys.stderr)
-    if force or not os.path.exists(LIB) or any(os.path.getmtime(o) > os.path.getmtime(LIB)
+    if force or not os.path.exists(lib) or any(os.path.getmtime(o) > os.path.getmtime(lib)
                                                 for o in objs):
-        cmd = [cc, *ARCH, "-shared", "-Xcompiler", "-fPIC", "-o", LIB, *objs]
+        cmd = [cc, *ARCH, "-shared", "-Xcompiler", "-fPIC", "-o", lib, *objs]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(verbose=True, ptxas_info="-v" in sys.argv, force="-f" in sys.argv))
+    print(build(verbose=True, ptxas_info="-v" in sys.argv, force="-f" in sys.argv,
+                debug="--debug" in sys.argv))

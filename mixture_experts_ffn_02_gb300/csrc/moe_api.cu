@@ -307,6 +307,7 @@ int shared_ffn(const moe_config* c, const moe_tensors* t, Call& k, bool fold_com
     d.valid = t->valid;
     d.comb_src = t->out_perm;
     d.comb_inv = t->inv;
+    d.comb_rows = (int)k.w.R_cap;
     d.comb_gates = t->gates;
     d.comb_k = c->k;
   } else {
@@ -336,7 +337,8 @@ int do_combine(const moe_config* c, const moe_tensors* t, Call& k) {
     MOE_NEED(t->s_out);
     s_out = t->s_out;
   }
-  MOE_CUDA(launch_combine(*c, t->out_perm, t->inv, t->gates, t->valid, s_out, t->y, k.s));
+  MOE_CUDA(launch_combine(*c, t->out_perm, t->inv, t->gates, t->valid, s_out, t->y,
+                          (long long)k.w.R_cap, k.status, k.s));
   return MOE_OK;
 }
 
@@ -381,7 +383,7 @@ int do_backward(const moe_config* c, const moe_tensors* t, const moe_grads* g, C
   MOE_CUDA(launch_combine_bwd(*c, g->dY, t->out_perm, t->inv, t->topk_idx, t->gates, t->logits,
                               t->f, t->counts, t->valid, t->row_offsets, d_out,
                               m ? m->dout_q : nullptr, m ? m->dout_s : nullptr, g->d_logits,
-                              k.status, k.s));
+                              (long long)R, k.status, k.s));
   if (m) {
     // (ii) dH = Q(d_out) Q(W_down^T) -> SwiGLU backward -> d_gu = [da | db]
     // in bf16 and, from the fp32 values, its codes along 2H
@@ -450,7 +452,7 @@ int do_backward(const moe_config* c, const moe_tensors* t, const moe_grads* g, C
     sx.A = ds_gu; sx.lda = 2 * Hs; sx.B = t->Ws_gu; sx.K = 2 * Hs; sx.N = c->d;
     sx.out0 = g->dx; sx.ld0 = c->d; sx.out_f32 = 0; sx.status = k.status;
     sx.valid = t->valid;
-    sx.comb_src = dx_perm; sx.comb_inv = t->inv; sx.comb_k = c->k;
+    sx.comb_src = dx_perm; sx.comb_inv = t->inv; sx.comb_k = c->k; sx.comb_rows = R;
     sx.dl = g->d_logits; sx.wr = t->Wr; sx.rE = router_small_path(*c) ? c->E : 0;
     sx.dxr = dxr;
     MOE_CUDA(launch_gemm(sx, k.s));
@@ -466,7 +468,7 @@ int do_backward(const moe_config* c, const moe_tensors* t, const moe_grads* g, C
     MOE_CUDA(launch_gemm(sg, k.s));
   } else {
     MOE_CUDA(launch_dx_gather(*c, dx_perm, t->inv, dxr, g->d_logits, t->Wr, t->valid, g->dx,
-                              k.s));
+                              (long long)R, k.status, k.s));
   }
   if (!router_tc_path(*c))
     MOE_CUDA(launch_router_dw(*c, t->x, g->d_logits, g->dWr, part, w.dwr_splits, k.s));
@@ -605,6 +607,8 @@ extern "C" {
 
 int moe_abi_version(void) { return MOE_ABI_VERSION; }
 
+int moe_debug_bounds(void) { return moe::kDebugBounds ? 1 : 0; }
+
 const char* moe_strerror(int code) {
   switch (code) {
     case MOE_OK: return "ok";
@@ -617,6 +621,7 @@ const char* moe_strerror(int code) {
     case MOE_ERR_TIMEOUT: return "a bounded wait inside a kernel expired";
     case MOE_ERR_INDEX: return "expert index out of range";
     case MOE_ERR_NONFINITE: return "non-finite router logit";
+    case MOE_ERR_BOUNDS: return "row index outside the buffer (debug bounds check)";
     default: return "unknown status code";
   }
 }

@@ -21,6 +21,32 @@ __device__ __forceinline__ void set_status(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
 }
 
+// Debug builds (compiled with MOE_DEBUG_BOUNDS) check each row index read
+// from an index buffer -- inv, and the padded segment table row_offsets --
+// against the rows that exist before it is used: a bad one latches
+// MOE_ERR_BOUNDS and the access is skipped (an inv entry is treated as an
+// unused slot, a bad segment table as no tiles).  Release builds trust the
+// indices, which the library's own permute writes, and compile the checks out.
+#ifdef MOE_DEBUG_BOUNDS
+constexpr bool kDebugBounds = true;
+#else
+constexpr bool kDebugBounds = false;
+#endif
+__device__ __forceinline__ int dbg_row(int r, long long rows, int* status) {
+  if (kDebugBounds && (r < -1 || r >= rows)) {
+    set_status(status, MOE_ERR_BOUNDS);
+    return -1;
+  }
+  return r;
+}
+// Debug builds: is the segment table roff[0..E] a valid padded layout of at
+// most `rows` rows (starting at 0, non-decreasing, 128-row segments)?
+__device__ __forceinline__ bool dbg_roff_ok(const int* roff, int E, long long rows) {
+  bool ok = roff[0] == 0;
+  for (int e = 0; e < E && ok; ++e) ok = roff[e + 1] >= roff[e] && (roff[e + 1] - roff[e]) % 128 == 0;
+  return ok && roff[E] <= rows;
+}
+
 // ----------------------------------------------------------------- bf16
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) {

@@ -1393,7 +1393,8 @@ perm_scatter_kernel(const bf16* __restrict__ x, const int32_t* __restrict__ topk
 __global__ void __launch_bounds__(kThreads)
 combine_kernel(const float* __restrict__ out_perm, const int32_t* __restrict__ inv,
                const float* __restrict__ gates, const uint8_t* __restrict__ valid,
-               const float* __restrict__ s_out, bf16* __restrict__ y, int T, int d, int k) {
+               const float* __restrict__ s_out, bf16* __restrict__ y, int T, int d, int k,
+               long long rows, int* status) {
   const int lane = threadIdx.x & 31;
   const int wpb = blockDim.x >> 5;
   for (int t = blockIdx.x * wpb + (threadIdx.x >> 5); t < T; t += gridDim.x * wpb) {
@@ -1401,7 +1402,7 @@ combine_kernel(const float* __restrict__ out_perm, const int32_t* __restrict__ i
     int my_r = -1;
     float my_g = 0.f;
     if (lane < k && real) {
-      my_r = inv[(size_t)t * k + lane];
+      my_r = dbg_row(inv[(size_t)t * k + lane], rows, status);
       my_g = gates[(size_t)t * k + lane];
     }
     bf16* yr = y + (size_t)t * d;
@@ -1447,7 +1448,8 @@ combine_bwd_kernel(const bf16* __restrict__ dY, const float* __restrict__ out_pe
                    const uint8_t* __restrict__ valid, const int32_t* __restrict__ row_offsets,
                    bf16* __restrict__ d_out, uint8_t* __restrict__ dq,
                    uint8_t* __restrict__ ds, float* __restrict__ d_logits, int T, int d, int E,
-                   int k, int norm_topk, float aux_coef, float z_coef) {
+                   int k, int norm_topk, float aux_coef, float z_coef, long long rows,
+                   int* status) {
   __shared__ float f_s[256];
   __shared__ float coef_s, zcoef_s;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -1473,7 +1475,7 @@ combine_bwd_kernel(const bf16* __restrict__ dY, const float* __restrict__ out_pe
     int my_r = -1, my_i = -1;
     float my_g = 0.f;
     if (lane < k) {
-      my_r = inv[(size_t)t * k + lane];
+      my_r = dbg_row(inv[(size_t)t * k + lane], rows, status);
       my_i = topk[(size_t)t * k + lane];
       my_g = gates[(size_t)t * k + lane];
     }
@@ -1588,7 +1590,7 @@ dx_gather_kernel(const float* __restrict__ dx_perm, const int32_t* __restrict__ 
                  const float* __restrict__ dxr,
                  const float* __restrict__ dL, const float* __restrict__ Wr,
                  const uint8_t* __restrict__ valid, bf16* __restrict__ dx, int T, int d,
-                 int k) {
+                 int k, long long rows, int* status) {
   extern __shared__ float wr_s[];
   if constexpr (ES > 0) {
     for (int i = threadIdx.x; i < d * ES; i += blockDim.x) {
@@ -1602,7 +1604,7 @@ dx_gather_kernel(const float* __restrict__ dx_perm, const int32_t* __restrict__ 
   for (int t = blockIdx.x * wpb + (threadIdx.x >> 5); t < T; t += gridDim.x * wpb) {
     const bool real = row_real(valid, t);
     int my_r = -1;
-    if (lane < k && real) my_r = inv[(size_t)t * k + lane];
+    if (lane < k && real) my_r = dbg_row(inv[(size_t)t * k + lane], rows, status);
     float dl[ES > 0 ? ES : 1];
     if constexpr (ES > 0) {
 #pragma unroll
@@ -2056,12 +2058,12 @@ cudaError_t launch_permute_mx(const moe_config& c, const void* x, const int32_t*
 
 cudaError_t launch_combine(const moe_config& c, const float* out_perm, const int32_t* inv,
                            const float* gates, const uint8_t* valid, const float* s_out,
-                           void* y, cudaStream_t s) {
+                           void* y, long long rows, int* status, cudaStream_t s) {
   DeviceInfo di;
   if (device_info(&di) != MOE_OK) return cudaErrorUnknown;
   const int grid = grid_for(kThreads / 32, c.T, di.num_sms * 8);
   combine_kernel<<<grid, kThreads, 0, s>>>(out_perm, inv, gates, valid, s_out,
-                                           static_cast<bf16*>(y), c.T, c.d, c.k);
+                                           static_cast<bf16*>(y), c.T, c.d, c.k, rows, status);
   return cudaGetLastError();
 }
 
@@ -2069,9 +2071,8 @@ cudaError_t launch_combine_bwd(const moe_config& c, const void* dY, const float*
                                const int32_t* inv, const int32_t* topk, const float* gates,
                                const float* L, const float* f, const int32_t* counts,
                                const uint8_t* valid, const int32_t* row_offsets, void* d_out,
-                               uint8_t* dout_q, uint8_t* dout_s, float* d_logits, int* status,
-                               cudaStream_t s) {
-  (void)status;
+                               uint8_t* dout_q, uint8_t* dout_s, float* d_logits, long long rows,
+                               int* status, cudaStream_t s) {
   if (dout_q != nullptr && (c.d % 256 != 0 || dout_s == nullptr)) return cudaErrorInvalidValue;
   DeviceInfo di;
   if (device_info(&di) != MOE_OK) return cudaErrorUnknown;
@@ -2082,7 +2083,7 @@ cudaError_t launch_combine_bwd(const moe_config& c, const void* dY, const float*
       static_cast<const bf16*>(dY), out_perm, inv, topk, gates, L, f,                          \
       counts, valid, row_offsets, static_cast<bf16*>(d_out), dout_q, dout_s, d_logits, c.T,    \
       c.d, c.E, c.k,                                                                           \
-      c.norm_topk, c.aux_coef, c.z_coef)
+      c.norm_topk, c.aux_coef, c.z_coef, rows, status)
   if (V <= 1) { MOE_CBWD(1); }
   else if (V <= 2) { MOE_CBWD(2); }
   else if (V <= 4) { MOE_CBWD(4); }
@@ -2093,7 +2094,8 @@ cudaError_t launch_combine_bwd(const moe_config& c, const void* dY, const float*
 
 cudaError_t launch_dx_gather(const moe_config& c, const float* dx_perm, const int32_t* inv,
                              const float* dxr, const float* d_logits,
-                             const float* Wr, const uint8_t* valid, void* dx, cudaStream_t s) {
+                             const float* Wr, const uint8_t* valid, void* dx, long long rows,
+                             int* status, cudaStream_t s) {
   DeviceInfo di;
   if (device_info(&di) != MOE_OK) return cudaErrorUnknown;
   const int grid = grid_for(kThreads / 32, c.T, di.num_sms * 4);
@@ -2105,14 +2107,14 @@ cudaError_t launch_dx_gather(const moe_config& c, const float* dx_perm, const in
   cudaFuncSetAttribute(dx_gather_kernel<EE>, cudaFuncAttributeMaxDynamicSharedMemorySize,     \
                        (int)smem);                                                            \
   dx_gather_kernel<EE><<<grid, kThreads, smem, s>>>(dp, inv, nullptr, d_logits, Wr, valid, o, \
-                                                    c.T, c.d, c.k)
+                                                    c.T, c.d, c.k, rows, status)
     if (c.E == 4) { MOE_DXG(4); }
     else if (c.E == 8) { MOE_DXG(8); }
     else { MOE_DXG(16); }
 #undef MOE_DXG
   } else {
     dx_gather_kernel<0><<<grid, kThreads, 0, s>>>(dp, inv, dxr, d_logits, Wr, valid, o, c.T,
-                                                  c.d, c.k);
+                                                  c.d, c.k, rows, status);
   }
   return cudaGetLastError();
 }

@@ -98,6 +98,7 @@ struct Params {
   const int32_t* comb_inv;
   const float* comb_gates;
   int comb_k;
+  int comb_rows;               // rows of comb_src (debug bounds checks)
   // GK_DX with the dx gather folded in (dense rows = tokens): dx[t] =
   // bf16(sum_j comb_src[comb_inv[t][j]] + acc + router term) into out0; the
   // router term is sum_e dl[t][e] wr[c][e] (rE > 0) or dxr[t][c]
@@ -125,6 +126,7 @@ struct Shared {
   uint32_t tmem_base;
   int abort_flag;
   int roff[257];               // padded segment offsets (row-grouped kinds)
+  int roff_bad;                // debug builds: the segment table failed its check
   int ppre[257];               // CTA pairs: 256-row tiles before expert e (GK_DW: expert order)
 };
 static_assert(sizeof(Shared) <= SHARED_RESERVE, "bookkeeping too large");
@@ -157,6 +159,7 @@ __device__ __forceinline__ int last_le(const int* a, int n, int v) {
 // and not stored), so ppre[] counts the pairs before each expert.
 template <int KIND, int CG>
 __device__ __forceinline__ int num_tiles(const Params& p, const Shared& sh) {
+  if (kDebugBounds && p.row_offsets && sh.roff_bad) return 0;
   if (KIND == GK_DW) return p.E * ((p.Mdw + BM * CG - 1) / (BM * CG)) * p.n_tiles;
   int units;
   if (!p.row_offsets) units = (p.rows + BM * CG - 1) / (BM * CG);
@@ -492,7 +495,7 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const Tile& t, ui
           for (int u = 0; u < 32; ++u) acc[u] = 0.f;
           if (real) {
             for (int j = 0; j < p.comb_k; ++j) {
-              const int r = inv_t[j];
+              const int r = dbg_row(inv_t[j], p.comb_rows, p.status);
               if (r < 0) continue;
               const float g = g_t[j];
               const float* src = p.comb_src + (size_t)r * p.N + col + c * 32;
@@ -538,7 +541,7 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const Tile& t, ui
           for (int u = 0; u < 16; ++u) acc[u] = 0.f;
           if (real) {
             for (int j = 0; j < p.comb_k; ++j) {
-              const int r = inv_t[j];
+              const int r = dbg_row(inv_t[j], p.comb_rows, p.status);
               if (r < 0) continue;
               const float* src = p.comb_src + (size_t)r * p.N + c0;
 #pragma unroll
@@ -704,6 +707,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   }
   tc_fence_before();
   __syncthreads();
+  if (kDebugBounds && p.row_offsets && threadIdx.x == 0) {
+    sh.roff_bad = dbg_roff_ok(sh.roff, p.E, p.rows) ? 0 : 1;
+    if (sh.roff_bad) set_status(p.status, MOE_ERR_BOUNDS);
+  }
   if (CG == 2 && KIND != GK_DW && p.row_offsets && warp == 3) {
     // 256-row tiles per expert (pairs of 128-row blocks), prefix over experts
     int carry = 0;
@@ -1077,6 +1084,7 @@ cudaError_t launch_gemm(const GemmCall& g, cudaStream_t s) {
   p.status = g.status;
   p.comb_src = g.comb_src;
   p.comb_inv = g.comb_inv;
+  p.comb_rows = g.comb_rows;
   p.comb_gates = g.comb_gates;
   p.comb_k = g.comb_k;
   p.dl = g.dl;

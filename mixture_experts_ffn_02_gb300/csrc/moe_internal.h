@@ -84,18 +84,21 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* to
                            int32_t* counts, int32_t* offsets, int32_t* row_offsets,
                            int32_t* perm, int32_t* inv, void* x_perm, char* ws,
                            const WsLayout& w, cudaStream_t s);
+// rows: the permuted rows that exist (R_cap); status: the workspace status
+// word, where debug builds latch MOE_ERR_BOUNDS for an inv entry past rows.
 cudaError_t launch_combine(const moe_config& c, const float* out_perm, const int32_t* inv,
                            const float* gates, const uint8_t* valid, const float* s_out,
-                           void* y, cudaStream_t s);
+                           void* y, long long rows, int* status, cudaStream_t s);
 cudaError_t launch_combine_bwd(const moe_config& c, const void* dY, const float* out_perm,
                                const int32_t* inv, const int32_t* topk, const float* gates,
                                const float* L, const float* f, const int32_t* counts,
                                const uint8_t* valid, const int32_t* row_offsets,
                                void* d_out, uint8_t* dout_q, uint8_t* dout_s,
-                               float* d_logits, int* status, cudaStream_t s);
+                               float* d_logits, long long rows, int* status, cudaStream_t s);
 cudaError_t launch_dx_gather(const moe_config& c, const float* dx_perm, const int32_t* inv,
                              const float* dxr, const float* d_logits,
-                             const float* Wr, const uint8_t* valid, void* dx, cudaStream_t s);
+                             const float* Wr, const uint8_t* valid, void* dx, long long rows,
+                             int* status, cudaStream_t s);
 // Router GEMMs on the CUDA cores (fp32 FMA).
 cudaError_t launch_router_dx(const moe_config& c, const float* d_logits, const float* Wr,
                              float* dxr, cudaStream_t s);
@@ -159,6 +162,7 @@ struct GemmCall {
   // out0 = y (bf16) = sum_j comb_gates[t][j] comb_src[comb_inv[t][j]] + result
   const float* comb_src;       // out_perm [R][N] fp32, or NULL (no combine)
   const int32_t* comb_inv;     // [rows][comb_k], -1 = unused slot
+  int comb_rows;               // rows of comb_src (R_cap), for debug bounds checks
   const float* comb_gates;     // [rows][comb_k]
   int comb_k;
   // GK_DX over dense token rows with the dx gather folded into the epilogue:

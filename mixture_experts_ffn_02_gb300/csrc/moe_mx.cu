@@ -119,6 +119,7 @@ struct XShared {
   int abort_flag;
   int roff[257];               // padded segment offsets
   int ppre[257];               // 256-row pair tiles before expert e
+  int roff_bad;                // debug builds: the segment table failed its check
 };
 static_assert(sizeof(XShared) <= XRESERVE, "bookkeeping too large");
 
@@ -326,6 +327,10 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   }
   tc_fence_before();
   __syncthreads();
+  if (kDebugBounds && p.row_offsets && threadIdx.x == 0) {
+    sh.roff_bad = dbg_roff_ok(sh.roff, p.E, p.row_limit) ? 0 : 1;
+    if (sh.roff_bad) set_status(p.status, MOE_ERR_BOUNDS);
+  }
   if (warp == 3) {
     // 256-row pair tiles per expert, prefix over experts
     int carry = 0;
@@ -347,7 +352,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   tc_fence_after();
   const uint32_t tmem = sh.tmem_base;
   volatile int* abort_flag = &sh.abort_flag;
-  const int ntiles = sh.ppre[p.E] * p.n_tiles;
+  const int ntiles = (kDebugBounds && p.row_offsets && sh.roff_bad) ? 0 : sh.ppre[p.E] * p.n_tiles;
 
   if (warp == 0 && lane == 0) {
     // ---------------- producer (both CTAs)

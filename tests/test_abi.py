@@ -148,3 +148,14 @@ def test_mx_sizes_and_shape_rule(clib):
     gr = binding.MoEGrads()
     assert clib.moe_mx_backward(ctypes.byref(tiny), ctypes.byref(t), ctypes.byref(m),
                                 ctypes.byref(gr), None, 0, None) == 2
+
+
+def test_debug_build_exports_the_abi():
+    """The checking variant (device bounds checks, MOE_DEBUG_BOUNDS) builds,
+    exports every declared symbol and says which build it is."""
+    dbg = binding.load(debug=True)
+    for n in declared_functions():
+        assert hasattr(dbg, n), n
+    assert dbg.moe_debug_bounds() == 1
+    assert binding.load().moe_debug_bounds() == 0
+    assert b"debug bounds" in dbg.moe_strerror(10)
