@@ -475,7 +475,7 @@ def fp8_gemm_peak(local):
 def hbm_bytes(s):
     """Algorithmic bytes of the memory-bound forward calls, each byte of the
     tensors they must read or write counted once, in the layouts the library
-    stores (out_perm and s_out are fp32; PAD rows of the segments are not
+    stores (out_perm bf16, s_out fp32; PAD rows of the segments are not
     counted)."""
     T, Tr, d, E, k = s.T, (s.T_real if s.T_real is not None else s.T), s.d, s.E, s.k
     M = Tr * k
@@ -486,8 +486,8 @@ def hbm_bytes(s):
         "router_route": T * d * 2 + d * E * 4 + T * E * 4 + T * k * 8 + valid + bias,
         # x rows in, x_perm rows out, topk_idx in, perm + inv out
         "permute": Tr * d * 2 + M * d * 2 + T * k * 4 + M * 4 + T * k * 4,
-        # out_perm (fp32) + s_out (fp32) in, inv + gates in, y out
-        "combine": M * d * 4 + (Tr * d * 4 if s.Hs_total else 0) + T * k * 8 + T * d * 2,
+        # out_perm (bf16) + s_out (fp32) in, inv + gates in, y out
+        "combine": M * d * 2 + (Tr * d * 4 if s.Hs_total else 0) + T * k * 8 + T * d * 2,
     }
 
 

@@ -59,7 +59,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 5
+#define MOE_ABI_VERSION 6
 #define MOE_ROW_ALIGN 128
 
 enum moe_status {
@@ -138,8 +138,8 @@ typedef struct moe_tensors {
   void* ab;             /* [R_cap][2H] bf16 pre-activations a|b (saved for
                            backward; NULL skips the save)                         */
   void* h;              /* [R_cap][H] bf16 silu(a) * b                            */
-  float* out_perm;      /* [R_cap][d] fp32 expert outputs per row (fp32 so the
-                           combine sums unrounded terms)                          */
+  void* out_perm;       /* [R_cap][d] bf16 expert output per row (each slot's
+                           output, summed by the combine in fp32)                 */
   void* s_ab;           /* [T][2Hs] bf16 shared pre-activations (or NULL)         */
   void* s_h;            /* [T][Hs] bf16 shared hidden (0 on PAD rows)             */
   float* s_out;         /* [T][d] fp32 shared expert output (0 on PAD rows):
@@ -194,7 +194,7 @@ int moe_workspace_bytes(const moe_config* cfg, int training, size_t* bytes);
  * inspection by tests and debuggers after the call:
  *   out[0] d_out   [R_cap][d]  bf16  g * dY of each routed row
  *   out[1] d_gu    [R_cap][2H] bf16  (da | db) of each routed row
- *   out[2] dx_perm [R_cap][d]  fp32  the dX product of each routed row
+ *   out[2] dx_perm [R_cap][d]  bf16  the dX product of each routed row
  *   out[3] ds_gu   [T][2Hs]    bf16  the shared expert's (da | db); 0 when
  *                                    n_shared == 0
  * Rows follow perm (pad rows hold unspecified values).  The layout is part
@@ -272,7 +272,7 @@ int moe_expert_gate_up(const moe_config* cfg, const moe_tensors* t,
                        void* workspace, size_t workspace_bytes, void* stream);
 
 /* a4. Grouped down GEMM: out_perm[r] = h[r] W_down[e]^T (tcgen05, bf16 in,
- * fp32 accumulate, fp32 out).  The down projection of each SwiGLU expert
+ * fp32 accumulate, bf16 out).  The down projection of each SwiGLU expert
  * ("KochiLLM v1.0" card, Configuration: SwiGLU experts, hidden 2 x dim), run
  * as one grouped GEMM over all experts' segments ("spark-gpt" README,
  * Hard-won facts: the MoE experts run on hand-written grouped GEMMs).
@@ -447,7 +447,8 @@ int moe_mx_permute(const moe_config* cfg, const moe_tensors* t, const moe_mx_ten
 int moe_mx_expert_gate_up(const moe_config* cfg, const moe_tensors* t, const moe_mx_tensors* mx,
                           void* workspace, size_t workspace_bytes, void* stream);
 
-/* a4 on MXFP8 operands: out_perm = h_q W_down_q^T (fp32).
+/* a4 on MXFP8 operands: out_perm = h_q W_down_q^T (fp32 accumulation, bf16
+ * rows).
  * in: h_q, h_s, row_offsets, W_down_q, W_down_s.  out: out_perm. */
 int moe_mx_expert_down(const moe_config* cfg, const moe_tensors* t, const moe_mx_tensors* mx,
                        void* workspace, size_t workspace_bytes, void* stream);

@@ -221,7 +221,7 @@ class Layer:
                  offsets=z(E + 1, dt=i32), row_offsets=z(E + 1, dt=i32), perm=z(R, dt=i32),
                  inv=z(T * k, dt=i32), x_perm=None if gather else z(R, d, dt=bf),
                  h=z(R, H, dt=bf),
-                 out_perm=z(R, d, dt=f32), y=z(T, d, dt=bf),
+                 out_perm=z(R, d, dt=bf), y=z(T, d, dt=bf),
                  ab=z(R, 2 * H, dt=bf) if training else None,
                  s_h=z(T, Hs, dt=bf) if Hs else None,
                  s_out=z(T, d, dt=f32) if Hs else None,
@@ -365,7 +365,7 @@ class Layer:
     def intermediates(self) -> dict:
         """Views of the backward's stored intermediates in the workspace
         (moe_workspace_offsets): d_out [R][d] bf16, d_gu [R][2H] bf16,
-        dx_perm [R][d] fp32, and ds_gu [T][2Hs] bf16 with a shared expert."""
+        dx_perm [R][d] bf16, and ds_gu [T][2Hs] bf16 with a shared expert."""
         import torch
         if not self.training:
             raise ValueError("only a training workspace holds the backward's intermediates")
@@ -380,7 +380,7 @@ class Layer:
             return self.ws[o:o + nb].view(dt).view(*shape)
         out = dict(d_out=view(off[0], R * d, torch.bfloat16, (R, d)),
                    d_gu=view(off[1], R * 2 * H, torch.bfloat16, (R, 2 * H)),
-                   dx_perm=view(off[2], R * d, torch.float32, (R, d)))
+                   dx_perm=view(off[2], R * d, torch.bfloat16, (R, d)))
         if Hs:
             out["ds_gu"] = view(off[3], self.cfg.T * 2 * Hs, torch.bfloat16,
                                 (self.cfg.T, 2 * Hs))

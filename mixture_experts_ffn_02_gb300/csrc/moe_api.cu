@@ -79,7 +79,7 @@ int ws_layout(const moe_config* c, int training, WsLayout* w) {
     const size_t R = (size_t)w->R_cap;
     w->d_out = take(R * c->d * 2);
     w->d_gu = take(R * 2 * (size_t)c->H * 2);
-    w->dx_perm = take(R * c->d * 4);
+    w->dx_perm = take(R * c->d * 2);
     if (Hs > 0) {
       w->ds_gu = take((size_t)c->T * 2 * Hs * 2);
     }
@@ -249,9 +249,9 @@ int do_down(const moe_config* c, const moe_tensors* t, Call& k) {
   g.B = t->W_down;
   g.K = c->H;
   g.N = c->d;
-  g.out0 = t->out_perm;
+  g.out0 = t->out_perm;                        // bf16: each slot's output row
   g.ld0 = c->d;
-  g.out_f32 = 1;
+  g.out_f32 = 0;
   g.status = k.status;
   MOE_CUDA(launch_gemm(g, k.s));
   return MOE_OK;
@@ -370,7 +370,7 @@ int do_backward(const moe_config* c, const moe_tensors* t, const moe_grads* g, C
   const WsLayout& w = k.w;
   void* d_out = k.ws + w.d_out;
   void* d_gu = k.ws + w.d_gu;
-  float* dx_perm = reinterpret_cast<float*>(k.ws + w.dx_perm);
+  void* dx_perm = k.ws + w.dx_perm;           // bf16 [R][d]
   const int R = (int)w.R_cap;
 
   if (m) {
@@ -396,6 +396,7 @@ int do_backward(const moe_config* c, const moe_tensors* t, const moe_grads* g, C
     MxGemmCall x{};
     x.row_offsets = t->row_offsets; x.E = c->E; x.rows = R; x.d = c->d; x.H = 2 * c->H;
     x.A = m->dgu_q; x.sfa = m->dgu_s; x.B = m->W_gu_tq; x.sfb = m->W_gu_ts; x.out = dx_perm;
+    x.out_bf16 = 1;
     x.status = k.status;
     MOE_CUDA(launch_mx_gemm(x, k.s));
   } else {
@@ -410,7 +411,7 @@ int do_backward(const moe_config* c, const moe_tensors* t, const moe_grads* g, C
     GemmCall gx{};
     gx.kind = GK_DX; gx.row_offsets = t->row_offsets; gx.E = c->E; gx.rows = R;
     gx.A = d_gu; gx.lda = 2 * c->H; gx.B = t->W_gu; gx.K = 2 * c->H; gx.N = c->d;
-    gx.out0 = dx_perm; gx.ld0 = c->d; gx.out_f32 = 1; gx.status = k.status;
+    gx.out0 = dx_perm; gx.ld0 = c->d; gx.out_f32 = 0; gx.status = k.status;
     MOE_CUDA(launch_gemm(gx, k.s));
   }
   // (iv) dW_down[e] = d_out_e^T h_e ; dW_gu[e] = d_gu_e^T x_perm_e
@@ -593,6 +594,7 @@ int do_mx_gemm(const moe_config* c, const moe_tensors* t, const moe_mx_tensors* 
     MOE_NEED32(t->out_perm);
     g.A = m->h_q; g.sfa = m->h_s; g.B = m->W_down_q; g.sfb = m->W_down_s;
     g.out = t->out_perm;
+    g.out_bf16 = 1;
   }
   MOE_CUDA(launch_mx_gemm(g, k.s));
   return MOE_OK;

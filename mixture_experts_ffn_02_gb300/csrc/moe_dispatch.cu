@@ -1391,7 +1391,7 @@ perm_scatter_kernel(const bf16* __restrict__ x, const int32_t* __restrict__ topk
 // a6: y[t] = sum_j g[t][j] out_perm[inv[t][j]] (+ s_out[t]); one warp/token.
 // --------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads)
-combine_kernel(const float* __restrict__ out_perm, const int32_t* __restrict__ inv,
+combine_kernel(const bf16* __restrict__ out_perm, const int32_t* __restrict__ inv,
                const float* __restrict__ gates, const uint8_t* __restrict__ valid,
                const float* __restrict__ s_out, bf16* __restrict__ y, int T, int d, int k,
                long long rows, int* status) {
@@ -1414,7 +1414,7 @@ combine_kernel(const float* __restrict__ out_perm, const int32_t* __restrict__ i
           const float g = __shfl_sync(0xffffffffu, my_g, j);
           if (r < 0) continue;
           float v[8];
-          ld8f(out_perm + (size_t)r * d + c0, v);
+          unpack8(ld_nc_v4(out_perm + (size_t)r * d + c0), v);
 #pragma unroll
           for (int u = 0; u < 8; ++u) acc[u] = fmaf(g, v[u], acc[u]);
         }
@@ -1441,7 +1441,7 @@ combine_kernel(const float* __restrict__ out_perm, const int32_t* __restrict__ i
 // --------------------------------------------------------------------------
 template <int V>
 __global__ void __launch_bounds__(kThreads)
-combine_bwd_kernel(const bf16* __restrict__ dY, const float* __restrict__ out_perm,
+combine_bwd_kernel(const bf16* __restrict__ dY, const bf16* __restrict__ out_perm,
                    const int32_t* __restrict__ inv, const int32_t* __restrict__ topk,
                    const float* __restrict__ gates, const float* __restrict__ L,
                    const float* __restrict__ f, const int32_t* __restrict__ counts,
@@ -1489,7 +1489,7 @@ combine_bwd_kernel(const bf16* __restrict__ dY, const float* __restrict__ out_pe
         for (int c0 = lane * 8; c0 < d; c0 += 256) {
           float dy[8], o[8], go[8];
           unpack8(ld_nc_v4(dyr + c0), dy);
-          ld8f(out_perm + (size_t)r * d + c0, o);
+          unpack8(ld_nc_v4(out_perm + (size_t)r * d + c0), o);
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
             dot = fmaf(dy[u], o[u], dot);
@@ -1586,7 +1586,7 @@ combine_bwd_kernel(const bf16* __restrict__ dY, const float* __restrict__ out_pe
 // --------------------------------------------------------------------------
 template <int ES>
 __global__ void __launch_bounds__(kThreads)
-dx_gather_kernel(const float* __restrict__ dx_perm, const int32_t* __restrict__ inv,
+dx_gather_kernel(const bf16* __restrict__ dx_perm, const int32_t* __restrict__ inv,
                  const float* __restrict__ dxr,
                  const float* __restrict__ dL, const float* __restrict__ Wr,
                  const uint8_t* __restrict__ valid, bf16* __restrict__ dx, int T, int d,
@@ -1617,7 +1617,7 @@ dx_gather_kernel(const float* __restrict__ dx_perm, const int32_t* __restrict__ 
           const int r = __shfl_sync(0xffffffffu, my_r, j);
           if (r < 0) continue;
           float v[8];
-          ld8f(dx_perm + (size_t)r * d + c0, v);
+          unpack8(ld_nc_v4(dx_perm + (size_t)r * d + c0), v);
 #pragma unroll
           for (int u = 0; u < 8; ++u) acc[u] += v[u];
         }
@@ -2056,18 +2056,19 @@ cudaError_t launch_permute_mx(const moe_config& c, const void* x, const int32_t*
                     static_cast<bf16*>(x_perm), x_q, x_s, xt_q, xt_s, (c.T + 127) / 128 * 128);
 }
 
-cudaError_t launch_combine(const moe_config& c, const float* out_perm, const int32_t* inv,
+cudaError_t launch_combine(const moe_config& c, const void* out_perm, const int32_t* inv,
                            const float* gates, const uint8_t* valid, const float* s_out,
                            void* y, long long rows, int* status, cudaStream_t s) {
   DeviceInfo di;
   if (device_info(&di) != MOE_OK) return cudaErrorUnknown;
   const int grid = grid_for(kThreads / 32, c.T, di.num_sms * 8);
-  combine_kernel<<<grid, kThreads, 0, s>>>(out_perm, inv, gates, valid, s_out,
+  combine_kernel<<<grid, kThreads, 0, s>>>(static_cast<const bf16*>(out_perm), inv, gates,
+                                           valid, s_out,
                                            static_cast<bf16*>(y), c.T, c.d, c.k, rows, status);
   return cudaGetLastError();
 }
 
-cudaError_t launch_combine_bwd(const moe_config& c, const void* dY, const float* out_perm,
+cudaError_t launch_combine_bwd(const moe_config& c, const void* dY, const void* out_perm,
                                const int32_t* inv, const int32_t* topk, const float* gates,
                                const float* L, const float* f, const int32_t* counts,
                                const uint8_t* valid, const int32_t* row_offsets, void* d_out,
@@ -2080,7 +2081,7 @@ cudaError_t launch_combine_bwd(const moe_config& c, const void* dY, const float*
   const int V = (c.E + 31) / 32;
 #define MOE_CBWD(VV)                                                                          \
   combine_bwd_kernel<VV><<<grid, kThreads, 0, s>>>(                                           \
-      static_cast<const bf16*>(dY), out_perm, inv, topk, gates, L, f,                          \
+      static_cast<const bf16*>(dY), static_cast<const bf16*>(out_perm), inv, topk, gates, L, f, \
       counts, valid, row_offsets, static_cast<bf16*>(d_out), dout_q, dout_s, d_logits, c.T,    \
       c.d, c.E, c.k,                                                                           \
       c.norm_topk, c.aux_coef, c.z_coef, rows, status)
@@ -2092,14 +2093,14 @@ cudaError_t launch_combine_bwd(const moe_config& c, const void* dY, const float*
   return cudaGetLastError();
 }
 
-cudaError_t launch_dx_gather(const moe_config& c, const float* dx_perm, const int32_t* inv,
+cudaError_t launch_dx_gather(const moe_config& c, const void* dx_perm, const int32_t* inv,
                              const float* dxr, const float* d_logits,
                              const float* Wr, const uint8_t* valid, void* dx, long long rows,
                              int* status, cudaStream_t s) {
   DeviceInfo di;
   if (device_info(&di) != MOE_OK) return cudaErrorUnknown;
   const int grid = grid_for(kThreads / 32, c.T, di.num_sms * 4);
-  const float* dp = dx_perm;
+  const bf16* dp = static_cast<const bf16*>(dx_perm);
   bf16* o = static_cast<bf16*>(dx);
   if (router_small_path(c)) {
     const size_t smem = wr_smem_bytes(c.d, c.E);

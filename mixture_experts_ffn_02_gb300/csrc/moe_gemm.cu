@@ -94,7 +94,7 @@ struct Params {
   int* status;
   // GK_DOWN with the combine folded in (dense rows = tokens): y[t] =
   // bf16(sum_j g[t][j] comb_src[comb_inv[t][j]] + acc) into out0 (bf16)
-  const float* comb_src;
+  const bf16* comb_src;        // per-slot rows [R][N] in bf16
   const int32_t* comb_inv;
   const float* comb_gates;
   int comb_k;
@@ -498,14 +498,13 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const Tile& t, ui
               const int r = dbg_row(inv_t[j], p.comb_rows, p.status);
               if (r < 0) continue;
               const float g = g_t[j];
-              const float* src = p.comb_src + (size_t)r * p.N + col + c * 32;
+              const bf16* src = p.comb_src + (size_t)r * p.N + col + c * 32;
 #pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                const uint4 v = ld_nc_v4(src + i * 4);
-                acc[i * 4 + 0] = fmaf(g, __uint_as_float(v.x), acc[i * 4 + 0]);
-                acc[i * 4 + 1] = fmaf(g, __uint_as_float(v.y), acc[i * 4 + 1]);
-                acc[i * 4 + 2] = fmaf(g, __uint_as_float(v.z), acc[i * 4 + 2]);
-                acc[i * 4 + 3] = fmaf(g, __uint_as_float(v.w), acc[i * 4 + 3]);
+              for (int i = 0; i < 4; ++i) {
+                float v[8];
+                unpack8(ld_nc_v4(src + i * 8), v);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) acc[i * 8 + u] = fmaf(g, v[u], acc[i * 8 + u]);
               }
             }
           }
@@ -543,14 +542,13 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const Tile& t, ui
             for (int j = 0; j < p.comb_k; ++j) {
               const int r = dbg_row(inv_t[j], p.comb_rows, p.status);
               if (r < 0) continue;
-              const float* src = p.comb_src + (size_t)r * p.N + c0;
+              const bf16* src = p.comb_src + (size_t)r * p.N + c0;
 #pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const uint4 v = ld_nc_v4(src + i * 4);
-                acc[i * 4 + 0] += __uint_as_float(v.x);
-                acc[i * 4 + 1] += __uint_as_float(v.y);
-                acc[i * 4 + 2] += __uint_as_float(v.z);
-                acc[i * 4 + 3] += __uint_as_float(v.w);
+              for (int i = 0; i < 2; ++i) {
+                float v[8];
+                unpack8(ld_nc_v4(src + i * 8), v);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) acc[i * 8 + u] += v[u];
               }
             }
           }
@@ -1082,7 +1080,7 @@ cudaError_t launch_gemm(const GemmCall& g, cudaStream_t s) {
   p.ld_aux = g.ld_aux;
   p.valid = g.valid;
   p.status = g.status;
-  p.comb_src = g.comb_src;
+  p.comb_src = static_cast<const bf16*>(g.comb_src);
   p.comb_inv = g.comb_inv;
   p.comb_rows = g.comb_rows;
   p.comb_gates = g.comb_gates;

@@ -86,16 +86,16 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* to
                            const WsLayout& w, cudaStream_t s);
 // rows: the permuted rows that exist (R_cap); status: the workspace status
 // word, where debug builds latch MOE_ERR_BOUNDS for an inv entry past rows.
-cudaError_t launch_combine(const moe_config& c, const float* out_perm, const int32_t* inv,
+cudaError_t launch_combine(const moe_config& c, const void* out_perm, const int32_t* inv,
                            const float* gates, const uint8_t* valid, const float* s_out,
                            void* y, long long rows, int* status, cudaStream_t s);
-cudaError_t launch_combine_bwd(const moe_config& c, const void* dY, const float* out_perm,
+cudaError_t launch_combine_bwd(const moe_config& c, const void* dY, const void* out_perm,
                                const int32_t* inv, const int32_t* topk, const float* gates,
                                const float* L, const float* f, const int32_t* counts,
                                const uint8_t* valid, const int32_t* row_offsets,
                                void* d_out, uint8_t* dout_q, uint8_t* dout_s,
                                float* d_logits, long long rows, int* status, cudaStream_t s);
-cudaError_t launch_dx_gather(const moe_config& c, const float* dx_perm, const int32_t* inv,
+cudaError_t launch_dx_gather(const moe_config& c, const void* dx_perm, const int32_t* inv,
                              const float* dxr, const float* d_logits,
                              const float* Wr, const uint8_t* valid, void* dx, long long rows,
                              int* status, cudaStream_t s);
@@ -160,7 +160,7 @@ struct GemmCall {
   int* status;
   // GK_DOWN over dense token rows with the combine folded into the epilogue:
   // out0 = y (bf16) = sum_j comb_gates[t][j] comb_src[comb_inv[t][j]] + result
-  const float* comb_src;       // out_perm [R][N] fp32, or NULL (no combine)
+  const void* comb_src;        // out_perm (dx_perm) [R][N] bf16, or NULL (no fold)
   const int32_t* comb_inv;     // [rows][comb_k], -1 = unused slot
   int comb_rows;               // rows of comb_src (R_cap), for debug bounds checks
   const float* comb_gates;     // [rows][comb_k]
@@ -214,7 +214,8 @@ struct MxGemmCall {
   uint8_t* hs;                 // gate/up out: h scale atoms
   void* hb;                    // gate/up out (training): h [rows][H] bf16, or NULL
   void* abo;                   // gate/up out (training): a | b [rows][2H] fp16, or NULL
-  float* out;                  // down out: [rows][d] fp32 (d is the output width)
+  void* out;                   // down out: [rows][d] (d is the output width), fp32 or,
+  int out_bf16;                //   with out_bf16, bf16 (the per-slot out_perm, dx_perm)
   const void* abi;             // dH in: saved a | b [rows][2H] fp16
   void* dgu;                   // dH out: da | db [rows][2H] bf16
   uint8_t* dgq;                // dH out: codes of d_gu [rows][2H]

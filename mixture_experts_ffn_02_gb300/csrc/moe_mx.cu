@@ -101,7 +101,8 @@ struct XParams {
   uint8_t* hs;                 // gate/up: h scale atoms [R/128][H/128][512]
   bf16* hb;                    // gate/up, training: h [R][H] bf16, or NULL
   __half* abo;                 // gate/up, training: a | b [R][2H] fp16, or NULL
-  float* out;                  // down: out_perm [R][d] fp32
+  void* out;                   // down: [rows][d], fp32 or (out_bf16) bf16
+  int out_bf16;
   const __half* abi;           // dH: the saved a | b [R][2H] fp16
   bf16* dgu;                   // dH: d_gu = da | db [R][2H] bf16
   uint8_t* dgq;                // dH: codes of d_gu [R][2H]
@@ -547,8 +548,21 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           }
         }
       } else {
-        float* o = p.out + (size_t)row * p.d + t.n0 + half * 128;
-        if (row_ok) {
+        const size_t o0 = (size_t)row * p.d + t.n0 + half * 128;
+        if (row_ok && p.out_bf16) {
+          // the per-slot rows (out_perm, dx_perm) in bf16: 64 bytes per chunk
+          bf16* o = static_cast<bf16*>(p.out) + o0;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t w[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u)
+              w[u] = pack_bf16(__uint_as_float(r[c][2 * u]), __uint_as_float(r[c][2 * u + 1]));
+            st_v8(o + 32 * c, w);
+            st_v8(o + 32 * c + 16, w + 8);
+          }
+        } else if (row_ok) {
+          float* o = static_cast<float*>(p.out) + o0;
 #pragma unroll
           for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -755,6 +769,7 @@ cudaError_t launch_mx_gemm(const MxGemmCall& g, cudaStream_t s) {
   p.hb = static_cast<bf16*>(g.hb);
   p.abo = static_cast<__half*>(g.abo);
   p.out = g.out;
+  p.out_bf16 = g.out_bf16;
   p.abi = static_cast<const __half*>(g.abi);
   p.dgu = static_cast<bf16*>(g.dgu);
   p.dgq = g.dgq;

@@ -214,8 +214,8 @@ def _exact(a):
 
 
 def _store(rnd, point, v, where):
-    """The value kept at storage point ``point`` ("h", "a", "b", "d_out",
-    "da", "db"): ``rnd(v)``, or ``rnd.store(point, v, where)`` when the hook
+    """The value kept at storage point ``point`` ("h", "out", "a", "b",
+    "d_out", "da", "db", "dxe"): ``rnd(v)``, or ``rnd.store(point, v, where)`` when the hook
     has that method (``where`` names the rows: expert e, slot j, token rows,
     or shared=True).  No arithmetic happens here."""
     if rnd is None:
@@ -275,7 +275,8 @@ def experts_forward(x, topk_idx, gates, W_gu, W_down, Ws_gu=None, Ws_down=None,
     over the tokens that chose the same expert in the same slot, one fp64
     matmul each), then the gated outputs are summed.
     Returns (y [T][d], routed [T][k][d] = F_{e_{t,j}}(x_t)).
-    ``rnd`` rounds the stored hidden activations (see :func:`swiglu_parts`).
+    ``rnd`` rounds the stored hidden activations (see :func:`swiglu_parts`)
+    and each routed slot's expert output before the gated sum (point "out").
     """
     x = _f64(x); W_gu = _f64(W_gu); W_down = _f64(W_down)
     idx = np.asarray(topk_idx); g = np.asarray(gates, dtype=f64)
@@ -288,8 +289,10 @@ def experts_forward(x, topk_idx, gates, W_gu, W_down, Ws_gu=None, Ws_down=None,
         for e in range(E):
             rows = np.nonzero(idx[:, j] == e)[0]
             if rows.size:
-                routed[rows, j], *_ = swiglu_parts(x[rows], Wg[e], Wu[e], W_down[e], rnd,
-                                                   dict(e=e, j=j, rows=rows))
+                where = dict(e=e, j=j, rows=rows)
+                out, *_ = swiglu_parts(x[rows], Wg[e], Wu[e], W_down[e], rnd, where)
+                # each slot's expert output is kept until the slots are summed
+                routed[rows, j] = _store(rnd, "out", out, where)
     y = np.einsum("tj,tjd->td", g, routed)
     real = np.ones(T, dtype=bool) if valid is None else (np.asarray(_np(valid)) != 0)
     if Ws_gu is not None:
@@ -388,10 +391,12 @@ def backward(x, Wr, W_gu, W_down, Ws_gu, Ws_down, fwd, dY, norm_topk=True,
     ``rnd`` (default: none) rounds the values a bf16-storage implementation
     keeps between its matrix products (see :func:`_store` for a hook that
     also receives the storage point and rows) -- the hidden h
-    (:func:`swiglu_parts`),
-    d_out = g dY of the routed rows (:func:`stored_d_out`), the saved
-    pre-activations a and b and the results (da, db) of the SwiGLU chain rule
-    (:func:`stored_swiglu_backward`) -- without changing any arithmetic step.
+    (:func:`swiglu_parts`), each routed slot's expert output ("out", read
+    for dg), d_out = g dY of the routed rows (:func:`stored_d_out`), the
+    saved pre-activations a and b and the results (da, db) of the SwiGLU
+    chain rule (:func:`stored_swiglu_backward`), and each routed slot's dx
+    contribution before the slots are summed ("dxe") -- without changing any
+    arithmetic step.
     The shared expert's d_out is dY itself (an input, not rounded again).
     With ``rnd`` None this is the exact gradient.
     """
@@ -416,10 +421,12 @@ def backward(x, Wr, W_gu, W_down, Ws_gu, Ws_down, fwd, dY, norm_topk=True,
             xr = x[rows]
             where = dict(e=e, j=j, rows=rows)
             out, a, b, h = swiglu_parts(xr, Wg[e], Wu[e], W_down[e], rnd, where)
+            out = _store(rnd, "out", out, where)
             dg[rows, j] = (dY[rows] * out).sum(axis=1)
             d_out = stored_d_out(g[rows, j], dY[rows], rnd, where)
             da, db = stored_swiglu_backward(d_out @ W_down[e], a, b, rnd, where)
-            dx[rows] += da @ Wg[e] + db @ Wu[e]
+            # the slot's dx contribution is kept until the slots are summed
+            dx[rows] += _store(rnd, "dxe", da @ Wg[e] + db @ Wu[e], where)
             dW_down[e] += d_out.T @ h
             dW_gu[e, :H] += da.T @ xr
             dW_gu[e, H:] += db.T @ xr

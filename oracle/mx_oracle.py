@@ -159,6 +159,8 @@ class _HiddenMX:
         self.rnd = rnd
 
     def store(self, point, v, where):
+        if point != "h":                      # the other storage points: the hook's
+            return mo._store(self.rnd, point, v, where)
         return _quantised(self.rnd, "q_h", v, mx_roundtrip, where)
 
 
@@ -241,7 +243,9 @@ def backward_mx(x, Wr, W_gu, W_down, Ws_gu, Ws_down, fwd, dY, norm_topk=True,
       which makes such moves about 8 times rarer).
     * The weight-gradient products take the saved h, d_out, d_gu and x at
       the bf16 storage points of the bf16 layer (``rnd``, the hook of
-      ``moe_oracle.backward``; h here is the hidden before its MX rounding).
+      ``moe_oracle.backward``; h here is the hidden before its MX rounding),
+      and each slot's expert output and dx contribution are kept in bf16
+      before the slots are summed, as there ("out", "dxe").
     * The quantisations of h, d_out and d_gu are points of the same hook
       (:func:`_quantised`: "q_h", "q_d_out", "q_d_gu"), so that a test can
       continue from another valid quantisation.
@@ -283,7 +287,7 @@ def backward_mx(x, Wr, W_gu, W_down, Ws_gu, Ws_down, fwd, dY, norm_topk=True,
             a = xq[rows] @ qg.T
             b = xq[rows] @ qu.T
             hf = mo.silu(a) * b
-            out = _quantised(rnd, "q_h", hf, quant, where) @ qd.T
+            out = mo._store(rnd, "out", _quantised(rnd, "q_h", hf, quant, where) @ qd.T, where)
             dg[rows, j] = (dY[rows] * out).sum(axis=1)
             h = mo._store(rnd, "h", hf, where)
             # d_out = g dY and d_gu = [da | db] enter their MX products
@@ -296,7 +300,8 @@ def backward_mx(x, Wr, W_gu, W_down, Ws_gu, Ws_down, fwd, dY, norm_topk=True,
                                             _store16(rnd, "b16", b, where))
             da, db = mo._store(rnd, "da", da_v, where), mo._store(rnd, "db", db_v, where)
             d_gu = np.concatenate([da_v, db_v], axis=1)
-            dx[rows] += _quantised(rnd, "q_d_gu", d_gu, quant, where) @ qgu_k
+            dx[rows] += mo._store(rnd, "dxe", _quantised(rnd, "q_d_gu", d_gu, quant, where) @ qgu_k,
+                                  where)
             dW_down[e] += d_out.T @ h
             dW_gu[e, :H] += da.T @ x[rows]
             dW_gu[e, H:] += db.T @ x[rows]

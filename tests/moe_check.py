@@ -106,7 +106,8 @@ class AdoptStored:
     """Storage hook for the oracle (``rnd=``) that continues from the GPU's
     own stored bf16 values wherever they are a valid rounding.
 
-    The layer keeps h, a, b, d_out, da and db in bf16, each the rounding of
+    The layer keeps h, each routed slot's output (out), a, b, d_out, da, db
+    and each routed slot's dx contribution (dxe) in bf16, each the rounding of
     an fp32 result (the MX training step keeps a and b in fp16: points a16,
     b16).  Where that result lies within its accumulation error of
     a rounding boundary, either bf16 neighbour is a correct outcome, as a
@@ -272,7 +273,9 @@ def stored_from_layer(lay, with_backward, cols=None, shared_cols=None):
             r = r[:, c0:c0 + n] if sel is None else r[:, sel]
             return np64(r)
         return get
-    out = {"h": (pick(b["h"], 0, H, cols), pick(b.get("s_h"), 0, Hs, shared_cols))}
+    out = {"h": (pick(b["h"], 0, H, cols), pick(b.get("s_h"), 0, Hs, shared_cols)),
+           # each routed slot's expert output (the shared expert's is not kept)
+           "out": (pick(b["out_perm"], 0, lay.cfg.d, None), None)}
     if b.get("ab") is not None:
         out["a"] = (pick(b["ab"], 0, H, cols), pick(b.get("s_ab"), 0, Hs, shared_cols))
         out["b"] = (pick(b["ab"], H, H, cols), pick(b.get("s_ab"), Hs, Hs, shared_cols))
@@ -281,6 +284,7 @@ def stored_from_layer(lay, with_backward, cols=None, shared_cols=None):
         out["d_out"] = (pick(it["d_out"], 0, lay.cfg.d, None), None)
         out["da"] = (pick(it["d_gu"], 0, H, cols), pick(it.get("ds_gu"), 0, Hs, shared_cols))
         out["db"] = (pick(it["d_gu"], H, H, cols), pick(it.get("ds_gu"), Hs, Hs, shared_cols))
+        out["dxe"] = (pick(it["dx_perm"], 0, lay.cfg.d, None), None)
     mx = getattr(lay, "mx", None)
     if mx is not None:
         # the MXFP8 path's quantised operands (codes + block scales per row;

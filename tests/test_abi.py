@@ -46,7 +46,7 @@ def test_library_exports_every_declared_symbol(clib):
 
 
 def test_abi_version_and_messages(clib):
-    assert clib.moe_abi_version() == 5
+    assert clib.moe_abi_version() == 6
     for code in range(10):
         assert clib.moe_strerror(code)
     assert b"unknown" in clib.moe_strerror(99)

@@ -43,8 +43,8 @@ def test_hbm_bytes_closed_forms():
     bp = bench.hbm_bytes(p)
     Tr, M = 60293, 60293 * 2
     assert bp["permute"] == Tr * 512 * 2 + M * 512 * 2 + 65536 * 2 * 4 + M * 4 + 65536 * 2 * 4
-    # out_perm fp32 in, no shared expert, inv + gates in, y (bf16, all positions) out
-    assert bp["combine"] == M * 512 * 4 + 65536 * 2 * 8 + 65536 * 512 * 2
+    # out_perm bf16 in, no shared expert, inv + gates in, y (bf16, all positions) out
+    assert bp["combine"] == M * 512 * 2 + 65536 * 2 * 8 + 65536 * 512 * 2
 
 
 def test_aggregate_single_rank():

@@ -83,7 +83,7 @@ def test_planted_inv_row_is_caught_and_skipped(dlib):
     r0 = int(inv[t * SHAPE.k])
     g0 = float(lay.bufs["gates"].view(-1)[t * SHAPE.k])
     ref = (torch.tensor(g0, dtype=torch.float32, device=y.device) *
-           lay.bufs["out_perm"][r0]).to(torch.bfloat16)      # fp32 product, one rounding
+           lay.bufs["out_perm"][r0].float()).to(torch.bfloat16)   # fp32 product, one rounding
     assert torch.equal(y[t], ref)
     inv[t * SHAPE.k + j] = keep
     lay.combine()

@@ -104,6 +104,25 @@ def route_like_gpu(s, inp, lay, rows=None):
     return r, x, valid
 
 
+def check_mx_y(chk, name, lay, s, x, topk, gates, W_gu, W_down, Ws_gu, Ws_down, valid,
+               tokens=None):
+    """y of the MX forward against the MX oracle at the bounds of every bf16
+    output: max-normalised |gpu - ideal| <= 1e-2, where ideal continues from
+    the GPU's valid choices at its rounding points (the h codes and each
+    routed slot's bf16 output), and Frobenius-relative |gpu - exact| <= 1e-2.
+    ``tokens``: the oracle's rows are these tokens of the batch.  Returns the
+    exact y."""
+    row_of_pair = lay.bufs["inv"].cpu().numpy()
+    adopt = AdoptStored(stored_from_layer(lay, False), row_of_pair, s.k, tokens=tokens)
+    args = (x, topk, gates, W_gu, W_down, Ws_gu, Ws_down, valid)
+    y_ex, _ = M.experts_forward_mx(*args)
+    y_id, _ = M.experts_forward_mx(*args, rnd=adopt)
+    gpu = lay.bufs["y"] if tokens is None else lay.bufs["y"][torch.from_numpy(tokens).cuda()]
+    chk.layer(name, gpu, y_ex, y_id)
+    adopt.check(chk)
+    return y_ex
+
+
 # cfg, tokens, overrides: the 64- and 128-expert shapes keep E, k, the bias
 # and the shared experts but get smaller d and H, so that the fp64 quantiser
 # of all their weights stays within seconds (the KochiLLM and packed shapes
@@ -173,13 +192,12 @@ def test_mx_forward_matches_oracle(cfg, T, over):
     inp, lay = mx_layer(s)
     r, x, valid = route_like_gpu(s, inp, lay)
     np.testing.assert_array_equal(lay.bufs["topk_idx"].cpu().numpy(), r["topk_idx"])
-    y_mx, _ = M.experts_forward_mx(x, r["topk_idx"], r["gates"], inp["W_gu"], inp["W_down"],
-                                   inp["Ws_gu"], inp["Ws_down"], valid)
     y_bf, _ = O.experts_forward(x, r["topk_idx"], r["gates"], inp["W_gu"], inp["W_down"],
                                 inp["Ws_gu"], inp["Ws_down"], valid)
     chk = Checker()
-    chk.close("y_mx", lay.bufs["y"], y_mx)
-    e_mx = chk.rows[-1][1]
+    y_mx = check_mx_y(chk, "y_mx", lay, s, x, r["topk_idx"], r["gates"], inp["W_gu"],
+                      inp["W_down"], inp["Ws_gu"], inp["Ws_down"], valid)
+    e_mx = chk.rows[0][1]                          # |gpu - ideal| max
     chk.done()
     # the bf16 layer's output is far outside the MX tolerance: the test
     # tells the two paths apart
@@ -240,10 +258,9 @@ def test_mx_full_size_kochillm_sampled():
     rows[-1] = s.T - 1
     r, x, valid = route_like_gpu(s, inp, lay, rows)
     np.testing.assert_array_equal(lay.bufs["topk_idx"].cpu().numpy()[rows], r["topk_idx"])
-    y_mx, _ = M.experts_forward_mx(x, r["topk_idx"], r["gates"], inp["W_gu"], inp["W_down"],
-                                   inp["Ws_gu"], inp["Ws_down"], valid)
     chk = Checker()
-    chk.close("y_mx[sample]", lay.bufs["y"][rows], y_mx)
+    check_mx_y(chk, "y_mx[sample]", lay, s, x, r["topk_idx"], r["gates"], inp["W_gu"],
+               inp["W_down"], inp["Ws_gu"], inp["Ws_down"], valid, tokens=rows)
     chk.done()
 
 
@@ -269,7 +286,7 @@ def test_mx_rejects_code_buffers_off_32_bytes():
     assert ei.value.code == 3
     lay.mx["h_q"] = keep
     keep = lay.bufs["out_perm"]
-    lay.bufs["out_perm"] = keep.view(-1)[4:]
+    lay.bufs["out_perm"] = keep.view(-1)[8:]          # 16 bytes in (bf16)
     with pytest.raises(binding.MoEError) as ei:
         lay.mx_down()
     assert ei.value.code == 3
@@ -316,10 +333,9 @@ def test_mx_full_size_sampled(cfg, n_tok):
     topk_c = np.where(topk >= 0, np.searchsorted(used, np.maximum(topk, 0)), -1)
     W_gu = inp["W_gu"][torch.from_numpy(used)]
     W_down = inp["W_down"][torch.from_numpy(used)]
-    y_mx, _ = M.experts_forward_mx(x, topk_c, r["gates"], W_gu, W_down, inp["Ws_gu"],
-                                   inp["Ws_down"], valid)
     chk = Checker()
-    chk.close("y_mx[sample]", lay.bufs["y"][rows], y_mx)
+    check_mx_y(chk, "y_mx[sample]", lay, s, x, topk_c, r["gates"], W_gu, W_down,
+               inp["Ws_gu"], inp["Ws_down"], valid, tokens=rows)
     chk.done()
     E, d, H = s.E, s.d, s.H
     q_gpu = u8(lay.mx["W_gu_q"], E * 2 * H * d).reshape(E, 2 * H, d)
@@ -369,10 +385,9 @@ def test_mx_edge_shapes(name, shape, bias):
     inp, lay = _mx_run(s, bias=b)
     r, x, valid = route_like_gpu(s, inp, lay)
     np.testing.assert_array_equal(lay.bufs["topk_idx"].cpu().numpy(), r["topk_idx"])
-    y_mx, _ = M.experts_forward_mx(x, r["topk_idx"], r["gates"], inp["W_gu"], inp["W_down"],
-                                   inp["Ws_gu"], inp["Ws_down"], valid)
     chk = Checker()
-    chk.close("y_mx", lay.bufs["y"], y_mx)
+    check_mx_y(chk, "y_mx", lay, s, x, r["topk_idx"], r["gates"], inp["W_gu"], inp["W_down"],
+               inp["Ws_gu"], inp["Ws_down"], valid)
     chk.done()
 
 

@@ -200,6 +200,9 @@ def _storage_pins_fail():
 def _values_fail(monkeypatch):
     """The value checks alone (a spy that records nothing) also catch it."""
     class Quiet(S.Spy):
+        def store(self, point, v, where):
+            return S.qpoint(point, v)
+
         def __call__(self, v):
             return S.q8(v)
     monkeypatch.setattr(S, "Spy", Quiet)
@@ -222,13 +225,26 @@ def test_unrounded_hidden_is_caught(monkeypatch):
     assert _values_fail(monkeypatch)
 
 
-def test_rounded_expert_output_is_caught(monkeypatch):
+def test_rounded_shared_expert_output_is_caught(monkeypatch):
+    """The shared expert's output is summed straight into y (no per-slot copy)."""
     orig = O.swiglu_parts
 
     def parts(xr, Wg, Wu, Wd, rnd=None, where=None):
         out, a, b, h = orig(xr, Wg, Wu, Wd, rnd, where)
-        return (rnd(out) if rnd else out), a, b, h
+        shared = where is not None and where.get("shared")
+        return (rnd(out) if rnd and shared else out), a, b, h
     monkeypatch.setattr(O, "swiglu_parts", parts)
+    assert _storage_pins_fail()
+    assert _values_fail(monkeypatch)
+
+
+@pytest.mark.parametrize("point", ["out", "dxe"])
+def test_unrounded_per_slot_value_is_caught(monkeypatch, point):
+    """A routed slot's expert output, or its dx contribution, not kept at its
+    storage point before the slots are summed."""
+    orig = O._store
+    monkeypatch.setattr(O, "_store", lambda rnd, p, v, where: v if p == point
+                        else orig(rnd, p, v, where))
     assert _storage_pins_fail()
     assert _values_fail(monkeypatch)
 
@@ -301,10 +317,10 @@ def test_mx_dgrad_weights_quantised_along_the_wrong_axis_are_caught(monkeypatch)
 
 def test_mx_dgrad_unquantised_d_gu_is_caught(monkeypatch):
     src = inspect.getsource(M.backward_mx)
-    needle = 'dx[rows] += _quantised(rnd, "q_d_gu", d_gu, quant, where) @'
+    needle = '_quantised(rnd, "q_d_gu", d_gu, quant, where) @ qgu_k'
     assert needle in src
     ns = dict(vars(M))
-    exec(src.replace(needle, "dx[rows] += d_gu @"), ns)
+    exec(src.replace(needle, "d_gu @ qgu_k"), ns)
     monkeypatch.setattr(M, "backward_mx", ns["backward_mx"])
     assert _fails(MXP.test_mx_backward_quantises_each_operand_along_its_reduction_axis)
     assert _fails(MXP.test_mx_backward_dense_masked_formulation)

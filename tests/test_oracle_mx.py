@@ -275,7 +275,7 @@ def test_mx_training_forward_has_the_bf16_shared_expert():
     x, Wr, W_gu, W_down, Ws_gu, Ws_down, dY, fwd = _train_case(11)
     y_t, _ = M.experts_forward_mx(x, fwd["topk_idx"], fwd["gates"], W_gu, W_down, Ws_gu,
                                   Ws_down, shared_mx=False, rnd=_bf16)
-    y_r, _ = M.experts_forward_mx(x, fwd["topk_idx"], fwd["gates"], W_gu, W_down)
+    y_r, _ = M.experts_forward_mx(x, fwd["topk_idx"], fwd["gates"], W_gu, W_down, rnd=_bf16)
     sg, su = O.split_gu(Ws_gu)
     shared, *_ = O.swiglu_parts(x, sg, su, Ws_down, _bf16)
     np.testing.assert_allclose(y_t - y_r, shared, rtol=1e-12, atol=1e-12)
@@ -347,7 +347,7 @@ def test_mx_backward_dense_masked_formulation():
         Wg, Wu = W_gu[e][:H], W_gu[e][H:]
         a = xq @ Q(Wg).T
         b = xq @ Q(Wu).T
-        out = Q(a / (1 + np.exp(-a)) * b) @ Q(W_down[e]).T
+        out = _bf16(Q(a / (1 + np.exp(-a)) * b) @ Q(W_down[e]).T)   # kept in bf16
         WdT = Q(W_down[e].T)                 # rows of W_down^T: blocks along d
         WguT = Q(W_gu[e].T)                  # rows of W_gu^T: blocks along 2H
         for j in range(fwd["topk_idx"].shape[1]):
@@ -359,7 +359,7 @@ def test_mx_backward_dense_masked_formulation():
             sa = 1 / (1 + np.exp(-a16))
             da = dH * b16 * sa * (1 + a16 * (1 - sa))
             db = dH * a16 * sa
-            dx += np.where(m[:, None], Q(np.concatenate([da, db], axis=1)) @ WguT.T, 0.0)
+            dx += np.where(m[:, None], _bf16(Q(np.concatenate([da, db], axis=1)) @ WguT.T), 0.0)
     dL = O.router_logit_grad(dg, fwd["topk_idx"], fwd["gates"], fwd["probs"], True)
     dL += O.aux_logit_grad(fwd["probs"], fwd["f"], fwd["real"], 0.01)
     dx += dL @ Wr.T
