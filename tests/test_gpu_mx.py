@@ -645,3 +645,87 @@ def test_mx_train_full_size_sampled(cfg, n_tok):
     chk.done()
     del lay
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name,shape,bias,valid_real", [
+    ("single_token", dict(T=1, d=256, E=8, k=2, H=256, n_shared=1, H_shared=128), None, None),
+    ("one_expert_full", dict(T=900, d=256, E=16, k=1, H=256, n_shared=0, H_shared=0),
+     [100.0] + [0.0] * 15, None),
+    ("half_pad", dict(T=600, d=256, E=8, k=2, H=128, n_shared=1, H_shared=128), None, 300),
+])
+def test_mx_train_edge_shapes(name, shape, bias, valid_real):
+    """The MX training step on one token (one padded 128-row block per
+    tensor), on every token sent to one expert (every other expert's
+    gradients exactly 0), and on a batch whose second half is PAD (dx and
+    d_logits exactly 0 there), against the MX training oracle."""
+    s = synth.MoEShape(name, training=True, **shape)
+    inp = synth.make_inputs(s, seed=3, with_grad=True)
+    if bias is not None:
+        inp["bias"] = torch.tensor(bias, dtype=torch.float32)
+    if valid_real is not None:
+        v = torch.zeros(s.T, dtype=torch.uint8)
+        v[:valid_real] = 1
+        inp["valid"] = v
+    lay = Layer.create(s, training=True)
+    dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    lay.set_inputs(dev["x"], dev["Wr"], dev["W_gu"], dev["W_down"], dev["Ws_gu"],
+                   dev["Ws_down"], bias=dev["bias"], valid=dev["valid"])
+    lay.mx_alloc()
+    lay.mx_quantize_weights()
+    lay.mx_step(dev["dY"])
+    torch.cuda.synchronize()
+    assert lay.status() == 0
+    r, x, valid = route_like_gpu(s, inp, lay)
+    np.testing.assert_array_equal(lay.bufs["topk_idx"].cpu().numpy(), r["topk_idx"])
+    fwd = train_fwd(s, inp, r)
+    adopt = AdoptStored(stored_from_layer(lay, True), padded_layout(r["topk_idx"], s.E)[2], s.k)
+    args = (x, inp["Wr"], inp["W_gu"], inp["W_down"], inp["Ws_gu"], inp["Ws_down"], fwd,
+            inp["dY"])
+    ex = M.backward_mx(*args, aux_coef=s.aux_coef)
+    idl = M.backward_mx(*args, aux_coef=s.aux_coef, rnd=adopt)
+    fw = (x, r["topk_idx"], r["gates"], inp["W_gu"], inp["W_down"], inp["Ws_gu"],
+          inp["Ws_down"], valid)
+    chk = Checker()
+    chk.layer("y", lay.bufs["y"], M.experts_forward_mx(*fw, shared_mx=False)[0],
+              M.experts_forward_mx(*fw, shared_mx=False, rnd=adopt)[0])
+    for n in ("dx", "dW_gu", "dW_down", "d_logits"):
+        chk.layer(n, lay.grads[n], ex[n], idl[n])
+    adopt.check(chk)
+    chk.done()
+    g = lay.grads
+    if name == "one_expert_full":
+        assert not g["dW_gu"][1:].any() and not g["dW_down"][1:].any()
+    if valid_real is not None:
+        assert not g["dx"][valid_real:].any() and not g["d_logits"][valid_real:].any()
+
+
+@pytest.mark.parametrize("norm_topk,z_coef", [(0, 0.0), (1, 1e-3)])
+def test_mx_train_raw_gates_and_z_loss(norm_topk, z_coef):
+    """The MX training step without gate renormalisation, and with the
+    router z-loss term, against the MX training oracle (the same router
+    terms as the bf16 layer's)."""
+    s = synth.scaled(synth.shape(5), T=700, d=512, H=256, norm_topk=norm_topk, z_coef=z_coef)
+    inp = synth.make_inputs(s, seed=4, with_grad=True)
+    lay = Layer.create(s, training=True)
+    dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    lay.set_inputs(dev["x"], dev["Wr"], dev["W_gu"], dev["W_down"], dev["Ws_gu"],
+                   dev["Ws_down"], bias=dev["bias"], valid=dev["valid"])
+    lay.mx_alloc()
+    lay.mx_quantize_weights()
+    lay.mx_step(dev["dY"])
+    torch.cuda.synchronize()
+    assert lay.status() == 0
+    r, x, valid = route_like_gpu(s, inp, lay)
+    np.testing.assert_array_equal(lay.bufs["topk_idx"].cpu().numpy(), r["topk_idx"])
+    fwd = train_fwd(s, inp, r)
+    fwd["logits"] = O.router_logits(x, inp["Wr"])
+    adopt = AdoptStored(stored_from_layer(lay, True), padded_layout(r["topk_idx"], s.E)[2], s.k)
+    args = (x, inp["Wr"], inp["W_gu"], inp["W_down"], None, None, fwd, inp["dY"])
+    kw = dict(norm_topk=bool(norm_topk), aux_coef=s.aux_coef, z_coef=z_coef)
+    ex = M.backward_mx(*args, **kw)
+    idl = M.backward_mx(*args, rnd=adopt, **kw)
+    chk = Checker()
+    for n in ("dx", "dW_gu", "dW_down", "d_logits", "dWr"):
+        chk.layer(n, lay.grads[n], ex[n], idl[n])
+    adopt.check(chk)
+    chk.done()
