@@ -714,8 +714,11 @@ def run_reference(args):
         return
     s = workload_shape(args)
     training = not args.fwd_only
-    # the same sample size as the cpu_baseline leg, so both report one rate
-    n, _ = oracle_sample_tokens(s, training)
+    # the cpu_baseline leg's sample size (about 3 s per pass), so both report
+    # one rate -- smaller when the step count would make the run longer than
+    # about 150 s of oracle work (a sample ends at most twice its target)
+    n, _ = oracle_sample_tokens(s, training,
+                                target_s=min(3.0, 75.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
         oracle_sample(s, n, training)
     dt = sum(oracle_sample(s, n, training) for _ in range(args.steps))
