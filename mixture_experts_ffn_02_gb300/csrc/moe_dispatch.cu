@@ -11,6 +11,8 @@
 #include <stdlib.h>
 #include <math.h>
 
+#include <utility>
+
 #include "moe_common.cuh"
 #include "moe_mx.cuh"
 #include "moe_internal.h"
@@ -231,7 +233,9 @@ router_dw_small_kernel(const bf16* __restrict__ x, const float* __restrict__ dL,
 template <int BE>
 __global__ void __launch_bounds__(256)
 router_logits_sgemm_kernel(const bf16* __restrict__ x, const float* __restrict__ Wr,
-                           float* __restrict__ L, int T, int d, int E) {
+                           float* __restrict__ L, int T, int d, int E, int tpb) {
+  // a block computes tokens [t0, t0 + tpb) (tpb <= 128, the register tile),
+  // so that the grid can be a whole number of waves over the SMs
   constexpr int BT = 128, BK = 16, TE = BE / 16;
   __shared__ __align__(16) float As[2][BK][BT + 4];
   __shared__ __align__(16) float Bs[2][BK][BE + 4];
@@ -240,7 +244,8 @@ router_logits_sgemm_kernel(const bf16* __restrict__ x, const float* __restrict__
   // j < TE/4, so that each quarter-warp reads one contiguous 128-byte span of
   // the B slice (no bank conflicts)
   const int tx = tid & 15, ty = tid >> 4;
-  const int t0 = blockIdx.y * BT, e0 = blockIdx.x * BE;
+  const int t0 = blockIdx.y * tpb, e0 = blockIdx.x * BE;
+  const int t_end = min(T, t0 + tpb);
   // A slice: thread -> token tid/2, k-half (tid%2)*8 (one 16-byte load)
   const int at = tid >> 1, ak = (tid & 1) * 8;
   // B slice: BK x BE floats, float4 per load
@@ -254,7 +259,7 @@ router_logits_sgemm_kernel(const bf16* __restrict__ x, const float* __restrict__
   float4 breg[BV];
   auto load = [&](int k0) {
     const int t = t0 + at;
-    areg = (t < T) ? ld_nc_v4(x + (size_t)t * d + k0 + ak) : make_uint4(0, 0, 0, 0);
+    areg = (t < t_end) ? ld_nc_v4(x + (size_t)t * d + k0 + ak) : make_uint4(0, 0, 0, 0);
 #pragma unroll
     for (int v = 0; v < BV; ++v) {
       const int idx = tid + v * 256;            // float4 index in the BK x BE/4 slice
@@ -308,7 +313,7 @@ router_logits_sgemm_kernel(const bf16* __restrict__ x, const float* __restrict__
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int t = t0 + ty * 8 + i;
-    if (t >= T) continue;
+    if (t >= t_end) continue;
 #pragma unroll
     for (int j = 0; j < TE; j += 4) {
       const int e = e0 + (j / 4) * 64 + tx * 4;
@@ -1721,14 +1726,37 @@ cudaError_t launch_router_logits(const moe_config& c, const void* x, const float
   }
   if (c.E % 32 == 0 && c.d % 16 == 0) {
     // L[T][E] = x[T][d] . Wr[d][E], register-tiled fp32 FMA
+    // token blocks: ceil(T / 128) rounded up to whole waves (SMs x resident
+    // blocks per SM for the expert columns of one block row), each block
+    // taking ceil(T / blocks) <= 128 tokens; a token's arithmetic does not
+    // depend on its block
+    DeviceInfo di;
+    if (device_info(&di) != MOE_OK) return cudaErrorUnknown;
+    auto waves = [&](auto kern, int gx) {
+      int per_sm = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, 0) != cudaSuccess ||
+          per_sm < 1) {
+        cudaGetLastError();
+        per_sm = 1;
+      }
+      const long long slots = (long long)di.num_sms * per_sm;
+      long long by = (c.T + 127) / 128;
+      const long long total = by * gx;
+      if (total % slots != 0 && total > slots / 2) {
+        const long long want = (total + slots - 1) / slots * slots;
+        by = (want + gx - 1) / gx;
+      }
+      const int tpb = (int)((c.T + by - 1) / by);
+      return std::make_pair(dim3((unsigned)gx, (unsigned)((c.T + tpb - 1) / tpb), 1), tpb);
+    };
     if (c.E % 128 == 0) {
-      dim3 grid(c.E / 128, (c.T + 127) / 128, 1);
-      router_logits_sgemm_kernel<128><<<grid, 256, 0, s>>>(static_cast<const bf16*>(x), Wr, L,
-                                                           c.T, c.d, c.E);
+      const auto g = waves(router_logits_sgemm_kernel<128>, c.E / 128);
+      router_logits_sgemm_kernel<128><<<g.first, 256, 0, s>>>(static_cast<const bf16*>(x), Wr,
+                                                              L, c.T, c.d, c.E, g.second);
     } else {
-      dim3 grid((c.E + 63) / 64, (c.T + 127) / 128, 1);
-      router_logits_sgemm_kernel<64><<<grid, 256, 0, s>>>(static_cast<const bf16*>(x), Wr, L,
-                                                          c.T, c.d, c.E);
+      const auto g = waves(router_logits_sgemm_kernel<64>, (c.E + 63) / 64);
+      router_logits_sgemm_kernel<64><<<g.first, 256, 0, s>>>(static_cast<const bf16*>(x), Wr,
+                                                             L, c.T, c.d, c.E, g.second);
     }
     return cudaGetLastError();
   }
