@@ -492,9 +492,10 @@ int moe_mx_forward_train(const moe_config* cfg, const moe_tensors* t, const moe_
  * it; dH = Q(d_out) Q(W_down[e]^T) runs on the block-scaled tcgen05 kernel
  * with the SwiGLU chain rule (on ab16) in its epilogue, which quantises the
  * fp32 d_gu = da | db along 2H (dgu_q/s) and stores it in bf16 for the
- * weight gradient; and dx = Q(d_gu) Q(W_gu[e]^T).  Each MX operand is thus
- * one rounding of its fp32 value, never of a bf16 copy.  The weight gradients, the shared expert and
- * the router are moe_backward's (bf16 operands, fp32 accumulation).  Needs a
+ * weight gradient; and dx = Q(d_gu) Q(W_gu[e]^T), written as bf16 dx_perm
+ * rows.  Each MX operand is thus one rounding of its fp32 value, never of a
+ * bf16 copy.  The weight gradients, the shared expert and the router are
+ * moe_backward's (bf16 operands, fp32 accumulation).  Needs a
  * training workspace (moe_workspace_bytes with training = 1), the forward
  * tensors of moe_mx_forward_train, the transposed weight codes of
  * moe_mx_quantize_weights, ab16, and dout_q/s, dgu_q/s (32-byte aligned
