@@ -528,10 +528,11 @@ def run_e2e(args, s, inp, lay, training, local):
     """The same layer step through moe_forward/moe_backward with host
     buffers, driven the way a training loop would: every step copies its
     inputs x and dY in from pinned host memory and its results y, aux and dx
-    back out, all inside the timed region.  The copies run on a copy stream
-    ordered by events: x, y and dx are double-buffered so the next step's x
-    upload overlaps this step's compute and this step's downloads overlap the
-    next step's; dY's upload overlaps the forward."""
+    back out, all inside the timed region.  Uploads run on one stream and
+    downloads on another (the two directions use separate copy engines),
+    ordered by events: x, dY, y and dx are double-buffered, so the next
+    step's uploads overlap this step's compute and this step's downloads
+    overlap the next step's."""
     import torch
     hx = inp["x"].pin_memory()
     hdy = inp["dY"].pin_memory()
@@ -539,26 +540,29 @@ def run_e2e(args, s, inp, lay, training, local):
     hdx = torch.empty_like(inp["x"]).pin_memory()
     haux = torch.empty(4, dtype=torch.float32).pin_memory()
     main = torch.cuda.current_stream()
-    copy = torch.cuda.Stream()
+    up = torch.cuda.Stream()
+    down = torch.cuda.Stream()
     xbuf = [lay.bufs["x"], torch.empty_like(lay.bufs["x"])]
+    dybuf = [torch.empty_like(lay.bufs["x"]), torch.empty_like(lay.bufs["x"])]
     dxbuf = [lay.grads["dx"], torch.empty_like(lay.bufs["x"])] if training else [None, None]
     ybuf = [lay.bufs["y"], torch.empty_like(lay.bufs["y"])]
-    dy_dev = torch.empty_like(lay.bufs["x"])
     ev = lambda: torch.cuda.Event()            # noqa: E731
-    x_ready, bwd_done, dx_out, y_out = [None, None], [None, None], [None, None], [None, None]
+    in_ready, step_done, dx_out, y_out = [None, None], [None, None], [None, None], [None, None]
 
-    def upload_x(i):
+    def upload(i):
         j = i % 2
-        if bwd_done[j] is not None:
-            copy.wait_event(bwd_done[j])       # step i-2 no longer reads this x buffer
-        with torch.cuda.stream(copy):
+        if step_done[j] is not None:
+            up.wait_event(step_done[j])        # step i-2 no longer reads these buffers
+        with torch.cuda.stream(up):
             xbuf[j].copy_(hx, non_blocking=True)
-        x_ready[j] = ev()
-        x_ready[j].record(copy)
+            if training:
+                dybuf[j].copy_(hdy, non_blocking=True)
+        in_ready[j] = ev()
+        in_ready[j].record(up)
 
     def step(i):
         j = i % 2
-        main.wait_event(x_ready[j])
+        main.wait_event(in_ready[j])
         if dx_out[j] is not None:
             main.wait_event(dx_out[j])         # step i-2's dx download is done
         if y_out[j] is not None:
@@ -567,38 +571,35 @@ def run_e2e(args, s, inp, lay, training, local):
         lay.bufs["y"] = ybuf[j]
         if training:
             lay.grads["dx"] = dxbuf[j]
-            copy.wait_stream(main)             # previous backward no longer reads dY
-            with torch.cuda.stream(copy):
-                dy_dev.copy_(hdy, non_blocking=True)
-            dy_ready = ev()
-            dy_ready.record(copy)
         lay.forward()
         haux.copy_(lay.bufs["aux"], non_blocking=True)   # 16 bytes, ordered on main
         y_ready = ev()
         y_ready.record(main)
-        copy.wait_event(y_ready)
-        with torch.cuda.stream(copy):
+        down.wait_event(y_ready)
+        with torch.cuda.stream(down):
             hy.copy_(ybuf[j], non_blocking=True)
         y_out[j] = ev()
-        y_out[j].record(copy)
-        upload_x(i + 1)                        # next step's input, during this backward
+        y_out[j].record(down)
         if training:
-            main.wait_event(dy_ready)
-            lay.backward(dy_dev)
-            bwd_done[j] = ev()
-            bwd_done[j].record(main)
-            copy.wait_event(bwd_done[j])
-            with torch.cuda.stream(copy):
+            lay.backward(dybuf[j])
+        step_done[j] = ev()
+        step_done[j].record(main)
+        upload(i + 2)                          # the step after next reuses these buffers
+        if training:
+            down.wait_event(step_done[j])
+            with torch.cuda.stream(down):
                 hdx.copy_(dxbuf[j], non_blocking=True)
             dx_out[j] = ev()
-            dx_out[j].record(copy)
+            dx_out[j].record(down)
 
     i = 0
-    upload_x(0)
+    upload(0)
+    upload(1)
     for _ in range(2):
         step(i)
         i += 1
-    main.wait_stream(copy)
+    main.wait_stream(up)
+    main.wait_stream(down)
     torch.cuda.synchronize()
     n = max(3, args.steps // 2)
     a = torch.cuda.Event(enable_timing=True)
@@ -607,7 +608,8 @@ def run_e2e(args, s, inp, lay, training, local):
     for _ in range(n):
         step(i)
         i += 1
-    main.wait_stream(copy)                     # every copy of the timed steps is done
+    main.wait_stream(up)                       # every copy issued in the timed steps is done
+    main.wait_stream(down)
     b.record(main)
     b.synchronize()
     lay.bufs["x"] = xbuf[0]
