@@ -164,11 +164,7 @@ __device__ __forceinline__ void x_fail(XShared& sh, int* status) {
 __device__ __forceinline__ float x_silu(float a) { return __fdividef(a, 1.f + __expf(-a)); }
 __device__ __forceinline__ float x_sigmoid(float a) { return __fdividef(1.f, 1.f + __expf(-a)); }
 
-// 32 consecutive bf16 values: four 16-byte loads / stores.
-__device__ __forceinline__ void x_ld32(const bf16* p, float* v) {
-#pragma unroll
-  for (int u = 0; u < 4; ++u) unpack8(ld_nc_v4(p + 8 * u), v + 8 * u);
-}
+// 32 consecutive bf16 values: four 16-byte stores.
 __device__ __forceinline__ void x_st32(bf16* p, const float* v) {
 #pragma unroll
   for (int u = 0; u < 4; ++u) st_v4(p + 8 * u, pack8(v + 8 * u));
@@ -189,13 +185,6 @@ __device__ __forceinline__ void x_st32_f16(__half* p, const uint32_t* r) {
   for (int u = 0; u < 16; ++u) w[u] = x_f16x2(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1]));
   st_v8(p, w);
   st_v8(p + 16, w + 8);
-}
-// 32-byte load through the non-coherent path (p 32-byte aligned).
-__device__ __forceinline__ void ld_nc_v8(const void* p, uint32_t* v) {
-  asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),
-                 "=r"(v[6]), "=r"(v[7])
-               : "l"(p));
 }
 __device__ __forceinline__ float x_f16_at(const uint32_t* w, int i) {
   const __half2 h = *reinterpret_cast<const __half2*>(&w[i >> 1]);
