@@ -214,7 +214,11 @@ __device__ __forceinline__ void x_prefetch_wait() {
 }
 __device__ __forceinline__ void ld_shared_v4(uint32_t a, uint32_t* v) {
   asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]) : "r"(a));
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]) : "r"(a) : "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t a, const uint32_t* v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};"
+               :: "r"(a), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]) : "memory");
 }
 
 // dH -> the SwiGLU chain rule for 32 columns [col, col + 32) of one row:
@@ -229,17 +233,22 @@ __device__ __forceinline__ void x_dh_chunk(const XParams& p, int row, int col,
   const size_t atom_row = (size_t)(row >> 7) * (2 * p.H / 128);
   float v[32];
   uint32_t cq[8];
-  // eight values at a time from the slot, so that little of a | b is live
+  // eight values at a time from the slot, so that little of a | b is live;
+  // silu(a) = a s(a) of those eight goes back into the 32 slot bytes they
+  // came from (fp32), so that db needs no second logistic
 #pragma unroll
   for (int u = 0; u < 4; ++u) {
-    uint32_t ah[4], bh[4];
+    uint32_t ah[4], bh[4], sl[8];
     ld_shared_v4(slot + 16 * u, ah);
     ld_shared_v4(slot + 64 + 16 * u, bh);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const float a = x_f16_at(ah, i), sg = x_sigmoid(a);
       v[8 * u + i] = __uint_as_float(acc[8 * u + i]) * x_f16_at(bh, i) * sg * (1.f + a * (1.f - sg));
+      sl[i] = __float_as_uint(a * sg);
     }
+    st_shared_v4(slot + 16 * u, sl);
+    st_shared_v4(slot + 64 + 16 * u, sl + 4);
   }
   uint32_t sbyte = mx_quant32(v, cq);
   st_v8(p.dgq + rb + col, cq);
@@ -248,13 +257,11 @@ __device__ __forceinline__ void x_dh_chunk(const XParams& p, int row, int col,
   x_st32(p.dgu + rb + col, v);
 #pragma unroll
   for (int u = 0; u < 4; ++u) {
-    uint32_t ah[4];
-    ld_shared_v4(slot + 16 * u, ah);
+    uint32_t sl[8];
+    ld_shared_v4(slot + 16 * u, sl);
+    ld_shared_v4(slot + 64 + 16 * u, sl + 4);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float a = x_f16_at(ah, i);
-      v[8 * u + i] = __uint_as_float(acc[8 * u + i]) * (a * x_sigmoid(a));
-    }
+    for (int i = 0; i < 8; ++i) v[8 * u + i] = __uint_as_float(acc[8 * u + i]) * __uint_as_float(sl[i]);
   }
   sbyte = mx_quant32(v, cq);
   st_v8(p.dgq + rb + p.H + col, cq);
