@@ -362,7 +362,8 @@ int do_backward(const moe_config* c, const moe_tensors* t, const moe_grads* g, C
   MOE_NEED(t->x); MOE_NEED(t->Wr); MOE_OPT(t->valid); MOE_NEED(t->W_gu); MOE_NEED(t->W_down);
   MOE_NEED(t->logits); MOE_NEED(t->topk_idx); MOE_NEED(t->gates); MOE_NEED(t->counts);
   MOE_NEED(t->f); MOE_NEED(t->row_offsets); MOE_NEED(t->inv); MOE_NEED(t->x_perm);
-  MOE_NEED(t->ab); MOE_NEED(t->h); MOE_NEED(t->out_perm);
+  MOE_NEED(t->h); MOE_NEED(t->out_perm);
+  if (!m) MOE_NEED(t->ab);                      // the MX step keeps a | b in mx->ab16
   if (Hs > 0) {
     MOE_NEED(t->Ws_gu); MOE_NEED(t->Ws_down); MOE_NEED(t->s_ab); MOE_NEED(t->s_h);
     MOE_NEED(g->dWs_gu); MOE_NEED(g->dWs_down);

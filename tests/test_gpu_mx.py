@@ -729,3 +729,18 @@ def test_mx_train_raw_gates_and_z_loss(norm_topk, z_coef):
         chk.layer(n, lay.grads[n], ex[n], idl[n])
     adopt.check(chk)
     chk.done()
+
+
+def test_mx_train_step_needs_no_bf16_ab():
+    """The MX training step keeps a | b in its own fp16 buffer (ab16): with
+    the bf16 layer's ab left NULL it runs and gives the same gradients bit
+    for bit."""
+    s = scaled_shape(5, 1300, dict(d=512, H=256))
+    inp, lay = mx_train_layer(s)
+    keep = {n: lay.grads[n].clone() for n in ("dx", "dW_gu", "dW_down", "d_logits")}
+    lay.bufs["ab"] = None
+    lay.mx_step(inp["dY"].cuda())
+    torch.cuda.synchronize()
+    assert lay.status() == 0
+    for n, v in keep.items():
+        assert torch.equal(v, lay.grads[n]), n
