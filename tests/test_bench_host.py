@@ -1,10 +1,14 @@
 """CPU checks of bench.py's host arithmetic: the algorithmic flops and bytes
 that the roofline fractions divide by, against closed forms worked out by
 hand for the five workloads (no GPU)."""
+import os
+
 import pytest
 
 import bench
 from mixture_experts_ffn_02_gb300 import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 # forward flop = 2 per multiply-add x 3 products (gate, up, down) x d x
@@ -50,3 +54,26 @@ def test_hbm_bytes_closed_forms():
 def test_aggregate_single_rank():
     ms, v = bench.aggregate_ranks(200.0, 32768, 5, 1)
     assert ms == 200.0 and v == pytest.approx(32768 * 5 / 0.2)
+
+
+def test_reference_arm_prints_the_contract_line():
+    """bench.py --impl reference runs the fp64 oracle (no GPU) and prints one
+    JSON line with the same metric, the impl tag, its CPU baseline and an
+    e2e block with no host copies."""
+    import json
+    import subprocess
+    import sys
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--config", "1", "--steps", "2", "--warmup", "1"],
+                       capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip().startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC
+    assert d["unit"] == "tokens/s" and d["value"] > 0 and d["higher_is_better"] is True
+    assert d["steps"] == 2 and d["warmup"] == 1 and d["dtype"] == "f64"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["cpu_baseline"]["cores"] >= 1 and d["cpu_baseline"]["nproc"] >= 1
+    assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
