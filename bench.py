@@ -124,7 +124,10 @@ def launches_per_step(s, fwd_only):
     small = s.E in (4, 8, 16) and s.d * s.E * 4 + (s.d // 8) * 16 <= 96 * 1024
     tc = not small and s.E % 32 == 0
     shared = s.Hs_total > 0
-    router_route = 1 if small else 2          # fused router + route, or the two kernels
+    # small E: the streamed fused router behind its zeroing kernel (2 launches;
+    # MOE_ROUTER_STREAM=0 selects the one-kernel register form); otherwise the
+    # logits kernel and the route kernel
+    router_route = (1 if os.environ.get("MOE_ROUTER_STREAM") == "0" else 2) if small else 2
     router_bwd = 5 if tc else (2 if small else 3)
     fwd = router_route + 3 + 1 + 1 + (2 if shared else 1)     # shared: combine in its down GEMM
     bwd = 1 + 1 + 1 + 2 + (4 if shared else 1) + router_bwd   # shared: dx sum in its dx GEMM

@@ -77,3 +77,22 @@ def test_reference_arm_prints_the_contract_line():
     assert d["cpu_baseline"]["cores"] >= 1 and d["cpu_baseline"]["nproc"] >= 1
     assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
+
+
+def test_launches_per_step_count_the_kernels_of_each_path(monkeypatch):
+    """The gpu_launches claim: kernels of this library per step, counted by
+    hand from the launch lists of each path.  E <= 16: the streamed router
+    (zeroing kernel + router, 2), the permute (3), gate/up and down, the
+    shared expert's two GEMMs with the combine folded in (or the combine
+    kernel), and the backward (combine backward, dH, dX, two dW, the shared
+    expert's four GEMMs or the dx gather, and the router's dW_r and its split
+    sum).  E a multiple of 32: the logits SGEMM and the route kernel, and the
+    router's five-launch tensor-core backward."""
+    monkeypatch.delenv("MOE_ROUTER_STREAM", raising=False)
+    expect = {1: (9, 20), 2: (9, 20), 3: (8, 16), 4: (9, 23), 5: (8, 19)}
+    for c, (fwd, both) in expect.items():
+        s = synth.shape(c)
+        assert bench.launches_per_step(s, True) == fwd, c
+        assert bench.launches_per_step(s, False) == both, c
+    monkeypatch.setenv("MOE_ROUTER_STREAM", "0")              # one-kernel fused router
+    assert bench.launches_per_step(synth.shape(2), False) == 19
