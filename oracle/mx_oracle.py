@@ -30,13 +30,20 @@ Readings (the pages say only "e4m3 values with UE8M0 per-32 block scales"):
   h = silu(a) * b, out = Q(h) Q(W_down)^T, with Q the quantise-dequantise
   round trip above and everything else exact (fp64).  The router and the
   combine are unchanged (no MX).
+* The training step (:func:`backward_mx`, "KohakUwULLM" README, Key features
+  and Selected measurements: MXFP8 training of the MoE experts) puts the
+  routed experts' two data-gradient products on MXFP8 operands, each one
+  rounding of its own value, and keeps the weight gradients, the shared
+  expert and the router in the bf16 layer's form; its docstring states the
+  reading in full.
 
 Pins: ``tests/test_oracle_mx.py`` (closed forms, torch's float8_e4m3fn
 conversion as a library routine, brute-force nearest rounding, round trips of
 representable blocks, row independence, the dense-masked formulation of the
 MX expert sum; for the training step the reduction to the bf16 layer's
-backward when the round trip is the identity, the axis of every quantised
-operand, and a dense-masked formulation of the MX data gradients).
+backward when the round trip is a bf16 one, the axis of every quantised
+operand, a dense-masked formulation of the MX data gradients, the
+quantisation points of the storage hook, and binary16 rounding by hand).
 """
 from __future__ import annotations
 
