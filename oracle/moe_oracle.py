@@ -32,12 +32,17 @@ notes of the repository):
   are one SwiGLU of hidden n*H_s with concatenated weights.
 * Backward: the gradient of  <dY, y> + aux_coef * aux  with the hard counts
   (f) held constant; the selection bias gets no gradient.
+* Storage points (the optional hook ``rnd``, see :func:`_store`): the values a
+  bf16-storage layer keeps between its products -- h, each routed slot's
+  expert output, d_out = g dY, a, b, (da, db) and each routed slot's dx
+  contribution -- may be rounded there; without the hook everything is exact.
 
 Weight layouts: W_gu [E][2H][d] (rows [0,H) gate, [H,2H) up),
 W_down [E][d][H], Ws_gu [2Hs][d], Ws_down [d][Hs], W_r [d][E].
 Parity pins: every function here is pinned by the tests in
 ``tests/test_oracle_pins.py`` (brute force, closed forms, invariants,
-finite differences); none is left unpinned.
+finite differences) and the storage hook by ``tests/test_oracle_storage.py``
+(a one-token layer worked out by hand); none is left unpinned.
 """
 from __future__ import annotations
 
