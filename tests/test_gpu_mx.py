@@ -545,7 +545,7 @@ def test_mx_train_step_is_deterministic():
         assert torch.equal(v, lay.grads[n]), n
 
 
-@pytest.mark.parametrize("cfg,n_tok", [(5, 3), (2, 8)])
+@pytest.mark.parametrize("cfg,n_tok", [(5, 3), (2, 8), (4, 3)])
 def test_mx_train_full_size_sampled(cfg, n_tok):
     """The training step at its full size, in the calls bench.py times
     (Layer.mx_step): the routing in full, and y, dx and d_logits of a few
